@@ -1,0 +1,224 @@
+"""CPU oracle for the attention stage -- TEST INFRASTRUCTURE ONLY.
+
+Only the test suite, ``__graft_entry__.smoke()`` and the benchmark's CPU-baseline
+leg may import this package.  The product path (the CUDA library and its Python
+binding) never imports it and shares no code with it.
+
+The arithmetic lives in ``minf_oracle.c`` (plain C, built here with gcc and
+``-ffp-contract=off``); this module only builds it and marshals numpy arrays.
+Every function cites the page and section it restates, in the C source.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "minf_oracle.c")
+_BUILD = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD, "liboracle.so")
+
+OK = 0
+ERR_ARG = 1
+ERR_GEOMETRY = 2
+ERR_POS = 4
+
+_lock = threading.Lock()
+_lib = None
+
+_f32p = ctypes.POINTER(ctypes.c_float)
+_f64p = ctypes.POINTER(ctypes.c_double)
+_i32p = ctypes.POINTER(ctypes.c_int32)
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle into ``oracle/_build/liboracle.so`` (gcc, -O2, no FMA contraction)."""
+    os.makedirs(_BUILD, exist_ok=True)
+    if not force and os.path.exists(_LIB_PATH) and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC):
+        return _LIB_PATH
+    tmp = _LIB_PATH + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math", "-fPIC", "-shared",
+           "-o", tmp, _SRC, "-lm", "-lpthread"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        lib = ctypes.CDLL(build())
+        lib.orc_rope_freqs.argtypes = [_f32p, ctypes.c_int, ctypes.c_float, ctypes.c_float]
+        lib.orc_rope_freqs.restype = None
+        lib.orc_rms_norm.argtypes = [_f32p, _f32p, _f32p, ctypes.c_int, ctypes.c_int, ctypes.c_float]
+        lib.orc_rms_norm.restype = None
+        lib.orc_rope.argtypes = [_f32p, _i32p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                 ctypes.c_float, ctypes.c_float, ctypes.c_int]
+        lib.orc_rope.restype = ctypes.c_int
+        lib.orc_kv_append.argtypes = [_f32p, _f32p, ctypes.c_int, ctypes.c_int, _f32p, _f32p, _i32p,
+                                      ctypes.c_int]
+        lib.orc_kv_append.restype = ctypes.c_int
+        lib.orc_gqa_attn.argtypes = [_f32p, _f32p, _f32p, _f32p, ctypes.c_int, _i32p, ctypes.c_int,
+                                     ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                     ctypes.c_float, ctypes.c_int]
+        lib.orc_gqa_attn.restype = ctypes.c_int
+        lib.orc_attn_bruteforce_f64.argtypes = [_f64p, _f32p, _f32p, _f32p, ctypes.c_int, _i32p,
+                                                ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                                ctypes.c_int, ctypes.c_int, ctypes.c_double]
+        lib.orc_attn_bruteforce_f64.restype = ctypes.c_int
+        lib.orc_silu_mul.argtypes = [_f32p, _f32p, _f32p, ctypes.c_long]
+        lib.orc_silu_mul.restype = None
+        lib.orc_layer_attn_step.argtypes = [
+            _f32p, _f32p, _f32p, ctypes.c_float, ctypes.c_int,
+            _f32p, _f32p, _f32p, _i32p, ctypes.c_int,
+            _f32p, _f32p, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+            ctypes.c_float, ctypes.c_float, ctypes.c_int, _f32p, ctypes.c_int]
+        lib.orc_layer_attn_step.restype = ctypes.c_int
+        _lib = lib
+        return lib
+
+
+class OracleError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        super().__init__(f"{what}: oracle status {status}")
+        self.status = status
+
+
+def _f32(a, writable=False):
+    a = np.asarray(a)
+    if a.dtype != np.float32 or not a.flags.c_contiguous:
+        if writable:
+            raise TypeError("in-place argument must be a C-contiguous float32 array")
+        a = np.ascontiguousarray(a, dtype=np.float32)
+    return a
+
+
+def _i32(a):
+    return np.ascontiguousarray(np.asarray(a), dtype=np.int32)
+
+
+def _p(a, t):
+    return a.ctypes.data_as(t)
+
+
+def rope_freqs(hd: int, theta: float, freq_scale: float = 1.0) -> np.ndarray:
+    out = np.zeros(hd // 2, dtype=np.float32)
+    _load().orc_rope_freqs(_p(out, _f32p), hd, theta, freq_scale)
+    return out
+
+
+def rms_norm(x, w=None, eps: float = 1e-6, out=None) -> np.ndarray:
+    """x: [rows, n] float32.  Returns y (or writes ``out``, which may be ``x``)."""
+    x = _f32(x)
+    rows, n = x.shape
+    y = np.empty_like(x) if out is None else _f32(out, writable=True)
+    wkeep = _f32(w) if w is not None else None
+    wp = _p(wkeep, _f32p) if wkeep is not None else None
+    _load().orc_rms_norm(_p(y, _f32p), _p(x, _f32p), wp, rows, n, eps)
+    return y
+
+
+def rope(x, pos, n_head: int, hd: int, theta: float, freq_scale: float = 1.0, style: int = 0):
+    """In place on a float32 array laid out [nt, n_head, hd]; returns it."""
+    x = _f32(x, writable=True)
+    pos = _i32(pos)
+    nt = pos.shape[0]
+    assert x.size == nt * n_head * hd
+    st = _load().orc_rope(_p(x, _f32p), _p(pos, _i32p), nt, n_head, hd, theta, freq_scale, style)
+    if st != OK:
+        raise OracleError(st, "rope")
+    return x
+
+
+def kv_append(k_reg, v_reg, k_rows, v_rows, pos, check=True) -> int:
+    """Regions [cap, W] (modified in place), rows [nt, W]."""
+    k_reg = _f32(k_reg, writable=True)
+    v_reg = _f32(v_reg, writable=True)
+    cap, W = k_reg.shape
+    k_rows = _f32(k_rows).reshape(-1, W)
+    v_rows = _f32(v_rows).reshape(-1, W)
+    pos = _i32(pos)
+    st = _load().orc_kv_append(_p(k_reg, _f32p), _p(v_reg, _f32p), cap, W, _p(k_rows, _f32p),
+                               _p(v_rows, _f32p), _p(pos, _i32p), pos.shape[0])
+    if check and st != OK:
+        raise OracleError(st, "kv_append")
+    return st
+
+
+def gqa_attn(q, k_reg, v_reg, pos, n_head: int, n_kv_head: int, hd: int, hd_kv: int,
+             scale: float | None = None, n_threads: int = 1, cap: int | None = None) -> np.ndarray:
+    """q [nt, n_head, hd]; regions [cap, n_kv_head*hd_kv]; returns out [nt, n_head*hd_kv]."""
+    q = _f32(q)
+    k_reg = _f32(k_reg)
+    v_reg = _f32(v_reg)
+    pos = _i32(pos)
+    nt = pos.shape[0]
+    if cap is None:
+        cap = k_reg.shape[0]
+    if scale is None:
+        scale = float(np.float32(1.0) / np.sqrt(np.float32(hd)))
+    out = np.zeros((nt, n_head * hd_kv), dtype=np.float32)
+    st = _load().orc_gqa_attn(_p(out, _f32p), _p(q, _f32p), _p(k_reg, _f32p), _p(v_reg, _f32p), cap,
+                              _p(pos, _i32p), nt, n_head, n_kv_head, hd, hd_kv, scale, n_threads)
+    if st != OK:
+        raise OracleError(st, "gqa_attn")
+    return out
+
+
+def attn_bruteforce_f64(q, k_reg, v_reg, pos, n_head: int, n_kv_head: int, hd: int, hd_kv: int,
+                        scale: float, cap: int | None = None) -> np.ndarray:
+    q = _f32(q)
+    k_reg = _f32(k_reg)
+    v_reg = _f32(v_reg)
+    pos = _i32(pos)
+    nt = pos.shape[0]
+    if cap is None:
+        cap = k_reg.shape[0]
+    out = np.zeros((nt, n_head * hd_kv), dtype=np.float64)
+    st = _load().orc_attn_bruteforce_f64(_p(out, _f64p), _p(q, _f32p), _p(k_reg, _f32p),
+                                         _p(v_reg, _f32p), cap, _p(pos, _i32p), nt, n_head,
+                                         n_kv_head, hd, hd_kv, scale)
+    if st != OK:
+        raise OracleError(st, "attn_bruteforce_f64")
+    return out
+
+
+def silu_mul(gate, up) -> np.ndarray:
+    gate = _f32(gate)
+    up = _f32(up)
+    y = np.empty_like(gate)
+    _load().orc_silu_mul(_p(y, _f32p), _p(gate, _f32p), _p(up, _f32p), gate.size)
+    return y
+
+
+def layer_attn_step(h, gain, q, k, v, pos, k_reg, v_reg, *, n_head: int, n_kv_head: int, hd: int,
+                    hd_kv: int, eps: float = 1e-6, theta: float = 1e6, freq_scale: float = 1.0,
+                    style: int = 0, n_threads: int = 1):
+    """One layer's attention stage.  q and k are rotated in place, the regions are
+    appended in place; returns (xn, out)."""
+    h = _f32(h)
+    gain = _f32(gain)
+    q = _f32(q, writable=True)
+    k = _f32(k, writable=True)
+    v = _f32(v)
+    pos = _i32(pos)
+    k_reg = _f32(k_reg, writable=True)
+    v_reg = _f32(v_reg, writable=True)
+    nt = pos.shape[0]
+    n_embd = h.size // max(nt, 1)
+    xn = np.empty_like(h)
+    out = np.zeros((nt, n_head * hd_kv), dtype=np.float32)
+    st = _load().orc_layer_attn_step(
+        _p(xn, _f32p), _p(h, _f32p), _p(gain, _f32p), eps, n_embd,
+        _p(q, _f32p), _p(k, _f32p), _p(v, _f32p), _p(pos, _i32p), nt,
+        _p(k_reg, _f32p), _p(v_reg, _f32p), k_reg.shape[0], n_head, n_kv_head, hd, hd_kv,
+        theta, freq_scale, style, _p(out, _f32p), n_threads)
+    if st != OK:
+        raise OracleError(st, "layer_attn_step")
+    return xn, out

@@ -1,0 +1,361 @@
+/*
+ * minf_oracle.c -- the CPU oracle for the attention stage (TEST INFRASTRUCTURE).
+ *
+ * This file is test infrastructure, not part of the product.  Only the test
+ * suite, the smoke check and the benchmark's CPU-baseline leg may load it.
+ * It shares no code, header, table or helper with the CUDA library: every
+ * formula below is written out again, plainly, from the pages it cites.
+ *
+ * Sources (page title, section):
+ *   [P1] "11 . Attention, vec ops, and the KV cache" (minfer walkthrough)
+ *   [P2] "IV.2: Zero-copy KV cache"
+ *   [P3] "13 . The decode loop and graph reuse" (minfer walkthrough)
+ *
+ * Precision follows what [P1] fixes: fp32 data, fp32 dot products and fp32
+ * weighted sums, an f64 sum of squares in RMSNorm and an f64 softmax
+ * denominator.  The brute-force reference (orc_attn_bruteforce_f64) is fp64
+ * throughout and is an independent formulation used to pin this one.
+ *
+ * Build with -ffp-contract=off so that x86-64 and aarch64 round every product
+ * separately (no fused multiply-add), giving identical results on both hosts.
+ *
+ * Parity status per function (what pins it is in tests/test_oracle_*.py):
+ *   orc_rope_freqs, orc_rms_norm, orc_rope, orc_kv_append, orc_gqa_attn,
+ *   orc_attn_bruteforce_f64, orc_silu_mul, orc_layer_attn_step -- all pinned.
+ */
+#include <math.h>
+#include <pthread.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+/* Status codes (the oracle's own; numerically chosen to match the library's
+ * public enum so tests can compare statuses, but not shared as a header). */
+#define ORC_OK 0
+#define ORC_ERR_ARG 1
+#define ORC_ERR_GEOMETRY 2
+#define ORC_ERR_POS 4
+
+#define ORC_MAX_HALF 128 /* [P1] §3.2.2: the angular-speed table holds hd/2 <= 128 entries */
+
+/* ------------------------------------------------------------------------ */
+/* RoPE angular speeds.  [P1] §2.3 and §3.2.2: freq_i = freq_scale / base^(2i/hd).
+ * The page evaluates this in f32 with powf, whose last bit differs between math
+ * libraries; the reading taken here is the exact quotient evaluated in double and
+ * rounded once to float, so any implementation can reproduce the table bit for bit. */
+void orc_rope_freqs(float *freqs, int hd, float theta, float freq_scale)
+{
+    int half = hd / 2;
+    for (int i = 0; i < half; ++i) {
+        double expo = (double)(2 * i) / (double)hd;
+        freqs[i] = (float)((double)freq_scale / pow((double)theta, expo));
+    }
+}
+
+/* ------------------------------------------------------------------------ */
+/* RMSNorm with gains.  [P1] §3.2.1: sum of squares in f64, mean rounded to f32,
+ * scale = 1/sqrt(mean + eps) in f32, y = x * scale, then y *= weight.  No mean
+ * subtraction.  y may alias x.  w == NULL means unit gains. */
+void orc_rms_norm(float *y, const float *x, const float *w, int rows, int n, float eps)
+{
+    for (int r = 0; r < rows; ++r) {
+        const float *xr = x + (size_t)r * n;
+        float *yr = y + (size_t)r * n;
+        double sum_sq = 0.0;
+        for (int i = 0; i < n; ++i)
+            sum_sq += (double)xr[i] * (double)xr[i];
+        float mean = (float)(sum_sq / (double)n);
+        float scale = 1.0f / sqrtf(mean + eps);
+        for (int i = 0; i < n; ++i) {
+            float v = xr[i] * scale;
+            yr[i] = w ? v * w[i] : v;
+        }
+    }
+}
+
+/* ------------------------------------------------------------------------ */
+/* Rotary position embedding, in place.  [P1] §3.2.2 (the cpu_rope core loop):
+ * per token t, head h and subspace i < hd/2, angle th = pos[t] * freq_i (f32
+ * product); the pair is (i, i+hd/2) for the NonInterleaved (Qwen/NEOX) style
+ * and (2i, 2i+1) for the Interleaved (Llama) style; the pair is rotated by
+ * +th: x0' = x0 cos - x1 sin, x1' = x0 sin + x1 cos.  sin and cos are taken
+ * in double and rounded to float (the reading for large positions).
+ * x is [nt, nh, hd] row-major.  style: 0 = NonInterleaved, 1 = Interleaved. */
+int orc_rope(float *x, const int32_t *pos, int nt, int nh, int hd,
+             float theta, float freq_scale, int style)
+{
+    if (hd <= 0 || (hd & 1) || hd / 2 > ORC_MAX_HALF || nh <= 0 || nt < 0)
+        return ORC_ERR_ARG;
+    if (style != 0 && style != 1)
+        return ORC_ERR_ARG;
+    int half = hd / 2;
+    float freqs[ORC_MAX_HALF];
+    orc_rope_freqs(freqs, hd, theta, freq_scale);
+    for (int t = 0; t < nt; ++t) {
+        if (pos[t] < 0)
+            return ORC_ERR_POS;
+        float p = (float)pos[t];
+        for (int h = 0; h < nh; ++h) {
+            size_t b = ((size_t)t * nh + h) * hd;
+            for (int i = 0; i < half; ++i) {
+                float th = p * freqs[i];
+                float sn = (float)sin((double)th);
+                float cs = (float)cos((double)th);
+                size_t i0 = style == 0 ? b + i : b + 2 * (size_t)i;
+                size_t i1 = style == 0 ? b + i + half : b + 2 * (size_t)i + 1;
+                float x0 = x[i0], x1 = x[i1];
+                x[i0] = x0 * cs - x1 * sn;
+                x[i1] = x0 * sn + x1 * cs;
+            }
+        }
+    }
+    return ORC_OK;
+}
+
+/* ------------------------------------------------------------------------ */
+/* KV store.  [P1] §3.2.3 (the KvcacheStore arm): for each token in order,
+ * p = pos[t]; p >= n_ctx is a hard error (return, never clamp); otherwise the
+ * K row and the V row (W floats each) are copied to offset p*W of the layer's
+ * persistent regions.  Like the page, the first bad position returns at once,
+ * after the rows before it were written.  [P2] (the in-place append with
+ * headroom) is the same copy with the region's row capacity as n_ctx. */
+int orc_kv_append(float *k_reg, float *v_reg, int cap, int W,
+                  const float *k_rows, const float *v_rows, const int32_t *pos, int nt)
+{
+    if (cap < 0 || W <= 0 || nt < 0)
+        return ORC_ERR_ARG;
+    for (int t = 0; t < nt; ++t) {
+        int p = pos[t];
+        if (p < 0 || p >= cap)
+            return ORC_ERR_POS;
+        memcpy(k_reg + (size_t)p * W, k_rows + (size_t)t * W, sizeof(float) * (size_t)W);
+        memcpy(v_reg + (size_t)p * W, v_rows + (size_t)t * W, sizeof(float) * (size_t)W);
+    }
+    return ORC_OK;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Grouped-query attention.  [P1] §3.2.4 (the Attn arm and the per-head worker)
+ * and §3.2.5 (softmax):
+ *   nkv = min(max_t pos[t] + 1, cap)                      (the window is data)
+ *   query head h reads kv head hk = h / (nh / nk)
+ *   vl  = min(pos[t] + 1, nkv)                            (causal by length)
+ *   s_j = dot_f32(q[t,h][0:hdkv], K[j, hk]) * scale for j < vl, -inf after
+ *   softmax over all nkv entries: exp(s - max) with an f64 sum, then scaled
+ *   by (float)(1/sum); out = sum_j w_j V[j, hk] over all nkv rows, ascending.
+ * q is [nt, nh, hd] (query head stride hd; the dot uses its first hdkv
+ * entries), the regions are [cap, nk*hdkv], out is [nt, nh*hdkv].
+ * Heads are split over n_threads workers; heads never reduce against each
+ * other, so the result is bit-identical at any thread count ([P1] §3.2.4). */
+typedef struct {
+    float *out;
+    const float *q, *k_reg, *v_reg;
+    const int32_t *pos;
+    int nt, nh, nk, hd, hdkv, nkv, h0, h1;
+    float scale;
+    int status;
+} orc_attn_job;
+
+static void *orc_attn_heads(void *arg)
+{
+    orc_attn_job *c = (orc_attn_job *)arg;
+    int gqa = c->nh / c->nk;
+    int W = c->nk * c->hdkv;
+    float *scrs = (float *)malloc(sizeof(float) * (size_t)(c->nkv > 0 ? c->nkv : 1));
+    if (!scrs) {
+        c->status = ORC_ERR_ARG;
+        return NULL;
+    }
+    for (int h = c->h0; h < c->h1; ++h) {
+        int hk = h / gqa;
+        for (int t = 0; t < c->nt; ++t) {
+            const float *q_row = c->q + ((size_t)t * c->nh + h) * c->hd;
+            float *out_row = c->out + ((size_t)t * c->nh + h) * c->hdkv;
+            int vl = c->pos[t] + 1 < c->nkv ? c->pos[t] + 1 : c->nkv;
+            float mx = -INFINITY;
+            for (int kv = 0; kv < vl; ++kv) {
+                const float *k_row = c->k_reg + (size_t)kv * W + (size_t)hk * c->hdkv;
+                float dot = 0.0f;
+                for (int d = 0; d < c->hdkv; ++d)
+                    dot += q_row[d] * k_row[d];
+                float s = dot * c->scale;
+                scrs[kv] = s;
+                if (s > mx)
+                    mx = s;
+            }
+            for (int kv = vl; kv < c->nkv; ++kv)
+                scrs[kv] = -INFINITY;
+            double sum = 0.0;
+            for (int kv = 0; kv < c->nkv; ++kv) {
+                float e = expf(scrs[kv] - mx);
+                scrs[kv] = e;
+                sum += (double)e;
+            }
+            float inv = (float)(1.0 / sum);
+            for (int kv = 0; kv < c->nkv; ++kv)
+                scrs[kv] *= inv;
+            for (int d = 0; d < c->hdkv; ++d)
+                out_row[d] = 0.0f;
+            for (int kv = 0; kv < c->nkv; ++kv) {
+                const float *v_row = c->v_reg + (size_t)kv * W + (size_t)hk * c->hdkv;
+                float wgt = scrs[kv];
+                for (int d = 0; d < c->hdkv; ++d)
+                    out_row[d] += wgt * v_row[d];
+            }
+        }
+    }
+    free(scrs);
+    return NULL;
+}
+
+int orc_gqa_attn(float *out, const float *q, const float *k_reg, const float *v_reg, int cap,
+                 const int32_t *pos, int nt, int nh, int nk, int hd, int hdkv, float scale,
+                 int n_threads)
+{
+    if (nt < 0 || nh <= 0 || nk <= 0 || hd <= 0 || hdkv <= 0 || cap < 0)
+        return ORC_ERR_ARG;
+    if (hd < hdkv || nh % nk != 0) /* [P1] §1: hd < hd_kv is refused */
+        return ORC_ERR_GEOMETRY;
+    if (nt == 0)
+        return ORC_OK;
+    long mx_pos1 = 0;
+    for (int t = 0; t < nt; ++t) {
+        if (pos[t] < 0)
+            return ORC_ERR_POS;
+        if ((long)pos[t] + 1 > mx_pos1)
+            mx_pos1 = (long)pos[t] + 1;
+    }
+    int nkv = (int)(mx_pos1 < cap ? mx_pos1 : cap);
+    if (n_threads < 1)
+        n_threads = 1;
+    if (n_threads > nh)
+        n_threads = nh;
+    orc_attn_job jobs[256];
+    pthread_t tids[256];
+    if (n_threads > 256)
+        n_threads = 256;
+    for (int w = 0; w < n_threads; ++w) {
+        orc_attn_job *j = &jobs[w];
+        j->out = out; j->q = q; j->k_reg = k_reg; j->v_reg = v_reg; j->pos = pos;
+        j->nt = nt; j->nh = nh; j->nk = nk; j->hd = hd; j->hdkv = hdkv; j->nkv = nkv;
+        j->h0 = (int)((long)nh * w / n_threads);
+        j->h1 = (int)((long)nh * (w + 1) / n_threads);
+        j->scale = scale;
+        j->status = ORC_OK;
+    }
+    if (n_threads == 1) {
+        orc_attn_heads(&jobs[0]);
+    } else {
+        for (int w = 0; w < n_threads; ++w)
+            pthread_create(&tids[w], NULL, orc_attn_heads, &jobs[w]);
+        for (int w = 0; w < n_threads; ++w)
+            pthread_join(tids[w], NULL);
+    }
+    for (int w = 0; w < n_threads; ++w)
+        if (jobs[w].status != ORC_OK)
+            return jobs[w].status;
+    return ORC_OK;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Brute-force masked attention in fp64: an independent formulation of [P1] §2.1
+ * steps 1-4 used only to pin orc_gqa_attn on small inputs.  It builds the
+ * explicit [nt x nkv] additive mask matrix (0 where key j <= pos[t], -inf
+ * elsewhere) that the pages deliberately avoid, maps query head h to kv head
+ * floor(h * nk / nh), takes a full softmax in double and a double weighted
+ * sum.  out is [nt, nh*hdkv] in double. */
+int orc_attn_bruteforce_f64(double *out, const float *q, const float *k_reg, const float *v_reg,
+                            int cap, const int32_t *pos, int nt, int nh, int nk, int hd, int hdkv,
+                            double scale)
+{
+    if (nt <= 0 || nh <= 0 || nk <= 0 || hd < hdkv || nh % nk != 0)
+        return ORC_ERR_GEOMETRY;
+    int W = nk * hdkv;
+    long nkv = 0;
+    for (int t = 0; t < nt; ++t)
+        if ((long)pos[t] + 1 > nkv)
+            nkv = (long)pos[t] + 1;
+    if (nkv > cap)
+        nkv = cap;
+    double *mask = (double *)malloc(sizeof(double) * (size_t)nt * (size_t)nkv);
+    double *logit = (double *)malloc(sizeof(double) * (size_t)nkv);
+    if (!mask || !logit) {
+        free(mask);
+        free(logit);
+        return ORC_ERR_ARG;
+    }
+    for (int t = 0; t < nt; ++t)
+        for (long j = 0; j < nkv; ++j)
+            mask[(size_t)t * nkv + j] = (j <= pos[t]) ? 0.0 : -INFINITY;
+    for (int t = 0; t < nt; ++t) {
+        for (int h = 0; h < nh; ++h) {
+            int hk = (int)(((long)h * nk) / nh);
+            const float *qr = q + ((size_t)t * nh + h) * hd;
+            double best = -INFINITY;
+            for (long j = 0; j < nkv; ++j) {
+                const float *kr = k_reg + (size_t)j * W + (size_t)hk * hdkv;
+                double acc = 0.0;
+                for (int d = 0; d < hdkv; ++d)
+                    acc += (double)qr[d] * (double)kr[d];
+                logit[j] = acc * scale + mask[(size_t)t * nkv + j];
+                if (logit[j] > best)
+                    best = logit[j];
+            }
+            double z = 0.0;
+            for (long j = 0; j < nkv; ++j) {
+                logit[j] = exp(logit[j] - best);
+                z += logit[j];
+            }
+            double *o = out + ((size_t)t * nh + h) * hdkv;
+            for (int d = 0; d < hdkv; ++d) {
+                double acc = 0.0;
+                for (long j = 0; j < nkv; ++j)
+                    acc += logit[j] * (double)v_reg[(size_t)j * W + (size_t)hk * hdkv + d];
+                o[d] = acc / z;
+            }
+        }
+    }
+    free(mask);
+    free(logit);
+    return ORC_OK;
+}
+
+/* ------------------------------------------------------------------------ */
+/* SiLU times up.  [P1] §3.2.5: silu(x) = x / (1 + e^-x); SwiGLU multiplies it
+ * by the up projection element-wise. */
+void orc_silu_mul(float *y, const float *gate, const float *up, long n)
+{
+    for (long i = 0; i < n; ++i) {
+        float g = gate[i];
+        float s = g / (1.0f + expf(-g));
+        y[i] = s * up[i];
+    }
+}
+
+/* ------------------------------------------------------------------------ */
+/* One layer's attention stage.  [P1] §1 (the decoder layer picture) and §3.4
+ * (store before attention): xn = RMSNorm(h) * gain; RoPE on q (nh heads of hd)
+ * and on k (nk heads of hdkv), in place; KV store of the rotated k and of v at
+ * pos[t]; attention over the regions with scale = 1/sqrt(hd) ([P1] §2.4).
+ * The q/k/v projections need trained weights and are outside this stage, so
+ * xn is a separate output and q, k, v are inputs. */
+int orc_layer_attn_step(float *xn, const float *h, const float *gain, float eps, int n_embd,
+                        float *q, float *k, const float *v, const int32_t *pos, int nt,
+                        float *k_reg, float *v_reg, int cap, int nh, int nk, int hd, int hdkv,
+                        float theta, float freq_scale, int style, float *out, int n_threads)
+{
+    if (hd < hdkv || nh <= 0 || nk <= 0 || nh % nk != 0)
+        return ORC_ERR_GEOMETRY;
+    orc_rms_norm(xn, h, gain, nt, n_embd, eps);
+    int st = orc_rope(q, pos, nt, nh, hd, theta, freq_scale, style);
+    if (st != ORC_OK)
+        return st;
+    st = orc_rope(k, pos, nt, nk, hdkv, theta, freq_scale, style);
+    if (st != ORC_OK)
+        return st;
+    st = orc_kv_append(k_reg, v_reg, cap, nk * hdkv, k, v, pos, nt);
+    if (st != ORC_OK)
+        return st;
+    float scale = 1.0f / sqrtf((float)hd);
+    return orc_gqa_attn(out, q, k_reg, v_reg, cap, pos, nt, nh, nk, hd, hdkv, scale, n_threads);
+}

@@ -1,0 +1,398 @@
+"""Pins for the CPU oracle: worked examples, closed forms, invariants and an
+independent fp64 brute force.  These run without a GPU and never touch the CUDA
+library; they establish that the oracle computes what the pages define before
+it is trusted as the reference for the kernels."""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _golden(name):
+    with open(os.path.join(GOLDEN, name)) as f:
+        return json.load(f)
+
+
+def _rng(seed):
+    return np.random.default_rng(seed)
+
+
+# --------------------------------------------------------------------------- RMSNorm
+def test_rmsnorm_worked_example(orc):
+    g = _golden("rmsnorm_worked_example.json")
+    y = orc.rms_norm(np.array([g["x"]], np.float32), np.array(g["gains"], np.float32), eps=g["eps"])[0]
+    tol = 0.5 * 10 ** -g["printed_decimals"] + 1e-7
+    np.testing.assert_allclose(y, g["normalized_printed"], atol=tol, rtol=0)
+    # closed form: x / sqrt(7.5)
+    exact = np.array(g["x"]) / math.sqrt(g["mean_sq"])
+    np.testing.assert_allclose(y, exact, rtol=3e-7, atol=0)
+
+
+@pytest.mark.parametrize("n", [4, 896, 1024, 1001])
+def test_rmsnorm_unit_rms_and_gains(orc, n):
+    r = _rng(n)
+    x = r.standard_normal((5, n)).astype(np.float32) * 3.0
+    y = orc.rms_norm(x, None, eps=0.0)
+    rms = np.sqrt(np.mean(y.astype(np.float64) ** 2, axis=1))
+    np.testing.assert_allclose(rms, 1.0, rtol=2e-6)
+    # eps shrinks the rms to sqrt(ms / (ms + eps))
+    eps = 0.5
+    y2 = orc.rms_norm(x, None, eps=eps)
+    ms = np.mean(x.astype(np.float64) ** 2, axis=1)
+    np.testing.assert_allclose(np.sqrt(np.mean(y2.astype(np.float64) ** 2, axis=1)),
+                               np.sqrt(ms / (ms + eps)), rtol=2e-6)
+    # gains multiply element-wise after normalisation
+    w = r.uniform(0.5, 1.5, n).astype(np.float32)
+    yw = orc.rms_norm(x, w, eps=0.0)
+    np.testing.assert_allclose(yw, y * w, rtol=2e-7, atol=0)
+
+
+def test_rmsnorm_no_mean_subtraction_and_alias(orc):
+    x = np.full((1, 8), -2.5, np.float32)
+    y = orc.rms_norm(x, None, eps=0.0)
+    np.testing.assert_array_equal(y, -np.ones_like(x))  # LayerNorm would give 0
+    r = _rng(1)
+    x = r.standard_normal((3, 64)).astype(np.float32)
+    ref = orc.rms_norm(x, None, eps=1e-6)
+    orc.rms_norm(x, None, eps=1e-6, out=x)  # y aliases x
+    np.testing.assert_array_equal(x, ref)
+
+
+def test_rmsnorm_scale_invariant(orc):
+    r = _rng(2)
+    x = r.standard_normal((4, 128)).astype(np.float32)
+    np.testing.assert_array_equal(orc.rms_norm(x, None, eps=0.0), orc.rms_norm(x * 8.0, None, eps=0.0))
+
+
+# --------------------------------------------------------------------------- RoPE
+def test_rope_freq_table_properties(orc):
+    g = _golden("rope_worked_example.json")
+    f = orc.rope_freqs(g["hd"], g["base"], 1.0)
+    np.testing.assert_array_equal(f, np.array(g["freqs_by_formula"], np.float32))
+    for hd, theta, fs in [(64, 1e6, 1.0), (128, 1e6, 1.0), (128, 1e4, 0.25)]:
+        f = orc.rope_freqs(hd, theta, fs).astype(np.float64)
+        assert f[0] == np.float32(fs)                       # subspace 0 spins at freq_scale
+        assert np.all(np.diff(f) < 0)                        # strictly slower
+        ratios = f[1:] / f[:-1]                              # geometric with ratio theta^(-2/hd)
+        np.testing.assert_allclose(ratios, theta ** (-2.0 / hd), rtol=2e-7)
+        # the middle subspace (2i/hd = 1/2) turns at freq_scale / sqrt(theta)
+        np.testing.assert_allclose(f[hd // 4], fs / math.sqrt(theta), rtol=6e-8)
+
+
+def test_rope_pos0_identity_and_norms(orc):
+    r = _rng(3)
+    x = r.standard_normal((3, 4, 64)).astype(np.float32)
+    y = orc.rope(x.copy(), [0, 0, 0], 4, 64, 1e6)
+    np.testing.assert_array_equal(y, x)  # cos 0 = 1, sin 0 = 0: bit-exact
+    pos = [5, 1000, 40960]
+    for style in (0, 1):
+        y = orc.rope(x.copy(), pos, 4, 64, 1e6, style=style)
+        if style == 0:
+            a, b = x[..., :32], x[..., 32:]
+            ya, yb = y[..., :32], y[..., 32:]
+        else:
+            a, b = x[..., 0::2], x[..., 1::2]
+            ya, yb = y[..., 0::2], y[..., 1::2]
+        n0 = np.hypot(a.astype(np.float64), b.astype(np.float64))
+        n1 = np.hypot(ya.astype(np.float64), yb.astype(np.float64))
+        np.testing.assert_allclose(n1, n0, rtol=3e-7, atol=1e-7)
+
+
+def test_rope_worked_example(orc):
+    g = _golden("rope_worked_example.json")
+    # NonInterleaved pairs for hd=4 are (0,2) and (1,3); put (1,0) in both
+    x = np.array([[1.0, 1.0, 0.0, 0.0]], np.float32)
+    y = orc.rope(x, [g["pos"]], 1, g["hd"], g["base"])[0]
+    a0 = g["pair0_angle_rad"]
+    a1 = g["pos"] * 0.01
+    np.testing.assert_allclose(y, [math.cos(a0), math.cos(a1), math.sin(a0), math.sin(a1)],
+                               rtol=0, atol=2e-7)
+
+
+def test_rope_rotation_direction(orc):
+    # hd = 2, freq_0 = freq_scale = pi/2, pos = 1: (1, 0) turns counter-clockwise to (0, 1)
+    y = orc.rope(np.array([1.0, 0.0], np.float32), [1], 1, 2, 1e4, freq_scale=math.pi / 2)
+    np.testing.assert_allclose(y, [0.0, 1.0], atol=1e-7)
+    y = orc.rope(np.array([0.0, 1.0], np.float32), [1], 1, 2, 1e4, freq_scale=math.pi / 2)
+    np.testing.assert_allclose(y, [-1.0, 0.0], atol=1e-7)
+
+
+def test_rope_relative_position(orc):
+    # q.k after RoPE depends only on m - n (11 · Attention..., §2.3)
+    r = _rng(4)
+    hd = 64
+    q = r.standard_normal(hd).astype(np.float32)
+    k = r.standard_normal(hd).astype(np.float32)
+    dots = []
+    for m, n in [(7, 3), (107, 103), (1007, 1003), (4, 0)]:
+        qa = orc.rope(q.copy(), [m], 1, hd, 1e4)
+        ka = orc.rope(k.copy(), [n], 1, hd, 1e4)
+        dots.append(float(np.dot(qa.astype(np.float64), ka.astype(np.float64))))
+    np.testing.assert_allclose(dots, dots[0], rtol=2e-4, atol=2e-4)
+    qa = orc.rope(q.copy(), [9], 1, hd, 1e4)
+    ka = orc.rope(k.copy(), [3], 1, hd, 1e4)
+    assert abs(float(np.dot(qa, ka)) - dots[0]) > 1e-2  # a different offset does change it
+
+
+def test_rope_styles_are_a_permutation(orc):
+    r = _rng(5)
+    hd, nh = 8, 3
+    x = r.standard_normal((2, nh, hd)).astype(np.float32)
+    perm = np.empty(hd, dtype=np.int64)  # NonInterleaved slot (i, i+half) -> Interleaved (2i, 2i+1)
+    half = hd // 2
+    for i in range(half):
+        perm[2 * i] = i
+        perm[2 * i + 1] = i + half
+    y_non = orc.rope(x.copy(), [3, 11], nh, hd, 1e4, style=0)
+    y_int = orc.rope(np.ascontiguousarray(x[..., perm]), [3, 11], nh, hd, 1e4, style=1)
+    np.testing.assert_array_equal(y_int, y_non[..., perm])
+
+
+# --------------------------------------------------------------------------- KV store
+def test_kv_append_placement_and_errors(orc):
+    r = _rng(6)
+    cap, W = 10, 16
+    k_reg = r.standard_normal((cap, W)).astype(np.float32)
+    v_reg = r.standard_normal((cap, W)).astype(np.float32)
+    k0, v0 = k_reg.copy(), v_reg.copy()
+    k = r.standard_normal((3, W)).astype(np.float32)
+    v = r.standard_normal((3, W)).astype(np.float32)
+    orc.kv_append(k_reg, v_reg, k, v, [4, 9, 0])
+    for t, p in enumerate([4, 9, 0]):
+        np.testing.assert_array_equal(k_reg[p], k[t])
+        np.testing.assert_array_equal(v_reg[p], v[t])
+    untouched = [i for i in range(cap) if i not in (4, 9, 0)]
+    np.testing.assert_array_equal(k_reg[untouched], k0[untouched])
+    np.testing.assert_array_equal(v_reg[untouched], v0[untouched])
+    # pos >= cap is an error, never a clamp; rows before it were written, rows after not
+    k1, v1 = k_reg.copy(), v_reg.copy()
+    st = orc.kv_append(k_reg, v_reg, k, v, [2, cap, 3], check=False)
+    assert st == orc.ERR_POS
+    np.testing.assert_array_equal(k_reg[2], k[0])
+    np.testing.assert_array_equal(k_reg[3], k1[3])
+    np.testing.assert_array_equal(v_reg[3], v1[3])
+    assert orc.kv_append(k_reg, v_reg, k[:1], v[:1], [-1], check=False) == orc.ERR_POS
+
+
+# --------------------------------------------------------------------------- attention
+def _example_regions():
+    g = _golden("attention_worked_examples.json")
+    k = np.array(g["k_rows"], np.float32)
+    v = np.array(g["v_rows"], np.float32)
+    return g, k, v
+
+
+def test_attention_worked_example_blend(orc):
+    g, k, v = _example_regions()
+    b = g["blend"]
+    q = np.array([b["q"]], np.float32)
+    out = orc.gqa_attn(q, k, v, [b["pos"]], 1, 1, 4, 4, scale=g["scale"])
+    np.testing.assert_array_equal(out[0], np.array(b["out_printed"], np.float32))
+    # with a masked third slot in the window (a second token at pos 2 makes nkv = 3)
+    q2 = np.array([b["q"], [0, 0, 0, 0]], np.float32)
+    out = orc.gqa_attn(q2, k, v, [b["pos"], 2], 1, 1, 4, 4, scale=g["scale"])
+    np.testing.assert_array_equal(out[0], np.array(b["out_printed"], np.float32))
+
+
+def test_attention_worked_example_tilt(orc):
+    g, k, v = _example_regions()
+    t = g["tilt"]
+    out = orc.gqa_attn(np.array([t["q"]], np.float32), k, v, [t["pos"]], 1, 1, 4, 4, scale=g["scale"])
+    w0 = 1.0 / (1.0 + math.exp(-0.5))
+    w1 = 1.0 - w0
+    exp = w0 * v[0].astype(np.float64) + w1 * v[1].astype(np.float64)
+    np.testing.assert_allclose(out[0], exp, rtol=0, atol=1e-6)
+    assert abs(w0 - t["weights_printed"][0]) > 0.1  # the printed weights are not the closed form
+
+
+def test_attention_worked_example_decode_step(orc):
+    g, k, v = _example_regions()
+    d = g["decode_step"]
+    # the three tokens of the page's decode example, as a 3-token prefill
+    q = np.array([[1, 1, 0, 0], g["blend"]["q"], d["q"]], np.float32)
+    out = orc.gqa_attn(q, k, v, [0, 1, 2], 1, 1, 4, 4, scale=g["scale"])
+    np.testing.assert_array_equal(out[0], v[0])              # token 0 sees only row 0
+    np.testing.assert_array_equal(out[1], np.array(g["blend"]["out_printed"], np.float32))
+    e = math.exp(0.5)
+    w = np.array([1.0, e, e]) / (1.0 + 2.0 * e)
+    np.testing.assert_allclose(w, [0.23270, 0.38365, 0.38365], atol=5e-6)
+    exp = w @ v.astype(np.float64)
+    np.testing.assert_allclose(out[2], exp, rtol=0, atol=2e-6)
+    assert abs(out[2][1] - 2.0) <= 2e-6
+    # the same token as a decode step (nt = 1 at pos 2) gives the same row
+    out_dec = orc.gqa_attn(q[2:3], k, v, [2], 1, 1, 4, 4, scale=g["scale"])
+    np.testing.assert_array_equal(out_dec[0], out[2])
+
+
+def test_single_cached_key_returns_its_value(orc):
+    r = _rng(7)
+    nh, nk, hd = 6, 2, 32
+    q = r.standard_normal((1, nh, hd)).astype(np.float32)
+    k = r.standard_normal((5, nk * hd)).astype(np.float32)
+    v = r.standard_normal((5, nk * hd)).astype(np.float32)
+    out = orc.gqa_attn(q, k, v, [0], nh, nk, hd, hd)
+    for h in range(nh):
+        hk = h // (nh // nk)
+        np.testing.assert_array_equal(out[0, h * hd:(h + 1) * hd], v[0, hk * hd:(hk + 1) * hd])
+
+
+def test_softmax_weights_sum_to_one(orc):
+    r = _rng(8)
+    nh, nk, hd, L = 4, 2, 64, 300
+    q = r.standard_normal((1, nh, hd)).astype(np.float32) * 2
+    k = r.standard_normal((L, nk * hd)).astype(np.float32)
+    v = np.ones((L, nk * hd), np.float32)
+    out = orc.gqa_attn(q, k, v, [L - 1], nh, nk, hd, hd)
+    np.testing.assert_allclose(out, 1.0, rtol=0, atol=3e-6)
+
+
+TINY_CASES = [
+    # (nh, nk, hd, hdkv, cap, positions)
+    (1, 1, 4, 4, 6, [0, 1, 2, 3, 4, 5]),          # MHA, full causal prefill
+    (14, 2, 64, 64, 20, [19]),                    # Qwen2.5-0.5B geometry, one decode step
+    (16, 8, 128, 128, 9, [3, 8, 0, 5]),           # Qwen3-0.6B geometry, scattered positions
+    (6, 3, 16, 16, 7, [2, 2, 6]),                 # repeated positions
+    (4, 2, 128, 64, 12, [11, 4]),                 # hd > hd_kv: dot over the first hd_kv
+    (4, 4, 8, 8, 5, [7, 1]),                      # pos beyond the region: window clamps at cap
+    (8, 1, 32, 32, 33, list(range(20, 33))),      # multi-query (one kv head)
+]
+
+
+@pytest.mark.parametrize("case", TINY_CASES)
+def test_attention_matches_bruteforce(orc, case):
+    nh, nk, hd, hdkv, cap, pos = case
+    r = _rng(hash(str(case)) & 0xFFFF)
+    nt = len(pos)
+    q = r.standard_normal((nt, nh, hd)).astype(np.float32)
+    k = r.standard_normal((cap, nk * hdkv)).astype(np.float32)
+    v = r.standard_normal((cap, nk * hdkv)).astype(np.float32)
+    scale = float(np.float32(1.0) / np.sqrt(np.float32(hd)))
+    out = orc.gqa_attn(q, k, v, pos, nh, nk, hd, hdkv, scale=scale)
+    ref = orc.attn_bruteforce_f64(q, k, v, pos, nh, nk, hd, hdkv, scale)
+    err = np.abs(out - ref)
+    assert np.all(err <= 1e-5 + 1e-4 * np.abs(ref)), float(err.max())
+
+
+def test_bruteforce_is_not_vacuous(orc):
+    # a wrong kv-head mapping, a wrong window or a dropped scale would all move the
+    # result by far more than the tolerance used above
+    r = _rng(9)
+    nh, nk, hd, cap = 4, 2, 16, 8
+    q = r.standard_normal((2, nh, hd)).astype(np.float32)
+    k = r.standard_normal((cap, nk * hd)).astype(np.float32)
+    v = r.standard_normal((cap, nk * hd)).astype(np.float32)
+    scale = 0.25
+    ref = orc.attn_bruteforce_f64(q, k, v, [5, 7], nh, nk, hd, hd, scale)
+    swapped = orc.attn_bruteforce_f64(q, k[:, ::-1].copy(), v[:, ::-1].copy(), [5, 7], nh, nk, hd, hd, scale)
+    assert np.abs(ref - swapped).max() > 1e-2
+    shorter = orc.attn_bruteforce_f64(q, k, v, [4, 7], nh, nk, hd, hd, scale)
+    assert np.abs(ref[0] - shorter[0]).max() > 1e-2
+    unscaled = orc.attn_bruteforce_f64(q, k, v, [5, 7], nh, nk, hd, hd, 1.0)
+    assert np.abs(ref - unscaled).max() > 1e-2
+
+
+def test_gqa_equals_mha_with_repeated_kv(orc):
+    r = _rng(10)
+    nh, nk, hd, cap = 14, 2, 64, 40
+    g = nh // nk
+    pos = [39, 17, 3]
+    q = r.standard_normal((3, nh, hd)).astype(np.float32)
+    k = r.standard_normal((cap, nk * hd)).astype(np.float32)
+    v = r.standard_normal((cap, nk * hd)).astype(np.float32)
+    rep = lambda a: np.repeat(a.reshape(cap, nk, hd), g, axis=1).reshape(cap, nh * hd)
+    out_gqa = orc.gqa_attn(q, k, v, pos, nh, nk, hd, hd)
+    out_mha = orc.gqa_attn(q, rep(k), rep(v), pos, nh, nh, hd, hd)
+    np.testing.assert_array_equal(out_gqa, out_mha)
+
+
+def test_prefill_equals_successive_decode_steps(orc):
+    r = _rng(11)
+    nh, nk, hd, nt = 8, 2, 32, 24
+    q = r.standard_normal((nt, nh, hd)).astype(np.float32)
+    k = r.standard_normal((nt + 4, nk * hd)).astype(np.float32)
+    v = r.standard_normal((nt + 4, nk * hd)).astype(np.float32)
+    pre = orc.gqa_attn(q, k, v, list(range(nt)), nh, nk, hd, hd)
+    for t in range(nt):
+        dec = orc.gqa_attn(q[t:t + 1], k, v, [t], nh, nk, hd, hd)
+        np.testing.assert_array_equal(dec[0], pre[t])
+
+
+def test_bit_identical_at_any_thread_count(orc):
+    r = _rng(12)
+    nh, nk, hd, nt = 16, 8, 128, 9
+    q = r.standard_normal((nt, nh, hd)).astype(np.float32)
+    k = r.standard_normal((64, nk * hd)).astype(np.float32)
+    v = r.standard_normal((64, nk * hd)).astype(np.float32)
+    pos = [63, 10, 0, 31, 32, 5, 60, 62, 1]
+    ref = orc.gqa_attn(q, k, v, pos, nh, nk, hd, hd, n_threads=1)
+    for n in (2, 3, 7, 16):
+        np.testing.assert_array_equal(orc.gqa_attn(q, k, v, pos, nh, nk, hd, hd, n_threads=n), ref)
+
+
+def test_masked_rows_contribute_nothing(orc):
+    r = _rng(13)
+    nh, nk, hd, cap = 2, 1, 8, 10
+    q = r.standard_normal((2, nh, hd)).astype(np.float32)
+    k = r.standard_normal((cap, nk * hd)).astype(np.float32)
+    v = r.standard_normal((cap, nk * hd)).astype(np.float32)
+    ref = orc.gqa_attn(q, k, v, [2, 5], nh, nk, hd, hd)
+    k2, v2 = k.copy(), v.copy()
+    k2[3:6] *= 1e3    # inside nkv = 6 but beyond token 0's window: weight exactly 0
+    v2[3:6] = 1e30
+    k2[6:] = np.nan   # beyond nkv: never read
+    v2[6:] = np.nan
+    out = orc.gqa_attn(q, k2, v2, [2, 5], nh, nk, hd, hd)
+    np.testing.assert_array_equal(out[0], ref[0])
+
+
+def test_geometry_errors(orc):
+    q = np.zeros((1, 4, 8), np.float32)
+    kv = np.zeros((4, 16), np.float32)
+    with pytest.raises(orc.OracleError) as e:
+        orc.gqa_attn(q, kv, kv, [0], 4, 1, 8, 16)   # hd < hd_kv is refused
+    assert e.value.status == orc.ERR_GEOMETRY
+    with pytest.raises(orc.OracleError) as e:
+        orc.gqa_attn(np.zeros((1, 5, 8), np.float32), kv, kv, [0], 5, 2, 8, 8)
+    assert e.value.status == orc.ERR_GEOMETRY
+
+
+# --------------------------------------------------------------------------- SiLU, layer step
+def test_silu_mul(orc):
+    x = np.array([0.0, 1.0, -1.0, 20.0, -20.0, 3.5], np.float32)
+    up = np.array([1.0, 2.0, 1.0, 1.0, 1.0, -1.0], np.float32)
+    y = orc.silu_mul(x, up)
+    exp = [v / (1.0 + math.exp(-v)) * u for v, u in zip(x.tolist(), up.tolist())]
+    np.testing.assert_allclose(y, exp, rtol=3e-7, atol=1e-12)
+    assert y[0] == 0.0
+
+
+def test_layer_step_is_the_composition(orc):
+    r = _rng(14)
+    nh, nk, hd, hdkv, n_embd, cap = 4, 2, 16, 16, 24, 12
+    nt = 3
+    pos = [7, 8, 9]
+    h = r.standard_normal((nt, n_embd)).astype(np.float32)
+    gain = r.uniform(0.5, 1.5, n_embd).astype(np.float32)
+    q = r.standard_normal((nt, nh * hd)).astype(np.float32)
+    k = r.standard_normal((nt, nk * hdkv)).astype(np.float32)
+    v = r.standard_normal((nt, nk * hdkv)).astype(np.float32)
+    K = r.standard_normal((cap, nk * hdkv)).astype(np.float32)
+    V = r.standard_normal((cap, nk * hdkv)).astype(np.float32)
+    qs, ks, Ks, Vs = q.copy(), k.copy(), K.copy(), V.copy()
+    xn, out = orc.layer_attn_step(h, gain, qs, ks, v, pos, Ks, Vs, n_head=nh, n_kv_head=nk, hd=hd,
+                                  hd_kv=hdkv, eps=1e-6, theta=1e6)
+    np.testing.assert_array_equal(xn, orc.rms_norm(h, gain, eps=1e-6))
+    q2 = orc.rope(q.copy(), pos, nh, hd, 1e6)
+    k2 = orc.rope(k.copy(), pos, nk, hdkv, 1e6)
+    np.testing.assert_array_equal(qs, q2)
+    np.testing.assert_array_equal(ks, k2)
+    K2, V2 = K.copy(), V.copy()
+    orc.kv_append(K2, V2, k2, v, pos)
+    np.testing.assert_array_equal(Ks, K2)
+    np.testing.assert_array_equal(Vs, V2)
+    ref = orc.attn_bruteforce_f64(q2, K2, V2, pos, nh, nk, hd, hdkv, 1.0 / math.sqrt(hd))
+    assert np.all(np.abs(out - ref) <= 1e-5 + 1e-4 * np.abs(ref))
