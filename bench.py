@@ -1,0 +1,683 @@
+#!/usr/bin/env python
+"""Benchmark of the attention stage on one GB300 (and N independent replicas).
+
+Headline workload: long-context decode, Qwen3-0.6B shape (16 q heads, 8 kv heads,
+hd = hd_kv = 128, n_embd = 1024), 28 layers, an fp32 cache of 40960 rows per layer
+(9.4 GB), one new token at pos = 40960.  One step = one decode token through all 28
+layers: RMSNorm, RoPE on q and k, the in-place K/V append and split-KV attention,
+replayed from one captured CUDA graph.  Metric: decode attention KV-read GB/s
+(bytes of cached K and V the step must read, over the step time).
+
+The same JSON line carries the other configurations' numbers under "secondary"
+(single-step latency, prefill tokens/s, the decode loop, batched decode and the
+cache-length sweep), the roofline of the decode attention kernel, the end-to-end
+number with host buffers and the CPU oracle timed on this host.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl minf|reference]
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "decode attn KV-read GB/s vs HBM peak; layer attn-step µs; prefill tok/s"
+WORKLOAD = "long-context decode, Qwen3-0.6B shape, 28 layers, nkv=40960 (token at pos 40960)"
+L2_BYTES = 129 * 1024 * 1024
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["minf", "reference"], default="minf")
+    ap.add_argument("--no-secondary", action="store_true", help="headline workload only")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0, help="budget of the CPU oracle sample")
+    return ap.parse_args(argv)
+
+
+# ----------------------------------------------------------------------------- distributed
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def init_dist(world, backend):
+    import torch.distributed as dist
+
+    if world > 1 and not dist.is_initialized():
+        dist.init_process_group(backend=backend)
+    return dist
+
+
+def max_over_ranks(value: float, world: int, device="cpu") -> float:
+    """Max of a per-rank float over all ranks (identity at world size 1)."""
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+# ----------------------------------------------------------------------------- clocks
+class ClockSampler:
+    """Samples SM clocks and throttle reasons with nvidia-smi while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        rows = []
+        try:
+            for line in open(self.path):
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        finally:
+            try:
+                os.remove(self.path)
+            except OSError:
+                pass
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            for i, n in enumerate(names):
+                if r[5 + i].lower().startswith("active"):
+                    reasons.add(n)
+        loaded = [s for s in sm if s > 0.5 * (max(mx) if mx else 1)] or sm
+        return {"sm_mhz": statistics.median(loaded) if loaded else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": sorted(reasons),
+                "samples": len(rows)}
+
+
+# ----------------------------------------------------------------------------- helpers
+def smi_gpu_id(local_index: int) -> str:
+    """nvidia-smi's id of torch's device `local_index` (CUDA_VISIBLE_DEVICES remaps indices)."""
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES", "").strip()
+    if vis:
+        ids = [x.strip() for x in vis.split(",") if x.strip()]
+        if local_index < len(ids):
+            return ids[local_index]
+    return str(local_index)
+
+
+def measured_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 6800.0, "fallback"
+
+
+def decode_traffic_record():
+    """DRAM bytes per decode-attention launch from the committed ncu summary, valid only
+    while the kernel source is unchanged since the counters were taken."""
+    path = os.path.join(ROOT, "profiles", "decode_attn_traffic.json")
+    src = os.path.join(ROOT, "gqa_attention_kv_rope_gb300", "csrc", "minf_decode.cu")
+    try:
+        rec = json.load(open(path))
+        sha = hashlib.sha256(open(src, "rb").read()).hexdigest()
+        if rec.get("kernel_src_sha256") != sha:
+            return None, rec
+        return rec, rec
+    except (OSError, ValueError):
+        return None, None
+
+
+class Timer:
+    def __init__(self, torch, stream):
+        self.torch, self.stream = torch, stream
+
+    def pair(self):
+        a = self.torch.cuda.Event(enable_timing=True)
+        b = self.torch.cuda.Event(enable_timing=True)
+        return a, b
+
+
+def flush_l2(buf):
+    buf.zero_()
+
+
+# ----------------------------------------------------------------------------- workloads
+def setup_long_context(m, torch, wl, n_cached, dev):
+    g = wl.QWEN3_06B
+    cap = wl.LONG_CONTEXT_CAP
+    regions = m.kv.KvRegions(g.n_layer, g.row_width, cap, device=dev)
+    for layer in range(g.n_layer):
+        k, v = regions.view(layer)
+        gen = torch.Generator(device=dev)
+        gen.manual_seed(wl.sub_seed("long-context", layer, "K"))
+        k.normal_(generator=gen)
+        gen.manual_seed(wl.sub_seed("long-context", layer, "V"))
+        v.normal_(generator=gen)
+    # per-layer step inputs packed [layers, h | q | k | v] so one copy moves them all
+    widths = (g.n_embd, g.q_width, g.row_width, g.row_width)
+    inputs = torch.empty(g.n_layer, sum(widths), device=dev)
+    for layer in range(g.n_layer):
+        d = wl.layer_inputs(g, "long-context", layer, 1)
+        inputs[layer] = torch.cat([d["h"][0], d["q"][0], d["k"][0], d["v"][0]]).to(dev)
+    gains = torch.stack([wl.layer_inputs(g, "long-context", l, 1)["gain"] for l in range(g.n_layer)]).to(dev)
+    outs = torch.empty(g.n_layer, g.n_embd + g.out_width, device=dev)  # xn | out
+    return {"g": g, "cap": cap, "regions": regions, "inputs": inputs, "gains": gains, "outs": outs,
+            "widths": widths, "pos": torch.tensor([n_cached], dtype=torch.int32, device=dev),
+            "err": torch.zeros(1, dtype=torch.int32, device=dev),
+            "ws": m.kv.decode_workspace(1, g.n_head, g.n_kv_head, g.hd_kv, cap, device=dev)}
+
+
+def views(S, layer):
+    g = S["g"]
+    x = S["inputs"][layer]
+    a, b, c, _ = S["widths"]
+    h = x[:a].view(1, a)
+    q = x[a:a + b].view(1, b)
+    k = x[a + b:a + b + c].view(1, c)
+    v = x[a + b + c:].view(1, c)
+    o = S["outs"][layer]
+    xn = o[:g.n_embd].view(1, g.n_embd)
+    out = o[g.n_embd:].view(1, g.out_width)
+    return h, q, k, v, xn, out
+
+
+def decode_step(m, S, layers=None):
+    g = S["g"]
+    for layer in range(g.n_layer) if layers is None else layers:
+        h, q, k, v, xn, out = views(S, layer)
+        K, V = S["regions"].view(layer)
+        m.binding.minf_layer_attn_step(xn, h, S["gains"][layer], g.eps, q, k, v, S["pos"], K, V, g.n_head,
+                                       g.n_kv_head, g.hd, g.hd_kv, g.theta, g.freq_scale, 0, out, S["ws"],
+                                       S["err"])
+
+
+def capture(torch, stream, fn):
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        fn()  # warm-up outside the capture
+    torch.cuda.synchronize()
+    with torch.cuda.graph(graph, stream=stream):
+        fn()
+    torch.cuda.synchronize()
+    return graph
+
+
+def kv_bytes_long_context(g, pos):
+    return g.n_layer * 2 * (pos + 1) * g.row_width * 4
+
+
+def run_headline(m, torch, wl, args, world, dev):
+    stream = torch.cuda.Stream()
+    n = wl.LONG_CONTEXT_SWEEP[-1]
+    S = setup_long_context(m, torch, wl, n, dev)
+    g = S["g"]
+    graph = capture(torch, stream, lambda: decode_step(m, S))
+    bytes_step = kv_bytes_long_context(g, n)
+    for _ in range(args.warmup):
+        graph.replay()
+    torch.cuda.synchronize()
+    barrier(world)
+    t0, t1 = Timer(torch, stream).pair()
+    with ClockSampler(smi_gpu_id(torch.cuda.current_device())) as clk:
+        torch.cuda.synchronize()
+        barrier(world)
+        with torch.cuda.stream(stream):
+            t0.record(stream)
+            for _ in range(args.steps):
+                graph.replay()
+            t1.record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+    ms_total = t0.elapsed_time(t1)
+    clocks = clk.summary()
+    ms_total = max_over_ranks(ms_total, world, device=dev)
+    ms_step = ms_total / args.steps
+    err = int(S["err"].item())
+
+    # the dominant kernel, timed alone per launch with events on its own stream
+    kern_ms = []
+    with torch.cuda.stream(stream):
+        for it in range(max(2, args.steps // 4)):
+            for layer in range(g.n_layer):
+                h, q, k, v, xn, out = views(S, layer)
+                K, V = S["regions"].view(layer)
+                m.binding.minf_rope_kv_append(q, k, v, S["pos"], g.n_head, g.n_kv_head, g.hd, g.hd_kv, g.theta,
+                                              g.freq_scale, 0, K, V, S["err"])
+                a, b = Timer(torch, stream).pair()
+                a.record(stream)
+                m.binding.minf_gqa_attn_decode(out, q, K, V, None, None, S["cap"], S["pos"], g.n_head,
+                                               g.n_kv_head, g.hd, g.hd_kv, 1.0 / (g.hd ** 0.5), S["ws"], S["err"])
+                b.record(stream)
+                kern_ms.append((a, b))
+    torch.cuda.synchronize()
+    kern = [a.elapsed_time(b) for a, b in kern_ms]
+    kern_avg_ms = sum(kern) / len(kern)
+
+    # end to end: the step's inputs from pinned host memory, its outputs back to the host
+    host_in = torch.empty_like(S["inputs"], device="cpu").pin_memory()
+    host_in.copy_(S["inputs"].cpu())
+    host_out = torch.empty_like(S["outs"], device="cpu").pin_memory()
+    e0, e1 = Timer(torch, stream).pair()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(args.steps):
+            S["inputs"].copy_(host_in, non_blocking=True)
+            graph.replay()
+            host_out.copy_(S["outs"], non_blocking=True)
+            stream.synchronize()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, world, device=dev)
+    h2d = S["inputs"].numel() * 4
+    d2h = S["outs"].numel() * 4
+    res = {"S": S, "graph": graph, "stream": stream, "ms_step": ms_step, "bytes_step": bytes_step,
+           "clocks": clocks, "err": err, "kern_avg_ms": kern_avg_ms, "kern_launches": len(kern),
+           "kern_bytes": 2 * (n + 1) * g.row_width * 4, "e2e_ms": e2e_ms, "h2d": h2d, "d2h": d2h,
+           "launches_per_step": 3 * g.n_layer}
+    return res
+
+
+def run_sweep(m, torch, wl, H, args):
+    S, graph, stream = H["S"], H["graph"], H["stream"]
+    g = S["g"]
+    flush = torch.empty(2 * L2_BYTES // 4, device=S["inputs"].device)
+    out = {}
+    for n in wl.LONG_CONTEXT_SWEEP:
+        S["pos"].fill_(n)
+        torch.cuda.synchronize()
+        for _ in range(2):
+            graph.replay()
+        times = []
+        for _ in range(max(3, args.steps // 2)):
+            flush_l2(flush)
+            a, b = Timer(torch, stream).pair()
+            with torch.cuda.stream(stream):
+                a.record(stream)
+                graph.replay()
+                b.record(stream)
+            torch.cuda.synchronize()
+            times.append(a.elapsed_time(b))
+        ms = statistics.median(times)
+        out[str(n)] = round(kv_bytes_long_context(g, n) / (ms * 1e-3) / 1e9, 1)
+    S["pos"].fill_(wl.LONG_CONTEXT_SWEEP[-1])
+    del flush
+    return out
+
+
+def run_single_step(m, torch, wl, dev, reps=1000):
+    """Single decode step, one layer, Qwen2.5-0.5B shape, 127 cached rows, token at pos 127."""
+    g = wl.QWEN25_05B
+    cap, p = 639, wl.SINGLE_STEP_CACHED_ROWS
+    kc, vc = wl.cache_rows(g, "single-step", 0, p)
+    K = torch.zeros(cap, g.row_width, device=dev)
+    V = torch.zeros(cap, g.row_width, device=dev)
+    K[:p], V[:p] = kc.to(dev), vc.to(dev)
+    d = {k: v.to(dev) for k, v in wl.layer_inputs(g, "single-step", 0, 1).items()}
+    pos = torch.tensor([p], dtype=torch.int32, device=dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    xn = torch.empty_like(d["h"])
+    out = torch.empty(1, g.out_width, device=dev)
+    ws = m.kv.decode_workspace(1, g.n_head, g.n_kv_head, g.hd_kv, cap, device=dev)
+    stream = torch.cuda.Stream()
+    fn = lambda: m.binding.minf_layer_attn_step(xn, d["h"], d["gain"], g.eps, d["q"], d["k"], d["v"], pos, K, V,
+                                                g.n_head, g.n_kv_head, g.hd, g.hd_kv, g.theta, 1.0, 0, out,
+                                                ws, err)
+    graph = capture(torch, stream, fn)
+    for _ in range(20):
+        graph.replay()
+    torch.cuda.synchronize()
+    pairs = []
+    with torch.cuda.stream(stream):
+        for _ in range(reps):
+            a, b = Timer(torch, stream).pair()
+            a.record(stream)
+            graph.replay()
+            b.record(stream)
+            pairs.append((a, b))
+    torch.cuda.synchronize()
+    us = [a.elapsed_time(b) * 1e3 for a, b in pairs]
+    return round(statistics.median(us), 2)
+
+
+def run_prefill(m, torch, wl, dev, steps):
+    """Causal prefill, Qwen2.5-0.5B shape, 24 layers, 512 tokens at positions 0..511."""
+    g = wl.QWEN25_05B
+    nt, cap = wl.PREFILL_TOKENS, wl.PREFILL_TOKENS + wl.KV_HEADROOM_ROWS
+    regions = m.kv.KvRegions(g.n_layer, g.row_width, cap, device=dev)
+    regions.k.zero_()
+    regions.v.zero_()
+    L = []
+    for layer in range(g.n_layer):
+        d = {k: v.to(dev) for k, v in wl.layer_inputs(g, "prefill", layer, nt).items()}
+        d["xn"] = torch.empty_like(d["h"])
+        d["out"] = torch.empty(nt, g.out_width, device=dev)
+        L.append(d)
+    pos = torch.arange(nt, dtype=torch.int32, device=dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    ws = m.kv.prefill_workspace(nt, g.n_head, g.n_kv_head, g.hd_kv, cap, device=dev)
+
+    def step():
+        for layer in range(g.n_layer):
+            d = L[layer]
+            K, V = regions.view(layer)
+            m.binding.minf_layer_attn_step(d["xn"], d["h"], d["gain"], g.eps, d["q"], d["k"], d["v"], pos, K, V,
+                                           g.n_head, g.n_kv_head, g.hd, g.hd_kv, g.theta, 1.0, 0, d["out"], ws,
+                                           err)
+
+    stream = torch.cuda.Stream()
+    graph = capture(torch, stream, step)
+    flush = torch.empty(2 * L2_BYTES // 4, device=dev)
+    times = []
+    for i in range(steps + 3):
+        flush_l2(flush)
+        a, b = Timer(torch, stream).pair()
+        with torch.cuda.stream(stream):
+            a.record(stream)
+            graph.replay()
+            b.record(stream)
+        torch.cuda.synchronize()
+        if i >= 3:
+            times.append(a.elapsed_time(b))
+    ms = statistics.median(times)
+    return round(nt / (ms * 1e-3), 1), round(ms * 1e3 / g.n_layer, 2)
+
+
+def run_decode_loop(m, torch, wl, dev):
+    """Decode loop, Qwen3-0.6B shape: 511-token prefill into 1023-row regions, then 64
+    decode steps (28 layers each) replayed from one graph with pos 511..574."""
+    g = wl.QWEN3_06B
+    n0, cap, steps = wl.DECODE_LOOP_PROMPT, wl.DECODE_LOOP_PROMPT + wl.KV_HEADROOM_ROWS, wl.DECODE_LOOP_STEPS
+    regions = m.kv.KvRegions(g.n_layer, g.row_width, cap, device=dev)
+    regions.k.zero_()
+    regions.v.zero_()
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    ws = m.kv.prefill_workspace(n0, g.n_head, g.n_kv_head, g.hd_kv, cap, device=dev)
+    pos_p = torch.arange(n0, dtype=torch.int32, device=dev)
+    for layer in range(g.n_layer):
+        d = {k: v.to(dev) for k, v in wl.layer_inputs(g, "decode-loop", layer, n0 + steps).items()}
+        K, V = regions.view(layer)
+        xn = torch.empty(n0, g.n_embd, device=dev)
+        out = torch.empty(n0, g.out_width, device=dev)
+        m.binding.minf_layer_attn_step(xn, d["h"][:n0].contiguous(), d["gain"], g.eps, d["q"][:n0].contiguous(),
+                                       d["k"][:n0].contiguous(), d["v"][:n0].contiguous(), pos_p, K, V, g.n_head,
+                                       g.n_kv_head, g.hd, g.hd_kv, g.theta, 1.0, 0, out, ws, err)
+    pos = torch.tensor([n0], dtype=torch.int32, device=dev)
+    wsd = m.kv.decode_workspace(1, g.n_head, g.n_kv_head, g.hd_kv, cap, device=dev)
+    bufs = [{"h": torch.randn(1, g.n_embd, device=dev), "gain": torch.ones(g.n_embd, device=dev),
+             "q": torch.randn(1, g.q_width, device=dev), "k": torch.randn(1, g.row_width, device=dev),
+             "v": torch.randn(1, g.row_width, device=dev), "xn": torch.empty(1, g.n_embd, device=dev),
+             "out": torch.empty(1, g.out_width, device=dev)} for _ in range(g.n_layer)]
+
+    def step():
+        for layer in range(g.n_layer):
+            b = bufs[layer]
+            K, V = regions.view(layer)
+            m.binding.minf_layer_attn_step(b["xn"], b["h"], b["gain"], g.eps, b["q"], b["k"], b["v"], pos, K, V,
+                                           g.n_head, g.n_kv_head, g.hd, g.hd_kv, g.theta, 1.0, 0, b["out"], wsd,
+                                           err)
+
+    stream = torch.cuda.Stream()
+    graph = capture(torch, stream, step)  # the capture's warm-up wrote row 511: rewritten below
+    pos_host = torch.empty(1, dtype=torch.int32).pin_memory()
+    times, kv = [], 0
+    for i in range(steps):
+        p = n0 + i
+        pos_host.fill_(p)
+        a, b = Timer(torch, stream).pair()
+        with torch.cuda.stream(stream):
+            pos.copy_(pos_host, non_blocking=True)
+            a.record(stream)
+            graph.replay()
+            b.record(stream)
+        torch.cuda.synchronize()
+        times.append(a.elapsed_time(b))
+        kv += g.n_layer * 2 * (p + 1) * g.row_width * 4
+    total_ms = sum(times)
+    return {"step_us_median": round(statistics.median(times) * 1e3, 2),
+            "kv_read_gbs": round(kv / (total_ms * 1e-3) / 1e9, 1), "err": int(err.item())}
+
+
+def run_batched(m, torch, wl, dev, steps):
+    """Batched decode: 64 sequences, lengths ~ U{1..8192} (seeded), 28 layers, one graph."""
+    g = wl.QWEN3_06B
+    lengths = wl.batched_lengths(seed=0)
+    caps = [ln + 1 + wl.KV_HEADROOM_ROWS for ln in lengths]
+    arena = m.kv.KvArena(g.n_layer, g.row_width, caps, device=dev)
+    gen = torch.Generator(device=dev)
+    for layer in range(g.n_layer):
+        gen.manual_seed(wl.sub_seed("batched", layer, "K"))
+        arena.k[layer].normal_(generator=gen)
+        gen.manual_seed(wl.sub_seed("batched", layer, "V"))
+        arena.v[layer].normal_(generator=gen)
+    n = len(lengths)
+    pos = torch.tensor(lengths, dtype=torch.int32, device=dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    ws = m.kv.decode_workspace(n, g.n_head, g.n_kv_head, g.hd_kv, arena.max_cap, device=dev)
+    L = []
+    for layer in range(g.n_layer):
+        d = {k: v.to(dev) for k, v in wl.layer_inputs(g, "batched", layer, n).items()}
+        d["xn"] = torch.empty_like(d["h"])
+        d["out"] = torch.empty(n, g.out_width, device=dev)
+        L.append(d)
+
+    def step():
+        for layer in range(g.n_layer):
+            d = L[layer]
+            K, V = arena.view(layer)
+            m.binding.minf_layer_attn_step_batched(d["xn"], d["h"], d["gain"], g.eps, d["q"], d["k"], d["v"], pos,
+                                                   K, V, arena.row_off, arena.cap, arena.max_cap, g.n_head,
+                                                   g.n_kv_head, g.hd, g.hd_kv, g.theta, 1.0, 0, d["out"], ws, err)
+
+    stream = torch.cuda.Stream()
+    graph = capture(torch, stream, step)
+    for _ in range(2):
+        graph.replay()
+    torch.cuda.synchronize()
+    a, b = Timer(torch, stream).pair()
+    with torch.cuda.stream(stream):
+        a.record(stream)
+        for _ in range(steps):
+            graph.replay()
+        b.record(stream)
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / steps
+    kv = g.n_layer * sum(2 * (ln + 1) * g.row_width * 4 for ln in lengths)
+    res = {"step_ms": round(ms, 3), "kv_read_gbs": round(kv / (ms * 1e-3) / 1e9, 1),
+           "kv_bytes_per_step": kv, "max_len": max(lengths), "err": int(err.item())}
+    del arena
+    torch.cuda.empty_cache()
+    return res
+
+
+# ----------------------------------------------------------------------------- CPU oracle
+def oracle_sample(budget_s: float, host_arrays=None):
+    """The oracle (as it stands) on a bounded sample of the headline workload: whole layer
+    steps at nkv=40960, head-parallel over this host's cores, until the budget is spent."""
+    import numpy as np
+
+    import oracle
+    from gqa_attention_kv_rope_gb300 import workloads as wl
+
+    oracle.build()
+    g = wl.QWEN3_06B
+    n = wl.LONG_CONTEXT_SWEEP[-1]
+    cap = n + 1
+    cores = os.cpu_count() or 1
+    rng = np.random.default_rng(wl.sub_seed("long-context-cpu", 0))
+    K = rng.standard_normal((cap, g.row_width), dtype=np.float32)
+    V = rng.standard_normal((cap, g.row_width), dtype=np.float32)
+    layers, t_total, kv = 0, 0.0, 0
+    while t_total < budget_s or layers == 0:
+        d = wl.layer_inputs(g, "long-context", layers % g.n_layer, 1)
+        q, k = d["q"].numpy().copy(), d["k"].numpy().copy()
+        t0 = time.perf_counter()
+        oracle.layer_attn_step(d["h"].numpy(), d["gain"].numpy(), q, k, d["v"].numpy(), [n], K, V,
+                               n_head=g.n_head, n_kv_head=g.n_kv_head, hd=g.hd, hd_kv=g.hd_kv, eps=g.eps,
+                               theta=g.theta, n_threads=cores)
+        t_total += time.perf_counter() - t0
+        kv += 2 * (n + 1) * g.row_width * 4
+        layers += 1
+    return {"value": round(kv / t_total / 1e9, 3), "unit": "GB/s", "cores": min(cores, g.n_head),
+            "kind": "oracle",
+            "sample": f"{layers} layer step(s) of the headline workload at nkv=40960 "
+                      f"(one layer = {2 * (n + 1) * g.row_width * 4} KV bytes), head-parallel threads"}
+
+
+def run_reference(args):
+    world, rank, _ = dist_env()
+    if world > 1:
+        init_dist(world, "gloo")
+        if rank != 0:
+            return 0
+    per_step = max(args.cpu_seconds / max(args.steps + args.warmup, 1), 0.5)
+    for _ in range(args.warmup):
+        oracle_sample(0.0)
+    vals = []
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        vals.append(oracle_sample(per_step))
+    wall = time.perf_counter() - t0
+    v = statistics.median(x["value"] for x in vals)
+    cb = dict(vals[0])
+    cb["value"] = v
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "GB/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(wall * 1e3 / args.steps, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic", "config": {"workload": WORKLOAD, "l2": "inputs larger than L2"},
+            "cpu_baseline": cb, "e2e": {"value": v, "unit": "GB/s", "h2d_bytes_per_step": 0,
+                                        "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+    return 0
+
+
+# ----------------------------------------------------------------------------- main
+def main(argv=None):
+    args = parse_args(argv)
+    if args.impl == "reference":
+        return run_reference(args)
+    import torch
+
+    world, rank, local = dist_env()
+    if not torch.cuda.is_available():
+        print(json.dumps({"metric": METRIC, "error": "no CUDA device"}))
+        return 1
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        init_dist(world, "nccl")
+    import __graft_entry__
+
+    if rank == 0:
+        __graft_entry__.build()
+    barrier(world)
+    import gqa_attention_kv_rope_gb300 as m
+    from gqa_attention_kv_rope_gb300 import workloads as wl
+
+    m.binding.lib()
+    H = run_headline(m, torch, wl, args, world, dev)
+    g = H["S"]["g"]
+    value = world * H["bytes_step"] / (H["ms_step"] * 1e-3) / 1e9
+    peak, peak_kind = measured_peaks()
+    achieved = H["kern_bytes"] / (H["kern_avg_ms"] * 1e-3) / 1e9
+    traffic_rec, _ = decode_traffic_record()
+    secondary = {}
+    if not args.no_secondary and rank == 0:
+        secondary["long_context_sweep_gbs"] = run_sweep(m, torch, wl, H, args)
+    errs = H["err"]
+    del H["graph"]
+    H["S"].clear()
+    torch.cuda.empty_cache()
+    if not args.no_secondary and rank == 0:
+        secondary["single_step_layer_attn_us"] = run_single_step(m, torch, wl, dev)
+        tok_s, layer_us = run_prefill(m, torch, wl, dev, max(5, args.steps // 2))
+        secondary["prefill_tok_s"] = tok_s
+        secondary["prefill_layer_us"] = layer_us
+        secondary["decode_loop"] = run_decode_loop(m, torch, wl, dev)
+        secondary["batched_decode"] = run_batched(m, torch, wl, dev, max(3, args.steps // 4))
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = oracle_sample(args.cpu_seconds)
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(H["ms_step"], 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "n_layer": g.n_layer, "n_head": g.n_head, "n_kv_head": g.n_kv_head,
+                   "hd": g.hd, "nkv": wl.LONG_CONTEXT_SWEEP[-1], "kv_bytes_per_step": H["bytes_step"],
+                   "l2": "inputs larger than L2 (9.4 GB cache per replica)", "graph": "one CUDA graph per step",
+                   "parallelism": f"replicas x{world}"},
+        "roofline": {"bound": "hbm", "kernel": "decode_split_kernel<128,2>", "achieved": round(achieved, 1),
+                     "peak": peak, "peak_kind": peak_kind, "unit": "GB/s", "frac": round(achieved / peak, 4),
+                     "traffic": traffic_rec["traffic_bytes_per_launch"] if traffic_rec else None,
+                     "algorithmic_bytes_per_launch": H["kern_bytes"], "avg_launch_us": round(H["kern_avg_ms"] * 1e3, 2),
+                     "launches_timed": H["kern_launches"]},
+        "e2e": {"value": round(world * H["bytes_step"] / (H["e2e_ms"] * 1e-3) / 1e9, 1), "unit": "GB/s",
+                "h2d_bytes_per_step": H["h2d"], "d2h_bytes_per_step": H["d2h"],
+                "ms_per_step": round(H["e2e_ms"], 4)},
+        "gpu_launches": H["launches_per_step"] * args.steps,
+        "clocks": H["clocks"],
+        "device_error_word": errs,
+        "secondary": secondary,
+    }
+    if cpu is not None:
+        line["cpu_baseline"] = cpu
+    if rank == 0:
+        print(json.dumps(line))
+    barrier(world)
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

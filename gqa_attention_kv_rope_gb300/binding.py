@@ -1,0 +1,210 @@
+"""Thin Python binding over libminf.so: argument marshalling only.
+
+Every function has the C ABI's name and argument order (include/minf.h), takes
+torch CUDA tensors in place of device pointers, and raises MinfError on a
+non-zero status.  All arithmetic runs in the library's kernels; there is no
+CPU path.  If the library is missing, the first call raises -- nothing falls
+back to another implementation.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+from . import build as _build
+
+_lock = threading.Lock()
+_lib = None
+
+MINF_OK = 0
+MINF_ERR_ARG = 1
+MINF_ERR_GEOMETRY = 2
+MINF_ERR_UNSUPPORTED = 3
+MINF_ERR_WORKSPACE = 5
+MINF_ERR_CUDA = 6
+ERRBIT_STORE_POS = 0x1
+ERRBIT_ROPE_POS = 0x2
+ERRBIT_ATTN_POS = 0x4
+
+_P = ctypes.c_void_p
+_I = ctypes.c_int
+_F = ctypes.c_float
+_SZ = ctypes.c_size_t
+_I64 = ctypes.c_int64
+
+_SIGS = {
+    "minf_status_string": ([_I], ctypes.c_char_p),
+    "minf_version": ([], _I),
+    "minf_rope_freqs": ([_P, _I, _F, _F], _I),
+    "minf_rms_norm": ([_P, _P, _P, _I, _I, _F, _P], _I),
+    "minf_rope": ([_P, _P, _I, _I, _I, _F, _F, _I, _P, _P], _I),
+    "minf_kv_append": ([_P, _P, _I, _I, _P, _P, _P, _I, _P, _P], _I),
+    "minf_rope_kv_append": ([_P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _F, _I, _P, _P, _I, _P, _P], _I),
+    "minf_attn_decode_workspace_bytes": ([_I, _I, _I, _I, _I], _SZ),
+    "minf_attn_prefill_workspace_bytes": ([_I, _I, _I, _I, _I], _SZ),
+    "minf_gqa_attn_decode": ([_P, _P, _P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _I, _F, _P, _SZ, _P, _P], _I),
+    "minf_gqa_attn_prefill": ([_P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _I, _F, _P, _SZ, _P, _P], _I),
+    "minf_layer_attn_step": ([_P, _P, _P, _F, _I, _P, _P, _P, _P, _I, _P, _P, _I, _I, _I, _I, _I,
+                              _F, _F, _I, _P, _P, _SZ, _P, _P], _I),
+    "minf_layer_attn_step_batched": ([_P, _P, _P, _F, _I, _P, _P, _P, _P, _I, _P, _P, _P, _P, _I,
+                                      _I, _I, _I, _I, _F, _F, _I, _P, _P, _SZ, _P, _P], _I),
+    "minf_silu_mul": ([_P, _P, _P, _I64, _P], _I),
+}
+
+
+class MinfError(RuntimeError):
+    def __init__(self, status: int, name: str):
+        msg = lib().minf_status_string(status).decode() if _lib is not None else str(status)
+        super().__init__(f"{name}: status {status} ({msg})")
+        self.status = status
+
+
+def lib_path() -> str:
+    return _build.LIB
+
+
+def lib():
+    """The loaded library (ctypes).  Raises if libminf.so has not been built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    with _lock:
+        if _lib is None:
+            path = _build.LIB
+            if not os.path.exists(path):
+                raise RuntimeError(f"libminf.so is not built ({path}); run "
+                                   "`python -c 'import __graft_entry__ as g; g.build()'` first")
+            handle = ctypes.CDLL(path)
+            for name, (args, res) in _SIGS.items():
+                fn = getattr(handle, name)
+                fn.argtypes = args
+                fn.restype = res
+            _lib = handle
+    return _lib
+
+
+def _check(status: int, name: str):
+    if status != MINF_OK:
+        raise MinfError(status, name)
+
+
+def _dev(t, dtype=torch.float32, name="tensor"):
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def minf_rope_freqs(hd: int, theta: float, freq_scale: float = 1.0) -> list[float]:
+    import array
+
+    buf = (ctypes.c_float * max(hd // 2, 1))()
+    _check(lib().minf_rope_freqs(ctypes.cast(buf, _P), hd, theta, freq_scale), "minf_rope_freqs")
+    return array.array("f", buf[: hd // 2])
+
+
+def minf_rms_norm(y, x, w, eps: float, stream=None):
+    rows, n = x.shape
+    _check(lib().minf_rms_norm(_dev(y, name="y"), _dev(x, name="x"), _dev(w, name="w"), rows, n, eps,
+                               _stream(stream)), "minf_rms_norm")
+
+
+def minf_rope(x, pos, n_head: int, hd: int, theta: float, freq_scale: float, style: int, err,
+              stream=None):
+    nt = pos.numel()
+    _check(lib().minf_rope(_dev(x, name="x"), _dev(pos, torch.int32, "pos"), nt, n_head, hd, theta,
+                           freq_scale, style, _dev(err, torch.int32, "err"), _stream(stream)),
+           "minf_rope")
+
+
+def minf_kv_append(k_reg, v_reg, k_rows, v_rows, pos, err, stream=None):
+    cap, W = k_reg.shape
+    _check(lib().minf_kv_append(_dev(k_reg, name="k_reg"), _dev(v_reg, name="v_reg"), cap, W,
+                                _dev(k_rows, name="k_rows"), _dev(v_rows, name="v_rows"),
+                                _dev(pos, torch.int32, "pos"), pos.numel(),
+                                _dev(err, torch.int32, "err"), _stream(stream)), "minf_kv_append")
+
+
+def minf_rope_kv_append(q, k, v, pos, n_head, n_kv_head, hd, hd_kv, theta, freq_scale, style, k_reg,
+                        v_reg, err, stream=None):
+    cap = k_reg.shape[0]
+    _check(lib().minf_rope_kv_append(_dev(q, name="q"), _dev(k, name="k"), _dev(v, name="v"),
+                                     _dev(pos, torch.int32, "pos"), pos.numel(), n_head, n_kv_head,
+                                     hd, hd_kv, theta, freq_scale, style, _dev(k_reg, name="k_reg"),
+                                     _dev(v_reg, name="v_reg"), cap, _dev(err, torch.int32, "err"),
+                                     _stream(stream)), "minf_rope_kv_append")
+
+
+def minf_attn_decode_workspace_bytes(n_seq, n_head, n_kv_head, hd_kv, max_cap) -> int:
+    return int(lib().minf_attn_decode_workspace_bytes(n_seq, n_head, n_kv_head, hd_kv, max_cap))
+
+
+def minf_attn_prefill_workspace_bytes(nt, n_head, n_kv_head, hd_kv, cap) -> int:
+    return int(lib().minf_attn_prefill_workspace_bytes(nt, n_head, n_kv_head, hd_kv, cap))
+
+
+def minf_gqa_attn_decode(out, q, k_reg, v_reg, seq_row_off, seq_cap, max_cap, pos, n_head, n_kv_head,
+                         hd, hd_kv, scale, ws, err, stream=None):
+    _check(lib().minf_gqa_attn_decode(
+        _dev(out, name="out"), _dev(q, name="q"), _dev(k_reg, name="k_reg"), _dev(v_reg, name="v_reg"),
+        _dev(seq_row_off, torch.int64, "seq_row_off"), _dev(seq_cap, torch.int32, "seq_cap"), max_cap,
+        _dev(pos, torch.int32, "pos"), pos.numel(), n_head, n_kv_head, hd, hd_kv, scale,
+        _dev(ws, torch.uint8, "ws"), ws.numel(), _dev(err, torch.int32, "err"), _stream(stream)),
+        "minf_gqa_attn_decode")
+
+
+def minf_gqa_attn_prefill(out, q, k_reg, v_reg, pos, n_head, n_kv_head, hd, hd_kv, scale, ws, err,
+                          stream=None):
+    cap = k_reg.shape[0]
+    _check(lib().minf_gqa_attn_prefill(
+        _dev(out, name="out"), _dev(q, name="q"), _dev(k_reg, name="k_reg"), _dev(v_reg, name="v_reg"),
+        cap, _dev(pos, torch.int32, "pos"), pos.numel(), n_head, n_kv_head, hd, hd_kv, scale,
+        _dev(ws, torch.uint8, "ws"), ws.numel(), _dev(err, torch.int32, "err"), _stream(stream)),
+        "minf_gqa_attn_prefill")
+
+
+def minf_layer_attn_step(xn, h, gain, eps, q, k, v, pos, k_reg, v_reg, n_head, n_kv_head, hd, hd_kv,
+                         theta, freq_scale, style, out, ws, err, stream=None):
+    nt, n_embd = h.shape
+    cap = k_reg.shape[0]
+    _check(lib().minf_layer_attn_step(
+        _dev(xn, name="xn"), _dev(h, name="h"), _dev(gain, name="gain"), eps, n_embd,
+        _dev(q, name="q"), _dev(k, name="k"), _dev(v, name="v"), _dev(pos, torch.int32, "pos"), nt,
+        _dev(k_reg, name="k_reg"), _dev(v_reg, name="v_reg"), cap, n_head, n_kv_head, hd, hd_kv,
+        theta, freq_scale, style, _dev(out, name="out"), _dev(ws, torch.uint8, "ws"), ws.numel(),
+        _dev(err, torch.int32, "err"), _stream(stream)), "minf_layer_attn_step")
+
+
+def minf_layer_attn_step_batched(xn, h, gain, eps, q, k, v, pos, k_arena, v_arena, seq_row_off, seq_cap,
+                                 max_cap, n_head, n_kv_head, hd, hd_kv, theta, freq_scale, style, out,
+                                 ws, err, stream=None):
+    n_seq, n_embd = h.shape
+    _check(lib().minf_layer_attn_step_batched(
+        _dev(xn, name="xn"), _dev(h, name="h"), _dev(gain, name="gain"), eps, n_embd,
+        _dev(q, name="q"), _dev(k, name="k"), _dev(v, name="v"), _dev(pos, torch.int32, "pos"), n_seq,
+        _dev(k_arena, name="k_arena"), _dev(v_arena, name="v_arena"),
+        _dev(seq_row_off, torch.int64, "seq_row_off"), _dev(seq_cap, torch.int32, "seq_cap"), max_cap,
+        n_head, n_kv_head, hd, hd_kv, theta, freq_scale, style, _dev(out, name="out"),
+        _dev(ws, torch.uint8, "ws"), ws.numel(), _dev(err, torch.int32, "err"), _stream(stream)),
+        "minf_layer_attn_step_batched")
+
+
+def minf_silu_mul(y, gate, up, stream=None):
+    _check(lib().minf_silu_mul(_dev(y, name="y"), _dev(gate, name="gate"), _dev(up, name="up"),
+                               gate.numel(), _stream(stream)), "minf_silu_mul")

@@ -1,0 +1,235 @@
+// minf_api.cu -- the C ABI: argument validation, then the stream-ordered launches.
+#include <cmath>
+
+#include "minf_common.cuh"
+#include "minf_kernels.h"
+
+using namespace minf;
+
+namespace {
+
+inline cudaStream_t cs(minf_stream_t s) { return reinterpret_cast<cudaStream_t>(s); }
+
+bool ok_f(const void *p) { return p != nullptr && aligned16(p); }
+
+// Head geometry shared by every attention entry point.
+int check_heads(int nh, int nk, int hd, int hd_kv) {
+    if (nh <= 0 || nk <= 0 || hd <= 0 || hd_kv <= 0) return MINF_ERR_ARG;
+    if (hd < hd_kv || nh % nk != 0) return MINF_ERR_GEOMETRY;  // hd < hd_kv is refused
+    if ((hd & 1) || (hd_kv & 1)) return MINF_ERR_ARG;
+    if (hd > 2 * kMaxHalf || hd_kv > 2 * kMaxHalf) return MINF_ERR_UNSUPPORTED;
+    return MINF_OK;
+}
+
+int check_attn(int nh, int nk, int hd, int hd_kv) {
+    int st = check_heads(nh, nk, hd, hd_kv);
+    if (st != MINF_OK) return st;
+    return decode_supported(nh, nk, hd, hd_kv) ? MINF_OK : MINF_ERR_UNSUPPORTED;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *minf_status_string(int status) {
+    switch (status) {
+        case MINF_OK: return "ok";
+        case MINF_ERR_ARG: return "invalid argument";
+        case MINF_ERR_GEOMETRY: return "invalid head geometry (hd < hd_kv or n_head % n_kv_head != 0)";
+        case MINF_ERR_UNSUPPORTED: return "shape not implemented by the kernels";
+        case MINF_ERR_WORKSPACE: return "workspace missing or too small";
+        case MINF_ERR_CUDA: return "CUDA launch failed";
+        default: return "unknown status";
+    }
+}
+
+int minf_version(void) { return 100; }
+
+int minf_rope_freqs(float *freqs, int hd, float theta, float freq_scale) {
+    if (!freqs || hd <= 0 || (hd & 1) || hd > 2 * kMaxHalf) return MINF_ERR_ARG;
+    RopeTable t;
+    rope_table(&t, hd, theta, freq_scale);
+    for (int i = 0; i < hd / 2; ++i) freqs[i] = t.f[i];
+    return MINF_OK;
+}
+
+int minf_rms_norm(float *y, const float *x, const float *w, int rows, int n, float eps,
+                  minf_stream_t stream) {
+    if (!y || !x || rows < 0 || n <= 0) return MINF_ERR_ARG;
+    return launch_rms_norm(y, x, w, rows, n, eps, cs(stream));
+}
+
+int minf_rope(float *x, const int32_t *pos, int nt, int n_head, int hd, float theta,
+              float freq_scale, int style, int32_t *err, minf_stream_t stream) {
+    if (!x || !pos || !err || nt < 0 || n_head <= 0 || hd <= 0 || (hd & 1) || hd > 2 * kMaxHalf)
+        return MINF_ERR_ARG;
+    if (style != 0 && style != 1) return MINF_ERR_ARG;
+    return launch_rope(x, pos, nt, n_head, hd, theta, freq_scale, style, err, cs(stream));
+}
+
+int minf_kv_append(float *k_reg, float *v_reg, int cap, int row_width, const float *k_rows,
+                   const float *v_rows, const int32_t *pos, int nt, int32_t *err,
+                   minf_stream_t stream) {
+    if (!ok_f(k_reg) || !ok_f(v_reg) || !ok_f(k_rows) || !ok_f(v_rows) || !pos || !err)
+        return MINF_ERR_ARG;
+    if (cap <= 0 || nt < 0 || row_width <= 0 || row_width % 4) return MINF_ERR_ARG;
+    return launch_kv_append(k_reg, v_reg, cap, row_width, k_rows, v_rows, pos, nt, err,
+                            cs(stream));
+}
+
+static int rope_kv(float *q, float *k, const float *v, const int32_t *pos, int nt, int nh, int nk,
+                   int hd, int hd_kv, float theta, float freq_scale, int style, float *k_reg,
+                   float *v_reg, const int64_t *row_off, const int32_t *caps, int cap,
+                   int32_t *err, cudaStream_t s) {
+    RopeKvArgs a;
+    a.q = q;
+    a.k = k;
+    a.v = v;
+    a.pos = pos;
+    a.k_reg = k_reg;
+    a.v_reg = v_reg;
+    a.row_off = row_off;
+    a.caps = caps;
+    a.cap = cap;
+    a.nt = nt;
+    a.nh = nh;
+    a.nk = nk;
+    a.hd = hd;
+    a.hd_kv = hd_kv;
+    a.style = style;
+    a.err = err;
+    return launch_rope_kv_append(a, theta, freq_scale, s);
+}
+
+int minf_rope_kv_append(float *q, float *k, const float *v, const int32_t *pos, int nt,
+                        int n_head, int n_kv_head, int hd, int hd_kv, float theta,
+                        float freq_scale, int style, float *k_reg, float *v_reg, int cap,
+                        int32_t *err, minf_stream_t stream) {
+    int st = check_heads(n_head, n_kv_head, hd, hd_kv);
+    if (st != MINF_OK) return st;
+    if (!ok_f(q) || !ok_f(k) || !ok_f(v) || !ok_f(k_reg) || !ok_f(v_reg) || !pos || !err)
+        return MINF_ERR_ARG;
+    if (nt < 0 || cap <= 0 || (style != 0 && style != 1) || (n_kv_head * hd_kv) % 4)
+        return MINF_ERR_ARG;
+    return rope_kv(q, k, v, pos, nt, n_head, n_kv_head, hd, hd_kv, theta, freq_scale, style,
+                   k_reg, v_reg, nullptr, nullptr, cap, err, cs(stream));
+}
+
+size_t minf_attn_decode_workspace_bytes(int n_seq, int n_head, int n_kv_head, int hd_kv,
+                                        int max_cap) {
+    return decode_workspace_bytes(n_seq, n_head, n_kv_head, hd_kv, max_cap);
+}
+
+size_t minf_attn_prefill_workspace_bytes(int nt, int n_head, int n_kv_head, int hd_kv, int cap) {
+    return decode_workspace_bytes(nt, n_head, n_kv_head, hd_kv, cap);
+}
+
+static int decode(float *out, const float *q, const float *k_reg, const float *v_reg,
+                  const int64_t *row_off, const int32_t *caps, int cap, const int32_t *pos,
+                  int n_seq, int nh, int nk, int hd, int hd_kv, float scale, void *ws,
+                  size_t ws_bytes, int32_t *err, cudaStream_t s) {
+    DecodeArgs d;
+    d.out = out;
+    d.q = q;
+    d.k_reg = k_reg;
+    d.v_reg = v_reg;
+    d.row_off = row_off;
+    d.caps = caps;
+    d.cap = cap;
+    d.pos = pos;
+    d.n_seq = n_seq;
+    d.nh = nh;
+    d.nk = nk;
+    d.hd = hd;
+    d.hd_kv = hd_kv;
+    d.scale = scale;
+    d.err = err;
+    d.ws = ws;
+    d.ws_bytes = ws_bytes;
+    return launch_decode(d, s);
+}
+
+int minf_gqa_attn_decode(float *out, const float *q, const float *k_reg, const float *v_reg,
+                         const int64_t *seq_row_off, const int32_t *seq_cap, int max_cap,
+                         const int32_t *pos, int n_seq, int n_head, int n_kv_head, int hd,
+                         int hd_kv, float scale, void *ws, size_t ws_bytes, int32_t *err,
+                         minf_stream_t stream) {
+    int st = check_attn(n_head, n_kv_head, hd, hd_kv);
+    if (st != MINF_OK) return st;
+    if (!ok_f(out) || !ok_f(q) || !ok_f(k_reg) || !ok_f(v_reg) || !pos || !err) return MINF_ERR_ARG;
+    if (n_seq < 0 || max_cap <= 0) return MINF_ERR_ARG;
+    return decode(out, q, k_reg, v_reg, seq_row_off, seq_cap, max_cap, pos, n_seq, n_head,
+                  n_kv_head, hd, hd_kv, scale, ws, ws_bytes, err, cs(stream));
+}
+
+int minf_gqa_attn_prefill(float *out, const float *q, const float *k_reg, const float *v_reg,
+                          int cap, const int32_t *pos, int nt, int n_head, int n_kv_head, int hd,
+                          int hd_kv, float scale, void *ws, size_t ws_bytes, int32_t *err,
+                          minf_stream_t stream) {
+    int st = check_attn(n_head, n_kv_head, hd, hd_kv);
+    if (st != MINF_OK) return st;
+    if (!ok_f(out) || !ok_f(q) || !ok_f(k_reg) || !ok_f(v_reg) || !pos || !err) return MINF_ERR_ARG;
+    if (nt < 0 || cap <= 0) return MINF_ERR_ARG;
+    // every token is a query over the same regions with its own window pos[t] + 1
+    return decode(out, q, k_reg, v_reg, nullptr, nullptr, cap, pos, nt, n_head, n_kv_head, hd,
+                  hd_kv, scale, ws, ws_bytes, err, cs(stream));
+}
+
+int minf_layer_attn_step(float *xn, const float *h, const float *gain, float eps, int n_embd,
+                         float *q, float *k, const float *v, const int32_t *pos, int nt,
+                         float *k_reg, float *v_reg, int cap, int n_head, int n_kv_head, int hd,
+                         int hd_kv, float theta, float freq_scale, int style, float *out,
+                         void *ws, size_t ws_bytes, int32_t *err, minf_stream_t stream) {
+    int st = check_attn(n_head, n_kv_head, hd, hd_kv);
+    if (st != MINF_OK) return st;
+    if (!xn || !h || n_embd <= 0 || nt < 0 || cap <= 0 || (style != 0 && style != 1))
+        return MINF_ERR_ARG;
+    if (!ok_f(q) || !ok_f(k) || !ok_f(v) || !ok_f(k_reg) || !ok_f(v_reg) || !ok_f(out) || !pos ||
+        !err)
+        return MINF_ERR_ARG;
+    if (nt == 0) return MINF_OK;
+    const size_t need = decode_workspace_bytes(nt, n_head, n_kv_head, hd_kv, cap);
+    if (!ws || ws_bytes < need) return MINF_ERR_WORKSPACE;
+    cudaStream_t s = cs(stream);
+    st = launch_rms_norm(xn, h, gain, nt, n_embd, eps, s);
+    if (st != MINF_OK) return st;
+    st = rope_kv(q, k, v, pos, nt, n_head, n_kv_head, hd, hd_kv, theta, freq_scale, style, k_reg,
+                 v_reg, nullptr, nullptr, cap, err, s);
+    if (st != MINF_OK) return st;
+    const float scale = 1.0f / sqrtf(static_cast<float>(hd));
+    return decode(out, q, k_reg, v_reg, nullptr, nullptr, cap, pos, nt, n_head, n_kv_head, hd,
+                  hd_kv, scale, ws, ws_bytes, err, s);
+}
+
+int minf_layer_attn_step_batched(float *xn, const float *h, const float *gain, float eps,
+                                 int n_embd, float *q, float *k, const float *v,
+                                 const int32_t *pos, int n_seq, float *k_arena, float *v_arena,
+                                 const int64_t *seq_row_off, const int32_t *seq_cap, int max_cap,
+                                 int n_head, int n_kv_head, int hd, int hd_kv, float theta,
+                                 float freq_scale, int style, float *out, void *ws,
+                                 size_t ws_bytes, int32_t *err, minf_stream_t stream) {
+    int st = check_attn(n_head, n_kv_head, hd, hd_kv);
+    if (st != MINF_OK) return st;
+    if (!xn || !h || n_embd <= 0 || n_seq < 0 || max_cap <= 0 || (style != 0 && style != 1))
+        return MINF_ERR_ARG;
+    if (!ok_f(q) || !ok_f(k) || !ok_f(v) || !ok_f(k_arena) || !ok_f(v_arena) || !ok_f(out) ||
+        !pos || !err || !seq_row_off || !seq_cap)
+        return MINF_ERR_ARG;
+    if (n_seq == 0) return MINF_OK;
+    cudaStream_t s = cs(stream);
+    st = launch_rms_norm(xn, h, gain, n_seq, n_embd, eps, s);
+    if (st != MINF_OK) return st;
+    st = rope_kv(q, k, v, pos, n_seq, n_head, n_kv_head, hd, hd_kv, theta, freq_scale, style,
+                 k_arena, v_arena, seq_row_off, seq_cap, max_cap, err, s);
+    if (st != MINF_OK) return st;
+    const float scale = 1.0f / sqrtf(static_cast<float>(hd));
+    return decode(out, q, k_arena, v_arena, seq_row_off, seq_cap, max_cap, pos, n_seq, n_head,
+                  n_kv_head, hd, hd_kv, scale, ws, ws_bytes, err, s);
+}
+
+int minf_silu_mul(float *y, const float *gate, const float *up, int64_t n, minf_stream_t stream) {
+    if (!y || !gate || !up || n < 0) return MINF_ERR_ARG;
+    return launch_silu_mul(y, gate, up, n, cs(stream));
+}
+
+}  // extern "C"

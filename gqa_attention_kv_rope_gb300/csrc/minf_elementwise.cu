@@ -1,0 +1,292 @@
+// minf_elementwise.cu -- RMSNorm, RoPE, the KV store, fused RoPE + KV store, SiLU*mul.
+//
+// These are memory-bound passes over short rows.  They use 128-bit loads where
+// the row width allows and one thread per independent element (or per rotated
+// pair), so every launch is a single coalesced sweep over its bytes.
+#include <cmath>
+
+#include "minf_common.cuh"
+#include "minf_kernels.h"
+
+namespace minf {
+
+void rope_table(RopeTable *t, int hd, float theta, float freq_scale) {
+    // "11 . Attention, vec ops, and the KV cache", §2.3/§3.2.2: the angular speed of
+    // subspace i is freq_scale / theta^(2i/hd); exact quotient in double, one rounding.
+    const int half = hd / 2;
+    for (int i = 0; i < kMaxHalf; ++i) {
+        if (i < half) {
+            double e = static_cast<double>(2 * i) / static_cast<double>(hd);
+            t->f[i] = static_cast<float>(static_cast<double>(freq_scale) /
+                                         std::pow(static_cast<double>(theta), e));
+        } else {
+            t->f[i] = 0.0f;
+        }
+    }
+}
+
+int sm_count() {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+        return 148;
+    return n;
+}
+
+// ----------------------------------------------------------------------------- RMSNorm
+// "11 . Attention, vec ops, and the KV cache", §3.2.1: y = x / sqrt(mean(x^2) + eps) * w.
+// One warp per row; the sum of squares is a per-lane fp32 sum folded by a butterfly.
+template <bool kVec>
+__global__ void __launch_bounds__(256) rms_norm_kernel(float *y, const float *x, const float *w,
+                                                       int rows, int n, float eps) {
+    const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int lane = threadIdx.x & 31;
+    if (warp >= rows) return;
+    const float *xr = x + static_cast<size_t>(warp) * n;
+    float *yr = y + static_cast<size_t>(warp) * n;
+    float ss = 0.0f;
+    if (kVec) {
+        const float4 *x4 = reinterpret_cast<const float4 *>(xr);
+        for (int i = lane; i < n / 4; i += 32) {
+            float4 v = x4[i];
+            ss = fmaf(v.x, v.x, ss);
+            ss = fmaf(v.y, v.y, ss);
+            ss = fmaf(v.z, v.z, ss);
+            ss = fmaf(v.w, v.w, ss);
+        }
+    } else {
+        for (int i = lane; i < n; i += 32) ss = fmaf(xr[i], xr[i], ss);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    const float mean = ss / static_cast<float>(n);
+    const float scale = 1.0f / sqrtf(mean + eps);
+    if (kVec) {
+        const float4 *x4 = reinterpret_cast<const float4 *>(xr);
+        const float4 *w4 = reinterpret_cast<const float4 *>(w);
+        float4 *y4 = reinterpret_cast<float4 *>(yr);
+        for (int i = lane; i < n / 4; i += 32) {
+            float4 v = x4[i];
+            float4 g = w ? w4[i] : make_float4(1.f, 1.f, 1.f, 1.f);
+            y4[i] = make_float4(v.x * scale * g.x, v.y * scale * g.y, v.z * scale * g.z,
+                                v.w * scale * g.w);
+        }
+    } else {
+        for (int i = lane; i < n; i += 32) {
+            float v = xr[i] * scale;
+            yr[i] = w ? v * w[i] : v;
+        }
+    }
+}
+
+int launch_rms_norm(float *y, const float *x, const float *w, int rows, int n, float eps,
+                    cudaStream_t s) {
+    if (rows == 0) return MINF_OK;
+    const bool vec = (n % 4 == 0) && aligned16(x) && aligned16(y) && (!w || aligned16(w));
+    const int threads = 256;
+    const int blocks = (rows + 7) / 8;
+    if (vec)
+        rms_norm_kernel<true><<<blocks, threads, 0, s>>>(y, x, w, rows, n, eps);
+    else
+        rms_norm_kernel<false><<<blocks, threads, 0, s>>>(y, x, w, rows, n, eps);
+    return cudaPeekAtLastError() == cudaSuccess ? MINF_OK : MINF_ERR_CUDA;
+}
+
+// ----------------------------------------------------------------------------- RoPE
+// "11 . Attention, vec ops, and the KV cache", §3.2.2: the pair is rotated by +th with
+// th = pos * freq_i in fp32.  Each product is rounded separately (no contraction), so
+// the only difference from an exact evaluation is sincosf's own rounding.
+__device__ __forceinline__ void rope_pair(float &x0, float &x1, float th) {
+    float sn, cs;
+    sincosf(th, &sn, &cs);
+    const float a = __fsub_rn(__fmul_rn(x0, cs), __fmul_rn(x1, sn));
+    const float b = __fadd_rn(__fmul_rn(x0, sn), __fmul_rn(x1, cs));
+    x0 = a;
+    x1 = b;
+}
+
+// Rotates pair i of head row `row` (hd floats) in place.
+__device__ __forceinline__ void rope_row_pair(float *row, int i, int hd, int style, float p,
+                                              const RopeTable &tab) {
+    const int half = hd >> 1;
+    const int i0 = style == 0 ? i : 2 * i;
+    const int i1 = style == 0 ? i + half : 2 * i + 1;
+    float x0 = row[i0], x1 = row[i1];
+    rope_pair(x0, x1, __fmul_rn(p, tab.f[i]));
+    row[i0] = x0;
+    row[i1] = x1;
+}
+
+__global__ void __launch_bounds__(256) rope_kernel(float *x, const int32_t *pos, int nt, int nh,
+                                                   int hd, int style, const RopeTable tab,
+                                                   int32_t *err) {
+    const int half = hd >> 1;
+    const long long total = static_cast<long long>(nt) * nh * half;
+    for (long long idx = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; idx < total;
+         idx += static_cast<long long>(gridDim.x) * blockDim.x) {
+        const int i = static_cast<int>(idx % half);
+        const long long th_idx = idx / half;  // t * nh + h
+        const int t = static_cast<int>(th_idx / nh);
+        const int p = __ldg(pos + t);
+        if (p < 0) {
+            if (i == 0 && th_idx % nh == 0) flag_error(err, MINF_ERRBIT_ROPE_POS);
+            continue;
+        }
+        rope_row_pair(x + th_idx * hd, i, hd, style, static_cast<float>(p), tab);
+    }
+}
+
+static int grid_for(long long work, int threads) {
+    long long b = (work + threads - 1) / threads;
+    const long long cap = static_cast<long long>(sm_count()) * 16;
+    if (b > cap) b = cap;
+    return static_cast<int>(b < 1 ? 1 : b);
+}
+
+int launch_rope(float *x, const int32_t *pos, int nt, int nh, int hd, float theta, float freq_scale,
+                int style, int32_t *err, cudaStream_t s) {
+    if (nt == 0) return MINF_OK;
+    RopeTable tab;
+    rope_table(&tab, hd, theta, freq_scale);
+    const long long work = static_cast<long long>(nt) * nh * (hd / 2);
+    rope_kernel<<<grid_for(work, 256), 256, 0, s>>>(x, pos, nt, nh, hd, style, tab, err);
+    return cudaPeekAtLastError() == cudaSuccess ? MINF_OK : MINF_ERR_CUDA;
+}
+
+// ----------------------------------------------------------------------------- KV store
+// "11 . Attention, vec ops, and the KV cache", §3.2.3: row pos[t] of each region gets the
+// token's row, a plain copy; an out-of-range position is reported and never written.
+__global__ void __launch_bounds__(256) kv_append_kernel(float *k_reg, float *v_reg, int cap, int W,
+                                                        const float *k_rows, const float *v_rows,
+                                                        const int32_t *pos, int nt, int32_t *err) {
+    const int w4 = W >> 2;
+    const long long total = static_cast<long long>(nt) * w4;
+    for (long long idx = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; idx < total;
+         idx += static_cast<long long>(gridDim.x) * blockDim.x) {
+        const int t = static_cast<int>(idx / w4);
+        const int c = static_cast<int>(idx % w4);
+        const int p = __ldg(pos + t);
+        if (p < 0 || p >= cap) {
+            if (c == 0) flag_error(err, MINF_ERRBIT_STORE_POS);
+            continue;
+        }
+        const size_t src = static_cast<size_t>(t) * w4 + c;
+        const size_t dst = static_cast<size_t>(p) * w4 + c;
+        reinterpret_cast<float4 *>(k_reg)[dst] = reinterpret_cast<const float4 *>(k_rows)[src];
+        reinterpret_cast<float4 *>(v_reg)[dst] = reinterpret_cast<const float4 *>(v_rows)[src];
+    }
+}
+
+int launch_kv_append(float *k_reg, float *v_reg, int cap, int W, const float *k_rows,
+                     const float *v_rows, const int32_t *pos, int nt, int32_t *err,
+                     cudaStream_t s) {
+    if (nt == 0) return MINF_OK;
+    const long long work = static_cast<long long>(nt) * (W / 4);
+    kv_append_kernel<<<grid_for(work, 256), 256, 0, s>>>(k_reg, v_reg, cap, W, k_rows, v_rows, pos,
+                                                          nt, err);
+    return cudaPeekAtLastError() == cudaSuccess ? MINF_OK : MINF_ERR_CUDA;
+}
+
+// ----------------------------------------------------------------------------- RoPE + store
+// One sweep per token over three kinds of work item: a q pair, a k pair (rotated, written
+// back in place and into the K region), and a float4 of v (copied into the V region).
+// Batched callers give each token its own arena offset and capacity.
+__global__ void __launch_bounds__(256) rope_kv_append_kernel(RopeKvArgs a, const RopeTable tq,
+                                                             const RopeTable tk) {
+    const int hq = a.hd >> 1, hk = a.hd_kv >> 1;
+    const int nq = a.nh * hq, nkp = a.nk * hk, W = a.nk * a.hd_kv, nv = W >> 2;
+    const int per_tok = nq + nkp + nv;
+    const long long total = static_cast<long long>(a.nt) * per_tok;
+    for (long long idx = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; idx < total;
+         idx += static_cast<long long>(gridDim.x) * blockDim.x) {
+        const int t = static_cast<int>(idx / per_tok);
+        int r = static_cast<int>(idx % per_tok);
+        const int p = __ldg(a.pos + t);
+        const int cap_t = a.caps ? __ldg(a.caps + t) : a.cap;
+        const long long base = a.row_off ? __ldg(a.row_off + t) : 0;
+        const bool store_ok = p >= 0 && p < cap_t;
+        if (r < nq) {  // q pair
+            if (p < 0) {
+                if (r == 0) flag_error(a.err, MINF_ERRBIT_ROPE_POS);
+                continue;
+            }
+            const int h = r / hq, i = r % hq;
+            rope_row_pair(a.q + (static_cast<size_t>(t) * a.nh + h) * a.hd, i, a.hd, a.style,
+                          static_cast<float>(p), tq);
+            continue;
+        }
+        r -= nq;
+        if (r < nkp) {  // k pair: rotate, write back, store
+            if (p < 0) continue;  // already flagged by the q branch
+            const int h = r / hk, i = r % hk;
+            float *row = a.k + (static_cast<size_t>(t) * a.nk + h) * a.hd_kv;
+            const int i0 = a.style == 0 ? i : 2 * i;
+            const int i1 = a.style == 0 ? i + hk : 2 * i + 1;
+            float x0 = row[i0], x1 = row[i1];
+            rope_pair(x0, x1, __fmul_rn(static_cast<float>(p), tk.f[i]));
+            row[i0] = x0;
+            row[i1] = x1;
+            if (store_ok) {
+                float *dst = a.k_reg + (static_cast<size_t>(base) + p) * W + h * a.hd_kv;
+                dst[i0] = x0;
+                dst[i1] = x1;
+            }
+            continue;
+        }
+        r -= nkp;  // float4 of v
+        if (!store_ok) {
+            if (r == 0) flag_error(a.err, MINF_ERRBIT_STORE_POS);
+            continue;
+        }
+        const float4 v = reinterpret_cast<const float4 *>(a.v)[static_cast<size_t>(t) * nv + r];
+        reinterpret_cast<float4 *>(a.v_reg)[(static_cast<size_t>(base) + p) * nv + r] = v;
+    }
+}
+
+int launch_rope_kv_append(const RopeKvArgs &a, float theta, float freq_scale, cudaStream_t s) {
+    if (a.nt == 0) return MINF_OK;
+    RopeTable tq, tk;
+    rope_table(&tq, a.hd, theta, freq_scale);
+    rope_table(&tk, a.hd_kv, theta, freq_scale);
+    const long long per_tok =
+        static_cast<long long>(a.nh) * (a.hd / 2) + a.nk * (a.hd_kv / 2) + a.nk * a.hd_kv / 4;
+    rope_kv_append_kernel<<<grid_for(per_tok * a.nt, 256), 256, 0, s>>>(a, tq, tk);
+    return cudaPeekAtLastError() == cudaSuccess ? MINF_OK : MINF_ERR_CUDA;
+}
+
+// ----------------------------------------------------------------------------- SiLU * up
+// "11 . Attention, vec ops, and the KV cache", §3.2.5: silu(x) = x / (1 + e^-x).
+__device__ __forceinline__ float silu_mul1(float g, float u) { return g / (1.0f + expf(-g)) * u; }
+
+__global__ void __launch_bounds__(256) silu_mul_vec_kernel(float4 *y, const float4 *g,
+                                                           const float4 *u, long long n4) {
+    for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < n4;
+         i += static_cast<long long>(gridDim.x) * blockDim.x) {
+        const float4 a = g[i], b = u[i];
+        y[i] = make_float4(silu_mul1(a.x, b.x), silu_mul1(a.y, b.y), silu_mul1(a.z, b.z),
+                           silu_mul1(a.w, b.w));
+    }
+}
+
+__global__ void __launch_bounds__(256) silu_mul_kernel(float *y, const float *g, const float *u,
+                                                       long long n) {
+    for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < n;
+         i += static_cast<long long>(gridDim.x) * blockDim.x)
+        y[i] = silu_mul1(g[i], u[i]);
+}
+
+int launch_silu_mul(float *y, const float *g, const float *u, long long n, cudaStream_t s) {
+    if (n == 0) return MINF_OK;
+    if (n % 4 == 0 && aligned16(y) && aligned16(g) && aligned16(u)) {
+        const long long n4 = n / 4;
+        const int blocks = grid_for(n4, 256);
+        silu_mul_vec_kernel<<<blocks, 256, 0, s>>>(reinterpret_cast<float4 *>(y),
+                                                   reinterpret_cast<const float4 *>(g),
+                                                   reinterpret_cast<const float4 *>(u), n4);
+    } else {
+        silu_mul_kernel<<<grid_for(n, 256), 256, 0, s>>>(y, g, u, n);
+    }
+    return cudaPeekAtLastError() == cudaSuccess ? MINF_OK : MINF_ERR_CUDA;
+}
+
+}  // namespace minf

@@ -1,0 +1,52 @@
+// minf_kernels.h -- internal launcher declarations (between the C ABI and the kernels).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace minf {
+
+struct RopeKvArgs {
+    float *q;               // [nt, nh, hd], rotated in place
+    float *k;               // [nt, nk, hd_kv], rotated in place
+    const float *v;         // [nt, nk*hd_kv]
+    const int32_t *pos;     // [nt]
+    float *k_reg, *v_reg;   // regions / arena [rows, nk*hd_kv]
+    const int64_t *row_off; // per token arena row offset (nullable: 0)
+    const int32_t *caps;    // per token capacity (nullable: cap)
+    int cap;
+    int nt, nh, nk, hd, hd_kv, style;
+    int32_t *err;
+};
+
+struct DecodeArgs {
+    float *out;              // [n_seq, nh*hd_kv]
+    const float *q;          // [n_seq, nh, hd]
+    const float *k_reg, *v_reg;
+    const int64_t *row_off;  // per sequence (nullable)
+    const int32_t *caps;     // per sequence (nullable)
+    int cap;                 // capacity when caps is null; also the host bound max_cap
+    const int32_t *pos;      // [n_seq]
+    int n_seq, nh, nk, hd, hd_kv;
+    float scale;
+    int32_t *err;
+    void *ws;
+    size_t ws_bytes;
+};
+
+int launch_rms_norm(float *y, const float *x, const float *w, int rows, int n, float eps,
+                    cudaStream_t s);
+int launch_rope(float *x, const int32_t *pos, int nt, int nh, int hd, float theta,
+                float freq_scale, int style, int32_t *err, cudaStream_t s);
+int launch_kv_append(float *k_reg, float *v_reg, int cap, int W, const float *k_rows,
+                     const float *v_rows, const int32_t *pos, int nt, int32_t *err,
+                     cudaStream_t s);
+int launch_rope_kv_append(const RopeKvArgs &a, float theta, float freq_scale, cudaStream_t s);
+int launch_silu_mul(float *y, const float *g, const float *u, long long n, cudaStream_t s);
+
+size_t decode_workspace_bytes(int n_seq, int nh, int nk, int hd_kv, int max_cap);
+bool decode_supported(int nh, int nk, int hd, int hd_kv);
+int launch_decode(const DecodeArgs &a, cudaStream_t s);
+
+}  // namespace minf

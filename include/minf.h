@@ -1,0 +1,218 @@
+/*
+ * minf.h -- C ABI of the GB300 attention-stage library (libminf.so).
+ *
+ * One layer's attention stage of a small decoder-only LLM: RMSNorm, rotary
+ * position embedding at positions passed in as data, an in-place append of the
+ * step's K/V rows into persistent per-layer regions addressed by position, and
+ * grouped-query attention over the causal window [0, pos].
+ *
+ * Sources (page title, section):
+ *   "11 . Attention, vec ops, and the KV cache" (minfer walkthrough)  [P1]
+ *   "IV.2: Zero-copy KV cache"                                         [P2]
+ *   "13 . The decode loop and graph reuse" (minfer walkthrough)        [P3]
+ *
+ * Conventions for every entry point:
+ *   - The caller owns all memory.  The library never allocates or frees device
+ *     memory and never synchronises; every call is enqueued on `stream`.
+ *   - All float tensors are fp32, row-major, contiguous, 16-byte aligned, in
+ *     device memory (unless stated otherwise).  int32 positions are device arrays,
+ *     so a captured CUDA graph can be replayed with only the positions changed
+ *     ([P3] §2.3: positions and n_past are data, not topology).
+ *   - Host-detectable problems return a status without launching anything.
+ *   - Problems only the device can see (a position outside a region) are never
+ *     clamped into a write: the kernel skips the write and ORs a bit into the
+ *     caller's device word `*err` ([P1] §3.2.3: an out-of-range KV position is a
+ *     hard error).  Check it after synchronising.  Kernels never trap.
+ *   - `stream` is a cudaStream_t (NULL = the legacy default stream).
+ *   - Shapes: nh = n_head, nk = n_kv_head, g = nh/nk, hd = query head dim,
+ *     hd_kv = key/value head dim, W = nk*hd_kv (the K/V row width).
+ */
+#ifndef MINF_H
+#define MINF_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+struct CUstream_st;
+typedef struct CUstream_st *minf_stream_t; /* identical to cudaStream_t */
+
+#if defined(__GNUC__)
+#define MINF_API __attribute__((visibility("default")))
+#else
+#define MINF_API
+#endif
+
+/* Status codes returned by every entry point. */
+enum {
+    MINF_OK = 0,
+    MINF_ERR_ARG = 1,         /* null/misaligned pointer, size out of range, bad style */
+    MINF_ERR_GEOMETRY = 2,    /* hd < hd_kv ([P1] §1: refused) or n_head % n_kv_head != 0 */
+    MINF_ERR_UNSUPPORTED = 3, /* valid geometry the kernels do not implement */
+    MINF_ERR_WORKSPACE = 5,   /* workspace missing or smaller than required */
+    MINF_ERR_CUDA = 6         /* a kernel launch failed */
+};
+
+/* Bits OR-ed into the device error word *err. */
+#define MINF_ERRBIT_STORE_POS 0x1  /* KV store: pos < 0 or pos >= cap; that row was not written */
+#define MINF_ERRBIT_ROPE_POS 0x2   /* RoPE: pos < 0; that token was left unrotated */
+#define MINF_ERRBIT_ATTN_POS 0x4   /* attention: pos < 0 (empty window, zero output) or
+                                      pos >= cap (window clamped to cap, as [P1] §3.2.4's
+                                      nkv = min(max pos + 1, n_ctx) does) */
+
+/* Human-readable name of a status code (static storage). */
+MINF_API const char *minf_status_string(int status);
+
+/* Library version, major*10000 + minor*100 + patch. */
+MINF_API int minf_version(void);
+
+/*
+ * RoPE angular speeds, host-side.  [P1] §2.3 and §3.2.2: freq_i =
+ * freq_scale / theta^(2i/hd) for i < hd/2.  Evaluated as the exact quotient in
+ * double and rounded once to float (so the table does not depend on a
+ * particular powf).  `freqs` is a HOST array of hd/2 floats.
+ * Errors: MINF_ERR_ARG if freqs is NULL, hd is odd, hd <= 0 or hd > 256.
+ */
+MINF_API int minf_rope_freqs(float *freqs, int hd, float theta, float freq_scale);
+
+/*
+ * RMSNorm with gains.  [P1] §3.2.1: y = x / sqrt(mean(x^2) + eps) * w, no mean
+ * subtraction.  x, y: [rows, n]; w: [n] (NULL = unit gains).  y may equal x.
+ * Errors: MINF_ERR_ARG for null x/y, rows < 0, n <= 0.  rows == 0 is a no-op.
+ */
+MINF_API int minf_rms_norm(float *y, const float *x, const float *w, int rows, int n, float eps,
+                  minf_stream_t stream);
+
+/*
+ * Rotary position embedding, in place.  [P1] §3.2.2: for token t, head h and
+ * i < hd/2, th = (float)pos[t] * freq_i; the pair (i, i+hd/2) (style 0,
+ * NonInterleaved: Qwen, NEOX) or (2i, 2i+1) (style 1, Interleaved: Llama) is
+ * rotated by +th.  x: [nt, n_head, hd]; pos: int32[nt] (device).
+ * Device errors: pos[t] < 0 -> MINF_ERRBIT_ROPE_POS, token left unchanged.
+ * Errors: MINF_ERR_ARG for null x/pos/err, nt < 0, n_head <= 0, odd hd,
+ * hd > 256, style not in {0, 1}.
+ */
+MINF_API int minf_rope(float *x, const int32_t *pos, int nt, int n_head, int hd, float theta,
+              float freq_scale, int style, int32_t *err, minf_stream_t stream);
+
+/*
+ * KV store: a pure copy, bit-exact.  [P1] §3.2.3 and [P2] (in-place append):
+ * for each token t with p = pos[t] in [0, cap): K region row p = k_rows[t],
+ * V region row p = v_rows[t].  Regions: [cap, row_width]; rows: [nt, row_width].
+ * Device errors: p < 0 or p >= cap -> MINF_ERRBIT_STORE_POS and that token's
+ * rows are not written (other tokens still are).
+ * Errors: MINF_ERR_ARG for null pointers, cap <= 0, nt < 0, row_width <= 0 or
+ * not a multiple of 4.
+ */
+MINF_API int minf_kv_append(float *k_reg, float *v_reg, int cap, int row_width, const float *k_rows,
+                   const float *v_rows, const int32_t *pos, int nt, int32_t *err,
+                   minf_stream_t stream);
+
+/*
+ * Fused RoPE on q and k plus the KV store ([P1] §3.2.2 and §3.2.3, store
+ * before attention per [P1] §3.4).  q: [nt, n_head, hd] and k: [nt, n_kv_head,
+ * hd_kv] are rotated in place; the rotated k rows and the v rows [nt, W] are
+ * then written to row pos[t] of the regions [cap, W].  The appended K row is
+ * bit-identical to minf_rope's output for the same k.
+ * Device errors: as minf_rope and minf_kv_append.
+ * Errors: MINF_ERR_ARG / MINF_ERR_GEOMETRY as above.
+ */
+MINF_API int minf_rope_kv_append(float *q, float *k, const float *v, const int32_t *pos, int nt,
+                        int n_head, int n_kv_head, int hd, int hd_kv, float theta,
+                        float freq_scale, int style, float *k_reg, float *v_reg, int cap,
+                        int32_t *err, minf_stream_t stream);
+
+/*
+ * Bytes of device workspace minf_gqa_attn_decode needs for n_seq sequences
+ * whose regions hold at most max_cap rows.  Returns 0 for invalid arguments.
+ * The workspace must be zero-filled before its first use; every call leaves
+ * it zero-filled again on return, so it can be reused (and captured in a CUDA
+ * graph) without clearing.  Two calls that run concurrently must not share it.
+ */
+MINF_API size_t minf_attn_decode_workspace_bytes(int n_seq, int n_head, int n_kv_head, int hd_kv,
+                                        int max_cap);
+
+/*
+ * Decode attention (one query token per sequence), split-KV.  [P1] §3.2.4 with
+ * [P1] §2.5 (split the KV axis across blocks, then reduce) and [P2] (the
+ * attention reads the cache through a view, never a copy):
+ *   for sequence s and query head h, hk = h / g, L = min(pos[s] + 1, cap_s),
+ *   out[s, h] = sum_{j < L} softmax_j(scale * q[s,h][0:hd_kv] . K[j, hk]) V[j, hk]
+ * where K[j] is row seq_row_off[s] + j of the arena.  Arena: k_reg/v_reg
+ * [rows, W]; q: [n_seq, n_head, hd]; out: [n_seq, n_head*hd_kv].
+ * seq_row_off: int64[n_seq] device (NULL = all 0); seq_cap: int32[n_seq]
+ * device (NULL = max_cap for all); max_cap: host upper bound of every cap_s
+ * (it sizes the split grid and the workspace; the grid never depends on pos,
+ * so the call can be graph-captured and replayed with new positions).
+ * Device errors: MINF_ERRBIT_ATTN_POS (see above).
+ * Errors: MINF_ERR_ARG, MINF_ERR_GEOMETRY, MINF_ERR_UNSUPPORTED (hd_kv not 64
+ * or 128, g > 8, hd > 256), MINF_ERR_WORKSPACE.
+ */
+MINF_API int minf_gqa_attn_decode(float *out, const float *q, const float *k_reg, const float *v_reg,
+                         const int64_t *seq_row_off, const int32_t *seq_cap, int max_cap,
+                         const int32_t *pos, int n_seq, int n_head, int n_kv_head, int hd,
+                         int hd_kv, float scale, void *ws, size_t ws_bytes, int32_t *err,
+                         minf_stream_t stream);
+
+/*
+ * Causal prefill attention over one sequence's regions.  [P1] §3.2.4: token t
+ * attends over rows [0, min(pos[t] + 1, cap)) of the K/V regions [cap, W]
+ * (store before attention: the tokens' own rows must already be appended).
+ * q: [nt, n_head, hd]; out: [nt, n_head*hd_kv].
+ * Device errors: MINF_ERRBIT_ATTN_POS.
+ * Errors: as minf_gqa_attn_decode.
+ */
+MINF_API int minf_gqa_attn_prefill(float *out, const float *q, const float *k_reg, const float *v_reg,
+                          int cap, const int32_t *pos, int nt, int n_head, int n_kv_head, int hd,
+                          int hd_kv, float scale, void *ws, size_t ws_bytes, int32_t *err,
+                          minf_stream_t stream);
+
+/* Workspace bytes minf_gqa_attn_prefill needs for nt tokens (0 if none). */
+MINF_API size_t minf_attn_prefill_workspace_bytes(int nt, int n_head, int n_kv_head, int hd_kv, int cap);
+
+/*
+ * One layer's attention stage for one sequence ([P1] §1, the decoder-layer
+ * picture, minus the weight matmuls): xn = RMSNorm(h) * gain ([nt, n_embd]);
+ * q [nt, n_head, hd] and k [nt, n_kv_head, hd_kv] rotated in place at pos;
+ * rotated k and v appended at pos into the regions [cap, W]; out [nt, n_head*hd_kv]
+ * = attention with scale 1/sqrt(hd) ([P1] §2.4).  nt == 1 runs the split-KV
+ * decode path, nt > 1 the prefill path.  ws/ws_bytes: at least
+ * max(decode bytes for 1 sequence, prefill bytes for nt tokens).
+ * Device errors: any of the bits above.
+ */
+MINF_API int minf_layer_attn_step(float *xn, const float *h, const float *gain, float eps, int n_embd,
+                         float *q, float *k, const float *v, const int32_t *pos, int nt,
+                         float *k_reg, float *v_reg, int cap, int n_head, int n_kv_head, int hd,
+                         int hd_kv, float theta, float freq_scale, int style, float *out,
+                         void *ws, size_t ws_bytes, int32_t *err, minf_stream_t stream);
+
+/*
+ * One layer's attention stage for a batch of n_seq independent sequences, one
+ * token each ([P2] batched decode; [P1] §2.2).  h: [n_seq, n_embd];
+ * q: [n_seq, n_head, hd]; k, v: [n_seq, W]; pos: int32[n_seq]; sequence s owns
+ * arena rows [seq_row_off[s], seq_row_off[s] + seq_cap[s]) and appends at
+ * row seq_row_off[s] + pos[s].  Both descriptor arrays are device memory and
+ * required.  ws: minf_attn_decode_workspace_bytes(n_seq, ..., max_cap).
+ */
+MINF_API int minf_layer_attn_step_batched(float *xn, const float *h, const float *gain, float eps,
+                                 int n_embd, float *q, float *k, const float *v,
+                                 const int32_t *pos, int n_seq, float *k_arena, float *v_arena,
+                                 const int64_t *seq_row_off, const int32_t *seq_cap, int max_cap,
+                                 int n_head, int n_kv_head, int hd, int hd_kv, float theta,
+                                 float freq_scale, int style, float *out, void *ws,
+                                 size_t ws_bytes, int32_t *err, minf_stream_t stream);
+
+/*
+ * SiLU times up ([P1] §3.2.5): y = gate / (1 + e^-gate) * up over n elements.
+ * Errors: MINF_ERR_ARG for null pointers or n < 0.
+ */
+MINF_API int minf_silu_mul(float *y, const float *gate, const float *up, int64_t n, minf_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MINF_H */
