@@ -45,6 +45,8 @@ def parse_args(argv=None):
     ap.add_argument("--no-secondary", action="store_true", help="headline workload only")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="budget of the CPU oracle sample")
+    ap.add_argument("--layers", type=int, default=28, help="layers of the headline workload (profiling cases)")
+    ap.add_argument("--nkv", type=int, default=40960, help="cached rows of the headline workload")
     return ap.parse_args(argv)
 
 
@@ -194,9 +196,13 @@ def flush_l2(buf):
 
 
 # ----------------------------------------------------------------------------- workloads
-def setup_long_context(m, torch, wl, n_cached, dev):
+def setup_long_context(m, torch, wl, n_cached, dev, n_layer=None):
+    import dataclasses
+
     g = wl.QWEN3_06B
-    cap = wl.LONG_CONTEXT_CAP
+    if n_layer is not None and n_layer != g.n_layer:
+        g = dataclasses.replace(g, n_layer=n_layer)
+    cap = max(wl.LONG_CONTEXT_CAP, n_cached + 1)
     regions = m.kv.KvRegions(g.n_layer, g.row_width, cap, device=dev)
     for layer in range(g.n_layer):
         k, v = regions.view(layer)
@@ -260,8 +266,8 @@ def kv_bytes_long_context(g, pos):
 
 def run_headline(m, torch, wl, args, world, dev):
     stream = torch.cuda.Stream()
-    n = wl.LONG_CONTEXT_SWEEP[-1]
-    S = setup_long_context(m, torch, wl, n, dev)
+    n = args.nkv
+    S = setup_long_context(m, torch, wl, n, dev, args.layers)
     g = S["g"]
     graph = capture(torch, stream, lambda: decode_step(m, S))
     bytes_step = kv_bytes_long_context(g, n)
@@ -286,19 +292,15 @@ def run_headline(m, torch, wl, args, world, dev):
     ms_step = ms_total / args.steps
     err = int(S["err"].item())
 
-    # the dominant kernel, timed alone per launch with events on its own stream
+    # the dominant kernel -- each layer step is one fused launch -- timed per launch with
+    # events on the stream it runs on
     kern_ms = []
     with torch.cuda.stream(stream):
         for it in range(max(2, args.steps // 4)):
             for layer in range(g.n_layer):
-                h, q, k, v, xn, out = views(S, layer)
-                K, V = S["regions"].view(layer)
-                m.binding.minf_rope_kv_append(q, k, v, S["pos"], g.n_head, g.n_kv_head, g.hd, g.hd_kv, g.theta,
-                                              g.freq_scale, 0, K, V, S["err"])
                 a, b = Timer(torch, stream).pair()
                 a.record(stream)
-                m.binding.minf_gqa_attn_decode(out, q, K, V, None, None, S["cap"], S["pos"], g.n_head,
-                                               g.n_kv_head, g.hd, g.hd_kv, 1.0 / (g.hd ** 0.5), S["ws"], S["err"])
+                decode_step(m, S, layers=[layer])
                 b.record(stream)
                 kern_ms.append((a, b))
     torch.cuda.synchronize()
@@ -326,7 +328,7 @@ def run_headline(m, torch, wl, args, world, dev):
     res = {"S": S, "graph": graph, "stream": stream, "ms_step": ms_step, "bytes_step": bytes_step,
            "clocks": clocks, "err": err, "kern_avg_ms": kern_avg_ms, "kern_launches": len(kern),
            "kern_bytes": 2 * (n + 1) * g.row_width * 4, "e2e_ms": e2e_ms, "h2d": h2d, "d2h": d2h,
-           "launches_per_step": 3 * g.n_layer}
+           "launches_per_step": g.n_layer}
     return res
 
 
@@ -654,11 +656,13 @@ def main(argv=None):
         "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(H["ms_step"], 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": {"workload": WORKLOAD, "n_layer": g.n_layer, "n_head": g.n_head, "n_kv_head": g.n_kv_head,
-                   "hd": g.hd, "nkv": wl.LONG_CONTEXT_SWEEP[-1], "kv_bytes_per_step": H["bytes_step"],
+        "config": {"workload": WORKLOAD if (args.layers, args.nkv) == (28, 40960) else
+                   f"long-context decode, Qwen3-0.6B shape, {g.n_layer} layers, nkv={args.nkv} (profiling case)",
+                   "n_layer": g.n_layer, "n_head": g.n_head, "n_kv_head": g.n_kv_head,
+                   "hd": g.hd, "nkv": args.nkv, "kv_bytes_per_step": H["bytes_step"],
                    "l2": "inputs larger than L2 (9.4 GB cache per replica)", "graph": "one CUDA graph per step",
                    "parallelism": f"replicas x{world}"},
-        "roofline": {"bound": "hbm", "kernel": "decode_split_kernel<128,2>", "achieved": round(achieved, 1),
+        "roofline": {"bound": "hbm", "kernel": "decode_kernel<128,2,fused> (one launch per layer step)", "achieved": round(achieved, 1),
                      "peak": peak, "peak_kind": peak_kind, "unit": "GB/s", "frac": round(achieved / peak, 4),
                      "traffic": traffic_rec["traffic_bytes_per_launch"] if traffic_rec else None,
                      "algorithmic_bytes_per_launch": H["kern_bytes"], "avg_launch_us": round(H["kern_avg_ms"] * 1e3, 2),

@@ -124,10 +124,10 @@ size_t minf_attn_prefill_workspace_bytes(int nt, int n_head, int n_kv_head, int 
     return decode_workspace_bytes(nt, n_head, n_kv_head, hd_kv, cap);
 }
 
-static int decode(float *out, const float *q, const float *k_reg, const float *v_reg,
-                  const int64_t *row_off, const int32_t *caps, int cap, const int32_t *pos,
-                  int n_seq, int nh, int nk, int hd, int hd_kv, float scale, void *ws,
-                  size_t ws_bytes, int32_t *err, cudaStream_t s) {
+static DecodeArgs decode_args(float *out, const float *q, const float *k_reg,
+                              const float *v_reg, const int64_t *row_off, const int32_t *caps,
+                              int cap, const int32_t *pos, int n_seq, int nh, int nk, int hd,
+                              int hd_kv, float scale, void *ws, size_t ws_bytes, int32_t *err) {
     DecodeArgs d;
     d.out = out;
     d.q = q;
@@ -146,7 +146,16 @@ static int decode(float *out, const float *q, const float *k_reg, const float *v
     d.err = err;
     d.ws = ws;
     d.ws_bytes = ws_bytes;
-    return launch_decode(d, s);
+    return d;
+}
+
+static int decode(float *out, const float *q, const float *k_reg, const float *v_reg,
+                  const int64_t *row_off, const int32_t *caps, int cap, const int32_t *pos,
+                  int n_seq, int nh, int nk, int hd, int hd_kv, float scale, void *ws,
+                  size_t ws_bytes, int32_t *err, cudaStream_t s) {
+    return launch_decode(decode_args(out, q, k_reg, v_reg, row_off, caps, cap, pos, n_seq, nh, nk,
+                                     hd, hd_kv, scale, ws, ws_bytes, err),
+                         s);
 }
 
 int minf_gqa_attn_decode(float *out, const float *q, const float *k_reg, const float *v_reg,
@@ -191,12 +200,20 @@ int minf_layer_attn_step(float *xn, const float *h, const float *gain, float eps
     const size_t need = decode_workspace_bytes(nt, n_head, n_kv_head, hd_kv, cap);
     if (!ws || ws_bytes < need) return MINF_ERR_WORKSPACE;
     cudaStream_t s = cs(stream);
+    const float scale = 1.0f / sqrtf(static_cast<float>(hd));
+    if (nt == 1 && fused_step_supported(n_head, n_kv_head, hd, hd_kv, n_embd) && aligned16(h) &&
+        aligned16(xn) && (!gain || aligned16(gain))) {
+        // one launch: RMSNorm, RoPE on q and k, the K/V append and split-KV attention
+        DecodeArgs d = decode_args(out, q, k_reg, v_reg, nullptr, nullptr, cap, pos, 1, n_head,
+                                   n_kv_head, hd, hd_kv, scale, ws, ws_bytes, err);
+        DecodeStepExtra x = {k, v, xn, h, gain, eps, theta, freq_scale, n_embd, style, true};
+        return launch_decode_step(d, x, s);
+    }
     st = launch_rms_norm(xn, h, gain, nt, n_embd, eps, s);
     if (st != MINF_OK) return st;
     st = rope_kv(q, k, v, pos, nt, n_head, n_kv_head, hd, hd_kv, theta, freq_scale, style, k_reg,
                  v_reg, nullptr, nullptr, cap, err, s);
     if (st != MINF_OK) return st;
-    const float scale = 1.0f / sqrtf(static_cast<float>(hd));
     return decode(out, q, k_reg, v_reg, nullptr, nullptr, cap, pos, nt, n_head, n_kv_head, hd,
                   hd_kv, scale, ws, ws_bytes, err, s);
 }
@@ -217,12 +234,19 @@ int minf_layer_attn_step_batched(float *xn, const float *h, const float *gain, f
         return MINF_ERR_ARG;
     if (n_seq == 0) return MINF_OK;
     cudaStream_t s = cs(stream);
+    const float scale = 1.0f / sqrtf(static_cast<float>(hd));
+    if (fused_step_supported(n_head, n_kv_head, hd, hd_kv, n_embd) && aligned16(h) &&
+        aligned16(xn) && (!gain || aligned16(gain))) {
+        DecodeArgs d = decode_args(out, q, k_arena, v_arena, seq_row_off, seq_cap, max_cap, pos,
+                                   n_seq, n_head, n_kv_head, hd, hd_kv, scale, ws, ws_bytes, err);
+        DecodeStepExtra x = {k, v, xn, h, gain, eps, theta, freq_scale, n_embd, style, false};
+        return launch_decode_step(d, x, s);
+    }
     st = launch_rms_norm(xn, h, gain, n_seq, n_embd, eps, s);
     if (st != MINF_OK) return st;
     st = rope_kv(q, k, v, pos, n_seq, n_head, n_kv_head, hd, hd_kv, theta, freq_scale, style,
                  k_arena, v_arena, seq_row_off, seq_cap, max_cap, err, s);
     if (st != MINF_OK) return st;
-    const float scale = 1.0f / sqrtf(static_cast<float>(hd));
     return decode(out, q, k_arena, v_arena, seq_row_off, seq_cap, max_cap, pos, n_seq, n_head,
                   n_kv_head, hd, hd_kv, scale, ws, ws_bytes, err, s);
 }

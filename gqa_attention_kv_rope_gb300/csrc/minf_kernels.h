@@ -45,8 +45,21 @@ int launch_kv_append(float *k_reg, float *v_reg, int cap, int W, const float *k_
 int launch_rope_kv_append(const RopeKvArgs &a, float theta, float freq_scale, cudaStream_t s);
 int launch_silu_mul(float *y, const float *g, const float *u, long long n, cudaStream_t s);
 
+// The rest of a decode layer step, fused into the attention launch (one token per sequence).
+struct DecodeStepExtra {
+    float *k;             // [n_seq, nk, hd_kv] rotated in place
+    const float *v;       // [n_seq, W]
+    float *xn;            // [n_seq, n_embd] RMSNorm output
+    const float *h, *gain;
+    float eps, theta, freq_scale;
+    int n_embd, style;
+    bool pdl;             // launch with programmatic stream serialization
+};
+
 size_t decode_workspace_bytes(int n_seq, int nh, int nk, int hd_kv, int max_cap);
 bool decode_supported(int nh, int nk, int hd, int hd_kv);
+bool fused_step_supported(int nh, int nk, int hd, int hd_kv, int n_embd);
 int launch_decode(const DecodeArgs &a, cudaStream_t s);
+int launch_decode_step(const DecodeArgs &a, const DecodeStepExtra &x, cudaStream_t s);
 
 }  // namespace minf

@@ -404,3 +404,159 @@ def test_host_errors_raise(m):
         m.minf_gqa_attn_decode(out, q, K, K, None, None, 8, dev(np.array([0], np.int32)), 4, 1, 64, 128,
                                0.1, ws, err_word())
     assert e.value.status == m.MINF_ERR_GEOMETRY
+
+
+# --------------------------------------------------------------------------- fused decode step
+def _step_inputs(g, nt, seed):
+    return {"h": rnd((nt, g.n_embd), seed), "gain": torch.rand(g.n_embd, generator=torch.Generator().manual_seed(seed + 1)) + 0.5,
+            "q": rnd((nt, g.q_width), seed + 2), "k": rnd((nt, g.row_width), seed + 3),
+            "v": rnd((nt, g.row_width), seed + 4)}
+
+
+def test_fused_step_multilayer_graph_with_shared_workspace(m, orc):
+    """Four layers captured in one graph (each layer one launch, programmatically dependent
+    on the previous one, all sharing one workspace), replayed at two positions."""
+    from gqa_attention_kv_rope_gb300 import workloads as wl
+
+    g = wl.QWEN3_06B
+    n_layer, cap = 4, 300
+    regions = m.kv.KvRegions(n_layer, g.row_width, cap)
+    Kh = [rnd((cap, g.row_width), 200 + i) for i in range(n_layer)]
+    Vh = [rnd((cap, g.row_width), 300 + i) for i in range(n_layer)]
+    for i in range(n_layer):
+        regions.k[i].copy_(Kh[i])
+        regions.v[i].copy_(Vh[i])
+    pos = torch.zeros(1, dtype=torch.int32, device="cuda")
+    err = err_word()
+    ws = m.kv.decode_workspace(1, g.n_head, g.n_kv_head, g.hd_kv, cap)
+    bufs = [{k: torch.empty_like(dev(v)) for k, v in _step_inputs(g, 1, 0).items()} for _ in range(n_layer)]
+    for b in bufs:
+        b["xn"] = torch.empty(1, g.n_embd, device="cuda")
+        b["out"] = torch.empty(1, g.out_width, device="cuda")
+
+    def step():
+        for i, b in enumerate(bufs):
+            K, V = regions.view(i)
+            m.minf_layer_attn_step(b["xn"], b["h"], b["gain"], g.eps, b["q"], b["k"], b["v"], pos, K, V, g.n_head,
+                                   g.n_kv_head, g.hd, g.hd_kv, g.theta, 1.0, 0, b["out"], ws, err)
+
+    stream = torch.cuda.Stream()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        step()
+    torch.cuda.synchronize()
+    Ko = [k.numpy().copy() for k in Kh]
+    Vo = [v.numpy().copy() for v in Vh]
+    for p in (257, 258):
+        inputs = [_step_inputs(g, 1, 1000 * p + i) for i in range(n_layer)]
+        for b, x in zip(bufs, inputs):
+            for key in ("h", "gain", "q", "k", "v"):
+                b[key].copy_(dev(x[key]))
+        pos.fill_(p)
+        graph.replay()
+        torch.cuda.synchronize()
+        for i, (b, x) in enumerate(zip(bufs, inputs)):
+            q, k = x["q"].numpy().copy(), x["k"].numpy().copy()
+            xn_ref, ref = orc.layer_attn_step(x["h"].numpy(), x["gain"].numpy(), q, k, x["v"].numpy(), [p], Ko[i],
+                                              Vo[i], n_head=g.n_head, n_kv_head=g.n_kv_head, hd=g.hd, hd_kv=g.hd_kv,
+                                              eps=g.eps, theta=g.theta)
+            close(b["out"].cpu(), ref, what=f"layer {i} out at pos {p}")
+            close(b["xn"].cpu(), xn_ref, what=f"layer {i} xn")
+            close(b["q"].cpu(), q, what=f"layer {i} q rotated")
+            close(b["k"].cpu(), k, what=f"layer {i} k rotated")
+            assert np.array_equal(regions.v[i].cpu().numpy(), Vo[i])
+            close(regions.k[i].cpu(), Ko[i], what=f"layer {i} K region")
+    assert err.item() == 0
+
+
+@pytest.mark.parametrize("style", [0, 1])
+def test_fused_step_matches_unfused_semantics(m, orc, style):
+    """The fused one-launch step and the oracle agree for both RoPE styles, including
+    the K row it appends, which must equal the standalone RoPE kernel's output bit for bit."""
+    from gqa_attention_kv_rope_gb300 import workloads as wl
+
+    g = wl.QWEN25_05B
+    cap, p = 200, 150
+    K = rnd((cap, g.row_width), 61)
+    V = rnd((cap, g.row_width), 62)
+    x = _step_inputs(g, 1, 63)
+    d = {k: dev(v) for k, v in x.items()}
+    Kd, Vd = dev(K), dev(V)
+    err = err_word()
+    xn = torch.empty_like(d["h"])
+    out = torch.empty(1, g.out_width, device="cuda")
+    ws = m.kv.decode_workspace(1, g.n_head, g.n_kv_head, g.hd_kv, cap)
+    k_alone = dev(x["k"])
+    m.minf_rope(k_alone, dev(np.array([p], np.int32)), g.n_kv_head, g.hd_kv, g.theta, 1.0, style, err)
+    m.minf_layer_attn_step(xn, d["h"], d["gain"], g.eps, d["q"], d["k"], d["v"], dev(np.array([p], np.int32)),
+                           Kd, Vd, g.n_head, g.n_kv_head, g.hd, g.hd_kv, g.theta, 1.0, style, out, ws, err)
+    torch.cuda.synchronize()
+    assert err.item() == 0
+    q, k = x["q"].numpy().copy(), x["k"].numpy().copy()
+    Ko, Vo = K.numpy().copy(), V.numpy().copy()
+    _, ref = orc.layer_attn_step(x["h"].numpy(), x["gain"].numpy(), q, k, x["v"].numpy(), [p], Ko, Vo,
+                                 n_head=g.n_head, n_kv_head=g.n_kv_head, hd=g.hd, hd_kv=g.hd_kv, eps=g.eps,
+                                 theta=g.theta, style=style)
+    close(out.cpu(), ref, what="out")
+    close(d["q"].cpu(), q, what="q")
+    assert torch.equal(d["k"].cpu(), k_alone.cpu())
+    assert torch.equal(Kd[p].cpu(), k_alone[0].cpu())
+    assert np.array_equal(Vd.cpu().numpy(), Vo)
+
+
+def test_fused_step_position_beyond_region(m, orc):
+    """pos >= cap: nothing is stored, both bits are set, the window is the whole region and
+    q and k are still rotated -- the same as the three-launch path."""
+    from gqa_attention_kv_rope_gb300 import workloads as wl
+
+    g = wl.QWEN3_06B
+    cap, p = 96, 96
+    K = rnd((cap + 4, g.row_width), 81)
+    V = rnd((cap + 4, g.row_width), 82)
+    x = _step_inputs(g, 1, 83)
+    d = {k: dev(v) for k, v in x.items()}
+    Kd, Vd = dev(K), dev(V)
+    err = err_word()
+    out = torch.empty(1, g.out_width, device="cuda")
+    ws = m.kv.decode_workspace(1, g.n_head, g.n_kv_head, g.hd_kv, cap)
+    m.minf_layer_attn_step(torch.empty_like(d["h"]), d["h"], d["gain"], g.eps, d["q"], d["k"], d["v"],
+                           dev(np.array([p], np.int32)), Kd[:cap], Vd[:cap], g.n_head, g.n_kv_head, g.hd, g.hd_kv,
+                           g.theta, 1.0, 0, out, ws, err)
+    torch.cuda.synchronize()
+    assert err.item() & m.ERRBIT_STORE_POS and err.item() & m.ERRBIT_ATTN_POS
+    assert torch.equal(Kd.cpu(), K) and torch.equal(Vd.cpu(), V)   # nothing written, guard rows intact
+    q_ref = orc.rope(x["q"].numpy().copy(), [p], g.n_head, g.hd, g.theta)
+    k_ref = orc.rope(x["k"].numpy().copy(), [p], g.n_kv_head, g.hd_kv, g.theta)
+    close(d["q"].cpu(), q_ref, what="q")
+    close(d["k"].cpu(), k_ref, what="k")
+    ref = orc.gqa_attn(q_ref, K[:cap].numpy(), V[:cap].numpy(), [p], g.n_head, g.n_kv_head, g.hd, g.hd_kv)
+    close(out.cpu(), ref, what="out (window clamped to the region)")
+
+
+def test_layer_step_unfused_geometry(m, orc):
+    """hd > hd_kv takes the three-launch path; same results as the oracle."""
+    nh, nk, hd, hdkv, n_embd, cap, p = 4, 2, 128, 64, 256, 50, 33
+    K = rnd((cap, nk * hdkv), 91)
+    V = rnd((cap, nk * hdkv), 92)
+    h = rnd((1, n_embd), 93)
+    gain = torch.rand(n_embd, generator=torch.Generator().manual_seed(94)) + 0.5
+    q = rnd((1, nh * hd), 95)
+    k = rnd((1, nk * hdkv), 96)
+    v = rnd((1, nk * hdkv), 97)
+    d = {n: dev(t) for n, t in dict(h=h, gain=gain, q=q, k=k, v=v).items()}
+    Kd, Vd = dev(K), dev(V)
+    err = err_word()
+    xn = torch.empty(1, n_embd, device="cuda")
+    out = torch.empty(1, nh * hdkv, device="cuda")
+    ws = m.kv.decode_workspace(1, nh, nk, hdkv, cap)
+    m.minf_layer_attn_step(xn, d["h"], d["gain"], 1e-6, d["q"], d["k"], d["v"], dev(np.array([p], np.int32)), Kd, Vd,
+                           nh, nk, hd, hdkv, 1e4, 1.0, 0, out, ws, err)
+    torch.cuda.synchronize()
+    qo, ko = q.numpy().copy(), k.numpy().copy()
+    Ko, Vo = K.numpy().copy(), V.numpy().copy()
+    xn_ref, ref = orc.layer_attn_step(h.numpy(), gain.numpy(), qo, ko, v.numpy(), [p], Ko, Vo, n_head=nh,
+                                      n_kv_head=nk, hd=hd, hd_kv=hdkv, eps=1e-6, theta=1e4)
+    assert err.item() == 0
+    close(out.cpu(), ref, what="out")
+    close(xn.cpu(), xn_ref, what="xn")
+    assert np.array_equal(Vd.cpu().numpy(), Vo)
