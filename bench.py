@@ -47,6 +47,8 @@ def parse_args(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="budget of the CPU oracle sample")
     ap.add_argument("--layers", type=int, default=28, help="layers of the headline workload (profiling cases)")
     ap.add_argument("--nkv", type=int, default=40960, help="cached rows of the headline workload")
+    ap.add_argument("--only", choices=["prefill"], default=None,
+                    help="time one secondary workload alone (a small case for profiling)")
     return ap.parse_args(argv)
 
 
@@ -629,6 +631,13 @@ def main(argv=None):
     from gqa_attention_kv_rope_gb300 import workloads as wl
 
     m.binding.lib()
+    if args.only == "prefill":
+        tok_s, layer_us = run_prefill(m, torch, wl, dev, args.steps)
+        if rank == 0:
+            print(json.dumps({"metric": "prefill tok/s", "value": tok_s, "unit": "tok/s",
+                              "layer_us": layer_us, "steps": args.steps,
+                              "config": {"workload": "causal prefill, Qwen2.5-0.5B shape, 24 layers, nt=512"}}))
+        return 0
     H = run_headline(m, torch, wl, args, world, dev)
     g = H["S"]["g"]
     value = world * H["bytes_step"] / (H["ms_step"] * 1e-3) / 1e9

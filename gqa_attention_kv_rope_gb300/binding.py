@@ -28,6 +28,7 @@ MINF_ERR_CUDA = 6
 ERRBIT_STORE_POS = 0x1
 ERRBIT_ROPE_POS = 0x2
 ERRBIT_ATTN_POS = 0x4
+ERRBIT_TIMEOUT = 0x8
 
 _P = ctypes.c_void_p
 _I = ctypes.c_int
@@ -45,11 +46,11 @@ _SIGS = {
     "minf_rope_kv_append": ([_P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _F, _I, _P, _P, _I, _P, _P], _I),
     "minf_attn_decode_workspace_bytes": ([_I, _I, _I, _I, _I], _SZ),
     "minf_attn_prefill_workspace_bytes": ([_I, _I, _I, _I, _I], _SZ),
-    "minf_gqa_attn_decode": ([_P, _P, _P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _I, _F, _P, _SZ, _P, _P], _I),
+    "minf_gqa_attn_decode": ([_P, _P, _P, _P, _P, _P, _I, _I64, _P, _I, _I, _I, _I, _I, _F, _P, _SZ, _P, _P], _I),
     "minf_gqa_attn_prefill": ([_P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _I, _F, _P, _SZ, _P, _P], _I),
     "minf_layer_attn_step": ([_P, _P, _P, _F, _I, _P, _P, _P, _P, _I, _P, _P, _I, _I, _I, _I, _I,
                               _F, _F, _I, _P, _P, _SZ, _P, _P], _I),
-    "minf_layer_attn_step_batched": ([_P, _P, _P, _F, _I, _P, _P, _P, _P, _I, _P, _P, _P, _P, _I,
+    "minf_layer_attn_step_batched": ([_P, _P, _P, _F, _I, _P, _P, _P, _P, _I, _P, _P, _P, _P, _I, _I64,
                                       _I, _I, _I, _I, _F, _F, _I, _P, _P, _SZ, _P, _P], _I),
     "minf_silu_mul": ([_P, _P, _P, _I64, _P], _I),
 }
@@ -101,6 +102,10 @@ def _dev(t, dtype=torch.float32, name="tensor"):
     if not t.is_contiguous():
         raise ValueError(f"{name} must be contiguous")
     return t.data_ptr()
+
+
+def _nbytes(t):
+    return 0 if t is None else t.numel() * t.element_size()
 
 
 def _stream(stream):
@@ -161,10 +166,11 @@ def minf_attn_prefill_workspace_bytes(nt, n_head, n_kv_head, hd_kv, cap) -> int:
 
 def minf_gqa_attn_decode(out, q, k_reg, v_reg, seq_row_off, seq_cap, max_cap, pos, n_head, n_kv_head,
                          hd, hd_kv, scale, ws, err, stream=None):
+    """k_reg/v_reg: the [rows, W] arena (or one sequence's [cap, W] regions)."""
     _check(lib().minf_gqa_attn_decode(
         _dev(out, name="out"), _dev(q, name="q"), _dev(k_reg, name="k_reg"), _dev(v_reg, name="v_reg"),
         _dev(seq_row_off, torch.int64, "seq_row_off"), _dev(seq_cap, torch.int32, "seq_cap"), max_cap,
-        _dev(pos, torch.int32, "pos"), pos.numel(), n_head, n_kv_head, hd, hd_kv, scale,
+        k_reg.shape[0], _dev(pos, torch.int32, "pos"), pos.numel(), n_head, n_kv_head, hd, hd_kv, scale,
         _dev(ws, torch.uint8, "ws"), ws.numel(), _dev(err, torch.int32, "err"), _stream(stream)),
         "minf_gqa_attn_decode")
 
@@ -175,7 +181,7 @@ def minf_gqa_attn_prefill(out, q, k_reg, v_reg, pos, n_head, n_kv_head, hd, hd_k
     _check(lib().minf_gqa_attn_prefill(
         _dev(out, name="out"), _dev(q, name="q"), _dev(k_reg, name="k_reg"), _dev(v_reg, name="v_reg"),
         cap, _dev(pos, torch.int32, "pos"), pos.numel(), n_head, n_kv_head, hd, hd_kv, scale,
-        _dev(ws, torch.uint8, "ws"), ws.numel(), _dev(err, torch.int32, "err"), _stream(stream)),
+        _dev(ws, torch.uint8, "ws"), _nbytes(ws), _dev(err, torch.int32, "err"), _stream(stream)),
         "minf_gqa_attn_prefill")
 
 
@@ -187,7 +193,7 @@ def minf_layer_attn_step(xn, h, gain, eps, q, k, v, pos, k_reg, v_reg, n_head, n
         _dev(xn, name="xn"), _dev(h, name="h"), _dev(gain, name="gain"), eps, n_embd,
         _dev(q, name="q"), _dev(k, name="k"), _dev(v, name="v"), _dev(pos, torch.int32, "pos"), nt,
         _dev(k_reg, name="k_reg"), _dev(v_reg, name="v_reg"), cap, n_head, n_kv_head, hd, hd_kv,
-        theta, freq_scale, style, _dev(out, name="out"), _dev(ws, torch.uint8, "ws"), ws.numel(),
+        theta, freq_scale, style, _dev(out, name="out"), _dev(ws, torch.uint8, "ws"), _nbytes(ws),
         _dev(err, torch.int32, "err"), _stream(stream)), "minf_layer_attn_step")
 
 
@@ -200,7 +206,7 @@ def minf_layer_attn_step_batched(xn, h, gain, eps, q, k, v, pos, k_arena, v_aren
         _dev(q, name="q"), _dev(k, name="k"), _dev(v, name="v"), _dev(pos, torch.int32, "pos"), n_seq,
         _dev(k_arena, name="k_arena"), _dev(v_arena, name="v_arena"),
         _dev(seq_row_off, torch.int64, "seq_row_off"), _dev(seq_cap, torch.int32, "seq_cap"), max_cap,
-        n_head, n_kv_head, hd, hd_kv, theta, freq_scale, style, _dev(out, name="out"),
+        k_arena.shape[0], n_head, n_kv_head, hd, hd_kv, theta, freq_scale, style, _dev(out, name="out"),
         _dev(ws, torch.uint8, "ws"), ws.numel(), _dev(err, torch.int32, "err"), _stream(stream)),
         "minf_layer_attn_step_batched")
 

@@ -121,14 +121,41 @@ size_t minf_attn_decode_workspace_bytes(int n_seq, int n_head, int n_kv_head, in
 }
 
 size_t minf_attn_prefill_workspace_bytes(int nt, int n_head, int n_kv_head, int hd_kv, int cap) {
-    return decode_workspace_bytes(nt, n_head, n_kv_head, hd_kv, cap);
+    (void)nt;
+    (void)n_head;
+    (void)n_kv_head;
+    (void)hd_kv;
+    (void)cap;
+    return 0;  // the tensor-core prefill keeps its state in shared memory and TMEM
+}
+
+static int prefill(float *out, const float *q, const float *k_reg, const float *v_reg, int cap,
+                   const int32_t *pos, int nt, int nh, int nk, int hd, int hd_kv, float scale,
+                   int32_t *err, cudaStream_t s) {
+    PrefillArgs a;
+    a.out = out;
+    a.q = q;
+    a.k_reg = k_reg;
+    a.v_reg = v_reg;
+    a.pos = pos;
+    a.err = err;
+    a.nt = nt;
+    a.nh = nh;
+    a.nk = nk;
+    a.hd = hd;
+    a.hd_kv = hd_kv;
+    a.cap = cap;
+    a.scale = scale;
+    return launch_prefill(a, s);
 }
 
 static DecodeArgs decode_args(float *out, const float *q, const float *k_reg,
                               const float *v_reg, const int64_t *row_off, const int32_t *caps,
                               int cap, const int32_t *pos, int n_seq, int nh, int nk, int hd,
-                              int hd_kv, float scale, void *ws, size_t ws_bytes, int32_t *err) {
+                              int hd_kv, float scale, void *ws, size_t ws_bytes, int32_t *err,
+                              long long arena_rows = 0) {
     DecodeArgs d;
+    d.arena_rows = arena_rows;
     d.out = out;
     d.q = q;
     d.k_reg = k_reg;
@@ -152,36 +179,37 @@ static DecodeArgs decode_args(float *out, const float *q, const float *k_reg,
 static int decode(float *out, const float *q, const float *k_reg, const float *v_reg,
                   const int64_t *row_off, const int32_t *caps, int cap, const int32_t *pos,
                   int n_seq, int nh, int nk, int hd, int hd_kv, float scale, void *ws,
-                  size_t ws_bytes, int32_t *err, cudaStream_t s) {
+                  size_t ws_bytes, int32_t *err, cudaStream_t s, long long arena_rows = 0) {
     return launch_decode(decode_args(out, q, k_reg, v_reg, row_off, caps, cap, pos, n_seq, nh, nk,
-                                     hd, hd_kv, scale, ws, ws_bytes, err),
+                                     hd, hd_kv, scale, ws, ws_bytes, err, arena_rows),
                          s);
 }
 
 int minf_gqa_attn_decode(float *out, const float *q, const float *k_reg, const float *v_reg,
                          const int64_t *seq_row_off, const int32_t *seq_cap, int max_cap,
-                         const int32_t *pos, int n_seq, int n_head, int n_kv_head, int hd,
-                         int hd_kv, float scale, void *ws, size_t ws_bytes, int32_t *err,
-                         minf_stream_t stream) {
+                         int64_t arena_rows, const int32_t *pos, int n_seq, int n_head,
+                         int n_kv_head, int hd, int hd_kv, float scale, void *ws,
+                         size_t ws_bytes, int32_t *err, minf_stream_t stream) {
     int st = check_attn(n_head, n_kv_head, hd, hd_kv);
     if (st != MINF_OK) return st;
     if (!ok_f(out) || !ok_f(q) || !ok_f(k_reg) || !ok_f(v_reg) || !pos || !err) return MINF_ERR_ARG;
-    if (n_seq < 0 || max_cap <= 0) return MINF_ERR_ARG;
+    if (n_seq < 0 || max_cap <= 0 || (seq_row_off && arena_rows <= 0)) return MINF_ERR_ARG;
     return decode(out, q, k_reg, v_reg, seq_row_off, seq_cap, max_cap, pos, n_seq, n_head,
-                  n_kv_head, hd, hd_kv, scale, ws, ws_bytes, err, cs(stream));
+                  n_kv_head, hd, hd_kv, scale, ws, ws_bytes, err, cs(stream), arena_rows);
 }
 
 int minf_gqa_attn_prefill(float *out, const float *q, const float *k_reg, const float *v_reg,
                           int cap, const int32_t *pos, int nt, int n_head, int n_kv_head, int hd,
                           int hd_kv, float scale, void *ws, size_t ws_bytes, int32_t *err,
                           minf_stream_t stream) {
+    (void)ws;
+    (void)ws_bytes;
     int st = check_attn(n_head, n_kv_head, hd, hd_kv);
     if (st != MINF_OK) return st;
     if (!ok_f(out) || !ok_f(q) || !ok_f(k_reg) || !ok_f(v_reg) || !pos || !err) return MINF_ERR_ARG;
     if (nt < 0 || cap <= 0) return MINF_ERR_ARG;
-    // every token is a query over the same regions with its own window pos[t] + 1
-    return decode(out, q, k_reg, v_reg, nullptr, nullptr, cap, pos, nt, n_head, n_kv_head, hd,
-                  hd_kv, scale, ws, ws_bytes, err, cs(stream));
+    return prefill(out, q, k_reg, v_reg, cap, pos, nt, n_head, n_kv_head, hd, hd_kv, scale, err,
+                   cs(stream));
 }
 
 int minf_layer_attn_step(float *xn, const float *h, const float *gain, float eps, int n_embd,
@@ -197,8 +225,10 @@ int minf_layer_attn_step(float *xn, const float *h, const float *gain, float eps
         !err)
         return MINF_ERR_ARG;
     if (nt == 0) return MINF_OK;
-    const size_t need = decode_workspace_bytes(nt, n_head, n_kv_head, hd_kv, cap);
-    if (!ws || ws_bytes < need) return MINF_ERR_WORKSPACE;
+    if (nt == 1) {
+        const size_t need = decode_workspace_bytes(1, n_head, n_kv_head, hd_kv, cap);
+        if (!ws || ws_bytes < need) return MINF_ERR_WORKSPACE;
+    }
     cudaStream_t s = cs(stream);
     const float scale = 1.0f / sqrtf(static_cast<float>(hd));
     if (nt == 1 && fused_step_supported(n_head, n_kv_head, hd, hd_kv, n_embd) && aligned16(h) &&
@@ -214,14 +244,17 @@ int minf_layer_attn_step(float *xn, const float *h, const float *gain, float eps
     st = rope_kv(q, k, v, pos, nt, n_head, n_kv_head, hd, hd_kv, theta, freq_scale, style, k_reg,
                  v_reg, nullptr, nullptr, cap, err, s);
     if (st != MINF_OK) return st;
-    return decode(out, q, k_reg, v_reg, nullptr, nullptr, cap, pos, nt, n_head, n_kv_head, hd,
-                  hd_kv, scale, ws, ws_bytes, err, s);
+    if (nt == 1)
+        return decode(out, q, k_reg, v_reg, nullptr, nullptr, cap, pos, 1, n_head, n_kv_head, hd,
+                      hd_kv, scale, ws, ws_bytes, err, s);
+    return prefill(out, q, k_reg, v_reg, cap, pos, nt, n_head, n_kv_head, hd, hd_kv, scale, err, s);
 }
 
 int minf_layer_attn_step_batched(float *xn, const float *h, const float *gain, float eps,
                                  int n_embd, float *q, float *k, const float *v,
                                  const int32_t *pos, int n_seq, float *k_arena, float *v_arena,
                                  const int64_t *seq_row_off, const int32_t *seq_cap, int max_cap,
+                                 int64_t arena_rows,
                                  int n_head, int n_kv_head, int hd, int hd_kv, float theta,
                                  float freq_scale, int style, float *out, void *ws,
                                  size_t ws_bytes, int32_t *err, minf_stream_t stream) {
@@ -230,7 +263,7 @@ int minf_layer_attn_step_batched(float *xn, const float *h, const float *gain, f
     if (!xn || !h || n_embd <= 0 || n_seq < 0 || max_cap <= 0 || (style != 0 && style != 1))
         return MINF_ERR_ARG;
     if (!ok_f(q) || !ok_f(k) || !ok_f(v) || !ok_f(k_arena) || !ok_f(v_arena) || !ok_f(out) ||
-        !pos || !err || !seq_row_off || !seq_cap)
+        !pos || !err || !seq_row_off || !seq_cap || arena_rows <= 0)
         return MINF_ERR_ARG;
     if (n_seq == 0) return MINF_OK;
     cudaStream_t s = cs(stream);
@@ -238,7 +271,8 @@ int minf_layer_attn_step_batched(float *xn, const float *h, const float *gain, f
     if (fused_step_supported(n_head, n_kv_head, hd, hd_kv, n_embd) && aligned16(h) &&
         aligned16(xn) && (!gain || aligned16(gain))) {
         DecodeArgs d = decode_args(out, q, k_arena, v_arena, seq_row_off, seq_cap, max_cap, pos,
-                                   n_seq, n_head, n_kv_head, hd, hd_kv, scale, ws, ws_bytes, err);
+                                   n_seq, n_head, n_kv_head, hd, hd_kv, scale, ws, ws_bytes, err,
+                                   arena_rows);
         DecodeStepExtra x = {k, v, xn, h, gain, eps, theta, freq_scale, n_embd, style, false};
         return launch_decode_step(d, x, s);
     }
@@ -248,7 +282,7 @@ int minf_layer_attn_step_batched(float *xn, const float *h, const float *gain, f
                  k_arena, v_arena, seq_row_off, seq_cap, max_cap, err, s);
     if (st != MINF_OK) return st;
     return decode(out, q, k_arena, v_arena, seq_row_off, seq_cap, max_cap, pos, n_seq, n_head,
-                  n_kv_head, hd, hd_kv, scale, ws, ws_bytes, err, s);
+                  n_kv_head, hd, hd_kv, scale, ws, ws_bytes, err, s, arena_rows);
 }
 
 int minf_silu_mul(float *y, const float *gate, const float *up, int64_t n, minf_stream_t stream) {

@@ -27,6 +27,7 @@ struct DecodeArgs {
     const int64_t *row_off;  // per sequence (nullable)
     const int32_t *caps;     // per sequence (nullable)
     int cap;                 // capacity when caps is null; also the host bound max_cap
+    long long arena_rows;    // rows of the K/V arena when row_off is given
     const int32_t *pos;      // [n_seq]
     int n_seq, nh, nk, hd, hd_kv;
     float scale;
@@ -55,6 +56,18 @@ struct DecodeStepExtra {
     int n_embd, style;
     bool pdl;             // launch with programmatic stream serialization
 };
+
+struct PrefillArgs {
+    float *out;               // [nt, nh*hd_kv]
+    const float *q;           // [nt, nh, hd] (rotated)
+    const float *k_reg, *v_reg;  // regions [cap, nk*hd_kv]
+    const int32_t *pos;       // [nt]
+    int32_t *err;
+    int nt, nh, nk, hd, hd_kv, cap;
+    float scale;
+};
+
+int launch_prefill(const PrefillArgs &a, cudaStream_t s);
 
 size_t decode_workspace_bytes(int n_seq, int nh, int nk, int hd_kv, int max_cap);
 bool decode_supported(int nh, int nk, int hd, int hd_kv);

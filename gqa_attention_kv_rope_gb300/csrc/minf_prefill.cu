@@ -1,0 +1,414 @@
+// minf_prefill.cu -- causal prefill attention on the 5th-generation tensor cores.
+//
+// "11 . Attention, vec ops, and the KV cache", §3.2.4 defines the result: token t attends
+// over rows [0, min(pos[t] + 1, cap)) of its kv head's K/V regions (causal by length, no
+// mask matrix), with softmax(scale * q . k) weights on V.  §2.5 names the GPU shape: tile
+// the (query, key) matrix and apply the softmax online, block by block.
+//
+// Tiling.  A CTA owns one query head and 128 consecutive query tokens (the M = 128 rows of
+// the tensor-core tiles) and walks the keys of that head's kv head in tiles of 32, up to the
+// largest window among its tokens.  Per key tile:
+//   S  = Q K^T        tcgen05.mma kind::tf32, M=128 N=32 K=hd_kv, fp32 accumulator in TMEM
+//   softmax            CUDA cores: one thread per query row reads its S row from TMEM,
+//                      masks keys beyond its window, updates its running max and sum, and
+//                      writes P = 2^(s*scale*log2e - m) into shared memory
+//   O_t = P V          tcgen05.mma kind::tf32, M=128 N=hd_kv K=32, into a second TMEM range
+//   O  = O*corr + O_t  in registers
+// Precision: every operand is split into two TF32 halves, x = hi + lo (hi = x rounded to
+// TF32, lo = the remainder rounded to TF32), and each product is the sum of three MMAs
+// hi*hi + hi*lo + lo*hi (the split-precision "3xTF32" scheme), which brings the tensor-core
+// result to fp32 accuracy.  Q and K tiles arrive by TMA (cp.async.bulk.tensor, 128-byte
+// swizzle) and are split in place by the softmax threads; V is transposed and split into the
+// K-major layout the MMA takes.  These are generic-proxy writes, fenced to the async proxy
+// before the MMA that reads them is released.  Warp 4 is the producer: one elected thread
+// issues the TMA copies, the MMAs and the commits.
+//
+// Every mbarrier wait is bounded by a 200 ms global-timer budget; a wait that expires sets
+// MINF_ERRBIT_TIMEOUT, makes every role leave its loop, and the CTA still frees its TMEM.
+#include <cuda.h>
+
+#include <cmath>
+
+#include "minf_common.cuh"
+#include "minf_kernels.h"
+#include "minf_sm103.cuh"
+
+namespace minf {
+
+namespace {
+
+constexpr int BM = 128;              // query rows per CTA
+constexpr int BN = 32;               // keys per tile
+constexpr int kSoftThreads = 128;    // warps 0-3: TMEM lanes 0..127, one query row each
+constexpr int kProducerWarp = 4;
+constexpr int kThreadsP = kSoftThreads + 32;
+constexpr uint32_t kTmemCols = 256;  // S at column 0 (BN wide), O at column 128
+constexpr uint32_t kOCol = 128;
+
+// Operands are held as hi + lo TF32 pairs (x = hi + lo to about 2^-22 relative): each
+// product is formed from three tensor-core MMAs, hi*hi + hi*lo + lo*hi, so the TF32 inputs
+// of the tensor core cost no accuracy beyond fp32 accumulation.
+template <int HDKV>
+struct Smem {
+    float qh[HDKV / 32][BM * 32], ql[HDKV / 32][BM * 32];    // Q: 32-column SW128 slabs
+    float kh[HDKV / 32][BN * 32], kl[HDKV / 32][BN * 32];    // K tile (TMA lands in kh)
+    float ph[BN / 32][BM * 32], pl[BN / 32][BM * 32];        // P: keys along K
+    float vh[BN / 32][HDKV * 32], vl[BN / 32][HDKV * 32];    // V^T: keys along K
+    unsigned long long bar_q, bar_k, bar_kv, bar_s, bar_p, bar_o;
+    uint32_t tmem_base;
+    int abort_flag;
+    int lmax;
+};
+
+// Shared-memory matrix descriptor: K-major operand in the 128-byte swizzle layout
+// (8-row x 128-byte atoms, atoms 1024 bytes apart along M/N).
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);  // start address
+    d |= static_cast<uint64_t>(1) << 16;                   // leading byte offset (unused here)
+    d |= static_cast<uint64_t>(1024 >> 4) << 32;           // stride byte offset: next 8 rows
+    d |= static_cast<uint64_t>(1) << 46;                   // descriptor version
+    d |= static_cast<uint64_t>(2) << 61;                   // 128-byte swizzle
+    return d;
+}
+
+// Instruction descriptor: kind::tf32, fp32 accumulate, A and B tf32, both K-major.
+__host__ __device__ constexpr uint32_t tf32_idesc(int M, int N) {
+    return (1u << 4) | (2u << 7) | (2u << 10) | (static_cast<uint32_t>(N >> 3) << 17) |
+           (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+__device__ __forceinline__ void mma_tf32(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
+                                         uint32_t accumulate) {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+        " tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n}" ::"r"(d_tmem),
+        "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+__device__ __forceinline__ void mma_commit(unsigned long long *bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(su32(bar))
+                 : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&r)[32]) {
+    uint32_t u[32];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(u[0]), "=r"(u[1]), "=r"(u[2]), "=r"(u[3]), "=r"(u[4]), "=r"(u[5]), "=r"(u[6]),
+          "=r"(u[7]), "=r"(u[8]), "=r"(u[9]), "=r"(u[10]), "=r"(u[11]), "=r"(u[12]), "=r"(u[13]),
+          "=r"(u[14]), "=r"(u[15]), "=r"(u[16]), "=r"(u[17]), "=r"(u[18]), "=r"(u[19]), "=r"(u[20]),
+          "=r"(u[21]), "=r"(u[22]), "=r"(u[23]), "=r"(u[24]), "=r"(u[25]), "=r"(u[26]), "=r"(u[27]),
+          "=r"(u[28]), "=r"(u[29]), "=r"(u[30]), "=r"(u[31])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 32; ++i) r[i] = __uint_as_float(u[i]);
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// Byte offset of element (row, col) of a K-major SW128 slab (col < 32 fp32).
+__device__ __forceinline__ uint32_t sw128_off(int row, int col) {
+    return static_cast<uint32_t>(row) * 128u +
+           ((static_cast<uint32_t>(col >> 2) ^ static_cast<uint32_t>(row & 7)) << 4) +
+           static_cast<uint32_t>(col & 3) * 4u;
+}
+
+struct PParams {
+    float *out;
+    const float *v_reg;
+    const int32_t *pos;
+    int32_t *err;
+    int nt, nh, nk, hd, cap, W;
+    float scale_log2;
+};
+
+// Round to the nearest TF32 value (10 explicit mantissa bits), ties away from zero.
+__device__ __forceinline__ float tf32_rna(float x) {
+    uint32_t r;
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+    return __uint_as_float(r);
+}
+
+__device__ __forceinline__ void split_tf32(float x, float &hi, float &lo) {
+    hi = tf32_rna(x);
+    lo = tf32_rna(x - hi);
+}
+
+// Splits the fp32 values of an SW128 slab region in place (hi) and into a twin region (lo).
+__device__ __forceinline__ void split_region(float *hi, float *lo, int n_float4, int tid) {
+    float4 *h4 = reinterpret_cast<float4 *>(hi);
+    float4 *l4 = reinterpret_cast<float4 *>(lo);
+    for (int i = tid; i < n_float4; i += kSoftThreads) {
+        float4 x = h4[i], a, b;
+        split_tf32(x.x, a.x, b.x);
+        split_tf32(x.y, a.y, b.y);
+        split_tf32(x.z, a.z, b.z);
+        split_tf32(x.w, a.w, b.w);
+        h4[i] = a;
+        l4[i] = b;
+    }
+}
+
+template <int HDKV>
+__global__ void __launch_bounds__(kThreadsP, 1)
+    prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                   const PParams a) {
+    extern __shared__ unsigned char smem_raw[];
+    Smem<HDKV> &sm = *reinterpret_cast<Smem<HDKV> *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int t0 = blockIdx.x * BM;
+    const int h = blockIdx.y;
+    const int g = a.nh / a.nk;
+    const int hk = h / g;
+    volatile int *abort_flag = &sm.abort_flag;
+
+    if (tid == 0) {
+        mbar_init(&sm.bar_q, 1);
+        mbar_init(&sm.bar_k, 1);
+        mbar_init(&sm.bar_kv, kSoftThreads);
+        mbar_init(&sm.bar_s, 1);
+        mbar_init(&sm.bar_p, kSoftThreads);
+        mbar_init(&sm.bar_o, 1);
+        sm.abort_flag = 0;
+        sm.lmax = 0;
+        mbar_init_fence();
+    }
+    if (warp == kProducerWarp) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         su32(&sm.tmem_base)),
+                     "r"(kTmemCols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    // this row's window ("11 . Attention...", §3.2.4: vl = min(pos[t] + 1, nkv), nkv <= n_ctx)
+    int L_t = 0;
+    const int t = t0 + tid;
+    if (tid < kSoftThreads && t < a.nt) {
+        const int p = __ldg(a.pos + t);
+        L_t = p < 0 ? 0 : (p + 1 < a.cap ? p + 1 : a.cap);
+        if ((p < 0 || p >= a.cap) && h == 0) flag_error(a.err, MINF_ERRBIT_ATTN_POS);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (tid < kSoftThreads) {
+        int mx = L_t;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+        if (lane == 0) atomicMax(&sm.lmax, mx);
+    }
+    __syncthreads();
+    const int lmax = sm.lmax;
+    const int n_tiles = (lmax + BN - 1) / BN;
+    const uint32_t tmem = sm.tmem_base;
+    constexpr uint32_t kQBytes = BM * HDKV * 4, kKBytes = BN * HDKV * 4;
+
+    if (warp == kProducerWarp) {
+        if (lane == 0 && n_tiles > 0) {
+            mbar_expect_tx(&sm.bar_q, kQBytes);
+#pragma unroll
+            for (int c = 0; c < HDKV / 32; ++c) tma_load_2d(sm.qh[c], &tm_q, h * a.hd + 32 * c, t0, &sm.bar_q);
+            mbar_expect_tx(&sm.bar_k, kKBytes);
+#pragma unroll
+            for (int c = 0; c < HDKV / 32; ++c) tma_load_2d(sm.kh[c], &tm_k, hk * HDKV + 32 * c, 0, &sm.bar_k);
+            for (int i = 0; i < n_tiles; ++i) {
+                // S = Q K^T once the softmax warps have split Q (first tile), K and V^T
+                if (!mbar_wait(&sm.bar_kv, i & 1, abort_flag, a.err)) break;
+                tc_fence_after();
+#pragma unroll
+                for (int kk = 0; kk < HDKV / 8; ++kk) {
+                    const uint32_t off = (kk & 3) * 32;
+                    const uint64_t qh = sw128_desc(su32(sm.qh[kk >> 2]) + off);
+                    const uint64_t ql = sw128_desc(su32(sm.ql[kk >> 2]) + off);
+                    const uint64_t kh = sw128_desc(su32(sm.kh[kk >> 2]) + off);
+                    const uint64_t kl = sw128_desc(su32(sm.kl[kk >> 2]) + off);
+                    mma_tf32(tmem, qh, kh, tf32_idesc(BM, BN), kk > 0);
+                    mma_tf32(tmem, qh, kl, tf32_idesc(BM, BN), 1);
+                    mma_tf32(tmem, ql, kh, tf32_idesc(BM, BN), 1);
+                }
+                mma_commit(&sm.bar_s);
+                if (i + 1 < n_tiles) {
+                    // the K tile is free once S(i) is complete
+                    if (!mbar_wait(&sm.bar_s, i & 1, abort_flag, a.err)) break;
+                    mbar_expect_tx(&sm.bar_k, kKBytes);
+#pragma unroll
+                    for (int c = 0; c < HDKV / 32; ++c)
+                        tma_load_2d(sm.kh[c], &tm_k, hk * HDKV + 32 * c, (i + 1) * BN, &sm.bar_k);
+                }
+                if (!mbar_wait(&sm.bar_p, i & 1, abort_flag, a.err)) break;
+                tc_fence_after();
+#pragma unroll
+                for (int kk = 0; kk < BN / 8; ++kk) {
+                    const uint32_t off = (kk & 3) * 32;
+                    const uint64_t ph = sw128_desc(su32(sm.ph[kk >> 2]) + off);
+                    const uint64_t pl = sw128_desc(su32(sm.pl[kk >> 2]) + off);
+                    const uint64_t vh = sw128_desc(su32(sm.vh[kk >> 2]) + off);
+                    const uint64_t vl = sw128_desc(su32(sm.vl[kk >> 2]) + off);
+                    mma_tf32(tmem + kOCol, ph, vh, tf32_idesc(BM, HDKV), kk > 0);
+                    mma_tf32(tmem + kOCol, ph, vl, tf32_idesc(BM, HDKV), 1);
+                    mma_tf32(tmem + kOCol, pl, vh, tf32_idesc(BM, HDKV), 1);
+                }
+                mma_commit(&sm.bar_o);
+            }
+        }
+    } else {
+        // softmax and epilogue: thread tid owns query row tid (TMEM lane tid)
+        const uint32_t trow = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+        const float sl = a.scale_log2;
+        float o[HDKV];
+#pragma unroll
+        for (int d = 0; d < HDKV; ++d) o[d] = 0.0f;
+        float m = -INFINITY, l = 0.0f;
+        const int vk = tid & (BN - 1), vq = tid / BN;  // V^T staging: key, quarter of the dims
+        if (n_tiles > 0 && mbar_wait(&sm.bar_q, 0, abort_flag, a.err))
+            split_region(&sm.qh[0][0], &sm.ql[0][0], BM * HDKV / 4, tid);
+        for (int i = 0; i < n_tiles; ++i) {
+            const int j0 = i * BN;
+            if (!mbar_wait(&sm.bar_k, i & 1, abort_flag, a.err)) break;
+            split_region(&sm.kh[0][0], &sm.kl[0][0], BN * HDKV / 4, tid);
+            {   // V tile -> V^T hi/lo (K-major, keys along K); keys past the widest window are zero
+                const int key = j0 + vk;
+                const float *vrow = a.v_reg + static_cast<size_t>(key) * a.W + hk * HDKV;
+                unsigned char *vth = reinterpret_cast<unsigned char *>(sm.vh[vk >> 5]);
+                unsigned char *vtl = reinterpret_cast<unsigned char *>(sm.vl[vk >> 5]);
+#pragma unroll 4
+                for (int d4 = vq * (HDKV / 16); d4 < (vq + 1) * (HDKV / 16); ++d4) {
+                    const float4 v = key < lmax ? reinterpret_cast<const float4 *>(vrow)[d4]
+                                                : make_float4(0.f, 0.f, 0.f, 0.f);
+                    const float vv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        float hi, lo;
+                        split_tf32(vv[e], hi, lo);
+                        const uint32_t off = sw128_off(4 * d4 + e, vk & 31);
+                        *reinterpret_cast<float *>(vth + off) = hi;
+                        *reinterpret_cast<float *>(vtl + off) = lo;
+                    }
+                }
+            }
+            fence_async_smem();  // split Q/K and V^T -> visible to the tensor cores
+            tc_fence_before();
+            mbar_arrive(&sm.bar_kv);
+            if (!mbar_wait(&sm.bar_s, i & 1, abort_flag, a.err)) break;
+            tc_fence_after();
+            float r[32];
+            tmem_ld32(trow, r);
+            float mx = -INFINITY;
+#pragma unroll
+            for (int e = 0; e < 32; ++e)
+                if (j0 + e < L_t) mx = fmaxf(mx, r[e] * sl);
+            const float m_new = fmaxf(m, mx);
+            const bool none = (m_new == -INFINITY);  // no key visible to this row yet
+            const float corr = none ? 1.0f : ex2_approx(m - m_new);
+            float ps = 0.0f;
+            unsigned char *pph = reinterpret_cast<unsigned char *>(sm.ph[0]);
+            unsigned char *ppl = reinterpret_cast<unsigned char *>(sm.pl[0]);
+#pragma unroll
+            for (int e4 = 0; e4 < 8; ++e4) {
+                float4 wh, wl;
+                float *whv = reinterpret_cast<float *>(&wh), *wlv = reinterpret_cast<float *>(&wl);
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int j = j0 + 4 * e4 + e;
+                    const float pe = (!none && j < L_t) ? ex2_approx(r[4 * e4 + e] * sl - m_new) : 0.0f;
+                    split_tf32(pe, whv[e], wlv[e]);
+                    ps += pe;
+                }
+                *reinterpret_cast<float4 *>(pph + sw128_off(tid, 4 * e4)) = wh;
+                *reinterpret_cast<float4 *>(ppl + sw128_off(tid, 4 * e4)) = wl;
+            }
+            l = fmaf(l, corr, ps);
+            m = m_new;
+            fence_async_smem();  // P hi/lo -> visible to the tensor cores
+            tc_fence_before();
+            mbar_arrive(&sm.bar_p);
+            if (!mbar_wait(&sm.bar_o, i & 1, abort_flag, a.err)) break;
+            tc_fence_after();
+#pragma unroll
+            for (int c = 0; c < HDKV / 32; ++c) {
+                tmem_ld32(trow + kOCol + 32 * c, r);
+#pragma unroll
+                for (int e = 0; e < 32; ++e) o[32 * c + e] = fmaf(o[32 * c + e], corr, r[e]);
+            }
+            tc_fence_before();
+        }
+        if (t < a.nt && !*abort_flag) {
+            float4 *dst = reinterpret_cast<float4 *>(a.out + (static_cast<size_t>(t) * a.nh + h) * HDKV);
+            const float inv = l > 0.0f ? 1.0f / l : 0.0f;
+#pragma unroll
+            for (int d4 = 0; d4 < HDKV / 4; ++d4)
+                dst[d4] = make_float4(o[4 * d4] * inv, o[4 * d4 + 1] * inv, o[4 * d4 + 2] * inv,
+                                      o[4 * d4 + 3] * inv);
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == kProducerWarp) {
+        if (*abort_flag && lane == 0) {
+            // let copies and MMAs that may still be in flight finish before TMEM and shared memory go away
+            const unsigned long long t0n = gtimer();
+            while (gtimer() - t0n < kWaitBudgetNs / 4) {
+            }
+        }
+        __syncwarp();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols)
+                     : "memory");
+    }
+}
+
+template <int HDKV>
+int launch_t(const PrefillArgs &pa, cudaStream_t s) {
+    CUtensorMap tq, tk;
+    if (!make_tensor_map_2d(&tq, pa.q, static_cast<uint64_t>(pa.nh) * pa.hd, pa.nt, 32, BM, true))
+        return MINF_ERR_CUDA;
+    if (!make_tensor_map_2d(&tk, pa.k_reg, static_cast<uint64_t>(pa.nk) * HDKV, pa.cap, 32, BN, true))
+        return MINF_ERR_CUDA;
+    PParams a;
+    a.out = pa.out;
+    a.v_reg = pa.v_reg;
+    a.pos = pa.pos;
+    a.err = pa.err;
+    a.nt = pa.nt;
+    a.nh = pa.nh;
+    a.nk = pa.nk;
+    a.hd = pa.hd;
+    a.cap = pa.cap;
+    a.W = pa.nk * HDKV;
+    a.scale_log2 = pa.scale * kLog2e;
+    const size_t smem = sizeof(Smem<HDKV>) + 1024;
+    static bool attr_set = false;
+    if (!attr_set) {
+        if (cudaFuncSetAttribute(prefill_kernel<HDKV>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(smem)) != cudaSuccess)
+            return MINF_ERR_CUDA;
+        attr_set = true;
+    }
+    const dim3 grid((pa.nt + BM - 1) / BM, pa.nh);
+    prefill_kernel<HDKV><<<grid, kThreadsP, smem, s>>>(tq, tk, a);
+    return cudaPeekAtLastError() == cudaSuccess ? MINF_OK : MINF_ERR_CUDA;
+}
+
+}  // namespace
+
+int launch_prefill(const PrefillArgs &pa, cudaStream_t s) {
+    if (pa.nt == 0) return MINF_OK;
+    if (pa.nt > 65535 * BM || pa.nh > 65535) return MINF_ERR_UNSUPPORTED;
+    if ((static_cast<long long>(pa.nh) * pa.hd) % 4 != 0) return MINF_ERR_UNSUPPORTED;
+    if (pa.hd_kv == 64) return launch_t<64>(pa, s);
+    if (pa.hd_kv == 128) return launch_t<128>(pa, s);
+    return MINF_ERR_UNSUPPORTED;
+}
+
+}  // namespace minf

@@ -62,6 +62,9 @@ enum {
 #define MINF_ERRBIT_ATTN_POS 0x4   /* attention: pos < 0 (empty window, zero output) or
                                       pos >= cap (window clamped to cap, as [P1] §3.2.4's
                                       nkv = min(max pos + 1, n_ctx) does) */
+#define MINF_ERRBIT_TIMEOUT 0x8    /* an internal pipeline wait exceeded its time budget (200 ms);
+                                      the call's outputs are invalid.  Kernels bound every wait
+                                      so that a fault in the pipeline returns instead of hanging. */
 
 /* Human-readable name of a status code (static storage). */
 MINF_API const char *minf_status_string(int status);
@@ -142,27 +145,35 @@ MINF_API size_t minf_attn_decode_workspace_bytes(int n_seq, int n_head, int n_kv
  *   for sequence s and query head h, hk = h / g, L = min(pos[s] + 1, cap_s),
  *   out[s, h] = sum_{j < L} softmax_j(scale * q[s,h][0:hd_kv] . K[j, hk]) V[j, hk]
  * where K[j] is row seq_row_off[s] + j of the arena.  Arena: k_reg/v_reg
- * [rows, W]; q: [n_seq, n_head, hd]; out: [n_seq, n_head*hd_kv].
- * seq_row_off: int64[n_seq] device (NULL = all 0); seq_cap: int32[n_seq]
- * device (NULL = max_cap for all); max_cap: host upper bound of every cap_s
- * (it sizes the split grid and the workspace; the grid never depends on pos,
- * so the call can be graph-captured and replayed with new positions).
+ * [arena_rows, W]; q: [n_seq, n_head, hd]; out: [n_seq, n_head*hd_kv].
+ * seq_row_off: int64[n_seq] device (NULL = all 0, and the arena is then
+ * max_cap rows); seq_cap: int32[n_seq] device (NULL = max_cap for all);
+ * max_cap: host upper bound of every cap_s (it sizes the split grid and the
+ * workspace; the grid never depends on pos, so the call can be graph-captured
+ * and replayed with new positions); arena_rows: rows of the arena when
+ * seq_row_off is given (the kernels read rows only inside it; ignored
+ * otherwise).  The cached rows stream through a TMA pipeline, so the K/V
+ * regions must stay in device memory that the tensor map can address.
  * Device errors: MINF_ERRBIT_ATTN_POS (see above).
  * Errors: MINF_ERR_ARG, MINF_ERR_GEOMETRY, MINF_ERR_UNSUPPORTED (hd_kv not 64
  * or 128, g > 8, hd > 256), MINF_ERR_WORKSPACE.
  */
 MINF_API int minf_gqa_attn_decode(float *out, const float *q, const float *k_reg, const float *v_reg,
                          const int64_t *seq_row_off, const int32_t *seq_cap, int max_cap,
-                         const int32_t *pos, int n_seq, int n_head, int n_kv_head, int hd,
-                         int hd_kv, float scale, void *ws, size_t ws_bytes, int32_t *err,
-                         minf_stream_t stream);
+                         int64_t arena_rows, const int32_t *pos, int n_seq, int n_head,
+                         int n_kv_head, int hd, int hd_kv, float scale, void *ws,
+                         size_t ws_bytes, int32_t *err, minf_stream_t stream);
 
 /*
  * Causal prefill attention over one sequence's regions.  [P1] §3.2.4: token t
  * attends over rows [0, min(pos[t] + 1, cap)) of the K/V regions [cap, W]
  * (store before attention: the tokens' own rows must already be appended).
- * q: [nt, n_head, hd]; out: [nt, n_head*hd_kv].
- * Device errors: MINF_ERRBIT_ATTN_POS.
+ * q: [nt, n_head, hd]; out: [nt, n_head*hd_kv].  Positions are arbitrary
+ * (a prefill that continues an existing cache passes pos = n_past..).
+ * The QK^T and PV products run on the tensor cores in TF32 with fp32
+ * accumulation (outputs agree with an fp32 evaluation to about 1e-3 absolute);
+ * max, exp and sums run in fp32.  ws may be NULL (no workspace is needed).
+ * Device errors: MINF_ERRBIT_ATTN_POS, MINF_ERRBIT_TIMEOUT.
  * Errors: as minf_gqa_attn_decode.
  */
 MINF_API int minf_gqa_attn_prefill(float *out, const float *q, const float *k_reg, const float *v_reg,
@@ -179,8 +190,10 @@ MINF_API size_t minf_attn_prefill_workspace_bytes(int nt, int n_head, int n_kv_h
  * q [nt, n_head, hd] and k [nt, n_kv_head, hd_kv] rotated in place at pos;
  * rotated k and v appended at pos into the regions [cap, W]; out [nt, n_head*hd_kv]
  * = attention with scale 1/sqrt(hd) ([P1] §2.4).  nt == 1 runs the split-KV
- * decode path, nt > 1 the prefill path.  ws/ws_bytes: at least
- * max(decode bytes for 1 sequence, prefill bytes for nt tokens).
+ * decode path (a single launch for the supported geometries), nt > 1 the
+ * tensor-core prefill path.  ws/ws_bytes: for nt == 1 at least
+ * minf_attn_decode_workspace_bytes(1, n_head, n_kv_head, hd_kv, cap); unused
+ * (may be NULL) for nt > 1.
  * Device errors: any of the bits above.
  */
 MINF_API int minf_layer_attn_step(float *xn, const float *h, const float *gain, float eps, int n_embd,
@@ -195,13 +208,15 @@ MINF_API int minf_layer_attn_step(float *xn, const float *h, const float *gain, 
  * q: [n_seq, n_head, hd]; k, v: [n_seq, W]; pos: int32[n_seq]; sequence s owns
  * arena rows [seq_row_off[s], seq_row_off[s] + seq_cap[s]) and appends at
  * row seq_row_off[s] + pos[s].  Both descriptor arrays are device memory and
- * required.  ws: minf_attn_decode_workspace_bytes(n_seq, ..., max_cap).
+ * required; arena_rows is the arena's row count.
+ * ws: minf_attn_decode_workspace_bytes(n_seq, ..., max_cap).
  */
 MINF_API int minf_layer_attn_step_batched(float *xn, const float *h, const float *gain, float eps,
                                  int n_embd, float *q, float *k, const float *v,
                                  const int32_t *pos, int n_seq, float *k_arena, float *v_arena,
                                  const int64_t *seq_row_off, const int32_t *seq_cap, int max_cap,
-                                 int n_head, int n_kv_head, int hd, int hd_kv, float theta,
+                                 int64_t arena_rows, int n_head, int n_kv_head, int hd, int hd_kv,
+                                 float theta,
                                  float freq_scale, int style, float *out, void *ws,
                                  size_t ws_bytes, int32_t *err, minf_stream_t stream);
 

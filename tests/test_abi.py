@@ -67,13 +67,13 @@ def test_host_validation_needs_no_gpu(lib):
     P = ctypes.c_void_p
     fake = P(0x1000)  # never dereferenced: validation rejects before any launch
     # hd < hd_kv is refused
-    assert lib.minf_gqa_attn_decode(fake, fake, fake, fake, None, None, 16, fake, 1, 4, 2, 64, 128,
+    assert lib.minf_gqa_attn_decode(fake, fake, fake, fake, None, None, 16, 0, fake, 1, 4, 2, 64, 128,
                                     0.1, fake, 1 << 20, fake, None) == b.MINF_ERR_GEOMETRY
     # n_head not a multiple of n_kv_head
-    assert lib.minf_gqa_attn_decode(fake, fake, fake, fake, None, None, 16, fake, 1, 5, 2, 64, 64,
+    assert lib.minf_gqa_attn_decode(fake, fake, fake, fake, None, None, 16, 0, fake, 1, 5, 2, 64, 64,
                                     0.1, fake, 1 << 20, fake, None) == b.MINF_ERR_GEOMETRY
     # an hd_kv the kernels do not implement
-    assert lib.minf_gqa_attn_decode(fake, fake, fake, fake, None, None, 16, fake, 1, 4, 2, 96, 96,
+    assert lib.minf_gqa_attn_decode(fake, fake, fake, fake, None, None, 16, 0, fake, 1, 4, 2, 96, 96,
                                     0.1, fake, 1 << 20, fake, None) == b.MINF_ERR_UNSUPPORTED
     # null pointers, odd head dim, bad style
     assert lib.minf_rope(None, fake, 1, 1, 64, 1e4, 1.0, 0, fake, None) == b.MINF_ERR_ARG
@@ -86,7 +86,7 @@ def test_host_validation_needs_no_gpu(lib):
     # a workspace smaller than required
     need = lib.minf_attn_decode_workspace_bytes(1, 16, 8, 128, 4096)
     assert need > 0
-    assert lib.minf_gqa_attn_decode(fake, fake, fake, fake, None, None, 4096, fake, 1, 16, 8, 128,
+    assert lib.minf_gqa_attn_decode(fake, fake, fake, fake, None, None, 4096, 0, fake, 1, 16, 8, 128,
                                     128, 0.1, fake, need - 256, fake, None) == b.MINF_ERR_WORKSPACE
     assert lib.minf_silu_mul(None, fake, fake, 4, None) == b.MINF_ERR_ARG
 
