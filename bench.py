@@ -47,7 +47,7 @@ def parse_args(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="budget of the CPU oracle sample")
     ap.add_argument("--layers", type=int, default=28, help="layers of the headline workload (profiling cases)")
     ap.add_argument("--nkv", type=int, default=40960, help="cached rows of the headline workload")
-    ap.add_argument("--only", choices=["prefill"], default=None,
+    ap.add_argument("--only", choices=["prefill", "single-step"], default=None,
                     help="time one secondary workload alone (a small case for profiling)")
     return ap.parse_args(argv)
 
@@ -637,6 +637,13 @@ def main(argv=None):
             print(json.dumps({"metric": "prefill tok/s", "value": tok_s, "unit": "tok/s",
                               "layer_us": layer_us, "steps": args.steps,
                               "config": {"workload": "causal prefill, Qwen2.5-0.5B shape, 24 layers, nt=512"}}))
+        return 0
+    if args.only == "single-step":
+        us = run_single_step(m, torch, wl, dev, reps=max(args.steps, 10))
+        if rank == 0:
+            print(json.dumps({"metric": "layer attn-step µs", "value": us, "unit": "µs", "steps": args.steps,
+                              "config": {"workload": "single decode step, one layer, Qwen2.5-0.5B shape, "
+                                                     "127 cached rows, token at pos 127"}}))
         return 0
     H = run_headline(m, torch, wl, args, world, dev)
     g = H["S"]["g"]
