@@ -47,6 +47,7 @@ _SIGS = {
     "minf_attn_decode_workspace_bytes": ([_I, _I, _I, _I, _I], _SZ),
     "minf_attn_prefill_workspace_bytes": ([_I, _I, _I, _I, _I], _SZ),
     "minf_gqa_attn_decode": ([_P, _P, _P, _P, _P, _P, _I, _I64, _P, _I, _I, _I, _I, _I, _F, _P, _SZ, _P, _P], _I),
+    "minf_gqa_attn_decode_static_ws": ([_P, _P, _P, _P, _P, _P, _I, _I64, _P, _I, _I, _I, _I, _I, _F, _P, _P], _I),
     "minf_gqa_attn_prefill": ([_P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _I, _F, _P, _SZ, _P, _P], _I),
     "minf_layer_attn_step": ([_P, _P, _P, _F, _I, _P, _P, _P, _P, _I, _P, _P, _I, _I, _I, _I, _I,
                               _F, _F, _I, _P, _P, _SZ, _P, _P], _I),
@@ -173,6 +174,17 @@ def minf_gqa_attn_decode(out, q, k_reg, v_reg, seq_row_off, seq_cap, max_cap, po
         k_reg.shape[0], _dev(pos, torch.int32, "pos"), pos.numel(), n_head, n_kv_head, hd, hd_kv, scale,
         _dev(ws, torch.uint8, "ws"), ws.numel(), _dev(err, torch.int32, "err"), _stream(stream)),
         "minf_gqa_attn_decode")
+
+
+def minf_gqa_attn_decode_static_ws(out, q, k_reg, v_reg, seq_row_off, seq_cap, max_cap, pos, n_head,
+                                   n_kv_head, hd, hd_kv, scale, err, stream=None):
+    """minf_gqa_attn_decode for callers that cannot allocate: the library's own fixed device
+    scratch replaces the workspace argument (see include/minf.h for its limits)."""
+    _check(lib().minf_gqa_attn_decode_static_ws(
+        _dev(out, name="out"), _dev(q, name="q"), _dev(k_reg, name="k_reg"), _dev(v_reg, name="v_reg"),
+        _dev(seq_row_off, torch.int64, "seq_row_off"), _dev(seq_cap, torch.int32, "seq_cap"), max_cap,
+        k_reg.shape[0], _dev(pos, torch.int32, "pos"), pos.numel(), n_head, n_kv_head, hd, hd_kv, scale,
+        _dev(err, torch.int32, "err"), _stream(stream)), "minf_gqa_attn_decode_static_ws")
 
 
 def minf_gqa_attn_prefill(out, q, k_reg, v_reg, pos, n_head, n_kv_head, hd, hd_kv, scale, ws, err,

@@ -165,6 +165,32 @@ MINF_API int minf_gqa_attn_decode(float *out, const float *q, const float *k_reg
                          size_t ws_bytes, int32_t *err, minf_stream_t stream);
 
 /*
+ * Decode attention without a caller-provided workspace.  None of the source pages has a
+ * counterpart: this entry point exists for callers that cannot allocate device memory --
+ * code embedded where it is handed only its input and output buffers, or callers that must
+ * not call the device allocator on their hot path (it can synchronise the device or
+ * fragment a memory pool they do not own).  It computes exactly what minf_gqa_attn_decode
+ * computes, with the same arguments minus ws/ws_bytes, and allocates nothing: the split
+ * partials and merge tickets live in a fixed 8 MiB array of device memory that the library
+ * owns (every GPU that loads the library holds it until the process exits).
+ *   - A call that would need more than 8 MiB of workspace (see
+ *     minf_attn_decode_workspace_bytes) returns MINF_ERR_WORKSPACE and launches nothing.
+ *   - The first call on a device looks up that device's copy of the array (with the device
+ *     current); make that first call before any stream capture on the device.
+ *   - Each call clears the part of the array it uses (an asynchronous memset on `stream`)
+ *     before its kernel.
+ *   - Every call shares the one array: calls whose work overlaps on the GPU (different
+ *     streams, or concurrent host threads) race on it and must be serialised by the caller.
+ * Device errors and other statuses: as minf_gqa_attn_decode.
+ */
+MINF_API int minf_gqa_attn_decode_static_ws(float *out, const float *q, const float *k_reg,
+                                   const float *v_reg, const int64_t *seq_row_off,
+                                   const int32_t *seq_cap, int max_cap, int64_t arena_rows,
+                                   const int32_t *pos, int n_seq, int n_head, int n_kv_head,
+                                   int hd, int hd_kv, float scale, int32_t *err,
+                                   minf_stream_t stream);
+
+/*
  * Causal prefill attention over one sequence's regions.  [P1] §3.2.4: token t
  * attends over rows [0, min(pos[t] + 1, cap)) of the K/V regions [cap, W]
  * (store before attention: the tokens' own rows must already be appended).
