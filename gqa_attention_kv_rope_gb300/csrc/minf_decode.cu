@@ -21,16 +21,17 @@
 // running (max, sum, acc) in the log2 domain, folded in shared memory at the end of a unit.
 //
 // Merge.  A unit writes its partial (m, l, acc) to the workspace; the last unit of a
-// (sequence, kv group) to arrive -- an atomic ticket, no spinning -- folds all partials,
-// staging the (m, l) pairs in shared memory and spreading the acc loads over every
-// consumer thread, then resets the ticket.
+// (sequence, kv group) to arrive -- an atomic ticket, no spinning -- folds all partials in
+// one round trip: every consumer thread loads its share of the (m, l, acc) triples at once
+// and folds them online, then the shares are folded in shared memory; it resets the ticket.
 //
 // Fused layer step (kFused).  For one query token per sequence the same launch also does
 // the rest of the layer's attention stage: each unit rotates its q heads in registers
 // (RoPE, the same rounding as the standalone kernel), the unit whose run ends at row pos
-// rotates k, writes the K/V row into the region and uses it from shared memory, extra
-// units compute the RMSNorm rows, and the last unit of a group writes the rotated q and k
-// back.  With programmatic stream serialization the producer starts streaming cached rows
+// rotates k, writes it back, appends the K/V row to the region and uses it from shared
+// memory, a utility warp computes the RMSNorm rows, and the last unit of a group writes the
+// rotated q back.  The loads of q, k and v are issued before anything that waits on the
+// position, so a unit's prologue costs one memory round trip.  With programmatic stream serialization the producer starts streaming cached rows
 // (which no preceding kernel writes) before griddepcontrol.wait; everything the preceding
 // kernel may produce -- q, k, v, h, the workspace, the outputs -- is touched only after it.
 #include <cudaTypedefs.h>
@@ -47,7 +48,9 @@ namespace {
 
 constexpr int kNW = 8;                  // consumer warps
 constexpr int kCons = kNW * 32;         // consumer threads (named barrier 1)
-constexpr int kThreads = kCons + 32;    // + the producer warp
+constexpr int kProducer = kNW;          // warp 8: TMA producer
+constexpr int kUtility = kNW + 1;       // warp 9: RMSNorm rows of the fused step
+constexpr int kThreads = kCons + 64;    // + producer + utility (same register budget as 9 warps)
 constexpr int kSub = 8;                 // rows per warp sub-tile
 constexpr int kNST = 3;                 // pipeline stages
 constexpr int kStageBytes = 64 * 1024;  // K + V tile of one stage
@@ -159,6 +162,30 @@ __device__ __forceinline__ void rope_lane(float4 (&x)[KF4], const float (&sn)[2 
     }
 }
 
+// Sin and cos of the pair angles a lane needs for rope_lane.  The 4 lanes of a warp with the
+// same `sub` (one per r4) need the same 2*KF4 angles, so each computes a quarter of them and
+// they are exchanged by shuffles.  Style 0: angle k is pair 4*sub + 32*(k/4) + k%4; style 1:
+// pair (4*sub + 32*(k/2))/2 + k%2 (matching rope_lane's indexing).
+template <int KF4>
+__device__ __forceinline__ void rope_angles(float (&sn)[2 * KF4], float (&cs)[2 * KF4], float pf,
+                                            const RopeTable &tab, int style, int sub, int r4) {
+    constexpr int NA = 2 * KF4;
+    constexpr int NQ = NA / 4;
+    float ms[NQ], mc[NQ];
+#pragma unroll
+    for (int q = 0; q < NQ; ++q) {
+        const int k = 4 * q + r4;
+        const int j = style == 0 ? 4 * sub + 32 * (k >> 2) + (k & 3) : (4 * sub + 32 * (k >> 1)) / 2 + (k & 1);
+        sincosf(__fmul_rn(pf, tab.f[j]), &ms[q], &mc[q]);
+    }
+#pragma unroll
+    for (int k = 0; k < NA; ++k) {
+        const int src = (k & 3) * 8 + sub;
+        sn[k] = __shfl_sync(0xffffffffu, ms[k >> 2], src);
+        cs[k] = __shfl_sync(0xffffffffu, mc[k >> 2], src);
+    }
+}
+
 // The unit u decodes to (sequence, pair, split) and, from the sequence's position, to the
 // run of rows it owns.  Producer and consumers derive it identically.
 struct Unit {
@@ -197,14 +224,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr int VJ = kSub / VRP;  // passes per sub-tile
     constexpr uint32_t kTileBytes = R * HDKV * 4;
     extern __shared__ unsigned char smem_raw[];
-    float *ring = reinterpret_cast<float *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                            ~static_cast<uintptr_t>(1023));
+    // 1024-aligned ring, derived from the shared array itself so loads stay in the shared space
+    float *ring = reinterpret_cast<float *>(smem_raw + ((1024u - (su32(smem_raw) & 1023u)) & 1023u));
     __shared__ unsigned long long full[kNST], empty[kNST];
     __shared__ float sm_m[kNW][GH], sm_l[kNW][GH];
     __shared__ float4 sm_acc[kNW][GH][VL];
-    __shared__ float sm_pm[GH][kMaxSplit], sm_pl[GH][kMaxSplit];
-    __shared__ float sm_L[GH];
     __shared__ float4 sm_red[kCons];
+    __shared__ float sm_redM[kCons], sm_redL[kCons];
     __shared__ __align__(16) float sm_knew[HDKV], sm_vnew[HDKV];
     __shared__ int sm_last, sm_abort;
 
@@ -212,7 +238,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int W = a.nk * HDKV;
     const int P = a.nk * a.groups;
     const int n_units = a.n_seq * P * a.n_split;
-    const int n_total = n_units + (kFused ? a.n_seq : 0);
     volatile int *abort_flag = &sm_abort;
 
     if (tid == 0) {
@@ -225,7 +250,37 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     __syncthreads();
 
-    if (warp == kNW) {
+    if (warp == kUtility) {
+        // ---------------------------------------------------------------- utility warp
+        // RMSNorm rows ("11 . Attention, vec ops, and the KV cache", §3.2.1), spread over the
+        // CTAs; h is produced upstream, so it is read only after the dependency wait.
+        gdc_wait();
+        for (int s = blockIdx.x; kFused && s < a.n_seq; s += gridDim.x) {
+            const float *hr = a.h + static_cast<size_t>(s) * a.n_embd;
+            float *yr = a.xn + static_cast<size_t>(s) * a.n_embd;
+            const int n4 = a.n_embd >> 2;
+            float ss = 0.0f;
+            for (int i = lane; i < n4; i += 32) {
+                const float4 v = reinterpret_cast<const float4 *>(hr)[i];
+                ss = fmaf(v.x, v.x, ss);
+                ss = fmaf(v.y, v.y, ss);
+                ss = fmaf(v.z, v.z, ss);
+                ss = fmaf(v.w, v.w, ss);
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+            const float scale = 1.0f / sqrtf(ss / static_cast<float>(a.n_embd) + a.eps);
+            for (int i = lane; i < n4; i += 32) {
+                const float4 v = reinterpret_cast<const float4 *>(hr)[i];
+                const float4 g = a.gain ? reinterpret_cast<const float4 *>(a.gain)[i]
+                                        : make_float4(1.f, 1.f, 1.f, 1.f);
+                reinterpret_cast<float4 *>(yr)[i] = make_float4(v.x * scale * g.x, v.y * scale * g.y,
+                                                                v.z * scale * g.z, v.w * scale * g.w);
+            }
+        }
+        return;  // writes only this kernel's own output: nothing a dependent launch may prefetch
+    }
+    if (warp == kProducer) {
         // ---------------------------------------------------------------- producer
         if (lane == 0) {
             uint32_t it = 0;
@@ -283,37 +338,31 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float sl = a.scale_log2;
     uint32_t it = 0;
 
-    for (int u = blockIdx.x; u < n_total; u += gridDim.x) {
-        if (kFused && u >= n_units) {
-            // RMSNorm row of a sequence ("11 . Attention, vec ops, and the KV cache", §3.2.1)
-            if (warp != 0) continue;
-            const int s = u - n_units;
-            const float *hr = a.h + static_cast<size_t>(s) * a.n_embd;
-            float *yr = a.xn + static_cast<size_t>(s) * a.n_embd;
-            const int n4 = a.n_embd >> 2;
-            float ss = 0.0f;
-            for (int i = lane; i < n4; i += 32) {
-                const float4 v = reinterpret_cast<const float4 *>(hr)[i];
-                ss = fmaf(v.x, v.x, ss);
-                ss = fmaf(v.y, v.y, ss);
-                ss = fmaf(v.z, v.z, ss);
-                ss = fmaf(v.w, v.w, ss);
-            }
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-            const float scale = 1.0f / sqrtf(ss / static_cast<float>(a.n_embd) + a.eps);
-            for (int i = lane; i < n4; i += 32) {
-                const float4 v = reinterpret_cast<const float4 *>(hr)[i];
-                const float4 g = a.gain ? reinterpret_cast<const float4 *>(a.gain)[i]
-                                        : make_float4(1.f, 1.f, 1.f, 1.f);
-                reinterpret_cast<float4 *>(yr)[i] = make_float4(v.x * scale * g.x, v.y * scale * g.y,
-                                                                v.z * scale * g.z, v.w * scale * g.w);
-            }
-            continue;
-        }
+    for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
         const Unit t = unit_of<R>(a, u);
         const int hk = t.y / a.groups;
         const int h0 = hk * (a.nh / a.nk) + (t.y % a.groups) * GH;  // first query head
+        // The inputs do not depend on the position: issue their loads before anything that
+        // does, so they overlap the position load instead of following it.
+        float4 qr[GH][KF4];
+#pragma unroll
+        for (int hh = 0; hh < GH; ++hh) {
+            const float4 *qh =
+                reinterpret_cast<const float4 *>(a.q + (static_cast<size_t>(t.s) * a.nh + h0 + hh) * a.hd);
+#pragma unroll
+            for (int i = 0; i < KF4; ++i) qr[hh][i] = qh[sub + 8 * i];
+        }
+        float4 kx[KF4], vx[KF4];
+        if (kFused && warp == 0 && r4 == 0) {
+            const float4 *kh =
+                reinterpret_cast<const float4 *>(a.k_io + (static_cast<size_t>(t.s) * a.nk + hk) * HDKV);
+            const float4 *vh = reinterpret_cast<const float4 *>(a.v_new + static_cast<size_t>(t.s) * W + hk * HDKV);
+#pragma unroll
+            for (int i = 0; i < KF4; ++i) {
+                kx[i] = kh[sub + 8 * i];
+                vx[i] = vh[sub + 8 * i];
+            }
+        }
         if (t.j == 0 && t.y == 0 && tid == 0) {
             int bits = 0;
             if (t.p < 0 || t.p >= t.cap_s) bits |= MINF_ERRBIT_ATTN_POS;
@@ -331,68 +380,36 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             continue;
         }
+        // The unit whose run ends at the window's last row owns k: it rotates it, writes it back
+        // and, when the row fits the region, appends the new K/V row (no other unit reads k).
+        const bool k_writer = kFused && t.r_end == t.L;
+        const bool own_new = k_writer && t.p < t.cap_s;
+        const int pnew = own_new ? t.p : -1;
         const float *Kg = a.k_reg + t.base * W + hk * HDKV;  // fused path only: the new row
         const float *Vg = a.v_reg + t.base * W + hk * HDKV;
-        const bool own_new = kFused && t.p < t.cap_s && t.r_end == t.L;
-        const int pnew = own_new ? t.p : -1;
-
-        float4 qr[GH][KF4];
-        float sn[2 * KF4], cs[2 * KF4];
         if (kFused) {
-            // style 0: element e of float4 i < KF4/2 is pair 4*sub + 32*i + e (its partner sits
-            // in float4 i + KF4/2); style 1: float4 i holds pairs (4*sub + 32*i)/2 + {0, 1}
-            const float pf = static_cast<float>(t.p);
-            if (a.style == 0) {
+            float sn[2 * KF4], cs[2 * KF4];
+            rope_angles<KF4>(sn, cs, static_cast<float>(t.p), a.tab, a.style, sub, r4);
 #pragma unroll
-                for (int i = 0; i < KF4 / 2; ++i)
-#pragma unroll
-                    for (int e = 0; e < 4; ++e)
-                        sincosf(__fmul_rn(pf, a.tab.f[4 * sub + 32 * i + e]), &sn[4 * i + e], &cs[4 * i + e]);
-            } else {
-#pragma unroll
-                for (int i = 0; i < KF4; ++i)
-#pragma unroll
-                    for (int e = 0; e < 2; ++e)
-                        sincosf(__fmul_rn(pf, a.tab.f[(4 * sub + 32 * i) / 2 + e]), &sn[2 * i + e],
-                                &cs[2 * i + e]);
-            }
-        }
-#pragma unroll
-        for (int hh = 0; hh < GH; ++hh) {
-            const float4 *qh =
-                reinterpret_cast<const float4 *>(a.q + (static_cast<size_t>(t.s) * a.nh + h0 + hh) * a.hd);
-#pragma unroll
-            for (int i = 0; i < KF4; ++i) qr[hh][i] = qh[sub + 8 * i];
-            if (kFused) rope_lane<KF4>(qr[hh], sn, cs, a.style);
-        }
-        if (kFused) {
-            if (own_new && warp == 0 && r4 == 0) {
-                // rotate this kv head's k, stage the new K/V row and store it in the region
-                float4 kx[KF4];
-                const float4 *kh =
-                    reinterpret_cast<const float4 *>(a.k_io + (static_cast<size_t>(t.s) * a.nk + hk) * HDKV);
-                const float4 *vh =
-                    reinterpret_cast<const float4 *>(a.v_new + static_cast<size_t>(t.s) * W + hk * HDKV);
-#pragma unroll
-                for (int i = 0; i < KF4; ++i) kx[i] = kh[sub + 8 * i];
+            for (int hh = 0; hh < GH; ++hh) rope_lane<KF4>(qr[hh], sn, cs, a.style);
+            if (k_writer && warp == 0 && r4 == 0) {
                 rope_lane<KF4>(kx, sn, cs, a.style);
-                float4 *kdst = reinterpret_cast<float4 *>(const_cast<float *>(Kg) + static_cast<size_t>(t.p) * W);
-                float4 *vdst = reinterpret_cast<float4 *>(const_cast<float *>(Vg) + static_cast<size_t>(t.p) * W);
+                float4 *kh = reinterpret_cast<float4 *>(a.k_io + (static_cast<size_t>(t.s) * a.nk + hk) * HDKV);
 #pragma unroll
-                for (int i = 0; i < KF4; ++i) {
-                    const float4 vx = vh[sub + 8 * i];
-                    reinterpret_cast<float4 *>(sm_knew)[sub + 8 * i] = kx[i];
-                    reinterpret_cast<float4 *>(sm_vnew)[sub + 8 * i] = vx;
-                    kdst[sub + 8 * i] = kx[i];
-                    vdst[sub + 8 * i] = vx;
+                for (int i = 0; i < KF4; ++i) kh[sub + 8 * i] = kx[i];
+                if (own_new) {
+                    float4 *kdst = reinterpret_cast<float4 *>(const_cast<float *>(Kg) + static_cast<size_t>(t.p) * W);
+                    float4 *vdst = reinterpret_cast<float4 *>(const_cast<float *>(Vg) + static_cast<size_t>(t.p) * W);
+#pragma unroll
+                    for (int i = 0; i < KF4; ++i) {
+                        reinterpret_cast<float4 *>(sm_knew)[sub + 8 * i] = kx[i];
+                        reinterpret_cast<float4 *>(sm_vnew)[sub + 8 * i] = vx[i];
+                        kdst[sub + 8 * i] = kx[i];
+                        vdst[sub + 8 * i] = vx[i];
+                    }
                 }
-                __threadfence();
             }
-            named_sync(1, kCons);
-        }
-        if (early && !released) {
-            gdc_launch_dependents();
-            released = true;
+            named_sync(1, kCons);  // the staged row is visible to every consumer warp
         }
         float m[GH], l[GH];
         float4 acc[GH];
@@ -487,6 +504,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[slot]);
+            if (early && !released && warp == 0) {
+                // release the dependent launch once the appended row (if any) is visible; one
+                // thread's trigger releases the CTA, so only warp 0 -- which wrote the row --
+                // triggers, after its fence
+                if (own_new && r4 == 0) __threadfence();
+                __syncwarp();
+                if (lane == 0) gdc_launch_dependents();
+                released = true;
+            }
         }
 
         // ------------------------------------------------------------ end of the unit
@@ -540,103 +566,74 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool last = true;
         int *ticket = a.ws_ticket + static_cast<size_t>(t.s) * P + t.y;
         if (t.n_act > 1) {
-            __threadfence();
             named_sync(1, kCons);
-            if (tid == 0) sm_last = (atomicAdd(ticket, 1) == t.n_act - 1);
+            if (tid == 0) {
+                // acq_rel: publishes this CTA's partials (ordered before it by the barrier) and,
+                // for the last arrival, makes every other unit's partials visible to its loads
+                int old;
+                asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], 1;" : "=r"(old) : "l"(ticket) : "memory");
+                sm_last = old == t.n_act - 1;
+            }
             named_sync(1, kCons);
             last = sm_last;
         }
         if (!last) continue;
 
-        if (kFused) {
-            // every other unit of this group has finished reading q and k: write them back
-            if (lane < 8) {
-#pragma unroll
-                for (int hh = 0; hh < GH; ++hh) {
-                    if (hh % kNW != warp) continue;
-                    float4 *qh =
-                        reinterpret_cast<float4 *>(a.q_io + (static_cast<size_t>(t.s) * a.nh + h0 + hh) * a.hd);
-#pragma unroll
-                    for (int i = 0; i < KF4; ++i) qh[lane + 8 * i] = qr[hh][i];
+        if (t.n_act > 1) {
+            // One round trip for the merge: each thread folds its share of the splits online
+            // (running max and rescaled sums), then the shares are folded in shared memory.
+            constexpr int kPairs = GH * VL;
+            constexpr int kWays = kCons / kPairs > 0 ? kCons / kPairs : 1;
+            for (int i = tid; i < kPairs * kWays; i += kCons) {
+                const int pair = i % kPairs, way = i / kPairs;
+                const int hh = pair / VL, c = pair % VL;
+                const size_t ph = part0 + static_cast<size_t>(hh) * a.n_split;
+                float M = -INFINITY, Ls = 0.0f;
+                float4 A = make_float4(0.f, 0.f, 0.f, 0.f);
+    #pragma unroll 8
+                for (int j = way; j < t.n_act; j += kWays) {
+                    const float2 ml = __ldcg(reinterpret_cast<const float2 *>(a.ws_ml) + (ph + j));
+                    const float4 x = __ldcg(reinterpret_cast<const float4 *>(a.ws_acc + (ph + j) * HDKV) + c);
+                    const float Mn = fmaxf(M, ml.x);
+                    const float fo = M == -INFINITY ? 0.0f : ex2_approx(M - Mn);
+                    const float fn = ex2_approx(ml.x - Mn);
+                    A = make_float4(fmaf(x.x, fn, A.x * fo), fmaf(x.y, fn, A.y * fo), fmaf(x.z, fn, A.z * fo),
+                                    fmaf(x.w, fn, A.w * fo));
+                    Ls = fmaf(ml.y, fn, Ls * fo);
+                    M = Mn;
                 }
+                sm_red[way * kPairs + pair] = A;
+                sm_redM[way * kPairs + pair] = M;
+                sm_redL[way * kPairs + pair] = Ls;
             }
-            // k is rotated in place even when its row could not be stored (pos >= cap); the
-            // owner of the new row already holds it rotated, any other unit rotates it again
-            // with the same angles and rounding
-            if (warp == kNW - 1 && r4 == 0) {
-                float4 kx[KF4];
-                float4 *kh = reinterpret_cast<float4 *>(a.k_io + (static_cast<size_t>(t.s) * a.nk + hk) * HDKV);
-                if (own_new) {
-#pragma unroll
-                    for (int i = 0; i < KF4; ++i) kx[i] = reinterpret_cast<const float4 *>(sm_knew)[sub + 8 * i];
-                } else {
-#pragma unroll
-                    for (int i = 0; i < KF4; ++i) kx[i] = kh[sub + 8 * i];
-                    rope_lane<KF4>(kx, sn, cs, a.style);
+            named_sync(1, kCons);
+            for (int i = tid; i < kPairs; i += kCons) {
+                const int hh = i / VL, c = i % VL;
+                float M = sm_redM[i];
+                for (int w = 1; w < kWays; ++w) M = fmaxf(M, sm_redM[w * kPairs + i]);
+                float Ls = 0.0f;
+                float4 A = make_float4(0.f, 0.f, 0.f, 0.f);
+                for (int w = 0; w < kWays; ++w) {
+                    const float mw = sm_redM[w * kPairs + i];
+                    const float f = mw == -INFINITY ? 0.0f : ex2_approx(mw - M);
+                    const float4 x = sm_red[w * kPairs + i];
+                    A = make_float4(fmaf(x.x, f, A.x), fmaf(x.y, f, A.y), fmaf(x.z, f, A.z), fmaf(x.w, f, A.w));
+                    Ls = fmaf(sm_redL[w * kPairs + i], f, Ls);
                 }
+                reinterpret_cast<float4 *>(out_s + hh * HDKV)[c] = f4scale(A, 1.0f / Ls);
+            }
+            if (tid == 0) *ticket = 0;  // ready for the next call or graph replay
+        }
+        if (kFused && lane < 8) {
+            // every other unit of this group has finished reading q: write it back rotated
 #pragma unroll
-                for (int i = 0; i < KF4; ++i) kh[sub + 8 * i] = kx[i];
-            }
-        }
-        if (t.n_act == 1) continue;
-
-        __threadfence();
-        for (int i = tid; i < GH * t.n_act; i += kCons) {
-            const int hh = i / t.n_act, j = i % t.n_act;
-            const size_t part = part0 + static_cast<size_t>(hh) * a.n_split + j;
-            const float2 ml = __ldcg(reinterpret_cast<const float2 *>(a.ws_ml) + part);
-            sm_pm[hh][j] = ml.x;
-            sm_pl[hh][j] = ml.y;
-        }
-        named_sync(1, kCons);
-        for (int hh = warp; hh < GH; hh += kNW) {
-            float M = -INFINITY;
-            for (int j = lane; j < t.n_act; j += 32) M = fmaxf(M, sm_pm[hh][j]);
+            for (int hh = 0; hh < GH; ++hh) {
+                if (hh % kNW != warp) continue;
+                float4 *qh = reinterpret_cast<float4 *>(a.q_io + (static_cast<size_t>(t.s) * a.nh + h0 + hh) * a.hd);
 #pragma unroll
-            for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-            float Ls = 0.0f;
-            for (int j = lane; j < t.n_act; j += 32) {
-                const float f = ex2_approx(sm_pm[hh][j] - M);
-                sm_pm[hh][j] = f;  // becomes the partial's weight
-                Ls = fmaf(sm_pl[hh][j], f, Ls);
+                for (int i = 0; i < KF4; ++i) qh[lane + 8 * i] = qr[hh][i];
             }
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) Ls += __shfl_xor_sync(0xffffffffu, Ls, o);
-            if (lane == 0) sm_L[hh] = Ls;
         }
-        named_sync(1, kCons);
-        constexpr int kPairs = GH * VL;
-        constexpr int kWays = kCons / kPairs > 0 ? kCons / kPairs : 1;
-        for (int i = tid; i < kPairs * kWays; i += kCons) {
-            const int pair = i % kPairs, way = i / kPairs;
-            const int hh = pair / VL, c = pair % VL;
-            const size_t ph = part0 + static_cast<size_t>(hh) * a.n_split;
-            float4 A = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 8
-            for (int j = way; j < t.n_act; j += kWays) {
-                const float f = sm_pm[hh][j];
-                const float4 x = __ldcg(reinterpret_cast<const float4 *>(a.ws_acc + (ph + j) * HDKV) + c);
-                A.x = fmaf(x.x, f, A.x);
-                A.y = fmaf(x.y, f, A.y);
-                A.z = fmaf(x.z, f, A.z);
-                A.w = fmaf(x.w, f, A.w);
-            }
-            sm_red[way * kPairs + pair] = A;
-        }
-        named_sync(1, kCons);
-        for (int i = tid; i < kPairs; i += kCons) {
-            const int hh = i / VL, c = i % VL;
-            float4 A = sm_red[i];
-            for (int w = 1; w < kWays; ++w) {
-                const float4 x = sm_red[w * kPairs + i];
-                A.x += x.x;
-                A.y += x.y;
-                A.z += x.z;
-                A.w += x.w;
-            }
-            reinterpret_cast<float4 *>(out_s + hh * HDKV)[c] = f4scale(A, 1.0f / sm_L[hh]);
-        }
-        if (tid == 0) *ticket = 0;  // ready for the next call or graph replay
     }
     if (!released) gdc_launch_dependents();
 }
@@ -713,7 +710,7 @@ int launch_impl(const DecodeArgs &d, const DecodeStepExtra *x, cudaStream_t s) {
     if (d.n_seq == 0) return MINF_OK;
     const Plan pl = plan_for(d.n_seq, d.nh, d.nk, d.hd_kv, d.cap);
     if (!d.ws || d.ws_bytes < pl.w.total || !aligned16(d.ws)) return MINF_ERR_WORKSPACE;
-    const long long units = static_cast<long long>(d.n_seq) * d.nk * pl.groups * pl.S + (x ? d.n_seq : 0);
+    const long long units = static_cast<long long>(d.n_seq) * d.nk * pl.groups * pl.S;
     if (units > 0x7fffffffLL) return MINF_ERR_UNSUPPORTED;
     const long long rows = d.row_off ? d.arena_rows : d.cap;
     if (rows <= 0) return MINF_ERR_ARG;
