@@ -121,18 +121,16 @@ size_t minf_attn_decode_workspace_bytes(int n_seq, int n_head, int n_kv_head, in
 }
 
 size_t minf_attn_prefill_workspace_bytes(int nt, int n_head, int n_kv_head, int hd_kv, int cap) {
-    (void)nt;
-    (void)n_head;
     (void)n_kv_head;
-    (void)hd_kv;
-    (void)cap;
-    return 0;  // the tensor-core prefill keeps its state in shared memory and TMEM
+    return prefill_workspace_bytes(nt, n_head, hd_kv, cap);
 }
 
 static int prefill(float *out, const float *q, const float *k_reg, const float *v_reg, int cap,
                    const int32_t *pos, int nt, int nh, int nk, int hd, int hd_kv, float scale,
-                   int32_t *err, cudaStream_t s) {
+                   void *ws, size_t ws_bytes, int32_t *err, cudaStream_t s) {
     PrefillArgs a;
+    a.ws = ws;
+    a.ws_bytes = ws_bytes;
     a.out = out;
     a.q = q;
     a.k_reg = k_reg;
@@ -202,14 +200,12 @@ int minf_gqa_attn_prefill(float *out, const float *q, const float *k_reg, const 
                           int cap, const int32_t *pos, int nt, int n_head, int n_kv_head, int hd,
                           int hd_kv, float scale, void *ws, size_t ws_bytes, int32_t *err,
                           minf_stream_t stream) {
-    (void)ws;
-    (void)ws_bytes;
     int st = check_attn(n_head, n_kv_head, hd, hd_kv);
     if (st != MINF_OK) return st;
     if (!ok_f(out) || !ok_f(q) || !ok_f(k_reg) || !ok_f(v_reg) || !pos || !err) return MINF_ERR_ARG;
     if (nt < 0 || cap <= 0) return MINF_ERR_ARG;
-    return prefill(out, q, k_reg, v_reg, cap, pos, nt, n_head, n_kv_head, hd, hd_kv, scale, err,
-                   cs(stream));
+    return prefill(out, q, k_reg, v_reg, cap, pos, nt, n_head, n_kv_head, hd, hd_kv, scale, ws,
+                   ws_bytes, err, cs(stream));
 }
 
 int minf_layer_attn_step(float *xn, const float *h, const float *gain, float eps, int n_embd,
@@ -225,10 +221,9 @@ int minf_layer_attn_step(float *xn, const float *h, const float *gain, float eps
         !err)
         return MINF_ERR_ARG;
     if (nt == 0) return MINF_OK;
-    if (nt == 1) {
-        const size_t need = decode_workspace_bytes(1, n_head, n_kv_head, hd_kv, cap);
-        if (!ws || ws_bytes < need) return MINF_ERR_WORKSPACE;
-    }
+    const size_t need = nt == 1 ? decode_workspace_bytes(1, n_head, n_kv_head, hd_kv, cap)
+                                : prefill_workspace_bytes(nt, n_head, hd_kv, cap);
+    if (need && (!ws || ws_bytes < need)) return MINF_ERR_WORKSPACE;
     cudaStream_t s = cs(stream);
     const float scale = 1.0f / sqrtf(static_cast<float>(hd));
     if (nt == 1 && fused_step_supported(n_head, n_kv_head, hd, hd_kv, n_embd) && aligned16(h) &&
@@ -247,7 +242,8 @@ int minf_layer_attn_step(float *xn, const float *h, const float *gain, float eps
     if (nt == 1)
         return decode(out, q, k_reg, v_reg, nullptr, nullptr, cap, pos, 1, n_head, n_kv_head, hd,
                       hd_kv, scale, ws, ws_bytes, err, s);
-    return prefill(out, q, k_reg, v_reg, cap, pos, nt, n_head, n_kv_head, hd, hd_kv, scale, err, s);
+    return prefill(out, q, k_reg, v_reg, cap, pos, nt, n_head, n_kv_head, hd, hd_kv, scale, ws, ws_bytes,
+                   err, s);
 }
 
 int minf_layer_attn_step_batched(float *xn, const float *h, const float *gain, float eps,

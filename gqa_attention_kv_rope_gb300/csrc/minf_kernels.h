@@ -65,8 +65,11 @@ struct PrefillArgs {
     int32_t *err;
     int nt, nh, nk, hd, hd_kv, cap;
     float scale;
+    void *ws;                 // key-chunk partials (prefill_workspace_bytes)
+    size_t ws_bytes;
 };
 
+size_t prefill_workspace_bytes(int nt, int nh, int hd_kv, int cap);
 int launch_prefill(const PrefillArgs &a, cudaStream_t s);
 
 size_t decode_workspace_bytes(int n_seq, int nh, int nk, int hd_kv, int max_cap);

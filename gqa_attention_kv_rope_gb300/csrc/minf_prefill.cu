@@ -5,9 +5,11 @@
 // mask matrix), with softmax(scale * q . k) weights on V.  §2.5 names the GPU shape: tile
 // the (query, key) matrix and apply the softmax online, block by block.
 //
-// Tiling.  A CTA owns one query head and 128 consecutive query tokens (the M = 128 rows of
-// the tensor-core tiles) and walks the keys of that head's kv head in tiles of 32, up to the
-// largest window among its tokens.  Per key tile:
+// Tiling.  A CTA owns one query head, 128 consecutive query tokens (the M = 128 rows of the
+// tensor-core tiles) and one chunk of the keys of that head's kv head, which it walks in tiles
+// of 32 up to the largest window among its tokens.  The chunks of a query tile run in separate
+// CTAs; each writes its rows' (max, sum, output) partials and the last chunk to arrive (an
+// atomic ticket) folds them, so a long causal window is spread over many SMs.  Per key tile:
 //   S  = Q K^T        tcgen05.mma kind::tf32, M=128 N=32 K=hd_kv, fp32 accumulator in TMEM
 //   softmax            CUDA cores: one thread per query row reads its S row from TMEM,
 //                      masks keys beyond its window, updates its running max and sum, and
@@ -129,7 +131,10 @@ struct PParams {
     const int32_t *pos;
     int32_t *err;
     int nt, nh, nk, hd, cap, W;
+    int n_qt, n_kc, kc_tiles;  // query tiles, key chunks per query tile, key tiles per chunk
     float scale_log2;
+    float *ws_o, *ws_ml;       // chunk partials: o as [.., d][row], (m, l) as [.., 2][row]
+    int *ws_ticket;            // one per (query tile, head)
 };
 
 // Round to the nearest TF32 value (10 explicit mantissa bits), ties away from zero.
@@ -167,8 +172,12 @@ __global__ void __launch_bounds__(kThreadsP, 1)
     Smem<HDKV> &sm = *reinterpret_cast<Smem<HDKV> *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int t0 = blockIdx.x * BM;
-    const int h = blockIdx.y;
+    // CTA -> (key chunk, head, query tile), the chunk slowest so the CTAs that have work are
+    // launched first (chunks past a tile's widest window leave at once)
+    const int kc = blockIdx.x / (a.nh * a.n_qt);
+    const int h = (blockIdx.x / a.n_qt) % a.nh;
+    const int qt = blockIdx.x % a.n_qt;
+    const int t0 = qt * BM;
     const int g = a.nh / a.nk;
     const int hk = h / g;
     volatile int *abort_flag = &sm.abort_flag;
@@ -184,24 +193,15 @@ __global__ void __launch_bounds__(kThreadsP, 1)
         sm.lmax = 0;
         mbar_init_fence();
     }
-    if (warp == kProducerWarp) {
-        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
-                         su32(&sm.tmem_base)),
-                     "r"(kTmemCols)
-                     : "memory");
-        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-    }
     // this row's window ("11 . Attention...", §3.2.4: vl = min(pos[t] + 1, nkv), nkv <= n_ctx)
     int L_t = 0;
     const int t = t0 + tid;
     if (tid < kSoftThreads && t < a.nt) {
         const int p = __ldg(a.pos + t);
         L_t = p < 0 ? 0 : (p + 1 < a.cap ? p + 1 : a.cap);
-        if ((p < 0 || p >= a.cap) && h == 0) flag_error(a.err, MINF_ERRBIT_ATTN_POS);
+        if ((p < 0 || p >= a.cap) && h == 0 && kc == 0) flag_error(a.err, MINF_ERRBIT_ATTN_POS);
     }
-    tc_fence_before();
     __syncthreads();
-    tc_fence_after();
     if (tid < kSoftThreads) {
         int mx = L_t;
 #pragma unroll
@@ -210,7 +210,21 @@ __global__ void __launch_bounds__(kThreadsP, 1)
     }
     __syncthreads();
     const int lmax = sm.lmax;
-    const int n_tiles = (lmax + BN - 1) / BN;
+    const int n_tiles_all = (lmax + BN - 1) / BN;
+    const int n_act = (n_tiles_all + a.kc_tiles - 1) / a.kc_tiles;  // chunks with keys for this tile
+    if (kc > 0 && kc >= n_act) return;  // nothing to do (chunk 0 always runs: it writes the output)
+    const int tile0 = kc * a.kc_tiles;
+    const int n_tiles = min(n_tiles_all - tile0, a.kc_tiles) > 0 ? min(n_tiles_all - tile0, a.kc_tiles) : 0;
+    if (warp == kProducerWarp) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         su32(&sm.tmem_base)),
+                     "r"(kTmemCols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
     const uint32_t tmem = sm.tmem_base;
     constexpr uint32_t kQBytes = BM * HDKV * 4, kKBytes = BN * HDKV * 4;
 
@@ -221,7 +235,8 @@ __global__ void __launch_bounds__(kThreadsP, 1)
             for (int c = 0; c < HDKV / 32; ++c) tma_load_2d(sm.qh[c], &tm_q, h * a.hd + 32 * c, t0, &sm.bar_q);
             mbar_expect_tx(&sm.bar_k, kKBytes);
 #pragma unroll
-            for (int c = 0; c < HDKV / 32; ++c) tma_load_2d(sm.kh[c], &tm_k, hk * HDKV + 32 * c, 0, &sm.bar_k);
+            for (int c = 0; c < HDKV / 32; ++c)
+                tma_load_2d(sm.kh[c], &tm_k, hk * HDKV + 32 * c, tile0 * BN, &sm.bar_k);
             for (int i = 0; i < n_tiles; ++i) {
                 // S = Q K^T once the softmax warps have split Q (first tile), K and V^T
                 if (!mbar_wait(&sm.bar_kv, i & 1, abort_flag, a.err)) break;
@@ -244,7 +259,7 @@ __global__ void __launch_bounds__(kThreadsP, 1)
                     mbar_expect_tx(&sm.bar_k, kKBytes);
 #pragma unroll
                     for (int c = 0; c < HDKV / 32; ++c)
-                        tma_load_2d(sm.kh[c], &tm_k, hk * HDKV + 32 * c, (i + 1) * BN, &sm.bar_k);
+                        tma_load_2d(sm.kh[c], &tm_k, hk * HDKV + 32 * c, (tile0 + i + 1) * BN, &sm.bar_k);
                 }
                 if (!mbar_wait(&sm.bar_p, i & 1, abort_flag, a.err)) break;
                 tc_fence_after();
@@ -274,7 +289,7 @@ __global__ void __launch_bounds__(kThreadsP, 1)
         if (n_tiles > 0 && mbar_wait(&sm.bar_q, 0, abort_flag, a.err))
             split_region(&sm.qh[0][0], &sm.ql[0][0], BM * HDKV / 4, tid);
         for (int i = 0; i < n_tiles; ++i) {
-            const int j0 = i * BN;
+            const int j0 = (tile0 + i) * BN;
             if (!mbar_wait(&sm.bar_k, i & 1, abort_flag, a.err)) break;
             split_region(&sm.kh[0][0], &sm.kl[0][0], BN * HDKV / 4, tid);
             {   // V tile -> V^T hi/lo (K-major, keys along K); keys past the widest window are zero
@@ -343,7 +358,46 @@ __global__ void __launch_bounds__(kThreadsP, 1)
             }
             tc_fence_before();
         }
-        if (t < a.nt && !*abort_flag) {
+        bool write_out = true;
+        if (n_act > 1) {
+            // more than one chunk of keys: publish this chunk's (m, l, o) per row; the last
+            // chunk of the (query tile, head) to arrive folds them (an atomic ticket, no wait)
+            const size_t blk = (static_cast<size_t>(qt) * a.nh + h) * a.n_kc;
+            float *po = a.ws_o + (blk + kc) * HDKV * BM;
+            float *pml = a.ws_ml + (blk + kc) * 2 * BM;
+#pragma unroll
+            for (int d = 0; d < HDKV; ++d) po[d * BM + tid] = o[d];
+            pml[tid] = m;
+            pml[BM + tid] = l;
+            named_sync(1, kSoftThreads);
+            if (tid == 0) {
+                int old;
+                asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], 1;"
+                             : "=r"(old)
+                             : "l"(a.ws_ticket + static_cast<size_t>(qt) * a.nh + h)
+                             : "memory");
+                sm.lmax = (old == n_act - 1) ? -1 : 0;  // reuse as the "last" flag
+            }
+            named_sync(1, kSoftThreads);
+            write_out = sm.lmax == -1;
+            if (write_out) {
+                for (int c = 0; c < n_act; ++c) {
+                    if (c == kc) continue;
+                    const float *qo = a.ws_o + (blk + c) * HDKV * BM;
+                    const float *qml = a.ws_ml + (blk + c) * 2 * BM;
+                    const float mc = __ldcg(qml + tid), lc = __ldcg(qml + BM + tid);
+                    const float mn = fmaxf(m, mc);
+                    const float fa = m == -INFINITY ? 0.0f : ex2_approx(m - mn);
+                    const float fb = mc == -INFINITY ? 0.0f : ex2_approx(mc - mn);
+#pragma unroll
+                    for (int d = 0; d < HDKV; ++d) o[d] = fmaf(o[d], fa, __ldcg(qo + d * BM + tid) * fb);
+                    l = fmaf(l, fa, lc * fb);
+                    m = mn;
+                }
+                if (tid == 0) a.ws_ticket[static_cast<size_t>(qt) * a.nh + h] = 0;  // ready for reuse
+            }
+        }
+        if (write_out && t < a.nt && !*abort_flag) {
             float4 *dst = reinterpret_cast<float4 *>(a.out + (static_cast<size_t>(t) * a.nh + h) * HDKV);
             const float inv = l > 0.0f ? 1.0f / l : 0.0f;
 #pragma unroll
@@ -368,6 +422,31 @@ __global__ void __launch_bounds__(kThreadsP, 1)
     }
 }
 
+struct PrefillPlan {
+    int n_qt, n_kc, kc_tiles;
+    size_t o_off, ml_off, ticket_off, total;
+};
+
+size_t align256p(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+// Key chunks: at least 128 keys each and at most 16 per query tile (so the launch never
+// depends on the positions and stays small for long regions).
+PrefillPlan prefill_plan(int nt, int nh, int hd_kv, int cap) {
+    PrefillPlan p;
+    p.n_qt = (nt + BM - 1) / BM;
+    long long kc_keys = (static_cast<long long>(cap) + 15) / 16;
+    kc_keys = ((kc_keys + BN - 1) / BN) * BN;
+    if (kc_keys < 128) kc_keys = 128;
+    p.kc_tiles = static_cast<int>(kc_keys / BN);
+    p.n_kc = static_cast<int>((cap + kc_keys - 1) / kc_keys);
+    const size_t parts = static_cast<size_t>(p.n_qt) * nh * p.n_kc;
+    p.o_off = 0;
+    p.ml_off = align256p(parts * hd_kv * BM * sizeof(float));
+    p.ticket_off = p.ml_off + align256p(parts * 2 * BM * sizeof(float));
+    p.total = p.ticket_off + align256p(static_cast<size_t>(p.n_qt) * nh * sizeof(int));
+    return p;
+}
+
 template <int HDKV>
 int launch_t(const PrefillArgs &pa, cudaStream_t s) {
     CUtensorMap tq, tk;
@@ -387,6 +466,15 @@ int launch_t(const PrefillArgs &pa, cudaStream_t s) {
     a.cap = pa.cap;
     a.W = pa.nk * HDKV;
     a.scale_log2 = pa.scale * kLog2e;
+    const PrefillPlan pl = prefill_plan(pa.nt, pa.nh, HDKV, pa.cap);
+    a.n_qt = pl.n_qt;
+    a.n_kc = pl.n_kc;
+    a.kc_tiles = pl.kc_tiles;
+    if (pl.n_kc > 1 && (!pa.ws || pa.ws_bytes < pl.total || !aligned16(pa.ws))) return MINF_ERR_WORKSPACE;
+    char *ws = static_cast<char *>(pa.ws);
+    a.ws_o = pl.n_kc > 1 ? reinterpret_cast<float *>(ws + pl.o_off) : nullptr;
+    a.ws_ml = pl.n_kc > 1 ? reinterpret_cast<float *>(ws + pl.ml_off) : nullptr;
+    a.ws_ticket = pl.n_kc > 1 ? reinterpret_cast<int *>(ws + pl.ticket_off) : nullptr;
     const size_t smem = sizeof(Smem<HDKV>) + 1024;
     static bool attr_set = false;
     if (!attr_set) {
@@ -395,16 +483,22 @@ int launch_t(const PrefillArgs &pa, cudaStream_t s) {
             return MINF_ERR_CUDA;
         attr_set = true;
     }
-    const dim3 grid((pa.nt + BM - 1) / BM, pa.nh);
-    prefill_kernel<HDKV><<<grid, kThreadsP, smem, s>>>(tq, tk, a);
+    const long long ctas = static_cast<long long>(pl.n_qt) * pa.nh * pl.n_kc;
+    if (ctas > 0x7fffffffLL) return MINF_ERR_UNSUPPORTED;
+    prefill_kernel<HDKV><<<static_cast<unsigned>(ctas), kThreadsP, smem, s>>>(tq, tk, a);
     return cudaPeekAtLastError() == cudaSuccess ? MINF_OK : MINF_ERR_CUDA;
 }
 
 }  // namespace
 
+size_t prefill_workspace_bytes(int nt, int nh, int hd_kv, int cap) {
+    if (nt <= 0 || nh <= 0 || hd_kv <= 0 || cap <= 0) return 0;
+    const PrefillPlan p = prefill_plan(nt, nh, hd_kv, cap);
+    return p.n_kc > 1 ? p.total : 0;
+}
+
 int launch_prefill(const PrefillArgs &pa, cudaStream_t s) {
     if (pa.nt == 0) return MINF_OK;
-    if (pa.nt > 65535 * BM || pa.nh > 65535) return MINF_ERR_UNSUPPORTED;
     if ((static_cast<long long>(pa.nh) * pa.hd) % 4 != 0) return MINF_ERR_UNSUPPORTED;
     if (pa.hd_kv == 64) return launch_t<64>(pa, s);
     if (pa.hd_kv == 128) return launch_t<128>(pa, s);

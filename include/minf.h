@@ -196,9 +196,13 @@ MINF_API int minf_gqa_attn_decode_static_ws(float *out, const float *q, const fl
  * (store before attention: the tokens' own rows must already be appended).
  * q: [nt, n_head, hd]; out: [nt, n_head*hd_kv].  Positions are arbitrary
  * (a prefill that continues an existing cache passes pos = n_past..).
- * The QK^T and PV products run on the tensor cores in TF32 with fp32
- * accumulation (outputs agree with an fp32 evaluation to about 1e-3 absolute);
- * max, exp and sums run in fp32.  ws may be NULL (no workspace is needed).
+ * The QK^T and PV products run on the tensor cores with split-precision TF32
+ * operands (hi + lo halves, three MMAs per product) and fp32 accumulation, which
+ * matches an fp32 evaluation to a few 1e-6; max, exp and sums run in fp32.
+ * The keys of a query tile are cut into chunks processed by separate CTAs whose
+ * partials are folded at the end: ws must hold minf_attn_prefill_workspace_bytes
+ * (zero-filled before its first use; every call leaves it zeroed; concurrent
+ * calls must not share it); it may be NULL when that size is 0.
  * Device errors: MINF_ERRBIT_ATTN_POS, MINF_ERRBIT_TIMEOUT.
  * Errors: as minf_gqa_attn_decode.
  */
@@ -207,7 +211,8 @@ MINF_API int minf_gqa_attn_prefill(float *out, const float *q, const float *k_re
                           int hd_kv, float scale, void *ws, size_t ws_bytes, int32_t *err,
                           minf_stream_t stream);
 
-/* Workspace bytes minf_gqa_attn_prefill needs for nt tokens (0 if none). */
+/* Workspace bytes minf_gqa_attn_prefill (and a layer step with nt > 1) needs for
+ * nt tokens over regions of cap rows (0 if none). */
 MINF_API size_t minf_attn_prefill_workspace_bytes(int nt, int n_head, int n_kv_head, int hd_kv, int cap);
 
 /*
@@ -218,8 +223,8 @@ MINF_API size_t minf_attn_prefill_workspace_bytes(int nt, int n_head, int n_kv_h
  * = attention with scale 1/sqrt(hd) ([P1] §2.4).  nt == 1 runs the split-KV
  * decode path (a single launch for the supported geometries), nt > 1 the
  * tensor-core prefill path.  ws/ws_bytes: for nt == 1 at least
- * minf_attn_decode_workspace_bytes(1, n_head, n_kv_head, hd_kv, cap); unused
- * (may be NULL) for nt > 1.
+ * minf_attn_decode_workspace_bytes(1, n_head, n_kv_head, hd_kv, cap), for nt > 1
+ * at least minf_attn_prefill_workspace_bytes(nt, n_head, n_kv_head, hd_kv, cap).
  * Device errors: any of the bits above.
  */
 MINF_API int minf_layer_attn_step(float *xn, const float *h, const float *gain, float eps, int n_embd,

@@ -270,7 +270,7 @@ def test_layer_step_prefill_then_graph_replayed_decode(m, orc):
     Kd = torch.zeros(cap, g.row_width, device="cuda")
     Vd = torch.zeros(cap, g.row_width, device="cuda")
     err = err_word()
-    ws = m.kv.decode_workspace(n_prompt, g.n_head, g.n_kv_head, g.hd_kv, cap)
+    ws = m.kv.prefill_workspace(n_prompt, g.n_head, g.n_kv_head, g.hd_kv, cap)
     d = {k: dev(v[:n_prompt]) for k, v in inp.items() if k != "gain"}
     gain = dev(inp["gain"])
     xn = torch.empty_like(d["h"])

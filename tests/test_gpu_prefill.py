@@ -33,9 +33,9 @@ def run_prefill(m, q, K, V, pos, nh, nk, hd, hdkv):
     out = torch.full((nt, nh * hdkv), float("nan"), device="cuda")
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
     scale = float(np.float32(1.0) / np.sqrt(np.float32(hd)))
+    ws = m.kv.prefill_workspace(nt, nh, nk, hdkv, K.shape[0])
     m.minf_gqa_attn_prefill(out, q.contiguous().cuda(), K.cuda(), V.cuda(),
-                            torch.as_tensor(np.asarray(pos, np.int32)).cuda(), nh, nk, hd, hdkv, scale,
-                            torch.zeros(256, dtype=torch.uint8, device="cuda"), err)
+                            torch.as_tensor(np.asarray(pos, np.int32)).cuda(), nh, nk, hd, hdkv, scale, ws, err)
     torch.cuda.synchronize()
     return out.cpu().numpy(), int(err.item()), scale
 
@@ -82,6 +82,20 @@ def test_prefill_continues_an_existing_cache(m, orc):
           "delta prefill")
 
 
+def test_prefill_repeated_calls_reuse_the_workspace(m, orc):
+    """Long windows split over several key chunks; back-to-back calls share one workspace."""
+    nh, nk, hd, cap = 16, 8, 128, 2048
+    K = rnd((cap, nk * hd), 11)
+    V = rnd((cap, nk * hd), 12)
+    for i, nt in enumerate((700, 1500)):
+        q = rnd((nt, nh, hd), 13 + i)
+        pos = np.arange(cap - nt, cap, dtype=np.int32)  # continue a long cache: windows up to 2048
+        got, err, scale = run_prefill(m, q, K, V, pos, nh, nk, hd, hd)
+        assert err == 0
+        check(got, orc.gqa_attn(q.numpy(), K.numpy(), V.numpy(), pos, nh, nk, hd, hd, scale=scale, n_threads=8),
+              f"long-window prefill {nt}")
+
+
 def test_prefill_scattered_positions_and_bad_ones(m, orc):
     nh, nk, hd, cap = 8, 2, 64, 150
     K = rnd((cap, nk * hd), 8)
@@ -110,8 +124,9 @@ def test_prefill_layer_step_matches_oracle(m, orc):
     xn = torch.empty_like(d["h"])
     out = torch.empty(nt, g.out_width, device="cuda")
     pos = torch.arange(nt, dtype=torch.int32, device="cuda")
+    ws = m.kv.prefill_workspace(nt, g.n_head, g.n_kv_head, g.hd_kv, cap)
     m.minf_layer_attn_step(xn, d["h"], d["gain"], g.eps, d["q"], d["k"], d["v"], pos, K, V, g.n_head, g.n_kv_head,
-                           g.hd, g.hd_kv, g.theta, 1.0, 0, out, None, err)
+                           g.hd, g.hd_kv, g.theta, 1.0, 0, out, ws, err)
     torch.cuda.synchronize()
     q, k = x["q"].numpy().copy(), x["k"].numpy().copy()
     Ko = np.zeros((cap, g.row_width), np.float32)
