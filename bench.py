@@ -546,6 +546,40 @@ def run_batched(m, torch, wl, dev, steps):
     return res
 
 
+def run_elementwise(m, torch, dev, reps=20):
+    """HBM throughput of the stand-alone RMSNorm (4096 x 1024 rows, gains) and SiLU*mul
+    (64 Mi elements) kernels, L2 flushed before every timed launch."""
+    flush = torch.empty(2 * L2_BYTES // 4, device=dev)
+    stream = torch.cuda.current_stream()
+    x = torch.randn(4096, 1024, device=dev)
+    w = torch.rand(1024, device=dev) + 0.5
+    y = torch.empty_like(x)
+    n = 64 << 20
+    g = torch.randn(n, device=dev)
+    u = torch.randn(n, device=dev)
+    o = torch.empty_like(g)
+
+    def timed(fn):
+        fn()
+        ts = []
+        for _ in range(reps):
+            flush_l2(flush)
+            a, b = Timer(torch, stream).pair()
+            a.record(stream)
+            fn()
+            b.record(stream)
+            torch.cuda.synchronize()
+            ts.append(a.elapsed_time(b))
+        return statistics.median(ts)
+
+    ms_rms = timed(lambda: m.binding.minf_rms_norm(y, x, w, 1e-6))
+    ms_silu = timed(lambda: m.binding.minf_silu_mul(o, g, u))
+    res = {"rms_norm_4096x1024_gbs": round((2 * x.numel() + w.numel()) * 4 / (ms_rms * 1e-3) / 1e9, 1),
+           "silu_mul_64Mi_gbs": round(3 * n * 4 / (ms_silu * 1e-3) / 1e9, 1)}
+    del flush, x, y, g, u, o
+    return res
+
+
 # ----------------------------------------------------------------------------- CPU oracle
 def oracle_sample(budget_s: float, host_arrays=None):
     """The oracle (as it stands) on a bounded sample of the headline workload: whole layer
@@ -665,6 +699,7 @@ def main(argv=None):
         secondary["prefill_layer_us"] = layer_us
         secondary["decode_loop"] = run_decode_loop(m, torch, wl, dev)
         secondary["batched_decode"] = run_batched(m, torch, wl, dev, max(3, args.steps // 4))
+        secondary["elementwise"] = run_elementwise(m, torch, dev)
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = oracle_sample(args.cpu_seconds)
