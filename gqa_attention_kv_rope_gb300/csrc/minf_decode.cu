@@ -10,15 +10,20 @@
 // from HBM once for all those heads.  The split count S is fixed on the host from the
 // sequence count and max_cap (never from pos); each launch reads the window length from
 // device memory and cuts it into at most S runs of whole pipeline stages.  The grid is
-// persistent -- one CTA per SM walks units u = blockIdx.x, +gridDim.x, ... -- so the shape
-// never depends on pos and a captured CUDA graph serves every position.
+// persistent -- one CTA per SM takes unit blockIdx.x, then further units from a counter in
+// the workspace (a batch is ordered longest sequence first) -- so the shape never depends on
+// pos and a captured CUDA graph serves every position.
 //
 // Streaming.  Warp 8 is the producer: one lane issues TMA tensor copies of K and V tiles
 // (R rows x hd_kv, 64 KB per stage) into a 3-stage ring of shared memory, running ahead
-// across units, gated by per-stage full/empty mbarriers.  Warps 0-7 consume: each takes an
-// 8-row sub-tile of the stage; 8 lanes share a K row for the dot products (three butterfly
-// steps) and each lane owns a float4 of the output for the V pass; each warp keeps its own
-// running (max, sum, acc) in the log2 domain, folded in shared memory at the end of a unit.
+// across units, gated by per-stage full/empty mbarriers; with each slot it publishes the
+// slot's (unit, stage), so the consumers follow the units it drew.  Warps 0-7 consume: each
+// takes an 8-row sub-tile of the stage; 8 lanes share a K row for the dot products (three
+// butterfly steps) and each lane owns a float4 of the output for the V pass; each warp keeps
+// its own running (max, sum, acc) in the log2 domain, folded in shared memory at the end of
+// a unit.  The consumer warps synchronise on an mbarrier rather than a named barrier, so
+// that, like every other wait here, the wait is bounded.  Warp 9 (the utility warp) zeroes
+// the outputs of empty windows and flags out-of-range positions.
 //
 // Merge.  A unit writes its partial (m, l, acc) to the workspace; the last unit of a
 // (sequence, kv group) to arrive -- an atomic ticket, no spinning -- folds all partials in
@@ -29,11 +34,12 @@
 // the rest of the layer's attention stage: each unit rotates its q heads in registers
 // (RoPE, the same rounding as the standalone kernel), the unit whose run ends at row pos
 // rotates k, writes it back, appends the K/V row to the region and uses it from shared
-// memory, a utility warp computes the RMSNorm rows, and the last unit of a group writes the
-// rotated q back.  The loads of q, k and v are issued before anything that waits on the
-// position, so a unit's prologue costs one memory round trip.  With programmatic stream serialization the producer starts streaming cached rows
-// (which no preceding kernel writes) before griddepcontrol.wait; everything the preceding
-// kernel may produce -- q, k, v, h, the workspace, the outputs -- is touched only after it.
+// memory, the utility warp computes the RMSNorm rows, and the last unit of a group writes
+// the rotated q back.  The loads of q, k and v are issued before anything that waits on the
+// position, so a unit's prologue costs one memory round trip.  With programmatic stream
+// serialization the producer starts streaming cached rows (which no preceding kernel
+// writes) before griddepcontrol.wait; everything the preceding kernel may produce -- q, k,
+// v, h, the workspace and its counters, the outputs -- is touched only after it.
 #include <cudaTypedefs.h>
 
 #include <cmath>
@@ -47,16 +53,18 @@ namespace minf {
 namespace {
 
 constexpr int kNW = 8;                  // consumer warps
-constexpr int kCons = kNW * 32;         // consumer threads (named barrier 1)
+constexpr int kCons = kNW * 32;         // consumer threads
 constexpr int kProducer = kNW;          // warp 8: TMA producer
-constexpr int kUtility = kNW + 1;       // warp 9: RMSNorm rows of the fused step
+constexpr int kUtility = kNW + 1;       // warp 9: RMSNorm rows, empty windows, position flags
 constexpr int kThreads = kCons + 64;    // + producer + utility (same register budget as 9 warps)
 constexpr int kSub = 8;                 // rows per warp sub-tile
 constexpr int kNST = 3;                 // pipeline stages
 constexpr int kStageBytes = 64 * 1024;  // K + V tile of one stage
 constexpr int kGridTarget = 152;        // GB300: one persistent CTA per SM
 constexpr int kMaxSplit = 64;           // partials per (sequence, kv group)
-constexpr int kMaxRows = 1024;          // longest unit when pairs outnumber the SMs
+constexpr int kMaxRows = 4096;          // longest unit when pairs outnumber the SMs
+constexpr int kBatchMinRows = 1024;     // shortest unit worth a split when pairs outnumber the SMs
+constexpr int kMaxSort = 256;           // batches up to this many sequences are visited longest first
 
 template <int HDKV>
 struct Cfg {
@@ -67,7 +75,7 @@ struct Cfg {
 inline int stage_rows(int hd_kv) { return kStageBytes / (2 * hd_kv * 4); }
 
 struct WsLayout {
-    size_t ml_off, acc_off, ticket_off, total;
+    size_t ml_off, acc_off, ticket_off, ctr_off, total;
 };
 
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
@@ -78,7 +86,8 @@ WsLayout ws_layout(int n_seq, int nh, int pairs_per_seq, int hd_kv, int splits) 
     w.ml_off = 0;
     w.acc_off = align256(parts * 2 * sizeof(float));
     w.ticket_off = w.acc_off + align256(parts * hd_kv * sizeof(float));
-    w.total = w.ticket_off + align256(static_cast<size_t>(n_seq) * pairs_per_seq * sizeof(int));
+    w.ctr_off = w.ticket_off + align256(static_cast<size_t>(n_seq) * pairs_per_seq * sizeof(int));
+    w.total = w.ctr_off + 256;
     return w;
 }
 
@@ -91,8 +100,9 @@ int heads_per_cta(int g, int hd_kv) {
     return g;
 }
 
-// Splits per (sequence, kv group): fill the SMs once when the pairs alone cannot, otherwise
-// cut long windows into units of at most kMaxRows so the persistent CTAs stay balanced.
+// Splits per (sequence, kv group): fill the SMs once when the pairs alone cannot; otherwise
+// (a batch) cut only long windows, into units of at most kMaxRows, since the persistent CTAs
+// take units from a shared counter, longest first.
 int choose_splits(long long pairs, int hd_kv, int max_cap) {
     const long long R = stage_rows(hd_kv);
     long long s = pairs < kGridTarget ? kGridTarget / pairs
@@ -111,10 +121,13 @@ struct KParams {
     const int32_t *caps;
     const int32_t *pos;
     int cap, n_seq, nh, nk, hd, n_split, groups;  // groups = g / GH
+    int min_rows;          // shortest unit (rows)
+    int sorted;            // visit sequences longest first
     float scale_log2;
     int32_t *err;
     float *ws_ml, *ws_acc;
     int *ws_ticket;
+    int *ws_ctr, *ws_done;  // dynamic unit counter and the count of finished producers
     // fused layer step only
     float *q_io, *k_io;    // rotated in place (q_io == q)
     float *k_reg, *v_reg;  // the new row is written here
@@ -186,31 +199,57 @@ __device__ __forceinline__ void rope_angles(float (&sn)[2 * KF4], float (&cs)[2 
     }
 }
 
-// The unit u decodes to (sequence, pair, split) and, from the sequence's position, to the
-// run of rows it owns.  Producer and consumers derive it identically.
 struct Unit {
     int s, y, j, p, cap_s, L, n_act, r_begin, r_end;
     long long base;
 };
 
+// Window of sequence s: rows [0, L) with L = min(pos + 1, cap); empty for a negative position.
+__device__ __forceinline__ int window_of(const KParams &a, int s) {
+    const int p = __ldg(a.pos + s);
+    const int cap_s = a.caps ? __ldg(a.caps + s) : a.cap;
+    return p < 0 ? 0 : (p + 1 < cap_s ? p + 1 : cap_s);
+}
+
+// The unit u decodes to (sequence, pair, split) and, from the sequence's position, to the
+// run of rows it owns.  Units [0, grid) are the CTAs' first units; in a batch, where the units
+// outnumber the CTAs, the rest are drawn from the counter, sequences longest first (`order`).
+// Split j of a window of L rows covers rows [j*T, (j+1)*T) with T the smallest multiple of the
+// stage height (and at least min_rows) that cuts L into at most n_split runs; the n_act
+// active splits fill partial slots [0, n_act).  Producer and consumers derive the unit
+// identically.
 template <int R>
-__device__ __forceinline__ Unit unit_of(const KParams &a, int u) {
+__device__ __forceinline__ Unit unit_of(const KParams &a, int u, const int *order) {
     Unit t;
     const int P = a.nk * a.groups;
     t.j = u % a.n_split;
     t.y = (u / a.n_split) % P;
-    t.s = u / (a.n_split * P);
+    const int rank = u / (a.n_split * P);
+    t.s = order ? order[rank] : rank;
     t.p = __ldg(a.pos + t.s);
     t.cap_s = a.caps ? __ldg(a.caps + t.s) : a.cap;
     t.L = t.p < 0 ? 0 : (t.p + 1 < t.cap_s ? t.p + 1 : t.cap_s);
     int T = (t.L + a.n_split - 1) / a.n_split;
     T = ((T + R - 1) / R) * R;
-    if (T < R) T = R;
+    if (T < a.min_rows) T = a.min_rows;
     t.n_act = t.L > 0 ? (t.L + T - 1) / T : 0;
     t.r_begin = t.j * T;
-    t.r_end = t.r_begin + T < t.L ? t.r_begin + T : t.L;
+    t.r_end = t.j < t.n_act ? (t.r_begin + T < t.L ? t.r_begin + T : t.L) : t.r_begin;
     t.base = a.row_off ? __ldg(a.row_off + t.s) : 0;
     return t;
+}
+
+__device__ __forceinline__ bool unit_active(const Unit &t) { return t.r_end > t.r_begin; }
+
+// Barrier of the consumer warps, on an mbarrier so that its wait is bounded like every other
+// wait in the kernel (one elected arrival per warp; release/acquire order the shared memory).
+__device__ __forceinline__ void cons_sync(unsigned long long *bar, uint32_t &phase, volatile int *abort_flag,
+                                          int32_t *err) {
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
+    mbar_wait(bar, phase, abort_flag, err);
+    phase ^= 1u;
+    __syncwarp();
 }
 
 template <int HDKV, int GH, bool kFused>
@@ -226,7 +265,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     extern __shared__ unsigned char smem_raw[];
     // 1024-aligned ring, derived from the shared array itself so loads stay in the shared space
     float *ring = reinterpret_cast<float *>(smem_raw + ((1024u - (su32(smem_raw) & 1023u)) & 1023u));
-    __shared__ unsigned long long full[kNST], empty[kNST];
+    __shared__ unsigned long long full[kNST], empty[kNST], meta_full[kNST], cons_bar;
+    __shared__ int2 sm_meta[kNST];  // (unit, stage) of each ring slot; unit < 0 ends the stream
+    __shared__ int sm_order[kMaxSort];
     __shared__ float sm_m[kNW][GH], sm_l[kNW][GH];
     __shared__ float4 sm_acc[kNW][GH][VL];
     __shared__ float4 sm_red[kCons];
@@ -244,9 +285,26 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int i = 0; i < kNST; ++i) {
             mbar_init(&full[i], 1);
             mbar_init(&empty[i], kNW);
+            mbar_init(&meta_full[i], 1);
         }
+        mbar_init(&cons_bar, kNW);
         sm_abort = 0;
         mbar_init_fence();
+    }
+    // A batch is visited longest sequence first (positions are not written by a preceding
+    // kernel, so this runs before the dependency wait): rank = number of longer windows.
+    const int *order = nullptr;
+    if (a.sorted) {
+        for (int s = tid; s < a.n_seq; s += blockDim.x) {
+            const int Ls = window_of(a, s);
+            int rank = 0;
+            for (int o = 0; o < a.n_seq; ++o) {
+                const int Lo = window_of(a, o);
+                rank += (Lo > Ls) || (Lo == Ls && o < s);
+            }
+            sm_order[rank] = s;
+        }
+        order = sm_order;
     }
     __syncthreads();
 
@@ -278,35 +336,71 @@ __global__ void __launch_bounds__(kThreads, 1)
                                                                 v.z * scale * g.z, v.w * scale * g.w);
             }
         }
-        return;  // writes only this kernel's own output: nothing a dependent launch may prefetch
+        // Outputs and error bits that belong to whole sequences: a sequence with an empty
+        // window has no unit, and its output is defined as zero.
+        for (int s = blockIdx.x; s < a.n_seq; s += gridDim.x) {
+            const int p = __ldg(a.pos + s);
+            const int cap_s = a.caps ? __ldg(a.caps + s) : a.cap;
+            if (lane == 0 && (p < 0 || p >= cap_s)) {
+                int bits = MINF_ERRBIT_ATTN_POS;
+                if (kFused) bits |= MINF_ERRBIT_STORE_POS | (p < 0 ? MINF_ERRBIT_ROPE_POS : 0);
+                flag_error(a.err, bits);
+            }
+            if (p < 0)
+                for (int i = lane; i < a.nh * HDKV; i += 32) a.out[static_cast<size_t>(s) * a.nh * HDKV + i] = 0.0f;
+        }
+        return;  // writes only this kernel's own outputs: nothing a dependent launch may prefetch
     }
     if (warp == kProducer) {
         // ---------------------------------------------------------------- producer
         if (lane == 0) {
             uint32_t it = 0;
             bool waited = false;
-            for (int u = blockIdx.x; u < n_units && !*abort_flag; u += gridDim.x) {
-                const Unit t = unit_of<R>(a, u);
-                if (t.L == 0 || t.j >= t.n_act) continue;
-                const int hk = t.y / a.groups;
-                const int n_st = (t.r_end - t.r_begin + R - 1) / R;
-                for (int st = 0; st < n_st; ++st, ++it) {
-                    const int slot = it % kNST;
-                    if (it >= kNST) {
-                        if (!waited) {  // cached rows need no wait; reusing the ring does
-                            gdc_wait();
-                            waited = true;
+            int u = blockIdx.x;  // the first unit is this CTA's own; the rest come from a counter
+            while (u < n_units && !*abort_flag) {
+                const Unit t = unit_of<R>(a, u, order);
+                if (unit_active(t)) {
+                    const int hk = t.y / a.groups;
+                    const int n_st = (t.r_end - t.r_begin + R - 1) / R;
+                    for (int st = 0; st < n_st && !*abort_flag; ++st, ++it) {
+                        const int slot = it % kNST;
+                        if (it >= kNST) {
+                            if (!waited) {  // cached rows need no wait; reusing the ring does
+                                gdc_wait();
+                                waited = true;
+                            }
+                            if (!mbar_wait(&empty[slot], ((it / kNST) & 1) ^ 1, abort_flag, a.err)) break;
                         }
-                        if (!mbar_wait(&empty[slot], ((it / kNST) & 1) ^ 1, abort_flag, a.err)) break;
+                        sm_meta[slot] = make_int2(u, st);
+                        mbar_arrive(&meta_full[slot]);  // publishes the slot's unit to the consumers
+                        float *kt = ring + static_cast<size_t>(slot) * (2 * R * HDKV);
+                        const int row = static_cast<int>(t.base) + t.r_begin + st * R;
+                        mbar_expect_tx(&full[slot], 2 * kTileBytes);
+                        tma_load_2d(kt, &tmK, hk * HDKV, row, &full[slot]);
+                        tma_load_2d(kt + R * HDKV, &tmV, hk * HDKV, row, &full[slot]);
                     }
-                    float *kt = ring + static_cast<size_t>(slot) * (2 * R * HDKV);
-                    const int row = static_cast<int>(t.base) + t.r_begin + st * R;
-                    mbar_expect_tx(&full[slot], 2 * kTileBytes);
-                    tma_load_2d(kt, &tmK, hk * HDKV, row, &full[slot]);
-                    tma_load_2d(kt + R * HDKV, &tmV, hk * HDKV, row, &full[slot]);
                 }
+                if (!waited) {  // the unit counter lives in the workspace a preceding launch may use
+                    gdc_wait();
+                    waited = true;
+                }
+                u = gridDim.x + atomicAdd(a.ws_ctr, 1);
             }
             if (!waited) gdc_wait();
+            // end of the stream for this CTA's consumers
+            const int slot = it % kNST;
+            if (it < kNST || mbar_wait(&empty[slot], ((it / kNST) & 1) ^ 1, abort_flag, a.err)) {
+                sm_meta[slot] = make_int2(-1, 0);
+                mbar_arrive(&meta_full[slot]);
+            }
+            // the last producer to finish resets the counters for the next call or graph replay
+            // (the fences order every producer's draws before its count, and the reset after)
+            __threadfence();
+            if (atomicAdd(a.ws_done, 1) == static_cast<int>(gridDim.x) - 1) {
+                __threadfence();
+                *a.ws_ctr = 0;
+                *a.ws_done = 0;
+            }
             if (*abort_flag) {
                 // let copies already issued land before the CTA's shared memory goes away
                 for (uint32_t k = it > kNST ? it - kNST : 0; k < it; ++k)
@@ -321,29 +415,40 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 
     // -------------------------------------------------------------------- consumers
-    gdc_wait();
     // A dependent launch may start streaming cached rows before its own wait, so release it only
-    // once every row this CTA appends is in memory: early when the CTA owns at most one unit
-    // (after that unit's append), otherwise when the CTA is done.
-    int my_units = 0;
-    for (int u = blockIdx.x; u < n_units; u += gridDim.x) ++my_units;
-    const bool early = my_units <= 1;
+    // once every row this CTA appends is in memory.  The run that ends at the window's last row
+    // appends; when every unit is a first unit, a CTA releases right after its append (or at
+    // once), otherwise when it is done.
+    const bool early = n_units <= static_cast<int>(gridDim.x);
     bool released = false;
-    if (my_units == 0) {
-        gdc_launch_dependents();
-        released = true;
-    }
     const int r4 = lane >> 3, sub = lane & 7;
     const int vrow = lane / VL, vcol = lane % VL;
     const float sl = a.scale_log2;
-    uint32_t it = 0;
-
-    for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
-        const Unit t = unit_of<R>(a, u);
+    uint32_t cphase = 0;
+    uint32_t it = 0;  // ring stage counter, in step with the producer's
+    // The first unit is this CTA's own and needs no word from the producer; its position is
+    // read before the dependency wait (no preceding kernel writes positions).
+    Unit t = unit_of<R>(a, blockIdx.x, order);
+    bool have = unit_active(t);
+    gdc_wait();
+    if (early && !(kFused && have && t.r_end == t.L)) {
+        gdc_launch_dependents();  // this CTA appends no row
+        released = true;
+    }
+    while (true) {
+        if (!have) {
+            // the producer publishes the unit it drew with the unit's first stage
+            const int slot = it % kNST;
+            if (!mbar_wait(&meta_full[slot], (it / kNST) & 1, abort_flag, a.err)) break;
+            const int u = sm_meta[slot].x;
+            if (u < 0) break;
+            t = unit_of<R>(a, u, order);
+        }
+        have = false;
+        // -------------------------------------------------------------- start of a unit
         const int hk = t.y / a.groups;
         const int h0 = hk * (a.nh / a.nk) + (t.y % a.groups) * GH;  // first query head
-        // The inputs do not depend on the position: issue their loads before anything that
-        // does, so they overlap the position load instead of following it.
+        const int n_st = (t.r_end - t.r_begin + R - 1) / R;
         float4 qr[GH][KF4];
 #pragma unroll
         for (int hh = 0; hh < GH; ++hh) {
@@ -352,64 +457,51 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int i = 0; i < KF4; ++i) qr[hh][i] = qh[sub + 8 * i];
         }
-        float4 kx[KF4], vx[KF4];
-        if (kFused && warp == 0 && r4 == 0) {
-            const float4 *kh =
-                reinterpret_cast<const float4 *>(a.k_io + (static_cast<size_t>(t.s) * a.nk + hk) * HDKV);
-            const float4 *vh = reinterpret_cast<const float4 *>(a.v_new + static_cast<size_t>(t.s) * W + hk * HDKV);
-#pragma unroll
-            for (int i = 0; i < KF4; ++i) {
-                kx[i] = kh[sub + 8 * i];
-                vx[i] = vh[sub + 8 * i];
-            }
-        }
-        if (t.j == 0 && t.y == 0 && tid == 0) {
-            int bits = 0;
-            if (t.p < 0 || t.p >= t.cap_s) bits |= MINF_ERRBIT_ATTN_POS;
-            if (kFused && (t.p < 0 || t.p >= t.cap_s)) bits |= MINF_ERRBIT_STORE_POS;
-            if (kFused && t.p < 0) bits |= MINF_ERRBIT_ROPE_POS;
-            if (bits) flag_error(a.err, bits);
-        }
-        float *out_s = a.out + (static_cast<size_t>(t.s) * a.nh + h0) * HDKV;
-        if (t.L == 0 || t.j >= t.n_act) {
-            if (t.L == 0 && t.j == 0)  // empty window: defined as a zero output
-                for (int i = tid; i < GH * HDKV; i += kCons) out_s[i] = 0.0f;
-            if (early && !released) {
-                gdc_launch_dependents();
-                released = true;
-            }
-            continue;
-        }
         // The unit whose run ends at the window's last row owns k: it rotates it, writes it back
-        // and, when the row fits the region, appends the new K/V row (no other unit reads k).
+        // and, when the row fits the region, appends the new K/V row and puts it, from shared
+        // memory, in place of what its tile copy read (no other unit reads k).
         const bool k_writer = kFused && t.r_end == t.L;
-        const bool own_new = k_writer && t.p < t.cap_s;
-        const int pnew = own_new ? t.p : -1;
-        const float *Kg = a.k_reg + t.base * W + hk * HDKV;  // fused path only: the new row
-        const float *Vg = a.v_reg + t.base * W + hk * HDKV;
+        const int pnew = k_writer && t.p < t.cap_s ? t.p : -1;
         if (kFused) {
             float sn[2 * KF4], cs[2 * KF4];
             rope_angles<KF4>(sn, cs, static_cast<float>(t.p), a.tab, a.style, sub, r4);
 #pragma unroll
             for (int hh = 0; hh < GH; ++hh) rope_lane<KF4>(qr[hh], sn, cs, a.style);
             if (k_writer && warp == 0 && r4 == 0) {
-                rope_lane<KF4>(kx, sn, cs, a.style);
                 float4 *kh = reinterpret_cast<float4 *>(a.k_io + (static_cast<size_t>(t.s) * a.nk + hk) * HDKV);
+                const float4 *vh = reinterpret_cast<const float4 *>(a.v_new + static_cast<size_t>(t.s) * W + hk * HDKV);
+                float4 kx[KF4], vx[KF4];
+#pragma unroll
+                for (int i = 0; i < KF4; ++i) {
+                    kx[i] = kh[sub + 8 * i];
+                    vx[i] = vh[sub + 8 * i];
+                }
+                rope_lane<KF4>(kx, sn, cs, a.style);
 #pragma unroll
                 for (int i = 0; i < KF4; ++i) kh[sub + 8 * i] = kx[i];
-                if (own_new) {
-                    float4 *kdst = reinterpret_cast<float4 *>(const_cast<float *>(Kg) + static_cast<size_t>(t.p) * W);
-                    float4 *vdst = reinterpret_cast<float4 *>(const_cast<float *>(Vg) + static_cast<size_t>(t.p) * W);
+                if (pnew >= 0) {
+                    float *Kg = a.k_reg + (t.base + t.p) * W + hk * HDKV;
+                    float *Vg = a.v_reg + (t.base + t.p) * W + hk * HDKV;
 #pragma unroll
                     for (int i = 0; i < KF4; ++i) {
+                        // staged for the same lanes, which patch the row's stage when it arrives
                         reinterpret_cast<float4 *>(sm_knew)[sub + 8 * i] = kx[i];
                         reinterpret_cast<float4 *>(sm_vnew)[sub + 8 * i] = vx[i];
-                        kdst[sub + 8 * i] = kx[i];
-                        vdst[sub + 8 * i] = vx[i];
+                        reinterpret_cast<float4 *>(Kg)[sub + 8 * i] = kx[i];
+                        reinterpret_cast<float4 *>(Vg)[sub + 8 * i] = vx[i];
                     }
                 }
             }
-            named_sync(1, kCons);  // the staged row is visible to every consumer warp
+            if (early && !released) {  // this first unit is the appending one
+                // the appended row is in memory before the dependent launch is released; one
+                // thread's trigger releases the CTA, so the warp that wrote the row triggers
+                if (warp == 0) {
+                    if (pnew >= 0) __threadfence();
+                    __syncwarp();
+                    if (lane == 0) gdc_launch_dependents();
+                }
+                released = true;
+            }
         }
         float m[GH], l[GH];
         float4 acc[GH];
@@ -420,13 +512,30 @@ __global__ void __launch_bounds__(kThreads, 1)
             acc[hh] = make_float4(0.f, 0.f, 0.f, 0.f);
         }
 
-        const int n_st = (t.r_end - t.r_begin + R - 1) / R;
+        // -------------------------------------------------------------- the unit's stages
         for (int st = 0; st < n_st; ++st, ++it) {
             const int slot = it % kNST;
             mbar_wait(&full[slot], (it / kNST) & 1, abort_flag, a.err);
-            const float *Ks = ring + static_cast<size_t>(slot) * (2 * R * HDKV);
-            const float *Vs = Ks + R * HDKV;
+            float *Ks = ring + static_cast<size_t>(slot) * (2 * R * HDKV);
+            float *Vs = Ks + R * HDKV;
             const int row0 = t.r_begin + st * R;
+            if (kFused && pnew >= row0 && pnew < row0 + R) {
+                // the tile may hold the row as it was before this launch appended it: the lanes
+                // that staged the new row put it in its place (and hand the slot back to the
+                // async proxy in order)
+                if (warp == 0 && r4 == 0) {
+                    const int rn = pnew - row0;
+#pragma unroll
+                    for (int i = 0; i < KF4; ++i) {
+                        reinterpret_cast<float4 *>(Ks + rn * HDKV)[sub + 8 * i] =
+                            reinterpret_cast<const float4 *>(sm_knew)[sub + 8 * i];
+                        reinterpret_cast<float4 *>(Vs + rn * HDKV)[sub + 8 * i] =
+                            reinterpret_cast<const float4 *>(sm_vnew)[sub + 8 * i];
+                    }
+                    fence_async_smem();
+                }
+                cons_sync(&cons_bar, cphase, abort_flag, a.err);
+            }
 #pragma unroll
             for (int sp = 0; sp < SPW; ++sp) {
                 const int rr0 = (warp * SPW + sp) * kSub;  // sub-tile's first row within the stage
@@ -435,9 +544,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int it2 = 0; it2 < 2; ++it2) {
                     const int rr = rr0 + 4 * it2 + r4;
-                    const float4 *src = (kFused && row0 + rr == pnew)
-                                            ? reinterpret_cast<const float4 *>(sm_knew)
-                                            : reinterpret_cast<const float4 *>(Ks + rr * HDKV);
+                    const float4 *src = reinterpret_cast<const float4 *>(Ks + rr * HDKV);
 #pragma unroll
                     for (int i = 0; i < KF4; ++i) kv[it2][i] = src[sub + 8 * i];
                 }
@@ -445,12 +552,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int jv = 0; jv < VJ; ++jv) {
                     const int rr = rr0 + vrow + VRP * jv;
                     const int row = row0 + rr;
-                    if (row >= t.r_end)
-                        vv[jv] = make_float4(0.f, 0.f, 0.f, 0.f);  // rows past the run may hold anything
-                    else if (kFused && row == pnew)
-                        vv[jv] = reinterpret_cast<const float4 *>(sm_vnew)[vcol];
-                    else
-                        vv[jv] = reinterpret_cast<const float4 *>(Vs + rr * HDKV)[vcol];
+                    vv[jv] = row < t.r_end ? reinterpret_cast<const float4 *>(Vs + rr * HDKV)[vcol]
+                                           : make_float4(0.f, 0.f, 0.f, 0.f);  // past the run: anything
                 }
                 float pr[2][GH];
 #pragma unroll
@@ -504,19 +607,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[slot]);
-            if (early && !released && warp == 0) {
-                // release the dependent launch once the appended row (if any) is visible; one
-                // thread's trigger releases the CTA, so only warp 0 -- which wrote the row --
-                // triggers, after its fence
-                if (own_new && r4 == 0) __threadfence();
-                __syncwarp();
-                if (lane == 0) gdc_launch_dependents();
-                released = true;
-            }
         }
 
         // ------------------------------------------------------------ end of the unit
-        named_sync(1, kCons);  // the previous unit's readers of the scratch are done
+        cons_sync(&cons_bar, cphase, abort_flag, a.err);  // the previous unit's scratch readers are done
 #pragma unroll
         for (int hh = 0; hh < GH; ++hh) {
 #pragma unroll
@@ -532,7 +626,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 sm_l[warp][hh] = l[hh];
             }
         }
-        named_sync(1, kCons);
+        cons_sync(&cons_bar, cphase, abort_flag, a.err);
+        float *out_s = a.out + (static_cast<size_t>(t.s) * a.nh + h0) * HDKV;
         const size_t part0 = (static_cast<size_t>(t.s) * a.nh + h0) * a.n_split;  // head h0, split 0
         for (int i = tid; i < GH * VL; i += kCons) {
             const int hh = i / VL, c = i % VL;
@@ -566,7 +661,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool last = true;
         int *ticket = a.ws_ticket + static_cast<size_t>(t.s) * P + t.y;
         if (t.n_act > 1) {
-            named_sync(1, kCons);
+            cons_sync(&cons_bar, cphase, abort_flag, a.err);
             if (tid == 0) {
                 // acq_rel: publishes this CTA's partials (ordered before it by the barrier) and,
                 // for the last arrival, makes every other unit's partials visible to its loads
@@ -574,7 +669,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], 1;" : "=r"(old) : "l"(ticket) : "memory");
                 sm_last = old == t.n_act - 1;
             }
-            named_sync(1, kCons);
+            cons_sync(&cons_bar, cphase, abort_flag, a.err);
             last = sm_last;
         }
         if (!last) continue;
@@ -587,13 +682,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int i = tid; i < kPairs * kWays; i += kCons) {
                 const int pair = i % kPairs, way = i / kPairs;
                 const int hh = pair / VL, c = pair % VL;
-                const size_t ph = part0 + static_cast<size_t>(hh) * a.n_split;
+                const size_t ph2 = part0 + static_cast<size_t>(hh) * a.n_split;
                 float M = -INFINITY, Ls = 0.0f;
                 float4 A = make_float4(0.f, 0.f, 0.f, 0.f);
-    #pragma unroll 8
+#pragma unroll 8
                 for (int j = way; j < t.n_act; j += kWays) {
-                    const float2 ml = __ldcg(reinterpret_cast<const float2 *>(a.ws_ml) + (ph + j));
-                    const float4 x = __ldcg(reinterpret_cast<const float4 *>(a.ws_acc + (ph + j) * HDKV) + c);
+                    const float2 ml = __ldcg(reinterpret_cast<const float2 *>(a.ws_ml) + (ph2 + j));
+                    const float4 x = __ldcg(reinterpret_cast<const float4 *>(a.ws_acc + (ph2 + j) * HDKV) + c);
                     const float Mn = fmaxf(M, ml.x);
                     const float fo = M == -INFINITY ? 0.0f : ex2_approx(M - Mn);
                     const float fn = ex2_approx(ml.x - Mn);
@@ -606,7 +701,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 sm_redM[way * kPairs + pair] = M;
                 sm_redL[way * kPairs + pair] = Ls;
             }
-            named_sync(1, kCons);
+            cons_sync(&cons_bar, cphase, abort_flag, a.err);
             for (int i = tid; i < kPairs; i += kCons) {
                 const int hh = i / VL, c = i % VL;
                 float M = sm_redM[i];
@@ -679,7 +774,7 @@ cudaError_t dispatch_gh(int gh, const CUtensorMap &tk, const CUtensorMap &tv, co
 }
 
 struct Plan {
-    int gh, groups, S;
+    int gh, groups, S, min_rows, sorted;
     WsLayout w;
 };
 
@@ -688,7 +783,11 @@ Plan plan_for(int n_seq, int nh, int nk, int hd_kv, int max_cap) {
     const int g = nh / nk;
     p.gh = heads_per_cta(g, hd_kv);
     p.groups = g / p.gh;
-    p.S = choose_splits(static_cast<long long>(n_seq) * nk * p.groups, hd_kv, max_cap);
+    const long long pairs = static_cast<long long>(n_seq) * nk * p.groups;
+    p.S = choose_splits(pairs, hd_kv, max_cap);
+    const bool batch = pairs >= kGridTarget;
+    p.min_rows = batch ? kBatchMinRows : stage_rows(hd_kv);
+    p.sorted = batch && n_seq > 1 && n_seq <= kMaxSort;
     p.w = ws_layout(n_seq, nh, nk * p.groups, hd_kv, p.S);
     return p;
 }
@@ -740,6 +839,10 @@ int launch_impl(const DecodeArgs &d, const DecodeStepExtra *x, cudaStream_t s) {
     k.ws_ml = reinterpret_cast<float *>(ws + pl.w.ml_off);
     k.ws_acc = reinterpret_cast<float *>(ws + pl.w.acc_off);
     k.ws_ticket = reinterpret_cast<int *>(ws + pl.w.ticket_off);
+    k.ws_ctr = reinterpret_cast<int *>(ws + pl.w.ctr_off);
+    k.ws_done = k.ws_ctr + 1;
+    k.min_rows = pl.min_rows;
+    k.sorted = pl.sorted;
     k.k_reg = const_cast<float *>(d.k_reg);
     k.v_reg = const_cast<float *>(d.v_reg);
     bool pdl = false;

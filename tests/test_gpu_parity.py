@@ -177,6 +177,9 @@ def _decode_case(m, orc, nh, nk, hd, hdkv, caps, lengths, seed, arena=True):
     got = out.cpu().numpy()
     for s in range(n_seq):
         o, c = int(offs[s]), int(caps[s])
+        if pos[s] < 0:  # empty window: defined as a zero output
+            assert not np.any(got[s]), f"decode seq {s}: empty window gave a non-zero output"
+            continue
         ref = orc.gqa_attn(q[s:s + 1].numpy(), K[o:o + c].numpy(), V[o:o + c].numpy(), [pos[s]], nh, nk,
                            hd, hdkv, scale=scale)
         close(got[s:s + 1], ref, what=f"decode seq {s} (L={pos[s] + 1})")
@@ -208,6 +211,39 @@ def test_decode_batched_ragged(m, orc):
     lengths = [int(x) for x in r.integers(1, 700, size=12)] + [1, 2, 699]
     caps = [ln + 5 for ln in lengths]
     err, _ = _decode_case(m, orc, 16, 8, 128, 128, caps, [ln - 1 for ln in lengths], seed=7)
+    assert err.item() == 0
+
+
+def test_decode_batch_longest_first_with_long_windows(m, orc):
+    # Enough (sequence, kv head) pairs to fill the SMs: the batch is visited longest first and
+    # units are drawn from the workspace counter; windows past 4096 rows are also split.  The
+    # second call reuses the workspace, so the counter and tickets must have been reset.
+    r = np.random.default_rng(11)
+    for call in range(2):
+        lengths = [int(x) for x in r.integers(1, 1500, size=21)] + [9001, 4097, 4096, 1, 2, 1025]
+        caps = [ln + 3 for ln in lengths]
+        caps[-3] = 1  # window clamped to a one-row region (pos >= cap flags the attention bit)
+        pos = [ln - 1 for ln in lengths]
+        pos[-3] = 5
+        err, _ = _decode_case(m, orc, 16, 8, 128, 128, caps, pos, seed=90 + call)
+        assert err.item() == 0x4
+
+
+def test_decode_batch_empty_window_is_zero_and_flagged(m, orc):
+    r = np.random.default_rng(12)
+    lengths = [int(x) for x in r.integers(1, 400, size=40)]
+    pos = [ln - 1 for ln in lengths]
+    pos[7] = -1
+    err, _ = _decode_case(m, orc, 14, 2, 64, 64, [ln + 2 for ln in lengths], pos, seed=13)
+    assert err.item() == 0x4
+
+
+def test_decode_batch_beyond_sort_limit(m, orc):
+    # more sequences than the longest-first ordering handles: visited in index order
+    r = np.random.default_rng(14)
+    lengths = [int(x) for x in r.integers(1, 200, size=300)]
+    err, _ = _decode_case(m, orc, 16, 8, 128, 128, [ln + 1 for ln in lengths], [ln - 1 for ln in lengths],
+                          seed=15)
     assert err.item() == 0
 
 
@@ -325,11 +361,13 @@ def test_layer_step_prefill_then_graph_replayed_decode(m, orc):
     assert err.item() == 0
 
 
-def test_layer_step_batched(m, orc):
+@pytest.mark.parametrize("n_seq,hi", [(9, 600), (24, 5000)])
+def test_layer_step_batched(m, orc, n_seq, hi):
+    # 24 sequences x 8 kv heads fill the SMs: the fused kernel then draws units longest first
     from gqa_attention_kv_rope_gb300 import workloads as wl
 
     g = wl.QWEN3_06B
-    lengths = wl.batched_lengths(seed=3, n_seq=9, lo=1, hi=600)
+    lengths = wl.batched_lengths(seed=3, n_seq=n_seq, lo=1, hi=hi)
     caps = [ln + 1 + 8 for ln in lengths]
     arena = m.kv.KvArena(1, g.row_width, caps)
     Kh = rnd((arena.rows, g.row_width), 70)
