@@ -33,6 +33,7 @@ _lib = None
 _f32p = ctypes.POINTER(ctypes.c_float)
 _f64p = ctypes.POINTER(ctypes.c_double)
 _i32p = ctypes.POINTER(ctypes.c_int32)
+_u16p = ctypes.POINTER(ctypes.c_uint16)
 
 
 def build(force: bool = False) -> str:
@@ -80,6 +81,20 @@ def _load():
             _f32p, _f32p, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
             ctypes.c_float, ctypes.c_float, ctypes.c_int, _f32p, ctypes.c_int]
         lib.orc_layer_attn_step.restype = ctypes.c_int
+        _u16p = ctypes.POINTER(ctypes.c_uint16)
+        lib.orc_f32_to_f16_array.argtypes = [_u16p, _f32p, ctypes.c_long]
+        lib.orc_f32_to_f16_array.restype = None
+        lib.orc_f16_to_f32_array.argtypes = [_f32p, _u16p, ctypes.c_long]
+        lib.orc_f16_to_f32_array.restype = None
+        lib.orc_kv_append_f16.argtypes = [_u16p, _u16p, ctypes.c_int, ctypes.c_int, _f32p, _f32p, _i32p,
+                                          ctypes.c_int]
+        lib.orc_kv_append_f16.restype = ctypes.c_int
+        lib.orc_layer_attn_step_f16.argtypes = [
+            _f32p, _f32p, _f32p, ctypes.c_float, ctypes.c_int,
+            _f32p, _f32p, _f32p, _i32p, ctypes.c_int,
+            _u16p, _u16p, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+            ctypes.c_float, ctypes.c_float, ctypes.c_int, _f32p, ctypes.c_int]
+        lib.orc_layer_attn_step_f16.restype = ctypes.c_int
         _lib = lib
         return lib
 
@@ -221,4 +236,71 @@ def layer_attn_step(h, gain, q, k, v, pos, k_reg, v_reg, *, n_head: int, n_kv_he
         theta, freq_scale, style, _p(out, _f32p), n_threads)
     if st != OK:
         raise OracleError(st, "layer_attn_step")
+    return xn, out
+
+
+# ----------------------------------------------------------------------------- f16 cache
+def _u16(a, writable=False):
+    a = np.asarray(a)
+    if a.dtype != np.uint16 or not a.flags.c_contiguous:
+        if writable:
+            raise TypeError("in-place argument must be a C-contiguous uint16 array")
+        a = np.ascontiguousarray(a, dtype=np.uint16)
+    return a
+
+
+def f32_to_f16(x) -> np.ndarray:
+    """binary16 bit patterns (uint16) of float32 values, round to nearest even."""
+    x = _f32(x)
+    out = np.empty(x.shape, dtype=np.uint16)
+    _load().orc_f32_to_f16_array(_p(out, _u16p), _p(x, _f32p), x.size)
+    return out
+
+
+def f16_to_f32(h) -> np.ndarray:
+    """float32 values of binary16 bit patterns (exact)."""
+    h = _u16(h)
+    out = np.empty(h.shape, dtype=np.float32)
+    _load().orc_f16_to_f32_array(_p(out, _f32p), _p(h, _u16p), h.size)
+    return out
+
+
+def kv_append_f16(k_reg, v_reg, k_rows, v_rows, pos, check=True) -> int:
+    """f16 regions [cap, W] as uint16 bit patterns (modified in place), fp32 rows [nt, W]."""
+    k_reg = _u16(k_reg, writable=True)
+    v_reg = _u16(v_reg, writable=True)
+    cap, W = k_reg.shape
+    k_rows = _f32(k_rows).reshape(-1, W)
+    v_rows = _f32(v_rows).reshape(-1, W)
+    pos = _i32(pos)
+    st = _load().orc_kv_append_f16(_p(k_reg, _u16p), _p(v_reg, _u16p), cap, W, _p(k_rows, _f32p),
+                                   _p(v_rows, _f32p), _p(pos, _i32p), pos.shape[0])
+    if check and st != OK:
+        raise OracleError(st, "kv_append_f16")
+    return st
+
+
+def layer_attn_step_f16(h, gain, q, k, v, pos, k_reg, v_reg, *, n_head: int, n_kv_head: int, hd: int,
+                        hd_kv: int, eps: float = 1e-6, theta: float = 1e6, freq_scale: float = 1.0,
+                        style: int = 0, n_threads: int = 1):
+    """layer_attn_step over f16 regions (uint16 bit patterns, appended in place)."""
+    h = _f32(h)
+    gain = _f32(gain)
+    q = _f32(q, writable=True)
+    k = _f32(k, writable=True)
+    v = _f32(v)
+    pos = _i32(pos)
+    k_reg = _u16(k_reg, writable=True)
+    v_reg = _u16(v_reg, writable=True)
+    nt = pos.shape[0]
+    n_embd = h.size // max(nt, 1)
+    xn = np.empty_like(h)
+    out = np.zeros((nt, n_head * hd_kv), dtype=np.float32)
+    st = _load().orc_layer_attn_step_f16(
+        _p(xn, _f32p), _p(h, _f32p), _p(gain, _f32p), eps, n_embd,
+        _p(q, _f32p), _p(k, _f32p), _p(v, _f32p), _p(pos, _i32p), nt,
+        _p(k_reg, _u16p), _p(v_reg, _u16p), k_reg.shape[0], n_head, n_kv_head, hd, hd_kv,
+        theta, freq_scale, style, _p(out, _f32p), n_threads)
+    if st != OK:
+        raise OracleError(st, "layer_attn_step_f16")
     return xn, out

@@ -21,7 +21,9 @@
  *
  * Parity status per function (what pins it is in tests/test_oracle_*.py):
  *   orc_rope_freqs, orc_rms_norm, orc_rope, orc_kv_append, orc_gqa_attn,
- *   orc_attn_bruteforce_f64, orc_silu_mul, orc_layer_attn_step -- all pinned.
+ *   orc_attn_bruteforce_f64, orc_silu_mul, orc_layer_attn_step,
+ *   orc_f32_to_f16, orc_f16_to_f32, orc_kv_append_f16,
+ *   orc_layer_attn_step_f16 -- all pinned.
  */
 #include <math.h>
 #include <pthread.h>
@@ -321,6 +323,100 @@ int orc_attn_bruteforce_f64(double *out, const float *q, const float *k_reg, con
 }
 
 /* ------------------------------------------------------------------------ */
+/* The f16 cache.  [P1] §2.5 ("What changes on the GPU"): the GPU backends may
+ * keep the K/V regions in f16, halving the bytes each attention read moves;
+ * the store converts and the attention read converts back.  The pages do not
+ * name a rounding, so the store takes IEEE 754 binary16 with round to nearest,
+ * ties to even (the format's default), written out here from the format's
+ * definition: 1 sign bit, 5 exponent bits (bias 15), 10 fraction bits;
+ * subnormals are m * 2^-24; magnitudes that round past 65504 become infinity;
+ * NaN stays NaN.  Reading back is exact (every binary16 value is an fp32). */
+uint16_t orc_f32_to_f16(float f)
+{
+    uint32_t x;
+    memcpy(&x, &f, sizeof x);
+    uint32_t sign = (x >> 16) & 0x8000u;
+    int exp = (int)((x >> 23) & 0xffu);
+    uint32_t frac = x & 0x7fffffu;
+    if (exp == 0xff) /* infinity, or NaN (kept quiet, payload truncated) */
+        return (uint16_t)(sign | 0x7c00u | (frac ? 0x200u | (frac >> 13) : 0u));
+    int e = exp - 127 + 15; /* the binary16 biased exponent of a normal result */
+    if (e >= 1) {
+        uint32_t m = frac >> 13, rest = frac & 0x1fffu;
+        if (rest > 0x1000u || (rest == 0x1000u && (m & 1u)))
+            ++m;
+        if (m == 0x400u) { /* the fraction overflowed into the exponent */
+            m = 0;
+            ++e;
+        }
+        if (e >= 31)
+            return (uint16_t)(sign | 0x7c00u);
+        return (uint16_t)(sign | ((uint32_t)e << 10) | m);
+    }
+    /* subnormal (or zero) result: value / 2^-24, rounded to an integer */
+    if (exp == 0)
+        return (uint16_t)sign; /* fp32 subnormals are far below 2^-25 */
+    uint32_t full = frac | 0x800000u; /* 24 significant bits, value = full * 2^(exp-150) */
+    int shift = 126 - exp;            /* value / 2^-24 = full >> shift */
+    if (shift > 24)
+        return (uint16_t)sign;
+    uint32_t m = full >> shift, rest = full & ((1u << shift) - 1u), half = 1u << (shift - 1);
+    if (rest > half || (rest == half && (m & 1u)))
+        ++m; /* m == 0x400 is the smallest normal, which the bits already spell */
+    return (uint16_t)(sign | m);
+}
+
+float orc_f16_to_f32(uint16_t h)
+{
+    uint32_t sign = (uint32_t)(h & 0x8000u) << 16;
+    int e = (h >> 10) & 0x1f;
+    uint32_t m = h & 0x3ffu;
+    float v;
+    if (e == 0) {
+        v = ldexpf((float)m, -24);
+        if (sign)
+            v = -v;
+        return v;
+    }
+    uint32_t x;
+    if (e == 31)
+        x = sign | 0x7f800000u | (m << 13);
+    else
+        x = sign | ((uint32_t)(e - 15 + 127) << 23) | (m << 13);
+    memcpy(&v, &x, sizeof v);
+    return v;
+}
+
+void orc_f32_to_f16_array(uint16_t *dst, const float *src, long n)
+{
+    for (long i = 0; i < n; ++i)
+        dst[i] = orc_f32_to_f16(src[i]);
+}
+
+void orc_f16_to_f32_array(float *dst, const uint16_t *src, long n)
+{
+    for (long i = 0; i < n; ++i)
+        dst[i] = orc_f16_to_f32(src[i]);
+}
+
+/* The KV store into f16 regions: the same placement as orc_kv_append, each
+ * element converted on the way in ([P1] §2.5: the store converts). */
+int orc_kv_append_f16(uint16_t *k_reg, uint16_t *v_reg, int cap, int W,
+                      const float *k_rows, const float *v_rows, const int32_t *pos, int nt)
+{
+    if (cap < 0 || W <= 0 || nt < 0)
+        return ORC_ERR_ARG;
+    for (int t = 0; t < nt; ++t) {
+        int p = pos[t];
+        if (p < 0 || p >= cap)
+            return ORC_ERR_POS;
+        orc_f32_to_f16_array(k_reg + (size_t)p * W, k_rows + (size_t)t * W, W);
+        orc_f32_to_f16_array(v_reg + (size_t)p * W, v_rows + (size_t)t * W, W);
+    }
+    return ORC_OK;
+}
+
+/* ------------------------------------------------------------------------ */
 /* SiLU times up.  [P1] §3.2.5: silu(x) = x / (1 + e^-x); SwiGLU multiplies it
  * by the up projection element-wise. */
 void orc_silu_mul(float *y, const float *gate, const float *up, long n)
@@ -358,4 +454,42 @@ int orc_layer_attn_step(float *xn, const float *h, const float *gain, float eps,
         return st;
     float scale = 1.0f / sqrtf((float)hd);
     return orc_gqa_attn(out, q, k_reg, v_reg, cap, pos, nt, nh, nk, hd, hdkv, scale, n_threads);
+}
+
+/* The same stage over f16 regions ([P1] §2.5): the store converts the rotated
+ * k and v to f16; the attention read converts the regions back (exactly) and
+ * runs the fp32 attention above on those values. */
+int orc_layer_attn_step_f16(float *xn, const float *h, const float *gain, float eps, int n_embd,
+                            float *q, float *k, const float *v, const int32_t *pos, int nt,
+                            uint16_t *k_reg, uint16_t *v_reg, int cap, int nh, int nk, int hd,
+                            int hdkv, float theta, float freq_scale, int style, float *out,
+                            int n_threads)
+{
+    if (hd < hdkv || nh <= 0 || nk <= 0 || nh % nk != 0)
+        return ORC_ERR_GEOMETRY;
+    orc_rms_norm(xn, h, gain, nt, n_embd, eps);
+    int st = orc_rope(q, pos, nt, nh, hd, theta, freq_scale, style);
+    if (st != ORC_OK)
+        return st;
+    st = orc_rope(k, pos, nt, nk, hdkv, theta, freq_scale, style);
+    if (st != ORC_OK)
+        return st;
+    int W = nk * hdkv;
+    st = orc_kv_append_f16(k_reg, v_reg, cap, W, k, v, pos, nt);
+    if (st != ORC_OK)
+        return st;
+    float *kf = malloc(sizeof(float) * (size_t)cap * W);
+    float *vf = malloc(sizeof(float) * (size_t)cap * W);
+    if (!kf || !vf) {
+        free(kf);
+        free(vf);
+        return ORC_ERR_ARG;
+    }
+    orc_f16_to_f32_array(kf, k_reg, (long)cap * W);
+    orc_f16_to_f32_array(vf, v_reg, (long)cap * W);
+    float scale = 1.0f / sqrtf((float)hd);
+    st = orc_gqa_attn(out, q, kf, vf, cap, pos, nt, nh, nk, hd, hdkv, scale, n_threads);
+    free(kf);
+    free(vf);
+    return st;
 }

@@ -396,3 +396,113 @@ def test_layer_step_is_the_composition(orc):
     np.testing.assert_array_equal(Vs, V2)
     ref = orc.attn_bruteforce_f64(q2, K2, V2, pos, nh, nk, hd, hdkv, 1.0 / math.sqrt(hd))
     assert np.all(np.abs(out - ref) <= 1e-5 + 1e-4 * np.abs(ref))
+
+
+# --------------------------------------------------------------------------- f16 cache
+# "11 . Attention, vec ops, and the KV cache", §2.5: the GPU backends may keep the K/V regions
+# in f16; the store converts and the attention read converts back.  The conversion is IEEE
+# binary16, round to nearest even (the pages name no rounding); numpy's float16 cast is an
+# independent implementation of the same definition.
+def test_f16_conversion_closed_forms(orc):
+    vals = {1.0: 0x3C00, -2.0: 0xC000, 65504.0: 0x7BFF, 2.0 ** -24: 0x0001, 2.0 ** -14: 0x0400,
+            0.5: 0x3800, 1.0 + 2.0 ** -10: 0x3C01, 1.0 + 2.0 ** -11: 0x3C00,  # tie -> even
+            1.0 + 3 * 2.0 ** -11: 0x3C02,  # tie -> even (up)
+            65520.0: 0x7C00, 2.0 ** -25: 0x0000, 3 * 2.0 ** -25: 0x0002, float("inf"): 0x7C00}
+    x = np.array(list(vals), np.float32)
+    got = orc.f32_to_f16(x)
+    assert [int(g) for g in got] == list(vals.values())
+    exact = [1.0, -2.0, 65504.0, 2.0 ** -24, 2.0 ** -14, 0.5, 1.0 + 2.0 ** -10]
+    np.testing.assert_array_equal(orc.f16_to_f32(orc.f32_to_f16(np.array(exact, np.float32))),
+                                  np.array(exact, np.float32))
+    assert np.isnan(orc.f16_to_f32(np.array([0x7E00], np.uint16)))[0]
+    assert np.isnan(orc.f16_to_f32(orc.f32_to_f16(np.array([np.nan], np.float32))))[0]
+
+
+def test_f16_conversion_matches_the_format_everywhere(orc):
+    r = _rng(40)
+    mag = np.exp2(r.uniform(-30, 17, 200000)).astype(np.float32)
+    x = np.concatenate([mag, -mag, r.standard_normal(50000).astype(np.float32),
+                        np.array([0.0, -0.0, 65519.996, 65520.0, 1e30, -1e30, 6.0e-8, 5.9e-8],
+                                 np.float32)])
+    with np.errstate(over="ignore"):
+        ref = x.astype(np.float16).view(np.uint16)
+    np.testing.assert_array_equal(orc.f32_to_f16(x), ref)
+    # every bit pattern reads back as numpy reads it
+    allh = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    got = orc.f16_to_f32(allh)
+    ref = allh.view(np.float16).astype(np.float32)
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(got), nan)
+    np.testing.assert_array_equal(got[~nan], ref[~nan])
+
+
+def test_kv_append_f16_placement_and_errors(orc):
+    r = _rng(41)
+    cap, W = 9, 16
+    k_reg = orc.f32_to_f16(r.standard_normal((cap, W)).astype(np.float32))
+    v_reg = orc.f32_to_f16(r.standard_normal((cap, W)).astype(np.float32))
+    k0, v0 = k_reg.copy(), v_reg.copy()
+    k = (r.standard_normal((3, W)) * 100).astype(np.float32)
+    v = r.standard_normal((3, W)).astype(np.float32)
+    orc.kv_append_f16(k_reg, v_reg, k, v, [5, 8, 0])
+    for t, p in enumerate([5, 8, 0]):
+        np.testing.assert_array_equal(k_reg[p], k[t].astype(np.float16).view(np.uint16))
+        np.testing.assert_array_equal(v_reg[p], v[t].astype(np.float16).view(np.uint16))
+    untouched = [i for i in range(cap) if i not in (5, 8, 0)]
+    np.testing.assert_array_equal(k_reg[untouched], k0[untouched])
+    np.testing.assert_array_equal(v_reg[untouched], v0[untouched])
+    k1 = k_reg.copy()
+    assert orc.kv_append_f16(k_reg, v_reg, k, v, [1, cap, 2], check=False) == orc.ERR_POS
+    np.testing.assert_array_equal(k_reg[2], k1[2])
+    assert orc.kv_append_f16(k_reg, v_reg, k[:1], v[:1], [-1], check=False) == orc.ERR_POS
+
+
+def test_f16_layer_step_equals_f32_step_on_representable_values(orc):
+    # At pos 0 RoPE is the identity, so with k, v and the cached rows already binary16 values the
+    # f16 store loses nothing: the f16 step must equal the fp32 step bit for bit.
+    r = _rng(42)
+    nh, nk, hd, hdkv, n_embd, cap = 4, 2, 16, 16, 24, 6
+    f16 = lambda a: a.astype(np.float16).astype(np.float32)
+    h = r.standard_normal((1, n_embd)).astype(np.float32)
+    gain = r.uniform(0.5, 1.5, n_embd).astype(np.float32)
+    q = r.standard_normal((1, nh * hd)).astype(np.float32)
+    k = f16(r.standard_normal((1, nk * hdkv)))
+    v = f16(r.standard_normal((1, nk * hdkv)))
+    K = f16(r.standard_normal((cap, nk * hdkv)))
+    V = f16(r.standard_normal((cap, nk * hdkv)))
+    pos = [0]
+    K16, V16 = orc.f32_to_f16(K), orc.f32_to_f16(V)
+    xa, oa = orc.layer_attn_step(h, gain, q.copy(), k.copy(), v, pos, K.copy(), V.copy(), n_head=nh,
+                                 n_kv_head=nk, hd=hd, hd_kv=hdkv)
+    xb, ob = orc.layer_attn_step_f16(h, gain, q.copy(), k.copy(), v, pos, K16, V16, n_head=nh,
+                                     n_kv_head=nk, hd=hd, hd_kv=hdkv)
+    np.testing.assert_array_equal(xa, xb)
+    np.testing.assert_array_equal(oa, ob)
+    np.testing.assert_array_equal(K16[0], orc.f32_to_f16(k[0]))
+
+
+def test_f16_layer_step_reads_what_it_stored(orc):
+    # Anywhere else the f16 step is the fp32 attention over the regions it leaves behind: the
+    # brute-force fp64 attention over the stored (rounded) values agrees within fp32 tolerance,
+    # and the rounding moves the output by no more than binary16 precision allows.
+    r = _rng(43)
+    nh, nk, hd, hdkv, n_embd, cap = 6, 2, 32, 32, 40, 20
+    nt, pos = 3, [11, 12, 13]
+    h = r.standard_normal((nt, n_embd)).astype(np.float32)
+    gain = np.ones(n_embd, np.float32)
+    q = r.standard_normal((nt, nh * hd)).astype(np.float32)
+    k = r.standard_normal((nt, nk * hdkv)).astype(np.float32)
+    v = r.standard_normal((nt, nk * hdkv)).astype(np.float32)
+    K = r.standard_normal((cap, nk * hdkv)).astype(np.float32)
+    V = r.standard_normal((cap, nk * hdkv)).astype(np.float32)
+    K16, V16 = orc.f32_to_f16(K), orc.f32_to_f16(V)
+    qs = q.copy()
+    _, out = orc.layer_attn_step_f16(h, gain, qs, k.copy(), v, pos, K16, V16, n_head=nh, n_kv_head=nk,
+                                     hd=hd, hd_kv=hdkv)
+    ref = orc.attn_bruteforce_f64(qs, orc.f16_to_f32(K16), orc.f16_to_f32(V16), pos, nh, nk, hd, hdkv,
+                                  1.0 / math.sqrt(hd))
+    assert np.all(np.abs(out - ref) <= 1e-5 + 1e-4 * np.abs(ref))
+    _, out32 = orc.layer_attn_step(h, gain, q.copy(), k.copy(), v, pos, K.copy(), V.copy(), n_head=nh,
+                                   n_kv_head=nk, hd=hd, hd_kv=hdkv)
+    d = np.abs(out - out32)
+    assert d.max() < 2e-2 and d.max() > 0  # binary16 keeps ~3 decimal digits, and it is not a no-op
