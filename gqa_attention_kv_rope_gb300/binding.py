@@ -54,6 +54,16 @@ _SIGS = {
     "minf_layer_attn_step_batched": ([_P, _P, _P, _F, _I, _P, _P, _P, _P, _I, _P, _P, _P, _P, _I, _I64,
                                       _I, _I, _I, _I, _F, _F, _I, _P, _P, _SZ, _P, _P], _I),
     "minf_silu_mul": ([_P, _P, _P, _I64, _P], _I),
+    # binary16 regions (torch.float16 tensors): the same arguments as the fp32 entry points
+    "minf_kv_append_f16": ([_P, _P, _I, _I, _P, _P, _P, _I, _P, _P], _I),
+    "minf_rope_kv_append_f16": ([_P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _F, _I, _P, _P, _I, _P, _P], _I),
+    "minf_gqa_attn_decode_f16": ([_P, _P, _P, _P, _P, _P, _I, _I64, _P, _I, _I, _I, _I, _I, _F, _P, _SZ, _P,
+                                  _P], _I),
+    "minf_gqa_attn_prefill_f16": ([_P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _I, _F, _P, _SZ, _P, _P], _I),
+    "minf_layer_attn_step_f16": ([_P, _P, _P, _F, _I, _P, _P, _P, _P, _I, _P, _P, _I, _I, _I, _I, _I,
+                                  _F, _F, _I, _P, _P, _SZ, _P, _P], _I),
+    "minf_layer_attn_step_batched_f16": ([_P, _P, _P, _F, _I, _P, _P, _P, _P, _I, _P, _P, _P, _P, _I, _I64,
+                                          _I, _I, _I, _I, _F, _F, _I, _P, _P, _SZ, _P, _P], _I),
 }
 
 
@@ -226,3 +236,72 @@ def minf_layer_attn_step_batched(xn, h, gain, eps, q, k, v, pos, k_arena, v_aren
 def minf_silu_mul(y, gate, up, stream=None):
     _check(lib().minf_silu_mul(_dev(y, name="y"), _dev(gate, name="gate"), _dev(up, name="up"),
                                gate.numel(), _stream(stream)), "minf_silu_mul")
+
+
+# ----------------------------------------------------------------------------- binary16 regions
+# The regions (or arena) are torch.float16 tensors; everything else is as for fp32 regions.
+_H = torch.float16
+
+
+def minf_kv_append_f16(k_reg, v_reg, k_rows, v_rows, pos, err, stream=None):
+    cap, W = k_reg.shape
+    _check(lib().minf_kv_append_f16(_dev(k_reg, _H, "k_reg"), _dev(v_reg, _H, "v_reg"), cap, W,
+                                    _dev(k_rows, name="k_rows"), _dev(v_rows, name="v_rows"),
+                                    _dev(pos, torch.int32, "pos"), pos.numel(),
+                                    _dev(err, torch.int32, "err"), _stream(stream)), "minf_kv_append_f16")
+
+
+def minf_rope_kv_append_f16(q, k, v, pos, n_head, n_kv_head, hd, hd_kv, theta, freq_scale, style, k_reg,
+                            v_reg, err, stream=None):
+    cap = k_reg.shape[0]
+    _check(lib().minf_rope_kv_append_f16(_dev(q, name="q"), _dev(k, name="k"), _dev(v, name="v"),
+                                         _dev(pos, torch.int32, "pos"), pos.numel(), n_head, n_kv_head,
+                                         hd, hd_kv, theta, freq_scale, style, _dev(k_reg, _H, "k_reg"),
+                                         _dev(v_reg, _H, "v_reg"), cap, _dev(err, torch.int32, "err"),
+                                         _stream(stream)), "minf_rope_kv_append_f16")
+
+
+def minf_gqa_attn_decode_f16(out, q, k_reg, v_reg, seq_row_off, seq_cap, max_cap, pos, n_head, n_kv_head,
+                             hd, hd_kv, scale, ws, err, stream=None):
+    _check(lib().minf_gqa_attn_decode_f16(
+        _dev(out, name="out"), _dev(q, name="q"), _dev(k_reg, _H, "k_reg"), _dev(v_reg, _H, "v_reg"),
+        _dev(seq_row_off, torch.int64, "seq_row_off"), _dev(seq_cap, torch.int32, "seq_cap"), max_cap,
+        k_reg.shape[0], _dev(pos, torch.int32, "pos"), pos.numel(), n_head, n_kv_head, hd, hd_kv, scale,
+        _dev(ws, torch.uint8, "ws"), ws.numel(), _dev(err, torch.int32, "err"), _stream(stream)),
+        "minf_gqa_attn_decode_f16")
+
+
+def minf_gqa_attn_prefill_f16(out, q, k_reg, v_reg, pos, n_head, n_kv_head, hd, hd_kv, scale, ws, err,
+                              stream=None):
+    cap = k_reg.shape[0]
+    _check(lib().minf_gqa_attn_prefill_f16(
+        _dev(out, name="out"), _dev(q, name="q"), _dev(k_reg, _H, "k_reg"), _dev(v_reg, _H, "v_reg"),
+        cap, _dev(pos, torch.int32, "pos"), pos.numel(), n_head, n_kv_head, hd, hd_kv, scale,
+        _dev(ws, torch.uint8, "ws"), _nbytes(ws), _dev(err, torch.int32, "err"), _stream(stream)),
+        "minf_gqa_attn_prefill_f16")
+
+
+def minf_layer_attn_step_f16(xn, h, gain, eps, q, k, v, pos, k_reg, v_reg, n_head, n_kv_head, hd, hd_kv,
+                             theta, freq_scale, style, out, ws, err, stream=None):
+    nt, n_embd = h.shape
+    cap = k_reg.shape[0]
+    _check(lib().minf_layer_attn_step_f16(
+        _dev(xn, name="xn"), _dev(h, name="h"), _dev(gain, name="gain"), eps, n_embd,
+        _dev(q, name="q"), _dev(k, name="k"), _dev(v, name="v"), _dev(pos, torch.int32, "pos"), nt,
+        _dev(k_reg, _H, "k_reg"), _dev(v_reg, _H, "v_reg"), cap, n_head, n_kv_head, hd, hd_kv,
+        theta, freq_scale, style, _dev(out, name="out"), _dev(ws, torch.uint8, "ws"), _nbytes(ws),
+        _dev(err, torch.int32, "err"), _stream(stream)), "minf_layer_attn_step_f16")
+
+
+def minf_layer_attn_step_batched_f16(xn, h, gain, eps, q, k, v, pos, k_arena, v_arena, seq_row_off, seq_cap,
+                                     max_cap, n_head, n_kv_head, hd, hd_kv, theta, freq_scale, style, out,
+                                     ws, err, stream=None):
+    n_seq, n_embd = h.shape
+    _check(lib().minf_layer_attn_step_batched_f16(
+        _dev(xn, name="xn"), _dev(h, name="h"), _dev(gain, name="gain"), eps, n_embd,
+        _dev(q, name="q"), _dev(k, name="k"), _dev(v, name="v"), _dev(pos, torch.int32, "pos"), n_seq,
+        _dev(k_arena, _H, "k_arena"), _dev(v_arena, _H, "v_arena"),
+        _dev(seq_row_off, torch.int64, "seq_row_off"), _dev(seq_cap, torch.int32, "seq_cap"), max_cap,
+        k_arena.shape[0], n_head, n_kv_head, hd, hd_kv, theta, freq_scale, style, _dev(out, name="out"),
+        _dev(ws, torch.uint8, "ws"), ws.numel(), _dev(err, torch.int32, "err"), _stream(stream)),
+        "minf_layer_attn_step_batched_f16")

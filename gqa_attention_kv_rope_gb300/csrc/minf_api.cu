@@ -67,19 +67,28 @@ int minf_rope(float *x, const int32_t *pos, int nt, int n_head, int hd, float th
     return launch_rope(x, pos, nt, n_head, hd, theta, freq_scale, style, err, cs(stream));
 }
 
+static int kv_append(void *k_reg, void *v_reg, int kv, int cap, int row_width, const float *k_rows,
+                     const float *v_rows, const int32_t *pos, int nt, int32_t *err, minf_stream_t stream) {
+    if (!ok_f(k_reg) || !ok_f(v_reg) || !ok_f(k_rows) || !ok_f(v_rows) || !pos || !err)
+        return MINF_ERR_ARG;
+    if (cap <= 0 || nt < 0 || row_width <= 0 || row_width % (kv == kKvF16 ? 8 : 4)) return MINF_ERR_ARG;
+    return launch_kv_append(k_reg, v_reg, kv, cap, row_width, k_rows, v_rows, pos, nt, err, cs(stream));
+}
+
 int minf_kv_append(float *k_reg, float *v_reg, int cap, int row_width, const float *k_rows,
                    const float *v_rows, const int32_t *pos, int nt, int32_t *err,
                    minf_stream_t stream) {
-    if (!ok_f(k_reg) || !ok_f(v_reg) || !ok_f(k_rows) || !ok_f(v_rows) || !pos || !err)
-        return MINF_ERR_ARG;
-    if (cap <= 0 || nt < 0 || row_width <= 0 || row_width % 4) return MINF_ERR_ARG;
-    return launch_kv_append(k_reg, v_reg, cap, row_width, k_rows, v_rows, pos, nt, err,
-                            cs(stream));
+    return kv_append(k_reg, v_reg, kKvF32, cap, row_width, k_rows, v_rows, pos, nt, err, stream);
+}
+
+int minf_kv_append_f16(uint16_t *k_reg, uint16_t *v_reg, int cap, int row_width, const float *k_rows,
+                       const float *v_rows, const int32_t *pos, int nt, int32_t *err, minf_stream_t stream) {
+    return kv_append(k_reg, v_reg, kKvF16, cap, row_width, k_rows, v_rows, pos, nt, err, stream);
 }
 
 static int rope_kv(float *q, float *k, const float *v, const int32_t *pos, int nt, int nh, int nk,
-                   int hd, int hd_kv, float theta, float freq_scale, int style, float *k_reg,
-                   float *v_reg, const int64_t *row_off, const int32_t *caps, int cap,
+                   int hd, int hd_kv, float theta, float freq_scale, int style, void *k_reg,
+                   void *v_reg, int kv, const int64_t *row_off, const int32_t *caps, int cap,
                    int32_t *err, cudaStream_t s) {
     RopeKvArgs a;
     a.q = q;
@@ -88,6 +97,7 @@ static int rope_kv(float *q, float *k, const float *v, const int32_t *pos, int n
     a.pos = pos;
     a.k_reg = k_reg;
     a.v_reg = v_reg;
+    a.kv = kv;
     a.row_off = row_off;
     a.caps = caps;
     a.cap = cap;
@@ -101,18 +111,32 @@ static int rope_kv(float *q, float *k, const float *v, const int32_t *pos, int n
     return launch_rope_kv_append(a, theta, freq_scale, s);
 }
 
-int minf_rope_kv_append(float *q, float *k, const float *v, const int32_t *pos, int nt,
-                        int n_head, int n_kv_head, int hd, int hd_kv, float theta,
-                        float freq_scale, int style, float *k_reg, float *v_reg, int cap,
-                        int32_t *err, minf_stream_t stream) {
+static int rope_kv_append(float *q, float *k, const float *v, const int32_t *pos, int nt, int n_head,
+                          int n_kv_head, int hd, int hd_kv, float theta, float freq_scale, int style,
+                          void *k_reg, void *v_reg, int kv, int cap, int32_t *err, minf_stream_t stream) {
     int st = check_heads(n_head, n_kv_head, hd, hd_kv);
     if (st != MINF_OK) return st;
     if (!ok_f(q) || !ok_f(k) || !ok_f(v) || !ok_f(k_reg) || !ok_f(v_reg) || !pos || !err)
         return MINF_ERR_ARG;
-    if (nt < 0 || cap <= 0 || (style != 0 && style != 1) || (n_kv_head * hd_kv) % 4)
+    if (nt < 0 || cap <= 0 || (style != 0 && style != 1) || (n_kv_head * hd_kv) % (kv == kKvF16 ? 8 : 4))
         return MINF_ERR_ARG;
     return rope_kv(q, k, v, pos, nt, n_head, n_kv_head, hd, hd_kv, theta, freq_scale, style,
-                   k_reg, v_reg, nullptr, nullptr, cap, err, cs(stream));
+                   k_reg, v_reg, kv, nullptr, nullptr, cap, err, cs(stream));
+}
+
+int minf_rope_kv_append(float *q, float *k, const float *v, const int32_t *pos, int nt,
+                        int n_head, int n_kv_head, int hd, int hd_kv, float theta,
+                        float freq_scale, int style, float *k_reg, float *v_reg, int cap,
+                        int32_t *err, minf_stream_t stream) {
+    return rope_kv_append(q, k, v, pos, nt, n_head, n_kv_head, hd, hd_kv, theta, freq_scale, style, k_reg,
+                          v_reg, kKvF32, cap, err, stream);
+}
+
+int minf_rope_kv_append_f16(float *q, float *k, const float *v, const int32_t *pos, int nt, int n_head,
+                            int n_kv_head, int hd, int hd_kv, float theta, float freq_scale, int style,
+                            uint16_t *k_reg, uint16_t *v_reg, int cap, int32_t *err, minf_stream_t stream) {
+    return rope_kv_append(q, k, v, pos, nt, n_head, n_kv_head, hd, hd_kv, theta, freq_scale, style, k_reg,
+                          v_reg, kKvF16, cap, err, stream);
 }
 
 size_t minf_attn_decode_workspace_bytes(int n_seq, int n_head, int n_kv_head, int hd_kv,
@@ -125,7 +149,7 @@ size_t minf_attn_prefill_workspace_bytes(int nt, int n_head, int n_kv_head, int 
     return prefill_workspace_bytes(nt, n_head, hd_kv, cap);
 }
 
-static int prefill(float *out, const float *q, const float *k_reg, const float *v_reg, int cap,
+static int prefill(float *out, const float *q, const void *k_reg, const void *v_reg, int kv, int cap,
                    const int32_t *pos, int nt, int nh, int nk, int hd, int hd_kv, float scale,
                    void *ws, size_t ws_bytes, int32_t *err, cudaStream_t s) {
     PrefillArgs a;
@@ -135,6 +159,7 @@ static int prefill(float *out, const float *q, const float *k_reg, const float *
     a.q = q;
     a.k_reg = k_reg;
     a.v_reg = v_reg;
+    a.kv = kv;
     a.pos = pos;
     a.err = err;
     a.nt = nt;
@@ -147,8 +172,8 @@ static int prefill(float *out, const float *q, const float *k_reg, const float *
     return launch_prefill(a, s);
 }
 
-static DecodeArgs decode_args(float *out, const float *q, const float *k_reg,
-                              const float *v_reg, const int64_t *row_off, const int32_t *caps,
+static DecodeArgs decode_args(float *out, const float *q, const void *k_reg,
+                              const void *v_reg, int kv, const int64_t *row_off, const int32_t *caps,
                               int cap, const int32_t *pos, int n_seq, int nh, int nk, int hd,
                               int hd_kv, float scale, void *ws, size_t ws_bytes, int32_t *err,
                               long long arena_rows = 0) {
@@ -158,6 +183,7 @@ static DecodeArgs decode_args(float *out, const float *q, const float *k_reg,
     d.q = q;
     d.k_reg = k_reg;
     d.v_reg = v_reg;
+    d.kv = kv;
     d.row_off = row_off;
     d.caps = caps;
     d.cap = cap;
@@ -174,13 +200,25 @@ static DecodeArgs decode_args(float *out, const float *q, const float *k_reg,
     return d;
 }
 
-static int decode(float *out, const float *q, const float *k_reg, const float *v_reg,
+static int decode(float *out, const float *q, const void *k_reg, const void *v_reg, int kv,
                   const int64_t *row_off, const int32_t *caps, int cap, const int32_t *pos,
                   int n_seq, int nh, int nk, int hd, int hd_kv, float scale, void *ws,
                   size_t ws_bytes, int32_t *err, cudaStream_t s, long long arena_rows = 0) {
-    return launch_decode(decode_args(out, q, k_reg, v_reg, row_off, caps, cap, pos, n_seq, nh, nk,
+    return launch_decode(decode_args(out, q, k_reg, v_reg, kv, row_off, caps, cap, pos, n_seq, nh, nk,
                                      hd, hd_kv, scale, ws, ws_bytes, err, arena_rows),
                          s);
+}
+
+static int gqa_attn_decode(float *out, const float *q, const void *k_reg, const void *v_reg, int kv,
+                           const int64_t *seq_row_off, const int32_t *seq_cap, int max_cap, int64_t arena_rows,
+                           const int32_t *pos, int n_seq, int n_head, int n_kv_head, int hd, int hd_kv,
+                           float scale, void *ws, size_t ws_bytes, int32_t *err, minf_stream_t stream) {
+    int st = check_attn(n_head, n_kv_head, hd, hd_kv);
+    if (st != MINF_OK) return st;
+    if (!ok_f(out) || !ok_f(q) || !ok_f(k_reg) || !ok_f(v_reg) || !pos || !err) return MINF_ERR_ARG;
+    if (n_seq < 0 || max_cap <= 0 || (seq_row_off && arena_rows <= 0)) return MINF_ERR_ARG;
+    return decode(out, q, k_reg, v_reg, kv, seq_row_off, seq_cap, max_cap, pos, n_seq, n_head,
+                  n_kv_head, hd, hd_kv, scale, ws, ws_bytes, err, cs(stream), arena_rows);
 }
 
 int minf_gqa_attn_decode(float *out, const float *q, const float *k_reg, const float *v_reg,
@@ -188,31 +226,49 @@ int minf_gqa_attn_decode(float *out, const float *q, const float *k_reg, const f
                          int64_t arena_rows, const int32_t *pos, int n_seq, int n_head,
                          int n_kv_head, int hd, int hd_kv, float scale, void *ws,
                          size_t ws_bytes, int32_t *err, minf_stream_t stream) {
+    return gqa_attn_decode(out, q, k_reg, v_reg, kKvF32, seq_row_off, seq_cap, max_cap, arena_rows, pos, n_seq,
+                           n_head, n_kv_head, hd, hd_kv, scale, ws, ws_bytes, err, stream);
+}
+
+int minf_gqa_attn_decode_f16(float *out, const float *q, const uint16_t *k_reg, const uint16_t *v_reg,
+                             const int64_t *seq_row_off, const int32_t *seq_cap, int max_cap, int64_t arena_rows,
+                             const int32_t *pos, int n_seq, int n_head, int n_kv_head, int hd, int hd_kv,
+                             float scale, void *ws, size_t ws_bytes, int32_t *err, minf_stream_t stream) {
+    return gqa_attn_decode(out, q, k_reg, v_reg, kKvF16, seq_row_off, seq_cap, max_cap, arena_rows, pos, n_seq,
+                           n_head, n_kv_head, hd, hd_kv, scale, ws, ws_bytes, err, stream);
+}
+
+static int gqa_attn_prefill(float *out, const float *q, const void *k_reg, const void *v_reg, int kv, int cap,
+                            const int32_t *pos, int nt, int n_head, int n_kv_head, int hd, int hd_kv, float scale,
+                            void *ws, size_t ws_bytes, int32_t *err, minf_stream_t stream) {
     int st = check_attn(n_head, n_kv_head, hd, hd_kv);
     if (st != MINF_OK) return st;
     if (!ok_f(out) || !ok_f(q) || !ok_f(k_reg) || !ok_f(v_reg) || !pos || !err) return MINF_ERR_ARG;
-    if (n_seq < 0 || max_cap <= 0 || (seq_row_off && arena_rows <= 0)) return MINF_ERR_ARG;
-    return decode(out, q, k_reg, v_reg, seq_row_off, seq_cap, max_cap, pos, n_seq, n_head,
-                  n_kv_head, hd, hd_kv, scale, ws, ws_bytes, err, cs(stream), arena_rows);
+    if (nt < 0 || cap <= 0) return MINF_ERR_ARG;
+    return prefill(out, q, k_reg, v_reg, kv, cap, pos, nt, n_head, n_kv_head, hd, hd_kv, scale, ws,
+                   ws_bytes, err, cs(stream));
 }
 
 int minf_gqa_attn_prefill(float *out, const float *q, const float *k_reg, const float *v_reg,
                           int cap, const int32_t *pos, int nt, int n_head, int n_kv_head, int hd,
                           int hd_kv, float scale, void *ws, size_t ws_bytes, int32_t *err,
                           minf_stream_t stream) {
-    int st = check_attn(n_head, n_kv_head, hd, hd_kv);
-    if (st != MINF_OK) return st;
-    if (!ok_f(out) || !ok_f(q) || !ok_f(k_reg) || !ok_f(v_reg) || !pos || !err) return MINF_ERR_ARG;
-    if (nt < 0 || cap <= 0) return MINF_ERR_ARG;
-    return prefill(out, q, k_reg, v_reg, cap, pos, nt, n_head, n_kv_head, hd, hd_kv, scale, ws,
-                   ws_bytes, err, cs(stream));
+    return gqa_attn_prefill(out, q, k_reg, v_reg, kKvF32, cap, pos, nt, n_head, n_kv_head, hd, hd_kv, scale, ws,
+                            ws_bytes, err, stream);
 }
 
-int minf_layer_attn_step(float *xn, const float *h, const float *gain, float eps, int n_embd,
-                         float *q, float *k, const float *v, const int32_t *pos, int nt,
-                         float *k_reg, float *v_reg, int cap, int n_head, int n_kv_head, int hd,
-                         int hd_kv, float theta, float freq_scale, int style, float *out,
-                         void *ws, size_t ws_bytes, int32_t *err, minf_stream_t stream) {
+int minf_gqa_attn_prefill_f16(float *out, const float *q, const uint16_t *k_reg, const uint16_t *v_reg, int cap,
+                              const int32_t *pos, int nt, int n_head, int n_kv_head, int hd, int hd_kv, float scale,
+                              void *ws, size_t ws_bytes, int32_t *err, minf_stream_t stream) {
+    return gqa_attn_prefill(out, q, k_reg, v_reg, kKvF16, cap, pos, nt, n_head, n_kv_head, hd, hd_kv, scale, ws,
+                            ws_bytes, err, stream);
+}
+
+static int layer_attn_step(float *xn, const float *h, const float *gain, float eps, int n_embd,
+                           float *q, float *k, const float *v, const int32_t *pos, int nt,
+                           void *k_reg, void *v_reg, int kv, int cap, int n_head, int n_kv_head, int hd,
+                           int hd_kv, float theta, float freq_scale, int style, float *out,
+                           void *ws, size_t ws_bytes, int32_t *err, minf_stream_t stream) {
     int st = check_attn(n_head, n_kv_head, hd, hd_kv);
     if (st != MINF_OK) return st;
     if (!xn || !h || n_embd <= 0 || nt < 0 || cap <= 0 || (style != 0 && style != 1))
@@ -229,7 +285,7 @@ int minf_layer_attn_step(float *xn, const float *h, const float *gain, float eps
     if (nt == 1 && fused_step_supported(n_head, n_kv_head, hd, hd_kv, n_embd) && aligned16(h) &&
         aligned16(xn) && (!gain || aligned16(gain))) {
         // one launch: RMSNorm, RoPE on q and k, the K/V append and split-KV attention
-        DecodeArgs d = decode_args(out, q, k_reg, v_reg, nullptr, nullptr, cap, pos, 1, n_head,
+        DecodeArgs d = decode_args(out, q, k_reg, v_reg, kv, nullptr, nullptr, cap, pos, 1, n_head,
                                    n_kv_head, hd, hd_kv, scale, ws, ws_bytes, err);
         DecodeStepExtra x = {k, v, xn, h, gain, eps, theta, freq_scale, n_embd, style, true};
         return launch_decode_step(d, x, s);
@@ -237,23 +293,41 @@ int minf_layer_attn_step(float *xn, const float *h, const float *gain, float eps
     st = launch_rms_norm(xn, h, gain, nt, n_embd, eps, s);
     if (st != MINF_OK) return st;
     st = rope_kv(q, k, v, pos, nt, n_head, n_kv_head, hd, hd_kv, theta, freq_scale, style, k_reg,
-                 v_reg, nullptr, nullptr, cap, err, s);
+                 v_reg, kv, nullptr, nullptr, cap, err, s);
     if (st != MINF_OK) return st;
     if (nt == 1)
-        return decode(out, q, k_reg, v_reg, nullptr, nullptr, cap, pos, 1, n_head, n_kv_head, hd,
+        return decode(out, q, k_reg, v_reg, kv, nullptr, nullptr, cap, pos, 1, n_head, n_kv_head, hd,
                       hd_kv, scale, ws, ws_bytes, err, s);
-    return prefill(out, q, k_reg, v_reg, cap, pos, nt, n_head, n_kv_head, hd, hd_kv, scale, ws, ws_bytes,
+    return prefill(out, q, k_reg, v_reg, kv, cap, pos, nt, n_head, n_kv_head, hd, hd_kv, scale, ws, ws_bytes,
                    err, s);
 }
 
-int minf_layer_attn_step_batched(float *xn, const float *h, const float *gain, float eps,
-                                 int n_embd, float *q, float *k, const float *v,
-                                 const int32_t *pos, int n_seq, float *k_arena, float *v_arena,
-                                 const int64_t *seq_row_off, const int32_t *seq_cap, int max_cap,
-                                 int64_t arena_rows,
-                                 int n_head, int n_kv_head, int hd, int hd_kv, float theta,
-                                 float freq_scale, int style, float *out, void *ws,
-                                 size_t ws_bytes, int32_t *err, minf_stream_t stream) {
+int minf_layer_attn_step(float *xn, const float *h, const float *gain, float eps, int n_embd,
+                         float *q, float *k, const float *v, const int32_t *pos, int nt,
+                         float *k_reg, float *v_reg, int cap, int n_head, int n_kv_head, int hd,
+                         int hd_kv, float theta, float freq_scale, int style, float *out,
+                         void *ws, size_t ws_bytes, int32_t *err, minf_stream_t stream) {
+    return layer_attn_step(xn, h, gain, eps, n_embd, q, k, v, pos, nt, k_reg, v_reg, kKvF32, cap, n_head,
+                           n_kv_head, hd, hd_kv, theta, freq_scale, style, out, ws, ws_bytes, err, stream);
+}
+
+int minf_layer_attn_step_f16(float *xn, const float *h, const float *gain, float eps, int n_embd, float *q,
+                             float *k, const float *v, const int32_t *pos, int nt, uint16_t *k_reg,
+                             uint16_t *v_reg, int cap, int n_head, int n_kv_head, int hd, int hd_kv, float theta,
+                             float freq_scale, int style, float *out, void *ws, size_t ws_bytes, int32_t *err,
+                             minf_stream_t stream) {
+    return layer_attn_step(xn, h, gain, eps, n_embd, q, k, v, pos, nt, k_reg, v_reg, kKvF16, cap, n_head,
+                           n_kv_head, hd, hd_kv, theta, freq_scale, style, out, ws, ws_bytes, err, stream);
+}
+
+static int layer_attn_step_batched(float *xn, const float *h, const float *gain, float eps,
+                                   int n_embd, float *q, float *k, const float *v,
+                                   const int32_t *pos, int n_seq, void *k_arena, void *v_arena, int kv,
+                                   const int64_t *seq_row_off, const int32_t *seq_cap, int max_cap,
+                                   int64_t arena_rows,
+                                   int n_head, int n_kv_head, int hd, int hd_kv, float theta,
+                                   float freq_scale, int style, float *out, void *ws,
+                                   size_t ws_bytes, int32_t *err, minf_stream_t stream) {
     int st = check_attn(n_head, n_kv_head, hd, hd_kv);
     if (st != MINF_OK) return st;
     if (!xn || !h || n_embd <= 0 || n_seq < 0 || max_cap <= 0 || (style != 0 && style != 1))
@@ -266,7 +340,7 @@ int minf_layer_attn_step_batched(float *xn, const float *h, const float *gain, f
     const float scale = 1.0f / sqrtf(static_cast<float>(hd));
     if (fused_step_supported(n_head, n_kv_head, hd, hd_kv, n_embd) && aligned16(h) &&
         aligned16(xn) && (!gain || aligned16(gain))) {
-        DecodeArgs d = decode_args(out, q, k_arena, v_arena, seq_row_off, seq_cap, max_cap, pos,
+        DecodeArgs d = decode_args(out, q, k_arena, v_arena, kv, seq_row_off, seq_cap, max_cap, pos,
                                    n_seq, n_head, n_kv_head, hd, hd_kv, scale, ws, ws_bytes, err,
                                    arena_rows);
         DecodeStepExtra x = {k, v, xn, h, gain, eps, theta, freq_scale, n_embd, style, false};
@@ -275,10 +349,32 @@ int minf_layer_attn_step_batched(float *xn, const float *h, const float *gain, f
     st = launch_rms_norm(xn, h, gain, n_seq, n_embd, eps, s);
     if (st != MINF_OK) return st;
     st = rope_kv(q, k, v, pos, n_seq, n_head, n_kv_head, hd, hd_kv, theta, freq_scale, style,
-                 k_arena, v_arena, seq_row_off, seq_cap, max_cap, err, s);
+                 k_arena, v_arena, kv, seq_row_off, seq_cap, max_cap, err, s);
     if (st != MINF_OK) return st;
-    return decode(out, q, k_arena, v_arena, seq_row_off, seq_cap, max_cap, pos, n_seq, n_head,
+    return decode(out, q, k_arena, v_arena, kv, seq_row_off, seq_cap, max_cap, pos, n_seq, n_head,
                   n_kv_head, hd, hd_kv, scale, ws, ws_bytes, err, s, arena_rows);
+}
+
+int minf_layer_attn_step_batched(float *xn, const float *h, const float *gain, float eps, int n_embd, float *q,
+                                 float *k, const float *v, const int32_t *pos, int n_seq, float *k_arena,
+                                 float *v_arena, const int64_t *seq_row_off, const int32_t *seq_cap, int max_cap,
+                                 int64_t arena_rows, int n_head, int n_kv_head, int hd, int hd_kv, float theta,
+                                 float freq_scale, int style, float *out, void *ws, size_t ws_bytes, int32_t *err,
+                                 minf_stream_t stream) {
+    return layer_attn_step_batched(xn, h, gain, eps, n_embd, q, k, v, pos, n_seq, k_arena, v_arena, kKvF32,
+                                   seq_row_off, seq_cap, max_cap, arena_rows, n_head, n_kv_head, hd, hd_kv, theta,
+                                   freq_scale, style, out, ws, ws_bytes, err, stream);
+}
+
+int minf_layer_attn_step_batched_f16(float *xn, const float *h, const float *gain, float eps, int n_embd,
+                                     float *q, float *k, const float *v, const int32_t *pos, int n_seq,
+                                     uint16_t *k_arena, uint16_t *v_arena, const int64_t *seq_row_off,
+                                     const int32_t *seq_cap, int max_cap, int64_t arena_rows, int n_head,
+                                     int n_kv_head, int hd, int hd_kv, float theta, float freq_scale, int style,
+                                     float *out, void *ws, size_t ws_bytes, int32_t *err, minf_stream_t stream) {
+    return layer_attn_step_batched(xn, h, gain, eps, n_embd, q, k, v, pos, n_seq, k_arena, v_arena, kKvF16,
+                                   seq_row_off, seq_cap, max_cap, arena_rows, n_head, n_kv_head, hd, hd_kv, theta,
+                                   freq_scale, style, out, ws, ws_bytes, err, stream);
 }
 
 int minf_silu_mul(float *y, const float *gate, const float *up, int64_t n, minf_stream_t stream) {

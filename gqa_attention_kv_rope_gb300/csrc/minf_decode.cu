@@ -1,78 +1,14 @@
-// minf_decode.cu -- split-KV grouped-query decode attention with an online-softmax merge,
-// and the fused single-launch decode layer step built on it.
-//
-// "11 . Attention, vec ops, and the KV cache", §3.2.4 defines the result (one query per
-// sequence attends over rows [0, pos] of its kv head's cached K/V) and §2.5 names the GPU
-// shape: split the KV axis across blocks, softmax online, then reduce the splits.
-//
-// Work.  A unit is (sequence, kv-head group, split): a contiguous run of cached rows of one
-// kv head and the GH query heads of the group that read it, so every K/V byte is fetched
-// from HBM once for all those heads.  The split count S is fixed on the host from the
-// sequence count and max_cap (never from pos); each launch reads the window length from
-// device memory and cuts it into at most S runs of whole pipeline stages.  The grid is
-// persistent -- one CTA per SM takes unit blockIdx.x, then further units from a counter in
-// the workspace (a batch is ordered longest sequence first) -- so the shape never depends on
-// pos and a captured CUDA graph serves every position.
-//
-// Streaming.  Warp 8 is the producer: one lane issues TMA tensor copies of K and V tiles
-// (R rows x hd_kv, 64 KB per stage) into a 3-stage ring of shared memory, running ahead
-// across units, gated by per-stage full/empty mbarriers; with each slot it publishes the
-// slot's (unit, stage), so the consumers follow the units it drew.  Warps 0-7 consume: each
-// takes an 8-row sub-tile of the stage; 8 lanes share a K row for the dot products (three
-// butterfly steps) and each lane owns a float4 of the output for the V pass; each warp keeps
-// its own running (max, sum, acc) in the log2 domain, folded in shared memory at the end of
-// a unit.  The consumer warps synchronise on an mbarrier rather than a named barrier, so
-// that, like every other wait here, the wait is bounded.  Warp 9 (the utility warp) zeroes
-// the outputs of empty windows and flags out-of-range positions.
-//
-// Merge.  A unit writes its partial (m, l, acc) to the workspace; the last unit of a
-// (sequence, kv group) to arrive -- an atomic ticket, no spinning -- folds all partials in
-// one round trip: every consumer thread loads its share of the (m, l, acc) triples at once
-// and folds them online, then the shares are folded in shared memory; it resets the ticket.
-//
-// Fused layer step (kFused).  For one query token per sequence the same launch also does
-// the rest of the layer's attention stage: each unit rotates its q heads in registers
-// (RoPE, the same rounding as the standalone kernel), the unit whose run ends at row pos
-// rotates k, writes it back, appends the K/V row to the region and uses it from shared
-// memory, the utility warp computes the RMSNorm rows, and the last unit of a group writes
-// the rotated q back.  The loads of q, k and v are issued before anything that waits on the
-// position, so a unit's prologue costs one memory round trip.  With programmatic stream
-// serialization the producer starts streaming cached rows (which no preceding kernel
-// writes) before griddepcontrol.wait; everything the preceding kernel may produce -- q, k,
-// v, h, the workspace and its counters, the outputs -- is touched only after it.
-#include <cudaTypedefs.h>
-
-#include <cmath>
-
-#include "minf_common.cuh"
-#include "minf_kernels.h"
-#include "minf_sm103.cuh"
+// minf_decode.cu -- plans and launches the decode kernel of minf_decode.cuh: split counts,
+// the workspace layout, tensor maps, and the fp32 instantiation of the kernel.
+#include "minf_decode.cuh"
 
 namespace minf {
 
 namespace {
 
-constexpr int kNW = 8;                  // consumer warps
-constexpr int kCons = kNW * 32;         // consumer threads
-constexpr int kProducer = kNW;          // warp 8: TMA producer
-constexpr int kUtility = kNW + 1;       // warp 9: RMSNorm rows, empty windows, position flags
-constexpr int kThreads = kCons + 64;    // + producer + utility (same register budget as 9 warps)
-constexpr int kSub = 8;                 // rows per warp sub-tile
-constexpr int kNST = 3;                 // pipeline stages
-constexpr int kStageBytes = 64 * 1024;  // K + V tile of one stage
-constexpr int kGridTarget = 152;        // GB300: one persistent CTA per SM
-constexpr int kMaxSplit = 64;           // partials per (sequence, kv group)
-constexpr int kMaxRows = 4096;          // longest unit when pairs outnumber the SMs
-constexpr int kBatchMinRows = 1024;     // shortest unit worth a split when pairs outnumber the SMs
-constexpr int kMaxSort = 256;           // batches up to this many sequences are visited longest first
+using namespace dec;
 
-template <int HDKV>
-struct Cfg {
-    static constexpr int R = kStageBytes / (2 * HDKV * 4);  // rows per stage: 64 or 128
-    static constexpr int SPW = R / (kSub * kNW);            // sub-tiles per warp per stage
-};
-
-inline int stage_rows(int hd_kv) { return kStageBytes / (2 * hd_kv * 4); }
+inline int stage_rows(int hd_kv, int elem_bytes) { return kStageBytes / (2 * hd_kv * elem_bytes); }
 
 struct WsLayout {
     size_t ml_off, acc_off, ticket_off, ctr_off, total;
@@ -103,8 +39,8 @@ int heads_per_cta(int g, int hd_kv) {
 // Splits per (sequence, kv group): fill the SMs once when the pairs alone cannot; otherwise
 // (a batch) cut only long windows, into units of at most kMaxRows, since the persistent CTAs
 // take units from a shared counter, longest first.
-int choose_splits(long long pairs, int hd_kv, int max_cap) {
-    const long long R = stage_rows(hd_kv);
+int choose_splits(long long pairs, int hd_kv, int max_cap, int elem_bytes) {
+    const long long R = stage_rows(hd_kv, elem_bytes);
     long long s = pairs < kGridTarget ? kGridTarget / pairs
                                       : (static_cast<long long>(max_cap) + kMaxRows - 1) / kMaxRows;
     const long long s_rows = (static_cast<long long>(max_cap) + R - 1) / R;
@@ -114,681 +50,25 @@ int choose_splits(long long pairs, int hd_kv, int max_cap) {
     return static_cast<int>(s);
 }
 
-struct KParams {
-    float *out;
-    const float *q;
-    const int64_t *row_off;
-    const int32_t *caps;
-    const int32_t *pos;
-    int cap, n_seq, nh, nk, hd, n_split, groups;  // groups = g / GH
-    int min_rows;          // shortest unit (rows)
-    int sorted;            // visit sequences longest first
-    float scale_log2;
-    int32_t *err;
-    float *ws_ml, *ws_acc;
-    int *ws_ticket;
-    int *ws_ctr, *ws_done;  // dynamic unit counter and the count of finished producers
-    // fused layer step only
-    float *q_io, *k_io;    // rotated in place (q_io == q)
-    float *k_reg, *v_reg;  // the new row is written here
-    const float *v_new;    // [n_seq, W]
-    float *xn;             // [n_seq, n_embd]
-    const float *h, *gain;
-    float eps;
-    int n_embd, style;
-    RopeTable tab;         // angular speeds for hd (== hd_kv on the fused path)
-};
-
-__device__ __forceinline__ float4 f4scale(float4 v, float s) {
-    return make_float4(v.x * s, v.y * s, v.z * s, v.w * s);
-}
-
-__device__ __forceinline__ void rope_rot(float &x0, float &x1, float sn, float cs) {
-    const float a = __fsub_rn(__fmul_rn(x0, cs), __fmul_rn(x1, sn));
-    const float b = __fadd_rn(__fmul_rn(x0, sn), __fmul_rn(x1, cs));
-    x0 = a;
-    x1 = b;
-}
-
-__device__ __forceinline__ float &f4at(float4 &v, int e) {
-    return e == 0 ? v.x : (e == 1 ? v.y : (e == 2 ? v.z : v.w));
-}
-
-// Rotates the KF4 float4s a lane holds (dims 4*sub + 32*i, i < KF4) of one head row of
-// width HDKV with precomputed sin/cos.  Style 0 pairs float4 i with i + KF4/2 element by
-// element (dims d and d + HDKV/2); style 1 pairs (x, y) and (z, w) inside each float4.
-template <int KF4>
-__device__ __forceinline__ void rope_lane(float4 (&x)[KF4], const float (&sn)[2 * KF4],
-                                          const float (&cs)[2 * KF4], int style) {
-    if (style == 0) {
-#pragma unroll
-        for (int i = 0; i < KF4 / 2; ++i)
-#pragma unroll
-            for (int e = 0; e < 4; ++e)
-                rope_rot(f4at(x[i], e), f4at(x[i + KF4 / 2], e), sn[4 * i + e], cs[4 * i + e]);
-    } else {
-#pragma unroll
-        for (int i = 0; i < KF4; ++i) {
-            rope_rot(x[i].x, x[i].y, sn[2 * i], cs[2 * i]);
-            rope_rot(x[i].z, x[i].w, sn[2 * i + 1], cs[2 * i + 1]);
-        }
-    }
-}
-
-// Sin and cos of the pair angles a lane needs for rope_lane.  The 4 lanes of a warp with the
-// same `sub` (one per r4) need the same 2*KF4 angles, so each computes a quarter of them and
-// they are exchanged by shuffles.  Style 0: angle k is pair 4*sub + 32*(k/4) + k%4; style 1:
-// pair (4*sub + 32*(k/2))/2 + k%2 (matching rope_lane's indexing).
-template <int KF4>
-__device__ __forceinline__ void rope_angles(float (&sn)[2 * KF4], float (&cs)[2 * KF4], float pf,
-                                            const RopeTable &tab, int style, int sub, int r4) {
-    constexpr int NA = 2 * KF4;
-    constexpr int NQ = NA / 4;
-    float ms[NQ], mc[NQ];
-#pragma unroll
-    for (int q = 0; q < NQ; ++q) {
-        const int k = 4 * q + r4;
-        const int j = style == 0 ? 4 * sub + 32 * (k >> 2) + (k & 3) : (4 * sub + 32 * (k >> 1)) / 2 + (k & 1);
-        sincosf(__fmul_rn(pf, tab.f[j]), &ms[q], &mc[q]);
-    }
-#pragma unroll
-    for (int k = 0; k < NA; ++k) {
-        const int src = (k & 3) * 8 + sub;
-        sn[k] = __shfl_sync(0xffffffffu, ms[k >> 2], src);
-        cs[k] = __shfl_sync(0xffffffffu, mc[k >> 2], src);
-    }
-}
-
-struct Unit {
-    int s, y, j, p, cap_s, L, n_act, r_begin, r_end;
-    long long base;
-};
-
-// Window of sequence s: rows [0, L) with L = min(pos + 1, cap); empty for a negative position.
-__device__ __forceinline__ int window_of(const KParams &a, int s) {
-    const int p = __ldg(a.pos + s);
-    const int cap_s = a.caps ? __ldg(a.caps + s) : a.cap;
-    return p < 0 ? 0 : (p + 1 < cap_s ? p + 1 : cap_s);
-}
-
-// The unit u decodes to (sequence, pair, split) and, from the sequence's position, to the
-// run of rows it owns.  Units [0, grid) are the CTAs' first units; in a batch, where the units
-// outnumber the CTAs, the rest are drawn from the counter, sequences longest first (`order`).
-// Split j of a window of L rows covers rows [j*T, (j+1)*T) with T the smallest multiple of the
-// stage height (and at least min_rows) that cuts L into at most n_split runs; the n_act
-// active splits fill partial slots [0, n_act).  Producer and consumers derive the unit
-// identically.
-template <int R>
-__device__ __forceinline__ Unit unit_of(const KParams &a, int u, const int *order) {
-    Unit t;
-    const int P = a.nk * a.groups;
-    t.j = u % a.n_split;
-    t.y = (u / a.n_split) % P;
-    const int rank = u / (a.n_split * P);
-    t.s = order ? order[rank] : rank;
-    t.p = __ldg(a.pos + t.s);
-    t.cap_s = a.caps ? __ldg(a.caps + t.s) : a.cap;
-    t.L = t.p < 0 ? 0 : (t.p + 1 < t.cap_s ? t.p + 1 : t.cap_s);
-    int T = (t.L + a.n_split - 1) / a.n_split;
-    T = ((T + R - 1) / R) * R;
-    if (T < a.min_rows) T = a.min_rows;
-    t.n_act = t.L > 0 ? (t.L + T - 1) / T : 0;
-    t.r_begin = t.j * T;
-    t.r_end = t.j < t.n_act ? (t.r_begin + T < t.L ? t.r_begin + T : t.L) : t.r_begin;
-    t.base = a.row_off ? __ldg(a.row_off + t.s) : 0;
-    return t;
-}
-
-__device__ __forceinline__ bool unit_active(const Unit &t) { return t.r_end > t.r_begin; }
-
-// Barrier of the consumer warps, on an mbarrier so that its wait is bounded like every other
-// wait in the kernel (one elected arrival per warp; release/acquire order the shared memory).
-__device__ __forceinline__ void cons_sync(unsigned long long *bar, uint32_t &phase, volatile int *abort_flag,
-                                          int32_t *err) {
-    __syncwarp();
-    if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
-    mbar_wait(bar, phase, abort_flag, err);
-    phase ^= 1u;
-    __syncwarp();
-}
-
-template <int HDKV, int GH, bool kFused>
-__global__ void __launch_bounds__(kThreads, 1)
-    decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
-                  const KParams a) {
-    constexpr int R = Cfg<HDKV>::R, SPW = Cfg<HDKV>::SPW;
-    constexpr int KF4 = HDKV / 32;  // float4 per lane per K row (8 lanes share a row)
-    constexpr int VL = HDKV / 4;    // lanes per V row (a float4 each)
-    constexpr int VRP = 32 / VL;    // V rows a warp covers per pass
-    constexpr int VJ = kSub / VRP;  // passes per sub-tile
-    constexpr uint32_t kTileBytes = R * HDKV * 4;
-    extern __shared__ unsigned char smem_raw[];
-    // 1024-aligned ring, derived from the shared array itself so loads stay in the shared space
-    float *ring = reinterpret_cast<float *>(smem_raw + ((1024u - (su32(smem_raw) & 1023u)) & 1023u));
-    __shared__ unsigned long long full[kNST], empty[kNST], meta_full[kNST], cons_bar;
-    __shared__ int2 sm_meta[kNST];  // (unit, stage) of each ring slot; unit < 0 ends the stream
-    __shared__ int sm_order[kMaxSort];
-    __shared__ float sm_m[kNW][GH], sm_l[kNW][GH];
-    __shared__ float4 sm_acc[kNW][GH][VL];
-    __shared__ float4 sm_red[kCons];
-    __shared__ float sm_redM[kCons], sm_redL[kCons];
-    __shared__ __align__(16) float sm_knew[HDKV], sm_vnew[HDKV];
-    __shared__ int sm_last, sm_abort;
-
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int W = a.nk * HDKV;
-    const int P = a.nk * a.groups;
-    const int n_units = a.n_seq * P * a.n_split;
-    volatile int *abort_flag = &sm_abort;
-
-    if (tid == 0) {
-        for (int i = 0; i < kNST; ++i) {
-            mbar_init(&full[i], 1);
-            mbar_init(&empty[i], kNW);
-            mbar_init(&meta_full[i], 1);
-        }
-        mbar_init(&cons_bar, kNW);
-        sm_abort = 0;
-        mbar_init_fence();
-    }
-    // A batch is visited longest sequence first (positions are not written by a preceding
-    // kernel, so this runs before the dependency wait): rank = number of longer windows.
-    const int *order = nullptr;
-    if (a.sorted) {
-        for (int s = tid; s < a.n_seq; s += blockDim.x) {
-            const int Ls = window_of(a, s);
-            int rank = 0;
-            for (int o = 0; o < a.n_seq; ++o) {
-                const int Lo = window_of(a, o);
-                rank += (Lo > Ls) || (Lo == Ls && o < s);
-            }
-            sm_order[rank] = s;
-        }
-        order = sm_order;
-    }
-    __syncthreads();
-
-    if (warp == kUtility) {
-        // ---------------------------------------------------------------- utility warp
-        // RMSNorm rows ("11 . Attention, vec ops, and the KV cache", §3.2.1), spread over the
-        // CTAs; h is produced upstream, so it is read only after the dependency wait.
-        gdc_wait();
-        for (int s = blockIdx.x; kFused && s < a.n_seq; s += gridDim.x) {
-            const float *hr = a.h + static_cast<size_t>(s) * a.n_embd;
-            float *yr = a.xn + static_cast<size_t>(s) * a.n_embd;
-            const int n4 = a.n_embd >> 2;
-            float ss = 0.0f;
-            for (int i = lane; i < n4; i += 32) {
-                const float4 v = reinterpret_cast<const float4 *>(hr)[i];
-                ss = fmaf(v.x, v.x, ss);
-                ss = fmaf(v.y, v.y, ss);
-                ss = fmaf(v.z, v.z, ss);
-                ss = fmaf(v.w, v.w, ss);
-            }
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-            const float scale = 1.0f / sqrtf(ss / static_cast<float>(a.n_embd) + a.eps);
-            for (int i = lane; i < n4; i += 32) {
-                const float4 v = reinterpret_cast<const float4 *>(hr)[i];
-                const float4 g = a.gain ? reinterpret_cast<const float4 *>(a.gain)[i]
-                                        : make_float4(1.f, 1.f, 1.f, 1.f);
-                reinterpret_cast<float4 *>(yr)[i] = make_float4(v.x * scale * g.x, v.y * scale * g.y,
-                                                                v.z * scale * g.z, v.w * scale * g.w);
-            }
-        }
-        // Outputs and error bits that belong to whole sequences: a sequence with an empty
-        // window has no unit, and its output is defined as zero.
-        for (int s = blockIdx.x; s < a.n_seq; s += gridDim.x) {
-            const int p = __ldg(a.pos + s);
-            const int cap_s = a.caps ? __ldg(a.caps + s) : a.cap;
-            if (lane == 0 && (p < 0 || p >= cap_s)) {
-                int bits = MINF_ERRBIT_ATTN_POS;
-                if (kFused) bits |= MINF_ERRBIT_STORE_POS | (p < 0 ? MINF_ERRBIT_ROPE_POS : 0);
-                flag_error(a.err, bits);
-            }
-            if (p < 0)
-                for (int i = lane; i < a.nh * HDKV; i += 32) a.out[static_cast<size_t>(s) * a.nh * HDKV + i] = 0.0f;
-        }
-        return;  // writes only this kernel's own outputs: nothing a dependent launch may prefetch
-    }
-    if (warp == kProducer) {
-        // ---------------------------------------------------------------- producer
-        if (lane == 0) {
-            uint32_t it = 0;
-            bool waited = false;
-            int u = blockIdx.x;  // the first unit is this CTA's own; the rest come from a counter
-            while (u < n_units && !*abort_flag) {
-                const Unit t = unit_of<R>(a, u, order);
-                if (unit_active(t)) {
-                    const int hk = t.y / a.groups;
-                    const int n_st = (t.r_end - t.r_begin + R - 1) / R;
-                    for (int st = 0; st < n_st && !*abort_flag; ++st, ++it) {
-                        const int slot = it % kNST;
-                        if (it >= kNST) {
-                            if (!waited) {  // cached rows need no wait; reusing the ring does
-                                gdc_wait();
-                                waited = true;
-                            }
-                            if (!mbar_wait(&empty[slot], ((it / kNST) & 1) ^ 1, abort_flag, a.err)) break;
-                        }
-                        sm_meta[slot] = make_int2(u, st);
-                        mbar_arrive(&meta_full[slot]);  // publishes the slot's unit to the consumers
-                        float *kt = ring + static_cast<size_t>(slot) * (2 * R * HDKV);
-                        const int row = static_cast<int>(t.base) + t.r_begin + st * R;
-                        mbar_expect_tx(&full[slot], 2 * kTileBytes);
-                        tma_load_2d(kt, &tmK, hk * HDKV, row, &full[slot]);
-                        tma_load_2d(kt + R * HDKV, &tmV, hk * HDKV, row, &full[slot]);
-                    }
-                }
-                if (!waited) {  // the unit counter lives in the workspace a preceding launch may use
-                    gdc_wait();
-                    waited = true;
-                }
-                u = gridDim.x + atomicAdd(a.ws_ctr, 1);
-            }
-            if (!waited) gdc_wait();
-            // end of the stream for this CTA's consumers
-            const int slot = it % kNST;
-            if (it < kNST || mbar_wait(&empty[slot], ((it / kNST) & 1) ^ 1, abort_flag, a.err)) {
-                sm_meta[slot] = make_int2(-1, 0);
-                mbar_arrive(&meta_full[slot]);
-            }
-            // the last producer to finish resets the counters for the next call or graph replay
-            // (the fences order every producer's draws before its count, and the reset after)
-            __threadfence();
-            if (atomicAdd(a.ws_done, 1) == static_cast<int>(gridDim.x) - 1) {
-                __threadfence();
-                *a.ws_ctr = 0;
-                *a.ws_done = 0;
-            }
-            if (*abort_flag) {
-                // let copies already issued land before the CTA's shared memory goes away
-                for (uint32_t k = it > kNST ? it - kNST : 0; k < it; ++k)
-                    if (!mbar_try(&full[k % kNST], (k / kNST) & 1)) {
-                        const unsigned long long t0 = gtimer();
-                        while (!mbar_try(&full[k % kNST], (k / kNST) & 1) && gtimer() - t0 < kWaitBudgetNs) {
-                        }
-                    }
-            }
-        }
-        return;  // the producer never releases dependents: only consumers know the rows are written
-    }
-
-    // -------------------------------------------------------------------- consumers
-    // A dependent launch may start streaming cached rows before its own wait, so release it only
-    // once every row this CTA appends is in memory.  The run that ends at the window's last row
-    // appends; when every unit is a first unit, a CTA releases right after its append (or at
-    // once), otherwise when it is done.
-    const bool early = n_units <= static_cast<int>(gridDim.x);
-    bool released = false;
-    const int r4 = lane >> 3, sub = lane & 7;
-    const int vrow = lane / VL, vcol = lane % VL;
-    const float sl = a.scale_log2;
-    uint32_t cphase = 0;
-    uint32_t it = 0;  // ring stage counter, in step with the producer's
-    // The first unit is this CTA's own and needs no word from the producer; its position is
-    // read before the dependency wait (no preceding kernel writes positions).
-    Unit t = unit_of<R>(a, blockIdx.x, order);
-    bool have = unit_active(t);
-    gdc_wait();
-    if (early && !(kFused && have && t.r_end == t.L)) {
-        gdc_launch_dependents();  // this CTA appends no row
-        released = true;
-    }
-    while (true) {
-        if (!have) {
-            // the producer publishes the unit it drew with the unit's first stage
-            const int slot = it % kNST;
-            if (!mbar_wait(&meta_full[slot], (it / kNST) & 1, abort_flag, a.err)) break;
-            const int u = sm_meta[slot].x;
-            if (u < 0) break;
-            t = unit_of<R>(a, u, order);
-        }
-        have = false;
-        // -------------------------------------------------------------- start of a unit
-        const int hk = t.y / a.groups;
-        const int h0 = hk * (a.nh / a.nk) + (t.y % a.groups) * GH;  // first query head
-        const int n_st = (t.r_end - t.r_begin + R - 1) / R;
-        float4 qr[GH][KF4];
-#pragma unroll
-        for (int hh = 0; hh < GH; ++hh) {
-            const float4 *qh =
-                reinterpret_cast<const float4 *>(a.q + (static_cast<size_t>(t.s) * a.nh + h0 + hh) * a.hd);
-#pragma unroll
-            for (int i = 0; i < KF4; ++i) qr[hh][i] = qh[sub + 8 * i];
-        }
-        // The unit whose run ends at the window's last row owns k: it rotates it, writes it back
-        // and, when the row fits the region, appends the new K/V row and puts it, from shared
-        // memory, in place of what its tile copy read (no other unit reads k).
-        const bool k_writer = kFused && t.r_end == t.L;
-        const int pnew = k_writer && t.p < t.cap_s ? t.p : -1;
-        if (kFused) {
-            float sn[2 * KF4], cs[2 * KF4];
-            rope_angles<KF4>(sn, cs, static_cast<float>(t.p), a.tab, a.style, sub, r4);
-#pragma unroll
-            for (int hh = 0; hh < GH; ++hh) rope_lane<KF4>(qr[hh], sn, cs, a.style);
-            if (k_writer && warp == 0 && r4 == 0) {
-                float4 *kh = reinterpret_cast<float4 *>(a.k_io + (static_cast<size_t>(t.s) * a.nk + hk) * HDKV);
-                const float4 *vh = reinterpret_cast<const float4 *>(a.v_new + static_cast<size_t>(t.s) * W + hk * HDKV);
-                float4 kx[KF4], vx[KF4];
-#pragma unroll
-                for (int i = 0; i < KF4; ++i) {
-                    kx[i] = kh[sub + 8 * i];
-                    vx[i] = vh[sub + 8 * i];
-                }
-                rope_lane<KF4>(kx, sn, cs, a.style);
-#pragma unroll
-                for (int i = 0; i < KF4; ++i) kh[sub + 8 * i] = kx[i];
-                if (pnew >= 0) {
-                    float *Kg = a.k_reg + (t.base + t.p) * W + hk * HDKV;
-                    float *Vg = a.v_reg + (t.base + t.p) * W + hk * HDKV;
-#pragma unroll
-                    for (int i = 0; i < KF4; ++i) {
-                        // staged for the same lanes, which patch the row's stage when it arrives
-                        reinterpret_cast<float4 *>(sm_knew)[sub + 8 * i] = kx[i];
-                        reinterpret_cast<float4 *>(sm_vnew)[sub + 8 * i] = vx[i];
-                        reinterpret_cast<float4 *>(Kg)[sub + 8 * i] = kx[i];
-                        reinterpret_cast<float4 *>(Vg)[sub + 8 * i] = vx[i];
-                    }
-                }
-            }
-            if (early && !released) {  // this first unit is the appending one
-                // the appended row is in memory before the dependent launch is released; one
-                // thread's trigger releases the CTA, so the warp that wrote the row triggers
-                if (warp == 0) {
-                    if (pnew >= 0) __threadfence();
-                    __syncwarp();
-                    if (lane == 0) gdc_launch_dependents();
-                }
-                released = true;
-            }
-        }
-        float m[GH], l[GH];
-        float4 acc[GH];
-#pragma unroll
-        for (int hh = 0; hh < GH; ++hh) {
-            m[hh] = -INFINITY;
-            l[hh] = 0.0f;
-            acc[hh] = make_float4(0.f, 0.f, 0.f, 0.f);
-        }
-
-        // -------------------------------------------------------------- the unit's stages
-        for (int st = 0; st < n_st; ++st, ++it) {
-            const int slot = it % kNST;
-            mbar_wait(&full[slot], (it / kNST) & 1, abort_flag, a.err);
-            float *Ks = ring + static_cast<size_t>(slot) * (2 * R * HDKV);
-            float *Vs = Ks + R * HDKV;
-            const int row0 = t.r_begin + st * R;
-            if (kFused && pnew >= row0 && pnew < row0 + R) {
-                // the tile may hold the row as it was before this launch appended it: the lanes
-                // that staged the new row put it in its place (and hand the slot back to the
-                // async proxy in order)
-                if (warp == 0 && r4 == 0) {
-                    const int rn = pnew - row0;
-#pragma unroll
-                    for (int i = 0; i < KF4; ++i) {
-                        reinterpret_cast<float4 *>(Ks + rn * HDKV)[sub + 8 * i] =
-                            reinterpret_cast<const float4 *>(sm_knew)[sub + 8 * i];
-                        reinterpret_cast<float4 *>(Vs + rn * HDKV)[sub + 8 * i] =
-                            reinterpret_cast<const float4 *>(sm_vnew)[sub + 8 * i];
-                    }
-                    fence_async_smem();
-                }
-                cons_sync(&cons_bar, cphase, abort_flag, a.err);
-            }
-#pragma unroll
-            for (int sp = 0; sp < SPW; ++sp) {
-                const int rr0 = (warp * SPW + sp) * kSub;  // sub-tile's first row within the stage
-                float4 kv[2][KF4];
-                float4 vv[VJ];
-#pragma unroll
-                for (int it2 = 0; it2 < 2; ++it2) {
-                    const int rr = rr0 + 4 * it2 + r4;
-                    const float4 *src = reinterpret_cast<const float4 *>(Ks + rr * HDKV);
-#pragma unroll
-                    for (int i = 0; i < KF4; ++i) kv[it2][i] = src[sub + 8 * i];
-                }
-#pragma unroll
-                for (int jv = 0; jv < VJ; ++jv) {
-                    const int rr = rr0 + vrow + VRP * jv;
-                    const int row = row0 + rr;
-                    vv[jv] = row < t.r_end ? reinterpret_cast<const float4 *>(Vs + rr * HDKV)[vcol]
-                                           : make_float4(0.f, 0.f, 0.f, 0.f);  // past the run: anything
-                }
-                float pr[2][GH];
-#pragma unroll
-                for (int hh = 0; hh < GH; ++hh) {
-                    float sc[2];
-#pragma unroll
-                    for (int it2 = 0; it2 < 2; ++it2) {
-                        float d = 0.0f;
-#pragma unroll
-                        for (int i = 0; i < KF4; ++i) {
-                            d = fmaf(qr[hh][i].x, kv[it2][i].x, d);
-                            d = fmaf(qr[hh][i].y, kv[it2][i].y, d);
-                            d = fmaf(qr[hh][i].z, kv[it2][i].z, d);
-                            d = fmaf(qr[hh][i].w, kv[it2][i].w, d);
-                        }
-                        d += __shfl_xor_sync(0xffffffffu, d, 1);
-                        d += __shfl_xor_sync(0xffffffffu, d, 2);
-                        d += __shfl_xor_sync(0xffffffffu, d, 4);
-                        sc[it2] = (row0 + rr0 + 4 * it2 + r4) < t.r_end ? d * sl : -INFINITY;
-                    }
-                    float mx = fmaxf(sc[0], sc[1]);
-                    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
-                    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
-                    const float m_new = fmaxf(m[hh], mx);
-                    // a sub-tile wholly past the run leaves the state untouched
-                    const bool none = (m_new == -INFINITY);
-                    const float corr = none ? 1.0f : ex2_approx(m[hh] - m_new);
-                    pr[0][hh] = none ? 0.0f : ex2_approx(sc[0] - m_new);
-                    pr[1][hh] = none ? 0.0f : ex2_approx(sc[1] - m_new);
-                    float ps = pr[0][hh] + pr[1][hh];
-                    ps += __shfl_xor_sync(0xffffffffu, ps, 8);
-                    ps += __shfl_xor_sync(0xffffffffu, ps, 16);
-                    l[hh] = fmaf(l[hh], corr, ps);
-                    acc[hh] = f4scale(acc[hh], corr);
-                    m[hh] = m_new;
-                }
-#pragma unroll
-                for (int jv = 0; jv < VJ; ++jv) {
-                    const int rl = vrow + VRP * jv;  // row within the sub-tile, 0..7
-                    const int it2 = (VRP * jv) / 4;  // the same for every lane of the pass
-                    const int src = (rl & 3) * 8;
-#pragma unroll
-                    for (int hh = 0; hh < GH; ++hh) {
-                        const float w = __shfl_sync(0xffffffffu, it2 ? pr[1][hh] : pr[0][hh], src);
-                        acc[hh].x = fmaf(w, vv[jv].x, acc[hh].x);
-                        acc[hh].y = fmaf(w, vv[jv].y, acc[hh].y);
-                        acc[hh].z = fmaf(w, vv[jv].z, acc[hh].z);
-                        acc[hh].w = fmaf(w, vv[jv].w, acc[hh].w);
-                    }
-                }
-            }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&empty[slot]);
-        }
-
-        // ------------------------------------------------------------ end of the unit
-        cons_sync(&cons_bar, cphase, abort_flag, a.err);  // the previous unit's scratch readers are done
-#pragma unroll
-        for (int hh = 0; hh < GH; ++hh) {
-#pragma unroll
-            for (int o = VL; o < 32; o <<= 1) {
-                acc[hh].x += __shfl_xor_sync(0xffffffffu, acc[hh].x, o);
-                acc[hh].y += __shfl_xor_sync(0xffffffffu, acc[hh].y, o);
-                acc[hh].z += __shfl_xor_sync(0xffffffffu, acc[hh].z, o);
-                acc[hh].w += __shfl_xor_sync(0xffffffffu, acc[hh].w, o);
-            }
-            if (lane < VL) sm_acc[warp][hh][lane] = acc[hh];
-            if (lane == 0) {
-                sm_m[warp][hh] = m[hh];
-                sm_l[warp][hh] = l[hh];
-            }
-        }
-        cons_sync(&cons_bar, cphase, abort_flag, a.err);
-        float *out_s = a.out + (static_cast<size_t>(t.s) * a.nh + h0) * HDKV;
-        const size_t part0 = (static_cast<size_t>(t.s) * a.nh + h0) * a.n_split;  // head h0, split 0
-        for (int i = tid; i < GH * VL; i += kCons) {
-            const int hh = i / VL, c = i % VL;
-            float M = sm_m[0][hh];
-#pragma unroll
-            for (int w = 1; w < kNW; ++w) M = fmaxf(M, sm_m[w][hh]);
-            float Ls = 0.0f;
-            float4 A = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-            for (int w = 0; w < kNW; ++w) {
-                const float f = sm_m[w][hh] == -INFINITY ? 0.0f : ex2_approx(sm_m[w][hh] - M);
-                Ls = fmaf(sm_l[w][hh], f, Ls);
-                const float4 x = sm_acc[w][hh][c];
-                A.x = fmaf(x.x, f, A.x);
-                A.y = fmaf(x.y, f, A.y);
-                A.z = fmaf(x.z, f, A.z);
-                A.w = fmaf(x.w, f, A.w);
-            }
-            if (t.n_act == 1) {
-                reinterpret_cast<float4 *>(out_s + hh * HDKV)[c] = f4scale(A, 1.0f / Ls);
-            } else {
-                const size_t part = part0 + static_cast<size_t>(hh) * a.n_split + t.j;
-                if (c == 0) {
-                    a.ws_ml[2 * part] = M;
-                    a.ws_ml[2 * part + 1] = Ls;
-                }
-                reinterpret_cast<float4 *>(a.ws_acc + part * HDKV)[c] = A;
-            }
-        }
-
-        bool last = true;
-        int *ticket = a.ws_ticket + static_cast<size_t>(t.s) * P + t.y;
-        if (t.n_act > 1) {
-            cons_sync(&cons_bar, cphase, abort_flag, a.err);
-            if (tid == 0) {
-                // acq_rel: publishes this CTA's partials (ordered before it by the barrier) and,
-                // for the last arrival, makes every other unit's partials visible to its loads
-                int old;
-                asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], 1;" : "=r"(old) : "l"(ticket) : "memory");
-                sm_last = old == t.n_act - 1;
-            }
-            cons_sync(&cons_bar, cphase, abort_flag, a.err);
-            last = sm_last;
-        }
-        if (!last) continue;
-
-        if (t.n_act > 1) {
-            // One round trip for the merge: each thread folds its share of the splits online
-            // (running max and rescaled sums), then the shares are folded in shared memory.
-            constexpr int kPairs = GH * VL;
-            constexpr int kWays = kCons / kPairs > 0 ? kCons / kPairs : 1;
-            for (int i = tid; i < kPairs * kWays; i += kCons) {
-                const int pair = i % kPairs, way = i / kPairs;
-                const int hh = pair / VL, c = pair % VL;
-                const size_t ph2 = part0 + static_cast<size_t>(hh) * a.n_split;
-                float M = -INFINITY, Ls = 0.0f;
-                float4 A = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 8
-                for (int j = way; j < t.n_act; j += kWays) {
-                    const float2 ml = __ldcg(reinterpret_cast<const float2 *>(a.ws_ml) + (ph2 + j));
-                    const float4 x = __ldcg(reinterpret_cast<const float4 *>(a.ws_acc + (ph2 + j) * HDKV) + c);
-                    const float Mn = fmaxf(M, ml.x);
-                    const float fo = M == -INFINITY ? 0.0f : ex2_approx(M - Mn);
-                    const float fn = ex2_approx(ml.x - Mn);
-                    A = make_float4(fmaf(x.x, fn, A.x * fo), fmaf(x.y, fn, A.y * fo), fmaf(x.z, fn, A.z * fo),
-                                    fmaf(x.w, fn, A.w * fo));
-                    Ls = fmaf(ml.y, fn, Ls * fo);
-                    M = Mn;
-                }
-                sm_red[way * kPairs + pair] = A;
-                sm_redM[way * kPairs + pair] = M;
-                sm_redL[way * kPairs + pair] = Ls;
-            }
-            cons_sync(&cons_bar, cphase, abort_flag, a.err);
-            for (int i = tid; i < kPairs; i += kCons) {
-                const int hh = i / VL, c = i % VL;
-                float M = sm_redM[i];
-                for (int w = 1; w < kWays; ++w) M = fmaxf(M, sm_redM[w * kPairs + i]);
-                float Ls = 0.0f;
-                float4 A = make_float4(0.f, 0.f, 0.f, 0.f);
-                for (int w = 0; w < kWays; ++w) {
-                    const float mw = sm_redM[w * kPairs + i];
-                    const float f = mw == -INFINITY ? 0.0f : ex2_approx(mw - M);
-                    const float4 x = sm_red[w * kPairs + i];
-                    A = make_float4(fmaf(x.x, f, A.x), fmaf(x.y, f, A.y), fmaf(x.z, f, A.z), fmaf(x.w, f, A.w));
-                    Ls = fmaf(sm_redL[w * kPairs + i], f, Ls);
-                }
-                reinterpret_cast<float4 *>(out_s + hh * HDKV)[c] = f4scale(A, 1.0f / Ls);
-            }
-            if (tid == 0) *ticket = 0;  // ready for the next call or graph replay
-        }
-        if (kFused && lane < 8) {
-            // every other unit of this group has finished reading q: write it back rotated
-#pragma unroll
-            for (int hh = 0; hh < GH; ++hh) {
-                if (hh % kNW != warp) continue;
-                float4 *qh = reinterpret_cast<float4 *>(a.q_io + (static_cast<size_t>(t.s) * a.nh + h0 + hh) * a.hd);
-#pragma unroll
-                for (int i = 0; i < KF4; ++i) qh[lane + 8 * i] = qr[hh][i];
-            }
-        }
-    }
-    if (!released) gdc_launch_dependents();
-}
-
-template <int HDKV, int GH, bool kFused>
-cudaError_t launch_t(const CUtensorMap &tk, const CUtensorMap &tv, const KParams &k, int grid, cudaStream_t s,
-                     bool pdl) {
-    const size_t smem = static_cast<size_t>(kNST) * kStageBytes + 1024;
-    static bool attr_set = false;
-    if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(decode_kernel<HDKV, GH, kFused>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-        if (e != cudaSuccess) return e;
-        attr_set = true;
-    }
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(grid);
-    cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = pdl ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, decode_kernel<HDKV, GH, kFused>, tk, tv, k);
-}
-
-template <int HDKV, bool kFused>
-cudaError_t dispatch_gh(int gh, const CUtensorMap &tk, const CUtensorMap &tv, const KParams &k, int grid,
-                        cudaStream_t s, bool pdl) {
-    switch (gh) {
-        case 1: return launch_t<HDKV, 1, kFused>(tk, tv, k, grid, s, pdl);
-        case 2: return launch_t<HDKV, 2, kFused>(tk, tv, k, grid, s, pdl);
-        case 3: return launch_t<HDKV, 3, kFused>(tk, tv, k, grid, s, pdl);
-        case 4: return launch_t<HDKV, 4, kFused>(tk, tv, k, grid, s, pdl);
-        case 5: return launch_t<HDKV, 5, kFused>(tk, tv, k, grid, s, pdl);
-        case 6: return launch_t<HDKV, 6, kFused>(tk, tv, k, grid, s, pdl);
-        case 7: return launch_t<HDKV, 7, kFused>(tk, tv, k, grid, s, pdl);
-        case 8: return launch_t<HDKV, 8, kFused>(tk, tv, k, grid, s, pdl);
-        default: return cudaErrorInvalidValue;
-    }
-}
-
 struct Plan {
     int gh, groups, S, min_rows, sorted;
     WsLayout w;
 };
 
-Plan plan_for(int n_seq, int nh, int nk, int hd_kv, int max_cap) {
+// elem_bytes: 4 for fp32 regions, 2 for binary16 (whose stages hold twice the rows).  The
+// workspace is laid out for fp32's split count, which is never below binary16's, so one
+// workspace size serves both storage types.
+Plan plan_for(int n_seq, int nh, int nk, int hd_kv, int max_cap, int elem_bytes) {
     Plan p;
     const int g = nh / nk;
     p.gh = heads_per_cta(g, hd_kv);
     p.groups = g / p.gh;
     const long long pairs = static_cast<long long>(n_seq) * nk * p.groups;
-    p.S = choose_splits(pairs, hd_kv, max_cap);
+    p.S = choose_splits(pairs, hd_kv, max_cap, elem_bytes);
     const bool batch = pairs >= kGridTarget;
-    p.min_rows = batch ? kBatchMinRows : stage_rows(hd_kv);
+    p.min_rows = batch ? kBatchMinRows : stage_rows(hd_kv, elem_bytes);
     p.sorted = batch && n_seq > 1 && n_seq <= kMaxSort;
-    p.w = ws_layout(n_seq, nh, nk * p.groups, hd_kv, p.S);
+    p.w = ws_layout(n_seq, nh, nk * p.groups, hd_kv, choose_splits(pairs, hd_kv, max_cap, 4));
     return p;
 }
 
@@ -807,18 +87,21 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 
 int launch_impl(const DecodeArgs &d, const DecodeStepExtra *x, cudaStream_t s) {
     if (d.n_seq == 0) return MINF_OK;
-    const Plan pl = plan_for(d.n_seq, d.nh, d.nk, d.hd_kv, d.cap);
+    const bool f16 = d.kv == kKvF16;
+    const int eb = f16 ? 2 : 4;
+    const Plan pl = plan_for(d.n_seq, d.nh, d.nk, d.hd_kv, d.cap, eb);
     if (!d.ws || d.ws_bytes < pl.w.total || !aligned16(d.ws)) return MINF_ERR_WORKSPACE;
     const long long units = static_cast<long long>(d.n_seq) * d.nk * pl.groups * pl.S;
     if (units > 0x7fffffffLL) return MINF_ERR_UNSUPPORTED;
     const long long rows = d.row_off ? d.arena_rows : d.cap;
     if (rows <= 0) return MINF_ERR_ARG;
     if (rows > 0x7fffffffLL) return MINF_ERR_UNSUPPORTED;
-    const int R = stage_rows(d.hd_kv);
+    const int R = stage_rows(d.hd_kv, eb);
     CUtensorMap tk, tv;
     const uint64_t W = static_cast<uint64_t>(d.nk) * d.hd_kv;
-    if (!make_tensor_map_2d(&tk, d.k_reg, W, static_cast<uint64_t>(rows), d.hd_kv, R, false) ||
-        !make_tensor_map_2d(&tv, d.v_reg, W, static_cast<uint64_t>(rows), d.hd_kv, R, false))
+    const CUtensorMapDataType dt = f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+    if (!make_tensor_map_2d(&tk, d.k_reg, dt, eb, W, static_cast<uint64_t>(rows), d.hd_kv, R, false) ||
+        !make_tensor_map_2d(&tv, d.v_reg, dt, eb, W, static_cast<uint64_t>(rows), d.hd_kv, R, false))
         return MINF_ERR_CUDA;
     char *ws = static_cast<char *>(d.ws);
     KParams k = {};
@@ -843,8 +126,8 @@ int launch_impl(const DecodeArgs &d, const DecodeStepExtra *x, cudaStream_t s) {
     k.ws_done = k.ws_ctr + 1;
     k.min_rows = pl.min_rows;
     k.sorted = pl.sorted;
-    k.k_reg = const_cast<float *>(d.k_reg);
-    k.v_reg = const_cast<float *>(d.v_reg);
+    k.k_reg = const_cast<void *>(d.k_reg);
+    k.v_reg = const_cast<void *>(d.v_reg);
     bool pdl = false;
     if (x) {
         k.q_io = const_cast<float *>(d.q);
@@ -861,28 +144,23 @@ int launch_impl(const DecodeArgs &d, const DecodeStepExtra *x, cudaStream_t s) {
     }
     const int sms = sm_count();
     const int grid = static_cast<int>(units < sms ? units : sms);
-    cudaError_t e;
-    if (x)
-        e = d.hd_kv == 64 ? dispatch_gh<64, true>(pl.gh, tk, tv, k, grid, s, pdl)
-                          : dispatch_gh<128, true>(pl.gh, tk, tv, k, grid, s, pdl);
-    else
-        e = d.hd_kv == 64 ? dispatch_gh<64, false>(pl.gh, tk, tv, k, grid, s, pdl)
-                          : dispatch_gh<128, false>(pl.gh, tk, tv, k, grid, s, pdl);
+    const cudaError_t e = f16 ? dispatch_decode_f16(d.hd_kv, x != nullptr, pl.gh, tk, tv, k, grid, s, pdl)
+                              : dispatch<float>(d.hd_kv, x != nullptr, pl.gh, tk, tv, k, grid, s, pdl);
     if (e == cudaErrorInvalidValue) return MINF_ERR_UNSUPPORTED;
     return e == cudaSuccess ? MINF_OK : MINF_ERR_CUDA;
 }
 
 }  // namespace
 
-bool make_tensor_map_2d(CUtensorMap *m, const float *base, uint64_t cols, uint64_t rows, uint32_t box_cols,
-                        uint32_t box_rows, bool swizzle128) {
+bool make_tensor_map_2d(CUtensorMap *m, const void *base, CUtensorMapDataType dt, uint32_t elem_bytes, uint64_t cols,
+                        uint64_t rows, uint32_t box_cols, uint32_t box_rows, bool swizzle128) {
     auto fn = encode_fn();
     if (!fn) return false;
     cuuint64_t dims[2] = {cols, rows};
-    cuuint64_t strides[1] = {cols * 4};
+    cuuint64_t strides[1] = {cols * elem_bytes};
     cuuint32_t box[2] = {box_cols, box_rows};
     cuuint32_t estr[2] = {1, 1};
-    return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float *>(base), dims, strides, box, estr,
+    return fn(m, dt, 2, const_cast<void *>(base), dims, strides, box, estr,
               CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -902,7 +180,7 @@ bool fused_step_supported(int nh, int nk, int hd, int hd_kv, int n_embd) {
 
 size_t decode_workspace_bytes(int n_seq, int nh, int nk, int hd_kv, int max_cap) {
     if (n_seq <= 0 || nh <= 0 || nk <= 0 || hd_kv <= 0 || max_cap <= 0 || nh % nk) return 0;
-    return plan_for(n_seq, nh, nk, hd_kv, max_cap).w.total;
+    return plan_for(n_seq, nh, nk, hd_kv, max_cap, 4).w.total;  // the layout serves both storage types
 }
 
 int launch_decode(const DecodeArgs &d, cudaStream_t s) { return launch_impl(d, nullptr, s); }

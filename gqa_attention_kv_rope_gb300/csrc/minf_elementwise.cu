@@ -3,12 +3,27 @@
 // These are memory-bound passes over short rows.  They use 128-bit loads where
 // the row width allows and one thread per independent element (or per rotated
 // pair), so every launch is a single coalesced sweep over its bytes.
+#include <cuda_fp16.h>
+
 #include <cmath>
 
 #include "minf_common.cuh"
 #include "minf_kernels.h"
 
 namespace minf {
+
+// Region elements: fp32 as is, binary16 converted with round to nearest even ("11 . Attention,
+// vec ops, and the KV cache", §2.5: the GPU backends may keep the K/V regions in f16).
+__device__ __forceinline__ void put1(float *p, size_t i, float v) { p[i] = v; }
+__device__ __forceinline__ void put1(__half *p, size_t i, float v) { p[i] = __float2half_rn(v); }
+__device__ __forceinline__ void put4(float *p, size_t i4, float4 v) { reinterpret_cast<float4 *>(p)[i4] = v; }
+__device__ __forceinline__ void put4(__half *p, size_t i4, float4 v) {
+    const __half2 a = __floats2half2_rn(v.x, v.y), b = __floats2half2_rn(v.z, v.w);
+    uint2 u;
+    u.x = *reinterpret_cast<const uint32_t *>(&a);
+    u.y = *reinterpret_cast<const uint32_t *>(&b);
+    reinterpret_cast<uint2 *>(p)[i4] = u;
+}
 
 void rope_table(RopeTable *t, int hd, float theta, float freq_scale) {
     // "11 . Attention, vec ops, and the KV cache", §2.3/§3.2.2: the angular speed of
@@ -156,7 +171,8 @@ int launch_rope(float *x, const int32_t *pos, int nt, int nh, int hd, float thet
 // ----------------------------------------------------------------------------- KV store
 // "11 . Attention, vec ops, and the KV cache", §3.2.3: row pos[t] of each region gets the
 // token's row, a plain copy; an out-of-range position is reported and never written.
-__global__ void __launch_bounds__(256) kv_append_kernel(float *k_reg, float *v_reg, int cap, int W,
+template <typename T>
+__global__ void __launch_bounds__(256) kv_append_kernel(T *k_reg, T *v_reg, int cap, int W,
                                                         const float *k_rows, const float *v_rows,
                                                         const int32_t *pos, int nt, int32_t *err) {
     const int w4 = W >> 2;
@@ -172,18 +188,22 @@ __global__ void __launch_bounds__(256) kv_append_kernel(float *k_reg, float *v_r
         }
         const size_t src = static_cast<size_t>(t) * w4 + c;
         const size_t dst = static_cast<size_t>(p) * w4 + c;
-        reinterpret_cast<float4 *>(k_reg)[dst] = reinterpret_cast<const float4 *>(k_rows)[src];
-        reinterpret_cast<float4 *>(v_reg)[dst] = reinterpret_cast<const float4 *>(v_rows)[src];
+        put4(k_reg, dst, reinterpret_cast<const float4 *>(k_rows)[src]);
+        put4(v_reg, dst, reinterpret_cast<const float4 *>(v_rows)[src]);
     }
 }
 
-int launch_kv_append(float *k_reg, float *v_reg, int cap, int W, const float *k_rows,
+int launch_kv_append(void *k_reg, void *v_reg, int kv, int cap, int W, const float *k_rows,
                      const float *v_rows, const int32_t *pos, int nt, int32_t *err,
                      cudaStream_t s) {
     if (nt == 0) return MINF_OK;
     const long long work = static_cast<long long>(nt) * (W / 4);
-    kv_append_kernel<<<grid_for(work, 256), 256, 0, s>>>(k_reg, v_reg, cap, W, k_rows, v_rows, pos,
-                                                          nt, err);
+    if (kv == kKvF16)
+        kv_append_kernel<<<grid_for(work, 256), 256, 0, s>>>(static_cast<__half *>(k_reg), static_cast<__half *>(v_reg),
+                                                              cap, W, k_rows, v_rows, pos, nt, err);
+    else
+        kv_append_kernel<<<grid_for(work, 256), 256, 0, s>>>(static_cast<float *>(k_reg), static_cast<float *>(v_reg),
+                                                              cap, W, k_rows, v_rows, pos, nt, err);
     return cudaPeekAtLastError() == cudaSuccess ? MINF_OK : MINF_ERR_CUDA;
 }
 
@@ -191,6 +211,7 @@ int launch_kv_append(float *k_reg, float *v_reg, int cap, int W, const float *k_
 // One sweep per token over three kinds of work item: a q pair, a k pair (rotated, written
 // back in place and into the K region), and a float4 of v (copied into the V region).
 // Batched callers give each token its own arena offset and capacity.
+template <typename T>
 __global__ void __launch_bounds__(256) rope_kv_append_kernel(RopeKvArgs a, const RopeTable tq,
                                                              const RopeTable tk) {
     const int hq = a.hd >> 1, hk = a.hd_kv >> 1;
@@ -227,9 +248,9 @@ __global__ void __launch_bounds__(256) rope_kv_append_kernel(RopeKvArgs a, const
             row[i0] = x0;
             row[i1] = x1;
             if (store_ok) {
-                float *dst = a.k_reg + (static_cast<size_t>(base) + p) * W + h * a.hd_kv;
-                dst[i0] = x0;
-                dst[i1] = x1;
+                T *dst = static_cast<T *>(a.k_reg) + (static_cast<size_t>(base) + p) * W + h * a.hd_kv;
+                put1(dst, i0, x0);
+                put1(dst, i1, x1);
             }
             continue;
         }
@@ -239,7 +260,7 @@ __global__ void __launch_bounds__(256) rope_kv_append_kernel(RopeKvArgs a, const
             continue;
         }
         const float4 v = reinterpret_cast<const float4 *>(a.v)[static_cast<size_t>(t) * nv + r];
-        reinterpret_cast<float4 *>(a.v_reg)[(static_cast<size_t>(base) + p) * nv + r] = v;
+        put4(static_cast<T *>(a.v_reg), (static_cast<size_t>(base) + p) * nv + r, v);
     }
 }
 
@@ -250,7 +271,10 @@ int launch_rope_kv_append(const RopeKvArgs &a, float theta, float freq_scale, cu
     rope_table(&tk, a.hd_kv, theta, freq_scale);
     const long long per_tok =
         static_cast<long long>(a.nh) * (a.hd / 2) + a.nk * (a.hd_kv / 2) + a.nk * a.hd_kv / 4;
-    rope_kv_append_kernel<<<grid_for(per_tok * a.nt, 256), 256, 0, s>>>(a, tq, tk);
+    if (a.kv == kKvF16)
+        rope_kv_append_kernel<__half><<<grid_for(per_tok * a.nt, 256), 256, 0, s>>>(a, tq, tk);
+    else
+        rope_kv_append_kernel<float><<<grid_for(per_tok * a.nt, 256), 256, 0, s>>>(a, tq, tk);
     return cudaPeekAtLastError() == cudaSuccess ? MINF_OK : MINF_ERR_CUDA;
 }
 

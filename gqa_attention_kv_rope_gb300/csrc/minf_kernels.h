@@ -7,12 +7,17 @@
 
 namespace minf {
 
+// Storage of the K/V regions: fp32, or IEEE binary16 (converted on the store with round to
+// nearest even, read back exactly; the arithmetic stays fp32).
+enum KvKind : int { kKvF32 = 0, kKvF16 = 1 };
+
 struct RopeKvArgs {
     float *q;               // [nt, nh, hd], rotated in place
     float *k;               // [nt, nk, hd_kv], rotated in place
     const float *v;         // [nt, nk*hd_kv]
     const int32_t *pos;     // [nt]
-    float *k_reg, *v_reg;   // regions / arena [rows, nk*hd_kv]
+    void *k_reg, *v_reg;    // regions / arena [rows, nk*hd_kv] of `kv` elements
+    int kv;                 // KvKind
     const int64_t *row_off; // per token arena row offset (nullable: 0)
     const int32_t *caps;    // per token capacity (nullable: cap)
     int cap;
@@ -23,7 +28,8 @@ struct RopeKvArgs {
 struct DecodeArgs {
     float *out;              // [n_seq, nh*hd_kv]
     const float *q;          // [n_seq, nh, hd]
-    const float *k_reg, *v_reg;
+    const void *k_reg, *v_reg;  // of `kv` elements
+    int kv;                  // KvKind
     const int64_t *row_off;  // per sequence (nullable)
     const int32_t *caps;     // per sequence (nullable)
     int cap;                 // capacity when caps is null; also the host bound max_cap
@@ -40,7 +46,7 @@ int launch_rms_norm(float *y, const float *x, const float *w, int rows, int n, f
                     cudaStream_t s);
 int launch_rope(float *x, const int32_t *pos, int nt, int nh, int hd, float theta,
                 float freq_scale, int style, int32_t *err, cudaStream_t s);
-int launch_kv_append(float *k_reg, float *v_reg, int cap, int W, const float *k_rows,
+int launch_kv_append(void *k_reg, void *v_reg, int kv, int cap, int W, const float *k_rows,
                      const float *v_rows, const int32_t *pos, int nt, int32_t *err,
                      cudaStream_t s);
 int launch_rope_kv_append(const RopeKvArgs &a, float theta, float freq_scale, cudaStream_t s);
@@ -60,7 +66,8 @@ struct DecodeStepExtra {
 struct PrefillArgs {
     float *out;               // [nt, nh*hd_kv]
     const float *q;           // [nt, nh, hd] (rotated)
-    const float *k_reg, *v_reg;  // regions [cap, nk*hd_kv]
+    const void *k_reg, *v_reg;  // regions [cap, nk*hd_kv] of `kv` elements
+    int kv;                   // KvKind
     const int32_t *pos;       // [nt]
     int32_t *err;
     int nt, nh, nk, hd, hd_kv, cap;

@@ -76,6 +76,7 @@ extern "C" int minf_gqa_attn_decode_static_ws(float *out, const float *q, const 
     d.q = q;
     d.k_reg = k_reg;
     d.v_reg = v_reg;
+    d.kv = kKvF32;
     d.row_off = seq_row_off;
     d.caps = seq_cap;
     d.cap = max_cap;

@@ -28,8 +28,10 @@
 // Every mbarrier wait is bounded by a 200 ms global-timer budget; a wait that expires sets
 // MINF_ERRBIT_TIMEOUT, makes every role leave its loop, and the CTA still frees its TMEM.
 #include <cuda.h>
+#include <cuda_fp16.h>
 
 #include <cmath>
+#include <type_traits>
 
 #include "minf_common.cuh"
 #include "minf_kernels.h"
@@ -127,7 +129,7 @@ __device__ __forceinline__ uint32_t sw128_off(int row, int col) {
 
 struct PParams {
     float *out;
-    const float *v_reg;
+    const void *k_reg, *v_reg;  // fp32 or binary16 elements (binary16 K is read without TMA)
     const int32_t *pos;
     int32_t *err;
     int nt, nh, nk, hd, cap, W;
@@ -164,10 +166,23 @@ __device__ __forceinline__ void split_region(float *hi, float *lo, int n_float4,
     }
 }
 
-template <int HDKV>
+// Four consecutive region elements as fp32 (binary16 converts exactly).
+__device__ __forceinline__ float4 ld4(const float *p, int i4) { return reinterpret_cast<const float4 *>(p)[i4]; }
+__device__ __forceinline__ float4 ld4(const __half *p, int i4) {
+    const uint2 u = reinterpret_cast<const uint2 *>(p)[i4];
+    const float2 x = __half22float2(*reinterpret_cast<const __half2 *>(&u.x));
+    const float2 y = __half22float2(*reinterpret_cast<const __half2 *>(&u.y));
+    return make_float4(x.x, x.y, y.x, y.y);
+}
+
+// fp32 regions: K tiles arrive by TMA into kh and are split in place.  binary16 regions: the
+// softmax threads read the K tile themselves, converting, and write both halves (a binary16
+// value is exact in TF32, so its low half is zero).
+template <int HDKV, typename T>
 __global__ void __launch_bounds__(kThreadsP, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const PParams a) {
+    constexpr bool kTmaK = std::is_same<T, float>::value;
     extern __shared__ unsigned char smem_raw[];
     Smem<HDKV> &sm = *reinterpret_cast<Smem<HDKV> *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -233,10 +248,12 @@ __global__ void __launch_bounds__(kThreadsP, 1)
             mbar_expect_tx(&sm.bar_q, kQBytes);
 #pragma unroll
             for (int c = 0; c < HDKV / 32; ++c) tma_load_2d(sm.qh[c], &tm_q, h * a.hd + 32 * c, t0, &sm.bar_q);
-            mbar_expect_tx(&sm.bar_k, kKBytes);
+            if (kTmaK) {
+                mbar_expect_tx(&sm.bar_k, kKBytes);
 #pragma unroll
-            for (int c = 0; c < HDKV / 32; ++c)
-                tma_load_2d(sm.kh[c], &tm_k, hk * HDKV + 32 * c, tile0 * BN, &sm.bar_k);
+                for (int c = 0; c < HDKV / 32; ++c)
+                    tma_load_2d(sm.kh[c], &tm_k, hk * HDKV + 32 * c, tile0 * BN, &sm.bar_k);
+            }
             for (int i = 0; i < n_tiles; ++i) {
                 // S = Q K^T once the softmax warps have split Q (first tile), K and V^T
                 if (!mbar_wait(&sm.bar_kv, i & 1, abort_flag, a.err)) break;
@@ -253,7 +270,7 @@ __global__ void __launch_bounds__(kThreadsP, 1)
                     mma_tf32(tmem, ql, kh, tf32_idesc(BM, BN), 1);
                 }
                 mma_commit(&sm.bar_s);
-                if (i + 1 < n_tiles) {
+                if (kTmaK && i + 1 < n_tiles) {
                     // the K tile is free once S(i) is complete
                     if (!mbar_wait(&sm.bar_s, i & 1, abort_flag, a.err)) break;
                     mbar_expect_tx(&sm.bar_k, kKBytes);
@@ -290,17 +307,35 @@ __global__ void __launch_bounds__(kThreadsP, 1)
             split_region(&sm.qh[0][0], &sm.ql[0][0], BM * HDKV / 4, tid);
         for (int i = 0; i < n_tiles; ++i) {
             const int j0 = (tile0 + i) * BN;
-            if (!mbar_wait(&sm.bar_k, i & 1, abort_flag, a.err)) break;
-            split_region(&sm.kh[0][0], &sm.kl[0][0], BN * HDKV / 4, tid);
+            if (kTmaK) {
+                if (!mbar_wait(&sm.bar_k, i & 1, abort_flag, a.err)) break;
+                split_region(&sm.kh[0][0], &sm.kl[0][0], BN * HDKV / 4, tid);
+            } else {  // K tile -> SW128 slabs (keys along N); keys past the widest window are zero
+                const int key = j0 + vk;
+                const T *krow = static_cast<const T *>(a.k_reg) + static_cast<size_t>(key) * a.W + hk * HDKV;
+#pragma unroll 4
+                for (int d4 = vq * (HDKV / 16); d4 < (vq + 1) * (HDKV / 16); ++d4) {
+                    const float4 kv = key < lmax ? ld4(krow, d4) : make_float4(0.f, 0.f, 0.f, 0.f);
+                    const float kk[4] = {kv.x, kv.y, kv.z, kv.w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int d = 4 * d4 + e;
+                        float hi, lo;
+                        split_tf32(kk[e], hi, lo);
+                        const uint32_t off = sw128_off(vk, d & 31);
+                        *reinterpret_cast<float *>(reinterpret_cast<unsigned char *>(sm.kh[d >> 5]) + off) = hi;
+                        *reinterpret_cast<float *>(reinterpret_cast<unsigned char *>(sm.kl[d >> 5]) + off) = lo;
+                    }
+                }
+            }
             {   // V tile -> V^T hi/lo (K-major, keys along K); keys past the widest window are zero
                 const int key = j0 + vk;
-                const float *vrow = a.v_reg + static_cast<size_t>(key) * a.W + hk * HDKV;
+                const T *vrow = static_cast<const T *>(a.v_reg) + static_cast<size_t>(key) * a.W + hk * HDKV;
                 unsigned char *vth = reinterpret_cast<unsigned char *>(sm.vh[vk >> 5]);
                 unsigned char *vtl = reinterpret_cast<unsigned char *>(sm.vl[vk >> 5]);
 #pragma unroll 4
                 for (int d4 = vq * (HDKV / 16); d4 < (vq + 1) * (HDKV / 16); ++d4) {
-                    const float4 v = key < lmax ? reinterpret_cast<const float4 *>(vrow)[d4]
-                                                : make_float4(0.f, 0.f, 0.f, 0.f);
+                    const float4 v = key < lmax ? ld4(vrow, d4) : make_float4(0.f, 0.f, 0.f, 0.f);
                     const float vv[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
@@ -447,15 +482,20 @@ PrefillPlan prefill_plan(int nt, int nh, int hd_kv, int cap) {
     return p;
 }
 
-template <int HDKV>
+template <int HDKV, typename T>
 int launch_t(const PrefillArgs &pa, cudaStream_t s) {
     CUtensorMap tq, tk;
-    if (!make_tensor_map_2d(&tq, pa.q, static_cast<uint64_t>(pa.nh) * pa.hd, pa.nt, 32, BM, true))
+    if (!make_tensor_map_2d(&tq, pa.q, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, static_cast<uint64_t>(pa.nh) * pa.hd, pa.nt,
+                            32, BM, true))
         return MINF_ERR_CUDA;
-    if (!make_tensor_map_2d(&tk, pa.k_reg, static_cast<uint64_t>(pa.nk) * HDKV, pa.cap, 32, BN, true))
+    if (!std::is_same<T, float>::value)
+        tk = tq;  // binary16 K is read by the softmax threads: the map argument goes unused
+    else if (!make_tensor_map_2d(&tk, pa.k_reg, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4,
+                                 static_cast<uint64_t>(pa.nk) * HDKV, pa.cap, 32, BN, true))
         return MINF_ERR_CUDA;
     PParams a;
     a.out = pa.out;
+    a.k_reg = pa.k_reg;
     a.v_reg = pa.v_reg;
     a.pos = pa.pos;
     a.err = pa.err;
@@ -476,16 +516,18 @@ int launch_t(const PrefillArgs &pa, cudaStream_t s) {
     a.ws_ml = pl.n_kc > 1 ? reinterpret_cast<float *>(ws + pl.ml_off) : nullptr;
     a.ws_ticket = pl.n_kc > 1 ? reinterpret_cast<int *>(ws + pl.ticket_off) : nullptr;
     const size_t smem = sizeof(Smem<HDKV>) + 1024;
-    static bool attr_set = false;
-    if (!attr_set) {
-        if (cudaFuncSetAttribute(prefill_kernel<HDKV>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return MINF_ERR_CUDA;
+    static bool attr_set[64] = {};
+    if (!attr_set[dev]) {
+        if (cudaFuncSetAttribute(prefill_kernel<HDKV, T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  static_cast<int>(smem)) != cudaSuccess)
             return MINF_ERR_CUDA;
-        attr_set = true;
+        attr_set[dev] = true;
     }
     const long long ctas = static_cast<long long>(pl.n_qt) * pa.nh * pl.n_kc;
     if (ctas > 0x7fffffffLL) return MINF_ERR_UNSUPPORTED;
-    prefill_kernel<HDKV><<<static_cast<unsigned>(ctas), kThreadsP, smem, s>>>(tq, tk, a);
+    prefill_kernel<HDKV, T><<<static_cast<unsigned>(ctas), kThreadsP, smem, s>>>(tq, tk, a);
     return cudaPeekAtLastError() == cudaSuccess ? MINF_OK : MINF_ERR_CUDA;
 }
 
@@ -500,8 +542,13 @@ size_t prefill_workspace_bytes(int nt, int nh, int hd_kv, int cap) {
 int launch_prefill(const PrefillArgs &pa, cudaStream_t s) {
     if (pa.nt == 0) return MINF_OK;
     if ((static_cast<long long>(pa.nh) * pa.hd) % 4 != 0) return MINF_ERR_UNSUPPORTED;
-    if (pa.hd_kv == 64) return launch_t<64>(pa, s);
-    if (pa.hd_kv == 128) return launch_t<128>(pa, s);
+    if (pa.kv == kKvF16) {
+        if (pa.hd_kv == 64) return launch_t<64, __half>(pa, s);
+        if (pa.hd_kv == 128) return launch_t<128, __half>(pa, s);
+        return MINF_ERR_UNSUPPORTED;
+    }
+    if (pa.hd_kv == 64) return launch_t<64, float>(pa, s);
+    if (pa.hd_kv == 128) return launch_t<128, float>(pa, s);
     return MINF_ERR_UNSUPPORTED;
 }
 

@@ -96,9 +96,10 @@ __device__ __forceinline__ void named_sync(int id, int threads) {
 __device__ __forceinline__ void gdc_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void gdc_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;"); }
 
-// Host: a 2-D fp32 tensor map over a row-major [rows, cols] matrix with a {box_cols, box_rows}
-// box.  swizzle128: the 128-byte swizzle the tensor cores read (box_cols must then be 32).
-bool make_tensor_map_2d(CUtensorMap *m, const float *base, uint64_t cols, uint64_t rows,
-                        uint32_t box_cols, uint32_t box_rows, bool swizzle128);
+// Host: a 2-D tensor map over a row-major [rows, cols] matrix of `dt` elements (elem_bytes
+// each) with a {box_cols, box_rows} box.  swizzle128: the 128-byte swizzle the tensor cores
+// read (the box's inner extent must then be 128 bytes).
+bool make_tensor_map_2d(CUtensorMap *m, const void *base, CUtensorMapDataType dt, uint32_t elem_bytes,
+                        uint64_t cols, uint64_t rows, uint32_t box_cols, uint32_t box_rows, bool swizzle128);
 
 }  // namespace minf

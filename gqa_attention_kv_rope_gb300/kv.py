@@ -11,6 +11,10 @@ reuse", §2.3/§2.5: the regions survive and positions are data).
 
 Growing past `cap` is an error reported by the kernels, never a silent move; a
 caller that needs more rows builds a new manager (and re-captures its graphs).
+
+Regions may also be kept in f16 (dtype=torch.float16: IEEE binary16, §2.5 of the
+same page: the GPU backends may keep the K/V regions in f16, halving the bytes an
+attention read moves); the library's `_f16` entry points read and write them.
 """
 from __future__ import annotations
 
@@ -22,12 +26,14 @@ from . import binding
 class KvRegions:
     """Per-layer regions for one sequence: k[layer], v[layer] are [cap, W] views."""
 
-    def __init__(self, n_layer: int, row_width: int, cap: int, device="cuda"):
+    def __init__(self, n_layer: int, row_width: int, cap: int, device="cuda", dtype=torch.float32):
         if n_layer <= 0 or row_width <= 0 or cap <= 0:
             raise ValueError("n_layer, row_width and cap must be positive")
-        self.n_layer, self.row_width, self.cap = n_layer, row_width, cap
-        self.k = torch.empty((n_layer, cap, row_width), dtype=torch.float32, device=device)
-        self.v = torch.empty((n_layer, cap, row_width), dtype=torch.float32, device=device)
+        if dtype not in (torch.float32, torch.float16):
+            raise ValueError("regions are float32 or float16")
+        self.n_layer, self.row_width, self.cap, self.dtype = n_layer, row_width, cap, dtype
+        self.k = torch.empty((n_layer, cap, row_width), dtype=dtype, device=device)
+        self.v = torch.empty((n_layer, cap, row_width), dtype=dtype, device=device)
 
     def view(self, layer: int):
         """(K region, V region) of a layer: views into the persistent storage."""
@@ -35,7 +41,7 @@ class KvRegions:
 
     @property
     def nbytes(self) -> int:
-        return 2 * self.k.numel() * 4
+        return 2 * self.k.numel() * self.k.element_size()
 
 
 class KvArena:
@@ -43,10 +49,12 @@ class KvArena:
     [row_off[s], row_off[s] + cap[s]).  The descriptors live on the device so a
     captured batched step reads them at replay time."""
 
-    def __init__(self, n_layer: int, row_width: int, caps: list[int], device="cuda"):
+    def __init__(self, n_layer: int, row_width: int, caps: list[int], device="cuda", dtype=torch.float32):
         if not caps or min(caps) <= 0:
             raise ValueError("every sequence needs a positive capacity")
-        self.n_layer, self.row_width = n_layer, row_width
+        if dtype not in (torch.float32, torch.float16):
+            raise ValueError("arenas are float32 or float16")
+        self.n_layer, self.row_width, self.dtype = n_layer, row_width, dtype
         self.caps_host = list(int(c) for c in caps)
         offs, acc = [], 0
         for c in self.caps_host:
@@ -55,8 +63,8 @@ class KvArena:
         self.offsets_host = offs
         self.rows = acc
         self.max_cap = max(self.caps_host)
-        self.k = torch.empty((n_layer, acc, row_width), dtype=torch.float32, device=device)
-        self.v = torch.empty((n_layer, acc, row_width), dtype=torch.float32, device=device)
+        self.k = torch.empty((n_layer, acc, row_width), dtype=dtype, device=device)
+        self.v = torch.empty((n_layer, acc, row_width), dtype=dtype, device=device)
         self.row_off = torch.tensor(offs, dtype=torch.int64, device=device)
         self.cap = torch.tensor(self.caps_host, dtype=torch.int32, device=device)
 

@@ -252,6 +252,48 @@ MINF_API int minf_layer_attn_step_batched(float *xn, const float *h, const float
                                  size_t ws_bytes, int32_t *err, minf_stream_t stream);
 
 /*
+ * The f16 cache ([P1] §2.5: the GPU backends may keep the K/V regions in f16,
+ * halving the bytes every attention read moves).  These entry points are the
+ * ones above with the regions (or arena) holding IEEE binary16 values instead of
+ * fp32, passed as uint16_t bit patterns, 16-byte aligned, row width W a multiple
+ * of 8.  The store converts each element with round to nearest, ties to even
+ * (the pages name no rounding; this is the format's default); the attention read
+ * converts back exactly and computes in fp32 as before, so the result is the
+ * fp32 attention over the values the regions hold.  q, k, v, out, h, xn stay
+ * fp32, and the rotated k written back to `k` is the unrounded fp32 value.
+ * Workspace sizes are the same functions as for fp32 regions.  Device errors and
+ * statuses: as the fp32 entry points (MINF_ERR_ARG also for W not a multiple of 8).
+ */
+MINF_API int minf_kv_append_f16(uint16_t *k_reg, uint16_t *v_reg, int cap, int row_width, const float *k_rows,
+                                const float *v_rows, const int32_t *pos, int nt, int32_t *err,
+                                minf_stream_t stream);
+MINF_API int minf_rope_kv_append_f16(float *q, float *k, const float *v, const int32_t *pos, int nt, int n_head,
+                                     int n_kv_head, int hd, int hd_kv, float theta, float freq_scale, int style,
+                                     uint16_t *k_reg, uint16_t *v_reg, int cap, int32_t *err,
+                                     minf_stream_t stream);
+MINF_API int minf_gqa_attn_decode_f16(float *out, const float *q, const uint16_t *k_reg, const uint16_t *v_reg,
+                                      const int64_t *seq_row_off, const int32_t *seq_cap, int max_cap,
+                                      int64_t arena_rows, const int32_t *pos, int n_seq, int n_head,
+                                      int n_kv_head, int hd, int hd_kv, float scale, void *ws, size_t ws_bytes,
+                                      int32_t *err, minf_stream_t stream);
+MINF_API int minf_gqa_attn_prefill_f16(float *out, const float *q, const uint16_t *k_reg, const uint16_t *v_reg,
+                                       int cap, const int32_t *pos, int nt, int n_head, int n_kv_head, int hd,
+                                       int hd_kv, float scale, void *ws, size_t ws_bytes, int32_t *err,
+                                       minf_stream_t stream);
+MINF_API int minf_layer_attn_step_f16(float *xn, const float *h, const float *gain, float eps, int n_embd,
+                                      float *q, float *k, const float *v, const int32_t *pos, int nt,
+                                      uint16_t *k_reg, uint16_t *v_reg, int cap, int n_head, int n_kv_head, int hd,
+                                      int hd_kv, float theta, float freq_scale, int style, float *out, void *ws,
+                                      size_t ws_bytes, int32_t *err, minf_stream_t stream);
+MINF_API int minf_layer_attn_step_batched_f16(float *xn, const float *h, const float *gain, float eps,
+                                              int n_embd, float *q, float *k, const float *v, const int32_t *pos,
+                                              int n_seq, uint16_t *k_arena, uint16_t *v_arena,
+                                              const int64_t *seq_row_off, const int32_t *seq_cap, int max_cap,
+                                              int64_t arena_rows, int n_head, int n_kv_head, int hd, int hd_kv,
+                                              float theta, float freq_scale, int style, float *out, void *ws,
+                                              size_t ws_bytes, int32_t *err, minf_stream_t stream);
+
+/*
  * SiLU times up ([P1] §3.2.5): y = gate / (1 + e^-gate) * up over n elements.
  * Errors: MINF_ERR_ARG for null pointers or n < 0.
  */
