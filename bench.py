@@ -168,14 +168,22 @@ def measured_peaks():
         return 6800.0, "fallback"
 
 
+def decode_source_sha256() -> str:
+    """Hash of the decode kernel's sources (the kernel header, then its launcher)."""
+    h = hashlib.sha256()
+    for f in ("minf_decode.cuh", "minf_decode.cu"):
+        with open(os.path.join(ROOT, "gqa_attention_kv_rope_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()
+
+
 def decode_traffic_record():
     """DRAM bytes per decode-attention launch from the committed ncu summary, valid only
     while the kernel source is unchanged since the counters were taken."""
     path = os.path.join(ROOT, "profiles", "decode_attn_traffic.json")
-    src = os.path.join(ROOT, "gqa_attention_kv_rope_gb300", "csrc", "minf_decode.cu")
     try:
         rec = json.load(open(path))
-        sha = hashlib.sha256(open(src, "rb").read()).hexdigest()
+        sha = decode_source_sha256()
         if rec.get("kernel_src_sha256") != sha:
             return None, rec
         return rec, rec
@@ -198,14 +206,14 @@ def flush_l2(buf):
 
 
 # ----------------------------------------------------------------------------- workloads
-def setup_long_context(m, torch, wl, n_cached, dev, n_layer=None):
+def setup_long_context(m, torch, wl, n_cached, dev, n_layer=None, dtype=None):
     import dataclasses
 
     g = wl.QWEN3_06B
     if n_layer is not None and n_layer != g.n_layer:
         g = dataclasses.replace(g, n_layer=n_layer)
     cap = max(wl.LONG_CONTEXT_CAP, n_cached + 1)
-    regions = m.kv.KvRegions(g.n_layer, g.row_width, cap, device=dev)
+    regions = m.kv.KvRegions(g.n_layer, g.row_width, cap, device=dev, dtype=dtype or torch.float32)
     for layer in range(g.n_layer):
         k, v = regions.view(layer)
         gen = torch.Generator(device=dev)
@@ -243,12 +251,12 @@ def views(S, layer):
 
 def decode_step(m, S, layers=None):
     g = S["g"]
+    fn = m.binding.minf_layer_attn_step_f16 if S["regions"].k.element_size() == 2 else m.binding.minf_layer_attn_step
     for layer in range(g.n_layer) if layers is None else layers:
         h, q, k, v, xn, out = views(S, layer)
         K, V = S["regions"].view(layer)
-        m.binding.minf_layer_attn_step(xn, h, S["gains"][layer], g.eps, q, k, v, S["pos"], K, V, g.n_head,
-                                       g.n_kv_head, g.hd, g.hd_kv, g.theta, g.freq_scale, 0, out, S["ws"],
-                                       S["err"])
+        fn(xn, h, S["gains"][layer], g.eps, q, k, v, S["pos"], K, V, g.n_head, g.n_kv_head, g.hd, g.hd_kv, g.theta,
+           g.freq_scale, 0, out, S["ws"], S["err"])
 
 
 def capture(torch, stream, fn):
@@ -496,12 +504,42 @@ def run_decode_loop(m, torch, wl, dev):
             "kv_read_gbs": round(kv / (total_ms * 1e-3) / 1e9, 1), "err": int(err.item())}
 
 
-def run_batched(m, torch, wl, dev, steps):
+def run_long_context_f16(m, torch, wl, dev, steps):
+    """The headline workload (28 layers, nkv = 40960) with binary16 regions: the bytes the
+    step reads halve, the arithmetic stays fp32."""
+    n = wl.LONG_CONTEXT_SWEEP[-1]
+    S = setup_long_context(m, torch, wl, n, dev, dtype=torch.float16)
+    g = S["g"]
+    stream = torch.cuda.Stream()
+    graph = capture(torch, stream, lambda: decode_step(m, S))
+    for _ in range(3):
+        graph.replay()
+    torch.cuda.synchronize()
+    a, b = Timer(torch, stream).pair()
+    with torch.cuda.stream(stream):
+        a.record(stream)
+        for _ in range(steps):
+            graph.replay()
+        b.record(stream)
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / steps
+    kv = kv_bytes_long_context(g, n) // 2
+    res = {"step_ms": round(ms, 4), "kv_read_gbs": round(kv / (ms * 1e-3) / 1e9, 1), "kv_bytes_per_step": kv,
+           "err": int(S["err"].item())}
+    del graph
+    S.clear()
+    torch.cuda.empty_cache()
+    return res
+
+
+def run_batched(m, torch, wl, dev, steps, dtype=None):
     """Batched decode: 64 sequences, lengths ~ U{1..8192} (seeded), 28 layers, one graph."""
     g = wl.QWEN3_06B
     lengths = wl.batched_lengths(seed=0)
     caps = [ln + 1 + wl.KV_HEADROOM_ROWS for ln in lengths]
-    arena = m.kv.KvArena(g.n_layer, g.row_width, caps, device=dev)
+    arena = m.kv.KvArena(g.n_layer, g.row_width, caps, device=dev, dtype=dtype or torch.float32)
+    eb = arena.k.element_size()
+    fn = m.binding.minf_layer_attn_step_batched_f16 if eb == 2 else m.binding.minf_layer_attn_step_batched
     gen = torch.Generator(device=dev)
     for layer in range(g.n_layer):
         gen.manual_seed(wl.sub_seed("batched", layer, "K"))
@@ -523,9 +561,8 @@ def run_batched(m, torch, wl, dev, steps):
         for layer in range(g.n_layer):
             d = L[layer]
             K, V = arena.view(layer)
-            m.binding.minf_layer_attn_step_batched(d["xn"], d["h"], d["gain"], g.eps, d["q"], d["k"], d["v"], pos,
-                                                   K, V, arena.row_off, arena.cap, arena.max_cap, g.n_head,
-                                                   g.n_kv_head, g.hd, g.hd_kv, g.theta, 1.0, 0, d["out"], ws, err)
+            fn(d["xn"], d["h"], d["gain"], g.eps, d["q"], d["k"], d["v"], pos, K, V, arena.row_off, arena.cap,
+               arena.max_cap, g.n_head, g.n_kv_head, g.hd, g.hd_kv, g.theta, 1.0, 0, d["out"], ws, err)
 
     stream = torch.cuda.Stream()
     graph = capture(torch, stream, step)
@@ -540,7 +577,7 @@ def run_batched(m, torch, wl, dev, steps):
         b.record(stream)
     torch.cuda.synchronize()
     ms = a.elapsed_time(b) / steps
-    kv = g.n_layer * sum(2 * (ln + 1) * g.row_width * 4 for ln in lengths)
+    kv = g.n_layer * sum(2 * (ln + 1) * g.row_width * eb for ln in lengths)
     res = {"step_ms": round(ms, 3), "kv_read_gbs": round(kv / (ms * 1e-3) / 1e9, 1),
            "kv_bytes_per_step": kv, "max_len": max(lengths), "err": int(err.item())}
     del arena
@@ -704,6 +741,9 @@ def main(argv=None):
         secondary["prefill_layer_us"] = layer_us
         secondary["decode_loop"] = run_decode_loop(m, torch, wl, dev)
         secondary["batched_decode"] = run_batched(m, torch, wl, dev, max(3, args.steps // 4))
+        secondary["long_context_f16"] = run_long_context_f16(m, torch, wl, dev, max(5, args.steps // 2))
+        secondary["batched_decode_f16"] = run_batched(m, torch, wl, dev, max(3, args.steps // 4),
+                                                      dtype=torch.float16)
         secondary["elementwise"] = run_elementwise(m, torch, dev)
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
