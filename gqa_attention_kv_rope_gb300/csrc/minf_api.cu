@@ -124,6 +124,32 @@ static int rope_kv_append(float *q, float *k, const float *v, const int32_t *pos
                    k_reg, v_reg, kv, nullptr, nullptr, cap, err, cs(stream));
 }
 
+static int layer_prologue(float *xn, const float *h, const float *gain, float eps, int n_embd, float *q, float *k,
+                          const float *v, const int32_t *pos, int nt, int nh, int nk, int hd, int hd_kv, float theta,
+                          float freq_scale, int style, void *k_reg, void *v_reg, int kv, const int64_t *row_off,
+                          const int32_t *caps, int cap, int32_t *err, cudaStream_t s) {
+    RopeKvArgs a;
+    a.q = q;
+    a.k = k;
+    a.v = v;
+    a.pos = pos;
+    a.k_reg = k_reg;
+    a.v_reg = v_reg;
+    a.kv = kv;
+    a.row_off = row_off;
+    a.caps = caps;
+    a.cap = cap;
+    a.nt = nt;
+    a.nh = nh;
+    a.nk = nk;
+    a.hd = hd;
+    a.hd_kv = hd_kv;
+    a.style = style;
+    a.err = err;
+    NormArgs nrm = {xn, h, gain, nt, n_embd, eps};
+    return launch_layer_prologue(a, theta, freq_scale, nrm, s);
+}
+
 int minf_rope_kv_append(float *q, float *k, const float *v, const int32_t *pos, int nt,
                         int n_head, int n_kv_head, int hd, int hd_kv, float theta,
                         float freq_scale, int style, float *k_reg, float *v_reg, int cap,
@@ -151,8 +177,9 @@ size_t minf_attn_prefill_workspace_bytes(int nt, int n_head, int n_kv_head, int 
 
 static int prefill(float *out, const float *q, const void *k_reg, const void *v_reg, int kv, int cap,
                    const int32_t *pos, int nt, int nh, int nk, int hd, int hd_kv, float scale,
-                   void *ws, size_t ws_bytes, int32_t *err, cudaStream_t s) {
+                   void *ws, size_t ws_bytes, int32_t *err, cudaStream_t s, bool pdl = false) {
     PrefillArgs a;
+    a.pdl = pdl;
     a.ws = ws;
     a.ws_bytes = ws_bytes;
     a.out = out;
@@ -290,16 +317,15 @@ static int layer_attn_step(float *xn, const float *h, const float *gain, float e
         DecodeStepExtra x = {k, v, xn, h, gain, eps, theta, freq_scale, n_embd, style, true};
         return launch_decode_step(d, x, s);
     }
-    st = launch_rms_norm(xn, h, gain, nt, n_embd, eps, s);
+    // one launch for RMSNorm, RoPE and the store, then the attention
+    st = layer_prologue(xn, h, gain, eps, n_embd, q, k, v, pos, nt, n_head, n_kv_head, hd, hd_kv, theta,
+                        freq_scale, style, k_reg, v_reg, kv, nullptr, nullptr, cap, err, s);
     if (st != MINF_OK) return st;
-    st = rope_kv(q, k, v, pos, nt, n_head, n_kv_head, hd, hd_kv, theta, freq_scale, style, k_reg,
-                 v_reg, kv, nullptr, nullptr, cap, err, s);
-    if (st != MINF_OK) return st;
-    if (nt == 1)
+    if (nt == 1)  // the decode kernel streams cached rows before its wait: no early start after a store
         return decode(out, q, k_reg, v_reg, kv, nullptr, nullptr, cap, pos, 1, n_head, n_kv_head, hd,
                       hd_kv, scale, ws, ws_bytes, err, s);
     return prefill(out, q, k_reg, v_reg, kv, cap, pos, nt, n_head, n_kv_head, hd, hd_kv, scale, ws, ws_bytes,
-                   err, s);
+                   err, s, true);
 }
 
 int minf_layer_attn_step(float *xn, const float *h, const float *gain, float eps, int n_embd,
@@ -346,10 +372,8 @@ static int layer_attn_step_batched(float *xn, const float *h, const float *gain,
         DecodeStepExtra x = {k, v, xn, h, gain, eps, theta, freq_scale, n_embd, style, false};
         return launch_decode_step(d, x, s);
     }
-    st = launch_rms_norm(xn, h, gain, n_seq, n_embd, eps, s);
-    if (st != MINF_OK) return st;
-    st = rope_kv(q, k, v, pos, n_seq, n_head, n_kv_head, hd, hd_kv, theta, freq_scale, style,
-                 k_arena, v_arena, kv, seq_row_off, seq_cap, max_cap, err, s);
+    st = layer_prologue(xn, h, gain, eps, n_embd, q, k, v, pos, n_seq, n_head, n_kv_head, hd, hd_kv, theta,
+                        freq_scale, style, k_arena, v_arena, kv, seq_row_off, seq_cap, max_cap, err, s);
     if (st != MINF_OK) return st;
     return decode(out, q, k_arena, v_arena, kv, seq_row_off, seq_cap, max_cap, pos, n_seq, n_head,
                   n_kv_head, hd, hd_kv, scale, ws, ws_bytes, err, s, arena_rows);

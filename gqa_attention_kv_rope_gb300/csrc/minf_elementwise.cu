@@ -52,11 +52,8 @@ int sm_count() {
 // "11 . Attention, vec ops, and the KV cache", §3.2.1: y = x / sqrt(mean(x^2) + eps) * w.
 // One warp per row; the sum of squares is a per-lane fp32 sum folded by a butterfly.
 template <bool kVec>
-__global__ void __launch_bounds__(256) rms_norm_kernel(float *y, const float *x, const float *w,
-                                                       int rows, int n, float eps) {
-    const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+__device__ __forceinline__ void rms_norm_row(float *y, const float *x, const float *w, int warp, int n, float eps) {
     const int lane = threadIdx.x & 31;
-    if (warp >= rows) return;
     const float *xr = x + static_cast<size_t>(warp) * n;
     float *yr = y + static_cast<size_t>(warp) * n;
     float ss = 0.0f;
@@ -92,6 +89,14 @@ __global__ void __launch_bounds__(256) rms_norm_kernel(float *y, const float *x,
             yr[i] = w ? v * w[i] : v;
         }
     }
+}
+
+template <bool kVec>
+__global__ void __launch_bounds__(256) rms_norm_kernel(float *y, const float *x, const float *w,
+                                                       int rows, int n, float eps) {
+    const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    if (warp >= rows) return;
+    rms_norm_row<kVec>(y, x, w, warp, n, eps);
 }
 
 int launch_rms_norm(float *y, const float *x, const float *w, int rows, int n, float eps,
@@ -212,14 +217,14 @@ int launch_kv_append(void *k_reg, void *v_reg, int kv, int cap, int W, const flo
 // back in place and into the K region), and a float4 of v (copied into the V region).
 // Batched callers give each token its own arena offset and capacity.
 template <typename T>
-__global__ void __launch_bounds__(256) rope_kv_append_kernel(RopeKvArgs a, const RopeTable tq,
-                                                             const RopeTable tk) {
+__device__ __forceinline__ void rope_kv_append_items(const RopeKvArgs &a, const RopeTable &tq, const RopeTable &tk,
+                                                     int block, int blocks) {
     const int hq = a.hd >> 1, hk = a.hd_kv >> 1;
     const int nq = a.nh * hq, nkp = a.nk * hk, W = a.nk * a.hd_kv, nv = W >> 2;
     const int per_tok = nq + nkp + nv;
     const long long total = static_cast<long long>(a.nt) * per_tok;
-    for (long long idx = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; idx < total;
-         idx += static_cast<long long>(gridDim.x) * blockDim.x) {
+    for (long long idx = block * static_cast<long long>(blockDim.x) + threadIdx.x; idx < total;
+         idx += static_cast<long long>(blocks) * blockDim.x) {
         const int t = static_cast<int>(idx / per_tok);
         int r = static_cast<int>(idx % per_tok);
         const int p = __ldg(a.pos + t);
@@ -262,6 +267,47 @@ __global__ void __launch_bounds__(256) rope_kv_append_kernel(RopeKvArgs a, const
         const float4 v = reinterpret_cast<const float4 *>(a.v)[static_cast<size_t>(t) * nv + r];
         put4(static_cast<T *>(a.v_reg), (static_cast<size_t>(base) + p) * nv + r, v);
     }
+}
+
+template <typename T>
+__global__ void __launch_bounds__(256) rope_kv_append_kernel(RopeKvArgs a, const RopeTable tq,
+                                                             const RopeTable tk) {
+    rope_kv_append_items<T>(a, tq, tk, blockIdx.x, gridDim.x);
+}
+
+// The layer step's prologue in one launch: the first `norm_blocks` blocks compute the
+// RMSNorm rows (one warp per row), the rest rotate q and k and store the rows.  It touches
+// nothing the attention kernel after it reads before its own dependency wait, so it lets that
+// launch start at once (programmatic dependent launch).
+template <typename T, bool kVec>
+__global__ void __launch_bounds__(256) layer_prologue_kernel(RopeKvArgs a, const RopeTable tq, const RopeTable tk,
+                                                             NormArgs nrm, int norm_blocks) {
+    asm volatile("griddepcontrol.launch_dependents;");
+    if (static_cast<int>(blockIdx.x) < norm_blocks) {
+        const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+        if (warp < nrm.rows) rms_norm_row<kVec>(nrm.y, nrm.x, nrm.w, warp, nrm.n, nrm.eps);
+        return;
+    }
+    rope_kv_append_items<T>(a, tq, tk, blockIdx.x - norm_blocks, gridDim.x - norm_blocks);
+}
+
+int launch_layer_prologue(const RopeKvArgs &a, float theta, float freq_scale, const NormArgs &nrm, cudaStream_t s) {
+    if (a.nt == 0 && nrm.rows == 0) return MINF_OK;
+    RopeTable tq, tk;
+    rope_table(&tq, a.hd, theta, freq_scale);
+    rope_table(&tk, a.hd_kv, theta, freq_scale);
+    const long long per_tok =
+        static_cast<long long>(a.nh) * (a.hd / 2) + a.nk * (a.hd_kv / 2) + a.nk * a.hd_kv / 4;
+    const int norm_blocks = (nrm.rows + 7) / 8;
+    const int blocks = norm_blocks + grid_for(per_tok * a.nt, 256);
+    const bool vec = (nrm.n % 4 == 0) && aligned16(nrm.x) && aligned16(nrm.y) && (!nrm.w || aligned16(nrm.w));
+    if (a.kv == kKvF16)
+        vec ? layer_prologue_kernel<__half, true><<<blocks, 256, 0, s>>>(a, tq, tk, nrm, norm_blocks)
+            : layer_prologue_kernel<__half, false><<<blocks, 256, 0, s>>>(a, tq, tk, nrm, norm_blocks);
+    else
+        vec ? layer_prologue_kernel<float, true><<<blocks, 256, 0, s>>>(a, tq, tk, nrm, norm_blocks)
+            : layer_prologue_kernel<float, false><<<blocks, 256, 0, s>>>(a, tq, tk, nrm, norm_blocks);
+    return cudaPeekAtLastError() == cudaSuccess ? MINF_OK : MINF_ERR_CUDA;
 }
 
 int launch_rope_kv_append(const RopeKvArgs &a, float theta, float freq_scale, cudaStream_t s) {

@@ -50,6 +50,16 @@ int launch_kv_append(void *k_reg, void *v_reg, int kv, int cap, int W, const flo
                      const float *v_rows, const int32_t *pos, int nt, int32_t *err,
                      cudaStream_t s);
 int launch_rope_kv_append(const RopeKvArgs &a, float theta, float freq_scale, cudaStream_t s);
+
+struct NormArgs {
+    float *y;
+    const float *x, *w;
+    int rows, n;
+    float eps;
+};
+// RMSNorm rows and RoPE + KV store in one launch (the layer step's prologue when the
+// attention is a separate launch); it releases the next launch at once.
+int launch_layer_prologue(const RopeKvArgs &a, float theta, float freq_scale, const NormArgs &nrm, cudaStream_t s);
 int launch_silu_mul(float *y, const float *g, const float *u, long long n, cudaStream_t s);
 
 // The rest of a decode layer step, fused into the attention launch (one token per sequence).
@@ -74,6 +84,7 @@ struct PrefillArgs {
     float scale;
     void *ws;                 // key-chunk partials (prefill_workspace_bytes)
     size_t ws_bytes;
+    bool pdl;                 // launch with programmatic stream serialization
 };
 
 size_t prefill_workspace_bytes(int nt, int nh, int hd_kv, int cap);

@@ -241,6 +241,9 @@ __global__ void __launch_bounds__(kThreadsP, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = sm.tmem_base;
+    // everything above reads only positions; q, the regions, the workspace and the output may
+    // still be written by the preceding launch (a no-op without programmatic dependent launch)
+    gdc_wait();
     constexpr uint32_t kQBytes = BM * HDKV * 4, kKBytes = BN * HDKV * 4;
 
     if (warp == kProducerWarp) {
@@ -527,8 +530,17 @@ int launch_t(const PrefillArgs &pa, cudaStream_t s) {
     }
     const long long ctas = static_cast<long long>(pl.n_qt) * pa.nh * pl.n_kc;
     if (ctas > 0x7fffffffLL) return MINF_ERR_UNSUPPORTED;
-    prefill_kernel<HDKV, T><<<static_cast<unsigned>(ctas), kThreadsP, smem, s>>>(tq, tk, a);
-    return cudaPeekAtLastError() == cudaSuccess ? MINF_OK : MINF_ERR_CUDA;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(ctas));
+    cfg.blockDim = dim3(kThreadsP);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pa.pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, prefill_kernel<HDKV, T>, tq, tk, a) == cudaSuccess ? MINF_OK : MINF_ERR_CUDA;
 }
 
 }  // namespace
