@@ -306,6 +306,18 @@ __global__ void __launch_bounds__(kThreadsP, 1)
         for (int d = 0; d < HDKV; ++d) o[d] = 0.0f;
         float m = -INFINITY, l = 0.0f;
         const int vk = tid & (BN - 1), vq = tid / BN;  // V^T staging: key, quarter of the dims
+        // This thread's slice of the next V tile is loaded one tile ahead, so its latency
+        // overlaps the current tile's products and softmax.
+        constexpr int kV4 = HDKV / 16;
+        float4 vnext[kV4];
+        auto load_v = [&](int tile) {
+            const int key = tile * BN + vk;
+            const T *vrow = static_cast<const T *>(a.v_reg) + static_cast<size_t>(key) * a.W + hk * HDKV;
+#pragma unroll
+            for (int c = 0; c < kV4; ++c)
+                vnext[c] = key < lmax ? ld4(vrow, vq * kV4 + c) : make_float4(0.f, 0.f, 0.f, 0.f);
+        };
+        if (n_tiles > 0) load_v(tile0);
         if (n_tiles > 0 && mbar_wait(&sm.bar_q, 0, abort_flag, a.err))
             split_region(&sm.qh[0][0], &sm.ql[0][0], BM * HDKV / 4, tid);
         for (int i = 0; i < n_tiles; ++i) {
@@ -332,14 +344,12 @@ __global__ void __launch_bounds__(kThreadsP, 1)
                 }
             }
             {   // V tile -> V^T hi/lo (K-major, keys along K); keys past the widest window are zero
-                const int key = j0 + vk;
-                const T *vrow = static_cast<const T *>(a.v_reg) + static_cast<size_t>(key) * a.W + hk * HDKV;
                 unsigned char *vth = reinterpret_cast<unsigned char *>(sm.vh[vk >> 5]);
                 unsigned char *vtl = reinterpret_cast<unsigned char *>(sm.vl[vk >> 5]);
-#pragma unroll 4
-                for (int d4 = vq * (HDKV / 16); d4 < (vq + 1) * (HDKV / 16); ++d4) {
-                    const float4 v = key < lmax ? ld4(vrow, d4) : make_float4(0.f, 0.f, 0.f, 0.f);
-                    const float vv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                for (int c = 0; c < kV4; ++c) {
+                    const int d4 = vq * kV4 + c;
+                    const float vv[4] = {vnext[c].x, vnext[c].y, vnext[c].z, vnext[c].w};
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
                         float hi, lo;
@@ -353,6 +363,7 @@ __global__ void __launch_bounds__(kThreadsP, 1)
             fence_async_smem();  // split Q/K and V^T -> visible to the tensor cores
             tc_fence_before();
             mbar_arrive(&sm.bar_kv);
+            if (i + 1 < n_tiles) load_v(tile0 + i + 1);
             if (!mbar_wait(&sm.bar_s, i & 1, abort_flag, a.err)) break;
             tc_fence_after();
             float r[32];
