@@ -95,6 +95,13 @@ def _load():
             _u16p, _u16p, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
             ctypes.c_float, ctypes.c_float, ctypes.c_int, _f32p, ctypes.c_int]
         lib.orc_layer_attn_step_f16.restype = ctypes.c_int
+        lib.orc_kv_append_paged.argtypes = [_f32p, _f32p, ctypes.c_int, ctypes.c_int, ctypes.c_int, _i32p,
+                                            ctypes.c_int, _f32p, _f32p, _i32p, ctypes.c_int]
+        lib.orc_kv_append_paged.restype = ctypes.c_int
+        lib.orc_gqa_attn_paged.argtypes = [_f32p, _f32p, _f32p, _f32p, ctypes.c_int, ctypes.c_int, _i32p,
+                                           ctypes.c_int, _i32p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                           ctypes.c_int, ctypes.c_int, ctypes.c_float]
+        lib.orc_gqa_attn_paged.restype = ctypes.c_int
         _lib = lib
         return lib
 
@@ -304,3 +311,43 @@ def layer_attn_step_f16(h, gain, q, k, v, pos, k_reg, v_reg, *, n_head: int, n_k
     if st != OK:
         raise OracleError(st, "layer_attn_step_f16")
     return xn, out
+
+
+# ----------------------------------------------------------------------------- paged regions
+def kv_append_paged(k_pool, v_pool, table, block_rows: int, k_rows, v_rows, pos, check=True) -> int:
+    """Pools [pool_blocks*block_rows, W] (modified in place); table int32 [n_seq, max_blocks];
+    one row per sequence, rows [n_seq, W], at pos[s]."""
+    k_pool = _f32(k_pool, writable=True)
+    v_pool = _f32(v_pool, writable=True)
+    rows, W = k_pool.shape
+    table = _i32(table)
+    n_seq, max_blocks = table.shape
+    k_rows = _f32(k_rows).reshape(-1, W)
+    v_rows = _f32(v_rows).reshape(-1, W)
+    pos = _i32(pos)
+    st = _load().orc_kv_append_paged(_p(k_pool, _f32p), _p(v_pool, _f32p), rows // block_rows, block_rows, W,
+                                     _p(table, _i32p), max_blocks, _p(k_rows, _f32p), _p(v_rows, _f32p),
+                                     _p(pos, _i32p), n_seq)
+    if check and st != OK:
+        raise OracleError(st, "kv_append_paged")
+    return st
+
+
+def gqa_attn_paged(q, k_pool, v_pool, table, block_rows: int, pos, n_head: int, n_kv_head: int, hd: int,
+                   hd_kv: int, scale: float | None = None) -> np.ndarray:
+    """Decode attention through a block table; q [n_seq, n_head, hd] -> out [n_seq, n_head*hd_kv]."""
+    q = _f32(q)
+    k_pool = _f32(k_pool)
+    v_pool = _f32(v_pool)
+    table = _i32(table)
+    n_seq, max_blocks = table.shape
+    pos = _i32(pos)
+    if scale is None:
+        scale = float(np.float32(1.0) / np.sqrt(np.float32(hd)))
+    out = np.zeros((n_seq, n_head * hd_kv), dtype=np.float32)
+    st = _load().orc_gqa_attn_paged(_p(out, _f32p), _p(q, _f32p), _p(k_pool, _f32p), _p(v_pool, _f32p),
+                                    k_pool.shape[0] // block_rows, block_rows, _p(table, _i32p), max_blocks,
+                                    _p(pos, _i32p), n_seq, n_head, n_kv_head, hd, hd_kv, scale)
+    if st != OK:
+        raise OracleError(st, "gqa_attn_paged")
+    return out

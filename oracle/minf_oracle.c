@@ -23,7 +23,7 @@
  *   orc_rope_freqs, orc_rms_norm, orc_rope, orc_kv_append, orc_gqa_attn,
  *   orc_attn_bruteforce_f64, orc_silu_mul, orc_layer_attn_step,
  *   orc_f32_to_f16, orc_f16_to_f32, orc_kv_append_f16,
- *   orc_layer_attn_step_f16 -- all pinned.
+ *   orc_layer_attn_step_f16, orc_kv_append_paged, orc_gqa_attn_paged -- all pinned.
  */
 #include <math.h>
 #include <pthread.h>
@@ -256,6 +256,88 @@ int orc_gqa_attn(float *out, const float *q, const float *k_reg, const float *v_
     for (int w = 0; w < n_threads; ++w)
         if (jobs[w].status != ORC_OK)
             return jobs[w].status;
+    return ORC_OK;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Paged regions.  [P2] "IV.2: Zero-copy KV cache" (the paged cache stores a
+ * sequence as scattered fixed-size blocks, so it cannot lend one contiguous
+ * view) and [P3] §2.2 (the attention reads the cells an explicit window
+ * names).  A pool holds pool_blocks blocks of block_rows rows of width W;
+ * sequence s owns the blocks its table row names: logical row j of s is pool
+ * row table[s*max_blocks + j/block_rows]*block_rows + j%block_rows, so its
+ * capacity is max_blocks*block_rows rows.  A block id outside the pool (or
+ * negative: not allocated) is an error wherever a row of it is needed. */
+static int orc_paged_row(const int32_t *table, int max_blocks, int block_rows, int pool_blocks, int s,
+                         long j, long *row)
+{
+    long blk = j / block_rows;
+    if (j < 0 || blk >= max_blocks)
+        return ORC_ERR_POS;
+    int b = table[(size_t)s * max_blocks + blk];
+    if (b < 0 || b >= pool_blocks)
+        return ORC_ERR_POS;
+    *row = (long)b * block_rows + j % block_rows;
+    return ORC_OK;
+}
+
+/* The KV store through the table: one token per sequence, at pos[s]. */
+int orc_kv_append_paged(float *k_pool, float *v_pool, int pool_blocks, int block_rows, int W,
+                        const int32_t *table, int max_blocks, const float *k_rows, const float *v_rows,
+                        const int32_t *pos, int n_seq)
+{
+    if (pool_blocks < 0 || block_rows <= 0 || W <= 0 || max_blocks <= 0 || n_seq < 0)
+        return ORC_ERR_ARG;
+    for (int s = 0; s < n_seq; ++s) {
+        long row;
+        int st = orc_paged_row(table, max_blocks, block_rows, pool_blocks, s, pos[s], &row);
+        if (st != ORC_OK)
+            return st;
+        memcpy(k_pool + (size_t)row * W, k_rows + (size_t)s * W, sizeof(float) * (size_t)W);
+        memcpy(v_pool + (size_t)row * W, v_rows + (size_t)s * W, sizeof(float) * (size_t)W);
+    }
+    return ORC_OK;
+}
+
+/* Decode attention through the table: for each sequence, the rows of its window
+ * [0, min(pos+1, max_blocks*block_rows)) are gathered in logical order and the
+ * attention above runs over them.  q is [n_seq, nh, hd], out [n_seq, nh*hdkv]. */
+int orc_gqa_attn_paged(float *out, const float *q, const float *k_pool, const float *v_pool, int pool_blocks,
+                       int block_rows, const int32_t *table, int max_blocks, const int32_t *pos, int n_seq,
+                       int nh, int nk, int hd, int hdkv, float scale)
+{
+    if (pool_blocks < 0 || block_rows <= 0 || max_blocks <= 0 || n_seq < 0 || nk <= 0 || hdkv <= 0)
+        return ORC_ERR_ARG;
+    int W = nk * hdkv;
+    long cap = (long)max_blocks * block_rows;
+    for (int s = 0; s < n_seq; ++s) {
+        if (pos[s] < 0)
+            return ORC_ERR_POS;
+        long L = (long)pos[s] + 1 < cap ? (long)pos[s] + 1 : cap;
+        float *kb = malloc(sizeof(float) * (size_t)L * W);
+        float *vb = malloc(sizeof(float) * (size_t)L * W);
+        if (!kb || !vb) {
+            free(kb);
+            free(vb);
+            return ORC_ERR_ARG;
+        }
+        int st = ORC_OK;
+        for (long j = 0; j < L && st == ORC_OK; ++j) {
+            long row;
+            st = orc_paged_row(table, max_blocks, block_rows, pool_blocks, s, j, &row);
+            if (st == ORC_OK) {
+                memcpy(kb + (size_t)j * W, k_pool + (size_t)row * W, sizeof(float) * (size_t)W);
+                memcpy(vb + (size_t)j * W, v_pool + (size_t)row * W, sizeof(float) * (size_t)W);
+            }
+        }
+        if (st == ORC_OK)
+            st = orc_gqa_attn(out + (size_t)s * nh * hdkv, q + (size_t)s * nh * hd, kb, vb, (int)L, pos + s, 1,
+                              nh, nk, hd, hdkv, scale, 1);
+        free(kb);
+        free(vb);
+        if (st != ORC_OK)
+            return st;
+    }
     return ORC_OK;
 }
 

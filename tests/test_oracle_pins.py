@@ -506,3 +506,71 @@ def test_f16_layer_step_reads_what_it_stored(orc):
                                    n_kv_head=nk, hd=hd, hd_kv=hdkv)
     d = np.abs(out - out32)
     assert d.max() < 2e-2 and d.max() > 0  # binary16 keeps ~3 decimal digits, and it is not a no-op
+
+
+# --------------------------------------------------------------------------- paged regions
+# "IV.2: Zero-copy KV cache": the paged cache keeps a sequence as scattered fixed-size blocks;
+# "13 . The decode loop and graph reuse", §2.2: the attention reads the cells a window names.
+# Reading through a block table must give exactly what the same rows give contiguously, in
+# whatever order the blocks sit in the pool.
+def _paged_case(r, n_seq, max_blocks, block_rows, W, shuffle):
+    n_blocks = n_seq * max_blocks
+    regions = r.standard_normal((n_seq, max_blocks * block_rows, W)).astype(np.float32)
+    perm = r.permutation(n_blocks) if shuffle else np.arange(n_blocks)
+    pool = np.empty((n_blocks * block_rows, W), np.float32)
+    table = np.empty((n_seq, max_blocks), np.int32)
+    for s in range(n_seq):
+        for b in range(max_blocks):
+            phys = int(perm[s * max_blocks + b])
+            table[s, b] = phys
+            pool[phys * block_rows:(phys + 1) * block_rows] = regions[s, b * block_rows:(b + 1) * block_rows]
+    return regions, pool, table
+
+
+@pytest.mark.parametrize("shuffle", [False, True])
+def test_paged_attention_equals_contiguous(orc, shuffle):
+    r = _rng(60 + shuffle)
+    nh, nk, hd, hdkv, block_rows, max_blocks, n_seq = 6, 2, 16, 16, 4, 5, 3
+    W = nk * hdkv
+    K, Kp, table = _paged_case(r, n_seq, max_blocks, block_rows, W, shuffle)
+    V, Vp, _ = _paged_case(np.random.default_rng(99), n_seq, max_blocks, block_rows, W, False)
+    # V follows the same table as K
+    Vp = np.empty_like(Kp)
+    for s in range(n_seq):
+        for b in range(max_blocks):
+            Vp[table[s, b] * block_rows:(table[s, b] + 1) * block_rows] = V[s, b * block_rows:(b + 1) * block_rows]
+    q = r.standard_normal((n_seq, nh, hd)).astype(np.float32)
+    pos = np.array([0, 9, 19], np.int32)  # one row, a partial block, the whole table
+    got = orc.gqa_attn_paged(q, Kp, Vp, table, block_rows, pos, nh, nk, hd, hdkv, scale=0.25)
+    for s in range(n_seq):
+        ref = orc.gqa_attn(q[s:s + 1], K[s], V[s], [pos[s]], nh, nk, hd, hdkv, scale=0.25)
+        np.testing.assert_array_equal(got[s:s + 1], ref)
+    # a window past the table is clamped to it, like a region's cap
+    far = orc.gqa_attn_paged(q, Kp, Vp, table, block_rows, [50, 50, 50], nh, nk, hd, hdkv, scale=0.25)
+    np.testing.assert_array_equal(far[2:], got[2:])
+
+
+def test_paged_append_places_rows_and_reports_missing_blocks(orc):
+    r = _rng(62)
+    block_rows, max_blocks, n_seq, W = 4, 3, 2, 8
+    _, Kp, table = _paged_case(r, n_seq, max_blocks, block_rows, W, True)
+    Vp = Kp.copy()
+    K0 = Kp.copy()
+    k = r.standard_normal((n_seq, W)).astype(np.float32)
+    v = r.standard_normal((n_seq, W)).astype(np.float32)
+    pos = [5, 11]
+    orc.kv_append_paged(Kp, Vp, table, block_rows, k, v, pos)
+    for s, p in enumerate(pos):
+        row = table[s, p // block_rows] * block_rows + p % block_rows
+        np.testing.assert_array_equal(Kp[row], k[s])
+        np.testing.assert_array_equal(Vp[row], v[s])
+    changed = np.flatnonzero(np.any(Kp != K0, axis=1))
+    assert sorted(changed) == sorted(table[s, p // block_rows] * block_rows + p % block_rows
+                                     for s, p in enumerate(pos))
+    missing = table.copy()
+    missing[0, 1] = -1
+    assert orc.kv_append_paged(Kp, Vp, missing, block_rows, k, v, [5, 0], check=False) == orc.ERR_POS
+    assert orc.kv_append_paged(Kp, Vp, table, block_rows, k, v, [12, 0], check=False) == orc.ERR_POS
+    with pytest.raises(orc.OracleError):
+        orc.gqa_attn_paged(r.standard_normal((2, 2, 8)).astype(np.float32), Kp, Vp, missing, block_rows, [6, 0],
+                           2, 1, 8, 8)
