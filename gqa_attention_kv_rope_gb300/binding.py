@@ -64,6 +64,17 @@ _SIGS = {
                                   _F, _F, _I, _P, _P, _SZ, _P, _P], _I),
     "minf_layer_attn_step_batched_f16": ([_P, _P, _P, _F, _I, _P, _P, _P, _P, _I, _P, _P, _P, _P, _I, _I64,
                                           _I, _I, _I, _I, _F, _F, _I, _P, _P, _SZ, _P, _P], _I),
+    # paged regions: a pool of blocks and a block table per sequence
+    "minf_kv_append_paged": ([_P, _P, _I64, _I, _P, _I, _I, _P, _P, _P, _I, _P, _P], _I),
+    "minf_kv_append_paged_f16": ([_P, _P, _I64, _I, _P, _I, _I, _P, _P, _P, _I, _P, _P], _I),
+    "minf_gqa_attn_decode_paged": ([_P, _P, _P, _P, _I64, _P, _I, _I, _P, _I, _I, _I, _I, _I, _F, _P, _SZ, _P, _P],
+                                   _I),
+    "minf_gqa_attn_decode_paged_f16": ([_P, _P, _P, _P, _I64, _P, _I, _I, _P, _I, _I, _I, _I, _I, _F, _P, _SZ, _P,
+                                        _P], _I),
+    "minf_layer_attn_step_paged": ([_P, _P, _P, _F, _I, _P, _P, _P, _P, _I, _P, _P, _I64, _P, _I, _I, _I, _I, _I,
+                                    _I, _F, _F, _I, _P, _P, _SZ, _P, _P], _I),
+    "minf_layer_attn_step_paged_f16": ([_P, _P, _P, _F, _I, _P, _P, _P, _P, _I, _P, _P, _I64, _P, _I, _I, _I, _I,
+                                        _I, _I, _F, _F, _I, _P, _P, _SZ, _P, _P], _I),
 }
 
 
@@ -305,3 +316,79 @@ def minf_layer_attn_step_batched_f16(xn, h, gain, eps, q, k, v, pos, k_arena, v_
         k_arena.shape[0], n_head, n_kv_head, hd, hd_kv, theta, freq_scale, style, _dev(out, name="out"),
         _dev(ws, torch.uint8, "ws"), ws.numel(), _dev(err, torch.int32, "err"), _stream(stream)),
         "minf_layer_attn_step_batched_f16")
+
+
+# ----------------------------------------------------------------------------- paged regions
+# k_pool/v_pool: [pool_rows, W] (float32, or float16 for the _f16 forms); block_table: int32
+# [n_seq, max_blocks] on the device; block_rows: rows per block.
+def _pool_dtype(name):
+    return _H if name.endswith("_f16") else torch.float32
+
+
+def _kv_append_paged(name, k_pool, v_pool, block_table, block_rows, k_rows, v_rows, pos, err, stream):
+    dt = _pool_dtype(name)
+    n_seq, max_blocks = block_table.shape
+    _check(getattr(lib(), name)(
+        _dev(k_pool, dt, "k_pool"), _dev(v_pool, dt, "v_pool"), k_pool.shape[0], k_pool.shape[1],
+        _dev(block_table, torch.int32, "block_table"), max_blocks, block_rows, _dev(k_rows, name="k_rows"),
+        _dev(v_rows, name="v_rows"), _dev(pos, torch.int32, "pos"), n_seq, _dev(err, torch.int32, "err"),
+        _stream(stream)), name)
+
+
+def minf_kv_append_paged(k_pool, v_pool, block_table, block_rows, k_rows, v_rows, pos, err, stream=None):
+    _kv_append_paged("minf_kv_append_paged", k_pool, v_pool, block_table, block_rows, k_rows, v_rows, pos, err,
+                     stream)
+
+
+def minf_kv_append_paged_f16(k_pool, v_pool, block_table, block_rows, k_rows, v_rows, pos, err, stream=None):
+    _kv_append_paged("minf_kv_append_paged_f16", k_pool, v_pool, block_table, block_rows, k_rows, v_rows, pos, err,
+                     stream)
+
+
+def _decode_paged(name, out, q, k_pool, v_pool, block_table, block_rows, pos, n_head, n_kv_head, hd, hd_kv, scale,
+                  ws, err, stream):
+    dt = _pool_dtype(name)
+    n_seq, max_blocks = block_table.shape
+    _check(getattr(lib(), name)(
+        _dev(out, name="out"), _dev(q, name="q"), _dev(k_pool, dt, "k_pool"), _dev(v_pool, dt, "v_pool"),
+        k_pool.shape[0], _dev(block_table, torch.int32, "block_table"), max_blocks, block_rows,
+        _dev(pos, torch.int32, "pos"), n_seq, n_head, n_kv_head, hd, hd_kv, scale, _dev(ws, torch.uint8, "ws"),
+        ws.numel(), _dev(err, torch.int32, "err"), _stream(stream)), name)
+
+
+def minf_gqa_attn_decode_paged(out, q, k_pool, v_pool, block_table, block_rows, pos, n_head, n_kv_head, hd, hd_kv,
+                               scale, ws, err, stream=None):
+    _decode_paged("minf_gqa_attn_decode_paged", out, q, k_pool, v_pool, block_table, block_rows, pos, n_head,
+                  n_kv_head, hd, hd_kv, scale, ws, err, stream)
+
+
+def minf_gqa_attn_decode_paged_f16(out, q, k_pool, v_pool, block_table, block_rows, pos, n_head, n_kv_head, hd,
+                                   hd_kv, scale, ws, err, stream=None):
+    _decode_paged("minf_gqa_attn_decode_paged_f16", out, q, k_pool, v_pool, block_table, block_rows, pos, n_head,
+                  n_kv_head, hd, hd_kv, scale, ws, err, stream)
+
+
+def _step_paged(name, xn, h, gain, eps, q, k, v, pos, k_pool, v_pool, block_table, block_rows, n_head, n_kv_head,
+                hd, hd_kv, theta, freq_scale, style, out, ws, err, stream):
+    dt = _pool_dtype(name)
+    n_seq, n_embd = h.shape
+    max_blocks = block_table.shape[1]
+    _check(getattr(lib(), name)(
+        _dev(xn, name="xn"), _dev(h, name="h"), _dev(gain, name="gain"), eps, n_embd,
+        _dev(q, name="q"), _dev(k, name="k"), _dev(v, name="v"), _dev(pos, torch.int32, "pos"), n_seq,
+        _dev(k_pool, dt, "k_pool"), _dev(v_pool, dt, "v_pool"), k_pool.shape[0],
+        _dev(block_table, torch.int32, "block_table"), max_blocks, block_rows, n_head, n_kv_head, hd, hd_kv, theta,
+        freq_scale, style, _dev(out, name="out"), _dev(ws, torch.uint8, "ws"), ws.numel(),
+        _dev(err, torch.int32, "err"), _stream(stream)), name)
+
+
+def minf_layer_attn_step_paged(xn, h, gain, eps, q, k, v, pos, k_pool, v_pool, block_table, block_rows, n_head,
+                               n_kv_head, hd, hd_kv, theta, freq_scale, style, out, ws, err, stream=None):
+    _step_paged("minf_layer_attn_step_paged", xn, h, gain, eps, q, k, v, pos, k_pool, v_pool, block_table,
+                block_rows, n_head, n_kv_head, hd, hd_kv, theta, freq_scale, style, out, ws, err, stream)
+
+
+def minf_layer_attn_step_paged_f16(xn, h, gain, eps, q, k, v, pos, k_pool, v_pool, block_table, block_rows, n_head,
+                                   n_kv_head, hd, hd_kv, theta, freq_scale, style, out, ws, err, stream=None):
+    _step_paged("minf_layer_attn_step_paged_f16", xn, h, gain, eps, q, k, v, pos, k_pool, v_pool, block_table,
+                block_rows, n_head, n_kv_head, hd, hd_kv, theta, freq_scale, style, out, ws, err, stream)

@@ -90,7 +90,7 @@ static int rope_kv(float *q, float *k, const float *v, const int32_t *pos, int n
                    int hd, int hd_kv, float theta, float freq_scale, int style, void *k_reg,
                    void *v_reg, int kv, const int64_t *row_off, const int32_t *caps, int cap,
                    int32_t *err, cudaStream_t s) {
-    RopeKvArgs a;
+    RopeKvArgs a = {};
     a.q = q;
     a.k = k;
     a.v = v;
@@ -124,11 +124,23 @@ static int rope_kv_append(float *q, float *k, const float *v, const int32_t *pos
                    k_reg, v_reg, kv, nullptr, nullptr, cap, err, cs(stream));
 }
 
+// A block table over a pool of K/V rows (paged regions).
+struct Paged {
+    const int32_t *table;
+    int max_blocks, block_rows, pool_blocks;
+};
+
 static int layer_prologue(float *xn, const float *h, const float *gain, float eps, int n_embd, float *q, float *k,
                           const float *v, const int32_t *pos, int nt, int nh, int nk, int hd, int hd_kv, float theta,
                           float freq_scale, int style, void *k_reg, void *v_reg, int kv, const int64_t *row_off,
-                          const int32_t *caps, int cap, int32_t *err, cudaStream_t s) {
-    RopeKvArgs a;
+                          const int32_t *caps, int cap, int32_t *err, cudaStream_t s, const Paged *pg = nullptr) {
+    RopeKvArgs a = {};
+    if (pg) {
+        a.table = pg->table;
+        a.max_blocks = pg->max_blocks;
+        a.block_rows = pg->block_rows;
+        a.pool_blocks = pg->pool_blocks;
+    }
     a.q = q;
     a.k = k;
     a.v = v;
@@ -178,7 +190,7 @@ size_t minf_attn_prefill_workspace_bytes(int nt, int n_head, int n_kv_head, int 
 static int prefill(float *out, const float *q, const void *k_reg, const void *v_reg, int kv, int cap,
                    const int32_t *pos, int nt, int nh, int nk, int hd, int hd_kv, float scale,
                    void *ws, size_t ws_bytes, int32_t *err, cudaStream_t s, bool pdl = false) {
-    PrefillArgs a;
+    PrefillArgs a = {};
     a.pdl = pdl;
     a.ws = ws;
     a.ws_bytes = ws_bytes;
@@ -204,7 +216,7 @@ static DecodeArgs decode_args(float *out, const float *q, const void *k_reg,
                               int cap, const int32_t *pos, int n_seq, int nh, int nk, int hd,
                               int hd_kv, float scale, void *ws, size_t ws_bytes, int32_t *err,
                               long long arena_rows = 0) {
-    DecodeArgs d;
+    DecodeArgs d = {};
     d.arena_rows = arena_rows;
     d.out = out;
     d.q = q;
@@ -404,6 +416,144 @@ int minf_layer_attn_step_batched_f16(float *xn, const float *h, const float *gai
 int minf_silu_mul(float *y, const float *gate, const float *up, int64_t n, minf_stream_t stream) {
     if (!y || !gate || !up || n < 0) return MINF_ERR_ARG;
     return launch_silu_mul(y, gate, up, n, cs(stream));
+}
+
+// ----------------------------------------------------------------------------- paged regions
+// "IV.2: Zero-copy KV cache": the paged cache keeps a sequence as scattered fixed-size blocks
+// of a shared pool; a table per sequence names them ("13 . The decode loop and graph reuse",
+// §2.2: the window the attention reads is an explicit input).
+
+static int check_paged(const void *k_pool, const void *v_pool, int kv, int64_t pool_rows, const int32_t *table,
+                       int max_blocks, int block_rows, Paged *pg) {
+    if (!ok_f(k_pool) || !ok_f(v_pool) || !table || pool_rows <= 0 || max_blocks <= 0) return MINF_ERR_ARG;
+    if (block_rows < 16 || block_rows > 4096 || (block_rows & (block_rows - 1))) return MINF_ERR_UNSUPPORTED;
+    if (pool_rows % block_rows || static_cast<long long>(max_blocks) * block_rows > 0x7fffffffLL - 4096 ||
+        pool_rows > 0x7fffffffLL - 4096)
+        return MINF_ERR_UNSUPPORTED;
+    (void)kv;
+    pg->table = table;
+    pg->max_blocks = max_blocks;
+    pg->block_rows = block_rows;
+    pg->pool_blocks = static_cast<int>(pool_rows / block_rows);
+    return MINF_OK;
+}
+
+static void set_paged(DecodeArgs &d, const Paged &pg, int64_t pool_rows) {
+    d.table = pg.table;
+    d.max_blocks = pg.max_blocks;
+    d.block_rows = pg.block_rows;
+    d.arena_rows = pool_rows;
+}
+
+static int kv_append_paged(void *k_pool, void *v_pool, int kv, int64_t pool_rows, int row_width,
+                           const int32_t *table, int max_blocks, int block_rows, const float *k_rows,
+                           const float *v_rows, const int32_t *pos, int n_seq, int32_t *err, minf_stream_t stream) {
+    Paged pg;
+    int st = check_paged(k_pool, v_pool, kv, pool_rows, table, max_blocks, block_rows, &pg);
+    if (st != MINF_OK) return st;
+    if (!ok_f(k_rows) || !ok_f(v_rows) || !pos || !err || n_seq < 0 || row_width <= 0 ||
+        row_width % (kv == kKvF16 ? 8 : 4))
+        return MINF_ERR_ARG;
+    return launch_kv_append_paged(k_pool, v_pool, kv, pg.pool_blocks, block_rows, row_width, table, max_blocks,
+                                  k_rows, v_rows, pos, n_seq, err, cs(stream));
+}
+
+int minf_kv_append_paged(float *k_pool, float *v_pool, int64_t pool_rows, int row_width, const int32_t *block_table,
+                         int max_blocks, int block_rows, const float *k_rows, const float *v_rows, const int32_t *pos,
+                         int n_seq, int32_t *err, minf_stream_t stream) {
+    return kv_append_paged(k_pool, v_pool, kKvF32, pool_rows, row_width, block_table, max_blocks, block_rows, k_rows,
+                           v_rows, pos, n_seq, err, stream);
+}
+
+int minf_kv_append_paged_f16(uint16_t *k_pool, uint16_t *v_pool, int64_t pool_rows, int row_width,
+                             const int32_t *block_table, int max_blocks, int block_rows, const float *k_rows,
+                             const float *v_rows, const int32_t *pos, int n_seq, int32_t *err, minf_stream_t stream) {
+    return kv_append_paged(k_pool, v_pool, kKvF16, pool_rows, row_width, block_table, max_blocks, block_rows, k_rows,
+                           v_rows, pos, n_seq, err, stream);
+}
+
+static int gqa_attn_decode_paged(float *out, const float *q, const void *k_pool, const void *v_pool, int kv,
+                                 int64_t pool_rows, const int32_t *table, int max_blocks, int block_rows,
+                                 const int32_t *pos, int n_seq, int n_head, int n_kv_head, int hd, int hd_kv,
+                                 float scale, void *ws, size_t ws_bytes, int32_t *err, minf_stream_t stream) {
+    int st = check_attn(n_head, n_kv_head, hd, hd_kv);
+    if (st != MINF_OK) return st;
+    Paged pg;
+    st = check_paged(k_pool, v_pool, kv, pool_rows, table, max_blocks, block_rows, &pg);
+    if (st != MINF_OK) return st;
+    if (!ok_f(out) || !ok_f(q) || !pos || !err || n_seq < 0) return MINF_ERR_ARG;
+    DecodeArgs d = decode_args(out, q, k_pool, v_pool, kv, nullptr, nullptr, max_blocks * block_rows, pos, n_seq,
+                               n_head, n_kv_head, hd, hd_kv, scale, ws, ws_bytes, err);
+    set_paged(d, pg, pool_rows);
+    return launch_decode(d, cs(stream));
+}
+
+int minf_gqa_attn_decode_paged(float *out, const float *q, const float *k_pool, const float *v_pool,
+                               int64_t pool_rows, const int32_t *block_table, int max_blocks, int block_rows,
+                               const int32_t *pos, int n_seq, int n_head, int n_kv_head, int hd, int hd_kv,
+                               float scale, void *ws, size_t ws_bytes, int32_t *err, minf_stream_t stream) {
+    return gqa_attn_decode_paged(out, q, k_pool, v_pool, kKvF32, pool_rows, block_table, max_blocks, block_rows, pos,
+                                 n_seq, n_head, n_kv_head, hd, hd_kv, scale, ws, ws_bytes, err, stream);
+}
+
+int minf_gqa_attn_decode_paged_f16(float *out, const float *q, const uint16_t *k_pool, const uint16_t *v_pool,
+                                   int64_t pool_rows, const int32_t *block_table, int max_blocks, int block_rows,
+                                   const int32_t *pos, int n_seq, int n_head, int n_kv_head, int hd, int hd_kv,
+                                   float scale, void *ws, size_t ws_bytes, int32_t *err, minf_stream_t stream) {
+    return gqa_attn_decode_paged(out, q, k_pool, v_pool, kKvF16, pool_rows, block_table, max_blocks, block_rows, pos,
+                                 n_seq, n_head, n_kv_head, hd, hd_kv, scale, ws, ws_bytes, err, stream);
+}
+
+static int layer_attn_step_paged(float *xn, const float *h, const float *gain, float eps, int n_embd, float *q,
+                                 float *k, const float *v, const int32_t *pos, int n_seq, void *k_pool, void *v_pool,
+                                 int kv, int64_t pool_rows, const int32_t *table, int max_blocks, int block_rows,
+                                 int n_head, int n_kv_head, int hd, int hd_kv, float theta, float freq_scale,
+                                 int style, float *out, void *ws, size_t ws_bytes, int32_t *err,
+                                 minf_stream_t stream) {
+    int st = check_attn(n_head, n_kv_head, hd, hd_kv);
+    if (st != MINF_OK) return st;
+    Paged pg;
+    st = check_paged(k_pool, v_pool, kv, pool_rows, table, max_blocks, block_rows, &pg);
+    if (st != MINF_OK) return st;
+    if (!xn || !h || n_embd <= 0 || n_seq < 0 || (style != 0 && style != 1)) return MINF_ERR_ARG;
+    if (!ok_f(q) || !ok_f(k) || !ok_f(v) || !ok_f(out) || !pos || !err) return MINF_ERR_ARG;
+    if (n_seq == 0) return MINF_OK;
+    cudaStream_t s = cs(stream);
+    const float scale = 1.0f / sqrtf(static_cast<float>(hd));
+    const int cap = max_blocks * block_rows;
+    DecodeArgs d = decode_args(out, q, k_pool, v_pool, kv, nullptr, nullptr, cap, pos, n_seq, n_head, n_kv_head, hd,
+                               hd_kv, scale, ws, ws_bytes, err);
+    set_paged(d, pg, pool_rows);
+    if (fused_step_supported(n_head, n_kv_head, hd, hd_kv, n_embd) && aligned16(h) && aligned16(xn) &&
+        (!gain || aligned16(gain))) {
+        DecodeStepExtra x = {k, v, xn, h, gain, eps, theta, freq_scale, n_embd, style, false};
+        return launch_decode_step(d, x, s);
+    }
+    st = layer_prologue(xn, h, gain, eps, n_embd, q, k, v, pos, n_seq, n_head, n_kv_head, hd, hd_kv, theta,
+                        freq_scale, style, k_pool, v_pool, kv, nullptr, nullptr, cap, err, s, &pg);
+    if (st != MINF_OK) return st;
+    return launch_decode(d, s);
+}
+
+int minf_layer_attn_step_paged(float *xn, const float *h, const float *gain, float eps, int n_embd, float *q, float *k,
+                               const float *v, const int32_t *pos, int n_seq, float *k_pool, float *v_pool,
+                               int64_t pool_rows, const int32_t *block_table, int max_blocks, int block_rows,
+                               int n_head, int n_kv_head, int hd, int hd_kv, float theta, float freq_scale, int style,
+                               float *out, void *ws, size_t ws_bytes, int32_t *err, minf_stream_t stream) {
+    return layer_attn_step_paged(xn, h, gain, eps, n_embd, q, k, v, pos, n_seq, k_pool, v_pool, kKvF32, pool_rows,
+                                 block_table, max_blocks, block_rows, n_head, n_kv_head, hd, hd_kv, theta, freq_scale,
+                                 style, out, ws, ws_bytes, err, stream);
+}
+
+int minf_layer_attn_step_paged_f16(float *xn, const float *h, const float *gain, float eps, int n_embd, float *q,
+                                   float *k, const float *v, const int32_t *pos, int n_seq, uint16_t *k_pool,
+                                   uint16_t *v_pool, int64_t pool_rows, const int32_t *block_table, int max_blocks,
+                                   int block_rows, int n_head, int n_kv_head, int hd, int hd_kv, float theta,
+                                   float freq_scale, int style, float *out, void *ws, size_t ws_bytes, int32_t *err,
+                                   minf_stream_t stream) {
+    return layer_attn_step_paged(xn, h, gain, eps, n_embd, q, k, v, pos, n_seq, k_pool, v_pool, kKvF16, pool_rows,
+                                 block_table, max_blocks, block_rows, n_head, n_kv_head, hd, hd_kv, theta, freq_scale,
+                                 style, out, ws, ws_bytes, err, stream);
 }
 
 }  // extern "C"

@@ -93,15 +93,17 @@ int launch_impl(const DecodeArgs &d, const DecodeStepExtra *x, cudaStream_t s) {
     if (!d.ws || d.ws_bytes < pl.w.total || !aligned16(d.ws)) return MINF_ERR_WORKSPACE;
     const long long units = static_cast<long long>(d.n_seq) * d.nk * pl.groups * pl.S;
     if (units > 0x7fffffffLL) return MINF_ERR_UNSUPPORTED;
-    const long long rows = d.row_off ? d.arena_rows : d.cap;
+    const long long rows = (d.row_off || d.table) ? d.arena_rows : d.cap;
     if (rows <= 0) return MINF_ERR_ARG;
-    if (rows > 0x7fffffffLL) return MINF_ERR_UNSUPPORTED;
+    if (rows > 0x7fffffffLL - 4096) return MINF_ERR_UNSUPPORTED;
     const int R = stage_rows(d.hd_kv, eb);
+    // paged: a stage is copied in pieces of one block (or one stage when blocks are larger)
+    const int box = d.table ? (d.block_rows < R ? d.block_rows : R) : R;
     CUtensorMap tk, tv;
     const uint64_t W = static_cast<uint64_t>(d.nk) * d.hd_kv;
     const CUtensorMapDataType dt = f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
-    if (!make_tensor_map_2d(&tk, d.k_reg, dt, eb, W, static_cast<uint64_t>(rows), d.hd_kv, R, false) ||
-        !make_tensor_map_2d(&tv, d.v_reg, dt, eb, W, static_cast<uint64_t>(rows), d.hd_kv, R, false))
+    if (!make_tensor_map_2d(&tk, d.k_reg, dt, eb, W, static_cast<uint64_t>(rows), d.hd_kv, box, false) ||
+        !make_tensor_map_2d(&tv, d.v_reg, dt, eb, W, static_cast<uint64_t>(rows), d.hd_kv, box, false))
         return MINF_ERR_CUDA;
     char *ws = static_cast<char *>(d.ws);
     KParams k = {};
@@ -126,6 +128,11 @@ int launch_impl(const DecodeArgs &d, const DecodeStepExtra *x, cudaStream_t s) {
     k.ws_done = k.ws_ctr + 1;
     k.min_rows = pl.min_rows;
     k.sorted = pl.sorted;
+    k.table = d.table;
+    k.max_blocks = d.max_blocks;
+    k.block_rows = d.block_rows;
+    k.box_rows = box;
+    k.pool_rows = rows;
     k.k_reg = const_cast<void *>(d.k_reg);
     k.v_reg = const_cast<void *>(d.v_reg);
     bool pdl = false;

@@ -102,6 +102,12 @@ struct KParams {
     const int32_t *pos;
     int cap, n_seq, nh, nk, hd, n_split, groups;  // groups = g / GH
     int min_rows;          // shortest unit (rows)
+    // paged regions (table non-null): logical row j of sequence s is pool row
+    // table[s*max_blocks + j/block_rows]*block_rows + j%block_rows; the pool has pool_rows rows;
+    // each stage is copied in pieces of box_rows rows (one block, or one stage if blocks are larger)
+    const int32_t *table;
+    int max_blocks, block_rows, box_rows;
+    long long pool_rows;
     int sorted;            // visit sequences longest first
     float scale_log2;
     int32_t *err;
@@ -354,10 +360,27 @@ __global__ void __launch_bounds__(kThreads, 1)
                         sm_meta[slot] = make_int2(u, st);
                         mbar_arrive(&meta_full[slot]);  // publishes the slot's unit to the consumers
                         T *kt = ring + static_cast<size_t>(slot) * (2 * R * HDKV);
-                        const int row = static_cast<int>(t.base) + t.r_begin + st * R;
                         mbar_expect_tx(&full[slot], 2 * kTileBytes);
-                        tma_load_2d(kt, &tmK, hk * HDKV, row, &full[slot]);
-                        tma_load_2d(kt + R * HDKV, &tmV, hk * HDKV, row, &full[slot]);
+                        if (!a.table) {
+                            const int row = static_cast<int>(t.base) + t.r_begin + st * R;
+                            tma_load_2d(kt, &tmK, hk * HDKV, row, &full[slot]);
+                            tma_load_2d(kt + R * HDKV, &tmV, hk * HDKV, row, &full[slot]);
+                        } else {
+                            // one copy per block piece; a block the table does not hold reads
+                            // as zeros (its rows start past the pool) and is reported
+                            for (int c = 0; c < R / a.box_rows; ++c) {
+                                const int lrow = t.r_begin + st * R + c * a.box_rows;
+                                const int blk = lrow / a.block_rows;
+                                const int b = blk < a.max_blocks ? __ldg(a.table + static_cast<size_t>(t.s) * a.max_blocks + blk)
+                                                                  : -1;
+                                const long long prow = static_cast<long long>(b) * a.block_rows + lrow % a.block_rows;
+                                const bool ok = b >= 0 && prow < a.pool_rows;
+                                if (!ok && lrow < t.L) flag_error(a.err, MINF_ERRBIT_BLOCK);
+                                const int row = ok ? static_cast<int>(prow) : static_cast<int>(a.pool_rows);
+                                tma_load_2d(kt + c * a.box_rows * HDKV, &tmK, hk * HDKV, row, &full[slot]);
+                                tma_load_2d(kt + R * HDKV + c * a.box_rows * HDKV, &tmV, hk * HDKV, row, &full[slot]);
+                            }
+                        }
                     }
                 }
                 if (!waited) {  // the unit counter lives in the workspace a preceding launch may use
@@ -460,15 +483,29 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int i = 0; i < KF4; ++i) kh[sub + 8 * i] = kx[i];
                 if (pnew >= 0) {
-                    T *Kg = static_cast<T *>(a.k_reg) + (t.base + t.p) * W + hk * HDKV;
-                    T *Vg = static_cast<T *>(a.v_reg) + (t.base + t.p) * W + hk * HDKV;
+                    long long prow = t.base + t.p;
+                    if (a.table) {  // the row's block, through the table
+                        const int b = __ldg(a.table + static_cast<size_t>(t.s) * a.max_blocks + t.p / a.block_rows);
+                        prow = static_cast<long long>(b) * a.block_rows + t.p % a.block_rows;
+                        if (b < 0 || prow >= a.pool_rows) {
+                            prow = -1;
+                            if (sub == 0) flag_error(a.err, MINF_ERRBIT_BLOCK);
+                        }
+                    }
 #pragma unroll
                     for (int i = 0; i < KF4; ++i) {
                         // staged for the same lanes, which patch the row's stage when it arrives
                         reinterpret_cast<float4 *>(sm_knew)[sub + 8 * i] = kx[i];
                         reinterpret_cast<float4 *>(sm_vnew)[sub + 8 * i] = vx[i];
-                        st4(Kg, sub + 8 * i, kx[i]);
-                        st4(Vg, sub + 8 * i, vx[i]);
+                    }
+                    if (prow >= 0) {
+                        T *Kg = static_cast<T *>(a.k_reg) + prow * W + hk * HDKV;
+                        T *Vg = static_cast<T *>(a.v_reg) + prow * W + hk * HDKV;
+#pragma unroll
+                        for (int i = 0; i < KF4; ++i) {
+                            st4(Kg, sub + 8 * i, kx[i]);
+                            st4(Vg, sub + 8 * i, vx[i]);
+                        }
                     }
                 }
             }

@@ -212,6 +212,52 @@ int launch_kv_append(void *k_reg, void *v_reg, int kv, int cap, int W, const flo
     return cudaPeekAtLastError() == cudaSuccess ? MINF_OK : MINF_ERR_CUDA;
 }
 
+// One row per sequence through a block table ("IV.2: Zero-copy KV cache": the paged cache
+// keeps a sequence as scattered fixed-size blocks).
+template <typename T>
+__global__ void __launch_bounds__(256) kv_append_paged_kernel(T *k_pool, T *v_pool, int pool_blocks, int block_rows,
+                                                              int W, const int32_t *table, int max_blocks,
+                                                              const float *k_rows, const float *v_rows,
+                                                              const int32_t *pos, int n_seq, int32_t *err) {
+    const int w4 = W >> 2;
+    const long long total = static_cast<long long>(n_seq) * w4;
+    for (long long idx = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; idx < total;
+         idx += static_cast<long long>(gridDim.x) * blockDim.x) {
+        const int s = static_cast<int>(idx / w4);
+        const int c = static_cast<int>(idx % w4);
+        const int p = __ldg(pos + s);
+        if (p < 0 || p >= max_blocks * block_rows) {
+            if (c == 0) flag_error(err, MINF_ERRBIT_STORE_POS);
+            continue;
+        }
+        const int b = __ldg(table + static_cast<size_t>(s) * max_blocks + p / block_rows);
+        if (b < 0 || b >= pool_blocks) {
+            if (c == 0) flag_error(err, MINF_ERRBIT_BLOCK);
+            continue;
+        }
+        const size_t dst = (static_cast<size_t>(b) * block_rows + p % block_rows) * w4 + c;
+        const size_t src = static_cast<size_t>(s) * w4 + c;
+        put4(k_pool, dst, reinterpret_cast<const float4 *>(k_rows)[src]);
+        put4(v_pool, dst, reinterpret_cast<const float4 *>(v_rows)[src]);
+    }
+}
+
+int launch_kv_append_paged(void *k_pool, void *v_pool, int kv, int pool_blocks, int block_rows, int W,
+                           const int32_t *table, int max_blocks, const float *k_rows, const float *v_rows,
+                           const int32_t *pos, int n_seq, int32_t *err, cudaStream_t s) {
+    if (n_seq == 0) return MINF_OK;
+    const long long work = static_cast<long long>(n_seq) * (W / 4);
+    if (kv == kKvF16)
+        kv_append_paged_kernel<<<grid_for(work, 256), 256, 0, s>>>(
+            static_cast<__half *>(k_pool), static_cast<__half *>(v_pool), pool_blocks, block_rows, W, table,
+            max_blocks, k_rows, v_rows, pos, n_seq, err);
+    else
+        kv_append_paged_kernel<<<grid_for(work, 256), 256, 0, s>>>(
+            static_cast<float *>(k_pool), static_cast<float *>(v_pool), pool_blocks, block_rows, W, table,
+            max_blocks, k_rows, v_rows, pos, n_seq, err);
+    return cudaPeekAtLastError() == cudaSuccess ? MINF_OK : MINF_ERR_CUDA;
+}
+
 // ----------------------------------------------------------------------------- RoPE + store
 // One sweep per token over three kinds of work item: a q pair, a k pair (rotated, written
 // back in place and into the K region), and a float4 of v (copied into the V region).
@@ -229,8 +275,14 @@ __device__ __forceinline__ void rope_kv_append_items(const RopeKvArgs &a, const 
         int r = static_cast<int>(idx % per_tok);
         const int p = __ldg(a.pos + t);
         const int cap_t = a.caps ? __ldg(a.caps + t) : a.cap;
-        const long long base = a.row_off ? __ldg(a.row_off + t) : 0;
-        const bool store_ok = p >= 0 && p < cap_t;
+        long long srow = (a.row_off ? __ldg(a.row_off + t) : 0) + p;  // the stored row
+        const bool in_range = p >= 0 && p < cap_t;
+        bool store_ok = in_range;
+        if (a.table && in_range) {  // paged: the row's block, through the table
+            const int b = __ldg(a.table + static_cast<size_t>(t) * a.max_blocks + p / a.block_rows);
+            srow = static_cast<long long>(b) * a.block_rows + p % a.block_rows;
+            store_ok = b >= 0 && b < a.pool_blocks;
+        }
         if (r < nq) {  // q pair
             if (p < 0) {
                 if (r == 0) flag_error(a.err, MINF_ERRBIT_ROPE_POS);
@@ -253,7 +305,7 @@ __device__ __forceinline__ void rope_kv_append_items(const RopeKvArgs &a, const 
             row[i0] = x0;
             row[i1] = x1;
             if (store_ok) {
-                T *dst = static_cast<T *>(a.k_reg) + (static_cast<size_t>(base) + p) * W + h * a.hd_kv;
+                T *dst = static_cast<T *>(a.k_reg) + static_cast<size_t>(srow) * W + h * a.hd_kv;
                 put1(dst, i0, x0);
                 put1(dst, i1, x1);
             }
@@ -261,11 +313,11 @@ __device__ __forceinline__ void rope_kv_append_items(const RopeKvArgs &a, const 
         }
         r -= nkp;  // float4 of v
         if (!store_ok) {
-            if (r == 0) flag_error(a.err, MINF_ERRBIT_STORE_POS);
+            if (r == 0) flag_error(a.err, in_range ? MINF_ERRBIT_BLOCK : MINF_ERRBIT_STORE_POS);
             continue;
         }
         const float4 v = reinterpret_cast<const float4 *>(a.v)[static_cast<size_t>(t) * nv + r];
-        put4(static_cast<T *>(a.v_reg), (static_cast<size_t>(base) + p) * nv + r, v);
+        put4(static_cast<T *>(a.v_reg), static_cast<size_t>(srow) * nv + r, v);
     }
 }
 

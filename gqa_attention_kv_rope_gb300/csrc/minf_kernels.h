@@ -23,6 +23,10 @@ struct RopeKvArgs {
     int cap;
     int nt, nh, nk, hd, hd_kv, style;
     int32_t *err;
+    // paged regions (table non-null): token t is sequence t's token; its row p is pool row
+    // table[t*max_blocks + p/block_rows]*block_rows + p%block_rows; cap = max_blocks*block_rows
+    const int32_t *table;
+    int max_blocks, block_rows, pool_blocks;
 };
 
 struct DecodeArgs {
@@ -40,6 +44,11 @@ struct DecodeArgs {
     int32_t *err;
     void *ws;
     size_t ws_bytes;
+    // paged regions (table non-null): the pool has arena_rows rows in blocks of block_rows;
+    // sequence s's row j is pool row table[s*max_blocks + j/block_rows]*block_rows + j%block_rows,
+    // and cap = max_blocks*block_rows
+    const int32_t *table;
+    int max_blocks, block_rows;
 };
 
 int launch_rms_norm(float *y, const float *x, const float *w, int rows, int n, float eps,
@@ -49,6 +58,10 @@ int launch_rope(float *x, const int32_t *pos, int nt, int nh, int hd, float thet
 int launch_kv_append(void *k_reg, void *v_reg, int kv, int cap, int W, const float *k_rows,
                      const float *v_rows, const int32_t *pos, int nt, int32_t *err,
                      cudaStream_t s);
+// One row per sequence through a block table (the pool has pool_blocks blocks).
+int launch_kv_append_paged(void *k_pool, void *v_pool, int kv, int pool_blocks, int block_rows, int W,
+                           const int32_t *table, int max_blocks, const float *k_rows, const float *v_rows,
+                           const int32_t *pos, int n_seq, int32_t *err, cudaStream_t s);
 int launch_rope_kv_append(const RopeKvArgs &a, float theta, float freq_scale, cudaStream_t s);
 
 struct NormArgs {

@@ -71,7 +71,7 @@ extern "C" int minf_gqa_attn_decode_static_ws(float *out, const float *q, const 
     // The merge tickets must start at zero; a previous call (or one that stopped early) may
     // have left anything behind, so the part this call uses is cleared first.
     if (cudaMemsetAsync(ws, 0, need, s) != cudaSuccess) return MINF_ERR_CUDA;
-    DecodeArgs d;
+    DecodeArgs d = {};
     d.out = out;
     d.q = q;
     d.k_reg = k_reg;

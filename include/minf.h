@@ -65,6 +65,10 @@ enum {
 #define MINF_ERRBIT_TIMEOUT 0x8    /* an internal pipeline wait exceeded its time budget (200 ms);
                                       the call's outputs are invalid.  Kernels bound every wait
                                       so that a fault in the pipeline returns instead of hanging. */
+#define MINF_ERRBIT_BLOCK 0x10     /* paged regions: a block the window or the store needs is
+                                      missing from the table (id < 0 or past the pool); its rows
+                                      read as zeros, the store is skipped, the outputs of that
+                                      sequence are invalid */
 
 /* Human-readable name of a status code (static storage). */
 MINF_API const char *minf_status_string(int status);
@@ -292,6 +296,58 @@ MINF_API int minf_layer_attn_step_batched_f16(float *xn, const float *h, const f
                                               int64_t arena_rows, int n_head, int n_kv_head, int hd, int hd_kv,
                                               float theta, float freq_scale, int style, float *out, void *ws,
                                               size_t ws_bytes, int32_t *err, minf_stream_t stream);
+
+/*
+ * Paged regions ([P2]: the paged cache keeps a sequence as scattered fixed-size
+ * blocks, so it has no contiguous view to lend; [P3] §2.2: the window the
+ * attention reads is an explicit input).  A pool k_pool / v_pool of pool_rows
+ * rows of width W (fp32, or binary16 for the _f16 forms) is cut into blocks of
+ * block_rows rows; block_table is an int32 device array [n_seq, max_blocks] of
+ * block ids: logical row j of sequence s is pool row
+ *   block_table[s * max_blocks + j / block_rows] * block_rows + j % block_rows,
+ * and the sequence's capacity is cap = max_blocks * block_rows.  One token per
+ * sequence, at pos[s]: the window is rows [0, min(pos[s] + 1, cap)) as for
+ * contiguous regions, and the store writes logical row pos[s].  Block ids may
+ * differ per call (a graph replays with a new table as with new positions).
+ * block_rows: a power of two in [16, 4096]; pool_rows a multiple of it.
+ * Workspace: minf_attn_decode_workspace_bytes(n_seq, ..., cap).
+ * Device errors: as the contiguous forms, plus MINF_ERRBIT_BLOCK when a block
+ * the window or the store needs has an id < 0 or past the pool (its rows read
+ * as zeros and the store is skipped; that sequence's outputs are invalid).
+ * Errors: MINF_ERR_UNSUPPORTED for block_rows outside the above; otherwise as the
+ * contiguous forms.
+ */
+MINF_API int minf_kv_append_paged(float *k_pool, float *v_pool, int64_t pool_rows, int row_width,
+                                  const int32_t *block_table, int max_blocks, int block_rows, const float *k_rows,
+                                  const float *v_rows, const int32_t *pos, int n_seq, int32_t *err,
+                                  minf_stream_t stream);
+MINF_API int minf_kv_append_paged_f16(uint16_t *k_pool, uint16_t *v_pool, int64_t pool_rows, int row_width,
+                                      const int32_t *block_table, int max_blocks, int block_rows,
+                                      const float *k_rows, const float *v_rows, const int32_t *pos, int n_seq,
+                                      int32_t *err, minf_stream_t stream);
+MINF_API int minf_gqa_attn_decode_paged(float *out, const float *q, const float *k_pool, const float *v_pool,
+                                        int64_t pool_rows, const int32_t *block_table, int max_blocks,
+                                        int block_rows, const int32_t *pos, int n_seq, int n_head, int n_kv_head,
+                                        int hd, int hd_kv, float scale, void *ws, size_t ws_bytes, int32_t *err,
+                                        minf_stream_t stream);
+MINF_API int minf_gqa_attn_decode_paged_f16(float *out, const float *q, const uint16_t *k_pool,
+                                            const uint16_t *v_pool, int64_t pool_rows, const int32_t *block_table,
+                                            int max_blocks, int block_rows, const int32_t *pos, int n_seq,
+                                            int n_head, int n_kv_head, int hd, int hd_kv, float scale, void *ws,
+                                            size_t ws_bytes, int32_t *err, minf_stream_t stream);
+MINF_API int minf_layer_attn_step_paged(float *xn, const float *h, const float *gain, float eps, int n_embd,
+                                        float *q, float *k, const float *v, const int32_t *pos, int n_seq,
+                                        float *k_pool, float *v_pool, int64_t pool_rows, const int32_t *block_table,
+                                        int max_blocks, int block_rows, int n_head, int n_kv_head, int hd,
+                                        int hd_kv, float theta, float freq_scale, int style, float *out, void *ws,
+                                        size_t ws_bytes, int32_t *err, minf_stream_t stream);
+MINF_API int minf_layer_attn_step_paged_f16(float *xn, const float *h, const float *gain, float eps, int n_embd,
+                                            float *q, float *k, const float *v, const int32_t *pos, int n_seq,
+                                            uint16_t *k_pool, uint16_t *v_pool, int64_t pool_rows,
+                                            const int32_t *block_table, int max_blocks, int block_rows, int n_head,
+                                            int n_kv_head, int hd, int hd_kv, float theta, float freq_scale,
+                                            int style, float *out, void *ws, size_t ws_bytes, int32_t *err,
+                                            minf_stream_t stream);
 
 /*
  * SiLU times up ([P1] §3.2.5): y = gate / (1 + e^-gate) * up over n elements.
