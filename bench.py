@@ -504,6 +504,68 @@ def run_decode_loop(m, torch, wl, dev):
             "kv_read_gbs": round(kv / (total_ms * 1e-3) / 1e9, 1), "err": int(err.item())}
 
 
+def run_batched_paged(m, torch, wl, dev, steps, block_rows=64):
+    """The batched workload (64 sequences, lengths ~ U{1..8192}, 28 layers) with each sequence's
+    rows in scattered 64-row blocks of one pool per layer, read through a block table."""
+    g = wl.QWEN3_06B
+    lengths = wl.batched_lengths(seed=0)
+    n = len(lengths)
+    blocks = [-(-(ln + 1 + wl.KV_HEADROOM_ROWS) // block_rows) for ln in lengths]
+    max_blocks, pool_blocks = max(blocks), sum(blocks)
+    perm = torch.randperm(pool_blocks, generator=torch.Generator().manual_seed(wl.sub_seed("paged", 0)))
+    table = torch.full((n, max_blocks), -1, dtype=torch.int32)
+    at = 0
+    for s, nb in enumerate(blocks):
+        table[s, :nb] = perm[at:at + nb].to(torch.int32)
+        at += nb
+    table = table.to(dev)
+    pool_rows = pool_blocks * block_rows
+    K = torch.empty(g.n_layer, pool_rows, g.row_width, device=dev)
+    V = torch.empty(g.n_layer, pool_rows, g.row_width, device=dev)
+    gen = torch.Generator(device=dev)
+    for layer in range(g.n_layer):
+        gen.manual_seed(wl.sub_seed("paged", layer, "K"))
+        K[layer].normal_(generator=gen)
+        gen.manual_seed(wl.sub_seed("paged", layer, "V"))
+        V[layer].normal_(generator=gen)
+    pos = torch.tensor(lengths, dtype=torch.int32, device=dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    ws = m.kv.decode_workspace(n, g.n_head, g.n_kv_head, g.hd_kv, max_blocks * block_rows, device=dev)
+    L = []
+    for layer in range(g.n_layer):
+        d = {k: v.to(dev) for k, v in wl.layer_inputs(g, "batched", layer, n).items()}
+        d["xn"] = torch.empty_like(d["h"])
+        d["out"] = torch.empty(n, g.out_width, device=dev)
+        L.append(d)
+
+    def step():
+        for layer in range(g.n_layer):
+            d = L[layer]
+            m.binding.minf_layer_attn_step_paged(d["xn"], d["h"], d["gain"], g.eps, d["q"], d["k"], d["v"], pos,
+                                                 K[layer], V[layer], table, block_rows, g.n_head, g.n_kv_head, g.hd,
+                                                 g.hd_kv, g.theta, 1.0, 0, d["out"], ws, err)
+
+    stream = torch.cuda.Stream()
+    graph = capture(torch, stream, step)
+    for _ in range(2):
+        graph.replay()
+    torch.cuda.synchronize()
+    a, b = Timer(torch, stream).pair()
+    with torch.cuda.stream(stream):
+        a.record(stream)
+        for _ in range(steps):
+            graph.replay()
+        b.record(stream)
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / steps
+    kv = g.n_layer * sum(2 * (ln + 1) * g.row_width * 4 for ln in lengths)
+    res = {"step_ms": round(ms, 3), "kv_read_gbs": round(kv / (ms * 1e-3) / 1e9, 1), "kv_bytes_per_step": kv,
+           "block_rows": block_rows, "err": int(err.item())}
+    del graph, K, V
+    torch.cuda.empty_cache()
+    return res
+
+
 def run_long_context_f16(m, torch, wl, dev, steps):
     """The headline workload (28 layers, nkv = 40960) with binary16 regions: the bytes the
     step reads halve, the arithmetic stays fp32."""
@@ -741,6 +803,7 @@ def main(argv=None):
         secondary["prefill_layer_us"] = layer_us
         secondary["decode_loop"] = run_decode_loop(m, torch, wl, dev)
         secondary["batched_decode"] = run_batched(m, torch, wl, dev, max(3, args.steps // 4))
+        secondary["batched_decode_paged"] = run_batched_paged(m, torch, wl, dev, max(3, args.steps // 4))
         secondary["long_context_f16"] = run_long_context_f16(m, torch, wl, dev, max(5, args.steps // 2))
         secondary["batched_decode_f16"] = run_batched(m, torch, wl, dev, max(3, args.steps // 4),
                                                       dtype=torch.float16)
