@@ -34,6 +34,7 @@ _f32p = ctypes.POINTER(ctypes.c_float)
 _f64p = ctypes.POINTER(ctypes.c_double)
 _i32p = ctypes.POINTER(ctypes.c_int32)
 _u16p = ctypes.POINTER(ctypes.c_uint16)
+_u8p = ctypes.POINTER(ctypes.c_uint8)
 
 
 def build(force: bool = False) -> str:
@@ -102,6 +103,15 @@ def _load():
                                            ctypes.c_int, _i32p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                            ctypes.c_int, ctypes.c_int, ctypes.c_float]
         lib.orc_gqa_attn_paged.restype = ctypes.c_int
+        _u8p = ctypes.POINTER(ctypes.c_uint8)
+        lib.orc_q8_row_bytes.argtypes = [ctypes.c_int]
+        lib.orc_q8_row_bytes.restype = ctypes.c_long
+        lib.orc_q8_quantize_rows.argtypes = [_u8p, _f32p, ctypes.c_long, ctypes.c_int]
+        lib.orc_q8_quantize_rows.restype = None
+        lib.orc_q8_dequant_rows.argtypes = [_f32p, _u8p, ctypes.c_long, ctypes.c_int]
+        lib.orc_q8_dequant_rows.restype = None
+        lib.orc_kv_append_q8.argtypes = [_u8p, _u8p, ctypes.c_int, ctypes.c_int, _f32p, _f32p, _i32p, ctypes.c_int]
+        lib.orc_kv_append_q8.restype = ctypes.c_int
         _lib = lib
         return lib
 
@@ -351,3 +361,43 @@ def gqa_attn_paged(q, k_pool, v_pool, table, block_rows: int, pos, n_head: int, 
     if st != OK:
         raise OracleError(st, "gqa_attn_paged")
     return out
+
+
+# ----------------------------------------------------------------------------- Q8_0 cache
+def q8_row_bytes(W: int) -> int:
+    """Bytes of one Q8_0 row of W values: W quants, W/32 binary16 scales, padding to 16 bytes."""
+    return int(_load().orc_q8_row_bytes(W))
+
+
+def q8_quantize(x) -> np.ndarray:
+    """[rows, W] float32 -> [rows, q8_row_bytes(W)] uint8."""
+    x = _f32(x)
+    rows, W = x.shape
+    out = np.empty((rows, q8_row_bytes(W)), dtype=np.uint8)
+    _load().orc_q8_quantize_rows(_p(out, _u8p), _p(x, _f32p), rows, W)
+    return out
+
+
+def q8_dequant(q, W: int) -> np.ndarray:
+    """[rows, q8_row_bytes(W)] uint8 -> [rows, W] float32 (the values the rows hold)."""
+    q = np.ascontiguousarray(q, dtype=np.uint8)
+    rows = q.shape[0]
+    out = np.empty((rows, W), dtype=np.float32)
+    _load().orc_q8_dequant_rows(_p(out, _f32p), _p(q, _u8p), rows, W)
+    return out
+
+
+def kv_append_q8(k_reg, v_reg, W: int, k_rows, v_rows, pos, check=True) -> int:
+    """Q8_0 regions [cap, q8_row_bytes(W)] uint8 (modified in place), fp32 rows [nt, W]."""
+    for r in (k_reg, v_reg):
+        if r.dtype != np.uint8 or not r.flags.c_contiguous:
+            raise TypeError("regions must be C-contiguous uint8 arrays")
+    cap = k_reg.shape[0]
+    k_rows = _f32(k_rows).reshape(-1, W)
+    v_rows = _f32(v_rows).reshape(-1, W)
+    pos = _i32(pos)
+    st = _load().orc_kv_append_q8(_p(k_reg, _u8p), _p(v_reg, _u8p), cap, W, _p(k_rows, _f32p), _p(v_rows, _f32p),
+                                  _p(pos, _i32p), pos.shape[0])
+    if check and st != OK:
+        raise OracleError(st, "kv_append_q8")
+    return st

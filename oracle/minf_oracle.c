@@ -23,7 +23,8 @@
  *   orc_rope_freqs, orc_rms_norm, orc_rope, orc_kv_append, orc_gqa_attn,
  *   orc_attn_bruteforce_f64, orc_silu_mul, orc_layer_attn_step,
  *   orc_f32_to_f16, orc_f16_to_f32, orc_kv_append_f16,
- *   orc_layer_attn_step_f16, orc_kv_append_paged, orc_gqa_attn_paged -- all pinned.
+ *   orc_layer_attn_step_f16, orc_kv_append_paged, orc_gqa_attn_paged,
+ *   orc_q8_quantize_row, orc_q8_dequant_row, orc_kv_append_q8 -- all pinned.
  */
 #include <math.h>
 #include <pthread.h>
@@ -37,6 +38,9 @@
 #define ORC_ERR_ARG 1
 #define ORC_ERR_GEOMETRY 2
 #define ORC_ERR_POS 4
+
+uint16_t orc_f32_to_f16(float f);
+float orc_f16_to_f32(uint16_t h);
 
 #define ORC_MAX_HALF 128 /* [P1] §3.2.2: the angular-speed table holds hd/2 <= 128 entries */
 
@@ -256,6 +260,94 @@ int orc_gqa_attn(float *out, const float *q, const float *k_reg, const float *v_
     for (int w = 0; w < n_threads; ++w)
         if (jobs[w].status != ORC_OK)
             return jobs[w].status;
+    return ORC_OK;
+}
+
+/* ------------------------------------------------------------------------ */
+/* The Q8_0 cache.  [P1] §2.5: the store quantizes each K/V row into Q8_0 block
+ * rows -- blocks of 32 consecutive values, each one f16 scale and 32 int8
+ * quants (34 bytes per 32 values, 3.76x smaller than f32) -- and the attention
+ * read dequantizes the window it uses.  The pages give the block format but not
+ * the quantizer; the reading taken is the symmetric absolute-maximum one the
+ * format is built for: d = max|x| / 127, q = round(x / d) (nearest, halves away
+ * from zero, so |q| <= 127), computed as x * (1/d) in fp32 with d = 0 giving
+ * q = 0; the block keeps f16(d) and reads back x' = f16(d) * q.
+ * Row layout (bytes): the W quants of the row in order, then its W/32 scales
+ * (binary16, block order), then zero padding to a multiple of 16 bytes. */
+long orc_q8_row_bytes(int W)
+{
+    long scales = (long)(W / 32) * 2;
+    return (long)W + ((scales + 15) / 16) * 16;
+}
+
+void orc_q8_quantize_row(uint8_t *dst, const float *x, int W)
+{
+    int nb = W / 32;
+    long rb = orc_q8_row_bytes(W);
+    memset(dst, 0, (size_t)rb);
+    for (int b = 0; b < nb; ++b) {
+        float amax = 0.0f;
+        for (int j = 0; j < 32; ++j) {
+            float a = fabsf(x[32 * b + j]);
+            if (a > amax)
+                amax = a;
+        }
+        float d = amax / 127.0f;
+        float id = d != 0.0f ? 1.0f / d : 0.0f;
+        for (int j = 0; j < 32; ++j) {
+            float qf = roundf(x[32 * b + j] * id);
+            int8_t qi = (int8_t)qf;
+            memcpy(dst + 32 * b + j, &qi, 1);
+        }
+        uint16_t h = orc_f32_to_f16(d);
+        memcpy(dst + W + 2 * b, &h, 2);
+    }
+}
+
+void orc_q8_dequant_row(float *x, const uint8_t *src, int W)
+{
+    int nb = W / 32;
+    for (int b = 0; b < nb; ++b) {
+        uint16_t h;
+        memcpy(&h, src + W + 2 * b, 2);
+        float d = orc_f16_to_f32(h);
+        for (int j = 0; j < 32; ++j) {
+            int8_t qi;
+            memcpy(&qi, src + 32 * b + j, 1);
+            x[32 * b + j] = d * (float)qi;
+        }
+    }
+}
+
+void orc_q8_quantize_rows(uint8_t *dst, const float *x, long rows, int W)
+{
+    long rb = orc_q8_row_bytes(W);
+    for (long r = 0; r < rows; ++r)
+        orc_q8_quantize_row(dst + r * rb, x + r * W, W);
+}
+
+void orc_q8_dequant_rows(float *x, const uint8_t *src, long rows, int W)
+{
+    long rb = orc_q8_row_bytes(W);
+    for (long r = 0; r < rows; ++r)
+        orc_q8_dequant_row(x + r * W, src + r * rb, W);
+}
+
+/* The KV store into Q8_0 regions ([cap, row_bytes] bytes): the same placement
+ * as orc_kv_append, each row quantized on the way in. */
+int orc_kv_append_q8(uint8_t *k_reg, uint8_t *v_reg, int cap, int W, const float *k_rows, const float *v_rows,
+                     const int32_t *pos, int nt)
+{
+    if (cap < 0 || W <= 0 || W % 32 || nt < 0)
+        return ORC_ERR_ARG;
+    long rb = orc_q8_row_bytes(W);
+    for (int t = 0; t < nt; ++t) {
+        int p = pos[t];
+        if (p < 0 || p >= cap)
+            return ORC_ERR_POS;
+        orc_q8_quantize_row(k_reg + (size_t)p * rb, k_rows + (size_t)t * W, W);
+        orc_q8_quantize_row(v_reg + (size_t)p * rb, v_rows + (size_t)t * W, W);
+    }
     return ORC_OK;
 }
 

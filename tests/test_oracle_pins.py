@@ -574,3 +574,80 @@ def test_paged_append_places_rows_and_reports_missing_blocks(orc):
     with pytest.raises(orc.OracleError):
         orc.gqa_attn_paged(r.standard_normal((2, 2, 8)).astype(np.float32), Kp, Vp, missing, block_rows, [6, 0],
                            2, 1, 8, 8)
+
+
+# --------------------------------------------------------------------------- Q8_0 cache
+# "11 . Attention, vec ops, and the KV cache", §2.5: Q8_0 block rows, 32 values to a block of one
+# f16 scale and 32 int8 quants (34 bytes), 3.76x smaller than f32; the store quantizes and the
+# read dequantizes.  Quantizer: d = max|x|/127, q = round(x/d), halves away from zero.
+def _q8_parts(q, W):
+    quants = q[:, :W].view(np.int8)
+    scales = q[:, W:W + W // 16].copy().view(np.uint16)
+    return quants, scales
+
+
+def test_q8_row_layout_and_size(orc):
+    assert orc.q8_row_bytes(1024) == 1088          # 32 blocks of 34 bytes: the pages' 3.76x
+    assert 4 * 1024 / orc.q8_row_bytes(1024) == pytest.approx(3.7647, abs=1e-4)
+    assert orc.q8_row_bytes(128) == 144             # 136 bytes, padded to a multiple of 16
+    assert orc.q8_row_bytes(64) == 80
+    x = _rng(70).standard_normal((3, 128)).astype(np.float32)
+    q = orc.q8_quantize(x)
+    assert q.shape == (3, 144) and not q[:, 136:].any()  # the padding is zero
+
+
+def test_q8_exact_when_the_block_is_on_the_grid(orc):
+    # values k * 2^-5 with max |k| = 127: d = 2^-5 exactly, so q = k and the read-back is exact
+    r = _rng(71)
+    k = r.integers(-127, 128, size=(4, 64))
+    k[:, 0] = 127
+    k[:, 32] = -127
+    x = (k * 2.0 ** -5).astype(np.float32)
+    q = orc.q8_quantize(x)
+    quants, scales = _q8_parts(q, 64)
+    np.testing.assert_array_equal(quants, k)
+    assert np.all(scales == 0x2800)                  # binary16 of 2^-5
+    np.testing.assert_array_equal(orc.q8_dequant(q, 64), x)
+
+
+def test_q8_rounding_ties_zero_blocks_and_symmetry(orc):
+    x = np.zeros((2, 32), np.float32)
+    x[0, :4] = [127.0, 2.5, -2.5, 0.5]               # d = 1: halves round away from zero
+    q = orc.q8_quantize(x)
+    quants, scales = _q8_parts(q, 32)
+    assert list(quants[0, :4]) == [127, 3, -3, 1]
+    assert scales[0, 0] == 0x3C00 and scales[1, 0] == 0 and not quants[1].any()  # an all-zero block
+    np.testing.assert_array_equal(orc.q8_dequant(q, 32)[1], np.zeros(32, np.float32))
+    y = _rng(72).standard_normal((5, 96)).astype(np.float32)
+    qa, qb = orc.q8_quantize(y), orc.q8_quantize(-y)
+    np.testing.assert_array_equal(_q8_parts(qa, 96)[0], -_q8_parts(qb, 96)[0].astype(np.int16))
+    np.testing.assert_array_equal(_q8_parts(qa, 96)[1], _q8_parts(qb, 96)[1])
+
+
+def test_q8_error_bound(orc):
+    # |x - x'| <= d/2 from the rounding, plus |q| * |f16(d) - d| from the scale, where binary16
+    # rounds d to within half an ulp: 2^-11 * d for normal scales, 2^-25 for subnormal ones
+    r = _rng(73)
+    x = (r.standard_normal((200, 256)) * np.exp2(r.uniform(-10, 10, (200, 1)))).astype(np.float32)
+    back = orc.q8_dequant(orc.q8_quantize(x), 256)
+    d = np.abs(x).reshape(200, 8, 32).max(axis=2) / 127.0
+    bound = np.repeat((0.5 * d + 127 * np.maximum(2.0 ** -11 * d, 2.0 ** -25)) * (1 + 1e-5), 32, axis=1)
+    assert np.all(np.abs(back - x) <= bound)
+    assert np.abs(back - x).max() > 0                # and it is not a copy
+
+
+def test_kv_append_q8_placement_and_errors(orc):
+    r = _rng(74)
+    cap, W = 7, 64
+    rb = orc.q8_row_bytes(W)
+    K0 = r.integers(0, 256, size=(cap, rb)).astype(np.uint8)
+    Kr, Vr = K0.copy(), K0.copy()
+    k = r.standard_normal((2, W)).astype(np.float32)
+    v = r.standard_normal((2, W)).astype(np.float32)
+    orc.kv_append_q8(Kr, Vr, W, k, v, [6, 1])
+    np.testing.assert_array_equal(Kr[[6, 1]], orc.q8_quantize(k))
+    np.testing.assert_array_equal(Vr[[6, 1]], orc.q8_quantize(v))
+    keep = [0, 2, 3, 4, 5]
+    np.testing.assert_array_equal(Kr[keep], K0[keep])
+    assert orc.kv_append_q8(Kr, Vr, W, k, v, [cap, 0], check=False) == orc.ERR_POS
+    assert orc.kv_append_q8(Kr, Vr, W, k[:1], v[:1], [-1], check=False) == orc.ERR_POS
