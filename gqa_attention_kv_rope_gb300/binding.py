@@ -64,6 +64,22 @@ _SIGS = {
                                   _F, _F, _I, _P, _P, _SZ, _P, _P], _I),
     "minf_layer_attn_step_batched_f16": ([_P, _P, _P, _F, _I, _P, _P, _P, _P, _I, _P, _P, _P, _P, _I, _I64,
                                           _I, _I, _I, _I, _F, _F, _I, _P, _P, _SZ, _P, _P], _I),
+    # Q8_0 regions (torch.uint8 tensors of rows of minf_q8_row_bytes(W) bytes)
+    "minf_q8_row_bytes": ([_I], _SZ),
+    "minf_kv_append_q8": ([_P, _P, _I, _I, _P, _P, _P, _I, _P, _P], _I),
+    "minf_rope_kv_append_q8": ([_P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _F, _I, _P, _P, _I, _P, _P], _I),
+    "minf_gqa_attn_decode_q8": ([_P, _P, _P, _P, _P, _P, _I, _I64, _P, _I, _I, _I, _I, _I, _F, _P, _SZ, _P, _P],
+                                _I),
+    "minf_gqa_attn_prefill_q8": ([_P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _I, _F, _P, _SZ, _P, _P], _I),
+    "minf_layer_attn_step_q8": ([_P, _P, _P, _F, _I, _P, _P, _P, _P, _I, _P, _P, _I, _I, _I, _I, _I,
+                                 _F, _F, _I, _P, _P, _SZ, _P, _P], _I),
+    "minf_layer_attn_step_batched_q8": ([_P, _P, _P, _F, _I, _P, _P, _P, _P, _I, _P, _P, _P, _P, _I, _I64,
+                                         _I, _I, _I, _I, _F, _F, _I, _P, _P, _SZ, _P, _P], _I),
+    "minf_kv_append_paged_q8": ([_P, _P, _I64, _I, _P, _I, _I, _P, _P, _P, _I, _P, _P], _I),
+    "minf_gqa_attn_decode_paged_q8": ([_P, _P, _P, _P, _I64, _P, _I, _I, _P, _I, _I, _I, _I, _I, _F, _P, _SZ, _P,
+                                       _P], _I),
+    "minf_layer_attn_step_paged_q8": ([_P, _P, _P, _F, _I, _P, _P, _P, _P, _I, _P, _P, _I64, _P, _I, _I, _I, _I,
+                                       _I, _I, _F, _F, _I, _P, _P, _SZ, _P, _P], _I),
     # paged regions: a pool of blocks and a block table per sequence
     "minf_kv_append_paged": ([_P, _P, _I64, _I, _P, _I, _I, _P, _P, _P, _I, _P, _P], _I),
     "minf_kv_append_paged_f16": ([_P, _P, _I64, _I, _P, _I, _I, _P, _P, _P, _I, _P, _P], _I),
@@ -322,7 +338,7 @@ def minf_layer_attn_step_batched_f16(xn, h, gain, eps, q, k, v, pos, k_arena, v_
 # k_pool/v_pool: [pool_rows, W] (float32, or float16 for the _f16 forms); block_table: int32
 # [n_seq, max_blocks] on the device; block_rows: rows per block.
 def _pool_dtype(name):
-    return _H if name.endswith("_f16") else torch.float32
+    return _H if name.endswith("_f16") else (torch.uint8 if name.endswith("_q8") else torch.float32)
 
 
 def _kv_append_paged(name, k_pool, v_pool, block_table, block_rows, k_rows, v_rows, pos, err, stream):
@@ -392,3 +408,94 @@ def minf_layer_attn_step_paged_f16(xn, h, gain, eps, q, k, v, pos, k_pool, v_poo
                                    n_kv_head, hd, hd_kv, theta, freq_scale, style, out, ws, err, stream=None):
     _step_paged("minf_layer_attn_step_paged_f16", xn, h, gain, eps, q, k, v, pos, k_pool, v_pool, block_table,
                 block_rows, n_head, n_kv_head, hd, hd_kv, theta, freq_scale, style, out, ws, err, stream)
+
+
+def minf_kv_append_paged_q8(k_pool, v_pool, block_table, block_rows, k_rows, v_rows, pos, err, stream=None):
+    """Pools [pool_rows, minf_q8_row_bytes(W)] uint8; W is taken from k_rows."""
+    n_seq, max_blocks = block_table.shape
+    _check(lib().minf_kv_append_paged_q8(
+        _dev(k_pool, torch.uint8, "k_pool"), _dev(v_pool, torch.uint8, "v_pool"), k_pool.shape[0], k_rows.shape[-1],
+        _dev(block_table, torch.int32, "block_table"), max_blocks, block_rows, _dev(k_rows, name="k_rows"),
+        _dev(v_rows, name="v_rows"), _dev(pos, torch.int32, "pos"), n_seq, _dev(err, torch.int32, "err"),
+        _stream(stream)), "minf_kv_append_paged_q8")
+
+
+def minf_gqa_attn_decode_paged_q8(out, q, k_pool, v_pool, block_table, block_rows, pos, n_head, n_kv_head, hd, hd_kv,
+                                  scale, ws, err, stream=None):
+    _decode_paged("minf_gqa_attn_decode_paged_q8", out, q, k_pool, v_pool, block_table, block_rows, pos, n_head,
+                  n_kv_head, hd, hd_kv, scale, ws, err, stream)
+
+
+def minf_layer_attn_step_paged_q8(xn, h, gain, eps, q, k, v, pos, k_pool, v_pool, block_table, block_rows, n_head,
+                                  n_kv_head, hd, hd_kv, theta, freq_scale, style, out, ws, err, stream=None):
+    _step_paged("minf_layer_attn_step_paged_q8", xn, h, gain, eps, q, k, v, pos, k_pool, v_pool, block_table,
+                block_rows, n_head, n_kv_head, hd, hd_kv, theta, freq_scale, style, out, ws, err, stream)
+
+
+# ----------------------------------------------------------------------------- Q8_0 regions
+# The regions (or arena) are torch.uint8 tensors [rows, minf_q8_row_bytes(W)]; the row width W
+# (values) comes from the fp32 rows or the head geometry.
+_U8 = torch.uint8
+
+
+def minf_q8_row_bytes(row_width: int) -> int:
+    return int(lib().minf_q8_row_bytes(row_width))
+
+
+def minf_kv_append_q8(k_reg, v_reg, k_rows, v_rows, pos, err, stream=None):
+    _check(lib().minf_kv_append_q8(_dev(k_reg, _U8, "k_reg"), _dev(v_reg, _U8, "v_reg"), k_reg.shape[0],
+                                   k_rows.shape[-1], _dev(k_rows, name="k_rows"), _dev(v_rows, name="v_rows"),
+                                   _dev(pos, torch.int32, "pos"), pos.numel(), _dev(err, torch.int32, "err"),
+                                   _stream(stream)), "minf_kv_append_q8")
+
+
+def minf_rope_kv_append_q8(q, k, v, pos, n_head, n_kv_head, hd, hd_kv, theta, freq_scale, style, k_reg, v_reg, err,
+                           stream=None):
+    _check(lib().minf_rope_kv_append_q8(_dev(q, name="q"), _dev(k, name="k"), _dev(v, name="v"),
+                                        _dev(pos, torch.int32, "pos"), pos.numel(), n_head, n_kv_head, hd, hd_kv,
+                                        theta, freq_scale, style, _dev(k_reg, _U8, "k_reg"), _dev(v_reg, _U8, "v_reg"),
+                                        k_reg.shape[0], _dev(err, torch.int32, "err"), _stream(stream)),
+           "minf_rope_kv_append_q8")
+
+
+def minf_gqa_attn_decode_q8(out, q, k_reg, v_reg, seq_row_off, seq_cap, max_cap, pos, n_head, n_kv_head, hd, hd_kv,
+                            scale, ws, err, stream=None):
+    _check(lib().minf_gqa_attn_decode_q8(
+        _dev(out, name="out"), _dev(q, name="q"), _dev(k_reg, _U8, "k_reg"), _dev(v_reg, _U8, "v_reg"),
+        _dev(seq_row_off, torch.int64, "seq_row_off"), _dev(seq_cap, torch.int32, "seq_cap"), max_cap,
+        k_reg.shape[0], _dev(pos, torch.int32, "pos"), pos.numel(), n_head, n_kv_head, hd, hd_kv, scale,
+        _dev(ws, torch.uint8, "ws"), ws.numel(), _dev(err, torch.int32, "err"), _stream(stream)),
+        "minf_gqa_attn_decode_q8")
+
+
+def minf_gqa_attn_prefill_q8(out, q, k_reg, v_reg, pos, n_head, n_kv_head, hd, hd_kv, scale, ws, err, stream=None):
+    _check(lib().minf_gqa_attn_prefill_q8(
+        _dev(out, name="out"), _dev(q, name="q"), _dev(k_reg, _U8, "k_reg"), _dev(v_reg, _U8, "v_reg"),
+        k_reg.shape[0], _dev(pos, torch.int32, "pos"), pos.numel(), n_head, n_kv_head, hd, hd_kv, scale,
+        _dev(ws, torch.uint8, "ws"), _nbytes(ws), _dev(err, torch.int32, "err"), _stream(stream)),
+        "minf_gqa_attn_prefill_q8")
+
+
+def minf_layer_attn_step_q8(xn, h, gain, eps, q, k, v, pos, k_reg, v_reg, n_head, n_kv_head, hd, hd_kv, theta,
+                            freq_scale, style, out, ws, err, stream=None):
+    nt, n_embd = h.shape
+    _check(lib().minf_layer_attn_step_q8(
+        _dev(xn, name="xn"), _dev(h, name="h"), _dev(gain, name="gain"), eps, n_embd,
+        _dev(q, name="q"), _dev(k, name="k"), _dev(v, name="v"), _dev(pos, torch.int32, "pos"), nt,
+        _dev(k_reg, _U8, "k_reg"), _dev(v_reg, _U8, "v_reg"), k_reg.shape[0], n_head, n_kv_head, hd, hd_kv,
+        theta, freq_scale, style, _dev(out, name="out"), _dev(ws, torch.uint8, "ws"), _nbytes(ws),
+        _dev(err, torch.int32, "err"), _stream(stream)), "minf_layer_attn_step_q8")
+
+
+def minf_layer_attn_step_batched_q8(xn, h, gain, eps, q, k, v, pos, k_arena, v_arena, seq_row_off, seq_cap, max_cap,
+                                    n_head, n_kv_head, hd, hd_kv, theta, freq_scale, style, out, ws, err,
+                                    stream=None):
+    n_seq, n_embd = h.shape
+    _check(lib().minf_layer_attn_step_batched_q8(
+        _dev(xn, name="xn"), _dev(h, name="h"), _dev(gain, name="gain"), eps, n_embd,
+        _dev(q, name="q"), _dev(k, name="k"), _dev(v, name="v"), _dev(pos, torch.int32, "pos"), n_seq,
+        _dev(k_arena, _U8, "k_arena"), _dev(v_arena, _U8, "v_arena"),
+        _dev(seq_row_off, torch.int64, "seq_row_off"), _dev(seq_cap, torch.int32, "seq_cap"), max_cap,
+        k_arena.shape[0], n_head, n_kv_head, hd, hd_kv, theta, freq_scale, style, _dev(out, name="out"),
+        _dev(ws, torch.uint8, "ws"), ws.numel(), _dev(err, torch.int32, "err"), _stream(stream)),
+        "minf_layer_attn_step_batched_q8")

@@ -67,12 +67,28 @@ int minf_rope(float *x, const int32_t *pos, int nt, int n_head, int hd, float th
     return launch_rope(x, pos, nt, n_head, hd, theta, freq_scale, style, err, cs(stream));
 }
 
+// Row widths each storage kind accepts: fp32 in float4s, binary16 in 16-byte pieces, Q8_0 in
+// whole 32-value blocks.
+static int row_multiple(int kv) { return kv == kKvQ8 ? 32 : (kv == kKvF16 ? 8 : 4); }
+
 static int kv_append(void *k_reg, void *v_reg, int kv, int cap, int row_width, const float *k_rows,
                      const float *v_rows, const int32_t *pos, int nt, int32_t *err, minf_stream_t stream) {
     if (!ok_f(k_reg) || !ok_f(v_reg) || !ok_f(k_rows) || !ok_f(v_rows) || !pos || !err)
         return MINF_ERR_ARG;
-    if (cap <= 0 || nt < 0 || row_width <= 0 || row_width % (kv == kKvF16 ? 8 : 4)) return MINF_ERR_ARG;
+    if (cap <= 0 || nt < 0 || row_width <= 0 || row_width % row_multiple(kv)) return MINF_ERR_ARG;
+    if (kv == kKvQ8)
+        return launch_kv_append_q8(k_reg, v_reg, cap, row_width, k_rows, v_rows, pos, nt, nullptr, nullptr, nullptr,
+                                   0, 0, 0, err, cs(stream));
     return launch_kv_append(k_reg, v_reg, kv, cap, row_width, k_rows, v_rows, pos, nt, err, cs(stream));
+}
+
+int minf_kv_append_q8(uint8_t *k_reg, uint8_t *v_reg, int cap, int row_width, const float *k_rows,
+                      const float *v_rows, const int32_t *pos, int nt, int32_t *err, minf_stream_t stream) {
+    return kv_append(k_reg, v_reg, kKvQ8, cap, row_width, k_rows, v_rows, pos, nt, err, stream);
+}
+
+size_t minf_q8_row_bytes(int row_width) {
+    return row_width > 0 && row_width % 32 == 0 ? static_cast<size_t>(q8_row_bytes(row_width)) : 0;
 }
 
 int minf_kv_append(float *k_reg, float *v_reg, int cap, int row_width, const float *k_rows,
@@ -108,6 +124,13 @@ static int rope_kv(float *q, float *k, const float *v, const int32_t *pos, int n
     a.hd_kv = hd_kv;
     a.style = style;
     a.err = err;
+    if (kv == kKvQ8) {  // rotate here, then quantize the rotated rows into the regions
+        a.k_reg = a.v_reg = nullptr;
+        const int st = launch_rope_kv_append(a, theta, freq_scale, s);
+        if (st != MINF_OK) return st;
+        return launch_kv_append_q8(k_reg, v_reg, cap, nk * hd_kv, k, v, pos, nt, row_off, caps, nullptr, 0, 0, 0, err,
+                                   s);
+    }
     return launch_rope_kv_append(a, theta, freq_scale, s);
 }
 
@@ -118,7 +141,7 @@ static int rope_kv_append(float *q, float *k, const float *v, const int32_t *pos
     if (st != MINF_OK) return st;
     if (!ok_f(q) || !ok_f(k) || !ok_f(v) || !ok_f(k_reg) || !ok_f(v_reg) || !pos || !err)
         return MINF_ERR_ARG;
-    if (nt < 0 || cap <= 0 || (style != 0 && style != 1) || (n_kv_head * hd_kv) % (kv == kKvF16 ? 8 : 4))
+    if (nt < 0 || cap <= 0 || (style != 0 && style != 1) || (n_kv_head * hd_kv) % row_multiple(kv))
         return MINF_ERR_ARG;
     return rope_kv(q, k, v, pos, nt, n_head, n_kv_head, hd, hd_kv, theta, freq_scale, style,
                    k_reg, v_reg, kv, nullptr, nullptr, cap, err, cs(stream));
@@ -159,6 +182,14 @@ static int layer_prologue(float *xn, const float *h, const float *gain, float ep
     a.style = style;
     a.err = err;
     NormArgs nrm = {xn, h, gain, nt, n_embd, eps};
+    if (kv == kKvQ8) {  // rotate in the prologue, then quantize the rotated rows into the regions
+        a.k_reg = a.v_reg = nullptr;
+        const int st = launch_layer_prologue(a, theta, freq_scale, nrm, s);
+        if (st != MINF_OK) return st;
+        return launch_kv_append_q8(k_reg, v_reg, cap, nk * hd_kv, k, v, pos, nt, row_off, caps,
+                                   pg ? pg->table : nullptr, pg ? pg->max_blocks : 0, pg ? pg->block_rows : 0,
+                                   pg ? pg->pool_blocks : 0, err, s);
+    }
     return launch_layer_prologue(a, theta, freq_scale, nrm, s);
 }
 
@@ -168,6 +199,13 @@ int minf_rope_kv_append(float *q, float *k, const float *v, const int32_t *pos, 
                         int32_t *err, minf_stream_t stream) {
     return rope_kv_append(q, k, v, pos, nt, n_head, n_kv_head, hd, hd_kv, theta, freq_scale, style, k_reg,
                           v_reg, kKvF32, cap, err, stream);
+}
+
+int minf_rope_kv_append_q8(float *q, float *k, const float *v, const int32_t *pos, int nt, int n_head, int n_kv_head,
+                           int hd, int hd_kv, float theta, float freq_scale, int style, uint8_t *k_reg, uint8_t *v_reg,
+                           int cap, int32_t *err, minf_stream_t stream) {
+    return rope_kv_append(q, k, v, pos, nt, n_head, n_kv_head, hd, hd_kv, theta, freq_scale, style, k_reg, v_reg,
+                          kKvQ8, cap, err, stream);
 }
 
 int minf_rope_kv_append_f16(float *q, float *k, const float *v, const int32_t *pos, int nt, int n_head,
@@ -269,6 +307,15 @@ int minf_gqa_attn_decode(float *out, const float *q, const float *k_reg, const f
                            n_head, n_kv_head, hd, hd_kv, scale, ws, ws_bytes, err, stream);
 }
 
+int minf_gqa_attn_decode_q8(float *out, const float *q, const uint8_t *k_reg, const uint8_t *v_reg,
+                            const int64_t *seq_row_off, const int32_t *seq_cap, int max_cap, int64_t arena_rows,
+                            const int32_t *pos, int n_seq, int n_head, int n_kv_head, int hd, int hd_kv, float scale,
+                            void *ws, size_t ws_bytes, int32_t *err, minf_stream_t stream) {
+    if ((n_kv_head * hd_kv) % 32) return MINF_ERR_ARG;
+    return gqa_attn_decode(out, q, k_reg, v_reg, kKvQ8, seq_row_off, seq_cap, max_cap, arena_rows, pos, n_seq, n_head,
+                           n_kv_head, hd, hd_kv, scale, ws, ws_bytes, err, stream);
+}
+
 int minf_gqa_attn_decode_f16(float *out, const float *q, const uint16_t *k_reg, const uint16_t *v_reg,
                              const int64_t *seq_row_off, const int32_t *seq_cap, int max_cap, int64_t arena_rows,
                              const int32_t *pos, int n_seq, int n_head, int n_kv_head, int hd, int hd_kv,
@@ -293,6 +340,14 @@ int minf_gqa_attn_prefill(float *out, const float *q, const float *k_reg, const 
                           int hd_kv, float scale, void *ws, size_t ws_bytes, int32_t *err,
                           minf_stream_t stream) {
     return gqa_attn_prefill(out, q, k_reg, v_reg, kKvF32, cap, pos, nt, n_head, n_kv_head, hd, hd_kv, scale, ws,
+                            ws_bytes, err, stream);
+}
+
+int minf_gqa_attn_prefill_q8(float *out, const float *q, const uint8_t *k_reg, const uint8_t *v_reg, int cap,
+                             const int32_t *pos, int nt, int n_head, int n_kv_head, int hd, int hd_kv, float scale,
+                             void *ws, size_t ws_bytes, int32_t *err, minf_stream_t stream) {
+    if ((n_kv_head * hd_kv) % 32) return MINF_ERR_ARG;
+    return gqa_attn_prefill(out, q, k_reg, v_reg, kKvQ8, cap, pos, nt, n_head, n_kv_head, hd, hd_kv, scale, ws,
                             ws_bytes, err, stream);
 }
 
@@ -349,6 +404,15 @@ int minf_layer_attn_step(float *xn, const float *h, const float *gain, float eps
                            n_kv_head, hd, hd_kv, theta, freq_scale, style, out, ws, ws_bytes, err, stream);
 }
 
+int minf_layer_attn_step_q8(float *xn, const float *h, const float *gain, float eps, int n_embd, float *q, float *k,
+                            const float *v, const int32_t *pos, int nt, uint8_t *k_reg, uint8_t *v_reg, int cap,
+                            int n_head, int n_kv_head, int hd, int hd_kv, float theta, float freq_scale, int style,
+                            float *out, void *ws, size_t ws_bytes, int32_t *err, minf_stream_t stream) {
+    if ((n_kv_head * hd_kv) % 32) return MINF_ERR_ARG;
+    return layer_attn_step(xn, h, gain, eps, n_embd, q, k, v, pos, nt, k_reg, v_reg, kKvQ8, cap, n_head, n_kv_head,
+                           hd, hd_kv, theta, freq_scale, style, out, ws, ws_bytes, err, stream);
+}
+
 int minf_layer_attn_step_f16(float *xn, const float *h, const float *gain, float eps, int n_embd, float *q,
                              float *k, const float *v, const int32_t *pos, int nt, uint16_t *k_reg,
                              uint16_t *v_reg, int cap, int n_head, int n_kv_head, int hd, int hd_kv, float theta,
@@ -398,6 +462,18 @@ int minf_layer_attn_step_batched(float *xn, const float *h, const float *gain, f
                                  float freq_scale, int style, float *out, void *ws, size_t ws_bytes, int32_t *err,
                                  minf_stream_t stream) {
     return layer_attn_step_batched(xn, h, gain, eps, n_embd, q, k, v, pos, n_seq, k_arena, v_arena, kKvF32,
+                                   seq_row_off, seq_cap, max_cap, arena_rows, n_head, n_kv_head, hd, hd_kv, theta,
+                                   freq_scale, style, out, ws, ws_bytes, err, stream);
+}
+
+int minf_layer_attn_step_batched_q8(float *xn, const float *h, const float *gain, float eps, int n_embd, float *q,
+                                    float *k, const float *v, const int32_t *pos, int n_seq, uint8_t *k_arena,
+                                    uint8_t *v_arena, const int64_t *seq_row_off, const int32_t *seq_cap, int max_cap,
+                                    int64_t arena_rows, int n_head, int n_kv_head, int hd, int hd_kv, float theta,
+                                    float freq_scale, int style, float *out, void *ws, size_t ws_bytes, int32_t *err,
+                                    minf_stream_t stream) {
+    if ((n_kv_head * hd_kv) % 32) return MINF_ERR_ARG;
+    return layer_attn_step_batched(xn, h, gain, eps, n_embd, q, k, v, pos, n_seq, k_arena, v_arena, kKvQ8,
                                    seq_row_off, seq_cap, max_cap, arena_rows, n_head, n_kv_head, hd, hd_kv, theta,
                                    freq_scale, style, out, ws, ws_bytes, err, stream);
 }
@@ -452,8 +528,11 @@ static int kv_append_paged(void *k_pool, void *v_pool, int kv, int64_t pool_rows
     int st = check_paged(k_pool, v_pool, kv, pool_rows, table, max_blocks, block_rows, &pg);
     if (st != MINF_OK) return st;
     if (!ok_f(k_rows) || !ok_f(v_rows) || !pos || !err || n_seq < 0 || row_width <= 0 ||
-        row_width % (kv == kKvF16 ? 8 : 4))
+        row_width % row_multiple(kv))
         return MINF_ERR_ARG;
+    if (kv == kKvQ8)
+        return launch_kv_append_q8(k_pool, v_pool, 0, row_width, k_rows, v_rows, pos, n_seq, nullptr, nullptr, table,
+                                   max_blocks, block_rows, pg.pool_blocks, err, cs(stream));
     return launch_kv_append_paged(k_pool, v_pool, kv, pg.pool_blocks, block_rows, row_width, table, max_blocks,
                                   k_rows, v_rows, pos, n_seq, err, cs(stream));
 }
@@ -462,6 +541,13 @@ int minf_kv_append_paged(float *k_pool, float *v_pool, int64_t pool_rows, int ro
                          int max_blocks, int block_rows, const float *k_rows, const float *v_rows, const int32_t *pos,
                          int n_seq, int32_t *err, minf_stream_t stream) {
     return kv_append_paged(k_pool, v_pool, kKvF32, pool_rows, row_width, block_table, max_blocks, block_rows, k_rows,
+                           v_rows, pos, n_seq, err, stream);
+}
+
+int minf_kv_append_paged_q8(uint8_t *k_pool, uint8_t *v_pool, int64_t pool_rows, int row_width,
+                            const int32_t *block_table, int max_blocks, int block_rows, const float *k_rows,
+                            const float *v_rows, const int32_t *pos, int n_seq, int32_t *err, minf_stream_t stream) {
+    return kv_append_paged(k_pool, v_pool, kKvQ8, pool_rows, row_width, block_table, max_blocks, block_rows, k_rows,
                            v_rows, pos, n_seq, err, stream);
 }
 
@@ -493,6 +579,15 @@ int minf_gqa_attn_decode_paged(float *out, const float *q, const float *k_pool, 
                                const int32_t *pos, int n_seq, int n_head, int n_kv_head, int hd, int hd_kv,
                                float scale, void *ws, size_t ws_bytes, int32_t *err, minf_stream_t stream) {
     return gqa_attn_decode_paged(out, q, k_pool, v_pool, kKvF32, pool_rows, block_table, max_blocks, block_rows, pos,
+                                 n_seq, n_head, n_kv_head, hd, hd_kv, scale, ws, ws_bytes, err, stream);
+}
+
+int minf_gqa_attn_decode_paged_q8(float *out, const float *q, const uint8_t *k_pool, const uint8_t *v_pool,
+                                  int64_t pool_rows, const int32_t *block_table, int max_blocks, int block_rows,
+                                  const int32_t *pos, int n_seq, int n_head, int n_kv_head, int hd, int hd_kv,
+                                  float scale, void *ws, size_t ws_bytes, int32_t *err, minf_stream_t stream) {
+    if ((n_kv_head * hd_kv) % 32) return MINF_ERR_ARG;
+    return gqa_attn_decode_paged(out, q, k_pool, v_pool, kKvQ8, pool_rows, block_table, max_blocks, block_rows, pos,
                                  n_seq, n_head, n_kv_head, hd, hd_kv, scale, ws, ws_bytes, err, stream);
 }
 
@@ -541,6 +636,18 @@ int minf_layer_attn_step_paged(float *xn, const float *h, const float *gain, flo
                                int n_head, int n_kv_head, int hd, int hd_kv, float theta, float freq_scale, int style,
                                float *out, void *ws, size_t ws_bytes, int32_t *err, minf_stream_t stream) {
     return layer_attn_step_paged(xn, h, gain, eps, n_embd, q, k, v, pos, n_seq, k_pool, v_pool, kKvF32, pool_rows,
+                                 block_table, max_blocks, block_rows, n_head, n_kv_head, hd, hd_kv, theta, freq_scale,
+                                 style, out, ws, ws_bytes, err, stream);
+}
+
+int minf_layer_attn_step_paged_q8(float *xn, const float *h, const float *gain, float eps, int n_embd, float *q,
+                                  float *k, const float *v, const int32_t *pos, int n_seq, uint8_t *k_pool,
+                                  uint8_t *v_pool, int64_t pool_rows, const int32_t *block_table, int max_blocks,
+                                  int block_rows, int n_head, int n_kv_head, int hd, int hd_kv, float theta,
+                                  float freq_scale, int style, float *out, void *ws, size_t ws_bytes, int32_t *err,
+                                  minf_stream_t stream) {
+    if ((n_kv_head * hd_kv) % 32) return MINF_ERR_ARG;
+    return layer_attn_step_paged(xn, h, gain, eps, n_embd, q, k, v, pos, n_seq, k_pool, v_pool, kKvQ8, pool_rows,
                                  block_table, max_blocks, block_rows, n_head, n_kv_head, hd, hd_kv, theta, freq_scale,
                                  style, out, ws, ws_bytes, err, stream);
 }

@@ -8,7 +8,12 @@ namespace {
 
 using namespace dec;
 
-inline int stage_rows(int hd_kv, int elem_bytes) { return kStageBytes / (2 * hd_kv * elem_bytes); }
+// Rows per pipeline stage for a region storage kind (as the kernel's Cfg has them).
+inline int stage_rows(int hd_kv, int kind) {
+    if (kind == kKvQ8) return hd_kv == 64 ? Cfg<64, Q8>::R : Cfg<128, Q8>::R;
+    const int eb = kind == kKvF16 ? 2 : 4;
+    return kStageBytes / (2 * hd_kv * eb);
+}
 
 struct WsLayout {
     size_t ml_off, acc_off, ticket_off, ctr_off, total;
@@ -39,8 +44,8 @@ int heads_per_cta(int g, int hd_kv) {
 // Splits per (sequence, kv group): fill the SMs once when the pairs alone cannot; otherwise
 // (a batch) cut only long windows, into units of at most kMaxRows, since the persistent CTAs
 // take units from a shared counter, longest first.
-int choose_splits(long long pairs, int hd_kv, int max_cap, int elem_bytes) {
-    const long long R = stage_rows(hd_kv, elem_bytes);
+int choose_splits(long long pairs, int hd_kv, int max_cap, int kind) {
+    const long long R = stage_rows(hd_kv, kind);
     long long s = pairs < kGridTarget ? kGridTarget / pairs
                                       : (static_cast<long long>(max_cap) + kMaxRows - 1) / kMaxRows;
     const long long s_rows = (static_cast<long long>(max_cap) + R - 1) / R;
@@ -55,20 +60,20 @@ struct Plan {
     WsLayout w;
 };
 
-// elem_bytes: 4 for fp32 regions, 2 for binary16 (whose stages hold twice the rows).  The
-// workspace is laid out for fp32's split count, which is never below binary16's, so one
-// workspace size serves both storage types.
-Plan plan_for(int n_seq, int nh, int nk, int hd_kv, int max_cap, int elem_bytes) {
+// kind: the region storage (binary16 and Q8_0 stages hold more rows than fp32 ones).  The
+// workspace is laid out for fp32's split count, which is never below the others', so one
+// workspace size serves every storage kind.
+Plan plan_for(int n_seq, int nh, int nk, int hd_kv, int max_cap, int kind) {
     Plan p;
     const int g = nh / nk;
     p.gh = heads_per_cta(g, hd_kv);
     p.groups = g / p.gh;
     const long long pairs = static_cast<long long>(n_seq) * nk * p.groups;
-    p.S = choose_splits(pairs, hd_kv, max_cap, elem_bytes);
+    p.S = choose_splits(pairs, hd_kv, max_cap, kind);
     const bool batch = pairs >= kGridTarget;
-    p.min_rows = batch ? kBatchMinRows : stage_rows(hd_kv, elem_bytes);
+    p.min_rows = batch ? kBatchMinRows : stage_rows(hd_kv, kind);
     p.sorted = batch && n_seq > 1 && n_seq <= kMaxSort;
-    p.w = ws_layout(n_seq, nh, nk * p.groups, hd_kv, choose_splits(pairs, hd_kv, max_cap, 4));
+    p.w = ws_layout(n_seq, nh, nk * p.groups, hd_kv, choose_splits(pairs, hd_kv, max_cap, kKvF32));
     return p;
 }
 
@@ -87,23 +92,31 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 
 int launch_impl(const DecodeArgs &d, const DecodeStepExtra *x, cudaStream_t s) {
     if (d.n_seq == 0) return MINF_OK;
-    const bool f16 = d.kv == kKvF16;
-    const int eb = f16 ? 2 : 4;
-    const Plan pl = plan_for(d.n_seq, d.nh, d.nk, d.hd_kv, d.cap, eb);
+    const bool f16 = d.kv == kKvF16, q8 = d.kv == kKvQ8;
+    const int eb = f16 ? 2 : (q8 ? 1 : 4);
+    const Plan pl = plan_for(d.n_seq, d.nh, d.nk, d.hd_kv, d.cap, d.kv);
     if (!d.ws || d.ws_bytes < pl.w.total || !aligned16(d.ws)) return MINF_ERR_WORKSPACE;
     const long long units = static_cast<long long>(d.n_seq) * d.nk * pl.groups * pl.S;
     if (units > 0x7fffffffLL) return MINF_ERR_UNSUPPORTED;
     const long long rows = (d.row_off || d.table) ? d.arena_rows : d.cap;
     if (rows <= 0) return MINF_ERR_ARG;
     if (rows > 0x7fffffffLL - 4096) return MINF_ERR_UNSUPPORTED;
-    const int R = stage_rows(d.hd_kv, eb);
+    const int R = stage_rows(d.hd_kv, d.kv);
     // paged: a stage is copied in pieces of one block (or one stage when blocks are larger)
     const int box = d.table ? (d.block_rows < R ? d.block_rows : R) : R;
-    CUtensorMap tk, tv;
+    CUtensorMap tk, tv, tks, tvs;
     const uint64_t W = static_cast<uint64_t>(d.nk) * d.hd_kv;
-    const CUtensorMapDataType dt = f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
-    if (!make_tensor_map_2d(&tk, d.k_reg, dt, eb, W, static_cast<uint64_t>(rows), d.hd_kv, box, false) ||
-        !make_tensor_map_2d(&tv, d.v_reg, dt, eb, W, static_cast<uint64_t>(rows), d.hd_kv, box, false))
+    // Q8_0 rows are bytes: the quants of this kv head, and a 16-byte slice of the scales
+    const uint64_t cols = q8 ? static_cast<uint64_t>(q8_row_bytes(static_cast<int>(W))) : W;
+    const CUtensorMapDataType dt = f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                       : (q8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32);
+    if (!make_tensor_map_2d(&tk, d.k_reg, dt, eb, cols, static_cast<uint64_t>(rows), d.hd_kv, box, false) ||
+        !make_tensor_map_2d(&tv, d.v_reg, dt, eb, cols, static_cast<uint64_t>(rows), d.hd_kv, box, false))
+        return MINF_ERR_CUDA;
+    tks = tk;
+    tvs = tv;
+    if (q8 && (!make_tensor_map_2d(&tks, d.k_reg, dt, 1, cols, static_cast<uint64_t>(rows), 16, box, false) ||
+               !make_tensor_map_2d(&tvs, d.v_reg, dt, 1, cols, static_cast<uint64_t>(rows), 16, box, false)))
         return MINF_ERR_CUDA;
     char *ws = static_cast<char *>(d.ws);
     KParams k = {};
@@ -133,6 +146,7 @@ int launch_impl(const DecodeArgs &d, const DecodeStepExtra *x, cudaStream_t s) {
     k.block_rows = d.block_rows;
     k.box_rows = box;
     k.pool_rows = rows;
+    k.row_bytes = q8 ? static_cast<long long>(cols) : 0;
     k.k_reg = const_cast<void *>(d.k_reg);
     k.v_reg = const_cast<void *>(d.v_reg);
     bool pdl = false;
@@ -151,8 +165,9 @@ int launch_impl(const DecodeArgs &d, const DecodeStepExtra *x, cudaStream_t s) {
     }
     const int sms = sm_count();
     const int grid = static_cast<int>(units < sms ? units : sms);
-    const cudaError_t e = f16 ? dispatch_decode_f16(d.hd_kv, x != nullptr, pl.gh, tk, tv, k, grid, s, pdl)
-                              : dispatch<float>(d.hd_kv, x != nullptr, pl.gh, tk, tv, k, grid, s, pdl);
+    const cudaError_t e = f16  ? dispatch_decode_f16(d.hd_kv, x != nullptr, pl.gh, tk, tv, tks, tvs, k, grid, s, pdl)
+                          : q8 ? dispatch_decode_q8(d.hd_kv, x != nullptr, pl.gh, tk, tv, tks, tvs, k, grid, s, pdl)
+                               : dispatch<float>(d.hd_kv, x != nullptr, pl.gh, tk, tv, tks, tvs, k, grid, s, pdl);
     if (e == cudaErrorInvalidValue) return MINF_ERR_UNSUPPORTED;
     return e == cudaSuccess ? MINF_OK : MINF_ERR_CUDA;
 }
@@ -187,7 +202,7 @@ bool fused_step_supported(int nh, int nk, int hd, int hd_kv, int n_embd) {
 
 size_t decode_workspace_bytes(int n_seq, int nh, int nk, int hd_kv, int max_cap) {
     if (n_seq <= 0 || nh <= 0 || nk <= 0 || hd_kv <= 0 || max_cap <= 0 || nh % nk) return 0;
-    return plan_for(n_seq, nh, nk, hd_kv, max_cap, 4).w.total;  // the layout serves both storage types
+    return plan_for(n_seq, nh, nk, hd_kv, max_cap, kKvF32).w.total;  // the layout serves every storage kind
 }
 
 int launch_decode(const DecodeArgs &d, cudaStream_t s) { return launch_impl(d, nullptr, s); }

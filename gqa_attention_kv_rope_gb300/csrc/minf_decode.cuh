@@ -50,6 +50,7 @@
 
 #include "minf_common.cuh"
 #include "minf_kernels.h"
+#include "minf_q8.cuh"
 #include "minf_sm103.cuh"
 
 namespace minf {
@@ -88,11 +89,46 @@ __device__ __forceinline__ void st4(__half *p, int i4, float4 v) {
     reinterpret_cast<uint2 *>(p)[i4] = u;
 }
 
+// Q8 (minf_q8.cuh) tags Q8_0 rows: the row's int8 quants, then one binary16 scale per 32
+// values, padded to 16 bytes; a value reads back as scale * quant.
+
+template <typename T>
+struct Elem {
+    static constexpr int bytes = sizeof(T);
+    static constexpr bool q8 = false;
+};
+template <>
+struct Elem<Q8> {
+    static constexpr int bytes = 1;
+    static constexpr bool q8 = true;
+};
+
+// A stage holds R rows of K and of V.  For Q8_0 each row also brings a 16-byte slice of its
+// scales (those of the 256/HDKV kv heads sharing that slice), and stages are smaller.
 template <int HDKV, typename T>
 struct Cfg {
-    static constexpr int R = kStageBytes / (2 * HDKV * static_cast<int>(sizeof(T)));  // rows per stage
-    static constexpr int SPW = R / (kSub * kNW);  // sub-tiles per warp per stage
+    static constexpr bool Q = Elem<T>::q8;
+    static constexpr int R = Q ? (HDKV == 64 ? 256 : 128) : kStageBytes / (2 * HDKV * Elem<T>::bytes);
+    static constexpr int SPW = R / (kSub * kNW);                  // sub-tiles per warp per stage
+    static constexpr int kQBytes = R * HDKV * Elem<T>::bytes;     // values (or quants) of one tensor
+    static constexpr int kSBytes = Q ? R * 16 : 0;                // scale slices of one tensor
+    static constexpr int kTensorBytes = kQBytes + kSBytes;
+    static constexpr int kSlotBytes = 2 * kTensorBytes;          // one ring slot: K then V
 };
+
+// Elements 4*i4 .. 4*i4+3 of a tile row: qrow is the row's values (or quants), srow its scale
+// slice, sc the index of this kv head's first scale in the slice.
+template <int HDKV, typename T>
+__device__ __forceinline__ float4 ld_row4(const unsigned char *qrow, const unsigned char *srow, int sc, int i4) {
+    if constexpr (Elem<T>::q8) {
+        const uint32_t q = reinterpret_cast<const uint32_t *>(qrow)[i4];
+        const float scale = __half2float(reinterpret_cast<const __half *>(srow)[sc + (i4 >> 3)]);
+        return deq4(q, scale);
+    } else {
+        return ld4(reinterpret_cast<const T *>(qrow), i4);
+    }
+}
+
 
 struct KParams {
     float *out;
@@ -108,6 +144,7 @@ struct KParams {
     const int32_t *table;
     int max_blocks, block_rows, box_rows;
     long long pool_rows;
+    long long row_bytes;   // Q8_0: bytes of a region row (quants, scales, padding)
     int sorted;            // visit sequences longest first
     float scale_log2;
     int32_t *err;
@@ -241,16 +278,21 @@ __device__ __forceinline__ void cons_sync(unsigned long long *bar, uint32_t &pha
 template <int HDKV, int GH, bool kFused, typename T>
 __global__ void __launch_bounds__(kThreads, 1)
     decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                  const __grid_constant__ CUtensorMap tmKs, const __grid_constant__ CUtensorMap tmVs,
                   const KParams a) {
-    constexpr int R = Cfg<HDKV, T>::R, SPW = Cfg<HDKV, T>::SPW;
+    using C = Cfg<HDKV, T>;
+    constexpr bool Q = C::Q;
+    constexpr int R = C::R, SPW = C::SPW;
+    constexpr int EB = Elem<T>::bytes;
+    constexpr int kScaleHeads = 256 / HDKV;  // Q8_0: kv heads whose scales share a 16-byte slice
     constexpr int KF4 = HDKV / 32;  // float4 per lane per K row (8 lanes share a row)
     constexpr int VL = HDKV / 4;    // lanes per V row (a float4 each)
     constexpr int VRP = 32 / VL;    // V rows a warp covers per pass
     constexpr int VJ = kSub / VRP;  // passes per sub-tile
-    constexpr uint32_t kTileBytes = R * HDKV * sizeof(T);
+
     extern __shared__ unsigned char smem_raw[];
     // 1024-aligned ring, derived from the shared array itself so loads stay in the shared space
-    T *ring = reinterpret_cast<T *>(smem_raw + ((1024u - (su32(smem_raw) & 1023u)) & 1023u));
+    unsigned char *ring = smem_raw + ((1024u - (su32(smem_raw) & 1023u)) & 1023u);
     __shared__ unsigned long long full[kNST], empty[kNST], meta_full[kNST], cons_bar;
     __shared__ int2 sm_meta[kNST];  // (unit, stage) of each ring slot; unit < 0 ends the stream
     __shared__ int sm_order[kMaxSort];
@@ -359,12 +401,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                         sm_meta[slot] = make_int2(u, st);
                         mbar_arrive(&meta_full[slot]);  // publishes the slot's unit to the consumers
-                        T *kt = ring + static_cast<size_t>(slot) * (2 * R * HDKV);
-                        mbar_expect_tx(&full[slot], 2 * kTileBytes);
+                        unsigned char *sb = ring + static_cast<size_t>(slot) * C::kSlotBytes;
+                        mbar_expect_tx(&full[slot], C::kSlotBytes);
+                        // x of the tile copies: in elements of the map (bytes for Q8_0, whose
+                        // scale slice of this kv head starts xs bytes into the row)
+                        const int xs = a.row_bytes ? static_cast<int>(W + (hk / kScaleHeads) * 16) : 0;
                         if (!a.table) {
                             const int row = static_cast<int>(t.base) + t.r_begin + st * R;
-                            tma_load_2d(kt, &tmK, hk * HDKV, row, &full[slot]);
-                            tma_load_2d(kt + R * HDKV, &tmV, hk * HDKV, row, &full[slot]);
+                            tma_load_2d(sb, &tmK, hk * HDKV, row, &full[slot]);
+                            tma_load_2d(sb + C::kTensorBytes, &tmV, hk * HDKV, row, &full[slot]);
+                            if (Q) {
+                                tma_load_2d(sb + C::kQBytes, &tmKs, xs, row, &full[slot]);
+                                tma_load_2d(sb + C::kTensorBytes + C::kQBytes, &tmVs, xs, row, &full[slot]);
+                            }
                         } else {
                             // one copy per block piece; a block the table does not hold reads
                             // as zeros (its rows start past the pool) and is reported
@@ -377,8 +426,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 const bool ok = b >= 0 && prow < a.pool_rows;
                                 if (!ok && lrow < t.L) flag_error(a.err, MINF_ERRBIT_BLOCK);
                                 const int row = ok ? static_cast<int>(prow) : static_cast<int>(a.pool_rows);
-                                tma_load_2d(kt + c * a.box_rows * HDKV, &tmK, hk * HDKV, row, &full[slot]);
-                                tma_load_2d(kt + R * HDKV + c * a.box_rows * HDKV, &tmV, hk * HDKV, row, &full[slot]);
+                                const int qo = c * a.box_rows * HDKV * EB;
+                                tma_load_2d(sb + qo, &tmK, hk * HDKV, row, &full[slot]);
+                                tma_load_2d(sb + C::kTensorBytes + qo, &tmV, hk * HDKV, row, &full[slot]);
+                                if (Q) {
+                                    const int so = C::kQBytes + c * a.box_rows * 16;
+                                    tma_load_2d(sb + so, &tmKs, xs, row, &full[slot]);
+                                    tma_load_2d(sb + C::kTensorBytes + so, &tmVs, xs, row, &full[slot]);
+                                }
                             }
                         }
                     }
@@ -492,19 +547,51 @@ __global__ void __launch_bounds__(kThreads, 1)
                             if (sub == 0) flag_error(a.err, MINF_ERRBIT_BLOCK);
                         }
                     }
-#pragma unroll
-                    for (int i = 0; i < KF4; ++i) {
-                        // staged for the same lanes, which patch the row's stage when it arrives
-                        reinterpret_cast<float4 *>(sm_knew)[sub + 8 * i] = kx[i];
-                        reinterpret_cast<float4 *>(sm_vnew)[sub + 8 * i] = vx[i];
-                    }
-                    if (prow >= 0) {
-                        T *Kg = static_cast<T *>(a.k_reg) + prow * W + hk * HDKV;
-                        T *Vg = static_cast<T *>(a.v_reg) + prow * W + hk * HDKV;
+                    if constexpr (Q) {
+                        // quantize the row's blocks (block i is element group i of lanes 0-7);
+                        // staged as bytes (quants, then scales) for the same lanes' patch
+                        unsigned char *Kg = static_cast<unsigned char *>(a.k_reg) + prow * a.row_bytes;
+                        unsigned char *Vg = static_cast<unsigned char *>(a.v_reg) + prow * a.row_bytes;
 #pragma unroll
                         for (int i = 0; i < KF4; ++i) {
-                            st4(Kg, sub + 8 * i, kx[i]);
-                            st4(Vg, sub + 8 * i, vx[i]);
+                            float dk, dv;
+                            const uint32_t qk = quant4(kx[i], 0xffu, dk), qv = quant4(vx[i], 0xffu, dv);
+                            reinterpret_cast<uint32_t *>(sm_knew)[sub + 8 * i] = qk;
+                            reinterpret_cast<uint32_t *>(sm_vnew)[sub + 8 * i] = qv;
+                            const __half hk16 = __float2half_rn(dk), hv16 = __float2half_rn(dv);
+                            if (sub == 0) {
+                                reinterpret_cast<__half *>(reinterpret_cast<unsigned char *>(sm_knew) + HDKV)[i] = hk16;
+                                reinterpret_cast<__half *>(reinterpret_cast<unsigned char *>(sm_vnew) + HDKV)[i] = hv16;
+                            }
+                            if (prow >= 0) {
+                                reinterpret_cast<uint32_t *>(Kg + hk * HDKV)[sub + 8 * i] = qk;
+                                reinterpret_cast<uint32_t *>(Vg + hk * HDKV)[sub + 8 * i] = qv;
+                                if (sub == 0) {
+                                    reinterpret_cast<__half *>(Kg + W)[hk * (HDKV / 32) + i] = hk16;
+                                    reinterpret_cast<__half *>(Vg + W)[hk * (HDKV / 32) + i] = hv16;
+                                }
+                            }
+                        }
+                        if (prow >= 0 && hk == 0 && sub == 0)  // the row's zero padding after its scales
+                            for (long long b = W + W / 16; b < a.row_bytes; b += 2) {
+                                *reinterpret_cast<uint16_t *>(Kg + b) = 0;
+                                *reinterpret_cast<uint16_t *>(Vg + b) = 0;
+                            }
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < KF4; ++i) {
+                            // staged for the same lanes, which patch the row's stage when it arrives
+                            reinterpret_cast<float4 *>(sm_knew)[sub + 8 * i] = kx[i];
+                            reinterpret_cast<float4 *>(sm_vnew)[sub + 8 * i] = vx[i];
+                        }
+                        if (prow >= 0) {
+                            T *Kg = static_cast<T *>(a.k_reg) + prow * W + hk * HDKV;
+                            T *Vg = static_cast<T *>(a.v_reg) + prow * W + hk * HDKV;
+#pragma unroll
+                            for (int i = 0; i < KF4; ++i) {
+                                st4(Kg, sub + 8 * i, kx[i]);
+                                st4(Vg, sub + 8 * i, vx[i]);
+                            }
                         }
                     }
                 }
@@ -533,8 +620,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int st = 0; st < n_st; ++st, ++it) {
             const int slot = it % kNST;
             mbar_wait(&full[slot], (it / kNST) & 1, abort_flag, a.err);
-            T *Ks = ring + static_cast<size_t>(slot) * (2 * R * HDKV);
-            T *Vs = Ks + R * HDKV;
+            unsigned char *Kq = ring + static_cast<size_t>(slot) * C::kSlotBytes;  // K values / quants
+            unsigned char *Ksc = Kq + C::kQBytes;                                 // K scale slices
+            unsigned char *Vq = Kq + C::kTensorBytes;
+            unsigned char *Vsc = Vq + C::kQBytes;
+            const int sc = (hk % kScaleHeads) * (HDKV / 32);  // this head's first scale in a slice
             const int row0 = t.r_begin + st * R;
             if (kFused && pnew >= row0 && pnew < row0 + R) {
                 // the tile may hold the row as it was before this launch appended it: the lanes
@@ -542,10 +632,28 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // async proxy in order)
                 if (warp == 0 && r4 == 0) {
                     const int rn = pnew - row0;
+                    if constexpr (Q) {
 #pragma unroll
-                    for (int i = 0; i < KF4; ++i) {
-                        st4(Ks + rn * HDKV, sub + 8 * i, reinterpret_cast<const float4 *>(sm_knew)[sub + 8 * i]);
-                        st4(Vs + rn * HDKV, sub + 8 * i, reinterpret_cast<const float4 *>(sm_vnew)[sub + 8 * i]);
+                        for (int i = 0; i < KF4; ++i) {
+                            reinterpret_cast<uint32_t *>(Kq + rn * HDKV)[sub + 8 * i] =
+                                reinterpret_cast<const uint32_t *>(sm_knew)[sub + 8 * i];
+                            reinterpret_cast<uint32_t *>(Vq + rn * HDKV)[sub + 8 * i] =
+                                reinterpret_cast<const uint32_t *>(sm_vnew)[sub + 8 * i];
+                            if (sub == 0) {
+                                reinterpret_cast<__half *>(Ksc + rn * 16)[sc + i] =
+                                    reinterpret_cast<const __half *>(reinterpret_cast<const unsigned char *>(sm_knew) + HDKV)[i];
+                                reinterpret_cast<__half *>(Vsc + rn * 16)[sc + i] =
+                                    reinterpret_cast<const __half *>(reinterpret_cast<const unsigned char *>(sm_vnew) + HDKV)[i];
+                            }
+                        }
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < KF4; ++i) {
+                            st4(reinterpret_cast<T *>(Kq) + rn * HDKV, sub + 8 * i,
+                                reinterpret_cast<const float4 *>(sm_knew)[sub + 8 * i]);
+                            st4(reinterpret_cast<T *>(Vq) + rn * HDKV, sub + 8 * i,
+                                reinterpret_cast<const float4 *>(sm_vnew)[sub + 8 * i]);
+                        }
                     }
                     fence_async_smem();
                 }
@@ -560,13 +668,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int it2 = 0; it2 < 2; ++it2) {
                     const int rr = rr0 + 4 * it2 + r4;
 #pragma unroll
-                    for (int i = 0; i < KF4; ++i) kv[it2][i] = ld4(Ks + rr * HDKV, sub + 8 * i);
+                    for (int i = 0; i < KF4; ++i)
+                        kv[it2][i] = ld_row4<HDKV, T>(Kq + rr * HDKV * EB, Ksc + rr * 16, sc, sub + 8 * i);
                 }
 #pragma unroll
                 for (int jv = 0; jv < VJ; ++jv) {
                     const int rr = rr0 + vrow + VRP * jv;
                     const int row = row0 + rr;
-                    vv[jv] = row < t.r_end ? ld4(Vs + rr * HDKV, vcol)
+                    vv[jv] = row < t.r_end ? ld_row4<HDKV, T>(Vq + rr * HDKV * EB, Vsc + rr * 16, sc, vcol)
                                            : make_float4(0.f, 0.f, 0.f, 0.f);  // past the run: anything
                 }
                 float pr[2][GH];
@@ -748,9 +857,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 template <int HDKV, int GH, bool kFused, typename T>
-cudaError_t launch_t(const CUtensorMap &tk, const CUtensorMap &tv, const KParams &k, int grid, cudaStream_t s,
+cudaError_t launch_t(const CUtensorMap &tk, const CUtensorMap &tv, const CUtensorMap &tks,
+                     const CUtensorMap &tvs, const KParams &k, int grid, cudaStream_t s,
                      bool pdl) {
-    const size_t smem = static_cast<size_t>(kNST) * kStageBytes + 1024;
+    const size_t smem = static_cast<size_t>(kNST) * Cfg<HDKV, T>::kSlotBytes + 1024;
     static bool attr_set = false;
     if (!attr_set) {
         cudaError_t e = cudaFuncSetAttribute(decode_kernel<HDKV, GH, kFused, T>,
@@ -768,21 +878,22 @@ cudaError_t launch_t(const CUtensorMap &tk, const CUtensorMap &tv, const KParams
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, decode_kernel<HDKV, GH, kFused, T>, tk, tv, k);
+    return cudaLaunchKernelEx(&cfg, decode_kernel<HDKV, GH, kFused, T>, tk, tv, tks, tvs, k);
 }
 
 template <int HDKV, bool kFused, typename T>
-cudaError_t dispatch_gh(int gh, const CUtensorMap &tk, const CUtensorMap &tv, const KParams &k, int grid,
+cudaError_t dispatch_gh(int gh, const CUtensorMap &tk, const CUtensorMap &tv, const CUtensorMap &tks,
+                     const CUtensorMap &tvs, const KParams &k, int grid,
                         cudaStream_t s, bool pdl) {
     switch (gh) {
-        case 1: return launch_t<HDKV, 1, kFused, T>(tk, tv, k, grid, s, pdl);
-        case 2: return launch_t<HDKV, 2, kFused, T>(tk, tv, k, grid, s, pdl);
-        case 3: return launch_t<HDKV, 3, kFused, T>(tk, tv, k, grid, s, pdl);
-        case 4: return launch_t<HDKV, 4, kFused, T>(tk, tv, k, grid, s, pdl);
-        case 5: return launch_t<HDKV, 5, kFused, T>(tk, tv, k, grid, s, pdl);
-        case 6: return launch_t<HDKV, 6, kFused, T>(tk, tv, k, grid, s, pdl);
-        case 7: return launch_t<HDKV, 7, kFused, T>(tk, tv, k, grid, s, pdl);
-        case 8: return launch_t<HDKV, 8, kFused, T>(tk, tv, k, grid, s, pdl);
+        case 1: return launch_t<HDKV, 1, kFused, T>(tk, tv, tks, tvs, k, grid, s, pdl);
+        case 2: return launch_t<HDKV, 2, kFused, T>(tk, tv, tks, tvs, k, grid, s, pdl);
+        case 3: return launch_t<HDKV, 3, kFused, T>(tk, tv, tks, tvs, k, grid, s, pdl);
+        case 4: return launch_t<HDKV, 4, kFused, T>(tk, tv, tks, tvs, k, grid, s, pdl);
+        case 5: return launch_t<HDKV, 5, kFused, T>(tk, tv, tks, tvs, k, grid, s, pdl);
+        case 6: return launch_t<HDKV, 6, kFused, T>(tk, tv, tks, tvs, k, grid, s, pdl);
+        case 7: return launch_t<HDKV, 7, kFused, T>(tk, tv, tks, tvs, k, grid, s, pdl);
+        case 8: return launch_t<HDKV, 8, kFused, T>(tk, tv, tks, tvs, k, grid, s, pdl);
         default: return cudaErrorInvalidValue;
     }
 }
@@ -790,19 +901,25 @@ cudaError_t dispatch_gh(int gh, const CUtensorMap &tk, const CUtensorMap &tv, co
 
 // Launch for a storage type: the geometry's head dimension, fused or not, heads per unit.
 template <typename T>
-cudaError_t dispatch(int hd_kv, bool fused, int gh, const CUtensorMap &tk, const CUtensorMap &tv, const KParams &k,
+cudaError_t dispatch(int hd_kv, bool fused, int gh, const CUtensorMap &tk, const CUtensorMap &tv, const CUtensorMap &tks,
+                     const CUtensorMap &tvs, const KParams &k,
                      int grid, cudaStream_t s, bool pdl) {
     if (fused)
-        return hd_kv == 64 ? dispatch_gh<64, true, T>(gh, tk, tv, k, grid, s, pdl)
-                           : dispatch_gh<128, true, T>(gh, tk, tv, k, grid, s, pdl);
-    return hd_kv == 64 ? dispatch_gh<64, false, T>(gh, tk, tv, k, grid, s, pdl)
-                       : dispatch_gh<128, false, T>(gh, tk, tv, k, grid, s, pdl);
+        return hd_kv == 64 ? dispatch_gh<64, true, T>(gh, tk, tv, tks, tvs, k, grid, s, pdl)
+                           : dispatch_gh<128, true, T>(gh, tk, tv, tks, tvs, k, grid, s, pdl);
+    return hd_kv == 64 ? dispatch_gh<64, false, T>(gh, tk, tv, tks, tvs, k, grid, s, pdl)
+                       : dispatch_gh<128, false, T>(gh, tk, tv, tks, tvs, k, grid, s, pdl);
 }
 
 }  // namespace dec
 
-// The binary16 instantiation lives in its own translation unit (minf_decode_f16.cu).
+// The binary16 and Q8_0 instantiations live in their own translation units
+// (minf_decode_f16.cu, minf_decode_q8.cu).
 cudaError_t dispatch_decode_f16(int hd_kv, bool fused, int gh, const CUtensorMap &tk, const CUtensorMap &tv,
-                                const dec::KParams &k, int grid, cudaStream_t s, bool pdl);
+                                const CUtensorMap &tks, const CUtensorMap &tvs, const dec::KParams &k, int grid,
+                                cudaStream_t s, bool pdl);
+cudaError_t dispatch_decode_q8(int hd_kv, bool fused, int gh, const CUtensorMap &tk, const CUtensorMap &tv,
+                               const CUtensorMap &tks, const CUtensorMap &tvs, const dec::KParams &k, int grid,
+                               cudaStream_t s, bool pdl);
 
 }  // namespace minf

@@ -9,6 +9,7 @@
 
 #include "minf_common.cuh"
 #include "minf_kernels.h"
+#include "minf_q8.cuh"
 
 namespace minf {
 
@@ -212,6 +213,65 @@ int launch_kv_append(void *k_reg, void *v_reg, int kv, int cap, int W, const flo
     return cudaPeekAtLastError() == cudaSuccess ? MINF_OK : MINF_ERR_CUDA;
 }
 
+// Q8_0 store: eight consecutive threads quantize one 32-value block (four values each) and
+// write its quants and scale.  Token t's row goes to row `row_of(t)` of the region (rb bytes a
+// row), or nowhere when that is negative (the error bit was set there).
+__device__ __forceinline__ void q8_store4(unsigned char *dst_row, int W, long long rb, int c, float4 x) {
+    const unsigned mask = 0xffu << (threadIdx.x & 24u);  // this 8-thread group of the warp
+    float d;
+    const uint32_t q = quant4(x, mask, d);
+    reinterpret_cast<uint32_t *>(dst_row)[c] = q;
+    if ((c & 7) == 0) reinterpret_cast<__half *>(dst_row + W)[c >> 3] = __float2half_rn(d);
+    if (c == 0)  // the row's zero padding after its scales
+        for (long long b = W + W / 16; b < rb; b += 2) *reinterpret_cast<uint16_t *>(dst_row + b) = 0;
+}
+
+__global__ void __launch_bounds__(256) kv_append_q8_kernel(unsigned char *k_reg, unsigned char *v_reg, int cap, int W,
+                                                           long long rb, const float *k_rows, const float *v_rows,
+                                                           const int32_t *pos, int nt, const int64_t *row_off,
+                                                           const int32_t *caps, const int32_t *table,
+                                                           int max_blocks, int block_rows, int pool_blocks,
+                                                           int32_t *err) {
+    const int w4 = W >> 2;  // a multiple of 8: blocks never straddle thread groups
+    const long long total = static_cast<long long>(nt) * w4;
+    for (long long idx = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; idx < total;
+         idx += static_cast<long long>(gridDim.x) * blockDim.x) {
+        const int t = static_cast<int>(idx / w4);
+        const int c = static_cast<int>(idx % w4);
+        const int p = __ldg(pos + t);
+        const int cap_t = table ? max_blocks * block_rows : (caps ? __ldg(caps + t) : cap);
+        if (p < 0 || p >= cap_t) {
+            if (c == 0) flag_error(err, MINF_ERRBIT_STORE_POS);
+            continue;
+        }
+        long long row = (row_off ? __ldg(row_off + t) : 0) + p;
+        if (table) {
+            const int b = __ldg(table + static_cast<size_t>(t) * max_blocks + p / block_rows);
+            if (b < 0 || b >= pool_blocks) {
+                if (c == 0) flag_error(err, MINF_ERRBIT_BLOCK);
+                continue;
+            }
+            row = static_cast<long long>(b) * block_rows + p % block_rows;
+        }
+        const size_t src = static_cast<size_t>(t) * w4 + c;
+        q8_store4(k_reg + row * rb, W, rb, c, reinterpret_cast<const float4 *>(k_rows)[src]);
+        q8_store4(v_reg + row * rb, W, rb, c, reinterpret_cast<const float4 *>(v_rows)[src]);
+    }
+}
+
+int launch_kv_append_q8(void *k_reg, void *v_reg, int cap, int W, const float *k_rows, const float *v_rows,
+                        const int32_t *pos, int nt, const int64_t *row_off, const int32_t *caps,
+                        const int32_t *table, int max_blocks, int block_rows, int pool_blocks, int32_t *err,
+                        cudaStream_t s) {
+    if (nt == 0) return MINF_OK;
+    const long long work = static_cast<long long>(nt) * (W / 4);
+    kv_append_q8_kernel<<<grid_for(work, 256), 256, 0, s>>>(static_cast<unsigned char *>(k_reg),
+                                                             static_cast<unsigned char *>(v_reg), cap, W, q8_row_bytes(W),
+                                                             k_rows, v_rows, pos, nt, row_off, caps, table, max_blocks,
+                                                             block_rows, pool_blocks, err);
+    return cudaPeekAtLastError() == cudaSuccess ? MINF_OK : MINF_ERR_CUDA;
+}
+
 // One row per sequence through a block table ("IV.2: Zero-copy KV cache": the paged cache
 // keeps a sequence as scattered fixed-size blocks).
 template <typename T>
@@ -277,7 +337,8 @@ __device__ __forceinline__ void rope_kv_append_items(const RopeKvArgs &a, const 
         const int cap_t = a.caps ? __ldg(a.caps + t) : a.cap;
         long long srow = (a.row_off ? __ldg(a.row_off + t) : 0) + p;  // the stored row
         const bool in_range = p >= 0 && p < cap_t;
-        bool store_ok = in_range;
+        const bool storing = a.k_reg != nullptr;  // null: rotate only (another launch stores)
+        bool store_ok = in_range && storing;
         if (a.table && in_range) {  // paged: the row's block, through the table
             const int b = __ldg(a.table + static_cast<size_t>(t) * a.max_blocks + p / a.block_rows);
             srow = static_cast<long long>(b) * a.block_rows + p % a.block_rows;
@@ -312,6 +373,7 @@ __device__ __forceinline__ void rope_kv_append_items(const RopeKvArgs &a, const 
             continue;
         }
         r -= nkp;  // float4 of v
+        if (!storing) continue;
         if (!store_ok) {
             if (r == 0) flag_error(a.err, in_range ? MINF_ERRBIT_BLOCK : MINF_ERRBIT_STORE_POS);
             continue;

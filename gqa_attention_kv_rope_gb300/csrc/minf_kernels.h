@@ -7,9 +7,15 @@
 
 namespace minf {
 
-// Storage of the K/V regions: fp32, or IEEE binary16 (converted on the store with round to
-// nearest even, read back exactly; the arithmetic stays fp32).
-enum KvKind : int { kKvF32 = 0, kKvF16 = 1 };
+// Storage of the K/V regions: fp32, IEEE binary16 (converted on the store with round to
+// nearest even, read back exactly), or Q8_0 blocks; the arithmetic stays fp32.
+enum KvKind : int { kKvF32 = 0, kKvF16 = 1, kKvQ8 = 2 };
+
+// Q8_0 storage ("11 . Attention, vec ops, and the KV cache", §2.5): a row of W values is W int8
+// quants, then W/32 binary16 block scales, then zero padding to a multiple of 16 bytes; the
+// store quantizes each 32-value block with d = max|x|/127, q = round(x * (1/d)) (halves away
+// from zero), and a value reads back as f16(d) * q.
+inline long long q8_row_bytes(int W) { return W + ((static_cast<long long>(W / 32) * 2 + 15) / 16) * 16; }
 
 struct RopeKvArgs {
     float *q;               // [nt, nh, hd], rotated in place
@@ -58,6 +64,12 @@ int launch_rope(float *x, const int32_t *pos, int nt, int nh, int hd, float thet
 int launch_kv_append(void *k_reg, void *v_reg, int kv, int cap, int W, const float *k_rows,
                      const float *v_rows, const int32_t *pos, int nt, int32_t *err,
                      cudaStream_t s);
+// Q8_0 store (one row per token at pos, at row_off[t] + pos with caps[t] when given; with a
+// table, token t is sequence t's token and its row goes through the table).
+int launch_kv_append_q8(void *k_reg, void *v_reg, int cap, int W, const float *k_rows, const float *v_rows,
+                        const int32_t *pos, int nt, const int64_t *row_off, const int32_t *caps,
+                        const int32_t *table, int max_blocks, int block_rows, int pool_blocks, int32_t *err,
+                        cudaStream_t s);
 // One row per sequence through a block table (the pool has pool_blocks blocks).
 int launch_kv_append_paged(void *k_pool, void *v_pool, int kv, int pool_blocks, int block_rows, int W,
                            const int32_t *table, int max_blocks, const float *k_rows, const float *v_rows,

@@ -35,6 +35,7 @@
 
 #include "minf_common.cuh"
 #include "minf_kernels.h"
+#include "minf_q8.cuh"
 #include "minf_sm103.cuh"
 
 namespace minf {
@@ -129,7 +130,8 @@ __device__ __forceinline__ uint32_t sw128_off(int row, int col) {
 
 struct PParams {
     float *out;
-    const void *k_reg, *v_reg;  // fp32 or binary16 elements (binary16 K is read without TMA)
+    const void *k_reg, *v_reg;  // fp32, binary16 or Q8_0 rows (only fp32 K is read by TMA)
+    long long row_bytes;        // Q8_0: bytes of a region row
     const int32_t *pos;
     int32_t *err;
     int nt, nh, nk, hd, cap, W;
@@ -310,12 +312,20 @@ __global__ void __launch_bounds__(kThreadsP, 1)
         // overlaps the current tile's products and softmax.
         constexpr int kV4 = HDKV / 16;
         float4 vnext[kV4];
+        // element group d4 (4 values) of this kv head in region row `key` (dequantized for Q8_0)
+        auto kv4 = [&](const void *reg, int key, int d4) -> float4 {
+            if constexpr (std::is_same<T, Q8>::value) {
+                const unsigned char *row = static_cast<const unsigned char *>(reg) + static_cast<size_t>(key) * a.row_bytes;
+                return ld4_q8(row, a.W, hk * (HDKV / 4) + d4);
+            } else {
+                return ld4(static_cast<const T *>(reg) + static_cast<size_t>(key) * a.W + hk * HDKV, d4);
+            }
+        };
         auto load_v = [&](int tile) {
             const int key = tile * BN + vk;
-            const T *vrow = static_cast<const T *>(a.v_reg) + static_cast<size_t>(key) * a.W + hk * HDKV;
 #pragma unroll
             for (int c = 0; c < kV4; ++c)
-                vnext[c] = key < lmax ? ld4(vrow, vq * kV4 + c) : make_float4(0.f, 0.f, 0.f, 0.f);
+                vnext[c] = key < lmax ? kv4(a.v_reg, key, vq * kV4 + c) : make_float4(0.f, 0.f, 0.f, 0.f);
         };
         if (n_tiles > 0) load_v(tile0);
         if (n_tiles > 0 && mbar_wait(&sm.bar_q, 0, abort_flag, a.err))
@@ -327,10 +337,9 @@ __global__ void __launch_bounds__(kThreadsP, 1)
                 split_region(&sm.kh[0][0], &sm.kl[0][0], BN * HDKV / 4, tid);
             } else {  // K tile -> SW128 slabs (keys along N); keys past the widest window are zero
                 const int key = j0 + vk;
-                const T *krow = static_cast<const T *>(a.k_reg) + static_cast<size_t>(key) * a.W + hk * HDKV;
 #pragma unroll 4
                 for (int d4 = vq * (HDKV / 16); d4 < (vq + 1) * (HDKV / 16); ++d4) {
-                    const float4 kv = key < lmax ? ld4(krow, d4) : make_float4(0.f, 0.f, 0.f, 0.f);
+                    const float4 kv = key < lmax ? kv4(a.k_reg, key, d4) : make_float4(0.f, 0.f, 0.f, 0.f);
                     const float kk[4] = {kv.x, kv.y, kv.z, kv.w};
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
@@ -511,6 +520,7 @@ int launch_t(const PrefillArgs &pa, cudaStream_t s) {
     a.out = pa.out;
     a.k_reg = pa.k_reg;
     a.v_reg = pa.v_reg;
+    a.row_bytes = q8_row_bytes(pa.nk * HDKV);
     a.pos = pa.pos;
     a.err = pa.err;
     a.nt = pa.nt;
@@ -568,6 +578,11 @@ int launch_prefill(const PrefillArgs &pa, cudaStream_t s) {
     if (pa.kv == kKvF16) {
         if (pa.hd_kv == 64) return launch_t<64, __half>(pa, s);
         if (pa.hd_kv == 128) return launch_t<128, __half>(pa, s);
+        return MINF_ERR_UNSUPPORTED;
+    }
+    if (pa.kv == kKvQ8) {
+        if (pa.hd_kv == 64) return launch_t<64, Q8>(pa, s);
+        if (pa.hd_kv == 128) return launch_t<128, Q8>(pa, s);
         return MINF_ERR_UNSUPPORTED;
     }
     if (pa.hd_kv == 64) return launch_t<64, float>(pa, s);

@@ -14,13 +14,28 @@ caller that needs more rows builds a new manager (and re-captures its graphs).
 
 Regions may also be kept in f16 (dtype=torch.float16: IEEE binary16, §2.5 of the
 same page: the GPU backends may keep the K/V regions in f16, halving the bytes an
-attention read moves); the library's `_f16` entry points read and write them.
+attention read moves) or in Q8_0 blocks (dtype=torch.uint8: each row is W int8 quants,
+W/32 binary16 scales and padding to 16 bytes, q8_row_bytes(W) bytes); the library's
+`_f16` and `_q8` entry points read and write them.
 """
 from __future__ import annotations
 
 import torch
 
 from . import binding
+
+_KINDS = (torch.float32, torch.float16, torch.uint8)
+
+
+def q8_row_bytes(row_width: int) -> int:
+    """Bytes of a Q8_0 row of row_width values (quants, scales, padding to 16 bytes)."""
+    if row_width <= 0 or row_width % 32:
+        raise ValueError("Q8_0 rows hold whole 32-value blocks")
+    return row_width + ((row_width // 32) * 2 + 15) // 16 * 16
+
+
+def _row_cols(row_width: int, dtype) -> int:
+    return q8_row_bytes(row_width) if dtype == torch.uint8 else row_width
 
 
 class KvRegions:
@@ -29,11 +44,12 @@ class KvRegions:
     def __init__(self, n_layer: int, row_width: int, cap: int, device="cuda", dtype=torch.float32):
         if n_layer <= 0 or row_width <= 0 or cap <= 0:
             raise ValueError("n_layer, row_width and cap must be positive")
-        if dtype not in (torch.float32, torch.float16):
-            raise ValueError("regions are float32 or float16")
+        if dtype not in _KINDS:
+            raise ValueError("regions are float32, float16 or uint8 (Q8_0 rows)")
         self.n_layer, self.row_width, self.cap, self.dtype = n_layer, row_width, cap, dtype
-        self.k = torch.empty((n_layer, cap, row_width), dtype=dtype, device=device)
-        self.v = torch.empty((n_layer, cap, row_width), dtype=dtype, device=device)
+        cols = _row_cols(row_width, dtype)
+        self.k = torch.empty((n_layer, cap, cols), dtype=dtype, device=device)
+        self.v = torch.empty((n_layer, cap, cols), dtype=dtype, device=device)
 
     def view(self, layer: int):
         """(K region, V region) of a layer: views into the persistent storage."""
@@ -52,8 +68,8 @@ class KvArena:
     def __init__(self, n_layer: int, row_width: int, caps: list[int], device="cuda", dtype=torch.float32):
         if not caps or min(caps) <= 0:
             raise ValueError("every sequence needs a positive capacity")
-        if dtype not in (torch.float32, torch.float16):
-            raise ValueError("arenas are float32 or float16")
+        if dtype not in _KINDS:
+            raise ValueError("arenas are float32, float16 or uint8 (Q8_0 rows)")
         self.n_layer, self.row_width, self.dtype = n_layer, row_width, dtype
         self.caps_host = list(int(c) for c in caps)
         offs, acc = [], 0
@@ -63,8 +79,9 @@ class KvArena:
         self.offsets_host = offs
         self.rows = acc
         self.max_cap = max(self.caps_host)
-        self.k = torch.empty((n_layer, acc, row_width), dtype=dtype, device=device)
-        self.v = torch.empty((n_layer, acc, row_width), dtype=dtype, device=device)
+        cols = _row_cols(row_width, dtype)
+        self.k = torch.empty((n_layer, acc, cols), dtype=dtype, device=device)
+        self.v = torch.empty((n_layer, acc, cols), dtype=dtype, device=device)
         self.row_off = torch.tensor(offs, dtype=torch.int64, device=device)
         self.cap = torch.tensor(self.caps_host, dtype=torch.int32, device=device)
 

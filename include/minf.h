@@ -298,6 +298,49 @@ MINF_API int minf_layer_attn_step_batched_f16(float *xn, const float *h, const f
                                               size_t ws_bytes, int32_t *err, minf_stream_t stream);
 
 /*
+ * The Q8_0 cache ([P1] §2.5: the store quantizes each row into Q8_0 blocks --
+ * 32 consecutive values kept as one binary16 scale and 32 int8 quants -- and
+ * the attention read dequantizes the window it uses).  These entry points are
+ * the fp32 ones with the regions (or arena, or pool) holding Q8_0 rows as bytes:
+ * a row of W values is W int8 quants, then W/32 binary16 scales, then zero
+ * padding to a multiple of 16 bytes -- minf_q8_row_bytes(W) bytes (1088 for
+ * W = 1024, the pages' 3.76x).  The store quantizes each block with
+ * d = max|x|/127 and q = round(x * (1/d)), halves away from zero (the pages
+ * name the format, not the rounding); a value reads back as f16(d) * q, exactly
+ * in fp32, and the attention is the fp32 attention over those values.  q, k, v,
+ * out, h, xn stay fp32; the rotated k written back to `k` is not quantized.
+ * W must be a multiple of 32.  Workspace sizes: the same functions as for fp32.
+ * Device errors and statuses: as the fp32 entry points.
+ */
+MINF_API size_t minf_q8_row_bytes(int row_width); /* 0 when row_width is not a positive multiple of 32 */
+MINF_API int minf_kv_append_q8(uint8_t *k_reg, uint8_t *v_reg, int cap, int row_width, const float *k_rows,
+                               const float *v_rows, const int32_t *pos, int nt, int32_t *err, minf_stream_t stream);
+MINF_API int minf_rope_kv_append_q8(float *q, float *k, const float *v, const int32_t *pos, int nt, int n_head,
+                                    int n_kv_head, int hd, int hd_kv, float theta, float freq_scale, int style,
+                                    uint8_t *k_reg, uint8_t *v_reg, int cap, int32_t *err, minf_stream_t stream);
+MINF_API int minf_gqa_attn_decode_q8(float *out, const float *q, const uint8_t *k_reg, const uint8_t *v_reg,
+                                     const int64_t *seq_row_off, const int32_t *seq_cap, int max_cap,
+                                     int64_t arena_rows, const int32_t *pos, int n_seq, int n_head, int n_kv_head,
+                                     int hd, int hd_kv, float scale, void *ws, size_t ws_bytes, int32_t *err,
+                                     minf_stream_t stream);
+MINF_API int minf_gqa_attn_prefill_q8(float *out, const float *q, const uint8_t *k_reg, const uint8_t *v_reg,
+                                      int cap, const int32_t *pos, int nt, int n_head, int n_kv_head, int hd,
+                                      int hd_kv, float scale, void *ws, size_t ws_bytes, int32_t *err,
+                                      minf_stream_t stream);
+MINF_API int minf_layer_attn_step_q8(float *xn, const float *h, const float *gain, float eps, int n_embd, float *q,
+                                     float *k, const float *v, const int32_t *pos, int nt, uint8_t *k_reg,
+                                     uint8_t *v_reg, int cap, int n_head, int n_kv_head, int hd, int hd_kv,
+                                     float theta, float freq_scale, int style, float *out, void *ws,
+                                     size_t ws_bytes, int32_t *err, minf_stream_t stream);
+MINF_API int minf_layer_attn_step_batched_q8(float *xn, const float *h, const float *gain, float eps, int n_embd,
+                                             float *q, float *k, const float *v, const int32_t *pos, int n_seq,
+                                             uint8_t *k_arena, uint8_t *v_arena, const int64_t *seq_row_off,
+                                             const int32_t *seq_cap, int max_cap, int64_t arena_rows, int n_head,
+                                             int n_kv_head, int hd, int hd_kv, float theta, float freq_scale,
+                                             int style, float *out, void *ws, size_t ws_bytes, int32_t *err,
+                                             minf_stream_t stream);
+
+/*
  * Paged regions ([P2]: the paged cache keeps a sequence as scattered fixed-size
  * blocks, so it has no contiguous view to lend; [P3] §2.2: the window the
  * attention reads is an explicit input).  A pool k_pool / v_pool of pool_rows
@@ -341,6 +384,22 @@ MINF_API int minf_layer_attn_step_paged(float *xn, const float *h, const float *
                                         int max_blocks, int block_rows, int n_head, int n_kv_head, int hd,
                                         int hd_kv, float theta, float freq_scale, int style, float *out, void *ws,
                                         size_t ws_bytes, int32_t *err, minf_stream_t stream);
+MINF_API int minf_kv_append_paged_q8(uint8_t *k_pool, uint8_t *v_pool, int64_t pool_rows, int row_width,
+                                     const int32_t *block_table, int max_blocks, int block_rows, const float *k_rows,
+                                     const float *v_rows, const int32_t *pos, int n_seq, int32_t *err,
+                                     minf_stream_t stream);
+MINF_API int minf_gqa_attn_decode_paged_q8(float *out, const float *q, const uint8_t *k_pool,
+                                           const uint8_t *v_pool, int64_t pool_rows, const int32_t *block_table,
+                                           int max_blocks, int block_rows, const int32_t *pos, int n_seq,
+                                           int n_head, int n_kv_head, int hd, int hd_kv, float scale, void *ws,
+                                           size_t ws_bytes, int32_t *err, minf_stream_t stream);
+MINF_API int minf_layer_attn_step_paged_q8(float *xn, const float *h, const float *gain, float eps, int n_embd,
+                                           float *q, float *k, const float *v, const int32_t *pos, int n_seq,
+                                           uint8_t *k_pool, uint8_t *v_pool, int64_t pool_rows,
+                                           const int32_t *block_table, int max_blocks, int block_rows, int n_head,
+                                           int n_kv_head, int hd, int hd_kv, float theta, float freq_scale,
+                                           int style, float *out, void *ws, size_t ws_bytes, int32_t *err,
+                                           minf_stream_t stream);
 MINF_API int minf_layer_attn_step_paged_f16(float *xn, const float *h, const float *gain, float eps, int n_embd,
                                             float *q, float *k, const float *v, const int32_t *pos, int n_seq,
                                             uint16_t *k_pool, uint16_t *v_pool, int64_t pool_rows,
