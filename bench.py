@@ -217,6 +217,14 @@ def setup_long_context(m, torch, wl, n_cached, dev, n_layer=None, dtype=None):
     for layer in range(g.n_layer):
         k, v = regions.view(layer)
         gen = torch.Generator(device=dev)
+        if regions.dtype == torch.uint8:
+            # Q8_0 rows: random quants with one scale (1/64) per block, a valid encoding
+            for t, name in ((k, "K"), (v, "V")):
+                gen.manual_seed(wl.sub_seed("long-context", layer, name))
+                t.random_(0, 256, generator=gen)
+                t[:, g.row_width:g.row_width + g.row_width // 16].view(torch.float16).fill_(1.0 / 64)
+                t[:, g.row_width + g.row_width // 16:] = 0
+            continue
         gen.manual_seed(wl.sub_seed("long-context", layer, "K"))
         k.normal_(generator=gen)
         gen.manual_seed(wl.sub_seed("long-context", layer, "V"))
@@ -251,7 +259,8 @@ def views(S, layer):
 
 def decode_step(m, S, layers=None):
     g = S["g"]
-    fn = m.binding.minf_layer_attn_step_f16 if S["regions"].k.element_size() == 2 else m.binding.minf_layer_attn_step
+    fn = {2: m.binding.minf_layer_attn_step_f16, 1: m.binding.minf_layer_attn_step_q8}.get(
+        S["regions"].k.element_size(), m.binding.minf_layer_attn_step)
     for layer in range(g.n_layer) if layers is None else layers:
         h, q, k, v, xn, out = views(S, layer)
         K, V = S["regions"].view(layer)
@@ -566,11 +575,11 @@ def run_batched_paged(m, torch, wl, dev, steps, block_rows=64):
     return res
 
 
-def run_long_context_f16(m, torch, wl, dev, steps):
-    """The headline workload (28 layers, nkv = 40960) with binary16 regions: the bytes the
-    step reads halve, the arithmetic stays fp32."""
+def run_long_context_kind(m, torch, wl, dev, steps, dtype):
+    """The headline workload (28 layers, nkv = 40960) with binary16 or Q8_0 regions: the bytes
+    the step reads shrink (2x, 3.76x), the arithmetic stays fp32."""
     n = wl.LONG_CONTEXT_SWEEP[-1]
-    S = setup_long_context(m, torch, wl, n, dev, dtype=torch.float16)
+    S = setup_long_context(m, torch, wl, n, dev, dtype=dtype)
     g = S["g"]
     stream = torch.cuda.Stream()
     graph = capture(torch, stream, lambda: decode_step(m, S))
@@ -585,7 +594,8 @@ def run_long_context_f16(m, torch, wl, dev, steps):
         b.record(stream)
     torch.cuda.synchronize()
     ms = a.elapsed_time(b) / steps
-    kv = kv_bytes_long_context(g, n) // 2
+    row_bytes = S["regions"].k.shape[-1] * S["regions"].k.element_size()  # per K (or V) row
+    kv = g.n_layer * 2 * (n + 1) * row_bytes
     res = {"step_ms": round(ms, 4), "kv_read_gbs": round(kv / (ms * 1e-3) / 1e9, 1), "kv_bytes_per_step": kv,
            "err": int(S["err"].item())}
     del graph
@@ -804,7 +814,10 @@ def main(argv=None):
         secondary["decode_loop"] = run_decode_loop(m, torch, wl, dev)
         secondary["batched_decode"] = run_batched(m, torch, wl, dev, max(3, args.steps // 4))
         secondary["batched_decode_paged"] = run_batched_paged(m, torch, wl, dev, max(3, args.steps // 4))
-        secondary["long_context_f16"] = run_long_context_f16(m, torch, wl, dev, max(5, args.steps // 2))
+        secondary["long_context_f16"] = run_long_context_kind(m, torch, wl, dev, max(5, args.steps // 2),
+                                                              torch.float16)
+        secondary["long_context_q8"] = run_long_context_kind(m, torch, wl, dev, max(5, args.steps // 2),
+                                                             torch.uint8)
         secondary["batched_decode_f16"] = run_batched(m, torch, wl, dev, max(3, args.steps // 4),
                                                       dtype=torch.float16)
         secondary["elementwise"] = run_elementwise(m, torch, dev)
