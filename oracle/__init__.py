@@ -112,6 +112,11 @@ def _load():
         lib.orc_q8_dequant_rows.restype = None
         lib.orc_kv_append_q8.argtypes = [_u8p, _u8p, ctypes.c_int, ctypes.c_int, _f32p, _f32p, _i32p, ctypes.c_int]
         lib.orc_kv_append_q8.restype = ctypes.c_int
+        lib.orc_fused_qkv.argtypes = [_f32p, _f32p, _f32p, _f32p, _f32p, _f32p, ctypes.c_float, ctypes.c_int,
+                                      _f32p, _f32p, _i32p, ctypes.c_int, _f32p, _f32p, ctypes.c_int, ctypes.c_int,
+                                      ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_float, ctypes.c_float,
+                                      ctypes.c_int]
+        lib.orc_fused_qkv.restype = ctypes.c_int
         _lib = lib
         return lib
 
@@ -401,3 +406,30 @@ def kv_append_q8(k_reg, v_reg, W: int, k_rows, v_rows, pos, check=True) -> int:
     if check and st != OK:
         raise OracleError(st, "kv_append_q8")
     return st
+
+
+# ----------------------------------------------------------------------------- fused QKV op
+def fused_qkv(h, gain, w, b, pos, k_reg, v_reg, *, n_head: int, n_kv_head: int, hd: int, hd_kv: int,
+              eps: float = 1e-6, theta: float = 1e6, freq_scale: float = 1.0, style: int = 0):
+    """RMSNorm, the q/k/v projections (w [n_out, n_embd], b [n_out] or None), RoPE on q and k,
+    and the K/V store at pos (regions modified in place).  Returns (xn, q, k, v)."""
+    h = _f32(h)
+    nt, n_embd = h.shape
+    gain = _f32(gain)
+    w = _f32(w)
+    bb = _f32(b) if b is not None else None
+    pos = _i32(pos)
+    k_reg = _f32(k_reg, writable=True)
+    v_reg = _f32(v_reg, writable=True)
+    W = n_kv_head * hd_kv
+    xn = np.empty_like(h)
+    q = np.empty((nt, n_head * hd), np.float32)
+    k = np.empty((nt, W), np.float32)
+    v = np.empty((nt, W), np.float32)
+    st = _load().orc_fused_qkv(_p(xn, _f32p), _p(q, _f32p), _p(k, _f32p), _p(v, _f32p), _p(h, _f32p),
+                               _p(gain, _f32p), eps, n_embd, _p(w, _f32p), _p(bb, _f32p) if bb is not None else None,
+                               _p(pos, _i32p), nt, _p(k_reg, _f32p), _p(v_reg, _f32p), k_reg.shape[0], n_head,
+                               n_kv_head, hd, hd_kv, theta, freq_scale, style)
+    if st != OK:
+        raise OracleError(st, "fused_qkv")
+    return xn, q, k, v

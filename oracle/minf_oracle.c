@@ -24,7 +24,7 @@
  *   orc_attn_bruteforce_f64, orc_silu_mul, orc_layer_attn_step,
  *   orc_f32_to_f16, orc_f16_to_f32, orc_kv_append_f16,
  *   orc_layer_attn_step_f16, orc_kv_append_paged, orc_gqa_attn_paged,
- *   orc_q8_quantize_row, orc_q8_dequant_row, orc_kv_append_q8 -- all pinned.
+ *   orc_q8_quantize_row, orc_q8_dequant_row, orc_kv_append_q8, orc_fused_qkv -- all pinned.
  */
 #include <math.h>
 #include <pthread.h>
@@ -588,6 +588,52 @@ int orc_kv_append_f16(uint16_t *k_reg, uint16_t *v_reg, int cap, int W,
         orc_f32_to_f16_array(v_reg + (size_t)p * W, v_rows + (size_t)t * W, W);
     }
     return ORC_OK;
+}
+
+/* ------------------------------------------------------------------------ */
+/* The fused QKV decode op.  [P3] §2.3: for a single token, a GPU build merges the
+ * three projection matmuls, their three biases, the two RoPEs and the two KV
+ * stores into one op.  Here, per token t: xn = RMSNorm(h) * gain ([P1] §3.2.1);
+ * y = W xn + b with W [n_out, n_embd] whose rows are the nh*hd q outputs, then
+ * the nk*hdkv k outputs, then the nk*hdkv v outputs, and b [n_out] (NULL: no
+ * bias), every output a dot product accumulated in double and rounded once to
+ * fp32 before the bias is added in fp32; then q and k rotated at pos ([P1]
+ * §3.2.2) and the rotated k and v stored at pos ([P1] §3.2.3). */
+int orc_fused_qkv(float *xn, float *q, float *k, float *v, const float *h, const float *gain, float eps,
+                  int n_embd, const float *w, const float *b, const int32_t *pos, int nt, float *k_reg,
+                  float *v_reg, int cap, int nh, int nk, int hd, int hdkv, float theta, float freq_scale, int style)
+{
+    if (hd < hdkv || nh <= 0 || nk <= 0 || nh % nk != 0)
+        return ORC_ERR_GEOMETRY;
+    if (n_embd <= 0 || nt < 0)
+        return ORC_ERR_ARG;
+    orc_rms_norm(xn, h, gain, nt, n_embd, eps);
+    int nq = nh * hd, W = nk * hdkv, n_out = nq + 2 * W;
+    for (int t = 0; t < nt; ++t) {
+        const float *x = xn + (size_t)t * n_embd;
+        for (int j = 0; j < n_out; ++j) {
+            const float *wr = w + (size_t)j * n_embd;
+            double acc = 0.0;
+            for (int i = 0; i < n_embd; ++i)
+                acc += (double)wr[i] * (double)x[i];
+            float y = (float)acc;
+            if (b)
+                y = y + b[j];
+            if (j < nq)
+                q[(size_t)t * nq + j] = y;
+            else if (j < nq + W)
+                k[(size_t)t * W + (j - nq)] = y;
+            else
+                v[(size_t)t * W + (j - nq - W)] = y;
+        }
+    }
+    int st = orc_rope(q, pos, nt, nh, hd, theta, freq_scale, style);
+    if (st != ORC_OK)
+        return st;
+    st = orc_rope(k, pos, nt, nk, hdkv, theta, freq_scale, style);
+    if (st != ORC_OK)
+        return st;
+    return orc_kv_append(k_reg, v_reg, cap, W, k, v, pos, nt);
 }
 
 /* ------------------------------------------------------------------------ */

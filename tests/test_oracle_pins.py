@@ -651,3 +651,56 @@ def test_kv_append_q8_placement_and_errors(orc):
     np.testing.assert_array_equal(Kr[keep], K0[keep])
     assert orc.kv_append_q8(Kr, Vr, W, k, v, [cap, 0], check=False) == orc.ERR_POS
     assert orc.kv_append_q8(Kr, Vr, W, k[:1], v[:1], [-1], check=False) == orc.ERR_POS
+
+
+# --------------------------------------------------------------------------- fused QKV op
+# "13 . The decode loop and graph reuse", §2.3: the fused QKV op merges the three projections,
+# their biases, the two RoPEs and the two KV stores.  Pins: the projections against numpy's
+# float64 matmul (an independent implementation), selection weights that reduce the op to the
+# already-pinned RMSNorm, RoPE and store, and the store's placement.
+def _qkv_case(r, nt=2, nh=4, nk=2, hd=16, hdkv=16, n_embd=48):
+    n_out = nh * hd + 2 * nk * hdkv
+    h = r.standard_normal((nt, n_embd)).astype(np.float32)
+    gain = r.uniform(0.5, 1.5, n_embd).astype(np.float32)
+    w = (r.standard_normal((n_out, n_embd)) / np.sqrt(n_embd)).astype(np.float32)
+    b = r.standard_normal(n_out).astype(np.float32)
+    return h, gain, w, b, (nh, nk, hd, hdkv)
+
+
+def test_fused_qkv_projection_matches_float64_matmul(orc):
+    r = _rng(80)
+    h, gain, w, b, (nh, nk, hd, hdkv) = _qkv_case(r)
+    cap, W = 10, nk * hdkv
+    K, V = np.zeros((cap, W), np.float32), np.zeros((cap, W), np.float32)
+    xn, q, k, v = orc.fused_qkv(h, gain, w, b, [0, 0], K, V, n_head=nh, n_kv_head=nk, hd=hd, hd_kv=hdkv)
+    np.testing.assert_array_equal(xn, orc.rms_norm(h, gain, eps=1e-6))
+    y = (xn.astype(np.float64) @ w.astype(np.float64).T).astype(np.float32) + b  # pos 0: RoPE is the identity
+    nq = nh * hd
+    np.testing.assert_allclose(q, y[:, :nq], rtol=0, atol=4e-7 * np.abs(y).max())
+    np.testing.assert_allclose(k, y[:, nq:nq + W], rtol=0, atol=4e-7 * np.abs(y).max())
+    np.testing.assert_allclose(v, y[:, nq + W:], rtol=0, atol=4e-7 * np.abs(y).max())
+
+
+def test_fused_qkv_with_selection_weights_is_rmsnorm_rope_store(orc):
+    r = _rng(81)
+    h, gain, _, b, (nh, nk, hd, hdkv) = _qkv_case(r, n_embd=64)
+    n_embd = h.shape[1]
+    nq, W = nh * hd, nk * hdkv
+    n_out = nq + 2 * W
+    sel = r.integers(0, n_embd, size=n_out)
+    w = np.zeros((n_out, n_embd), np.float32)
+    w[np.arange(n_out), sel] = 1.0                    # output j picks xn[sel[j]] exactly
+    cap, pos = 12, [3, 7]
+    K, V = r.standard_normal((cap, W)).astype(np.float32), r.standard_normal((cap, W)).astype(np.float32)
+    K0, V0 = K.copy(), V.copy()
+    xn, q, k, v = orc.fused_qkv(h, gain, w, b, pos, K, V, n_head=nh, n_kv_head=nk, hd=hd, hd_kv=hdkv)
+    y = xn[:, sel] + b
+    np.testing.assert_array_equal(q, orc.rope(y[:, :nq].copy(), pos, nh, hd, 1e6))
+    np.testing.assert_array_equal(k, orc.rope(y[:, nq:nq + W].copy(), pos, nk, hdkv, 1e6))
+    np.testing.assert_array_equal(v, y[:, nq + W:])
+    orc.kv_append(K0, V0, k, v, pos)
+    np.testing.assert_array_equal(K, K0)
+    np.testing.assert_array_equal(V, V0)
+    # without a bias the outputs are the selected values themselves
+    _, q2, _, _ = orc.fused_qkv(h, gain, w, None, [0, 0], K, V, n_head=nh, n_kv_head=nk, hd=hd, hd_kv=hdkv)
+    np.testing.assert_array_equal(q2, xn[:, sel[:nq]])
