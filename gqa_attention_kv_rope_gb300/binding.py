@@ -80,6 +80,11 @@ _SIGS = {
                                        _P], _I),
     "minf_layer_attn_step_paged_q8": ([_P, _P, _P, _F, _I, _P, _P, _P, _P, _I, _P, _P, _I64, _P, _I, _I, _I, _I,
                                        _I, _I, _F, _F, _I, _P, _P, _SZ, _P, _P], _I),
+    # the fused QKV decode op
+    "minf_fused_qkv": ([_P, _P, _P, _F, _I, _P, _P, _P, _I, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _F, _I, _P,
+                        _P], _I),
+    "minf_layer_attn_step_qkv": ([_P, _P, _P, _F, _I, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _F, _F,
+                                  _I, _P, _P, _SZ, _P, _P], _I),
     # paged regions: a pool of blocks and a block table per sequence
     "minf_kv_append_paged": ([_P, _P, _I64, _I, _P, _I, _I, _P, _P, _P, _I, _P, _P], _I),
     "minf_kv_append_paged_f16": ([_P, _P, _I64, _I, _P, _I, _I, _P, _P, _P, _I, _P, _P], _I),
@@ -499,3 +504,25 @@ def minf_layer_attn_step_batched_q8(xn, h, gain, eps, q, k, v, pos, k_arena, v_a
         k_arena.shape[0], n_head, n_kv_head, hd, hd_kv, theta, freq_scale, style, _dev(out, name="out"),
         _dev(ws, torch.uint8, "ws"), ws.numel(), _dev(err, torch.int32, "err"), _stream(stream)),
         "minf_layer_attn_step_batched_q8")
+
+
+# ----------------------------------------------------------------------------- fused QKV op
+def minf_fused_qkv(xn, h, gain, eps, w_qkv, b_qkv, pos, q, k, v, k_reg, v_reg, n_head, n_kv_head, hd, hd_kv, theta,
+                   freq_scale, style, err, stream=None):
+    nt, n_embd = h.shape
+    _check(lib().minf_fused_qkv(
+        _dev(xn, name="xn"), _dev(h, name="h"), _dev(gain, name="gain"), eps, n_embd, _dev(w_qkv, name="w_qkv"),
+        _dev(b_qkv, name="b_qkv"), _dev(pos, torch.int32, "pos"), nt, _dev(q, name="q"), _dev(k, name="k"),
+        _dev(v, name="v"), _dev(k_reg, name="k_reg"), _dev(v_reg, name="v_reg"), k_reg.shape[0], n_head, n_kv_head,
+        hd, hd_kv, theta, freq_scale, style, _dev(err, torch.int32, "err"), _stream(stream)), "minf_fused_qkv")
+
+
+def minf_layer_attn_step_qkv(xn, h, gain, eps, w_qkv, b_qkv, pos, q, k, v, k_reg, v_reg, n_head, n_kv_head, hd, hd_kv,
+                             theta, freq_scale, style, out, ws, err, stream=None):
+    n_embd = h.shape[-1]
+    _check(lib().minf_layer_attn_step_qkv(
+        _dev(xn, name="xn"), _dev(h, name="h"), _dev(gain, name="gain"), eps, n_embd, _dev(w_qkv, name="w_qkv"),
+        _dev(b_qkv, name="b_qkv"), _dev(pos, torch.int32, "pos"), _dev(q, name="q"), _dev(k, name="k"),
+        _dev(v, name="v"), _dev(k_reg, name="k_reg"), _dev(v_reg, name="v_reg"), k_reg.shape[0], n_head, n_kv_head,
+        hd, hd_kv, theta, freq_scale, style, _dev(out, name="out"), _dev(ws, torch.uint8, "ws"), ws.numel(),
+        _dev(err, torch.int32, "err"), _stream(stream)), "minf_layer_attn_step_qkv")

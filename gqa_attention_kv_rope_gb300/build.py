@@ -18,7 +18,7 @@ CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "libminf.so")
 SOURCES = ["minf_api.cu", "minf_elementwise.cu", "minf_decode.cu", "minf_decode_f16.cu", "minf_decode_q8.cu",
-           "minf_prefill.cu", "minf_noalloc.cu"]
+           "minf_prefill.cu", "minf_noalloc.cu", "minf_qkv.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
          "--expt-relaxed-constexpr", f"-I{os.path.join(ROOT, 'include')}"]

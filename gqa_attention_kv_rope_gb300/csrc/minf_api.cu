@@ -663,4 +663,71 @@ int minf_layer_attn_step_paged_f16(float *xn, const float *h, const float *gain,
                                  style, out, ws, ws_bytes, err, stream);
 }
 
+// ----------------------------------------------------------------------------- fused QKV op
+// "13 . The decode loop and graph reuse", §2.3: the decode step's three projections, biases,
+// RoPEs and KV stores as one op (here with the RMSNorm in front).
+
+static int fused_qkv(float *xn, const float *h, const float *gain, float eps, int n_embd, const float *w_qkv,
+                     const float *b_qkv, const int32_t *pos, int nt, float *q, float *k, float *v, float *k_reg,
+                     float *v_reg, int cap, int n_head, int n_kv_head, int hd, int hd_kv, float theta,
+                     float freq_scale, int style, int32_t *err, cudaStream_t s) {
+    int st = check_heads(n_head, n_kv_head, hd, hd_kv);
+    if (st != MINF_OK) return st;
+    if (!ok_f(xn) || !ok_f(h) || (gain && !ok_f(gain)) || !ok_f(w_qkv) || !ok_f(q) || !ok_f(k) || !ok_f(v) ||
+        !ok_f(k_reg) || !ok_f(v_reg) || !pos || !err)
+        return MINF_ERR_ARG;
+    if (n_embd <= 0 || n_embd % 4 || nt < 0 || cap <= 0 || (style != 0 && style != 1)) return MINF_ERR_ARG;
+    if (nt > kQkvMaxTok) return MINF_ERR_UNSUPPORTED;
+    QkvArgs a = {};
+    a.xn = xn;
+    a.h = h;
+    a.gain = gain;
+    a.eps = eps;
+    a.n_embd = n_embd;
+    a.w = w_qkv;
+    a.b = b_qkv;
+    a.pos = pos;
+    a.nt = nt;
+    a.q = q;
+    a.k = k;
+    a.v = v;
+    a.k_reg = k_reg;
+    a.v_reg = v_reg;
+    a.cap = cap;
+    a.nh = n_head;
+    a.nk = n_kv_head;
+    a.hd = hd;
+    a.hd_kv = hd_kv;
+    a.style = style;
+    a.err = err;
+    return launch_fused_qkv(a, theta, freq_scale, s);
+}
+
+int minf_fused_qkv(float *xn, const float *h, const float *gain, float eps, int n_embd, const float *w_qkv,
+                   const float *b_qkv, const int32_t *pos, int nt, float *q, float *k, float *v, float *k_reg,
+                   float *v_reg, int cap, int n_head, int n_kv_head, int hd, int hd_kv, float theta, float freq_scale,
+                   int style, int32_t *err, minf_stream_t stream) {
+    return fused_qkv(xn, h, gain, eps, n_embd, w_qkv, b_qkv, pos, nt, q, k, v, k_reg, v_reg, cap, n_head, n_kv_head,
+                     hd, hd_kv, theta, freq_scale, style, err, cs(stream));
+}
+
+int minf_layer_attn_step_qkv(float *xn, const float *h, const float *gain, float eps, int n_embd, const float *w_qkv,
+                             const float *b_qkv, const int32_t *pos, float *q, float *k, float *v, float *k_reg,
+                             float *v_reg, int cap, int n_head, int n_kv_head, int hd, int hd_kv, float theta,
+                             float freq_scale, int style, float *out, void *ws, size_t ws_bytes, int32_t *err,
+                             minf_stream_t stream) {
+    int st = check_attn(n_head, n_kv_head, hd, hd_kv);
+    if (st != MINF_OK) return st;
+    if (!ok_f(out)) return MINF_ERR_ARG;
+    const size_t need = decode_workspace_bytes(1, n_head, n_kv_head, hd_kv, cap);
+    if (!ws || ws_bytes < need) return MINF_ERR_WORKSPACE;
+    cudaStream_t s = cs(stream);
+    st = fused_qkv(xn, h, gain, eps, n_embd, w_qkv, b_qkv, pos, 1, q, k, v, k_reg, v_reg, cap, n_head, n_kv_head, hd,
+                   hd_kv, theta, freq_scale, style, err, s);
+    if (st != MINF_OK) return st;
+    const float scale = 1.0f / sqrtf(static_cast<float>(hd));
+    return decode(out, q, k_reg, v_reg, kKvF32, nullptr, nullptr, cap, pos, 1, n_head, n_kv_head, hd, hd_kv, scale,
+                  ws, ws_bytes, err, s);
+}
+
 }  // extern "C"

@@ -87,6 +87,24 @@ struct NormArgs {
 int launch_layer_prologue(const RopeKvArgs &a, float theta, float freq_scale, const NormArgs &nrm, cudaStream_t s);
 int launch_silu_mul(float *y, const float *g, const float *u, long long n, cudaStream_t s);
 
+// The fused QKV decode op (RMSNorm, q/k/v projections with biases, RoPE, K/V store) for up to
+// kQkvMaxTok tokens of one sequence.
+constexpr int kQkvMaxTok = 16;
+struct QkvArgs {
+    float *xn;                 // [nt, n_embd] RMSNorm output
+    const float *h, *gain;     // [nt, n_embd], [n_embd] (gain nullable)
+    float eps;
+    int n_embd;
+    const float *w, *b;        // [n_out, n_embd] (q rows, k rows, v rows), [n_out] (nullable)
+    const int32_t *pos;        // [nt]
+    int nt;
+    float *q, *k, *v;          // [nt, nh*hd] rotated, [nt, W] rotated, [nt, W]
+    float *k_reg, *v_reg;      // regions [cap, W]
+    int cap, nh, nk, hd, hd_kv, style;
+    int32_t *err;
+};
+int launch_fused_qkv(const QkvArgs &a, float theta, float freq_scale, cudaStream_t s);
+
 // The rest of a decode layer step, fused into the attention launch (one token per sequence).
 struct DecodeStepExtra {
     float *k;             // [n_seq, nk, hd_kv] rotated in place

@@ -409,6 +409,38 @@ MINF_API int minf_layer_attn_step_paged_f16(float *xn, const float *h, const flo
                                             minf_stream_t stream);
 
 /*
+ * The fused QKV decode op ([P3] §2.3: for a single token the three projection
+ * matmuls, their biases, the two RoPEs and the two KV stores become one op),
+ * here with the RMSNorm in front, for nt <= 16 tokens of one sequence:
+ *   xn = RMSNorm(h) * gain                    ([P1] §3.2.1; xn [nt, n_embd])
+ *   y  = w_qkv xn + b_qkv                     (w_qkv [n_out, n_embd] fp32, rows: the
+ *        n_head*hd q outputs, then n_kv_head*hd_kv k outputs, then as many v outputs;
+ *        b_qkv [n_out] or NULL)
+ *   q [nt, n_head*hd] and k [nt, W] written rotated at pos ([P1] §3.2.2), v [nt, W];
+ *   the rotated k and v stored at row pos of the regions [cap, W] ([P1] §3.2.3).
+ * Each output is an fp32 dot product over n_embd (within 1e-5 + 1e-4|y| of an exact
+ * one for unit-variance inputs and weights scaled by 1/sqrt(n_embd)).
+ * Device errors: pos < 0 -> MINF_ERRBIT_ROPE_POS (q, k left unrotated) and
+ * MINF_ERRBIT_STORE_POS; pos >= cap -> MINF_ERRBIT_STORE_POS (not stored).
+ * Errors: MINF_ERR_UNSUPPORTED for nt > 16; MINF_ERR_ARG for n_embd not a multiple
+ * of 4 or unaligned pointers; MINF_ERR_GEOMETRY as elsewhere.
+ *
+ * minf_layer_attn_step_qkv: one decode token (nt = 1) from the hidden state h to the
+ * attention output: the fused QKV op, then the split-KV decode attention over
+ * [0, pos] (out [1, n_head*hd_kv]); ws as for minf_gqa_attn_decode with n_seq = 1.
+ */
+MINF_API int minf_fused_qkv(float *xn, const float *h, const float *gain, float eps, int n_embd,
+                            const float *w_qkv, const float *b_qkv, const int32_t *pos, int nt, float *q, float *k,
+                            float *v, float *k_reg, float *v_reg, int cap, int n_head, int n_kv_head, int hd,
+                            int hd_kv, float theta, float freq_scale, int style, int32_t *err,
+                            minf_stream_t stream);
+MINF_API int minf_layer_attn_step_qkv(float *xn, const float *h, const float *gain, float eps, int n_embd,
+                                      const float *w_qkv, const float *b_qkv, const int32_t *pos, float *q,
+                                      float *k, float *v, float *k_reg, float *v_reg, int cap, int n_head,
+                                      int n_kv_head, int hd, int hd_kv, float theta, float freq_scale, int style,
+                                      float *out, void *ws, size_t ws_bytes, int32_t *err, minf_stream_t stream);
+
+/*
  * SiLU times up ([P1] §3.2.5): y = gate / (1 + e^-gate) * up over n elements.
  * Errors: MINF_ERR_ARG for null pointers or n < 0.
  */

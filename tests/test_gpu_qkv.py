@@ -1,0 +1,135 @@
+"""GPU parity of the fused QKV decode op ("13 . The decode loop and graph reuse", §2.3: the
+three projections, their biases, the two RoPEs and the two KV stores as one op; here with the
+RMSNorm in front).  Synthetic weights ~ N(0, 1/n_embd) and biases ~ N(0, 1): outputs within
+1e-5 + 1e-4|ref| of the oracle (double-accumulated projections); V rows stored as computed
+(compared with the oracle at the same tolerance); the attention after the op against the
+oracle's attention over the regions the GPU left."""
+import numpy as np
+import pytest
+import torch
+
+pytestmark = pytest.mark.gpu
+
+ATOL, RTOL = 1e-5, 1e-4
+
+
+@pytest.fixture(scope="module")
+def m():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import gqa_attention_kv_rope_gb300 as pkg
+    from gqa_attention_kv_rope_gb300 import build
+
+    build.build()
+    pkg.binding.lib()
+    return pkg
+
+
+def close(got, ref, what=""):
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    assert got.shape == ref.shape, (what, got.shape, ref.shape)
+    d = np.abs(got - ref)
+    bad = d > ATOL + RTOL * np.abs(ref)
+    assert not bad.any(), f"{what}: {int(bad.sum())} elements off, max abs {d.max():.3g}"
+
+
+def rnd(shape, seed, scale=1.0):
+    return (torch.randn(*shape, generator=torch.Generator().manual_seed(seed)) * scale).numpy()
+
+
+def dev(x):
+    return None if x is None else torch.as_tensor(np.ascontiguousarray(x)).cuda()
+
+
+def err_word():
+    return torch.zeros(1, dtype=torch.int32, device="cuda")
+
+
+def _case(g, nt, seed, bias=True):
+    n_out = g.q_width + 2 * g.row_width
+    h = rnd((nt, g.n_embd), seed)
+    gain = np.random.default_rng(seed).uniform(0.5, 1.5, g.n_embd).astype(np.float32)
+    w = rnd((n_out, g.n_embd), seed + 1, scale=1.0 / np.sqrt(g.n_embd))
+    b = rnd((n_out,), seed + 2) if bias else None
+    return h, gain, w, b
+
+
+@pytest.mark.parametrize("which,nt,bias,style", [("qwen25", 1, True, 0), ("qwen3", 1, False, 0),
+                                                 ("qwen3", 7, True, 0), ("qwen25", 16, True, 1)])
+def test_fused_qkv(m, orc, which, nt, bias, style):
+    from gqa_attention_kv_rope_gb300 import workloads as wl
+
+    g = wl.QWEN25_05B if which == "qwen25" else wl.QWEN3_06B
+    cap = 900
+    h, gain, w, b = _case(g, nt, 10 + nt, bias)
+    pos = np.sort(np.random.default_rng(nt).choice(cap, nt, replace=False)).astype(np.int32)
+    K0, V0 = rnd((cap, g.row_width), 20), rnd((cap, g.row_width), 21)
+    Kd, Vd = dev(K0), dev(V0)
+    xn = torch.empty(nt, g.n_embd, device="cuda")
+    q = torch.empty(nt, g.q_width, device="cuda")
+    k = torch.empty(nt, g.row_width, device="cuda")
+    v = torch.empty(nt, g.row_width, device="cuda")
+    err = err_word()
+    m.minf_fused_qkv(xn, dev(h), dev(gain), g.eps, dev(w), dev(b), dev(pos), q, k, v, Kd, Vd, g.n_head, g.n_kv_head,
+                     g.hd, g.hd_kv, g.theta, 1.0, style, err)
+    torch.cuda.synchronize()
+    assert err.item() == 0
+    Ko, Vo = K0.copy(), V0.copy()
+    xn_r, q_r, k_r, v_r = orc.fused_qkv(h, gain, w, b, pos, Ko, Vo, n_head=g.n_head, n_kv_head=g.n_kv_head, hd=g.hd,
+                                        hd_kv=g.hd_kv, eps=g.eps, theta=g.theta, style=style)
+    close(xn.cpu().numpy(), xn_r, what="xn")
+    close(q.cpu().numpy(), q_r, what="q")
+    kg, vg = k.cpu().numpy(), v.cpu().numpy()
+    close(kg, k_r, what="k")
+    close(vg, v_r, what="v")
+    Kn, Vn = Kd.cpu().numpy(), Vd.cpu().numpy()
+    assert np.array_equal(Kn[pos], kg) and np.array_equal(Vn[pos], vg)  # stored exactly what it returned
+    keep = np.setdiff1d(np.arange(cap), pos)
+    assert np.array_equal(Kn[keep], K0[keep]) and np.array_equal(Vn[keep], V0[keep])
+
+
+def test_fused_qkv_position_errors(m):
+    from gqa_attention_kv_rope_gb300 import workloads as wl
+
+    g = wl.QWEN3_06B
+    cap = 64
+    h, gain, w, b = _case(g, 2, 30)
+    K0 = rnd((cap, g.row_width), 31)
+    Kd, Vd = dev(K0), dev(K0)
+    bufs = [torch.empty(2, n, device="cuda") for n in (g.n_embd, g.q_width, g.row_width, g.row_width)]
+    err = err_word()
+    m.minf_fused_qkv(bufs[0], dev(h), dev(gain), g.eps, dev(w), dev(b), dev(np.array([-1, cap], np.int32)), *bufs[1:],
+                     Kd, Vd, g.n_head, g.n_kv_head, g.hd, g.hd_kv, g.theta, 1.0, 0, err)
+    torch.cuda.synchronize()
+    assert err.item() == 0x1 | 0x2  # not rotated (pos < 0), not stored (both)
+    assert np.array_equal(Kd.cpu().numpy(), K0) and np.array_equal(Vd.cpu().numpy(), K0)
+
+
+@pytest.mark.parametrize("which", ["qwen25", "qwen3"])
+def test_layer_step_qkv_decode(m, orc, which):
+    from gqa_attention_kv_rope_gb300 import workloads as wl
+
+    g = wl.QWEN25_05B if which == "qwen25" else wl.QWEN3_06B
+    cap, p = 1200, 777
+    h, gain, w, b = _case(g, 1, 40, bias=which == "qwen25")
+    K0, V0 = rnd((cap, g.row_width), 41), rnd((cap, g.row_width), 42)
+    Kd, Vd = dev(K0), dev(V0)
+    xn = torch.empty(1, g.n_embd, device="cuda")
+    q = torch.empty(1, g.q_width, device="cuda")
+    k = torch.empty(1, g.row_width, device="cuda")
+    v = torch.empty(1, g.row_width, device="cuda")
+    out, err = torch.empty(1, g.out_width, device="cuda"), err_word()
+    ws = m.kv.decode_workspace(1, g.n_head, g.n_kv_head, g.hd_kv, cap)
+    m.minf_layer_attn_step_qkv(xn, dev(h), dev(gain), g.eps, dev(w), dev(b), dev(np.array([p], np.int32)), q, k, v,
+                               Kd, Vd, g.n_head, g.n_kv_head, g.hd, g.hd_kv, g.theta, 1.0, 0, out, ws, err)
+    torch.cuda.synchronize()
+    assert err.item() == 0
+    Ko, Vo = K0.copy(), V0.copy()
+    _, q_r, _, _ = orc.fused_qkv(h, gain, w, b, [p], Ko, Vo, n_head=g.n_head, n_kv_head=g.n_kv_head, hd=g.hd,
+                                 hd_kv=g.hd_kv, eps=g.eps, theta=g.theta)
+    close(q.cpu().numpy(), q_r, what="q")
+    scale = float(np.float32(1.0) / np.sqrt(np.float32(g.hd)))
+    ref = orc.gqa_attn(q.cpu().numpy().reshape(1, g.n_head, g.hd), Kd.cpu().numpy(), Vd.cpu().numpy(), [p],
+                       g.n_head, g.n_kv_head, g.hd, g.hd_kv, scale=scale)
+    close(out.cpu().numpy(), ref, what="out")
