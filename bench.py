@@ -575,6 +575,56 @@ def run_batched_paged(m, torch, wl, dev, steps, block_rows=64):
     return res
 
 
+def run_fused_qkv(m, torch, wl, dev, steps):
+    """The fused QKV decode op for one token through 28 layers (Qwen3-0.6B shape, synthetic
+    weights ~ N(0, 1/n_embd), one weight matrix per layer): weight GB/s (the op reads each
+    layer's 4096 x 1024 fp32 matrix once) and microseconds per layer."""
+    import numpy as np
+
+    g = wl.QWEN3_06B
+    n_out = g.q_width + 2 * g.row_width
+    cap = 2048
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(wl.sub_seed("qkv", 0))
+    Wt = torch.randn(g.n_layer, n_out, g.n_embd, device=dev, generator=gen) / float(np.sqrt(g.n_embd))
+    Bt = torch.randn(g.n_layer, n_out, device=dev, generator=gen)
+    K = torch.zeros(g.n_layer, cap, g.row_width, device=dev)
+    V = torch.zeros_like(K)
+    h = torch.randn(g.n_layer, 1, g.n_embd, device=dev, generator=gen)
+    gain = torch.ones(g.n_embd, device=dev)
+    xn = torch.empty(1, g.n_embd, device=dev)
+    q = torch.empty(1, g.q_width, device=dev)
+    k = torch.empty(1, g.row_width, device=dev)
+    v = torch.empty(1, g.row_width, device=dev)
+    pos = torch.tensor([cap // 2], dtype=torch.int32, device=dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    def step():
+        for layer in range(g.n_layer):
+            m.binding.minf_fused_qkv(xn, h[layer], gain, g.eps, Wt[layer], Bt[layer], pos, q, k, v, K[layer],
+                                     V[layer], g.n_head, g.n_kv_head, g.hd, g.hd_kv, g.theta, 1.0, 0, err)
+
+    stream = torch.cuda.Stream()
+    graph = capture(torch, stream, step)
+    for _ in range(3):
+        graph.replay()
+    torch.cuda.synchronize()
+    a, b = Timer(torch, stream).pair()
+    with torch.cuda.stream(stream):
+        a.record(stream)
+        for _ in range(steps):
+            graph.replay()
+        b.record(stream)
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / steps
+    wbytes = g.n_layer * n_out * g.n_embd * 4
+    res = {"layer_us": round(ms * 1e3 / g.n_layer, 2), "weight_gbs": round(wbytes / (ms * 1e-3) / 1e9, 1),
+           "err": int(err.item())}
+    del graph, Wt, K, V
+    torch.cuda.empty_cache()
+    return res
+
+
 def run_long_context_kind(m, torch, wl, dev, steps, dtype):
     """The headline workload (28 layers, nkv = 40960) with binary16 or Q8_0 regions: the bytes
     the step reads shrink (2x, 3.76x), the arithmetic stays fp32."""
@@ -814,6 +864,7 @@ def main(argv=None):
         secondary["decode_loop"] = run_decode_loop(m, torch, wl, dev)
         secondary["batched_decode"] = run_batched(m, torch, wl, dev, max(3, args.steps // 4))
         secondary["batched_decode_paged"] = run_batched_paged(m, torch, wl, dev, max(3, args.steps // 4))
+        secondary["fused_qkv"] = run_fused_qkv(m, torch, wl, dev, max(5, args.steps // 2))
         secondary["long_context_f16"] = run_long_context_kind(m, torch, wl, dev, max(5, args.steps // 2),
                                                               torch.float16)
         secondary["long_context_q8"] = run_long_context_kind(m, torch, wl, dev, max(5, args.steps // 2),
