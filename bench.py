@@ -47,7 +47,7 @@ def parse_args(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="budget of the CPU oracle sample")
     ap.add_argument("--layers", type=int, default=28, help="layers of the headline workload (profiling cases)")
     ap.add_argument("--nkv", type=int, default=40960, help="cached rows of the headline workload")
-    ap.add_argument("--only", choices=["prefill", "single-step"], default=None,
+    ap.add_argument("--only", choices=["prefill", "single-step", "fused-qkv"], default=None,
                     help="time one secondary workload alone (a small case for profiling)")
     return ap.parse_args(argv)
 
@@ -839,6 +839,14 @@ def main(argv=None):
             print(json.dumps({"metric": "layer attn-step µs", "value": us, "unit": "µs", "steps": args.steps,
                               "config": {"workload": "single decode step, one layer, Qwen2.5-0.5B shape, "
                                                      "127 cached rows, token at pos 127"}}))
+        return 0
+    if args.only == "fused-qkv":
+        r = run_fused_qkv(m, torch, wl, dev, args.steps)
+        if rank == 0:
+            print(json.dumps({"metric": "fused QKV weight GB/s", "value": r["weight_gbs"], "unit": "GB/s",
+                              "layer_us": r["layer_us"], "err": r["err"], "steps": args.steps,
+                              "config": {"workload": "fused QKV decode op, one token, Qwen3-0.6B shape, "
+                                                     "28 layers of synthetic weights"}}))
         return 0
     H = run_headline(m, torch, wl, args, world, dev)
     g = H["S"]["g"]

@@ -229,6 +229,11 @@ MINF_API size_t minf_attn_prefill_workspace_bytes(int nt, int n_head, int n_kv_h
  * tensor-core prefill path.  ws/ws_bytes: for nt == 1 at least
  * minf_attn_decode_workspace_bytes(1, n_head, n_kv_head, hd_kv, cap), for nt > 1
  * at least minf_attn_prefill_workspace_bytes(nt, n_head, n_kv_head, hd_kv, cap).
+ * Early start: the nt == 1 path is a programmatic dependent launch that reads pos and
+ * begins streaming the cached rows [0, pos) of the regions before the launch just before
+ * it on the stream has finished (h, gain, q, k, v, ws and every output only after): pos
+ * and those rows must not be written by that launch (a host-to-device copy is not a
+ * launch).  The nt > 1 path starts early only after its own first launch.
  * Device errors: any of the bits above.
  */
 MINF_API int minf_layer_attn_step(float *xn, const float *h, const float *gain, float eps, int n_embd,
@@ -422,8 +427,12 @@ MINF_API int minf_layer_attn_step_paged_f16(float *xn, const float *h, const flo
  * one for unit-variance inputs and weights scaled by 1/sqrt(n_embd)).
  * Device errors: pos < 0 -> MINF_ERRBIT_ROPE_POS (q, k left unrotated) and
  * MINF_ERRBIT_STORE_POS; pos >= cap -> MINF_ERRBIT_STORE_POS (not stored).
- * Errors: MINF_ERR_UNSUPPORTED for nt > 16; MINF_ERR_ARG for n_embd not a multiple
- * of 4 or unaligned pointers; MINF_ERR_GEOMETRY as elsewhere.
+ * Errors: MINF_ERR_UNSUPPORTED for nt > 16 or nt * n_embd * 4 > 227 KB (the normalized
+ * tokens are held in shared memory); MINF_ERR_ARG for n_embd not a multiple of 4 or
+ * unaligned pointers; MINF_ERR_GEOMETRY as elsewhere.
+ * Early start: the op is a programmatic dependent launch and begins reading w_qkv and
+ * b_qkv before the launch just before it on the stream has finished (h, gain, pos and
+ * every output only after): the weights must not be written by that launch.
  *
  * minf_layer_attn_step_qkv: one decode token (nt = 1) from the hidden state h to the
  * attention output: the fused QKV op, then the split-KV decode attention over

@@ -1,9 +1,11 @@
 """GPU parity of the fused QKV decode op ("13 . The decode loop and graph reuse", §2.3: the
 three projections, their biases, the two RoPEs and the two KV stores as one op; here with the
-RMSNorm in front).  Synthetic weights ~ N(0, 1/n_embd) and biases ~ N(0, 1): outputs within
+RMSNorm in front), for the two model shapes and a wide one.  Synthetic weights ~ N(0, 1/n_embd) and biases ~ N(0, 1): outputs within
 1e-5 + 1e-4|ref| of the oracle (double-accumulated projections); V rows stored as computed
 (compared with the oracle at the same tolerance); the attention after the op against the
 oracle's attention over the regions the GPU left."""
+from types import SimpleNamespace
+
 import numpy as np
 import pytest
 import torch
@@ -55,12 +57,24 @@ def _case(g, nt, seed, bias=True):
     return h, gain, w, b
 
 
-@pytest.mark.parametrize("which,nt,bias,style", [("qwen25", 1, True, 0), ("qwen3", 1, False, 0),
-                                                 ("qwen3", 7, True, 0), ("qwen25", 16, True, 1)])
-def test_fused_qkv(m, orc, which, nt, bias, style):
+# A wide geometry (n_embd 4096: four 128-bit loads a lane per weight row) beside the two model
+# shapes.
+WIDE = SimpleNamespace(n_embd=4096, n_head=32, n_kv_head=8, hd=128, hd_kv=128, eps=1e-6, theta=1e6,
+                       q_width=32 * 128, row_width=8 * 128)
+
+
+def geometry(which):
     from gqa_attention_kv_rope_gb300 import workloads as wl
 
-    g = wl.QWEN25_05B if which == "qwen25" else wl.QWEN3_06B
+    return {"qwen25": wl.QWEN25_05B, "qwen3": wl.QWEN3_06B, "wide": WIDE}[which]
+
+
+@pytest.mark.parametrize("which,nt,bias,style", [("qwen25", 1, True, 0), ("qwen3", 1, False, 0),
+                                                 ("qwen3", 7, True, 0), ("qwen25", 16, True, 1),
+                                                 ("qwen3", 3, True, 1), ("wide", 1, True, 0),
+                                                 ("wide", 5, False, 1), ("wide", 13, True, 0)])
+def test_fused_qkv(m, orc, which, nt, bias, style):
+    g = geometry(which)
     cap = 900
     h, gain, w, b = _case(g, nt, 10 + nt, bias)
     pos = np.sort(np.random.default_rng(nt).choice(cap, nt, replace=False)).astype(np.int32)
@@ -87,6 +101,22 @@ def test_fused_qkv(m, orc, which, nt, bias, style):
     assert np.array_equal(Kn[pos], kg) and np.array_equal(Vn[pos], vg)  # stored exactly what it returned
     keep = np.setdiff1d(np.arange(cap), pos)
     assert np.array_equal(Kn[keep], K0[keep]) and np.array_equal(Vn[keep], V0[keep])
+
+
+def test_fused_qkv_too_wide(m):
+    """16 tokens of 4096 values are 256 KB of normalized inputs: more shared memory than a CTA
+    has, refused on the host before any launch."""
+    g, nt = WIDE, 16
+    h, gain, w, b = _case(g, nt, 50)
+    bufs = [torch.empty(nt, n, device="cuda") for n in (g.n_embd, g.q_width, g.row_width, g.row_width)]
+    Kd = dev(rnd((8, g.row_width), 51))
+    err = err_word()
+    with pytest.raises(m.binding.MinfError) as e:
+        m.minf_fused_qkv(bufs[0], dev(h), dev(gain), g.eps, dev(w), dev(b), dev(np.arange(nt, dtype=np.int32) % 8),
+                         *bufs[1:], Kd, Kd.clone(), g.n_head, g.n_kv_head, g.hd, g.hd_kv, g.theta, 1.0, 0, err)
+    assert e.value.status == 3
+    torch.cuda.synchronize()
+    assert err.item() == 0
 
 
 def test_fused_qkv_position_errors(m):
