@@ -47,7 +47,8 @@ def parse_args(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="budget of the CPU oracle sample")
     ap.add_argument("--layers", type=int, default=28, help="layers of the headline workload (profiling cases)")
     ap.add_argument("--nkv", type=int, default=40960, help="cached rows of the headline workload")
-    ap.add_argument("--only", choices=["prefill", "single-step", "fused-qkv"], default=None,
+    ap.add_argument("--only", choices=["prefill", "single-step", "fused-qkv", "long-context-f16",
+                                       "long-context-q8"], default=None,
                     help="time one secondary workload alone (a small case for profiling)")
     return ap.parse_args(argv)
 
@@ -625,11 +626,12 @@ def run_fused_qkv(m, torch, wl, dev, steps):
     return res
 
 
-def run_long_context_kind(m, torch, wl, dev, steps, dtype):
+def run_long_context_kind(m, torch, wl, dev, steps, dtype, n=None, n_layer=None):
     """The headline workload (28 layers, nkv = 40960) with binary16 or Q8_0 regions: the bytes
-    the step reads shrink (2x, 3.76x), the arithmetic stays fp32."""
-    n = wl.LONG_CONTEXT_SWEEP[-1]
-    S = setup_long_context(m, torch, wl, n, dev, dtype=dtype)
+    the step reads shrink (2x, 3.76x), the arithmetic stays fp32.  n / n_layer: a smaller case
+    of the same kernel (profiling)."""
+    n = wl.LONG_CONTEXT_SWEEP[-1] if n is None else n
+    S = setup_long_context(m, torch, wl, n, dev, n_layer=n_layer, dtype=dtype)
     g = S["g"]
     stream = torch.cuda.Stream()
     graph = capture(torch, stream, lambda: decode_step(m, S))
@@ -839,6 +841,15 @@ def main(argv=None):
             print(json.dumps({"metric": "layer attn-step µs", "value": us, "unit": "µs", "steps": args.steps,
                               "config": {"workload": "single decode step, one layer, Qwen2.5-0.5B shape, "
                                                      "127 cached rows, token at pos 127"}}))
+        return 0
+    if args.only in ("long-context-f16", "long-context-q8"):
+        dt = torch.float16 if args.only.endswith("f16") else torch.uint8
+        r = run_long_context_kind(m, torch, wl, dev, args.steps, dt, n=args.nkv, n_layer=args.layers)
+        if rank == 0:
+            print(json.dumps({"metric": "decode attn KV-read GB/s", "value": r["kv_read_gbs"], "unit": "GB/s",
+                              "step_ms": r["step_ms"], "err": r["err"], "steps": args.steps,
+                              "config": {"workload": f"long-context decode, Qwen3-0.6B shape, {args.layers} layers, "
+                                                     f"nkv={args.nkv}, {args.only[13:]} regions"}}))
         return 0
     if args.only == "fused-qkv":
         r = run_fused_qkv(m, torch, wl, dev, args.steps)

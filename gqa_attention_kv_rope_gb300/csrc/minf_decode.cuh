@@ -129,6 +129,34 @@ __device__ __forceinline__ float4 ld_row4(const unsigned char *qrow, const unsig
     }
 }
 
+// The same four elements without the Q8_0 scale (exact integers as floats; the values
+// themselves for fp32 and binary16): the kernel applies a block's scale once to a partial sum.
+template <int HDKV, typename T>
+__device__ __forceinline__ float4 ld_row4_raw(const unsigned char *qrow, int i4) {
+    if constexpr (Elem<T>::q8) {
+        return deq4(reinterpret_cast<const uint32_t *>(qrow)[i4], 1.0f);
+    } else {
+        return ld4(reinterpret_cast<const T *>(qrow), i4);
+    }
+}
+
+// Q8_0: the scales of this kv head's HDKV/32 blocks in a row's scale slice (srow), as floats.
+template <int HDKV>
+__device__ __forceinline__ void ld_scales(const unsigned char *srow, int sc, float (&s)[HDKV / 32]) {
+    if constexpr (HDKV == 128) {
+        const uint2 u = *reinterpret_cast<const uint2 *>(srow + 2 * sc);
+        const float2 a = __half22float2(*reinterpret_cast<const __half2 *>(&u.x));
+        const float2 b = __half22float2(*reinterpret_cast<const __half2 *>(&u.y));
+        s[0] = a.x;
+        s[1] = a.y;
+        s[2] = b.x;
+        s[3] = b.y;
+    } else {
+        const float2 a = __half22float2(*reinterpret_cast<const __half2 *>(srow + 2 * sc));
+        s[0] = a.x;
+        s[1] = a.y;
+    }
+}
 
 struct KParams {
     float *out;
@@ -289,6 +317,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr int VL = HDKV / 4;    // lanes per V row (a float4 each)
     constexpr int VRP = 32 / VL;    // V rows a warp covers per pass
     constexpr int VJ = kSub / VRP;  // passes per sub-tile
+    constexpr int NACC = GH <= 2 ? 2 : 1;  // V accumulator sets a lane keeps per head
+    // sub-tiles whose rows share one online-softmax update (their scores are held at once)
+    constexpr int GRP = GH <= 2 ? SPW : (GH <= 4 ? (SPW < 2 ? SPW : 2) : 1);
+    static_assert(SPW % GRP == 0, "sub-tile groups");
 
     extern __shared__ unsigned char smem_raw[];
     // 1024-aligned ring, derived from the shared array itself so loads stay in the shared space
@@ -608,12 +640,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
         float m[GH], l[GH];
-        float4 acc[GH];
+        float4 accs[NACC][GH];  // V rows alternate between NACC accumulators (shorter FMA chains)
 #pragma unroll
         for (int hh = 0; hh < GH; ++hh) {
             m[hh] = -INFINITY;
             l[hh] = 0.0f;
-            acc[hh] = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+            for (int c = 0; c < NACC; ++c) accs[c][hh] = make_float4(0.f, 0.f, 0.f, 0.f);
         }
 
         // -------------------------------------------------------------- the unit's stages
@@ -624,7 +657,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             unsigned char *Ksc = Kq + C::kQBytes;                                 // K scale slices
             unsigned char *Vq = Kq + C::kTensorBytes;
             unsigned char *Vsc = Vq + C::kQBytes;
-            const int sc = (hk % kScaleHeads) * (HDKV / 32);  // this head's first scale in a slice
+            const int sc0 = (hk % kScaleHeads) * (HDKV / 32);  // this head's first scale in a slice
             const int row0 = t.r_begin + st * R;
             if (kFused && pnew >= row0 && pnew < row0 + R) {
                 // the tile may hold the row as it was before this launch appended it: the lanes
@@ -640,9 +673,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                             reinterpret_cast<uint32_t *>(Vq + rn * HDKV)[sub + 8 * i] =
                                 reinterpret_cast<const uint32_t *>(sm_vnew)[sub + 8 * i];
                             if (sub == 0) {
-                                reinterpret_cast<__half *>(Ksc + rn * 16)[sc + i] =
+                                reinterpret_cast<__half *>(Ksc + rn * 16)[sc0 + i] =
                                     reinterpret_cast<const __half *>(reinterpret_cast<const unsigned char *>(sm_knew) + HDKV)[i];
-                                reinterpret_cast<__half *>(Vsc + rn * 16)[sc + i] =
+                                reinterpret_cast<__half *>(Vsc + rn * 16)[sc0 + i] =
                                     reinterpret_cast<const __half *>(reinterpret_cast<const unsigned char *>(sm_vnew) + HDKV)[i];
                             }
                         }
@@ -659,81 +692,117 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 cons_sync(&cons_bar, cphase, abort_flag, a.err);
             }
+            // The warp's SPW sub-tiles of 8 rows, GRP at a time: the scores of all their rows
+            // first (a K row is spread over 8 lanes, four rows per pass), then one online-softmax
+            // update for them, then their V rows (one per pass of VL lanes).  Q8_0 blocks apply
+            // their scale once: to a block's partial dot product (K), and to the weight (V).
+#pragma unroll 1
+            for (int g0 = 0; g0 < SPW; g0 += GRP) {  // one pass when the heads are few
+            float sc[GRP][2][GH];
 #pragma unroll
-            for (int sp = 0; sp < SPW; ++sp) {
-                const int rr0 = (warp * SPW + sp) * kSub;  // sub-tile's first row within the stage
-                float4 kv[2][KF4];
-                float4 vv[VJ];
+            for (int sp = 0; sp < GRP; ++sp) {
+                const int rr0 = (warp * SPW + g0 + sp) * kSub;  // sub-tile's first row within the stage
 #pragma unroll
                 for (int it2 = 0; it2 < 2; ++it2) {
                     const int rr = rr0 + 4 * it2 + r4;
+                    float4 kv[KF4];
 #pragma unroll
-                    for (int i = 0; i < KF4; ++i)
-                        kv[it2][i] = ld_row4<HDKV, T>(Kq + rr * HDKV * EB, Ksc + rr * 16, sc, sub + 8 * i);
-                }
+                    for (int i = 0; i < KF4; ++i) kv[i] = ld_row4_raw<HDKV, T>(Kq + rr * HDKV * EB, sub + 8 * i);
+                    float ks[Q ? KF4 : 1];
+                    if constexpr (Q) ld_scales<HDKV>(Ksc + rr * 16, sc0, ks);
 #pragma unroll
-                for (int jv = 0; jv < VJ; ++jv) {
-                    const int rr = rr0 + vrow + VRP * jv;
-                    const int row = row0 + rr;
-                    vv[jv] = row < t.r_end ? ld_row4<HDKV, T>(Vq + rr * HDKV * EB, Vsc + rr * 16, sc, vcol)
-                                           : make_float4(0.f, 0.f, 0.f, 0.f);  // past the run: anything
-                }
-                float pr[2][GH];
-#pragma unroll
-                for (int hh = 0; hh < GH; ++hh) {
-                    float sc[2];
-#pragma unroll
-                    for (int it2 = 0; it2 < 2; ++it2) {
+                    for (int hh = 0; hh < GH; ++hh) {
                         float d = 0.0f;
 #pragma unroll
                         for (int i = 0; i < KF4; ++i) {
-                            d = fmaf(qr[hh][i].x, kv[it2][i].x, d);
-                            d = fmaf(qr[hh][i].y, kv[it2][i].y, d);
-                            d = fmaf(qr[hh][i].z, kv[it2][i].z, d);
-                            d = fmaf(qr[hh][i].w, kv[it2][i].w, d);
+                            float b = Q ? 0.0f : d;
+                            b = fmaf(qr[hh][i].x, kv[i].x, b);
+                            b = fmaf(qr[hh][i].y, kv[i].y, b);
+                            b = fmaf(qr[hh][i].z, kv[i].z, b);
+                            b = fmaf(qr[hh][i].w, kv[i].w, b);
+                            if constexpr (Q) d = fmaf(ks[i], b, d);
+                            else d = b;
                         }
                         d += __shfl_xor_sync(0xffffffffu, d, 1);
                         d += __shfl_xor_sync(0xffffffffu, d, 2);
                         d += __shfl_xor_sync(0xffffffffu, d, 4);
-                        sc[it2] = (row0 + rr0 + 4 * it2 + r4) < t.r_end ? d * sl : -INFINITY;
+                        sc[sp][it2][hh] = (row0 + rr) < t.r_end ? d * sl : -INFINITY;
                     }
-                    float mx = fmaxf(sc[0], sc[1]);
-                    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
-                    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
-                    const float m_new = fmaxf(m[hh], mx);
-                    // a sub-tile wholly past the run leaves the state untouched
-                    const bool none = (m_new == -INFINITY);
-                    const float corr = none ? 1.0f : ex2_approx(m[hh] - m_new);
-                    pr[0][hh] = none ? 0.0f : ex2_approx(sc[0] - m_new);
-                    pr[1][hh] = none ? 0.0f : ex2_approx(sc[1] - m_new);
-                    float ps = pr[0][hh] + pr[1][hh];
-                    ps += __shfl_xor_sync(0xffffffffu, ps, 8);
-                    ps += __shfl_xor_sync(0xffffffffu, ps, 16);
-                    l[hh] = fmaf(l[hh], corr, ps);
-                    acc[hh] = f4scale(acc[hh], corr);
-                    m[hh] = m_new;
                 }
+            }
+#pragma unroll
+            for (int hh = 0; hh < GH; ++hh) {
+                float mx = sc[0][0][hh];
+#pragma unroll
+                for (int sp = 0; sp < GRP; ++sp)
+#pragma unroll
+                    for (int it2 = 0; it2 < 2; ++it2) mx = fmaxf(mx, sc[sp][it2][hh]);
+                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+                const float m_new = fmaxf(m[hh], mx);
+                // rows wholly past the run leave the state untouched
+                const bool none = (m_new == -INFINITY);
+                const float corr = none ? 1.0f : ex2_approx(m[hh] - m_new);
+                float ps = 0.0f;
+#pragma unroll
+                for (int sp = 0; sp < GRP; ++sp)
+#pragma unroll
+                    for (int it2 = 0; it2 < 2; ++it2) {
+                        const float pv = none ? 0.0f : ex2_approx(sc[sp][it2][hh] - m_new);
+                        sc[sp][it2][hh] = pv;  // from here on: the row's weight
+                        ps += pv;
+                    }
+                ps += __shfl_xor_sync(0xffffffffu, ps, 8);
+                ps += __shfl_xor_sync(0xffffffffu, ps, 16);
+                l[hh] = fmaf(l[hh], corr, ps);
+#pragma unroll
+                for (int c = 0; c < NACC; ++c) accs[c][hh] = f4scale(accs[c][hh], corr);
+                m[hh] = m_new;
+            }
+#pragma unroll
+            for (int sp = 0; sp < GRP; ++sp) {
+                const int rr0 = (warp * SPW + g0 + sp) * kSub;
 #pragma unroll
                 for (int jv = 0; jv < VJ; ++jv) {
                     const int rl = vrow + VRP * jv;  // row within the sub-tile, 0..7
+                    const int rr = rr0 + rl;
+                    const bool in_run = row0 + rr < t.r_end;
+                    // past the run: anything finite (its weight is 0)
+                    const float4 v = in_run ? ld_row4_raw<HDKV, T>(Vq + rr * HDKV * EB, vcol)
+                                            : make_float4(0.f, 0.f, 0.f, 0.f);
+                    float vs = 1.0f;
+                    if constexpr (Q)
+                        vs = __half2float(reinterpret_cast<const __half *>(Vsc + rr * 16)[sc0 + (vcol >> 3)]);
                     const int it2 = (VRP * jv) / 4;  // the same for every lane of the pass
                     const int src = (rl & 3) * 8;
 #pragma unroll
                     for (int hh = 0; hh < GH; ++hh) {
-                        const float w = __shfl_sync(0xffffffffu, it2 ? pr[1][hh] : pr[0][hh], src);
-                        acc[hh].x = fmaf(w, vv[jv].x, acc[hh].x);
-                        acc[hh].y = fmaf(w, vv[jv].y, acc[hh].y);
-                        acc[hh].z = fmaf(w, vv[jv].z, acc[hh].z);
-                        acc[hh].w = fmaf(w, vv[jv].w, acc[hh].w);
+                        float w = __shfl_sync(0xffffffffu, sc[sp][it2][hh], src);
+                        if constexpr (Q) w *= vs;
+                        float4 &ac = accs[((g0 + sp) * VJ + jv) % NACC][hh];
+                        ac.x = fmaf(w, v.x, ac.x);
+                        ac.y = fmaf(w, v.y, ac.y);
+                        ac.z = fmaf(w, v.z, ac.z);
+                        ac.w = fmaf(w, v.w, ac.w);
                     }
                 }
             }
+            }  // sub-tile group
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[slot]);
         }
 
         // ------------------------------------------------------------ end of the unit
         cons_sync(&cons_bar, cphase, abort_flag, a.err);  // the previous unit's scratch readers are done
+        float4 acc[GH];
+#pragma unroll
+        for (int hh = 0; hh < GH; ++hh) {
+            acc[hh] = accs[0][hh];
+#pragma unroll
+            for (int c = 1; c < NACC; ++c)
+                acc[hh] = make_float4(acc[hh].x + accs[c][hh].x, acc[hh].y + accs[c][hh].y,
+                                      acc[hh].z + accs[c][hh].z, acc[hh].w + accs[c][hh].w);
+        }
 #pragma unroll
         for (int hh = 0; hh < GH; ++hh) {
 #pragma unroll
