@@ -134,25 +134,32 @@ __device__ __forceinline__ float4 ld_row4(const unsigned char *qrow, const unsig
 template <int HDKV, typename T>
 __device__ __forceinline__ float4 ld_row4_raw(const unsigned char *qrow, int i4) {
     if constexpr (Elem<T>::q8) {
-        return deq4(reinterpret_cast<const uint32_t *>(qrow)[i4], 1.0f);
+        return int8x4_to_float4(reinterpret_cast<const uint32_t *>(qrow)[i4]);
     } else {
         return ld4(reinterpret_cast<const T *>(qrow), i4);
     }
 }
 
-// Q8_0: the scales of this kv head's HDKV/32 blocks in a row's scale slice (srow), as floats.
+// Q8_0: the scales of this kv head's HDKV/32 blocks in a row's scale slice (srow), as floats,
+// in the lane's rotated block order: s[i] is block (i + rot) mod HDKV/32.
 template <int HDKV>
-__device__ __forceinline__ void ld_scales(const unsigned char *srow, int sc, float (&s)[HDKV / 32]) {
+__device__ __forceinline__ void ld_scales(const unsigned char *srow, int sc, int rot, float (&s)[HDKV / 32]) {
     if constexpr (HDKV == 128) {
         const uint2 u = *reinterpret_cast<const uint2 *>(srow + 2 * sc);
-        const float2 a = __half22float2(*reinterpret_cast<const __half2 *>(&u.x));
-        const float2 b = __half22float2(*reinterpret_cast<const __half2 *>(&u.y));
+        // rotate the four halves right by rot places (a 64-bit rotation by 16 * rot bits)
+        const uint32_t x = (rot & 2) ? u.y : u.x, y = (rot & 2) ? u.x : u.y;
+        const int sh = (rot & 1) * 16;
+        const uint32_t lo = __funnelshift_r(x, y, sh), hi = __funnelshift_r(y, x, sh);
+        const float2 a = __half22float2(*reinterpret_cast<const __half2 *>(&lo));
+        const float2 b = __half22float2(*reinterpret_cast<const __half2 *>(&hi));
         s[0] = a.x;
         s[1] = a.y;
         s[2] = b.x;
         s[3] = b.y;
     } else {
-        const float2 a = __half22float2(*reinterpret_cast<const __half2 *>(srow + 2 * sc));
+        uint32_t u = *reinterpret_cast<const uint32_t *>(srow + 2 * sc);
+        u = __funnelshift_r(u, u, (rot & 1) * 16);
+        const float2 a = __half22float2(*reinterpret_cast<const __half2 *>(&u));
         s[0] = a.x;
         s[1] = a.y;
     }
@@ -191,7 +198,8 @@ struct KParams {
 };
 
 __device__ __forceinline__ float4 f4scale(float4 v, float s) {
-    return make_float4(v.x * s, v.y * s, v.z * s, v.w * s);
+    const float2 ss = make_float2(s, s);
+    return cat2(mul2(lo2(v), ss), mul2(hi2(v), ss));
 }
 
 __device__ __forceinline__ void rope_rot(float &x0, float &x1, float sn, float cs) {
@@ -512,6 +520,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool early = n_units <= static_cast<int>(gridDim.x);
     bool released = false;
     const int r4 = lane >> 3, sub = lane & 7;
+    // The four rows of a K pass (r4) take their 16-byte blocks in rotated order, block
+    // (i + rot) mod KF4 at step i, so narrow rows (binary16, Q8_0) land in different banks.
+    const int rot = r4 & (KF4 - 1);
     const int vrow = lane / VL, vcol = lane % VL;
     const float sl = a.scale_log2;
     uint32_t cphase = 0;
@@ -639,6 +650,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                 released = true;
             }
         }
+        // q's blocks in the lane's rotated order (the lanes that write q back have rot = 0)
+#pragma unroll
+        for (int hh = 0; hh < GH; ++hh) {
+            float4 t0[KF4];
+#pragma unroll
+            for (int i = 0; i < KF4; ++i) t0[i] = qr[hh][i];
+#pragma unroll
+            for (int i = 0; i < KF4; ++i) {
+                float4 v = t0[i];
+#pragma unroll
+                for (int r = 1; r < KF4; ++r)
+                    if (rot == r) v = t0[(i + r) & (KF4 - 1)];
+                qr[hh][i] = v;
+            }
+        }
         float m[GH], l[GH];
         float4 accs[NACC][GH];  // V rows alternate between NACC accumulators (shorter FMA chains)
 #pragma unroll
@@ -707,22 +733,26 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const int rr = rr0 + 4 * it2 + r4;
                     float4 kv[KF4];
 #pragma unroll
-                    for (int i = 0; i < KF4; ++i) kv[i] = ld_row4_raw<HDKV, T>(Kq + rr * HDKV * EB, sub + 8 * i);
+                    for (int i = 0; i < KF4; ++i)
+                        kv[i] = ld_row4_raw<HDKV, T>(Kq + rr * HDKV * EB, sub + 8 * ((i + rot) & (KF4 - 1)));
                     float ks[Q ? KF4 : 1];
-                    if constexpr (Q) ld_scales<HDKV>(Ksc + rr * 16, sc0, ks);
+                    if constexpr (Q) ld_scales<HDKV>(Ksc + rr * 16, sc0, rot, ks);
 #pragma unroll
                     for (int hh = 0; hh < GH; ++hh) {
-                        float d = 0.0f;
+                        // packed pairs: even and odd elements summed apart, added at the end
+                        float2 d2 = make_float2(0.0f, 0.0f);
 #pragma unroll
                         for (int i = 0; i < KF4; ++i) {
-                            float b = Q ? 0.0f : d;
-                            b = fmaf(qr[hh][i].x, kv[i].x, b);
-                            b = fmaf(qr[hh][i].y, kv[i].y, b);
-                            b = fmaf(qr[hh][i].z, kv[i].z, b);
-                            b = fmaf(qr[hh][i].w, kv[i].w, b);
-                            if constexpr (Q) d = fmaf(ks[i], b, d);
-                            else d = b;
+                            if constexpr (Q) {
+                                float2 b2 = mul2(lo2(qr[hh][i]), lo2(kv[i]));
+                                b2 = fma2(hi2(qr[hh][i]), hi2(kv[i]), b2);
+                                d2 = fma2(make_float2(ks[i], ks[i]), b2, d2);
+                            } else {
+                                d2 = fma2(lo2(qr[hh][i]), lo2(kv[i]), d2);
+                                d2 = fma2(hi2(qr[hh][i]), hi2(kv[i]), d2);
+                            }
                         }
+                        float d = d2.x + d2.y;
                         d += __shfl_xor_sync(0xffffffffu, d, 1);
                         d += __shfl_xor_sync(0xffffffffu, d, 2);
                         d += __shfl_xor_sync(0xffffffffu, d, 4);
@@ -780,10 +810,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                         float w = __shfl_sync(0xffffffffu, sc[sp][it2][hh], src);
                         if constexpr (Q) w *= vs;
                         float4 &ac = accs[((g0 + sp) * VJ + jv) % NACC][hh];
-                        ac.x = fmaf(w, v.x, ac.x);
-                        ac.y = fmaf(w, v.y, ac.y);
-                        ac.z = fmaf(w, v.z, ac.z);
-                        ac.w = fmaf(w, v.w, ac.w);
+                        const float2 w2 = make_float2(w, w);
+                        ac = cat2(fma2(w2, lo2(v), lo2(ac)), fma2(w2, hi2(v), hi2(ac)));
                     }
                 }
             }

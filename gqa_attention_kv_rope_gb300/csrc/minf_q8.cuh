@@ -11,19 +11,29 @@
 #include <cuda_fp16.h>
 #include <stdint.h>
 
+#include "minf_common.cuh"
+
 namespace minf {
 
 struct Q8 {};  // storage tag: Q8_0 rows
 
-// Four Q8_0 values: quants q (4 bytes, element order), block scale s.  Each byte is placed in
-// the mantissa of 2^23 (offset by 128) and the offset subtracted: an exact int8 -> float.
-__device__ __forceinline__ float4 deq4(uint32_t q, float s) {
+// Four Q8_0 quants q (4 bytes, element order) as exact floats: each byte is placed in the
+// mantissa of 2^23 (offset by 128) and the offset subtracted.
+__device__ __forceinline__ float4 int8x4_to_float4(uint32_t q) {
     const uint32_t u = q ^ 0x80808080u;
-    const float a = __int_as_float(__byte_perm(u, 0x4B000000u, 0x7440)) - 8388736.0f;
-    const float b = __int_as_float(__byte_perm(u, 0x4B000000u, 0x7441)) - 8388736.0f;
-    const float c = __int_as_float(__byte_perm(u, 0x4B000000u, 0x7442)) - 8388736.0f;
-    const float d = __int_as_float(__byte_perm(u, 0x4B000000u, 0x7443)) - 8388736.0f;
-    return make_float4(s * a, s * b, s * c, s * d);
+    const float2 off = make_float2(-8388736.0f, -8388736.0f);
+    const float2 ab = add2(make_float2(__int_as_float(__byte_perm(u, 0x4B000000u, 0x7440)),
+                                       __int_as_float(__byte_perm(u, 0x4B000000u, 0x7441))), off);
+    const float2 cd = add2(make_float2(__int_as_float(__byte_perm(u, 0x4B000000u, 0x7442)),
+                                       __int_as_float(__byte_perm(u, 0x4B000000u, 0x7443))), off);
+    return cat2(ab, cd);
+}
+
+// Four Q8_0 values: quants q, block scale s.
+__device__ __forceinline__ float4 deq4(uint32_t q, float s) {
+    const float4 x = int8x4_to_float4(q);
+    const float2 ss = make_float2(s, s);
+    return cat2(mul2(lo2(x), ss), mul2(hi2(x), ss));
 }
 
 // Quantization of one 32-value block held as four values by each of eight consecutive lanes
