@@ -311,6 +311,88 @@ __device__ __forceinline__ void cons_sync(unsigned long long *bar, uint32_t &pha
     __syncwarp();
 }
 
+// The fused step's new row, by the lanes of one warp with r4 == 0 (sub = lane): rotates k
+// (sin/cos from rope_angles) and writes it back, stores the K/V row at pos -- through the
+// block table when paged, a missing block flagged -- and stages it in shared memory for the
+// tile patch.  pnew < 0: the row is past the region (rotated and written back only).
+template <int HDKV, typename T>
+__device__ __forceinline__ void append_new_row(const KParams &a, const Unit &t, int hk, int pnew,
+                                               const float (&sn)[HDKV / 16], const float (&cs)[HDKV / 16],
+                                               int sub, float *sm_knew, float *sm_vnew) {
+    constexpr int KF4 = HDKV / 32;
+    constexpr bool Q = Elem<T>::q8;
+    const int W = a.nk * HDKV;
+    float4 *kh = reinterpret_cast<float4 *>(a.k_io + (static_cast<size_t>(t.s) * a.nk + hk) * HDKV);
+    const float4 *vh = reinterpret_cast<const float4 *>(a.v_new + static_cast<size_t>(t.s) * W + hk * HDKV);
+    float4 kx[KF4], vx[KF4];
+#pragma unroll
+    for (int i = 0; i < KF4; ++i) {
+        kx[i] = kh[sub + 8 * i];
+        vx[i] = vh[sub + 8 * i];
+    }
+    rope_lane<KF4>(kx, sn, cs, a.style);
+#pragma unroll
+    for (int i = 0; i < KF4; ++i) kh[sub + 8 * i] = kx[i];
+    if (pnew >= 0) {
+        long long prow = t.base + t.p;
+        if (a.table) {  // the row's block, through the table
+            const int b = __ldg(a.table + static_cast<size_t>(t.s) * a.max_blocks + t.p / a.block_rows);
+            prow = static_cast<long long>(b) * a.block_rows + t.p % a.block_rows;
+            if (b < 0 || prow >= a.pool_rows) {
+                prow = -1;
+                if (sub == 0) flag_error(a.err, MINF_ERRBIT_BLOCK);
+            }
+        }
+        if constexpr (Q) {
+            // quantize the row's blocks (block i is element group i of lanes 0-7);
+            // staged as bytes (quants, then scales) for the same lanes' patch
+            unsigned char *Kg = static_cast<unsigned char *>(a.k_reg) + prow * a.row_bytes;
+            unsigned char *Vg = static_cast<unsigned char *>(a.v_reg) + prow * a.row_bytes;
+#pragma unroll
+            for (int i = 0; i < KF4; ++i) {
+                float dk, dv;
+                const uint32_t qk = quant4(kx[i], 0xffu, dk), qv = quant4(vx[i], 0xffu, dv);
+                reinterpret_cast<uint32_t *>(sm_knew)[sub + 8 * i] = qk;
+                reinterpret_cast<uint32_t *>(sm_vnew)[sub + 8 * i] = qv;
+                const __half hk16 = __float2half_rn(dk), hv16 = __float2half_rn(dv);
+                if (sub == 0) {
+                    reinterpret_cast<__half *>(reinterpret_cast<unsigned char *>(sm_knew) + HDKV)[i] = hk16;
+                    reinterpret_cast<__half *>(reinterpret_cast<unsigned char *>(sm_vnew) + HDKV)[i] = hv16;
+                }
+                if (prow >= 0) {
+                    reinterpret_cast<uint32_t *>(Kg + hk * HDKV)[sub + 8 * i] = qk;
+                    reinterpret_cast<uint32_t *>(Vg + hk * HDKV)[sub + 8 * i] = qv;
+                    if (sub == 0) {
+                        reinterpret_cast<__half *>(Kg + W)[hk * (HDKV / 32) + i] = hk16;
+                        reinterpret_cast<__half *>(Vg + W)[hk * (HDKV / 32) + i] = hv16;
+                    }
+                }
+            }
+            if (prow >= 0 && hk == 0 && sub == 0)  // the row's zero padding after its scales
+                for (long long b = W + W / 16; b < a.row_bytes; b += 2) {
+                    *reinterpret_cast<uint16_t *>(Kg + b) = 0;
+                    *reinterpret_cast<uint16_t *>(Vg + b) = 0;
+                }
+        } else {
+#pragma unroll
+            for (int i = 0; i < KF4; ++i) {
+                // staged for the same lanes, which patch the row's stage when it arrives
+                reinterpret_cast<float4 *>(sm_knew)[sub + 8 * i] = kx[i];
+                reinterpret_cast<float4 *>(sm_vnew)[sub + 8 * i] = vx[i];
+            }
+            if (prow >= 0) {
+                T *Kg = static_cast<T *>(a.k_reg) + prow * W + hk * HDKV;
+                T *Vg = static_cast<T *>(a.v_reg) + prow * W + hk * HDKV;
+#pragma unroll
+                for (int i = 0; i < KF4; ++i) {
+                    st4(Kg, sub + 8 * i, kx[i]);
+                    st4(Vg, sub + 8 * i, vx[i]);
+                }
+            }
+        }
+    }
+}
+
 template <int HDKV, int GH, bool kFused, typename T>
 __global__ void __launch_bounds__(kThreads, 1)
     decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
@@ -333,7 +415,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     extern __shared__ unsigned char smem_raw[];
     // 1024-aligned ring, derived from the shared array itself so loads stay in the shared space
     unsigned char *ring = smem_raw + ((1024u - (su32(smem_raw) & 1023u)) & 1023u);
-    __shared__ unsigned long long full[kNST], empty[kNST], meta_full[kNST], cons_bar;
+    __shared__ unsigned long long full[kNST], empty[kNST], meta_full[kNST], cons_bar, knew_bar;
     __shared__ int2 sm_meta[kNST];  // (unit, stage) of each ring slot; unit < 0 ends the stream
     __shared__ int sm_order[kMaxSort];
     __shared__ float sm_m[kNW][GH], sm_l[kNW][GH];
@@ -356,6 +438,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&meta_full[i], 1);
         }
         mbar_init(&cons_bar, kNW);
+        mbar_init(&knew_bar, 1);
         sm_abort = 0;
         mbar_init_fence();
     }
@@ -375,12 +458,32 @@ __global__ void __launch_bounds__(kThreads, 1)
         order = sm_order;
     }
     __syncthreads();
+    // When every unit is a first unit (one per CTA), the CTA whose unit ends at the window's
+    // last row has its utility warp append the new row, beside the consumers' start; the
+    // consumers patch it into its tile from shared memory once knew_bar says it is staged.
+    const bool early = n_units <= static_cast<int>(gridDim.x);
+    const Unit t0 = unit_of<R>(a, blockIdx.x, order);  // positions: not written by a preceding kernel
+    const bool util_append = kFused && early && unit_active(t0) && t0.r_end == t0.L;
 
     if (warp == kUtility) {
         // ---------------------------------------------------------------- utility warp
+        gdc_wait();
+        if (util_append) {
+            // the rotated k written back, the K/V row stored and staged, then -- the row in
+            // memory -- the dependent launch released for this CTA
+            const int hk = t0.y / a.groups;
+            const int pnew = t0.p < t0.cap_s ? t0.p : -1;
+            float sn[2 * KF4], cs[2 * KF4];
+            rope_angles<KF4>(sn, cs, static_cast<float>(t0.p), a.tab, a.style, lane & 7, lane >> 3);
+            if (lane < 8) append_new_row<HDKV, T>(a, t0, hk, pnew, sn, cs, lane, sm_knew, sm_vnew);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&knew_bar);
+            if (pnew >= 0) __threadfence();
+            __syncwarp();
+            if (lane == 0) gdc_launch_dependents();
+        }
         // RMSNorm rows ("11 . Attention, vec ops, and the KV cache", §3.2.1), spread over the
         // CTAs; h is produced upstream, so it is read only after the dependency wait.
-        gdc_wait();
         for (int s = blockIdx.x; kFused && s < a.n_seq; s += gridDim.x) {
             const float *hr = a.h + static_cast<size_t>(s) * a.n_embd;
             float *yr = a.xn + static_cast<size_t>(s) * a.n_embd;
@@ -515,9 +618,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // -------------------------------------------------------------------- consumers
     // A dependent launch may start streaming cached rows before its own wait, so release it only
     // once every row this CTA appends is in memory.  The run that ends at the window's last row
-    // appends; when every unit is a first unit, a CTA releases right after its append (or at
-    // once), otherwise when it is done.
-    const bool early = n_units <= static_cast<int>(gridDim.x);
+    // appends; when every unit is a first unit, a CTA releases at once, or -- when it appends --
+    // its utility warp does right after the append; otherwise a CTA releases when it is done.
     bool released = false;
     const int r4 = lane >> 3, sub = lane & 7;
     // The four rows of a K pass (r4) take their 16-byte blocks in rotated order, block
@@ -527,13 +629,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float sl = a.scale_log2;
     uint32_t cphase = 0;
     uint32_t it = 0;  // ring stage counter, in step with the producer's
-    // The first unit is this CTA's own and needs no word from the producer; its position is
-    // read before the dependency wait (no preceding kernel writes positions).
-    Unit t = unit_of<R>(a, blockIdx.x, order);
+    // The first unit is this CTA's own and needs no word from the producer.
+    Unit t = t0;
     bool have = unit_active(t);
+    bool first_unit = true;
     gdc_wait();
-    if (early && !(kFused && have && t.r_end == t.L)) {
-        gdc_launch_dependents();  // this CTA appends no row
+    if (early) {
+        if (!util_append) gdc_launch_dependents();  // this CTA appends no row
         released = true;
     }
     while (true) {
@@ -563,92 +665,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         // memory, in place of what its tile copy read (no other unit reads k).
         const bool k_writer = kFused && t.r_end == t.L;
         const int pnew = k_writer && t.p < t.cap_s ? t.p : -1;
+        const bool util_unit = util_append && first_unit;  // appended by the utility warp
+        first_unit = false;
         if (kFused) {
             float sn[2 * KF4], cs[2 * KF4];
             rope_angles<KF4>(sn, cs, static_cast<float>(t.p), a.tab, a.style, sub, r4);
 #pragma unroll
             for (int hh = 0; hh < GH; ++hh) rope_lane<KF4>(qr[hh], sn, cs, a.style);
-            if (k_writer && warp == 0 && r4 == 0) {
-                float4 *kh = reinterpret_cast<float4 *>(a.k_io + (static_cast<size_t>(t.s) * a.nk + hk) * HDKV);
-                const float4 *vh = reinterpret_cast<const float4 *>(a.v_new + static_cast<size_t>(t.s) * W + hk * HDKV);
-                float4 kx[KF4], vx[KF4];
-#pragma unroll
-                for (int i = 0; i < KF4; ++i) {
-                    kx[i] = kh[sub + 8 * i];
-                    vx[i] = vh[sub + 8 * i];
-                }
-                rope_lane<KF4>(kx, sn, cs, a.style);
-#pragma unroll
-                for (int i = 0; i < KF4; ++i) kh[sub + 8 * i] = kx[i];
-                if (pnew >= 0) {
-                    long long prow = t.base + t.p;
-                    if (a.table) {  // the row's block, through the table
-                        const int b = __ldg(a.table + static_cast<size_t>(t.s) * a.max_blocks + t.p / a.block_rows);
-                        prow = static_cast<long long>(b) * a.block_rows + t.p % a.block_rows;
-                        if (b < 0 || prow >= a.pool_rows) {
-                            prow = -1;
-                            if (sub == 0) flag_error(a.err, MINF_ERRBIT_BLOCK);
-                        }
-                    }
-                    if constexpr (Q) {
-                        // quantize the row's blocks (block i is element group i of lanes 0-7);
-                        // staged as bytes (quants, then scales) for the same lanes' patch
-                        unsigned char *Kg = static_cast<unsigned char *>(a.k_reg) + prow * a.row_bytes;
-                        unsigned char *Vg = static_cast<unsigned char *>(a.v_reg) + prow * a.row_bytes;
-#pragma unroll
-                        for (int i = 0; i < KF4; ++i) {
-                            float dk, dv;
-                            const uint32_t qk = quant4(kx[i], 0xffu, dk), qv = quant4(vx[i], 0xffu, dv);
-                            reinterpret_cast<uint32_t *>(sm_knew)[sub + 8 * i] = qk;
-                            reinterpret_cast<uint32_t *>(sm_vnew)[sub + 8 * i] = qv;
-                            const __half hk16 = __float2half_rn(dk), hv16 = __float2half_rn(dv);
-                            if (sub == 0) {
-                                reinterpret_cast<__half *>(reinterpret_cast<unsigned char *>(sm_knew) + HDKV)[i] = hk16;
-                                reinterpret_cast<__half *>(reinterpret_cast<unsigned char *>(sm_vnew) + HDKV)[i] = hv16;
-                            }
-                            if (prow >= 0) {
-                                reinterpret_cast<uint32_t *>(Kg + hk * HDKV)[sub + 8 * i] = qk;
-                                reinterpret_cast<uint32_t *>(Vg + hk * HDKV)[sub + 8 * i] = qv;
-                                if (sub == 0) {
-                                    reinterpret_cast<__half *>(Kg + W)[hk * (HDKV / 32) + i] = hk16;
-                                    reinterpret_cast<__half *>(Vg + W)[hk * (HDKV / 32) + i] = hv16;
-                                }
-                            }
-                        }
-                        if (prow >= 0 && hk == 0 && sub == 0)  // the row's zero padding after its scales
-                            for (long long b = W + W / 16; b < a.row_bytes; b += 2) {
-                                *reinterpret_cast<uint16_t *>(Kg + b) = 0;
-                                *reinterpret_cast<uint16_t *>(Vg + b) = 0;
-                            }
-                    } else {
-#pragma unroll
-                        for (int i = 0; i < KF4; ++i) {
-                            // staged for the same lanes, which patch the row's stage when it arrives
-                            reinterpret_cast<float4 *>(sm_knew)[sub + 8 * i] = kx[i];
-                            reinterpret_cast<float4 *>(sm_vnew)[sub + 8 * i] = vx[i];
-                        }
-                        if (prow >= 0) {
-                            T *Kg = static_cast<T *>(a.k_reg) + prow * W + hk * HDKV;
-                            T *Vg = static_cast<T *>(a.v_reg) + prow * W + hk * HDKV;
-#pragma unroll
-                            for (int i = 0; i < KF4; ++i) {
-                                st4(Kg, sub + 8 * i, kx[i]);
-                                st4(Vg, sub + 8 * i, vx[i]);
-                            }
-                        }
-                    }
-                }
-            }
-            if (early && !released) {  // this first unit is the appending one
-                // the appended row is in memory before the dependent launch is released; one
-                // thread's trigger releases the CTA, so the warp that wrote the row triggers
-                if (warp == 0) {
-                    if (pnew >= 0) __threadfence();
-                    __syncwarp();
-                    if (lane == 0) gdc_launch_dependents();
-                }
-                released = true;
-            }
+            if (k_writer && !util_unit && warp == 0 && r4 == 0)
+                append_new_row<HDKV, T>(a, t, hk, pnew, sn, cs, sub, sm_knew, sm_vnew);
         }
         // q's blocks in the lane's rotated order (the lanes that write q back have rot = 0)
 #pragma unroll
@@ -689,6 +714,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // the tile may hold the row as it was before this launch appended it: the lanes
                 // that staged the new row put it in its place (and hand the slot back to the
                 // async proxy in order)
+                if (util_unit && warp == 0) mbar_wait(&knew_bar, 0, abort_flag, a.err);
                 if (warp == 0 && r4 == 0) {
                     const int rn = pnew - row0;
                     if constexpr (Q) {
