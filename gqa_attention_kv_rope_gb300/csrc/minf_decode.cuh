@@ -197,6 +197,13 @@ struct KParams {
     RopeTable tab;         // angular speeds for hd (== hd_kv on the fused path)
 };
 
+// Requests the 128-byte lines [p, p + bytes) into L2, one line per lane (a hint: the load that
+// follows may come after a dependency wait, when the data is current in L2 either way).
+__device__ __forceinline__ void prefetch_l2(const void *p, int bytes, int lane) {
+    for (int off = lane * 128; off < bytes; off += 32 * 128)
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(static_cast<const char *>(p) + off));
+}
+
 __device__ __forceinline__ float4 f4scale(float4 v, float s) {
     const float2 ss = make_float2(s, s);
     return cat2(mul2(lo2(v), ss), mul2(hi2(v), ss));
@@ -467,6 +474,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (warp == kUtility) {
         // ---------------------------------------------------------------- utility warp
+        if (kFused && util_append) {  // the rows it will read after the wait, into L2 now
+            const int hk = t0.y / a.groups;
+            prefetch_l2(a.k_io + (static_cast<size_t>(t0.s) * a.nk + hk) * HDKV, HDKV * 4, lane);
+            prefetch_l2(a.v_new + static_cast<size_t>(t0.s) * W + hk * HDKV, HDKV * 4, lane);
+        }
+        if (kFused && static_cast<int>(blockIdx.x) < a.n_seq)
+            prefetch_l2(a.h + static_cast<size_t>(blockIdx.x) * a.n_embd, a.n_embd * 4, lane);
         gdc_wait();
         if (util_append) {
             // the rotated k written back, the K/V row stored and staged, then -- the row in
@@ -633,6 +647,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     Unit t = t0;
     bool have = unit_active(t);
     bool first_unit = true;
+    if (have && warp < GH) {  // this unit's q rows, into L2 before the wait
+        const int h0 = (t.y / a.groups) * (a.nh / a.nk) + (t.y % a.groups) * GH;
+        prefetch_l2(a.q + (static_cast<size_t>(t.s) * a.nh + h0 + warp) * a.hd, HDKV * 4, lane);
+    }
     gdc_wait();
     if (early) {
         if (!util_append) gdc_launch_dependents();  // this CTA appends no row
