@@ -53,13 +53,16 @@ constexpr uint32_t kOCol = 128;
 // Operands are held as hi + lo TF32 pairs (x = hi + lo to about 2^-22 relative): each
 // product is formed from three tensor-core MMAs, hi*hi + hi*lo + lo*hi, so the TF32 inputs
 // of the tensor core cost no accuracy beyond fp32 accumulation.
+// K and V^T tiles are double-buffered where shared memory allows (hd_kv 64): key tile j lives
+// in buffer j % NB.
 template <int HDKV>
 struct Smem {
-    float qh[HDKV / 32][BM * 32], ql[HDKV / 32][BM * 32];    // Q: 32-column SW128 slabs
-    float kh[HDKV / 32][BN * 32], kl[HDKV / 32][BN * 32];    // K tile (TMA lands in kh)
-    float ph[BN / 32][BM * 32], pl[BN / 32][BM * 32];        // P: keys along K
-    float vh[BN / 32][HDKV * 32], vl[BN / 32][HDKV * 32];    // V^T: keys along K
-    unsigned long long bar_q, bar_k, bar_kv, bar_s, bar_p, bar_o;
+    static constexpr int NB = HDKV == 64 ? 2 : 1;
+    float qh[HDKV / 32][BM * 32], ql[HDKV / 32][BM * 32];            // Q: 32-column SW128 slabs
+    float kh[NB][HDKV / 32][BN * 32], kl[NB][HDKV / 32][BN * 32];    // K tiles (TMA lands in kh)
+    float ph[BN / 32][BM * 32], pl[BN / 32][BM * 32];                // P: keys along K
+    float vh[NB][BN / 32][HDKV * 32], vl[NB][BN / 32][HDKV * 32];    // V^T: keys along K
+    unsigned long long bar_q, bar_k[NB], bar_kk, bar_vv, bar_s, bar_p, bar_o;
     uint32_t tmem_base;
     int abort_flag;
     int lmax;
@@ -201,8 +204,9 @@ __global__ void __launch_bounds__(kThreadsP, 1)
 
     if (tid == 0) {
         mbar_init(&sm.bar_q, 1);
-        mbar_init(&sm.bar_k, 1);
-        mbar_init(&sm.bar_kv, kSoftThreads);
+        for (int b = 0; b < Smem<HDKV>::NB; ++b) mbar_init(&sm.bar_k[b], 1);
+        mbar_init(&sm.bar_kk, kSoftThreads);
+        mbar_init(&sm.bar_vv, kSoftThreads);
         mbar_init(&sm.bar_s, 1);
         mbar_init(&sm.bar_p, kSoftThreads);
         mbar_init(&sm.bar_o, 1);
@@ -248,50 +252,54 @@ __global__ void __launch_bounds__(kThreadsP, 1)
     gdc_wait();
     constexpr uint32_t kQBytes = BM * HDKV * 4, kKBytes = BN * HDKV * 4;
 
+    constexpr int NB = Smem<HDKV>::NB;
     if (warp == kProducerWarp) {
         if (lane == 0 && n_tiles > 0) {
             mbar_expect_tx(&sm.bar_q, kQBytes);
 #pragma unroll
             for (int c = 0; c < HDKV / 32; ++c) tma_load_2d(sm.qh[c], &tm_q, h * a.hd + 32 * c, t0, &sm.bar_q);
-            if (kTmaK) {
-                mbar_expect_tx(&sm.bar_k, kKBytes);
+            auto load_k = [&](int j) {  // key tile j -> buffer j % NB
+                const int b = j % NB;
+                mbar_expect_tx(&sm.bar_k[b], kKBytes);
 #pragma unroll
                 for (int c = 0; c < HDKV / 32; ++c)
-                    tma_load_2d(sm.kh[c], &tm_k, hk * HDKV + 32 * c, tile0 * BN, &sm.bar_k);
-            }
+                    tma_load_2d(sm.kh[b][c], &tm_k, hk * HDKV + 32 * c, (tile0 + j) * BN, &sm.bar_k[b]);
+            };
+            if (kTmaK)
+                for (int j = 0; j < NB && j < n_tiles; ++j) load_k(j);
             for (int i = 0; i < n_tiles; ++i) {
-                // S = Q K^T once the softmax warps have split Q (first tile), K and V^T
-                if (!mbar_wait(&sm.bar_kv, i & 1, abort_flag, a.err)) break;
+                const int b = i % NB;
+                // S = Q K^T once the softmax warps have split Q (first tile) and this K tile
+                if (!mbar_wait(&sm.bar_kk, i & 1, abort_flag, a.err)) break;
                 tc_fence_after();
 #pragma unroll
                 for (int kk = 0; kk < HDKV / 8; ++kk) {
                     const uint32_t off = (kk & 3) * 32;
                     const uint64_t qh = sw128_desc(su32(sm.qh[kk >> 2]) + off);
                     const uint64_t ql = sw128_desc(su32(sm.ql[kk >> 2]) + off);
-                    const uint64_t kh = sw128_desc(su32(sm.kh[kk >> 2]) + off);
-                    const uint64_t kl = sw128_desc(su32(sm.kl[kk >> 2]) + off);
+                    const uint64_t kh = sw128_desc(su32(sm.kh[b][kk >> 2]) + off);
+                    const uint64_t kl = sw128_desc(su32(sm.kl[b][kk >> 2]) + off);
                     mma_tf32(tmem, qh, kh, tf32_idesc(BM, BN), kk > 0);
                     mma_tf32(tmem, qh, kl, tf32_idesc(BM, BN), 1);
                     mma_tf32(tmem, ql, kh, tf32_idesc(BM, BN), 1);
                 }
                 mma_commit(&sm.bar_s);
-                if (kTmaK && i + 1 < n_tiles) {
-                    // the K tile is free once S(i) is complete
+                if (kTmaK && i + NB < n_tiles) {
+                    // the K buffer is free once S(i) is complete
                     if (!mbar_wait(&sm.bar_s, i & 1, abort_flag, a.err)) break;
-                    mbar_expect_tx(&sm.bar_k, kKBytes);
-#pragma unroll
-                    for (int c = 0; c < HDKV / 32; ++c)
-                        tma_load_2d(sm.kh[c], &tm_k, hk * HDKV + 32 * c, (tile0 + i + 1) * BN, &sm.bar_k);
+                    load_k(i + NB);
                 }
+                // O_t = P V once P(i) is written and V^T(i) staged
                 if (!mbar_wait(&sm.bar_p, i & 1, abort_flag, a.err)) break;
+                if (!mbar_wait(&sm.bar_vv, i & 1, abort_flag, a.err)) break;
                 tc_fence_after();
 #pragma unroll
                 for (int kk = 0; kk < BN / 8; ++kk) {
                     const uint32_t off = (kk & 3) * 32;
                     const uint64_t ph = sw128_desc(su32(sm.ph[kk >> 2]) + off);
                     const uint64_t pl = sw128_desc(su32(sm.pl[kk >> 2]) + off);
-                    const uint64_t vh = sw128_desc(su32(sm.vh[kk >> 2]) + off);
-                    const uint64_t vl = sw128_desc(su32(sm.vl[kk >> 2]) + off);
+                    const uint64_t vh = sw128_desc(su32(sm.vh[b][kk >> 2]) + off);
+                    const uint64_t vl = sw128_desc(su32(sm.vl[b][kk >> 2]) + off);
                     mma_tf32(tmem + kOCol, ph, vh, tf32_idesc(BM, HDKV), kk > 0);
                     mma_tf32(tmem + kOCol, ph, vl, tf32_idesc(BM, HDKV), 1);
                     mma_tf32(tmem + kOCol, pl, vh, tf32_idesc(BM, HDKV), 1);
@@ -327,16 +335,15 @@ __global__ void __launch_bounds__(kThreadsP, 1)
             for (int c = 0; c < kV4; ++c)
                 vnext[c] = key < lmax ? kv4(a.v_reg, key, vq * kV4 + c) : make_float4(0.f, 0.f, 0.f, 0.f);
         };
-        if (n_tiles > 0) load_v(tile0);
-        if (n_tiles > 0 && mbar_wait(&sm.bar_q, 0, abort_flag, a.err))
-            split_region(&sm.qh[0][0], &sm.ql[0][0], BM * HDKV / 4, tid);
-        for (int i = 0; i < n_tiles; ++i) {
-            const int j0 = (tile0 + i) * BN;
+        // K tile j -> buffer j % NB, split into TF32 halves (fp32: in place after its TMA copy;
+        // binary16 / Q8_0: read and converted here; keys past the widest window are zero)
+        auto stage_k = [&](int j) -> bool {
+            const int b = j % NB;
             if (kTmaK) {
-                if (!mbar_wait(&sm.bar_k, i & 1, abort_flag, a.err)) break;
-                split_region(&sm.kh[0][0], &sm.kl[0][0], BN * HDKV / 4, tid);
-            } else {  // K tile -> SW128 slabs (keys along N); keys past the widest window are zero
-                const int key = j0 + vk;
+                if (!mbar_wait(&sm.bar_k[b], (j / NB) & 1, abort_flag, a.err)) return false;
+                split_region(&sm.kh[b][0][0], &sm.kl[b][0][0], BN * HDKV / 4, tid);
+            } else {
+                const int key = (tile0 + j) * BN + vk;
 #pragma unroll 4
                 for (int d4 = vq * (HDKV / 16); d4 < (vq + 1) * (HDKV / 16); ++d4) {
                     const float4 kv = key < lmax ? kv4(a.k_reg, key, d4) : make_float4(0.f, 0.f, 0.f, 0.f);
@@ -347,32 +354,53 @@ __global__ void __launch_bounds__(kThreadsP, 1)
                         float hi, lo;
                         split_tf32(kk[e], hi, lo);
                         const uint32_t off = sw128_off(vk, d & 31);
-                        *reinterpret_cast<float *>(reinterpret_cast<unsigned char *>(sm.kh[d >> 5]) + off) = hi;
-                        *reinterpret_cast<float *>(reinterpret_cast<unsigned char *>(sm.kl[d >> 5]) + off) = lo;
+                        *reinterpret_cast<float *>(reinterpret_cast<unsigned char *>(sm.kh[b][d >> 5]) + off) = hi;
+                        *reinterpret_cast<float *>(reinterpret_cast<unsigned char *>(sm.kl[b][d >> 5]) + off) = lo;
                     }
                 }
             }
-            {   // V tile -> V^T hi/lo (K-major, keys along K); keys past the widest window are zero
-                unsigned char *vth = reinterpret_cast<unsigned char *>(sm.vh[vk >> 5]);
-                unsigned char *vtl = reinterpret_cast<unsigned char *>(sm.vl[vk >> 5]);
-#pragma unroll
-                for (int c = 0; c < kV4; ++c) {
-                    const int d4 = vq * kV4 + c;
-                    const float vv[4] = {vnext[c].x, vnext[c].y, vnext[c].z, vnext[c].w};
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        float hi, lo;
-                        split_tf32(vv[e], hi, lo);
-                        const uint32_t off = sw128_off(4 * d4 + e, vk & 31);
-                        *reinterpret_cast<float *>(vth + off) = hi;
-                        *reinterpret_cast<float *>(vtl + off) = lo;
-                    }
-                }
-            }
-            fence_async_smem();  // split Q/K and V^T -> visible to the tensor cores
+            fence_async_smem();  // split K -> visible to the tensor cores
             tc_fence_before();
-            mbar_arrive(&sm.bar_kv);
-            if (i + 1 < n_tiles) load_v(tile0 + i + 1);
+            mbar_arrive(&sm.bar_kk);
+            return true;
+        };
+        // V tile j (held in vnext) -> V^T hi/lo in buffer j % NB (K-major, keys along K)
+        auto stage_v = [&](int j) {
+            const int b = j % NB;
+            unsigned char *vth = reinterpret_cast<unsigned char *>(sm.vh[b][vk >> 5]);
+            unsigned char *vtl = reinterpret_cast<unsigned char *>(sm.vl[b][vk >> 5]);
+#pragma unroll
+            for (int c = 0; c < kV4; ++c) {
+                const int d4 = vq * kV4 + c;
+                const float vv[4] = {vnext[c].x, vnext[c].y, vnext[c].z, vnext[c].w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    float hi, lo;
+                    split_tf32(vv[e], hi, lo);
+                    const uint32_t off = sw128_off(4 * d4 + e, vk & 31);
+                    *reinterpret_cast<float *>(vth + off) = hi;
+                    *reinterpret_cast<float *>(vtl + off) = lo;
+                }
+            }
+            fence_async_smem();  // V^T -> visible to the tensor cores
+            tc_fence_before();
+            mbar_arrive(&sm.bar_vv);
+            if (j + 1 < n_tiles) load_v(tile0 + j + 1);
+        };
+        // Order per tile i: P(i) from S(i); then K(i+1) (and, with two buffers, V^T(i+1)) staged
+        // while the tensor cores form O_t(i), so S(i+1) can follow O_t(i) at once; then O += O_t.
+        bool ok = n_tiles > 0;
+        if (ok) {
+            load_v(tile0);
+            ok = mbar_wait(&sm.bar_q, 0, abort_flag, a.err);
+        }
+        if (ok) {
+            split_region(&sm.qh[0][0], &sm.ql[0][0], BM * HDKV / 4, tid);
+            ok = stage_k(0);
+        }
+        if (ok) stage_v(0);
+        for (int i = 0; ok && i < n_tiles; ++i) {
+            const int j0 = (tile0 + i) * BN;
             if (!mbar_wait(&sm.bar_s, i & 1, abort_flag, a.err)) break;
             tc_fence_after();
             float r[32];
@@ -406,6 +434,10 @@ __global__ void __launch_bounds__(kThreadsP, 1)
             fence_async_smem();  // P hi/lo -> visible to the tensor cores
             tc_fence_before();
             mbar_arrive(&sm.bar_p);
+            if (i + 1 < n_tiles) {
+                if (!stage_k(i + 1)) break;
+                if (NB == 2) stage_v(i + 1);  // its buffer was last read by O_t(i - 1)
+            }
             if (!mbar_wait(&sm.bar_o, i & 1, abort_flag, a.err)) break;
             tc_fence_after();
 #pragma unroll
@@ -415,6 +447,7 @@ __global__ void __launch_bounds__(kThreadsP, 1)
                 for (int e = 0; e < 32; ++e) o[32 * c + e] = fmaf(o[32 * c + e], corr, r[e]);
             }
             tc_fence_before();
+            if (NB == 1 && i + 1 < n_tiles) stage_v(i + 1);  // one buffer: after O_t(i) has read it
         }
         bool write_out = true;
         if (n_act > 1) {
