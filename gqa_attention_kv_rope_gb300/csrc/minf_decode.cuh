@@ -247,7 +247,7 @@ __device__ __forceinline__ void rope_lane(float4 (&x)[KF4], const float (&sn)[2 
 // pair (4*sub + 32*(k/2))/2 + k%2 (matching rope_lane's indexing).
 template <int KF4>
 __device__ __forceinline__ void rope_angles(float (&sn)[2 * KF4], float (&cs)[2 * KF4], float pf,
-                                            const RopeTable &tab, int style, int sub, int r4) {
+                                            const float *tab, int style, int sub, int r4) {
     constexpr int NA = 2 * KF4;
     constexpr int NQ = NA / 4;
     float ms[NQ], mc[NQ];
@@ -255,7 +255,7 @@ __device__ __forceinline__ void rope_angles(float (&sn)[2 * KF4], float (&cs)[2 
     for (int q = 0; q < NQ; ++q) {
         const int k = 4 * q + r4;
         const int j = style == 0 ? 4 * sub + 32 * (k >> 2) + (k & 3) : (4 * sub + 32 * (k >> 1)) / 2 + (k & 1);
-        sincosf(__fmul_rn(pf, tab.f[j]), &ms[q], &mc[q]);
+        sincosf(__fmul_rn(pf, tab[j]), &ms[q], &mc[q]);
     }
 #pragma unroll
     for (int k = 0; k < NA; ++k) {
@@ -431,6 +431,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __shared__ float sm_redM[kCons], sm_redL[kCons];
     __shared__ __align__(16) float sm_knew[HDKV], sm_vnew[HDKV];
     __shared__ int sm_last, sm_abort;
+    __shared__ float sm_tab[kFused ? HDKV / 2 : 1];  // angular speeds, read by lane-varying index
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int W = a.nk * HDKV;
@@ -438,6 +439,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int n_units = a.n_seq * P * a.n_split;
     volatile int *abort_flag = &sm_abort;
 
+    if (kFused)
+        for (int i = tid; i < HDKV / 2; i += blockDim.x) sm_tab[i] = a.tab.f[i];
     if (tid == 0) {
         for (int i = 0; i < kNST; ++i) {
             mbar_init(&full[i], 1);
@@ -488,7 +491,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int hk = t0.y / a.groups;
             const int pnew = t0.p < t0.cap_s ? t0.p : -1;
             float sn[2 * KF4], cs[2 * KF4];
-            rope_angles<KF4>(sn, cs, static_cast<float>(t0.p), a.tab, a.style, lane & 7, lane >> 3);
+            rope_angles<KF4>(sn, cs, static_cast<float>(t0.p), sm_tab, a.style, lane & 7, lane >> 3);
             if (lane < 8) append_new_row<HDKV, T>(a, t0, hk, pnew, sn, cs, lane, sm_knew, sm_vnew);
             __syncwarp();
             if (lane == 0) mbar_arrive(&knew_bar);
@@ -503,6 +506,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             float *yr = a.xn + static_cast<size_t>(s) * a.n_embd;
             const int n4 = a.n_embd >> 2;
             float ss = 0.0f;
+#pragma unroll 8
             for (int i = lane; i < n4; i += 32) {
                 const float4 v = reinterpret_cast<const float4 *>(hr)[i];
                 ss = fmaf(v.x, v.x, ss);
@@ -513,6 +517,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
             const float scale = 1.0f / sqrtf(ss / static_cast<float>(a.n_embd) + a.eps);
+#pragma unroll 8
             for (int i = lane; i < n4; i += 32) {
                 const float4 v = reinterpret_cast<const float4 *>(hr)[i];
                 const float4 g = a.gain ? reinterpret_cast<const float4 *>(a.gain)[i]
@@ -687,7 +692,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         first_unit = false;
         if (kFused) {
             float sn[2 * KF4], cs[2 * KF4];
-            rope_angles<KF4>(sn, cs, static_cast<float>(t.p), a.tab, a.style, sub, r4);
+            rope_angles<KF4>(sn, cs, static_cast<float>(t.p), sm_tab, a.style, sub, r4);
 #pragma unroll
             for (int hh = 0; hh < GH; ++hh) rope_lane<KF4>(qr[hh], sn, cs, a.style);
             if (k_writer && !util_unit && warp == 0 && r4 == 0)

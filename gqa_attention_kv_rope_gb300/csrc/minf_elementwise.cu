@@ -51,7 +51,8 @@ int sm_count() {
 
 // ----------------------------------------------------------------------------- RMSNorm
 // "11 . Attention, vec ops, and the KV cache", §3.2.1: y = x / sqrt(mean(x^2) + eps) * w.
-// One warp per row; the sum of squares is a per-lane fp32 sum folded by a butterfly.
+// One warp per row; the sum of squares is a per-lane fp32 sum folded by a butterfly.  The loops
+// are unrolled so that a lane's loads of a row are in flight together.
 template <bool kVec>
 __device__ __forceinline__ void rms_norm_row(float *y, const float *x, const float *w, int warp, int n, float eps) {
     const int lane = threadIdx.x & 31;
@@ -60,6 +61,7 @@ __device__ __forceinline__ void rms_norm_row(float *y, const float *x, const flo
     float ss = 0.0f;
     if (kVec) {
         const float4 *x4 = reinterpret_cast<const float4 *>(xr);
+#pragma unroll 8
         for (int i = lane; i < n / 4; i += 32) {
             float4 v = x4[i];
             ss = fmaf(v.x, v.x, ss);
@@ -68,6 +70,7 @@ __device__ __forceinline__ void rms_norm_row(float *y, const float *x, const flo
             ss = fmaf(v.w, v.w, ss);
         }
     } else {
+#pragma unroll 8
         for (int i = lane; i < n; i += 32) ss = fmaf(xr[i], xr[i], ss);
     }
 #pragma unroll
@@ -78,6 +81,7 @@ __device__ __forceinline__ void rms_norm_row(float *y, const float *x, const flo
         const float4 *x4 = reinterpret_cast<const float4 *>(xr);
         const float4 *w4 = reinterpret_cast<const float4 *>(w);
         float4 *y4 = reinterpret_cast<float4 *>(yr);
+#pragma unroll 8
         for (int i = lane; i < n / 4; i += 32) {
             float4 v = x4[i];
             float4 g = w ? w4[i] : make_float4(1.f, 1.f, 1.f, 1.f);
@@ -85,6 +89,7 @@ __device__ __forceinline__ void rms_norm_row(float *y, const float *x, const flo
                                 v.w * scale * g.w);
         }
     } else {
+#pragma unroll 8
         for (int i = lane; i < n; i += 32) {
             float v = xr[i] * scale;
             yr[i] = w ? v * w[i] : v;
@@ -126,22 +131,30 @@ __device__ __forceinline__ void rope_pair(float &x0, float &x1, float th) {
     x1 = b;
 }
 
-// Rotates pair i of head row `row` (hd floats) in place.
-__device__ __forceinline__ void rope_row_pair(float *row, int i, int hd, int style, float p,
-                                              const RopeTable &tab) {
+// Rotates pair i of head row `row` (hd floats) in place; f: the angular speeds.
+__device__ __forceinline__ void rope_row_pair(float *row, int i, int hd, int style, float p, const float *f) {
     const int half = hd >> 1;
     const int i0 = style == 0 ? i : 2 * i;
     const int i1 = style == 0 ? i + half : 2 * i + 1;
     float x0 = row[i0], x1 = row[i1];
-    rope_pair(x0, x1, __fmul_rn(p, tab.f[i]));
+    rope_pair(x0, x1, __fmul_rn(p, f[i]));
     row[i0] = x0;
     row[i1] = x1;
+}
+
+// The angular speeds, copied from the launch's table (kernel parameters, which lanes would read
+// at different offsets one by one) into shared memory once per block.
+__device__ __forceinline__ void table_to_smem(float *dst, const RopeTable &tab, int n) {
+    for (int i = threadIdx.x; i < n; i += blockDim.x) dst[i] = tab.f[i];
 }
 
 __global__ void __launch_bounds__(256) rope_kernel(float *x, const int32_t *pos, int nt, int nh,
                                                    int hd, int style, const RopeTable tab,
                                                    int32_t *err) {
     const int half = hd >> 1;
+    __shared__ float sf[kMaxHalf];
+    table_to_smem(sf, tab, half);
+    __syncthreads();
     const long long total = static_cast<long long>(nt) * nh * half;
     for (long long idx = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; idx < total;
          idx += static_cast<long long>(gridDim.x) * blockDim.x) {
@@ -153,7 +166,7 @@ __global__ void __launch_bounds__(256) rope_kernel(float *x, const int32_t *pos,
             if (i == 0 && th_idx % nh == 0) flag_error(err, MINF_ERRBIT_ROPE_POS);
             continue;
         }
-        rope_row_pair(x + th_idx * hd, i, hd, style, static_cast<float>(p), tab);
+        rope_row_pair(x + th_idx * hd, i, hd, style, static_cast<float>(p), sf);
     }
 }
 
@@ -321,18 +334,18 @@ int launch_kv_append_paged(void *k_pool, void *v_pool, int kv, int pool_blocks, 
 // ----------------------------------------------------------------------------- RoPE + store
 // One sweep per token over three kinds of work item: a q pair, a k pair (rotated, written
 // back in place and into the K region), and a float4 of v (copied into the V region).
-// Batched callers give each token its own arena offset and capacity.
+// Batched callers give each token its own arena offset and capacity.  fq, fk: the angular
+// speeds (in shared memory).  Item indices are 32-bit (the host keeps nt * items below 2^31).
 template <typename T>
-__device__ __forceinline__ void rope_kv_append_items(const RopeKvArgs &a, const RopeTable &tq, const RopeTable &tk,
+__device__ __forceinline__ void rope_kv_append_items(const RopeKvArgs &a, const float *fq, const float *fk,
                                                      int block, int blocks) {
     const int hq = a.hd >> 1, hk = a.hd_kv >> 1;
     const int nq = a.nh * hq, nkp = a.nk * hk, W = a.nk * a.hd_kv, nv = W >> 2;
     const int per_tok = nq + nkp + nv;
-    const long long total = static_cast<long long>(a.nt) * per_tok;
-    for (long long idx = block * static_cast<long long>(blockDim.x) + threadIdx.x; idx < total;
-         idx += static_cast<long long>(blocks) * blockDim.x) {
-        const int t = static_cast<int>(idx / per_tok);
-        int r = static_cast<int>(idx % per_tok);
+    const int total = a.nt * per_tok;
+    for (int idx = block * blockDim.x + threadIdx.x; idx < total; idx += blocks * blockDim.x) {
+        const int t = idx / per_tok;
+        int r = idx - t * per_tok;
         const int p = __ldg(a.pos + t);
         const int cap_t = a.caps ? __ldg(a.caps + t) : a.cap;
         long long srow = (a.row_off ? __ldg(a.row_off + t) : 0) + p;  // the stored row
@@ -349,20 +362,20 @@ __device__ __forceinline__ void rope_kv_append_items(const RopeKvArgs &a, const 
                 if (r == 0) flag_error(a.err, MINF_ERRBIT_ROPE_POS);
                 continue;
             }
-            const int h = r / hq, i = r % hq;
+            const int h = r / hq, i = r - h * hq;
             rope_row_pair(a.q + (static_cast<size_t>(t) * a.nh + h) * a.hd, i, a.hd, a.style,
-                          static_cast<float>(p), tq);
+                          static_cast<float>(p), fq);
             continue;
         }
         r -= nq;
         if (r < nkp) {  // k pair: rotate, write back, store
             if (p < 0) continue;  // already flagged by the q branch
-            const int h = r / hk, i = r % hk;
+            const int h = r / hk, i = r - h * hk;
             float *row = a.k + (static_cast<size_t>(t) * a.nk + h) * a.hd_kv;
             const int i0 = a.style == 0 ? i : 2 * i;
             const int i1 = a.style == 0 ? i + hk : 2 * i + 1;
             float x0 = row[i0], x1 = row[i1];
-            rope_pair(x0, x1, __fmul_rn(static_cast<float>(p), tk.f[i]));
+            rope_pair(x0, x1, __fmul_rn(static_cast<float>(p), fk[i]));
             row[i0] = x0;
             row[i1] = x1;
             if (store_ok) {
@@ -383,10 +396,19 @@ __device__ __forceinline__ void rope_kv_append_items(const RopeKvArgs &a, const 
     }
 }
 
+// Work items of a RoPE + store sweep over nt tokens.
+inline long long rope_kv_items(const RopeKvArgs &a) {
+    return (static_cast<long long>(a.nh) * (a.hd / 2) + a.nk * (a.hd_kv / 2) + a.nk * a.hd_kv / 4) * a.nt;
+}
+
 template <typename T>
 __global__ void __launch_bounds__(256) rope_kv_append_kernel(RopeKvArgs a, const RopeTable tq,
                                                              const RopeTable tk) {
-    rope_kv_append_items<T>(a, tq, tk, blockIdx.x, gridDim.x);
+    __shared__ float fq[kMaxHalf], fk[kMaxHalf];
+    table_to_smem(fq, tq, a.hd >> 1);
+    table_to_smem(fk, tk, a.hd_kv >> 1);
+    __syncthreads();
+    rope_kv_append_items<T>(a, fq, fk, blockIdx.x, gridDim.x);
 }
 
 // The layer step's prologue in one launch: the first `norm_blocks` blocks compute the
@@ -402,7 +424,11 @@ __global__ void __launch_bounds__(256) layer_prologue_kernel(RopeKvArgs a, const
         if (warp < nrm.rows) rms_norm_row<kVec>(nrm.y, nrm.x, nrm.w, warp, nrm.n, nrm.eps);
         return;
     }
-    rope_kv_append_items<T>(a, tq, tk, blockIdx.x - norm_blocks, gridDim.x - norm_blocks);
+    __shared__ float fq[kMaxHalf], fk[kMaxHalf];  // norm blocks have returned: block-uniform
+    table_to_smem(fq, tq, a.hd >> 1);
+    table_to_smem(fk, tk, a.hd_kv >> 1);
+    __syncthreads();
+    rope_kv_append_items<T>(a, fq, fk, blockIdx.x - norm_blocks, gridDim.x - norm_blocks);
 }
 
 int launch_layer_prologue(const RopeKvArgs &a, float theta, float freq_scale, const NormArgs &nrm, cudaStream_t s) {
@@ -410,10 +436,9 @@ int launch_layer_prologue(const RopeKvArgs &a, float theta, float freq_scale, co
     RopeTable tq, tk;
     rope_table(&tq, a.hd, theta, freq_scale);
     rope_table(&tk, a.hd_kv, theta, freq_scale);
-    const long long per_tok =
-        static_cast<long long>(a.nh) * (a.hd / 2) + a.nk * (a.hd_kv / 2) + a.nk * a.hd_kv / 4;
+    if (rope_kv_items(a) >= (1ll << 31)) return MINF_ERR_UNSUPPORTED;
     const int norm_blocks = (nrm.rows + 7) / 8;
-    const int blocks = norm_blocks + grid_for(per_tok * a.nt, 256);
+    const int blocks = norm_blocks + grid_for(rope_kv_items(a), 256);
     const bool vec = (nrm.n % 4 == 0) && aligned16(nrm.x) && aligned16(nrm.y) && (!nrm.w || aligned16(nrm.w));
     if (a.kv == kKvF16)
         vec ? layer_prologue_kernel<__half, true><<<blocks, 256, 0, s>>>(a, tq, tk, nrm, norm_blocks)
@@ -429,12 +454,12 @@ int launch_rope_kv_append(const RopeKvArgs &a, float theta, float freq_scale, cu
     RopeTable tq, tk;
     rope_table(&tq, a.hd, theta, freq_scale);
     rope_table(&tk, a.hd_kv, theta, freq_scale);
-    const long long per_tok =
-        static_cast<long long>(a.nh) * (a.hd / 2) + a.nk * (a.hd_kv / 2) + a.nk * a.hd_kv / 4;
+    if (rope_kv_items(a) >= (1ll << 31)) return MINF_ERR_UNSUPPORTED;
+    const int blocks = grid_for(rope_kv_items(a), 256);
     if (a.kv == kKvF16)
-        rope_kv_append_kernel<__half><<<grid_for(per_tok * a.nt, 256), 256, 0, s>>>(a, tq, tk);
+        rope_kv_append_kernel<__half><<<blocks, 256, 0, s>>>(a, tq, tk);
     else
-        rope_kv_append_kernel<float><<<grid_for(per_tok * a.nt, 256), 256, 0, s>>>(a, tq, tk);
+        rope_kv_append_kernel<float><<<blocks, 256, 0, s>>>(a, tq, tk);
     return cudaPeekAtLastError() == cudaSuccess ? MINF_OK : MINF_ERR_CUDA;
 }
 
