@@ -144,11 +144,12 @@ struct PParams {
     int *ws_ticket;            // one per (query tile, head)
 };
 
-// Round to the nearest TF32 value (10 explicit mantissa bits), ties away from zero.
+// Round to the nearest TF32 value (10 explicit mantissa bits), ties away from zero: half a TF32
+// unit (bit 12) is added to the magnitude's bit pattern and the 13 low bits are cleared; a
+// carry moves into the exponent as it should.  The same result as cvt.rna.tf32.f32 for every
+// finite input, on the integer pipe instead of the conversion unit.
 __device__ __forceinline__ float tf32_rna(float x) {
-    uint32_t r;
-    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
-    return __uint_as_float(r);
+    return __uint_as_float((__float_as_uint(x) + 0x1000u) & 0xFFFFE000u);
 }
 
 __device__ __forceinline__ void split_tf32(float x, float &hi, float &lo) {
