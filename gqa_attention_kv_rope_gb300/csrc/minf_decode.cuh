@@ -265,6 +265,19 @@ __device__ __forceinline__ void rope_angles(float (&sn)[2 * KF4], float (&cs)[2 
     }
 }
 
+// The same angles from shared tables of the sines and cosines of every pair (tsn[i], tcs[i]
+// for pair i), indexed as rope_angles indexes its angles.
+template <int KF4>
+__device__ __forceinline__ void rope_angles_tab(float (&sn)[2 * KF4], float (&cs)[2 * KF4], const float *tsn,
+                                                const float *tcs, int style, int sub) {
+#pragma unroll
+    for (int k = 0; k < 2 * KF4; ++k) {
+        const int j = style == 0 ? 4 * sub + 32 * (k >> 2) + (k & 3) : (4 * sub + 32 * (k >> 1)) / 2 + (k & 1);
+        sn[k] = tsn[j];
+        cs[k] = tcs[j];
+    }
+}
+
 struct Unit {
     int s, y, j, p, cap_s, L, n_act, r_begin, r_end;
     long long base;
@@ -280,6 +293,11 @@ __device__ __forceinline__ int window_of(const KParams &a, int s) {
 // The unit u decodes to (sequence, pair, split) and, from the sequence's position, to the
 // run of rows it owns.  Units [0, grid) are the CTAs' first units; in a batch, where the units
 // outnumber the CTAs, the rest are drawn from the counter, sequences longest first (`order`).
+// Within a sequence the pair varies fastest and the split slowest, so the highest CTA indices
+// hold the last splits of every pair: the shortest run (the window's ragged end) and the
+// splits a short window leaves empty.  The block scheduler places CTAs in index order as SMs
+// free up, so those light units land on the SMs that the previous launch left last -- the ones
+// whose CTA merged a group -- and a late start there does not delay this launch's merges.
 // Split j of a window of L rows covers rows [j*T, (j+1)*T) with T the smallest multiple of the
 // stage height (and at least min_rows) that cuts L into at most n_split runs; the n_act
 // active splits fill partial slots [0, n_act).  Producer and consumers derive the unit
@@ -288,8 +306,9 @@ template <int R>
 __device__ __forceinline__ Unit unit_of(const KParams &a, int u, const int *order) {
     Unit t;
     const int P = a.nk * a.groups;
-    t.j = u % a.n_split;
-    t.y = (u / a.n_split) % P;
+    const int w = u % (a.n_split * P);
+    t.y = w % P;
+    t.j = w / P;
     const int rank = u / (a.n_split * P);
     t.s = order ? order[rank] : rank;
     t.p = __ldg(a.pos + t.s);
@@ -432,6 +451,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __shared__ __align__(16) float sm_knew[HDKV], sm_vnew[HDKV];
     __shared__ int sm_last, sm_abort;
     __shared__ float sm_tab[kFused ? HDKV / 2 : 1];  // angular speeds, read by lane-varying index
+    __shared__ float sm_sn[kFused ? HDKV / 2 : 1], sm_cs[kFused ? HDKV / 2 : 1];  // first unit's sin, cos
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int W = a.nk * HDKV;
@@ -484,14 +504,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (kFused && static_cast<int>(blockIdx.x) < a.n_seq)
             prefetch_l2(a.h + static_cast<size_t>(blockIdx.x) * a.n_embd, a.n_embd * 4, lane);
+        // the appended row's angles: its position is not written by a preceding kernel
+        float sn[2 * KF4], cs[2 * KF4];
+        if (util_append) rope_angles<KF4>(sn, cs, static_cast<float>(t0.p), sm_tab, a.style, lane & 7, lane >> 3);
         gdc_wait();
         if (util_append) {
             // the rotated k written back, the K/V row stored and staged, then -- the row in
             // memory -- the dependent launch released for this CTA
             const int hk = t0.y / a.groups;
             const int pnew = t0.p < t0.cap_s ? t0.p : -1;
-            float sn[2 * KF4], cs[2 * KF4];
-            rope_angles<KF4>(sn, cs, static_cast<float>(t0.p), sm_tab, a.style, lane & 7, lane >> 3);
             if (lane < 8) append_new_row<HDKV, T>(a, t0, hk, pnew, sn, cs, lane, sm_knew, sm_vnew);
             __syncwarp();
             if (lane == 0) mbar_arrive(&knew_bar);
@@ -652,9 +673,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     Unit t = t0;
     bool have = unit_active(t);
     bool first_unit = true;
+    bool scratch_used = false;  // a previous unit of this CTA has read sm_acc, sm_m, sm_l, sm_red
     if (have && warp < GH) {  // this unit's q rows, into L2 before the wait
         const int h0 = (t.y / a.groups) * (a.nh / a.nk) + (t.y % a.groups) * GH;
         prefetch_l2(a.q + (static_cast<size_t>(t.s) * a.nh + h0 + warp) * a.hd, HDKV * 4, lane);
+    }
+    // The first unit's RoPE sines and cosines, one pair a thread, before the wait (the position
+    // is not written by a preceding kernel): after it, rotating q costs only table reads.
+    const bool pre_ang = kFused && have;
+    if (kFused) {
+        if (pre_ang)
+            for (int i = tid; i < HDKV / 2; i += kCons)
+                sincosf(__fmul_rn(static_cast<float>(t.p), sm_tab[i]), &sm_sn[i], &sm_cs[i]);
+        cons_sync(&cons_bar, cphase, abort_flag, a.err);
     }
     gdc_wait();
     if (early) {
@@ -689,10 +720,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool k_writer = kFused && t.r_end == t.L;
         const int pnew = k_writer && t.p < t.cap_s ? t.p : -1;
         const bool util_unit = util_append && first_unit;  // appended by the utility warp
+        const bool tab_unit = pre_ang && first_unit;        // angles already in shared memory
         first_unit = false;
         if (kFused) {
             float sn[2 * KF4], cs[2 * KF4];
-            rope_angles<KF4>(sn, cs, static_cast<float>(t.p), sm_tab, a.style, sub, r4);
+            if (tab_unit)
+                rope_angles_tab<KF4>(sn, cs, sm_sn, sm_cs, a.style, sub);
+            else
+                rope_angles<KF4>(sn, cs, static_cast<float>(t.p), sm_tab, a.style, sub, r4);
 #pragma unroll
             for (int hh = 0; hh < GH; ++hh) rope_lane<KF4>(qr[hh], sn, cs, a.style);
             if (k_writer && !util_unit && warp == 0 && r4 == 0)
@@ -870,7 +905,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
 
         // ------------------------------------------------------------ end of the unit
-        cons_sync(&cons_bar, cphase, abort_flag, a.err);  // the previous unit's scratch readers are done
+        if (scratch_used)  // the previous unit's readers of the shared scratch are done
+            cons_sync(&cons_bar, cphase, abort_flag, a.err);
+        scratch_used = true;
         float4 acc[GH];
 #pragma unroll
         for (int hh = 0; hh < GH; ++hh) {
