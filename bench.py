@@ -710,13 +710,16 @@ def run_batched(m, torch, wl, dev, steps, dtype=None):
 
 
 def run_elementwise(m, torch, dev, reps=20):
-    """HBM throughput of the stand-alone RMSNorm (4096 x 1024 rows, gains) and SiLU*mul
-    (64 Mi elements) kernels, L2 flushed before every timed launch."""
+    """HBM throughput of the stand-alone RMSNorm (4096 and 32768 rows of 1024, gains) and
+    SiLU*mul (64 Mi elements) kernels, L2 flushed before every timed launch.  The 32768-row
+    case moves 128 MiB each way (more than L2); the 4096-row case is latency-bound."""
     flush = torch.empty(2 * L2_BYTES // 4, device=dev)
     stream = torch.cuda.current_stream()
     x = torch.randn(4096, 1024, device=dev)
     w = torch.rand(1024, device=dev) + 0.5
     y = torch.empty_like(x)
+    xl = torch.randn(32768, 1024, device=dev)
+    yl = torch.empty_like(xl)
     n = 64 << 20
     g = torch.randn(n, device=dev)
     u = torch.randn(n, device=dev)
@@ -736,10 +739,12 @@ def run_elementwise(m, torch, dev, reps=20):
         return statistics.median(ts)
 
     ms_rms = timed(lambda: m.binding.minf_rms_norm(y, x, w, 1e-6))
+    ms_rms_l = timed(lambda: m.binding.minf_rms_norm(yl, xl, w, 1e-6))
     ms_silu = timed(lambda: m.binding.minf_silu_mul(o, g, u))
     res = {"rms_norm_4096x1024_gbs": round((2 * x.numel() + w.numel()) * 4 / (ms_rms * 1e-3) / 1e9, 1),
+           "rms_norm_32768x1024_gbs": round((2 * xl.numel() + w.numel()) * 4 / (ms_rms_l * 1e-3) / 1e9, 1),
            "silu_mul_64Mi_gbs": round(3 * n * 4 / (ms_silu * 1e-3) / 1e9, 1)}
-    del flush, x, y, g, u, o
+    del flush, x, y, xl, yl, g, u, o
     return res
 
 

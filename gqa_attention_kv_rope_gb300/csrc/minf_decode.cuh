@@ -63,6 +63,7 @@ constexpr int kUtility = kNW + 1;       // warp 9: RMSNorm rows, empty windows, 
 constexpr int kThreads = kCons + 64;    // + producer + utility (same register budget as 9 warps)
 constexpr int kSub = 8;                 // rows per warp sub-tile
 constexpr int kNST = 3;                 // pipeline stages
+constexpr int kPreWait = 2;             // stages a producer issues before the dependency wait
 constexpr int kStageBytes = 64 * 1024;  // K + V tile of one stage
 constexpr int kGridTarget = 152;        // GB300: one persistent CTA per SM
 constexpr int kMaxSplit = 64;           // partials per (sequence, kv group)
@@ -575,11 +576,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const int n_st = (t.r_end - t.r_begin + R - 1) / R;
                     for (int st = 0; st < n_st && !*abort_flag; ++st, ++it) {
                         const int slot = it % kNST;
+                        // Cached rows need no wait, but only kPreWait stages go out before it:
+                        // a deeper burst, issued while the previous launch merges its splits and
+                        // completes, slows that launch's round trips more than it saves here.
+                        if (!waited && it >= kPreWait) {
+                            gdc_wait();
+                            waited = true;
+                        }
                         if (it >= kNST) {
-                            if (!waited) {  // cached rows need no wait; reusing the ring does
-                                gdc_wait();
-                                waited = true;
-                            }
                             if (!mbar_wait(&empty[slot], ((it / kNST) & 1) ^ 1, abort_flag, a.err)) break;
                         }
                         sm_meta[slot] = make_int2(u, st);

@@ -105,13 +105,59 @@ __global__ void __launch_bounds__(256) rms_norm_kernel(float *y, const float *x,
     rms_norm_row<kVec>(y, x, w, warp, n, eps);
 }
 
+// Rows of NV*128 values: a lane holds its NV float4s of the row in registers between the sum of
+// squares and the scaling, so x is read once.  Same arithmetic in the same order as
+// rms_norm_row (bit-identical results).
+template <int NV>
+__global__ void __launch_bounds__(256) rms_norm_reg_kernel(float *y, const float *x, const float *w, int rows,
+                                                           float eps) {
+    const int row = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    if (row >= rows) return;
+    const int lane = threadIdx.x & 31;
+    constexpr int n = NV * 128;
+    const float4 *x4 = reinterpret_cast<const float4 *>(x + static_cast<size_t>(row) * n);
+    float4 v[NV];
+#pragma unroll
+    for (int k = 0; k < NV; ++k) v[k] = x4[lane + 32 * k];
+    float ss = 0.0f;
+#pragma unroll
+    for (int k = 0; k < NV; ++k) {
+        ss = fmaf(v[k].x, v[k].x, ss);
+        ss = fmaf(v[k].y, v[k].y, ss);
+        ss = fmaf(v[k].z, v[k].z, ss);
+        ss = fmaf(v[k].w, v[k].w, ss);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    const float scale = 1.0f / sqrtf(ss / static_cast<float>(n) + eps);
+    const float4 *w4 = reinterpret_cast<const float4 *>(w);
+    float4 *y4 = reinterpret_cast<float4 *>(y + static_cast<size_t>(row) * n);
+#pragma unroll
+    for (int k = 0; k < NV; ++k) {
+        const float4 g = w ? w4[lane + 32 * k] : make_float4(1.f, 1.f, 1.f, 1.f);
+        y4[lane + 32 * k] = make_float4(v[k].x * scale * g.x, v[k].y * scale * g.y, v[k].z * scale * g.z,
+                                        v[k].w * scale * g.w);
+    }
+}
+
+template <int NV>
+void launch_rms_norm_reg(float *y, const float *x, const float *w, int rows, int n, float eps, int blocks,
+                         cudaStream_t s) {
+    if constexpr (NV > 1) {
+        if (n != NV * 128) return launch_rms_norm_reg<NV - 1>(y, x, w, rows, n, eps, blocks, s);
+    }
+    rms_norm_reg_kernel<NV><<<blocks, 256, 0, s>>>(y, x, w, rows, eps);
+}
+
 int launch_rms_norm(float *y, const float *x, const float *w, int rows, int n, float eps,
                     cudaStream_t s) {
     if (rows == 0) return MINF_OK;
     const bool vec = (n % 4 == 0) && aligned16(x) && aligned16(y) && (!w || aligned16(w));
     const int threads = 256;
     const int blocks = (rows + 7) / 8;
-    if (vec)
+    if (vec && n % 128 == 0 && n <= 16 * 128)
+        launch_rms_norm_reg<16>(y, x, w, rows, n, eps, blocks, s);
+    else if (vec)
         rms_norm_kernel<true><<<blocks, threads, 0, s>>>(y, x, w, rows, n, eps);
     else
         rms_norm_kernel<false><<<blocks, threads, 0, s>>>(y, x, w, rows, n, eps);

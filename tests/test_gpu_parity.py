@@ -49,7 +49,10 @@ def err_word():
 
 
 # --------------------------------------------------------------------------- RMSNorm
-@pytest.mark.parametrize("rows,n", [(1, 896), (512, 896), (1, 1024), (4096, 1024), (3, 1001), (7, 4)])
+# rows of 128..2048 values in whole 128-value chunks take the register-resident kernel (one
+# read of x); the others (2176, 1001, 4) the two-pass one
+@pytest.mark.parametrize("rows,n", [(1, 896), (512, 896), (1, 1024), (4096, 1024), (5, 128), (9, 2048),
+                                    (3, 640), (2, 2176), (3, 1001), (7, 4)])
 def test_rms_norm(m, orc, rows, n):
     x = rnd((rows, n), 1 + n)
     w = torch.rand(n, generator=torch.Generator().manual_seed(2)) + 0.5
