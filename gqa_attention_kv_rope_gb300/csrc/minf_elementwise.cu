@@ -460,12 +460,15 @@ __global__ void __launch_bounds__(256) rope_kv_append_kernel(RopeKvArgs a, const
 // The layer step's prologue in one launch: the first `norm_blocks` blocks compute the
 // RMSNorm rows (one warp per row), the rest rotate q and k and store the rows.  It touches
 // nothing the attention kernel after it reads before its own dependency wait, so it lets that
-// launch start at once (programmatic dependent launch).
+// launch start at once (programmatic dependent launch).  It is itself launched early: its
+// blocks load the angular-speed tables, then wait for the preceding kernel before they read
+// or write anything in memory (positions included).
 template <typename T, bool kVec>
 __global__ void __launch_bounds__(256) layer_prologue_kernel(RopeKvArgs a, const RopeTable tq, const RopeTable tk,
                                                              NormArgs nrm, int norm_blocks) {
     asm volatile("griddepcontrol.launch_dependents;");
     if (static_cast<int>(blockIdx.x) < norm_blocks) {
+        asm volatile("griddepcontrol.wait;" ::: "memory");
         const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
         if (warp < nrm.rows) rms_norm_row<kVec>(nrm.y, nrm.x, nrm.w, warp, nrm.n, nrm.eps);
         return;
@@ -474,6 +477,7 @@ __global__ void __launch_bounds__(256) layer_prologue_kernel(RopeKvArgs a, const
     table_to_smem(fq, tq, a.hd >> 1);
     table_to_smem(fk, tk, a.hd_kv >> 1);
     __syncthreads();
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     rope_kv_append_items<T>(a, fq, fk, blockIdx.x - norm_blocks, gridDim.x - norm_blocks);
 }
 
@@ -486,13 +490,25 @@ int launch_layer_prologue(const RopeKvArgs &a, float theta, float freq_scale, co
     const int norm_blocks = (nrm.rows + 7) / 8;
     const int blocks = norm_blocks + grid_for(rope_kv_items(a), 256);
     const bool vec = (nrm.n % 4 == 0) && aligned16(nrm.x) && aligned16(nrm.y) && (!nrm.w || aligned16(nrm.w));
+    // programmatic stream serialization: the blocks may be scheduled before the preceding kernel
+    // completes; they wait for it (griddepcontrol.wait) before touching memory
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(blocks);
+    cfg.blockDim = dim3(256);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e;
     if (a.kv == kKvF16)
-        vec ? layer_prologue_kernel<__half, true><<<blocks, 256, 0, s>>>(a, tq, tk, nrm, norm_blocks)
-            : layer_prologue_kernel<__half, false><<<blocks, 256, 0, s>>>(a, tq, tk, nrm, norm_blocks);
+        e = vec ? cudaLaunchKernelEx(&cfg, layer_prologue_kernel<__half, true>, a, tq, tk, nrm, norm_blocks)
+                : cudaLaunchKernelEx(&cfg, layer_prologue_kernel<__half, false>, a, tq, tk, nrm, norm_blocks);
     else
-        vec ? layer_prologue_kernel<float, true><<<blocks, 256, 0, s>>>(a, tq, tk, nrm, norm_blocks)
-            : layer_prologue_kernel<float, false><<<blocks, 256, 0, s>>>(a, tq, tk, nrm, norm_blocks);
-    return cudaPeekAtLastError() == cudaSuccess ? MINF_OK : MINF_ERR_CUDA;
+        e = vec ? cudaLaunchKernelEx(&cfg, layer_prologue_kernel<float, true>, a, tq, tk, nrm, norm_blocks)
+                : cudaLaunchKernelEx(&cfg, layer_prologue_kernel<float, false>, a, tq, tk, nrm, norm_blocks);
+    return e == cudaSuccess ? MINF_OK : MINF_ERR_CUDA;
 }
 
 int launch_rope_kv_append(const RopeKvArgs &a, float theta, float freq_scale, cudaStream_t s) {

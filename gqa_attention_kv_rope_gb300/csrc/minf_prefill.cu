@@ -20,10 +20,17 @@
 // TF32, lo = the remainder rounded to TF32), and each product is the sum of three MMAs
 // hi*hi + hi*lo + lo*hi (the split-precision "3xTF32" scheme), which brings the tensor-core
 // result to fp32 accuracy.  Q and K tiles arrive by TMA (cp.async.bulk.tensor, 128-byte
-// swizzle) and are split in place by the softmax threads; V is transposed and split into the
-// K-major layout the MMA takes.  These are generic-proxy writes, fenced to the async proxy
-// before the MMA that reads them is released.  Warp 4 is the producer: one elected thread
-// issues the TMA copies, the MMAs and the commits.
+// swizzle); Q is split in place by the softmax threads, K by two staging warps, which also
+// transpose and split V into the K-major layout the MMA takes.  These are generic-proxy writes,
+// fenced to the async proxy before the MMA that reads them is released.  Warp 4 is the
+// producer: one elected thread issues the TMA copies, the MMAs and the commits.
+//
+// Pipelining.  S has two TMEM buffers and the producer issues S(i+1) as soon as key tile i+1
+// is split, ahead of P(i)V(i), so the tensor cores form the next scores while the softmax
+// warps work on the current ones.  O_t has two TMEM buffers as well: the softmax warps publish
+// P(i) first and fold O_t(i-1) into their registers after it, while the tensor cores form
+// O_t(i) (with hd_kv 64 P also has two buffers in shared memory; with hd_kv 128, where shared
+// memory holds one, P(i) waits until O_t(i-1) has read P(i-1)).
 //
 // Every mbarrier wait is bounded by a 200 ms global-timer budget; a wait that expires sets
 // MINF_ERRBIT_TIMEOUT, makes every role leave its loop, and the CTA still frees its TMEM.
@@ -46,9 +53,15 @@ constexpr int BM = 128;              // query rows per CTA
 constexpr int BN = 32;               // keys per tile
 constexpr int kSoftThreads = 128;    // warps 0-3: TMEM lanes 0..127, one query row each
 constexpr int kProducerWarp = 4;
-constexpr int kThreadsP = kSoftThreads + 32;
-constexpr uint32_t kTmemCols = 256;  // S at column 0 (BN wide), O at column 128
-constexpr uint32_t kOCol = 128;
+constexpr int kStageWarp0 = 5;       // warps 5-6: K split, V^T staging
+constexpr int kStageThreads = 64;
+constexpr int kThreadsP = kSoftThreads + 32 + kStageThreads;
+// TMEM: S(i) at column (i % 2) * BN, O_t(i) at column 128 + (i % 2) * HDKV
+template <int HDKV>
+constexpr uint32_t tmem_cols() { return 128 + 2 * HDKV <= 256 ? 256 : 512; }
+template <int HDKV>
+__device__ __forceinline__ uint32_t o_col(int i) { return 128u + static_cast<uint32_t>(i & 1) * HDKV; }
+__device__ __forceinline__ uint32_t s_col(int i) { return static_cast<uint32_t>(i & 1) * BN; }
 
 // Operands are held as hi + lo TF32 pairs (x = hi + lo to about 2^-22 relative): each
 // product is formed from three tensor-core MMAs, hi*hi + hi*lo + lo*hi, so the TF32 inputs
@@ -57,12 +70,13 @@ constexpr uint32_t kOCol = 128;
 // in buffer j % NB.
 template <int HDKV>
 struct Smem {
-    static constexpr int NB = HDKV == 64 ? 2 : 1;
+    static constexpr int NB = HDKV == 64 ? 2 : 1;   // K and V^T tile buffers
+    static constexpr int NP = HDKV == 64 ? 2 : 1;   // P buffers
     float qh[HDKV / 32][BM * 32], ql[HDKV / 32][BM * 32];            // Q: 32-column SW128 slabs
     float kh[NB][HDKV / 32][BN * 32], kl[NB][HDKV / 32][BN * 32];    // K tiles (TMA lands in kh)
-    float ph[BN / 32][BM * 32], pl[BN / 32][BM * 32];                // P: keys along K
+    float ph[NP][BN / 32][BM * 32], pl[NP][BN / 32][BM * 32];        // P: keys along K
     float vh[NB][BN / 32][HDKV * 32], vl[NB][BN / 32][HDKV * 32];    // V^T: keys along K
-    unsigned long long bar_q, bar_k[NB], bar_kk, bar_vv, bar_s, bar_p, bar_o;
+    unsigned long long bar_q, bar_k[NB], bar_qs, bar_kk[NB], bar_vv[NB], bar_s[2], bar_p[2], bar_o[2];
     uint32_t tmem_base;
     int abort_flag;
     int lmax;
@@ -86,12 +100,16 @@ __host__ __device__ constexpr uint32_t tf32_idesc(int M, int N) {
            (static_cast<uint32_t>(M >> 4) << 24);
 }
 
-__device__ __forceinline__ void mma_tf32(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
-                                         uint32_t accumulate) {
+// One split-precision product step: D (+)= Ah*Bh + Ah*Bl + Al*Bh, three MMAs issued together
+// (the first accumulates into D only when `accumulate` is non-zero).
+__device__ __forceinline__ void mma3_tf32(uint32_t d_tmem, uint64_t ah, uint64_t al, uint64_t bh, uint64_t bl,
+                                          uint32_t idesc, uint32_t accumulate) {
     asm volatile(
-        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-        " tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n}" ::"r"(d_tmem),
-        "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
+        "{\n .reg .pred p, t;\n setp.ne.b32 p, %5, 0;\n setp.ne.b32 t, %7, 0;\n"
+        " tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %3, %6, p;\n"
+        " tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %4, %6, t;\n"
+        " tcgen05.mma.cta_group::1.kind::tf32 [%0], %2, %3, %6, t;\n}" ::"r"(d_tmem),
+        "l"(ah), "l"(al), "l"(bh), "l"(bl), "r"(accumulate), "r"(idesc), "r"(1u)
         : "memory");
 }
 
@@ -157,11 +175,12 @@ __device__ __forceinline__ void split_tf32(float x, float &hi, float &lo) {
     lo = tf32_rna(x - hi);
 }
 
-// Splits the fp32 values of an SW128 slab region in place (hi) and into a twin region (lo).
-__device__ __forceinline__ void split_region(float *hi, float *lo, int n_float4, int tid) {
+// Splits the fp32 values of an SW128 slab region in place (hi) and into a twin region (lo);
+// thread `tid` of `nthreads` takes every nthreads-th float4.
+__device__ __forceinline__ void split_region(float *hi, float *lo, int n_float4, int tid, int nthreads) {
     float4 *h4 = reinterpret_cast<float4 *>(hi);
     float4 *l4 = reinterpret_cast<float4 *>(lo);
-    for (int i = tid; i < n_float4; i += kSoftThreads) {
+    for (int i = tid; i < n_float4; i += nthreads) {
         float4 x = h4[i], a, b;
         split_tf32(x.x, a.x, b.x);
         split_tf32(x.y, a.y, b.y);
@@ -181,6 +200,35 @@ __device__ __forceinline__ float4 ld4(const __half *p, int i4) {
     return make_float4(x.x, x.y, y.x, y.y);
 }
 
+// The (query tile, key chunk) pair of pair index idx.  Pairs with kc <= qt come first (chunk
+// slowest), then the others: in a causal prefill from position 0 with chunks as long as query
+// tiles, the first set is exactly the pairs with keys, so every CTA with work is in the first
+// wave and no CTA with work waits behind ones that leave at once.  (Any order is correct; this
+// one only decides which CTAs start first.)
+__device__ __forceinline__ void pair_of(int idx, int n_qt, int n_kc, int &qt, int &kc) {
+    int base = 0;
+    for (int c = 0; c < n_kc && c < n_qt; ++c) {  // kc <= qt: qt = c .. n_qt-1
+        const int cnt = n_qt - c;
+        if (idx < base + cnt) {
+            kc = c;
+            qt = c + (idx - base);
+            return;
+        }
+        base += cnt;
+    }
+    for (int c = 1; c < n_kc; ++c) {  // kc > qt: qt = 0 .. min(c, n_qt)-1
+        const int cnt = c < n_qt ? c : n_qt;
+        if (idx < base + cnt) {
+            kc = c;
+            qt = idx - base;
+            return;
+        }
+        base += cnt;
+    }
+    kc = n_kc;  // idx past the last pair: no work
+    qt = 0;
+}
+
 // fp32 regions: K tiles arrive by TMA into kh and are split in place.  binary16 regions: the
 // softmax threads read the K tile themselves, converting, and write both halves (a binary16
 // value is exact in TF32, so its low half is zero).
@@ -193,24 +241,31 @@ __global__ void __launch_bounds__(kThreadsP, 1)
     Smem<HDKV> &sm = *reinterpret_cast<Smem<HDKV> *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    // CTA -> (key chunk, head, query tile), the chunk slowest so the CTAs that have work are
-    // launched first (chunks past a tile's widest window leave at once)
-    const int kc = blockIdx.x / (a.nh * a.n_qt);
-    const int h = (blockIdx.x / a.n_qt) % a.nh;
-    const int qt = blockIdx.x % a.n_qt;
+    // CTA -> (query tile, key chunk) pair and head, the head fastest (chunks past a tile's
+    // widest window leave at once)
+    const int h = blockIdx.x % a.nh;
+    int qt, kc;
+    pair_of(blockIdx.x / a.nh, a.n_qt, a.n_kc, qt, kc);
     const int t0 = qt * BM;
     const int g = a.nh / a.nk;
     const int hk = h / g;
     volatile int *abort_flag = &sm.abort_flag;
 
     if (tid == 0) {
+        // One barrier per buffer, so that no role can complete a phase twice before another
+        // role waits on it (every refill of a buffer waits on the consumer of its last phase).
         mbar_init(&sm.bar_q, 1);
-        for (int b = 0; b < Smem<HDKV>::NB; ++b) mbar_init(&sm.bar_k[b], 1);
-        mbar_init(&sm.bar_kk, kSoftThreads);
-        mbar_init(&sm.bar_vv, kSoftThreads);
-        mbar_init(&sm.bar_s, 1);
-        mbar_init(&sm.bar_p, kSoftThreads);
-        mbar_init(&sm.bar_o, 1);
+        mbar_init(&sm.bar_qs, kSoftThreads);
+        for (int b = 0; b < Smem<HDKV>::NB; ++b) {
+            mbar_init(&sm.bar_k[b], 1);
+            mbar_init(&sm.bar_kk[b], kStageThreads);
+            mbar_init(&sm.bar_vv[b], kStageThreads);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&sm.bar_s[b], 1);
+            mbar_init(&sm.bar_p[b], kSoftThreads);
+            mbar_init(&sm.bar_o[b], 1);
+        }
         sm.abort_flag = 0;
         sm.lmax = 0;
         mbar_init_fence();
@@ -240,7 +295,7 @@ __global__ void __launch_bounds__(kThreadsP, 1)
     if (warp == kProducerWarp) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                          su32(&sm.tmem_base)),
-                     "r"(kTmemCols)
+                     "r"(tmem_cols<HDKV>())
                      : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
@@ -251,9 +306,13 @@ __global__ void __launch_bounds__(kThreadsP, 1)
     // everything above reads only positions; q, the regions, the workspace and the output may
     // still be written by the preceding launch (a no-op without programmatic dependent launch)
     gdc_wait();
+    // The launch that follows may start now: this kernel writes no K/V rows (a following decode
+    // kernel streams cached rows before its own wait), and every launch before it has completed.
+    gdc_launch_dependents();
     constexpr uint32_t kQBytes = BM * HDKV * 4, kKBytes = BN * HDKV * 4;
 
     constexpr int NB = Smem<HDKV>::NB;
+    constexpr int NP = Smem<HDKV>::NP;
     if (warp == kProducerWarp) {
         if (lane == 0 && n_tiles > 0) {
             mbar_expect_tx(&sm.bar_q, kQBytes);
@@ -268,58 +327,88 @@ __global__ void __launch_bounds__(kThreadsP, 1)
             };
             if (kTmaK)
                 for (int j = 0; j < NB && j < n_tiles; ++j) load_k(j);
-            for (int i = 0; i < n_tiles; ++i) {
-                const int b = i % NB;
-                // S = Q K^T once the softmax warps have split Q (first tile) and this K tile
-                if (!mbar_wait(&sm.bar_kk, i & 1, abort_flag, a.err)) break;
+            // Descriptors of every operand slab, built once: a K step of 8 (32 bytes) moves
+            // the start-address field (address / 16) by 2 within a 1024-aligned slab.
+            uint64_t dq[2][HDKV / 32], dk[NB][2][HDKV / 32], dp[NP][2][BN / 32], dv[NB][2][BN / 32];
+#pragma unroll
+            for (int c = 0; c < HDKV / 32; ++c) {
+                dq[0][c] = sw128_desc(su32(sm.qh[c]));
+                dq[1][c] = sw128_desc(su32(sm.ql[c]));
+#pragma unroll
+                for (int b = 0; b < NB; ++b) {
+                    dk[b][0][c] = sw128_desc(su32(sm.kh[b][c]));
+                    dk[b][1][c] = sw128_desc(su32(sm.kl[b][c]));
+                }
+            }
+#pragma unroll
+            for (int c = 0; c < BN / 32; ++c) {
+#pragma unroll
+                for (int b = 0; b < NP; ++b) {
+                    dp[b][0][c] = sw128_desc(su32(sm.ph[b][c]));
+                    dp[b][1][c] = sw128_desc(su32(sm.pl[b][c]));
+                }
+#pragma unroll
+                for (int b = 0; b < NB; ++b) {
+                    dv[b][0][c] = sw128_desc(su32(sm.vh[b][c]));
+                    dv[b][1][c] = sw128_desc(su32(sm.vl[b][c]));
+                }
+            }
+            constexpr uint32_t kIdS = tf32_idesc(BM, BN), kIdO = tf32_idesc(BM, HDKV);
+            // S(j) = Q K(j)^T into S buffer j % 2 (Q and K tile j split by then)
+            auto issue_s = [&](int j) {
+                const int b = j % NB;
                 tc_fence_after();
 #pragma unroll
                 for (int kk = 0; kk < HDKV / 8; ++kk) {
-                    const uint32_t off = (kk & 3) * 32;
-                    const uint64_t qh = sw128_desc(su32(sm.qh[kk >> 2]) + off);
-                    const uint64_t ql = sw128_desc(su32(sm.ql[kk >> 2]) + off);
-                    const uint64_t kh = sw128_desc(su32(sm.kh[b][kk >> 2]) + off);
-                    const uint64_t kl = sw128_desc(su32(sm.kl[b][kk >> 2]) + off);
-                    mma_tf32(tmem, qh, kh, tf32_idesc(BM, BN), kk > 0);
-                    mma_tf32(tmem, qh, kl, tf32_idesc(BM, BN), 1);
-                    mma_tf32(tmem, ql, kh, tf32_idesc(BM, BN), 1);
+                    const uint64_t o = 2 * (kk & 3);
+                    const int c = kk >> 2;
+                    // (buffer chosen by selects: a run-time index would move the array to local memory)
+                    const uint64_t kh = (NB == 2 && b) ? dk[NB - 1][0][c] : dk[0][0][c];
+                    const uint64_t kl = (NB == 2 && b) ? dk[NB - 1][1][c] : dk[0][1][c];
+                    mma3_tf32(tmem + s_col(j), dq[0][c] + o, dq[1][c] + o, kh + o, kl + o, kIdS, kk > 0);
                 }
-                mma_commit(&sm.bar_s);
+                mma_commit(&sm.bar_s[j & 1]);
+            };
+            bool ok = mbar_wait(&sm.bar_qs, 0, abort_flag, a.err) && mbar_wait(&sm.bar_kk[0], 0, abort_flag, a.err);
+            if (ok) issue_s(0);
+            for (int i = 0; ok && i < n_tiles; ++i) {
+                // K buffer i % NB is free once S(i) is complete: the copy of key tile i + NB
                 if (kTmaK && i + NB < n_tiles) {
-                    // the K buffer is free once S(i) is complete
-                    if (!mbar_wait(&sm.bar_s, i & 1, abort_flag, a.err)) break;
+                    if (!mbar_wait(&sm.bar_s[i & 1], (i >> 1) & 1, abort_flag, a.err)) break;
                     load_k(i + NB);
                 }
-                // O_t = P V once P(i) is written and V^T(i) staged
-                if (!mbar_wait(&sm.bar_p, i & 1, abort_flag, a.err)) break;
-                if (!mbar_wait(&sm.bar_vv, i & 1, abort_flag, a.err)) break;
+                // S(i+1) ahead of O_t(i): its S buffer last held S(i-1), whose P(i-1) this thread
+                // saw published before O_t(i-1)
+                if (i + 1 < n_tiles) {
+                    const int j = i + 1;
+                    if (!mbar_wait(&sm.bar_kk[j % NB], (j / NB) & 1, abort_flag, a.err)) break;
+                    issue_s(j);
+                }
+                // O_t(i) = P(i) V(i) into O buffer i % 2 once P(i) is published and V^T(i) staged
+                if (!mbar_wait(&sm.bar_p[i & 1], (i >> 1) & 1, abort_flag, a.err)) break;
+                if (!mbar_wait(&sm.bar_vv[i % NB], (i / NB) & 1, abort_flag, a.err)) break;
                 tc_fence_after();
+                const int b = i % NB, pb = i % NP;
 #pragma unroll
                 for (int kk = 0; kk < BN / 8; ++kk) {
-                    const uint32_t off = (kk & 3) * 32;
-                    const uint64_t ph = sw128_desc(su32(sm.ph[kk >> 2]) + off);
-                    const uint64_t pl = sw128_desc(su32(sm.pl[kk >> 2]) + off);
-                    const uint64_t vh = sw128_desc(su32(sm.vh[b][kk >> 2]) + off);
-                    const uint64_t vl = sw128_desc(su32(sm.vl[b][kk >> 2]) + off);
-                    mma_tf32(tmem + kOCol, ph, vh, tf32_idesc(BM, HDKV), kk > 0);
-                    mma_tf32(tmem + kOCol, ph, vl, tf32_idesc(BM, HDKV), 1);
-                    mma_tf32(tmem + kOCol, pl, vh, tf32_idesc(BM, HDKV), 1);
+                    const uint64_t o = 2 * (kk & 3);
+                    const int c = kk >> 2;
+                    const uint64_t ph = (NP == 2 && pb) ? dp[NP - 1][0][c] : dp[0][0][c];
+                    const uint64_t pl = (NP == 2 && pb) ? dp[NP - 1][1][c] : dp[0][1][c];
+                    const uint64_t vh = (NB == 2 && b) ? dv[NB - 1][0][c] : dv[0][0][c];
+                    const uint64_t vl = (NB == 2 && b) ? dv[NB - 1][1][c] : dv[0][1][c];
+                    mma3_tf32(tmem + o_col<HDKV>(i), ph + o, pl + o, vh + o, vl + o, kIdO, kk > 0);
                 }
-                mma_commit(&sm.bar_o);
+                mma_commit(&sm.bar_o[i & 1]);
             }
         }
-    } else {
-        // softmax and epilogue: thread tid owns query row tid (TMEM lane tid)
-        const uint32_t trow = tmem + (static_cast<uint32_t>(warp * 32) << 16);
-        const float sl = a.scale_log2;
-        float o[HDKV];
-#pragma unroll
-        for (int d = 0; d < HDKV; ++d) o[d] = 0.0f;
-        float m = -INFINITY, l = 0.0f;
-        const int vk = tid & (BN - 1), vq = tid / BN;  // V^T staging: key, quarter of the dims
+    } else if (warp >= kStageWarp0) {
+        // staging: K tiles split into TF32 halves, V tiles transposed and split (K-major)
+        const int st = tid - (kSoftThreads + 32);  // 0 .. kStageThreads-1
+        const int vk = st & (BN - 1), vq = st / BN;  // key of the tile, half of the dims
+        constexpr int kV4 = HDKV / 8;                // float4 of a V row per thread
         // This thread's slice of the next V tile is loaded one tile ahead, so its latency
-        // overlaps the current tile's products and softmax.
-        constexpr int kV4 = HDKV / 16;
+        // overlaps the current tile's work.
         float4 vnext[kV4];
         // element group d4 (4 values) of this kv head in region row `key` (dequantized for Q8_0)
         auto kv4 = [&](const void *reg, int key, int d4) -> float4 {
@@ -342,11 +431,16 @@ __global__ void __launch_bounds__(kThreadsP, 1)
             const int b = j % NB;
             if (kTmaK) {
                 if (!mbar_wait(&sm.bar_k[b], (j / NB) & 1, abort_flag, a.err)) return false;
-                split_region(&sm.kh[b][0][0], &sm.kl[b][0][0], BN * HDKV / 4, tid);
+                split_region(&sm.kh[b][0][0], &sm.kl[b][0][0], BN * HDKV / 4, st, kStageThreads);
             } else {
+                // the buffer last held key tile j - NB: S(j - NB) must have read it
+                if (j >= NB) {
+                    if (!mbar_wait(&sm.bar_s[(j - NB) & 1], ((j - NB) >> 1) & 1, abort_flag, a.err)) return false;
+                    tc_fence_after();
+                }
                 const int key = (tile0 + j) * BN + vk;
 #pragma unroll 4
-                for (int d4 = vq * (HDKV / 16); d4 < (vq + 1) * (HDKV / 16); ++d4) {
+                for (int d4 = vq * kV4; d4 < (vq + 1) * kV4; ++d4) {
                     const float4 kv = key < lmax ? kv4(a.k_reg, key, d4) : make_float4(0.f, 0.f, 0.f, 0.f);
                     const float kk[4] = {kv.x, kv.y, kv.z, kv.w};
 #pragma unroll
@@ -362,12 +456,16 @@ __global__ void __launch_bounds__(kThreadsP, 1)
             }
             fence_async_smem();  // split K -> visible to the tensor cores
             tc_fence_before();
-            mbar_arrive(&sm.bar_kk);
+            mbar_arrive(&sm.bar_kk[b]);
             return true;
         };
-        // V tile j (held in vnext) -> V^T hi/lo in buffer j % NB (K-major, keys along K)
-        auto stage_v = [&](int j) {
+        // V tile j (held in vnext) -> V^T hi/lo in buffer j % NB, once O_t(j - NB) has read it
+        auto stage_v = [&](int j) -> bool {
             const int b = j % NB;
+            if (j >= NB) {
+                if (!mbar_wait(&sm.bar_o[(j - NB) & 1], ((j - NB) >> 1) & 1, abort_flag, a.err)) return false;
+                tc_fence_after();
+            }
             unsigned char *vth = reinterpret_cast<unsigned char *>(sm.vh[b][vk >> 5]);
             unsigned char *vtl = reinterpret_cast<unsigned char *>(sm.vl[b][vk >> 5]);
 #pragma unroll
@@ -385,27 +483,60 @@ __global__ void __launch_bounds__(kThreadsP, 1)
             }
             fence_async_smem();  // V^T -> visible to the tensor cores
             tc_fence_before();
-            mbar_arrive(&sm.bar_vv);
+            mbar_arrive(&sm.bar_vv[b]);
             if (j + 1 < n_tiles) load_v(tile0 + j + 1);
+            return true;
         };
-        // Order per tile i: P(i) from S(i); then K(i+1) (and, with two buffers, V^T(i+1)) staged
-        // while the tensor cores form O_t(i), so S(i+1) can follow O_t(i) at once; then O += O_t.
+        // K runs a tile ahead of V where there are two buffers (S(i+1) is issued before O_t(i));
+        // with one buffer, K(i+1) can only land once S(i) is complete, so V(i) goes first.
         bool ok = n_tiles > 0;
         if (ok) {
             load_v(tile0);
-            ok = mbar_wait(&sm.bar_q, 0, abort_flag, a.err);
-        }
-        if (ok) {
-            split_region(&sm.qh[0][0], &sm.ql[0][0], BM * HDKV / 4, tid);
             ok = stage_k(0);
         }
-        if (ok) stage_v(0);
+        for (int i = 0; ok && i < n_tiles; ++i) {
+            if (NB == 2 && i + 1 < n_tiles && !stage_k(i + 1)) break;
+            if (!stage_v(i)) break;
+            if (NB == 1 && i + 1 < n_tiles && !stage_k(i + 1)) break;
+        }
+    } else {
+        // softmax and epilogue: thread tid owns query row tid (TMEM lane tid)
+        const uint32_t trow = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+        const float sl = a.scale_log2;
+        float o[HDKV];
+#pragma unroll
+        for (int d = 0; d < HDKV; ++d) o[d] = 0.0f;
+        float m = -INFINITY, l = 0.0f;
+        float corr_prev = 1.0f;  // the correction that goes with O_t(i-1)
+        // o = o * c + O_t(j), from O buffer j % 2
+        auto fold_o = [&](int j, float c) {
+#pragma unroll
+            for (int cc = 0; cc < HDKV / 32; ++cc) {
+                float r[32];
+                tmem_ld32(trow + o_col<HDKV>(j) + 32 * cc, r);
+#pragma unroll
+                for (int e = 0; e < 32; ++e) o[32 * cc + e] = fmaf(o[32 * cc + e], c, r[e]);
+            }
+        };
+        bool ok = n_tiles > 0;
+        if (ok) ok = mbar_wait(&sm.bar_q, 0, abort_flag, a.err);
+        if (ok) {
+            split_region(&sm.qh[0][0], &sm.ql[0][0], BM * HDKV / 4, tid, kSoftThreads);
+            fence_async_smem();  // split Q -> visible to the tensor cores
+            tc_fence_before();
+            mbar_arrive(&sm.bar_qs);
+        }
+        // Per tile i: P(i) from S(i), published; then O_t(i-1) folded in while the tensor
+        // cores form O_t(i) and S(i+1).
         for (int i = 0; ok && i < n_tiles; ++i) {
             const int j0 = (tile0 + i) * BN;
-            if (!mbar_wait(&sm.bar_s, i & 1, abort_flag, a.err)) break;
+            if (!mbar_wait(&sm.bar_s[i & 1], (i >> 1) & 1, abort_flag, a.err)) {
+                ok = false;
+                break;
+            }
             tc_fence_after();
             float r[32];
-            tmem_ld32(trow, r);
+            tmem_ld32(trow + s_col(i), r);
             float mx = -INFINITY;
 #pragma unroll
             for (int e = 0; e < 32; ++e)
@@ -413,9 +544,14 @@ __global__ void __launch_bounds__(kThreadsP, 1)
             const float m_new = fmaxf(m, mx);
             const bool none = (m_new == -INFINITY);  // no key visible to this row yet
             const float corr = none ? 1.0f : ex2_approx(m - m_new);
+            // one P buffer: O_t(i-1) must have read P(i-1) before it is overwritten
+            if (NP == 1 && i > 0 && !mbar_wait(&sm.bar_o[(i - 1) & 1], ((i - 1) >> 1) & 1, abort_flag, a.err)) {
+                ok = false;
+                break;
+            }
             float ps = 0.0f;
-            unsigned char *pph = reinterpret_cast<unsigned char *>(sm.ph[0]);
-            unsigned char *ppl = reinterpret_cast<unsigned char *>(sm.pl[0]);
+            unsigned char *pph = reinterpret_cast<unsigned char *>(sm.ph[i % NP][0]);
+            unsigned char *ppl = reinterpret_cast<unsigned char *>(sm.pl[i % NP][0]);
 #pragma unroll
             for (int e4 = 0; e4 < 8; ++e4) {
                 float4 wh, wl;
@@ -434,21 +570,24 @@ __global__ void __launch_bounds__(kThreadsP, 1)
             m = m_new;
             fence_async_smem();  // P hi/lo -> visible to the tensor cores
             tc_fence_before();
-            mbar_arrive(&sm.bar_p);
-            if (i + 1 < n_tiles) {
-                if (!stage_k(i + 1)) break;
-                if (NB == 2) stage_v(i + 1);  // its buffer was last read by O_t(i - 1)
+            mbar_arrive(&sm.bar_p[i & 1]);
+            if (i > 0) {
+                if (!mbar_wait(&sm.bar_o[(i - 1) & 1], ((i - 1) >> 1) & 1, abort_flag, a.err)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                fold_o(i - 1, corr_prev);
+                tc_fence_before();  // the O buffer is read before the next P lets O_t(i+1) overwrite it
             }
-            if (!mbar_wait(&sm.bar_o, i & 1, abort_flag, a.err)) break;
-            tc_fence_after();
-#pragma unroll
-            for (int c = 0; c < HDKV / 32; ++c) {
-                tmem_ld32(trow + kOCol + 32 * c, r);
-#pragma unroll
-                for (int e = 0; e < 32; ++e) o[32 * c + e] = fmaf(o[32 * c + e], corr, r[e]);
+            corr_prev = corr;
+        }
+        if (ok) {  // the last tile's O_t
+            const int j = n_tiles - 1;
+            if (mbar_wait(&sm.bar_o[j & 1], (j >> 1) & 1, abort_flag, a.err)) {
+                tc_fence_after();
+                fold_o(j, corr_prev);
             }
-            tc_fence_before();
-            if (NB == 1 && i + 1 < n_tiles) stage_v(i + 1);  // one buffer: after O_t(i) has read it
         }
         bool write_out = true;
         if (n_act > 1) {
@@ -509,7 +648,7 @@ __global__ void __launch_bounds__(kThreadsP, 1)
             }
         }
         __syncwarp();
-        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols)
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(tmem_cols<HDKV>())
                      : "memory");
     }
 }

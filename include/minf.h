@@ -233,7 +233,10 @@ MINF_API size_t minf_attn_prefill_workspace_bytes(int nt, int n_head, int n_kv_h
  * begins streaming the cached rows [0, pos) of the regions before the launch just before
  * it on the stream has finished (h, gain, q, k, v, ws and every output only after): pos
  * and those rows must not be written by that launch (a host-to-device copy is not a
- * launch).  The nt > 1 path starts early only after its own first launch.
+ * launch).  For nt > 1 the first launch (RMSNorm, RoPE and the store) is a programmatic
+ * dependent launch too; it touches memory only once the launch before it has finished, but
+ * the attention launch after it reads pos as soon as every block of the first has started:
+ * pos must not be written by the launch just before the step on either path.
  * Device errors: any of the bits above.
  */
 MINF_API int minf_layer_attn_step(float *xn, const float *h, const float *gain, float eps, int n_embd,
