@@ -158,7 +158,7 @@ struct PParams {
     int nt, nh, nk, hd, cap, W;
     int n_qt, n_kc, kc_tiles;  // query tiles, key chunks per query tile, key tiles per chunk
     float scale_log2;
-    float *ws_o, *ws_ml;       // chunk partials: o as [.., d][row], (m, l) as [.., 2][row]
+    float *ws_o, *ws_ml;       // chunk partials: o as [.., d/4][row] of float4, (m, l) as [.., 2][row]
     int *ws_ticket;            // one per (query tile, head)
 };
 
@@ -229,9 +229,9 @@ __device__ __forceinline__ void pair_of(int idx, int n_qt, int n_kc, int &qt, in
     qt = 0;
 }
 
-// fp32 regions: K tiles arrive by TMA into kh and are split in place.  binary16 regions: the
-// softmax threads read the K tile themselves, converting, and write both halves (a binary16
-// value is exact in TF32, so its low half is zero).
+// fp32 regions: K tiles arrive by TMA into kh and are split in place.  binary16 and Q8_0
+// regions: the staging warps read the K tile themselves, converting, and write both halves (a
+// binary16 value is exact in TF32, so its low half is zero).
 template <int HDKV, typename T>
 __global__ void __launch_bounds__(kThreadsP, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -597,7 +597,9 @@ __global__ void __launch_bounds__(kThreadsP, 1)
             float *po = a.ws_o + (blk + kc) * HDKV * BM;
             float *pml = a.ws_ml + (blk + kc) * 2 * BM;
 #pragma unroll
-            for (int d = 0; d < HDKV; ++d) po[d * BM + tid] = o[d];
+            for (int d4 = 0; d4 < HDKV / 4; ++d4)  // float4 of dims, rows adjacent: coalesced vector access
+                reinterpret_cast<float4 *>(po)[d4 * BM + tid] =
+                    make_float4(o[4 * d4], o[4 * d4 + 1], o[4 * d4 + 2], o[4 * d4 + 3]);
             pml[tid] = m;
             pml[BM + tid] = l;
             named_sync(1, kSoftThreads);
@@ -612,29 +614,67 @@ __global__ void __launch_bounds__(kThreadsP, 1)
             named_sync(1, kSoftThreads);
             write_out = sm.lmax == -1;
             if (write_out) {
-                for (int c = 0; c < n_act; ++c) {
-                    if (c == kc) continue;
-                    const float *qo = a.ws_o + (blk + c) * HDKV * BM;
-                    const float *qml = a.ws_ml + (blk + c) * 2 * BM;
-                    const float mc = __ldcg(qml + tid), lc = __ldcg(qml + BM + tid);
-                    const float mn = fmaxf(m, mc);
-                    const float fa = m == -INFINITY ? 0.0f : ex2_approx(m - mn);
-                    const float fb = mc == -INFINITY ? 0.0f : ex2_approx(mc - mn);
+                // The (max, sum) pairs of every chunk first, in one round trip, so the combined
+                // max and every chunk's factor are known before the partial outputs are read;
+                // then each chunk's outputs, scaled, are added (at most 16 chunks a tile).
+                constexpr int kMaxKc = 16;
+                float mcs[kMaxKc], lcs[kMaxKc];
 #pragma unroll
-                    for (int d = 0; d < HDKV; ++d) o[d] = fmaf(o[d], fa, __ldcg(qo + d * BM + tid) * fb);
-                    l = fmaf(l, fa, lc * fb);
-                    m = mn;
+                for (int c = 0; c < kMaxKc; ++c) {
+                    const bool use = c < n_act && c != kc;
+                    const float *qml = a.ws_ml + (blk + c) * 2 * BM;
+                    mcs[c] = use ? __ldcg(qml + tid) : -INFINITY;
+                    lcs[c] = use ? __ldcg(qml + BM + tid) : 0.0f;
                 }
+                float M = m;
+#pragma unroll
+                for (int c = 0; c < kMaxKc; ++c) M = fmaxf(M, mcs[c]);
+                const float fa = m == -INFINITY ? 0.0f : ex2_approx(m - M);
+                l *= fa;
+#pragma unroll
+                for (int d = 0; d < HDKV; ++d) o[d] *= fa;
+#pragma unroll
+                for (int c = 0; c < kMaxKc; ++c) {
+                    if (c < n_act && c != kc) {
+                        const float fb = mcs[c] == -INFINITY ? 0.0f : ex2_approx(mcs[c] - M);
+                        const float *qo = a.ws_o + (blk + c) * HDKV * BM;
+                        l = fmaf(lcs[c], fb, l);
+#pragma unroll
+                        for (int d4 = 0; d4 < HDKV / 4; ++d4) {
+                            const float4 x = __ldcg(reinterpret_cast<const float4 *>(qo) + d4 * BM + tid);
+                            o[4 * d4] = fmaf(x.x, fb, o[4 * d4]);
+                            o[4 * d4 + 1] = fmaf(x.y, fb, o[4 * d4 + 1]);
+                            o[4 * d4 + 2] = fmaf(x.z, fb, o[4 * d4 + 2]);
+                            o[4 * d4 + 3] = fmaf(x.w, fb, o[4 * d4 + 3]);
+                        }
+                    }
+                }
+                m = M;
                 if (tid == 0) a.ws_ticket[static_cast<size_t>(qt) * a.nh + h] = 0;  // ready for reuse
             }
         }
-        if (write_out && t < a.nt && !*abort_flag) {
-            float4 *dst = reinterpret_cast<float4 *>(a.out + (static_cast<size_t>(t) * a.nh + h) * HDKV);
+        if (write_out) {  // the same in every softmax thread
+            // Rows pass through shared memory (the Q slabs: every S has completed) so that each
+            // warp writes whole output rows, which lie n_head*hd_kv floats apart.
+            constexpr int kRS = HDKV + 4;  // padded row stride in floats (no bank conflicts)
+            static_assert(BM * kRS <= 2 * HDKV * BM, "staging fits the Q slabs");
+            float *stg = &sm.qh[0][0];
             const float inv = l > 0.0f ? 1.0f / l : 0.0f;
 #pragma unroll
             for (int d4 = 0; d4 < HDKV / 4; ++d4)
-                dst[d4] = make_float4(o[4 * d4] * inv, o[4 * d4 + 1] * inv, o[4 * d4 + 2] * inv,
-                                      o[4 * d4 + 3] * inv);
+                reinterpret_cast<float4 *>(stg + tid * kRS)[d4] =
+                    make_float4(o[4 * d4] * inv, o[4 * d4 + 1] * inv, o[4 * d4 + 2] * inv, o[4 * d4 + 3] * inv);
+            named_sync(1, kSoftThreads);
+            constexpr int kF4 = HDKV / 4;       // float4 of a row
+            constexpr int kRowsPer = 32 / kF4;  // rows a warp writes per instruction
+            if (!*abort_flag)
+#pragma unroll 4
+                for (int r0 = warp * 32; r0 < warp * 32 + 32; r0 += kRowsPer) {
+                    const int r = r0 + lane / kF4, c = lane % kF4;
+                    if (t0 + r < a.nt)
+                        reinterpret_cast<float4 *>(a.out + (static_cast<size_t>(t0 + r) * a.nh + h) * HDKV)[c] =
+                            reinterpret_cast<const float4 *>(stg + r * kRS)[c];
+                }
         }
     }
     tc_fence_before();
