@@ -96,6 +96,20 @@ def test_prefill_repeated_calls_reuse_the_workspace(m, orc):
               f"long-window prefill {nt}")
 
 
+def test_prefill_long_windows_hd64(m, orc):
+    """hd_kv 64 (two K, V^T and P buffers) with windows of 1449..2048 keys: 12 to 16 key chunks
+    per query tile, all folded by the last chunk to arrive."""
+    nh, nk, hd, cap, nt = 8, 2, 64, 2048, 600
+    K = rnd((cap, nk * hd), 21)
+    V = rnd((cap, nk * hd), 22)
+    q = rnd((nt, nh, hd), 23)
+    pos = np.arange(cap - nt, cap, dtype=np.int32)
+    got, err, scale = run_prefill(m, q, K, V, pos, nh, nk, hd, hd)
+    assert err == 0
+    check(got, orc.gqa_attn(q.numpy(), K.numpy(), V.numpy(), pos, nh, nk, hd, hd, scale=scale, n_threads=8),
+          "long-window prefill hd_kv 64")
+
+
 def test_prefill_scattered_positions_and_bad_ones(m, orc):
     nh, nk, hd, cap = 8, 2, 64, 150
     K = rnd((cap, nk * hd), 8)
