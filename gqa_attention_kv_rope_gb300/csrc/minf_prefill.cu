@@ -23,7 +23,8 @@
 // swizzle); Q is split in place by the softmax threads, K by two staging warps, which also
 // transpose and split V into the K-major layout the MMA takes.  These are generic-proxy writes,
 // fenced to the async proxy before the MMA that reads them is released.  Warp 4 is the
-// producer: one elected thread issues the TMA copies, the MMAs and the commits.
+// producer: one elected thread issues the TMA copies and the S products; warp 7's first thread
+// issues the P*V products (each thread commits its own).
 //
 // Pipelining.  S has two TMEM buffers and the producer issues S(i+1) as soon as key tile i+1
 // is split, ahead of P(i)V(i), so the tensor cores form the next scores while the softmax
@@ -55,7 +56,8 @@ constexpr int kSoftThreads = 128;    // warps 0-3: TMEM lanes 0..127, one query 
 constexpr int kProducerWarp = 4;
 constexpr int kStageWarp0 = 5;       // warps 5-6: K split, V^T staging
 constexpr int kStageThreads = 64;
-constexpr int kThreadsP = kSoftThreads + 32 + kStageThreads;
+constexpr int kPvWarp = 7;           // issues the P*V products
+constexpr int kThreadsP = kSoftThreads + 32 + kStageThreads + 32;
 // TMEM: S(i) at column (i % 2) * BN, O_t(i) at column 128 + (i % 2) * HDKV
 template <int HDKV>
 constexpr uint32_t tmem_cols() { return 128 + 2 * HDKV <= 256 ? 256 : 512; }
@@ -329,7 +331,7 @@ __global__ void __launch_bounds__(kThreadsP, 1)
                 for (int j = 0; j < NB && j < n_tiles; ++j) load_k(j);
             // Descriptors of every operand slab, built once: a K step of 8 (32 bytes) moves
             // the start-address field (address / 16) by 2 within a 1024-aligned slab.
-            uint64_t dq[2][HDKV / 32], dk[NB][2][HDKV / 32], dp[NP][2][BN / 32], dv[NB][2][BN / 32];
+            uint64_t dq[2][HDKV / 32], dk[NB][2][HDKV / 32];
 #pragma unroll
             for (int c = 0; c < HDKV / 32; ++c) {
                 dq[0][c] = sw128_desc(su32(sm.qh[c]));
@@ -340,20 +342,7 @@ __global__ void __launch_bounds__(kThreadsP, 1)
                     dk[b][1][c] = sw128_desc(su32(sm.kl[b][c]));
                 }
             }
-#pragma unroll
-            for (int c = 0; c < BN / 32; ++c) {
-#pragma unroll
-                for (int b = 0; b < NP; ++b) {
-                    dp[b][0][c] = sw128_desc(su32(sm.ph[b][c]));
-                    dp[b][1][c] = sw128_desc(su32(sm.pl[b][c]));
-                }
-#pragma unroll
-                for (int b = 0; b < NB; ++b) {
-                    dv[b][0][c] = sw128_desc(su32(sm.vh[b][c]));
-                    dv[b][1][c] = sw128_desc(su32(sm.vl[b][c]));
-                }
-            }
-            constexpr uint32_t kIdS = tf32_idesc(BM, BN), kIdO = tf32_idesc(BM, HDKV);
+            constexpr uint32_t kIdS = tf32_idesc(BM, BN);
             // S(j) = Q K(j)^T into S buffer j % 2 (Q and K tile j split by then)
             auto issue_s = [&](int j) {
                 const int b = j % NB;
@@ -377,14 +366,37 @@ __global__ void __launch_bounds__(kThreadsP, 1)
                     if (!mbar_wait(&sm.bar_s[i & 1], (i >> 1) & 1, abort_flag, a.err)) break;
                     load_k(i + NB);
                 }
-                // S(i+1) ahead of O_t(i): its S buffer last held S(i-1), whose P(i-1) this thread
-                // saw published before O_t(i-1)
+                // S(i+1) ahead of O_t(i): its S buffer last held S(i-1), read before P(i-1) was
+                // published
                 if (i + 1 < n_tiles) {
                     const int j = i + 1;
+                    if (j >= 2 && !mbar_wait(&sm.bar_p[j & 1], ((j - 2) >> 1) & 1, abort_flag, a.err)) break;
                     if (!mbar_wait(&sm.bar_kk[j % NB], (j / NB) & 1, abort_flag, a.err)) break;
                     issue_s(j);
                 }
-                // O_t(i) = P(i) V(i) into O buffer i % 2 once P(i) is published and V^T(i) staged
+            }
+        }
+    } else if (warp == kPvWarp) {
+        // O_t(i) = P(i) V(i) into O buffer i % 2 once P(i) is published and V^T(i) staged, from
+        // a second thread: one thread issues a tensor-core instruction only every ~35-50 ns, and
+        // S(i+1) and O_t(i) need not wait behind each other's issue
+        if (lane == 0 && n_tiles > 0) {
+            uint64_t dp[NP][2][BN / 32], dv[NB][2][BN / 32];
+#pragma unroll
+            for (int c = 0; c < BN / 32; ++c) {
+#pragma unroll
+                for (int b = 0; b < NP; ++b) {
+                    dp[b][0][c] = sw128_desc(su32(sm.ph[b][c]));
+                    dp[b][1][c] = sw128_desc(su32(sm.pl[b][c]));
+                }
+#pragma unroll
+                for (int b = 0; b < NB; ++b) {
+                    dv[b][0][c] = sw128_desc(su32(sm.vh[b][c]));
+                    dv[b][1][c] = sw128_desc(su32(sm.vl[b][c]));
+                }
+            }
+            constexpr uint32_t kIdO = tf32_idesc(BM, HDKV);
+            for (int i = 0; i < n_tiles; ++i) {
                 if (!mbar_wait(&sm.bar_p[i & 1], (i >> 1) & 1, abort_flag, a.err)) break;
                 if (!mbar_wait(&sm.bar_vv[i % NB], (i / NB) & 1, abort_flag, a.err)) break;
                 tc_fence_after();
