@@ -27,8 +27,10 @@
 // issues the P*V products (each thread commits its own).
 //
 // Pipelining.  S has two TMEM buffers and the producer issues S(i+1) as soon as key tile i+1
-// is split, ahead of P(i)V(i), so the tensor cores form the next scores while the softmax
-// warps work on the current ones.  O_t has two TMEM buffers as well: the softmax warps publish
+// is split (and P(i-1) has been published, so S(i-1)'s buffer is free), without waiting for
+// P(i)V(i), which the other thread issues: the tensor cores form the next scores while the
+// softmax warps work on the current ones, and neither product waits behind the other's issue
+// (a thread issues a tensor-core instruction only every ~35-50 ns).  O_t has two TMEM buffers as well: the softmax warps publish
 // P(i) first and fold O_t(i-1) into their registers after it, while the tensor cores form
 // O_t(i) (with hd_kv 64 P also has two buffers in shared memory; with hd_kv 128, where shared
 // memory holds one, P(i) waits until O_t(i-1) has read P(i-1)).
