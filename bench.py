@@ -89,6 +89,75 @@ def barrier(world: int):
 
 
 # ----------------------------------------------------------------------------- clocks
+class NvmlClockSampler:
+    """Samples the SM clock and the clock-event reasons through NVML (the driver's
+    libnvidia-ml, read-only queries) every ~2 ms on a thread while the timed region runs, so
+    that even a timed region of a few tens of milliseconds is covered."""
+
+    # clock-event reason bits of the NVML API
+    REASONS = {0x8: "hw_slowdown", 0x40: "hw_thermal_slowdown", 0x20: "sw_thermal_slowdown", 0x4: "sw_power_cap"}
+    GPU_IDLE = 0x1
+
+    def __init__(self, gpu_id: str):
+        import ctypes
+        import threading
+
+        self.ct = ctypes
+        lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if lib.nvmlInit_v2() != 0:
+            raise OSError("nvmlInit failed")
+        self.lib = lib
+        self.dev = ctypes.c_void_p()
+        if gpu_id.startswith(("GPU-", "MIG-")):
+            rc = lib.nvmlDeviceGetHandleByUUID(gpu_id.encode(), ctypes.byref(self.dev))
+        else:
+            rc = lib.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(int(gpu_id)), ctypes.byref(self.dev))
+        if rc != 0:
+            raise OSError("no NVML handle for GPU " + gpu_id)
+        self.reasons_fn = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            lib.nvmlDeviceGetCurrentClocksThrottleReasons
+        mx = ctypes.c_uint()
+        lib.nvmlDeviceGetMaxClockInfo(self.dev, 1, ctypes.byref(mx))  # 1: the SM clock
+        self.max_mhz = float(mx.value)
+        self.samples = []
+        self.stop = threading.Event()
+        self.thread = threading.Thread(target=self._run, daemon=True)
+
+    def _run(self):
+        ct = self.ct
+        clk, rs = ct.c_uint(), ct.c_ulonglong()
+        while not self.stop.is_set():
+            if self.lib.nvmlDeviceGetClockInfo(self.dev, 1, ct.byref(clk)) == 0 and \
+                    self.reasons_fn(self.dev, ct.byref(rs)) == 0:
+                self.samples.append((float(clk.value), int(rs.value)))
+            time.sleep(0.002)
+
+    def __enter__(self):
+        self.thread.start()
+        return self
+
+    def __exit__(self, *exc):
+        self.stop.set()
+        self.thread.join(timeout=5)
+        self.lib.nvmlShutdown()
+
+    def summary(self):
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": ["unsampled"], "source": "nvml"}
+        busy = [s for s in self.samples if not s[1] & self.GPU_IDLE] or self.samples
+        reasons = sorted({n for s in busy for bit, n in self.REASONS.items() if s[1] & bit})
+        return {"sm_mhz": statistics.median(s[0] for s in busy), "sm_max_mhz": self.max_mhz, "reasons": reasons,
+                "samples": len(busy), "source": "nvml"}
+
+
+def clock_sampler(gpu_id: str):
+    """NVML sampling where the driver's library loads, else nvidia-smi at 100 ms."""
+    try:
+        return NvmlClockSampler(gpu_id)
+    except (OSError, AttributeError, ValueError):
+        return ClockSampler(gpu_id)
+
+
 class ClockSampler:
     """Samples SM clocks and throttle reasons with nvidia-smi while the timed region runs."""
 
@@ -146,7 +215,7 @@ class ClockSampler:
         loaded = [s for s in sm if s > 0.5 * (max(mx) if mx else 1)] or sm
         return {"sm_mhz": statistics.median(loaded) if loaded else None,
                 "sm_max_mhz": max(mx) if mx else None, "reasons": sorted(reasons),
-                "samples": len(rows)}
+                "samples": len(rows), "source": "nvidia-smi"}
 
 
 # ----------------------------------------------------------------------------- helpers
@@ -296,7 +365,7 @@ def run_headline(m, torch, wl, args, world, dev):
     torch.cuda.synchronize()
     barrier(world)
     t0, t1 = Timer(torch, stream).pair()
-    with ClockSampler(smi_gpu_id(torch.cuda.current_device())) as clk:
+    with clock_sampler(smi_gpu_id(torch.cuda.current_device())) as clk:
         torch.cuda.synchronize()
         barrier(world)
         with torch.cuda.stream(stream):
