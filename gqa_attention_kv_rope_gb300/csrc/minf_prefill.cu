@@ -10,17 +10,20 @@
 // of 32 up to the largest window among its tokens.  The chunks of a query tile run in separate
 // CTAs; each writes its rows' (max, sum, output) partials and the last chunk to arrive (an
 // atomic ticket) folds them, so a long causal window is spread over many SMs.  Per key tile:
-//   S  = Q K^T        tcgen05.mma kind::tf32, M=128 N=32 K=hd_kv, fp32 accumulator in TMEM
+//   S  = Q K^T        tcgen05.mma kind::f16, M=128 N=32 K=hd_kv, fp32 accumulator in TMEM
 //   softmax            CUDA cores: one thread per query row reads its S row from TMEM,
 //                      masks keys beyond its window, updates its running max and sum, and
 //                      writes P = 2^(s*scale*log2e - m) into shared memory
 //   O_t = P V          tcgen05.mma kind::tf32, M=128 N=hd_kv K=32, into a second TMEM range
 //   O  = O*corr + O_t  in registers
-// Precision: every operand is split into two TF32 halves, x = hi + lo (hi = x rounded to
-// TF32, lo = the remainder rounded to TF32), and each product is the sum of three MMAs
-// hi*hi + hi*lo + lo*hi (the split-precision "3xTF32" scheme), which brings the tensor-core
-// result to fp32 accuracy.  Q and K tiles arrive by TMA (cp.async.bulk.tensor, 128-byte
-// swizzle); Q is split in place by the softmax threads, K by two staging warps, which also
+// Precision: every operand is split into two halves, x = hi + lo, and each product is the sum
+// of three MMAs hi*hi + hi*lo + lo*hi, which brings the tensor-core result to fp32 accuracy.
+// For S the halves are binary16: each Q row and each K row is first scaled by a power of two
+// that puts its largest magnitude in [2^14, 2^15), so that both halves stay normal, and the
+// scales are undone exactly on S (K = 16 per instruction: half the instructions of TF32).  P
+// and V^T use TF32 halves (hi = x rounded to TF32, lo = the remainder rounded to TF32: the
+// split-precision "3xTF32" scheme).  Q and K tiles arrive by TMA (cp.async.bulk.tensor,
+// 128-byte swizzle); Q is converted by the softmax threads, K by two staging warps, which also
 // transpose and split V into the K-major layout the MMA takes.  These are generic-proxy writes,
 // fenced to the async proxy before the MMA that reads them is released.  Warp 4 is the
 // producer: one elected thread issues the TMA copies and the S products; warp 7's first thread
@@ -41,6 +44,7 @@
 #include <cuda_fp16.h>
 
 #include <cmath>
+#include <cstddef>
 #include <type_traits>
 
 #include "minf_common.cuh"
@@ -67,23 +71,46 @@ template <int HDKV>
 __device__ __forceinline__ uint32_t o_col(int i) { return 128u + static_cast<uint32_t>(i & 1) * HDKV; }
 __device__ __forceinline__ uint32_t s_col(int i) { return static_cast<uint32_t>(i & 1) * BN; }
 
-// Operands are held as hi + lo TF32 pairs (x = hi + lo to about 2^-22 relative): each
-// product is formed from three tensor-core MMAs, hi*hi + hi*lo + lo*hi, so the TF32 inputs
-// of the tensor core cost no accuracy beyond fp32 accumulation.
+// Operands are held as hi + lo pairs (x = hi + lo to about 2^-22 relative; binary16 halves of
+// scaled rows for Q and K, TF32 halves for P and V^T): each product is formed from three
+// tensor-core MMAs, hi*hi + hi*lo + lo*hi, so the narrow inputs of the tensor core cost no
+// accuracy beyond fp32 accumulation.
 // K and V^T tiles are double-buffered where shared memory allows (hd_kv 64): key tile j lives
 // in buffer j % NB.
 template <int HDKV>
 struct Smem {
     static constexpr int NB = HDKV == 64 ? 2 : 1;   // K and V^T tile buffers
     static constexpr int NP = HDKV == 64 ? 2 : 1;   // P buffers
-    float qh[HDKV / 32][BM * 32], ql[HDKV / 32][BM * 32];            // Q: 32-column SW128 slabs
-    float kh[NB][HDKV / 32][BN * 32], kl[NB][HDKV / 32][BN * 32];    // K tiles (TMA lands in kh)
+    // Q and K arrive by TMA as fp32 in qh and kh (32-column SW128 slabs); their binary16
+    // hi + lo halves (64-column SW128 slabs, hi then lo) are written into ql and kl
+    float qh[HDKV / 32][BM * 32], ql[HDKV / 32][BM * 32];
+    float kh[NB][HDKV / 32][BN * 32], kl[NB][HDKV / 32][BN * 32];
     float ph[NP][BN / 32][BM * 32], pl[NP][BN / 32][BM * 32];        // P: keys along K
     float vh[NB][BN / 32][HDKV * 32], vl[NB][BN / 32][HDKV * 32];    // V^T: keys along K
     unsigned long long bar_q, bar_k[NB], bar_qs, bar_kk[NB], bar_vv[NB], bar_s[2], bar_p[2], bar_o[2];
+    unsigned long long bar_ks[4];  // slot j % 4 of ks written (key tile j)
+    unsigned long long bar_m;      // merge: other chunks' partial outputs copied in
+    alignas(16) float ks[4][BN];  // per key of tile j (slot j % 4): the factor undoing its row's scale
     uint32_t tmem_base;
     int abort_flag;
     int lmax;
+};
+
+// After the last product of a CTA its shared memory is free.  The output rows are staged from
+// the start of qh (kStg bytes, padded rows); the merge of key chunks copies other chunks'
+// partial outputs (kPart bytes each) into the kN slots that follow, up to the end of vl.
+template <int HDKV>
+struct MergeSlots {
+    static constexpr int kRS = HDKV + 4;  // staged row stride in floats (no bank conflicts)
+    static constexpr size_t kStg = (static_cast<size_t>(BM) * kRS * 4 + 127) & ~static_cast<size_t>(127);
+    static constexpr size_t kPart = static_cast<size_t>(HDKV) * BM * 4;
+    static constexpr size_t kEnd = offsetof(Smem<HDKV>, vl) + sizeof(Smem<HDKV>::vl) - offsetof(Smem<HDKV>, qh);
+    static constexpr int kN = static_cast<int>((kEnd - kStg) / kPart);
+    static_assert(kEnd == sizeof(Smem<HDKV>::qh) + sizeof(Smem<HDKV>::ql) + sizeof(Smem<HDKV>::kh) +
+                              sizeof(Smem<HDKV>::kl) + sizeof(Smem<HDKV>::ph) + sizeof(Smem<HDKV>::pl) +
+                              sizeof(Smem<HDKV>::vh) + sizeof(Smem<HDKV>::vl),
+                  "qh .. vl are contiguous");
+    static_assert(kN >= 1, "one chunk's partials fit");
 };
 
 // Shared-memory matrix descriptor: K-major operand in the 128-byte swizzle layout
@@ -106,6 +133,59 @@ __host__ __device__ constexpr uint32_t tf32_idesc(int M, int N) {
 
 // One split-precision product step: D (+)= Ah*Bh + Ah*Bl + Al*Bh, three MMAs issued together
 // (the first accumulates into D only when `accumulate` is non-zero).
+// kind::f16 with binary16 A and B, fp32 accumulate, both K-major.
+__host__ __device__ constexpr uint32_t f16_idesc(int M, int N) {
+    return (1u << 4) | (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+// One split-precision product step on binary16 halves (K = 16): D (+)= Ah*Bh + Ah*Bl + Al*Bh.
+__device__ __forceinline__ void mma3_f16(uint32_t d_tmem, uint64_t ah, uint64_t al, uint64_t bh, uint64_t bl,
+                                         uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n .reg .pred p, t;\n setp.ne.b32 p, %5, 0;\n setp.ne.b32 t, %7, 0;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %3, %6, p;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %4, %6, t;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], %2, %3, %6, t;\n}" ::"r"(d_tmem),
+        "l"(ah), "l"(al), "l"(bh), "l"(bl), "r"(accumulate), "r"(idesc), "r"(1u)
+        : "memory");
+}
+
+// The scores' operands as binary16 halves.  A row (a query row of Q, a key row of K) is scaled
+// by a power of two that puts its largest magnitude in [2^14, 2^15); then hi = fp16(x*s) and
+// lo = fp16(x*s - hi) are both normal binary16 values for every element within 2^28 of that
+// largest one, and hi + lo carries x*s to about 2^-22 relative -- the accuracy of the TF32
+// split, at twice the K of a TF32 instruction.  The scale is exact and undone in fp32 on S.
+// Returns the factor 1/s (1 for a zero row).
+__device__ __forceinline__ float f16_row_scale(float amax, float &s) {
+    const int ex = static_cast<int>((__float_as_uint(amax) >> 23) & 0xff) - 127;  // floor(log2(amax))
+    int sh = amax > 0.0f ? 14 - ex : 0;
+    sh = sh > 126 ? 126 : (sh < -126 ? -126 : sh);
+    s = __uint_as_float(static_cast<uint32_t>(sh + 127) << 23);
+    return __uint_as_float(static_cast<uint32_t>(127 - sh) << 23);
+}
+
+// Eight scaled values -> eight hi and eight lo binary16 values (16 bytes each).
+__device__ __forceinline__ void f16_split8(const float (&x)[8], float s, uint4 &hi, uint4 &lo) {
+    uint32_t h[4], l[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float a = x[2 * i] * s, b = x[2 * i + 1] * s;
+        const __half ah = __float2half_rn(a), bh = __float2half_rn(b);
+        const __half al = __float2half_rn(a - __half2float(ah)), bl = __float2half_rn(b - __half2float(bh));
+        const __half2 hh = __halves2half2(ah, bh), ll = __halves2half2(al, bl);
+        h[i] = *reinterpret_cast<const uint32_t *>(&hh);
+        l[i] = *reinterpret_cast<const uint32_t *>(&ll);
+    }
+    hi = make_uint4(h[0], h[1], h[2], h[3]);
+    lo = make_uint4(l[0], l[1], l[2], l[3]);
+}
+
+// Byte offset of the 16-byte chunk holding binary16 elements 8c..8c+7 of `row` in a 64-column
+// SW128 slab (128-byte rows).
+__device__ __forceinline__ uint32_t sw128_off16(int row, int c) {
+    return static_cast<uint32_t>(row) * 128u + ((static_cast<uint32_t>(c) ^ static_cast<uint32_t>(row & 7)) << 4);
+}
+
 __device__ __forceinline__ void mma3_tf32(uint32_t d_tmem, uint64_t ah, uint64_t al, uint64_t bh, uint64_t bl,
                                           uint32_t idesc, uint32_t accumulate) {
     asm volatile(
@@ -179,22 +259,6 @@ __device__ __forceinline__ void split_tf32(float x, float &hi, float &lo) {
     lo = tf32_rna(x - hi);
 }
 
-// Splits the fp32 values of an SW128 slab region in place (hi) and into a twin region (lo);
-// thread `tid` of `nthreads` takes every nthreads-th float4.
-__device__ __forceinline__ void split_region(float *hi, float *lo, int n_float4, int tid, int nthreads) {
-    float4 *h4 = reinterpret_cast<float4 *>(hi);
-    float4 *l4 = reinterpret_cast<float4 *>(lo);
-    for (int i = tid; i < n_float4; i += nthreads) {
-        float4 x = h4[i], a, b;
-        split_tf32(x.x, a.x, b.x);
-        split_tf32(x.y, a.y, b.y);
-        split_tf32(x.z, a.z, b.z);
-        split_tf32(x.w, a.w, b.w);
-        h4[i] = a;
-        l4[i] = b;
-    }
-}
-
 // Four consecutive region elements as fp32 (binary16 converts exactly).
 __device__ __forceinline__ float4 ld4(const float *p, int i4) { return reinterpret_cast<const float4 *>(p)[i4]; }
 __device__ __forceinline__ float4 ld4(const __half *p, int i4) {
@@ -233,9 +297,8 @@ __device__ __forceinline__ void pair_of(int idx, int n_qt, int n_kc, int &qt, in
     qt = 0;
 }
 
-// fp32 regions: K tiles arrive by TMA into kh and are split in place.  binary16 and Q8_0
-// regions: the staging warps read the K tile themselves, converting, and write both halves (a
-// binary16 value is exact in TF32, so its low half is zero).
+// fp32 regions: K tiles arrive by TMA into kh and the staging warps convert them into kl.
+// binary16 and Q8_0 regions: the staging warps read the K tile themselves, converting.
 template <int HDKV, typename T>
 __global__ void __launch_bounds__(kThreadsP, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -265,11 +328,13 @@ __global__ void __launch_bounds__(kThreadsP, 1)
             mbar_init(&sm.bar_kk[b], kStageThreads);
             mbar_init(&sm.bar_vv[b], kStageThreads);
         }
+        for (int b = 0; b < 4; ++b) mbar_init(&sm.bar_ks[b], kStageThreads);
         for (int b = 0; b < 2; ++b) {
             mbar_init(&sm.bar_s[b], 1);
             mbar_init(&sm.bar_p[b], kSoftThreads);
             mbar_init(&sm.bar_o[b], 1);
         }
+        mbar_init(&sm.bar_m, 1);
         sm.abort_flag = 0;
         sm.lmax = 0;
         mbar_init_fence();
@@ -331,32 +396,35 @@ __global__ void __launch_bounds__(kThreadsP, 1)
             };
             if (kTmaK)
                 for (int j = 0; j < NB && j < n_tiles; ++j) load_k(j);
-            // Descriptors of every operand slab, built once: a K step of 8 (32 bytes) moves
-            // the start-address field (address / 16) by 2 within a 1024-aligned slab.
-            uint64_t dq[2][HDKV / 32], dk[NB][2][HDKV / 32];
+            // Descriptors of the binary16 slabs of Q and of every K buffer (64 columns, 128-byte
+            // rows; hi slabs then lo slabs), built once: a K step of 16 (32 bytes) moves the
+            // start-address field (address / 16) by 2 within a 1024-aligned slab
+            uint64_t dq[2][HDKV / 64], dk[NB][2][HDKV / 64];
 #pragma unroll
-            for (int c = 0; c < HDKV / 32; ++c) {
-                dq[0][c] = sw128_desc(su32(sm.qh[c]));
-                dq[1][c] = sw128_desc(su32(sm.ql[c]));
+            for (int c = 0; c < HDKV / 64; ++c) {
+                const uint32_t qb = su32(&sm.ql[0][0]);
+                dq[0][c] = sw128_desc(qb + c * (BM * 128));
+                dq[1][c] = sw128_desc(qb + (HDKV / 64 + c) * (BM * 128));
 #pragma unroll
                 for (int b = 0; b < NB; ++b) {
-                    dk[b][0][c] = sw128_desc(su32(sm.kh[b][c]));
-                    dk[b][1][c] = sw128_desc(su32(sm.kl[b][c]));
+                    const uint32_t kb = su32(&sm.kl[b][0][0]);
+                    dk[b][0][c] = sw128_desc(kb + c * (BN * 128));
+                    dk[b][1][c] = sw128_desc(kb + (HDKV / 64 + c) * (BN * 128));
                 }
             }
-            constexpr uint32_t kIdS = tf32_idesc(BM, BN);
-            // S(j) = Q K(j)^T into S buffer j % 2 (Q and K tile j split by then)
+            constexpr uint32_t kIdS = f16_idesc(BM, BN);
+            // S(j) = Q K(j)^T into S buffer j % 2 (Q and K tile j converted by then)
             auto issue_s = [&](int j) {
                 const int b = j % NB;
                 tc_fence_after();
 #pragma unroll
-                for (int kk = 0; kk < HDKV / 8; ++kk) {
+                for (int kk = 0; kk < HDKV / 16; ++kk) {
                     const uint64_t o = 2 * (kk & 3);
                     const int c = kk >> 2;
                     // (buffer chosen by selects: a run-time index would move the array to local memory)
                     const uint64_t kh = (NB == 2 && b) ? dk[NB - 1][0][c] : dk[0][0][c];
                     const uint64_t kl = (NB == 2 && b) ? dk[NB - 1][1][c] : dk[0][1][c];
-                    mma3_tf32(tmem + s_col(j), dq[0][c] + o, dq[1][c] + o, kh + o, kl + o, kIdS, kk > 0);
+                    mma3_f16(tmem + s_col(j), dq[0][c] + o, dq[1][c] + o, kh + o, kl + o, kIdS, kk > 0);
                 }
                 mma_commit(&sm.bar_s[j & 1]);
             };
@@ -417,7 +485,7 @@ __global__ void __launch_bounds__(kThreadsP, 1)
             }
         }
     } else if (warp >= kStageWarp0) {
-        // staging: K tiles split into TF32 halves, V tiles transposed and split (K-major)
+        // staging: K tiles into scaled binary16 halves, V tiles transposed and split into TF32 (K-major)
         const int st = tid - (kSoftThreads + 32);  // 0 .. kStageThreads-1
         const int vk = st & (BN - 1), vq = st / BN;  // key of the tile, half of the dims
         constexpr int kV4 = HDKV / 8;                // float4 of a V row per thread
@@ -439,35 +507,58 @@ __global__ void __launch_bounds__(kThreadsP, 1)
             for (int c = 0; c < kV4; ++c)
                 vnext[c] = key < lmax ? kv4(a.v_reg, key, vq * kV4 + c) : make_float4(0.f, 0.f, 0.f, 0.f);
         };
-        // K tile j -> buffer j % NB, split into TF32 halves (fp32: in place after its TMA copy;
-        // binary16 / Q8_0: read and converted here; keys past the widest window are zero)
+        // K tile j -> buffer j % NB as scaled binary16 hi + lo halves, a key row per pair of
+        // adjacent lanes (each half the row; the row's largest magnitude by one shuffle), and
+        // the key's unscale factor into slot j % 4 (fp32 K: read from its TMA copy; binary16 and
+        // Q8_0: read and converted here; keys past the widest window are zero)
         auto stage_k = [&](int j) -> bool {
             const int b = j % NB;
+            const int key = st >> 1, h2 = st & 1;  // key of the tile, half of the row
+            constexpr int kH4 = HDKV / 8;          // float4 of half a row
+            float4 kv[kH4];
+            // (the pair exchange below is a warp shuffle: the warp leaves together or not at all)
             if (kTmaK) {
-                if (!mbar_wait(&sm.bar_k[b], (j / NB) & 1, abort_flag, a.err)) return false;
-                split_region(&sm.kh[b][0][0], &sm.kl[b][0][0], BN * HDKV / 4, st, kStageThreads);
+                if (!__all_sync(0xffffffffu, mbar_wait(&sm.bar_k[b], (j / NB) & 1, abort_flag, a.err))) return false;
+#pragma unroll
+                for (int c = 0; c < kH4; ++c) {
+                    const int d4 = h2 * kH4 + c;
+                    kv[c] = *reinterpret_cast<const float4 *>(
+                        reinterpret_cast<const unsigned char *>(sm.kh[b][d4 >> 3]) + sw128_off(key, 4 * (d4 & 7)));
+                }
             } else {
                 // the buffer last held key tile j - NB: S(j - NB) must have read it
                 if (j >= NB) {
-                    if (!mbar_wait(&sm.bar_s[(j - NB) & 1], ((j - NB) >> 1) & 1, abort_flag, a.err)) return false;
+                    if (!__all_sync(0xffffffffu,
+                                    mbar_wait(&sm.bar_s[(j - NB) & 1], ((j - NB) >> 1) & 1, abort_flag, a.err)))
+                        return false;
                     tc_fence_after();
                 }
-                const int key = (tile0 + j) * BN + vk;
-#pragma unroll 4
-                for (int d4 = vq * kV4; d4 < (vq + 1) * kV4; ++d4) {
-                    const float4 kv = key < lmax ? kv4(a.k_reg, key, d4) : make_float4(0.f, 0.f, 0.f, 0.f);
-                    const float kk[4] = {kv.x, kv.y, kv.z, kv.w};
+                const int gkey = (tile0 + j) * BN + key;
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int d = 4 * d4 + e;
-                        float hi, lo;
-                        split_tf32(kk[e], hi, lo);
-                        const uint32_t off = sw128_off(vk, d & 31);
-                        *reinterpret_cast<float *>(reinterpret_cast<unsigned char *>(sm.kh[b][d >> 5]) + off) = hi;
-                        *reinterpret_cast<float *>(reinterpret_cast<unsigned char *>(sm.kl[b][d >> 5]) + off) = lo;
-                    }
-                }
+                for (int c = 0; c < kH4; ++c)
+                    kv[c] = gkey < lmax ? kv4(a.k_reg, gkey, h2 * kH4 + c) : make_float4(0.f, 0.f, 0.f, 0.f);
             }
+            float amax = 0.0f;
+#pragma unroll
+            for (int c = 0; c < kH4; ++c)
+                amax = fmaxf(amax, fmaxf(fmaxf(fabsf(kv[c].x), fabsf(kv[c].y)), fmaxf(fabsf(kv[c].z), fabsf(kv[c].w))));
+            amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+            float ksc;
+            const float kinv = f16_row_scale(amax, ksc);
+            unsigned char *k16 = reinterpret_cast<unsigned char *>(&sm.kl[b][0][0]);
+#pragma unroll
+            for (int c = 0; c < kH4 / 2; ++c) {
+                const float x[8] = {kv[2 * c].x, kv[2 * c].y, kv[2 * c].z, kv[2 * c].w,
+                                    kv[2 * c + 1].x, kv[2 * c + 1].y, kv[2 * c + 1].z, kv[2 * c + 1].w};
+                uint4 hi, lo;
+                f16_split8(x, ksc, hi, lo);
+                const int g = h2 * (kH4 / 2) + c;  // group of 8 binary16 elements in the row
+                const uint32_t off = static_cast<uint32_t>(g >> 3) * (BN * 128) + sw128_off16(key, g & 7);
+                *reinterpret_cast<uint4 *>(k16 + off) = hi;
+                *reinterpret_cast<uint4 *>(k16 + (HDKV / 64) * (BN * 128) + off) = lo;
+            }
+            if (h2 == 0) sm.ks[j & 3][key] = kinv * a.scale_log2;  // exact: kinv is a power of two
+            mbar_arrive(&sm.bar_ks[j & 3]);  // the factors, to the softmax threads (tile j + 4 needs P(j) first)
             fence_async_smem();  // split K -> visible to the tensor cores
             tc_fence_before();
             mbar_arrive(&sm.bar_kk[b]);
@@ -516,7 +607,7 @@ __global__ void __launch_bounds__(kThreadsP, 1)
     } else {
         // softmax and epilogue: thread tid owns query row tid (TMEM lane tid)
         const uint32_t trow = tmem + (static_cast<uint32_t>(warp * 32) << 16);
-        const float sl = a.scale_log2;
+        float qinv = 1.0f;  // the factor undoing this query row's binary16 scale (a power of two)
         float o[HDKV];
 #pragma unroll
         for (int d = 0; d < HDKV; ++d) o[d] = 0.0f;
@@ -535,7 +626,30 @@ __global__ void __launch_bounds__(kThreadsP, 1)
         bool ok = n_tiles > 0;
         if (ok) ok = mbar_wait(&sm.bar_q, 0, abort_flag, a.err);
         if (ok) {
-            split_region(&sm.qh[0][0], &sm.ql[0][0], BM * HDKV / 4, tid, kSoftThreads);
+            // this thread's query row (row tid) into binary16 hi and lo halves, scaled
+            auto q4 = [&](int d4) {  // fp32 elements 4*d4.. of the row, from the TMA slabs
+                return *reinterpret_cast<const float4 *>(reinterpret_cast<const unsigned char *>(sm.qh[d4 >> 3]) +
+                                                        sw128_off(tid, 4 * (d4 & 7)));
+            };
+            float amax = 0.0f;
+#pragma unroll 8
+            for (int d4 = 0; d4 < HDKV / 4; ++d4) {
+                const float4 v = q4(d4);
+                amax = fmaxf(amax, fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
+            }
+            float qs;
+            qinv = f16_row_scale(amax, qs);
+            unsigned char *q16 = reinterpret_cast<unsigned char *>(&sm.ql[0][0]);
+#pragma unroll 4
+            for (int g = 0; g < HDKV / 8; ++g) {
+                const float4 u = q4(2 * g), w = q4(2 * g + 1);
+                const float x[8] = {u.x, u.y, u.z, u.w, w.x, w.y, w.z, w.w};
+                uint4 hi, lo;
+                f16_split8(x, qs, hi, lo);
+                const uint32_t off = static_cast<uint32_t>(g >> 3) * (BM * 128) + sw128_off16(tid, g & 7);
+                *reinterpret_cast<uint4 *>(q16 + off) = hi;
+                *reinterpret_cast<uint4 *>(q16 + (HDKV / 64) * (BM * 128) + off) = lo;
+            }
             fence_async_smem();  // split Q -> visible to the tensor cores
             tc_fence_before();
             mbar_arrive(&sm.bar_qs);
@@ -544,18 +658,30 @@ __global__ void __launch_bounds__(kThreadsP, 1)
         // cores form O_t(i) and S(i+1).
         for (int i = 0; ok && i < n_tiles; ++i) {
             const int j0 = (tile0 + i) * BN;
-            if (!mbar_wait(&sm.bar_s[i & 1], (i >> 1) & 1, abort_flag, a.err)) {
+            if (!mbar_wait(&sm.bar_s[i & 1], (i >> 1) & 1, abort_flag, a.err) ||
+                !mbar_wait(&sm.bar_ks[i & 3], (i >> 2) & 1, abort_flag, a.err)) {
                 ok = false;
                 break;
             }
             tc_fence_after();
             float r[32];
             tmem_ld32(trow + s_col(i), r);
+            // r * ks: the key's binary16 scale undone and scale * log2(e) applied (one rounding);
+            // the query row's scale, a power of two, is undone exactly on the max and inside the
+            // exponent's fused multiply-add
+#pragma unroll
+            for (int e4 = 0; e4 < 8; ++e4) {
+                const float4 f = reinterpret_cast<const float4 *>(sm.ks[i & 3])[e4];
+                r[4 * e4] *= f.x;
+                r[4 * e4 + 1] *= f.y;
+                r[4 * e4 + 2] *= f.z;
+                r[4 * e4 + 3] *= f.w;
+            }
             float mx = -INFINITY;
 #pragma unroll
             for (int e = 0; e < 32; ++e)
-                if (j0 + e < L_t) mx = fmaxf(mx, r[e] * sl);
-            const float m_new = fmaxf(m, mx);
+                if (j0 + e < L_t) mx = fmaxf(mx, r[e]);
+            const float m_new = fmaxf(m, mx * qinv);
             const bool none = (m_new == -INFINITY);  // no key visible to this row yet
             const float corr = none ? 1.0f : ex2_approx(m - m_new);
             // one P buffer: O_t(i-1) must have read P(i-1) before it is overwritten
@@ -573,7 +699,7 @@ __global__ void __launch_bounds__(kThreadsP, 1)
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
                     const int j = j0 + 4 * e4 + e;
-                    const float pe = (!none && j < L_t) ? ex2_approx(r[4 * e4 + e] * sl - m_new) : 0.0f;
+                    const float pe = (!none && j < L_t) ? ex2_approx(fmaf(r[4 * e4 + e], qinv, -m_new)) : 0.0f;
                     split_tf32(pe, whv[e], wlv[e]);
                     ps += pe;
                 }
@@ -628,10 +754,28 @@ __global__ void __launch_bounds__(kThreadsP, 1)
             named_sync(1, kSoftThreads);
             write_out = sm.lmax == -1;
             if (write_out) {
-                // The (max, sum) pairs of every chunk first, in one round trip, so the combined
-                // max and every chunk's factor are known before the partial outputs are read;
-                // then each chunk's outputs, scaled, are added (at most 16 chunks a tile).
+                // The other chunks' partial outputs are bulk-copied into the free shared memory,
+                // kN chunks at a time, all copies of a batch in flight together; meanwhile the
+                // (max, sum) pairs of every chunk come in one round trip, so the combined max and
+                // every chunk's factor are known when the outputs land.  Then each chunk's
+                // outputs, scaled, are added in chunk order (at most 16 chunks a tile).
+                using MS = MergeSlots<HDKV>;
                 constexpr int kMaxKc = 16;
+                unsigned char *slots = reinterpret_cast<unsigned char *>(&sm.qh[0][0]) + MS::kStg;
+                auto issue_batch = [&](int c0) {  // chunks c0 .. c0 + kN - 1 other than kc
+                    if (tid != 0 || *abort_flag) return;
+                    uint32_t bytes = 0;
+                    for (int c = c0; c < c0 + MS::kN && c < n_act; ++c)
+                        if (c != kc) bytes += static_cast<uint32_t>(MS::kPart);
+                    if (bytes == 0) return;
+                    fence_async_global();  // the partials acquired through the ticket, to the copy engine
+                    mbar_expect_tx(&sm.bar_m, bytes);
+                    for (int c = c0; c < c0 + MS::kN && c < n_act; ++c)
+                        if (c != kc)
+                            bulk_load(slots + (c - c0) * MS::kPart, a.ws_o + (blk + c) * HDKV * BM,
+                                      static_cast<uint32_t>(MS::kPart), &sm.bar_m);
+                };
+                issue_batch(0);
                 float mcs[kMaxKc], lcs[kMaxKc];
 #pragma unroll
                 for (int c = 0; c < kMaxKc; ++c) {
@@ -645,22 +789,43 @@ __global__ void __launch_bounds__(kThreadsP, 1)
                 for (int c = 0; c < kMaxKc; ++c) M = fmaxf(M, mcs[c]);
                 const float fa = m == -INFINITY ? 0.0f : ex2_approx(m - M);
                 l *= fa;
-#pragma unroll
-                for (int d = 0; d < HDKV; ++d) o[d] *= fa;
+                float fbs[kMaxKc];  // every chunk's factor (the sum takes them in chunk order)
 #pragma unroll
                 for (int c = 0; c < kMaxKc; ++c) {
-                    if (c < n_act && c != kc) {
-                        const float fb = mcs[c] == -INFINITY ? 0.0f : ex2_approx(mcs[c] - M);
-                        const float *qo = a.ws_o + (blk + c) * HDKV * BM;
-                        l = fmaf(lcs[c], fb, l);
+                    fbs[c] = mcs[c] == -INFINITY ? 0.0f : ex2_approx(mcs[c] - M);
+                    if (c < n_act && c != kc) l = fmaf(lcs[c], fbs[c], l);
+                }
 #pragma unroll
-                        for (int d4 = 0; d4 < HDKV / 4; ++d4) {
-                            const float4 x = __ldcg(reinterpret_cast<const float4 *>(qo) + d4 * BM + tid);
-                            o[4 * d4] = fmaf(x.x, fb, o[4 * d4]);
-                            o[4 * d4 + 1] = fmaf(x.y, fb, o[4 * d4 + 1]);
-                            o[4 * d4 + 2] = fmaf(x.z, fb, o[4 * d4 + 2]);
-                            o[4 * d4 + 3] = fmaf(x.w, fb, o[4 * d4 + 3]);
+                for (int d = 0; d < HDKV; ++d) o[d] *= fa;
+                uint32_t mph = 0;  // phase of bar_m
+#pragma unroll 1
+                for (int c0 = 0; c0 < kMaxKc; c0 += MS::kN) {
+                    if (c0 >= n_act) break;
+                    const int cnt = min(MS::kN, n_act - c0);
+                    if (cnt > 1 || c0 != kc) {  // the batch holds a chunk other than kc: copies to wait for
+                        // (one decision for every row: the threads meet at named barriers below)
+                        if (!named_all(1, kSoftThreads, mbar_wait(&sm.bar_m, mph, abort_flag, a.err))) break;
+                        mph ^= 1u;
+                    }
+#pragma unroll
+                    for (int cc = 0; cc < MS::kN; ++cc) {
+                        const int c = c0 + cc;
+                        if (c < kMaxKc && c < n_act && c != kc) {
+                            const float fb = fbs[c];
+                            const float4 *qo = reinterpret_cast<const float4 *>(slots + cc * MS::kPart);
+#pragma unroll
+                            for (int d4 = 0; d4 < HDKV / 4; ++d4) {
+                                const float4 x = qo[d4 * BM + tid];
+                                o[4 * d4] = fmaf(x.x, fb, o[4 * d4]);
+                                o[4 * d4 + 1] = fmaf(x.y, fb, o[4 * d4 + 1]);
+                                o[4 * d4 + 2] = fmaf(x.z, fb, o[4 * d4 + 2]);
+                                o[4 * d4 + 3] = fmaf(x.w, fb, o[4 * d4 + 3]);
+                            }
                         }
+                    }
+                    if (c0 + MS::kN < n_act) {  // every row has read the slots before they refill
+                        named_sync(1, kSoftThreads);
+                        issue_batch(c0 + MS::kN);
                     }
                 }
                 m = M;
@@ -670,7 +835,7 @@ __global__ void __launch_bounds__(kThreadsP, 1)
         if (write_out) {  // the same in every softmax thread
             // Rows pass through shared memory (the Q slabs: every S has completed) so that each
             // warp writes whole output rows, which lie n_head*hd_kv floats apart.
-            constexpr int kRS = HDKV + 4;  // padded row stride in floats (no bank conflicts)
+            constexpr int kRS = MergeSlots<HDKV>::kRS;
             static_assert(BM * kRS <= 2 * HDKV * BM, "staging fits the Q slabs");
             float *stg = &sm.qh[0][0];
             const float inv = l > 0.0f ? 1.0f / l : 0.0f;

@@ -1,8 +1,8 @@
-"""GPU parity of the tensor-core causal prefill (QK^T and PV on tcgen05 with split-precision
-TF32 operands, fp32 softmax) against the CPU oracle.  Two bounds: the tensor-core tolerance
-(max-abs 2e-3), and -- because the hi/lo operand split makes the products fp32-accurate --
-the fp32 tolerance |d| <= 1e-5 + 1e-4 |ref| used for the CUDA-core kernels.  Window and
-error handling are exact."""
+"""GPU parity of the tensor-core causal prefill (QK^T on tcgen05 with binary16 hi/lo halves of
+power-of-two-scaled rows, PV with TF32 hi/lo halves, fp32 softmax) against the CPU oracle.  Two
+bounds: the tensor-core tolerance (max-abs 2e-3), and -- because the hi/lo operand split makes
+the products fp32-accurate -- the fp32 tolerance |d| <= 1e-5 + 1e-4 |ref| used for the
+CUDA-core kernels.  Window and error handling are exact."""
 import numpy as np
 import pytest
 import torch
