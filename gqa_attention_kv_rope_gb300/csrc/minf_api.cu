@@ -225,9 +225,9 @@ size_t minf_attn_prefill_workspace_bytes(int nt, int n_head, int n_kv_head, int 
     return prefill_workspace_bytes(nt, n_head, hd_kv, cap);
 }
 
-static int prefill(float *out, const float *q, const void *k_reg, const void *v_reg, int kv, int cap,
-                   const int32_t *pos, int nt, int nh, int nk, int hd, int hd_kv, float scale,
-                   void *ws, size_t ws_bytes, int32_t *err, cudaStream_t s, bool pdl = false) {
+static PrefillArgs prefill_args(float *out, const float *q, const void *k_reg, const void *v_reg, int kv, int cap,
+                                const int32_t *pos, int nt, int nh, int nk, int hd, int hd_kv, float scale,
+                                void *ws, size_t ws_bytes, int32_t *err, bool pdl) {
     PrefillArgs a = {};
     a.pdl = pdl;
     a.ws = ws;
@@ -246,7 +246,14 @@ static int prefill(float *out, const float *q, const void *k_reg, const void *v_
     a.hd_kv = hd_kv;
     a.cap = cap;
     a.scale = scale;
-    return launch_prefill(a, s);
+    return a;
+}
+
+static int prefill(float *out, const float *q, const void *k_reg, const void *v_reg, int kv, int cap,
+                   const int32_t *pos, int nt, int nh, int nk, int hd, int hd_kv, float scale,
+                   void *ws, size_t ws_bytes, int32_t *err, cudaStream_t s, bool pdl = false) {
+    return launch_prefill(
+        prefill_args(out, q, k_reg, v_reg, kv, cap, pos, nt, nh, nk, hd, hd_kv, scale, ws, ws_bytes, err, pdl), s);
 }
 
 static DecodeArgs decode_args(float *out, const float *q, const void *k_reg,
@@ -383,6 +390,14 @@ static int layer_attn_step(float *xn, const float *h, const float *gain, float e
                                    n_kv_head, hd, hd_kv, scale, ws, ws_bytes, err);
         DecodeStepExtra x = {k, v, xn, h, gain, eps, theta, freq_scale, n_embd, style, true};
         return launch_decode_step(d, x, s);
+    }
+    if (nt > 1 && kv != kKvQ8) {
+        // one launch: the row work, a grid barrier, then the attention items
+        const PrefillArgs pa = prefill_args(out, q, k_reg, v_reg, kv, cap, pos, nt, n_head, n_kv_head, hd, hd_kv,
+                                            scale, ws, ws_bytes, err, true);
+        const PrefillStepExtra x = {q, k, v, xn, h, gain, eps, theta, freq_scale, n_embd, style};
+        st = launch_prefill_step(pa, x, s);
+        if (st != MINF_ERR_UNSUPPORTED) return st;
     }
     // one launch for RMSNorm, RoPE and the store, then the attention
     st = layer_prologue(xn, h, gain, eps, n_embd, q, k, v, pos, nt, n_head, n_kv_head, hd, hd_kv, theta,

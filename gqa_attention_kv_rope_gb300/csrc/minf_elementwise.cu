@@ -9,22 +9,10 @@
 
 #include "minf_common.cuh"
 #include "minf_kernels.h"
+#include "minf_prologue.cuh"
 #include "minf_q8.cuh"
 
 namespace minf {
-
-// Region elements: fp32 as is, binary16 converted with round to nearest even ("11 . Attention,
-// vec ops, and the KV cache", §2.5: the GPU backends may keep the K/V regions in f16).
-__device__ __forceinline__ void put1(float *p, size_t i, float v) { p[i] = v; }
-__device__ __forceinline__ void put1(__half *p, size_t i, float v) { p[i] = __float2half_rn(v); }
-__device__ __forceinline__ void put4(float *p, size_t i4, float4 v) { reinterpret_cast<float4 *>(p)[i4] = v; }
-__device__ __forceinline__ void put4(__half *p, size_t i4, float4 v) {
-    const __half2 a = __floats2half2_rn(v.x, v.y), b = __floats2half2_rn(v.z, v.w);
-    uint2 u;
-    u.x = *reinterpret_cast<const uint32_t *>(&a);
-    u.y = *reinterpret_cast<const uint32_t *>(&b);
-    reinterpret_cast<uint2 *>(p)[i4] = u;
-}
 
 void rope_table(RopeTable *t, int hd, float theta, float freq_scale) {
     // "11 . Attention, vec ops, and the KV cache", §2.3/§3.2.2: the angular speed of
@@ -50,53 +38,7 @@ int sm_count() {
 }
 
 // ----------------------------------------------------------------------------- RMSNorm
-// "11 . Attention, vec ops, and the KV cache", §3.2.1: y = x / sqrt(mean(x^2) + eps) * w.
-// One warp per row; the sum of squares is a per-lane fp32 sum folded by a butterfly.  The loops
-// are unrolled so that a lane's loads of a row are in flight together.
-template <bool kVec>
-__device__ __forceinline__ void rms_norm_row(float *y, const float *x, const float *w, int warp, int n, float eps) {
-    const int lane = threadIdx.x & 31;
-    const float *xr = x + static_cast<size_t>(warp) * n;
-    float *yr = y + static_cast<size_t>(warp) * n;
-    float ss = 0.0f;
-    if (kVec) {
-        const float4 *x4 = reinterpret_cast<const float4 *>(xr);
-#pragma unroll 8
-        for (int i = lane; i < n / 4; i += 32) {
-            float4 v = x4[i];
-            ss = fmaf(v.x, v.x, ss);
-            ss = fmaf(v.y, v.y, ss);
-            ss = fmaf(v.z, v.z, ss);
-            ss = fmaf(v.w, v.w, ss);
-        }
-    } else {
-#pragma unroll 8
-        for (int i = lane; i < n; i += 32) ss = fmaf(xr[i], xr[i], ss);
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-    const float mean = ss / static_cast<float>(n);
-    const float scale = 1.0f / sqrtf(mean + eps);
-    if (kVec) {
-        const float4 *x4 = reinterpret_cast<const float4 *>(xr);
-        const float4 *w4 = reinterpret_cast<const float4 *>(w);
-        float4 *y4 = reinterpret_cast<float4 *>(yr);
-#pragma unroll 8
-        for (int i = lane; i < n / 4; i += 32) {
-            float4 v = x4[i];
-            float4 g = w ? w4[i] : make_float4(1.f, 1.f, 1.f, 1.f);
-            y4[i] = make_float4(v.x * scale * g.x, v.y * scale * g.y, v.z * scale * g.z,
-                                v.w * scale * g.w);
-        }
-    } else {
-#pragma unroll 8
-        for (int i = lane; i < n; i += 32) {
-            float v = xr[i] * scale;
-            yr[i] = w ? v * w[i] : v;
-        }
-    }
-}
-
+// "11 . Attention, vec ops, and the KV cache", §3.2.1: one warp per row (rms_norm_row).
 template <bool kVec>
 __global__ void __launch_bounds__(256) rms_norm_kernel(float *y, const float *x, const float *w,
                                                        int rows, int n, float eps) {
@@ -165,18 +107,7 @@ int launch_rms_norm(float *y, const float *x, const float *w, int rows, int n, f
 }
 
 // ----------------------------------------------------------------------------- RoPE
-// "11 . Attention, vec ops, and the KV cache", §3.2.2: the pair is rotated by +th with
-// th = pos * freq_i in fp32.  Each product is rounded separately (no contraction), so
-// the only difference from an exact evaluation is sincosf's own rounding.
-__device__ __forceinline__ void rope_pair(float &x0, float &x1, float th) {
-    float sn, cs;
-    sincosf(th, &sn, &cs);
-    const float a = __fsub_rn(__fmul_rn(x0, cs), __fmul_rn(x1, sn));
-    const float b = __fadd_rn(__fmul_rn(x0, sn), __fmul_rn(x1, cs));
-    x0 = a;
-    x1 = b;
-}
-
+// (the rotation of a pair, rope_pair, is in minf_prologue.cuh)
 // Rotates pair i of head row `row` (hd floats) in place; f: the angular speeds.
 __device__ __forceinline__ void rope_row_pair(float *row, int i, int hd, int style, float p, const float *f) {
     const int half = hd >> 1;

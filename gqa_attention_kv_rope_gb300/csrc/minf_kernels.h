@@ -133,6 +133,20 @@ struct PrefillArgs {
 size_t prefill_workspace_bytes(int nt, int nh, int hd_kv, int cap);
 int launch_prefill(const PrefillArgs &a, cudaStream_t s);
 
+// The rest of a prefill layer step, fused into the attention launch (one sequence, contiguous
+// fp32 or binary16 regions).  launch_prefill_step returns MINF_ERR_UNSUPPORTED, launching
+// nothing, where the fused kernel does not apply (the caller then runs the prologue launch and
+// launch_prefill).
+struct PrefillStepExtra {
+    float *q, *k;         // [nt, nh, hd], [nt, nk, hd_kv] rotated in place (q: the PrefillArgs q)
+    const float *v;       // [nt, W]
+    float *xn;            // [nt, n_embd] RMSNorm output
+    const float *h, *gain;
+    float eps, theta, freq_scale;
+    int n_embd, style;
+};
+int launch_prefill_step(const PrefillArgs &a, const PrefillStepExtra &x, cudaStream_t s);
+
 size_t decode_workspace_bytes(int n_seq, int nh, int nk, int hd_kv, int max_cap);
 bool decode_supported(int nh, int nk, int hd, int hd_kv);
 bool fused_step_supported(int nh, int nk, int hd, int hd_kv, int n_embd);

@@ -49,6 +49,7 @@
 
 #include "minf_common.cuh"
 #include "minf_kernels.h"
+#include "minf_prologue.cuh"
 #include "minf_q8.cuh"
 #include "minf_sm103.cuh"
 
@@ -297,87 +298,53 @@ __device__ __forceinline__ void pair_of(int idx, int n_qt, int n_kc, int &qt, in
     qt = 0;
 }
 
+constexpr int kStepMaxQt = 64;  // query tiles (nt <= 8192) the items are enumerated over
+
+struct StepParams {
+    float *q, *k;           // [nt, nh, hd], [nt, nk, hd_kv]: rotated in place
+    const float *v;         // [nt, W]
+    void *k_st, *v_st;      // the regions (written at pos; the items read them as a.k_reg, a.v_reg)
+    int style;              // 0: pairs (i, i + hd/2); 1: pairs (2i, 2i + 1)
+    float *xn;              // [nt, n_embd] RMSNorm output
+    const float *hx, *gain; // [nt, n_embd], [n_embd] (gain nullable)
+    int n_embd, norm_vec;   // norm_vec: float4 rows (n_embd % 4 == 0, 16-byte aligned rows and gain)
+    float eps;
+    int *bar;               // grid barrier: arrivals, departures (zero between launches)
+};
+
+
+// A CTA of the fused step counts its departure from the grid barrier once it has left the
+// wait; the last to depart zeroes both counts for the next launch.
+__device__ __forceinline__ void step_depart(const StepParams &x) {
+    const int old = atomicAdd(x.bar + 1, 1);
+    if (old == static_cast<int>(gridDim.x) - 1) {
+        x.bar[0] = 0;
+        x.bar[1] = 0;
+    }
+}
+
+// One work item: query tile qt of head h against key chunk kc (tiles tile0 .. tile0 + n_tiles - 1
+// of the keys), by every role of the CTA; its TMEM and mbarriers are ready (barriers in their
+// first phase).  lmax: the widest window among the tile's tokens; L_t: this thread's row window
+// (-1: the softmax threads read their positions themselves, while the Q tile is copied).
+struct Item {
+    int h, hk, qt, kc, t0, L_t, lmax, n_act, tile0, n_tiles;
+    uint32_t tmem;
+    const StepParams *dep;  // fused step: this CTA departs the grid barrier during this item
+};
+
 // fp32 regions: K tiles arrive by TMA into kh and the staging warps convert them into kl.
 // binary16 and Q8_0 regions: the staging warps read the K tile themselves, converting.
 template <int HDKV, typename T>
-__global__ void __launch_bounds__(kThreadsP, 1)
-    prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                   const PParams a) {
+__device__ __forceinline__ void attend(Smem<HDKV> &sm, const CUtensorMap &tm_q, const CUtensorMap &tm_k,
+                                       const PParams &a, const Item &it) {
     constexpr bool kTmaK = std::is_same<T, float>::value;
-    extern __shared__ unsigned char smem_raw[];
-    Smem<HDKV> &sm = *reinterpret_cast<Smem<HDKV> *>(
-        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    // CTA -> (query tile, key chunk) pair and head, the head fastest (chunks past a tile's
-    // widest window leave at once)
-    const int h = blockIdx.x % a.nh;
-    int qt, kc;
-    pair_of(blockIdx.x / a.nh, a.n_qt, a.n_kc, qt, kc);
-    const int t0 = qt * BM;
-    const int g = a.nh / a.nk;
-    const int hk = h / g;
+    const int h = it.h, hk = it.hk, qt = it.qt, kc = it.kc, t0 = it.t0, lmax = it.lmax;
+    int L_t = it.L_t;
+    const int n_act = it.n_act, tile0 = it.tile0, n_tiles = it.n_tiles;
+    const uint32_t tmem = it.tmem;
     volatile int *abort_flag = &sm.abort_flag;
-
-    if (tid == 0) {
-        // One barrier per buffer, so that no role can complete a phase twice before another
-        // role waits on it (every refill of a buffer waits on the consumer of its last phase).
-        mbar_init(&sm.bar_q, 1);
-        mbar_init(&sm.bar_qs, kSoftThreads);
-        for (int b = 0; b < Smem<HDKV>::NB; ++b) {
-            mbar_init(&sm.bar_k[b], 1);
-            mbar_init(&sm.bar_kk[b], kStageThreads);
-            mbar_init(&sm.bar_vv[b], kStageThreads);
-        }
-        for (int b = 0; b < 4; ++b) mbar_init(&sm.bar_ks[b], kStageThreads);
-        for (int b = 0; b < 2; ++b) {
-            mbar_init(&sm.bar_s[b], 1);
-            mbar_init(&sm.bar_p[b], kSoftThreads);
-            mbar_init(&sm.bar_o[b], 1);
-        }
-        mbar_init(&sm.bar_m, 1);
-        sm.abort_flag = 0;
-        sm.lmax = 0;
-        mbar_init_fence();
-    }
-    // this row's window ("11 . Attention...", §3.2.4: vl = min(pos[t] + 1, nkv), nkv <= n_ctx)
-    int L_t = 0;
-    const int t = t0 + tid;
-    if (tid < kSoftThreads && t < a.nt) {
-        const int p = __ldg(a.pos + t);
-        L_t = p < 0 ? 0 : (p + 1 < a.cap ? p + 1 : a.cap);
-        if ((p < 0 || p >= a.cap) && h == 0 && kc == 0) flag_error(a.err, MINF_ERRBIT_ATTN_POS);
-    }
-    __syncthreads();
-    if (tid < kSoftThreads) {
-        int mx = L_t;
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-        if (lane == 0) atomicMax(&sm.lmax, mx);
-    }
-    __syncthreads();
-    const int lmax = sm.lmax;
-    const int n_tiles_all = (lmax + BN - 1) / BN;
-    const int n_act = (n_tiles_all + a.kc_tiles - 1) / a.kc_tiles;  // chunks with keys for this tile
-    if (kc > 0 && kc >= n_act) return;  // nothing to do (chunk 0 always runs: it writes the output)
-    const int tile0 = kc * a.kc_tiles;
-    const int n_tiles = min(n_tiles_all - tile0, a.kc_tiles) > 0 ? min(n_tiles_all - tile0, a.kc_tiles) : 0;
-    if (warp == kProducerWarp) {
-        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
-                         su32(&sm.tmem_base)),
-                     "r"(tmem_cols<HDKV>())
-                     : "memory");
-        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-    }
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    const uint32_t tmem = sm.tmem_base;
-    // everything above reads only positions; q, the regions, the workspace and the output may
-    // still be written by the preceding launch (a no-op without programmatic dependent launch)
-    gdc_wait();
-    // The launch that follows may start now: this kernel writes no K/V rows (a following decode
-    // kernel streams cached rows before its own wait), and every launch before it has completed.
-    gdc_launch_dependents();
     constexpr uint32_t kQBytes = BM * HDKV * 4, kKBytes = BN * HDKV * 4;
 
     constexpr int NB = Smem<HDKV>::NB;
@@ -450,6 +417,7 @@ __global__ void __launch_bounds__(kThreadsP, 1)
         // O_t(i) = P(i) V(i) into O buffer i % 2 once P(i) is published and V^T(i) staged, from
         // a second thread: one thread issues a tensor-core instruction only every ~35-50 ns, and
         // S(i+1) and O_t(i) need not wait behind each other's issue
+        if (lane == 0 && it.dep) step_depart(*it.dep);  // (P(0) is microseconds away)
         if (lane == 0 && n_tiles > 0) {
             uint64_t dp[NP][2][BN / 32], dv[NB][2][BN / 32];
 #pragma unroll
@@ -606,6 +574,10 @@ __global__ void __launch_bounds__(kThreadsP, 1)
         }
     } else {
         // softmax and epilogue: thread tid owns query row tid (TMEM lane tid)
+        if (L_t < 0) {  // ("11 . Attention...", §3.2.4: vl = min(pos[t] + 1, nkv))
+            const int p = t0 + tid < a.nt ? __ldg(a.pos + t0 + tid) : -1;
+            L_t = p < 0 ? 0 : (p + 1 < a.cap ? p + 1 : a.cap);
+        }
         const uint32_t trow = tmem + (static_cast<uint32_t>(warp * 32) << 16);
         float qinv = 1.0f;  // the factor undoing this query row's binary16 scale (a power of two)
         float o[HDKV];
@@ -856,6 +828,89 @@ __global__ void __launch_bounds__(kThreadsP, 1)
                 }
         }
     }
+}
+
+// One CTA per (query tile, key chunk, head) item.
+template <int HDKV, typename T>
+__global__ void __launch_bounds__(kThreadsP, 1)
+    prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                   const PParams a) {
+    extern __shared__ unsigned char smem_raw[];
+    Smem<HDKV> &sm = *reinterpret_cast<Smem<HDKV> *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    // CTA -> (query tile, key chunk) pair and head, the head fastest (chunks past a tile's
+    // widest window leave at once)
+    const int h = blockIdx.x % a.nh;
+    int qt, kc;
+    pair_of(blockIdx.x / a.nh, a.n_qt, a.n_kc, qt, kc);
+    const int t0 = qt * BM;
+    const int g = a.nh / a.nk;
+    const int hk = h / g;
+    volatile int *abort_flag = &sm.abort_flag;
+
+    if (tid == 0) {
+        // One barrier per buffer, so that no role can complete a phase twice before another
+        // role waits on it (every refill of a buffer waits on the consumer of its last phase).
+        mbar_init(&sm.bar_q, 1);
+        mbar_init(&sm.bar_qs, kSoftThreads);
+        for (int b = 0; b < Smem<HDKV>::NB; ++b) {
+            mbar_init(&sm.bar_k[b], 1);
+            mbar_init(&sm.bar_kk[b], kStageThreads);
+            mbar_init(&sm.bar_vv[b], kStageThreads);
+        }
+        for (int b = 0; b < 4; ++b) mbar_init(&sm.bar_ks[b], kStageThreads);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&sm.bar_s[b], 1);
+            mbar_init(&sm.bar_p[b], kSoftThreads);
+            mbar_init(&sm.bar_o[b], 1);
+        }
+        mbar_init(&sm.bar_m, 1);
+        sm.abort_flag = 0;
+        sm.lmax = 0;
+        mbar_init_fence();
+    }
+    // this row's window ("11 . Attention...", §3.2.4: vl = min(pos[t] + 1, nkv), nkv <= n_ctx)
+    int L_t = 0;
+    const int t = t0 + tid;
+    if (tid < kSoftThreads && t < a.nt) {
+        const int p = __ldg(a.pos + t);
+        L_t = p < 0 ? 0 : (p + 1 < a.cap ? p + 1 : a.cap);
+        if ((p < 0 || p >= a.cap) && h == 0 && kc == 0) flag_error(a.err, MINF_ERRBIT_ATTN_POS);
+    }
+    __syncthreads();
+    if (tid < kSoftThreads) {
+        int mx = L_t;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+        if (lane == 0) atomicMax(&sm.lmax, mx);
+    }
+    __syncthreads();
+    const int lmax = sm.lmax;
+    const int n_tiles_all = (lmax + BN - 1) / BN;
+    const int n_act = (n_tiles_all + a.kc_tiles - 1) / a.kc_tiles;  // chunks with keys for this tile
+    if (kc > 0 && kc >= n_act) return;  // nothing to do (chunk 0 always runs: it writes the output)
+    const int tile0 = kc * a.kc_tiles;
+    const int n_tiles = min(n_tiles_all - tile0, a.kc_tiles) > 0 ? min(n_tiles_all - tile0, a.kc_tiles) : 0;
+    if (warp == kProducerWarp) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         su32(&sm.tmem_base)),
+                     "r"(tmem_cols<HDKV>())
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = sm.tmem_base;
+    // everything above reads only positions; q, the regions, the workspace and the output may
+    // still be written by the preceding launch (a no-op without programmatic dependent launch)
+    gdc_wait();
+    // The launch that follows may start now: this kernel writes no K/V rows (a following decode
+    // kernel streams cached rows before its own wait), and every launch before it has completed.
+    gdc_launch_dependents();
+    const Item it = {h, hk, qt, kc, t0, L_t, lmax, n_act, tile0, n_tiles, tmem, nullptr};
+    attend<HDKV, T>(sm, tm_q, tm_k, a, it);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -872,9 +927,333 @@ __global__ void __launch_bounds__(kThreadsP, 1)
     }
 }
 
+// ----------------------------------------------------------------------------- fused step
+// The prefill layer step in one launch ("11 . Attention, vec ops, and the KV cache", §3.2.1 -
+// §3.2.4: RMSNorm, RoPE on q and k at the tokens' positions, the K/V store, then the causal
+// attention over the regions).  A grid of at most one CTA an SM, all resident together (a
+// cooperative launch), first does the step's row work split over every thread of the grid; a
+// grid barrier makes the rotated q and the stored rows visible to every CTA; then the CTAs take
+// the (query tile, key chunk, head) items that have keys in turn, each as the per-item kernel
+// does.  No second launch sits between two layer steps, and no CTA is spent on an empty item.
+
+// Shared memory of the step beyond the items' own: the query tiles' widest windows and the
+// prefix sums of their chunk counts (the item enumeration).
+struct StepSmem {
+    int lmq[kStepMaxQt];
+    int pref[kStepMaxQt + 1];
+};
+
+// The row work of the step, spread over every thread of the grid.  The first warps take the
+// RMSNorm rows (a warp a row); every other thread takes one unit at a time: a RoPE unit -- pair
+// group j (pairs 4j .. 4j+3) of token t in up to kRopeHeads q heads or k heads, rotated in place,
+// the k rows also stored at pos -- or a float4 of v, stored at pos.  A RoPE unit computes its
+// four angles' sines and cosines once for its heads and loads all of its heads before it stores
+// any, so that those loads are in flight together.  A pair group is two float4: elements
+// i..i+3 and i+hd/2.. (style 0) or 8j..8j+7 (style 1).  The error bits are those of the
+// separate RoPE + store launch.
+constexpr int kRopeHeads = 8;
+
+struct RopeGroup {
+    float4 u0[kRopeHeads], u1[kRopeHeads];
+};
+
+__device__ __forceinline__ void rope_group_load(RopeGroup &g, const StepParams &x, const float *base, int nheads,
+                                                int hd, int j) {
+    const int i0 = x.style == 0 ? 4 * j : 8 * j;
+    const int i1 = x.style == 0 ? 4 * j + (hd >> 1) : 8 * j + 4;
+#pragma unroll
+    for (int e = 0; e < kRopeHeads; ++e)
+        if (e < nheads) {
+            const float *row = base + static_cast<size_t>(e) * hd;
+            g.u0[e] = *reinterpret_cast<const float4 *>(row + i0);
+            g.u1[e] = *reinterpret_cast<const float4 *>(row + i1);
+        }
+}
+
+template <typename T>
+__device__ __forceinline__ void rope_group_store(const RopeGroup &g, const StepParams &x, float *base, int nheads,
+                                                 int hd, int j, const float *sn, const float *cs, T *reg_row) {
+    const int i0 = x.style == 0 ? 4 * j : 8 * j;
+    const int i1 = x.style == 0 ? 4 * j + (hd >> 1) : 8 * j + 4;
+#pragma unroll
+    for (int e = 0; e < kRopeHeads; ++e)
+        if (e < nheads) {
+            float4 w0 = g.u0[e], w1 = g.u1[e];
+            if (x.style == 0) {  // pair c: (w0[c], w1[c])
+                rope_pair_sc(w0.x, w1.x, sn[0], cs[0]);
+                rope_pair_sc(w0.y, w1.y, sn[1], cs[1]);
+                rope_pair_sc(w0.z, w1.z, sn[2], cs[2]);
+                rope_pair_sc(w0.w, w1.w, sn[3], cs[3]);
+            } else {  // pairs (w0.x, w0.y), (w0.z, w0.w), (w1.x, w1.y), (w1.z, w1.w)
+                rope_pair_sc(w0.x, w0.y, sn[0], cs[0]);
+                rope_pair_sc(w0.z, w0.w, sn[1], cs[1]);
+                rope_pair_sc(w1.x, w1.y, sn[2], cs[2]);
+                rope_pair_sc(w1.z, w1.w, sn[3], cs[3]);
+            }
+            float *row = base + static_cast<size_t>(e) * hd;
+            *reinterpret_cast<float4 *>(row + i0) = w0;
+            *reinterpret_cast<float4 *>(row + i1) = w1;
+            if (reg_row) {
+                const size_t b4 = static_cast<size_t>(e) * (hd >> 2);
+                put4(reg_row, b4 + (i0 >> 2), w0);
+                put4(reg_row, b4 + (i1 >> 2), w1);
+            }
+        }
+}
+
+template <typename T>
+__device__ __forceinline__ void step_rows(const PParams &a, const StepParams &x, const float *fq, const float *fk) {
+    const int warps = gridDim.x * (blockDim.x >> 5);
+    const int norm_warps = a.nt < warps / 2 ? a.nt : warps / 2;
+    const int gw = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    if (gw < norm_warps) {
+        for (int r = gw; r < a.nt; r += norm_warps) {  // RMSNorm: a warp per row
+            if (x.norm_vec)
+                rms_norm_row<true>(x.xn, x.hx, x.gain, r, x.n_embd, x.eps);
+            else
+                rms_norm_row<false>(x.xn, x.hx, x.gain, r, x.n_embd, x.eps);
+        }
+        return;
+    }
+    const int G = (warps - norm_warps) * 32;
+    const int gt = (gw - norm_warps) * 32 + (threadIdx.x & 31);
+    const int hd_kv = a.W / a.nk;
+    const int gq = a.hd >> 3, gk = hd_kv >> 3;  // pair groups of a head
+    const int bq = (a.nh + kRopeHeads - 1) / kRopeHeads, bk = (a.nk + kRopeHeads - 1) / kRopeHeads;
+    const int per_tok = gq * bq + gk * bk;  // RoPE units of a token
+    const int nvu = a.W >> 2;
+    const int n_rope = a.nt * per_tok;  // the host keeps nt * (per_tok + nvu) below 2^30
+    const int total = n_rope + a.nt * nvu;
+    for (int u = gt; u < total; u += G) {
+        if (u >= n_rope) {  // a float4 of v (loaded together with its position)
+            const int w = u - n_rope;
+            const int t = w / nvu, c = w - t * nvu;
+            const int p = __ldg(a.pos + t);
+            const float4 vv = reinterpret_cast<const float4 *>(x.v)[static_cast<size_t>(t) * nvu + c];
+            if (p < 0 || p >= a.cap) {
+                if (c == 0) flag_error(a.err, MINF_ERRBIT_STORE_POS);
+                continue;
+            }
+            put4(static_cast<T *>(x.v_st), static_cast<size_t>(p) * nvu + c, vv);
+            continue;
+        }
+        const int t = u / per_tok;
+        int r = u - t * per_tok;
+        const bool is_q = r < gq * bq;
+        if (!is_q) r -= gq * bq;
+        const int ng = is_q ? gq : gk;
+        const int b = r / ng, j = r - b * ng;  // head batch, pair group
+        const int nheads = is_q ? a.nh : a.nk, hd = is_q ? a.hd : hd_kv;
+        const int h0 = b * kRopeHeads;
+        const int nb = nheads - h0 < kRopeHeads ? nheads - h0 : kRopeHeads;
+        float *base = (is_q ? x.q + static_cast<size_t>(t) * a.nh * a.hd : x.k + static_cast<size_t>(t) * a.W) +
+                      static_cast<size_t>(h0) * hd;
+        // the heads' pairs and the position in flight together
+        const int p = __ldg(a.pos + t);
+        RopeGroup grp;
+        rope_group_load(grp, x, base, nb, hd, j);
+        if (p < 0) {
+            if (is_q && r == 0) flag_error(a.err, MINF_ERRBIT_ROPE_POS);
+            continue;
+        }
+        const float pf = static_cast<float>(p);
+        const float *f = is_q ? fq : fk;
+        float sn[4], cs[4];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) sincosf(__fmul_rn(pf, f[4 * j + c]), &sn[c], &cs[c]);
+        T *reg = (!is_q && p < a.cap) ? static_cast<T *>(x.k_st) + static_cast<size_t>(p) * a.W + h0 * hd : nullptr;
+        rope_group_store<T>(grp, x, base, nb, hd, j, sn, cs, reg);
+    }
+}
+
+template <int HDKV, typename T>
+__global__ void __launch_bounds__(kThreadsP, 1)
+    prefill_step_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                        const PParams a, const StepParams x, const RopeTable tq, const RopeTable tk) {
+    extern __shared__ unsigned char smem_raw[];
+    Smem<HDKV> &sm = *reinterpret_cast<Smem<HDKV> *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    StepSmem &ss = *reinterpret_cast<StepSmem *>(reinterpret_cast<unsigned char *>(&sm) + sizeof(Smem<HDKV>));
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    volatile int *abort_flag = &sm.abort_flag;
+    auto init_barriers = [&](bool again) {  // thread 0
+        unsigned long long *bars[] = {&sm.bar_q, &sm.bar_qs, &sm.bar_m};
+        for (unsigned long long *b : bars)
+            if (again) mbar_inval(b);
+        if (again) {
+            for (int b = 0; b < Smem<HDKV>::NB; ++b) {
+                mbar_inval(&sm.bar_k[b]);
+                mbar_inval(&sm.bar_kk[b]);
+                mbar_inval(&sm.bar_vv[b]);
+            }
+            for (int b = 0; b < 4; ++b) mbar_inval(&sm.bar_ks[b]);
+            for (int b = 0; b < 2; ++b) {
+                mbar_inval(&sm.bar_s[b]);
+                mbar_inval(&sm.bar_p[b]);
+                mbar_inval(&sm.bar_o[b]);
+            }
+        }
+        mbar_init(&sm.bar_q, 1);
+        mbar_init(&sm.bar_qs, kSoftThreads);
+        for (int b = 0; b < Smem<HDKV>::NB; ++b) {
+            mbar_init(&sm.bar_k[b], 1);
+            mbar_init(&sm.bar_kk[b], kStageThreads);
+            mbar_init(&sm.bar_vv[b], kStageThreads);
+        }
+        for (int b = 0; b < 4; ++b) mbar_init(&sm.bar_ks[b], kStageThreads);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&sm.bar_s[b], 1);
+            mbar_init(&sm.bar_p[b], kSoftThreads);
+            mbar_init(&sm.bar_o[b], 1);
+        }
+        mbar_init(&sm.bar_m, 1);
+        mbar_init_fence();
+    };
+    if (tid == 0) {
+        init_barriers(false);
+        sm.abort_flag = 0;
+    }
+    // the angular-speed tables, into shared memory the items overwrite later
+    float *fq = &sm.kh[0][0][0], *fk = fq + kMaxHalf;
+    for (int i = tid; i < kMaxHalf; i += kThreadsP) {
+        fq[i] = tq.f[i];
+        fk[i] = tk.f[i];
+    }
+    if (warp == kProducerWarp) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         su32(&sm.tmem_base)),
+                     "r"(tmem_cols<HDKV>())
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = sm.tmem_base;
+    gdc_wait();  // every input (pos included) and the workspace, only after the launch before this one
+
+    // Every query tile's widest window ("11 . Attention...", §3.2.4: vl = min(pos[t] + 1, nkv)),
+    // in every CTA (the positions are few): the first tiles' positions are loaded before the row
+    // work and folded after it, so that the loads are in flight meanwhile.
+    if (tid < a.n_qt) ss.lmq[tid] = 0;
+    constexpr int kEarly = 8;
+    int pw[kEarly];
+#pragma unroll
+    for (int k = 0; k < kEarly; ++k) {  // (volatile: issued here, not sunk past the row work)
+        const int t = k * BM + tid;
+        pw[k] = 0;
+        if (tid < BM && k < a.n_qt && t < a.nt)
+            asm volatile("ld.global.nc.b32 %0, [%1];" : "=r"(pw[k]) : "l"(a.pos + t) : "memory");
+    }
+    step_rows<T>(a, x, fq, fk);
+
+    // Grid barrier: every CTA's row work before any item reads it.  Arrivals are counted; a CTA
+    // leaves once all have arrived and later counts its departure; the last to depart zeroes both
+    // counts for the next launch (every CTA has left the wait by then).  The tiles' windows and
+    // the item enumeration are computed between the arrival and the wait.
+    __syncthreads();
+    // release: the CTA's writes (ordered before by the barrier above) before the arrival; it
+    // waits for those writes to complete, so a thread outside the window loop below makes it
+    if (tid == kProducerWarp * 32)
+        asm volatile("red.release.gpu.global.add.s32 [%0], 1;" ::"l"(x.bar) : "memory");
+    if (tid < BM) {
+        for (int qt = 0; qt < a.n_qt; ++qt) {
+            const int t = qt * BM + tid;
+            int p = 0;
+#pragma unroll
+            for (int k = 0; k < kEarly; ++k)
+                if (k == qt) p = pw[k];
+            if (qt >= kEarly && t < a.nt) p = __ldg(a.pos + t);
+            int L = 0;
+            if (t < a.nt) {
+                L = p < 0 ? 0 : (p + 1 < a.cap ? p + 1 : a.cap);
+                if ((p < 0 || p >= a.cap) && blockIdx.x == 0) flag_error(a.err, MINF_ERRBIT_ATTN_POS);
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) L = max(L, __shfl_xor_sync(0xffffffffu, L, o));
+            if (lane == 0) atomicMax(&ss.lmq[qt], L);
+        }
+    }
+    __syncthreads();
+    if (tid == 0) {
+        // the items: chunks with keys of every tile (chunk 0 always: it writes the output)
+        int acc = 0;
+        for (int q = 0; q < a.n_qt; ++q) {
+            ss.pref[q] = acc;
+            const int nta = (ss.lmq[q] + BN - 1) / BN;
+            const int na = (nta + a.kc_tiles - 1) / a.kc_tiles;
+            acc += na > 1 ? na : 1;
+        }
+        ss.pref[a.n_qt] = acc;
+        // acquire: every other CTA's writes before this CTA's reads after the wait
+        const unsigned long long t0n = gtimer();
+        while (true) {
+            int n;
+            asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(n) : "l"(x.bar) : "memory");
+            if (n >= static_cast<int>(gridDim.x)) break;
+            if (gtimer() - t0n > kWaitBudgetNs) {
+                sm.abort_flag = 1;
+                flag_error(a.err, MINF_ERRBIT_TIMEOUT);
+                break;
+            }
+        }
+    }
+    __syncthreads();
+    // the rows stored by other CTAs are read next by bulk tensor copies (the async proxy), which
+    // the producer thread issues
+    if (warp == kProducerWarp && lane == 0) fence_async_global();
+    // The launch after this one may start: the rows it may stream before its own wait are stored.
+    gdc_launch_dependents();
+
+    const int g = a.nh / a.nk;
+    const int n_items = *abort_flag ? 0 : ss.pref[a.n_qt] * a.nh;
+    // the departure: by the first item's P*V thread while it waits for P(0), else here
+    if (static_cast<int>(blockIdx.x) >= n_items && tid == 0) step_depart(x);
+    for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
+        const int h = item % a.nh, pr = item / a.nh;
+        int qt = 0;
+        while (qt + 1 < a.n_qt && ss.pref[qt + 1] <= pr) ++qt;
+        const int kc = pr - ss.pref[qt];
+        const int lmax = ss.lmq[qt];
+        const int t0 = qt * BM;
+        if (tid == 0) {
+            if (item != static_cast<int>(blockIdx.x)) init_barriers(true);
+            sm.lmax = 0;  // the merge's "last chunk" flag
+        }
+        const int n_tiles_all = (lmax + BN - 1) / BN;
+        const int n_act = (n_tiles_all + a.kc_tiles - 1) / a.kc_tiles;
+        const int tile0 = kc * a.kc_tiles;
+        const int n_tiles = min(n_tiles_all - tile0, a.kc_tiles) > 0 ? min(n_tiles_all - tile0, a.kc_tiles) : 0;
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
+        const Item it = {h, h / g, qt, kc, t0, -1, lmax, n_act, tile0, n_tiles, tmem,
+                         item == static_cast<int>(blockIdx.x) ? &x : nullptr};
+        attend<HDKV, T>(sm, tm_q, tm_k, a, it);
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
+        if (*abort_flag) break;
+    }
+    __syncthreads();
+    if (warp == kProducerWarp) {
+        if (*abort_flag && lane == 0) {
+            // let copies and MMAs that may still be in flight finish before TMEM and shared memory go away
+            const unsigned long long t0n = gtimer();
+            while (gtimer() - t0n < kWaitBudgetNs / 4) {
+            }
+        }
+        __syncwarp();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(tmem_cols<HDKV>())
+                     : "memory");
+    }
+}
+
+static_assert(sizeof(Smem<128>) + sizeof(StepSmem) + 1024 <= 232448, "the fused step fits 227 KB of shared memory");
+
 struct PrefillPlan {
     int n_qt, n_kc, kc_tiles;
-    size_t o_off, ml_off, ticket_off, total;
+    size_t step_off, o_off, ml_off, ticket_off, total;  // step: the fused step's barrier counts
 };
 
 size_t align256p(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
@@ -890,22 +1269,23 @@ PrefillPlan prefill_plan(int nt, int nh, int hd_kv, int cap) {
     p.kc_tiles = static_cast<int>(kc_keys / BN);
     p.n_kc = static_cast<int>((cap + kc_keys - 1) / kc_keys);
     const size_t parts = static_cast<size_t>(p.n_qt) * nh * p.n_kc;
-    p.o_off = 0;
-    p.ml_off = align256p(parts * hd_kv * BM * sizeof(float));
-    p.ticket_off = p.ml_off + align256p(parts * 2 * BM * sizeof(float));
-    p.total = p.ticket_off + align256p(static_cast<size_t>(p.n_qt) * nh * sizeof(int));
+    p.step_off = 0;
+    p.o_off = align256p(2 * sizeof(int));
+    p.ml_off = p.o_off + (p.n_kc > 1 ? align256p(parts * hd_kv * BM * sizeof(float)) : 0);
+    p.ticket_off = p.ml_off + (p.n_kc > 1 ? align256p(parts * 2 * BM * sizeof(float)) : 0);
+    p.total = p.ticket_off + (p.n_kc > 1 ? align256p(static_cast<size_t>(p.n_qt) * nh * sizeof(int)) : 0);
     return p;
 }
 
+// Tensor maps and kernel parameters of a prefill launch, shared by both kernels.
 template <int HDKV, typename T>
-int launch_t(const PrefillArgs &pa, cudaStream_t s) {
-    CUtensorMap tq, tk;
-    if (!make_tensor_map_2d(&tq, pa.q, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, static_cast<uint64_t>(pa.nh) * pa.hd, pa.nt,
+int prefill_setup(const PrefillArgs &pa, CUtensorMap *tq, CUtensorMap *tk, PParams *out, PrefillPlan *plan) {
+    if (!make_tensor_map_2d(tq, pa.q, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, static_cast<uint64_t>(pa.nh) * pa.hd, pa.nt,
                             32, BM, true))
         return MINF_ERR_CUDA;
     if (!std::is_same<T, float>::value)
-        tk = tq;  // binary16 K is read by the softmax threads: the map argument goes unused
-    else if (!make_tensor_map_2d(&tk, pa.k_reg, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4,
+        *tk = *tq;  // binary16 and Q8_0 K are read by the staging warps: the map argument goes unused
+    else if (!make_tensor_map_2d(tk, pa.k_reg, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4,
                                  static_cast<uint64_t>(pa.nk) * HDKV, pa.cap, 32, BN, true))
         return MINF_ERR_CUDA;
     PParams a;
@@ -931,6 +1311,18 @@ int launch_t(const PrefillArgs &pa, cudaStream_t s) {
     a.ws_o = pl.n_kc > 1 ? reinterpret_cast<float *>(ws + pl.o_off) : nullptr;
     a.ws_ml = pl.n_kc > 1 ? reinterpret_cast<float *>(ws + pl.ml_off) : nullptr;
     a.ws_ticket = pl.n_kc > 1 ? reinterpret_cast<int *>(ws + pl.ticket_off) : nullptr;
+    *out = a;
+    *plan = pl;
+    return MINF_OK;
+}
+
+template <int HDKV, typename T>
+int launch_t(const PrefillArgs &pa, cudaStream_t s) {
+    CUtensorMap tq, tk;
+    PParams a;
+    PrefillPlan pl;
+    const int st = prefill_setup<HDKV, T>(pa, &tq, &tk, &a, &pl);
+    if (st != MINF_OK) return st;
     const size_t smem = sizeof(Smem<HDKV>) + 1024;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return MINF_ERR_CUDA;
@@ -956,12 +1348,99 @@ int launch_t(const PrefillArgs &pa, cudaStream_t s) {
     return cudaLaunchKernelEx(&cfg, prefill_kernel<HDKV, T>, tq, tk, a) == cudaSuccess ? MINF_OK : MINF_ERR_CUDA;
 }
 
+// The fused step: MINF_ERR_UNSUPPORTED (nothing launched) where its conditions do not hold.
+template <int HDKV, typename T>
+int launch_step_t(const PrefillArgs &pa, const PrefillStepExtra &xs, cudaStream_t s) {
+    const PrefillPlan plan = prefill_plan(pa.nt, pa.nh, HDKV, pa.cap);
+    if (plan.n_qt > kStepMaxQt || pa.hd % 8 != 0 || pa.hd > 2 * kMaxHalf || !pa.ws || pa.ws_bytes < plan.total ||
+        !aligned16(pa.ws) || !aligned16(xs.q) || !aligned16(xs.k) || !aligned16(xs.v) || !aligned16(pa.k_reg) ||
+        !aligned16(pa.v_reg))
+        return MINF_ERR_UNSUPPORTED;
+    const long long units =
+        static_cast<long long>(pa.nt) * ((pa.hd / 8) * ((pa.nh + kRopeHeads - 1) / kRopeHeads) +
+                                         (HDKV / 8) * ((pa.nk + kRopeHeads - 1) / kRopeHeads) + pa.nk * HDKV / 4);
+    if (units >= (1ll << 30)) return MINF_ERR_UNSUPPORTED;
+    CUtensorMap tq, tk;
+    PParams a;
+    PrefillPlan pl;
+    int st = prefill_setup<HDKV, T>(pa, &tq, &tk, &a, &pl);
+    if (st != MINF_OK) return st;
+    StepParams x;
+    x.q = xs.q;
+    x.k = xs.k;
+    x.v = xs.v;
+    x.k_st = const_cast<void *>(pa.k_reg);
+    x.v_st = const_cast<void *>(pa.v_reg);
+    x.style = xs.style;
+    x.xn = xs.xn;
+    x.hx = xs.h;
+    x.gain = xs.gain;
+    x.n_embd = xs.n_embd;
+    x.norm_vec = (xs.n_embd % 4 == 0) && aligned16(xs.h) && aligned16(xs.xn) && (!xs.gain || aligned16(xs.gain));
+    x.eps = xs.eps;
+    char *ws = static_cast<char *>(pa.ws);
+    x.bar = reinterpret_cast<int *>(ws + pl.step_off);
+    RopeTable rq, rk;
+    rope_table(&rq, pa.hd, xs.theta, xs.freq_scale);
+    rope_table(&rk, HDKV, xs.theta, xs.freq_scale);
+    const size_t smem = sizeof(Smem<HDKV>) + sizeof(StepSmem) + 1024;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return MINF_ERR_CUDA;
+    static int resident[64] = {};  // CTAs that can be resident at once (0: not yet known)
+    static bool no_pdl[64] = {};   // the runtime refused the cooperative launch with early start
+    if (!resident[dev]) {
+        if (cudaFuncSetAttribute(prefill_step_kernel<HDKV, T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(smem)) != cudaSuccess)
+            return MINF_ERR_CUDA;
+        int per_sm = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, prefill_step_kernel<HDKV, T>, kThreadsP, smem) !=
+                cudaSuccess ||
+            per_sm < 1)
+            return MINF_ERR_UNSUPPORTED;
+        resident[dev] = per_sm * sm_count();
+    }
+    const long long items = static_cast<long long>(pl.n_qt) * pa.nh * pl.n_kc;
+    const int grid = static_cast<int>(items < resident[dev] ? items : resident[dev]);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid));
+    cfg.blockDim = dim3(kThreadsP);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeCooperative;  // the grid barrier needs every CTA resident
+    attr[0].val.cooperative = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = no_pdl[dev] ? 1 : 2;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, prefill_step_kernel<HDKV, T>, tq, tk, a, x, rq, rk);
+    if (e != cudaSuccess && !no_pdl[dev]) {
+        (void)cudaGetLastError();
+        no_pdl[dev] = true;
+        cfg.numAttrs = 1;
+        e = cudaLaunchKernelEx(&cfg, prefill_step_kernel<HDKV, T>, tq, tk, a, x, rq, rk);
+    }
+    return e == cudaSuccess ? MINF_OK : MINF_ERR_CUDA;
+}
+
 }  // namespace
 
 size_t prefill_workspace_bytes(int nt, int nh, int hd_kv, int cap) {
     if (nt <= 0 || nh <= 0 || hd_kv <= 0 || cap <= 0) return 0;
-    const PrefillPlan p = prefill_plan(nt, nh, hd_kv, cap);
-    return p.n_kc > 1 ? p.total : 0;
+    return prefill_plan(nt, nh, hd_kv, cap).total;
+}
+
+int launch_prefill_step(const PrefillArgs &pa, const PrefillStepExtra &x, cudaStream_t s) {
+    if (pa.nt == 0) return MINF_OK;
+    if ((static_cast<long long>(pa.nh) * pa.hd) % 4 != 0) return MINF_ERR_UNSUPPORTED;
+    if (pa.kv == kKvF16) {
+        if (pa.hd_kv == 64) return launch_step_t<64, __half>(pa, x, s);
+        if (pa.hd_kv == 128) return launch_step_t<128, __half>(pa, x, s);
+    } else if (pa.kv == kKvF32) {
+        if (pa.hd_kv == 64) return launch_step_t<64, float>(pa, x, s);
+        if (pa.hd_kv == 128) return launch_step_t<128, float>(pa, x, s);
+    }
+    return MINF_ERR_UNSUPPORTED;
 }
 
 int launch_prefill(const PrefillArgs &pa, cudaStream_t s) {

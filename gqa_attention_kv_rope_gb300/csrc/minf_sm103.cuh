@@ -28,6 +28,12 @@ __device__ __forceinline__ void mbar_init(unsigned long long *b, uint32_t count)
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(su32(b)), "r"(count) : "memory");
 }
 
+// Ends an mbarrier's use (all its phases complete and no wait pending), so that its word can
+// be initialized again.
+__device__ __forceinline__ void mbar_inval(unsigned long long *b) {
+    asm volatile("mbarrier.inval.shared::cta.b64 [%0];" ::"r"(su32(b)) : "memory");
+}
+
 // Makes barrier initialisation visible to the async proxy (TMA, tensor cores).
 __device__ __forceinline__ void mbar_init_fence() {
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
