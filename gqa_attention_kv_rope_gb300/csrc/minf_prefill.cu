@@ -1131,6 +1131,10 @@ __global__ void __launch_bounds__(kThreadsP, 1)
     tc_fence_after();
     const uint32_t tmem = sm.tmem_base;
     gdc_wait();  // every input (pos included) and the workspace, only after the launch before this one
+    // This call's merge tickets start at zero whatever an earlier call of another shape left in
+    // their words (its partial outputs, say): no item takes a ticket before the grid barrier.
+    if (a.ws_ticket)
+        for (int i = blockIdx.x * kThreadsP + tid; i < a.n_qt * a.nh; i += gridDim.x * kThreadsP) a.ws_ticket[i] = 0;
 
     // Every query tile's widest window ("11 . Attention...", §3.2.4: vl = min(pos[t] + 1, nkv)),
     // in every CTA (the positions are few): the first tiles' positions are loaded before the row

@@ -200,13 +200,16 @@ MINF_API int minf_gqa_attn_decode_static_ws(float *out, const float *q, const fl
  * (store before attention: the tokens' own rows must already be appended).
  * q: [nt, n_head, hd]; out: [nt, n_head*hd_kv].  Positions are arbitrary
  * (a prefill that continues an existing cache passes pos = n_past..).
- * The QK^T and PV products run on the tensor cores with split-precision TF32
- * operands (hi + lo halves, three MMAs per product) and fp32 accumulation, which
- * matches an fp32 evaluation to a few 1e-6; max, exp and sums run in fp32.
+ * The QK^T and PV products run on the tensor cores with split-precision operands
+ * (hi + lo halves, three MMAs per product: binary16 halves of power-of-two-scaled
+ * q and k rows for QK^T, TF32 halves for PV) and fp32 accumulation, which matches
+ * an fp32 evaluation to a few 1e-6; max, exp and sums run in fp32.
  * The keys of a query tile are cut into chunks processed by separate CTAs whose
  * partials are folded at the end: ws must hold minf_attn_prefill_workspace_bytes
- * (zero-filled before its first use; every call leaves it zeroed; concurrent
- * calls must not share it); it may be NULL when that size is 0.
+ * (zero-filled before its first use; every call leaves its counters at zero, the
+ * partial outputs not, so a workspace used for another shape, or for decode, must
+ * be zero-filled again first; concurrent calls must not share it); it may be NULL
+ * when no query tile has more than one key chunk.
  * Device errors: MINF_ERRBIT_ATTN_POS, MINF_ERRBIT_TIMEOUT.
  * Errors: as minf_gqa_attn_decode.
  */
@@ -216,7 +219,7 @@ MINF_API int minf_gqa_attn_prefill(float *out, const float *q, const float *k_re
                           minf_stream_t stream);
 
 /* Workspace bytes minf_gqa_attn_prefill (and a layer step with nt > 1) needs for
- * nt tokens over regions of cap rows (0 if none). */
+ * nt tokens over regions of cap rows (at least 256 for nt > 0; 0 for nt <= 0). */
 MINF_API size_t minf_attn_prefill_workspace_bytes(int nt, int n_head, int n_kv_head, int hd_kv, int cap);
 
 /*
@@ -226,17 +229,26 @@ MINF_API size_t minf_attn_prefill_workspace_bytes(int nt, int n_head, int n_kv_h
  * rotated k and v appended at pos into the regions [cap, W]; out [nt, n_head*hd_kv]
  * = attention with scale 1/sqrt(hd) ([P1] §2.4).  nt == 1 runs the split-KV
  * decode path (a single launch for the supported geometries), nt > 1 the
- * tensor-core prefill path.  ws/ws_bytes: for nt == 1 at least
+ * tensor-core prefill path: a single cooperative launch (the row work over the
+ * whole grid, a grid barrier, then the attention) when hd % 8 == 0, hd <= 256,
+ * nt <= 8192, q, k, v and the regions are 16-byte aligned and ws is given, else
+ * a launch for RMSNorm, RoPE and the store followed by the attention launch.
+ * ws/ws_bytes: for nt == 1 at least
  * minf_attn_decode_workspace_bytes(1, n_head, n_kv_head, hd_kv, cap), for nt > 1
- * at least minf_attn_prefill_workspace_bytes(nt, n_head, n_kv_head, hd_kv, cap).
+ * at least minf_attn_prefill_workspace_bytes(nt, n_head, n_kv_head, hd_kv, cap);
+ * zero-filled before its first use.  The single-launch prefill keeps its first
+ * 256 bytes (the grid barrier's counts) at zero between calls and resets its own
+ * merge counters, so consecutive nt > 1 steps of any shape may share one
+ * workspace; a workspace that decode has used must be zero-filled again first.
  * Early start: the nt == 1 path is a programmatic dependent launch that reads pos and
  * begins streaming the cached rows [0, pos) of the regions before the launch just before
  * it on the stream has finished (h, gain, q, k, v, ws and every output only after): pos
  * and those rows must not be written by that launch (a host-to-device copy is not a
- * launch).  For nt > 1 the first launch (RMSNorm, RoPE and the store) is a programmatic
- * dependent launch too; it touches memory only once the launch before it has finished, but
- * the attention launch after it reads pos as soon as every block of the first has started:
- * pos must not be written by the launch just before the step on either path.
+ * launch).  For nt > 1 the first launch is a programmatic dependent launch too; it touches
+ * memory only once the launch before it has finished (on the two-launch path the attention
+ * launch after it reads pos as soon as every block of the first has started): pos must not be
+ * written by the launch just before the step on either path.  A launch after an nt > 1 step
+ * may start early once the step's rows are stored (its grid barrier).
  * Device errors: any of the bits above.
  */
 MINF_API int minf_layer_attn_step(float *xn, const float *h, const float *gain, float eps, int n_embd,
