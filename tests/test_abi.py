@@ -97,3 +97,22 @@ def test_workspace_sizes(lib):
     b = lib.minf_attn_decode_workspace_bytes(1, 16, 8, 128, 40961)
     assert 0 < a <= b
     assert lib.minf_attn_decode_workspace_bytes(64, 16, 8, 128, 8705) > b // 64
+
+
+def test_prefill_workspace_sizes(lib):
+    """Every nt > 0 needs at least the single-launch step's 256 bytes of grid-barrier counts;
+    more tokens or a longer region never need less."""
+    from gqa_attention_kv_rope_gb300 import binding as b
+
+    assert lib.minf_attn_prefill_workspace_bytes(0, 14, 2, 64, 1024) == 0
+    sizes = [lib.minf_attn_prefill_workspace_bytes(nt, 14, 2, 64, 1024) for nt in (1, 2, 128, 129, 512, 900)]
+    assert sizes[0] >= 256 and sizes == sorted(sizes)
+    assert lib.minf_attn_prefill_workspace_bytes(512, 14, 2, 64, 4096) >= sizes[4]
+    # the layer step refuses a short workspace before it launches anything
+    P = ctypes.c_void_p
+    fake = P(0x1000)
+    need = lib.minf_attn_prefill_workspace_bytes(512, 14, 2, 64, 1024)
+    assert lib.minf_layer_attn_step(fake, fake, fake, 1e-6, 896, fake, fake, fake, fake, 512, fake, fake, 1024, 14, 2,
+                                    64, 64, 1e6, 1.0, 0, fake, fake, need - 1, fake, None) == b.MINF_ERR_WORKSPACE
+    assert lib.minf_layer_attn_step(fake, fake, fake, 1e-6, 896, fake, fake, fake, fake, 512, fake, fake, 1024, 14, 2,
+                                    64, 64, 1e6, 1.0, 0, fake, None, 0, fake, None) == b.MINF_ERR_WORKSPACE
