@@ -30,7 +30,7 @@
 // issues the P*V products (each thread commits its own).
 //
 // Pipelining.  S has two TMEM buffers and the producer issues S(i+1) as soon as key tile i+1
-// is split (and P(i-1) has been published, so S(i-1)'s buffer is free), without waiting for
+// is converted (and P(i-1) has been published, so S(i-1)'s buffer is free), without waiting for
 // P(i)V(i), which the other thread issues: the tensor cores form the next scores while the
 // softmax warps work on the current ones, and neither product waits behind the other's issue
 // (a thread issues a tensor-core instruction only every ~35-50 ns).  O_t has two TMEM buffers as well: the softmax warps publish
@@ -38,8 +38,14 @@
 // O_t(i) (with hd_kv 64 P also has two buffers in shared memory; with hd_kv 128, where shared
 // memory holds one, P(i) waits until O_t(i-1) has read P(i-1)).
 //
-// Every mbarrier wait is bounded by a 200 ms global-timer budget; a wait that expires sets
-// MINF_ERRBIT_TIMEOUT, makes every role leave its loop, and the CTA still frees its TMEM.
+// Two kernels run these items.  prefill_kernel is one CTA per item (the attention alone, after
+// a separate RoPE + store launch).  prefill_step_kernel is a whole prefill layer step in one
+// cooperative launch of at most one CTA an SM: the step's row work (RMSNorm, RoPE on q and k,
+// the K/V store) over the whole grid, a grid barrier, then the items that have keys in turn.
+//
+// Every mbarrier wait and the grid barrier are bounded by a 200 ms global-timer budget; a wait
+// that expires sets MINF_ERRBIT_TIMEOUT, makes every role leave its loop, and the CTA still
+// frees its TMEM.
 #include <cuda.h>
 #include <cuda_fp16.h>
 
