@@ -238,13 +238,36 @@ def measured_peaks():
         return 6800.0, "fallback"
 
 
-def decode_source_sha256() -> str:
-    """Hash of the decode kernel's sources (the kernel header, then its launcher)."""
+def measured_bf16_peak():
+    """Dense bf16 tensor throughput (burst) measured on the GB300s, TFLOP/s."""
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 1900.0, "fallback"
+
+
+def source_sha256(files) -> str:
     h = hashlib.sha256()
-    for f in ("minf_decode.cuh", "minf_decode.cu"):
+    for f in files:
         with open(os.path.join(ROOT, "gqa_attention_kv_rope_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()
+
+
+def decode_source_sha256() -> str:
+    """Hash of the decode kernel's sources (the kernel header, then its launcher)."""
+    return source_sha256(("minf_decode.cuh", "minf_decode.cu"))
+
+
+def prefill_profile_record():
+    """The prefill step's ncu tensor-pipe figures from the committed summary, valid only while
+    the prefill source is unchanged since the counters were taken."""
+    try:
+        rec = json.load(open(os.path.join(ROOT, "profiles", "prefill_step_tensor_pipe.json")))
+        return rec if rec.get("kernel_src_sha256") == source_sha256(("minf_prefill.cu",)) else None
+    except (OSError, ValueError):
+        return None
 
 
 def decode_traffic_record():
@@ -328,9 +351,12 @@ def views(S, layer):
 
 
 def decode_step(m, S, layers=None):
+    """The step's layers, each one launch.  The early-start (_chained) forms: the launch before
+    each layer step is the previous layer's, which writes neither the position nor the rows
+    the next layer streams before its dependency wait."""
     g = S["g"]
-    fn = {2: m.binding.minf_layer_attn_step_f16, 1: m.binding.minf_layer_attn_step_q8}.get(
-        S["regions"].k.element_size(), m.binding.minf_layer_attn_step)
+    fn = {2: m.binding.minf_layer_attn_step_chained_f16, 1: m.binding.minf_layer_attn_step_chained_q8}.get(
+        S["regions"].k.element_size(), m.binding.minf_layer_attn_step_chained)
     for layer in range(g.n_layer) if layers is None else layers:
         h, q, k, v, xn, out = views(S, layer)
         K, V = S["regions"].view(layer)
@@ -463,9 +489,10 @@ def run_single_step(m, torch, wl, dev, reps=1000):
     out = torch.empty(1, g.out_width, device=dev)
     ws = m.kv.decode_workspace(1, g.n_head, g.n_kv_head, g.hd_kv, cap, device=dev)
     stream = torch.cuda.Stream()
-    fn = lambda: m.binding.minf_layer_attn_step(xn, d["h"], d["gain"], g.eps, d["q"], d["k"], d["v"], pos, K, V,
-                                                g.n_head, g.n_kv_head, g.hd, g.hd_kv, g.theta, 1.0, 0, out,
-                                                ws, err)
+    # early start: the launch before the replay (a sleep kernel) writes neither pos nor cached rows
+    fn = lambda: m.binding.minf_layer_attn_step_chained(xn, d["h"], d["gain"], g.eps, d["q"], d["k"], d["v"], pos, K,
+                                                        V, g.n_head, g.n_kv_head, g.hd, g.hd_kv, g.theta, 1.0, 0,
+                                                        out, ws, err)
     graph = capture(torch, stream, fn)
     for _ in range(20):
         graph.replay()
@@ -485,8 +512,10 @@ def run_single_step(m, torch, wl, dev, reps=1000):
     return round(statistics.median(us), 2)
 
 
-def run_prefill(m, torch, wl, dev, steps):
-    """Causal prefill, Qwen2.5-0.5B shape, 24 layers, 512 tokens at positions 0..511."""
+def setup_prefill(m, torch, wl, dev):
+    """Causal prefill, Qwen2.5-0.5B shape, 24 layers, 512 tokens at positions 0..511: each
+    layer's seeded inputs (kept unrotated in `orig`, since the step rotates q and k in place),
+    zeroed regions, and the step function the bench captures."""
     g = wl.QWEN25_05B
     nt, cap = wl.PREFILL_TOKENS, wl.PREFILL_TOKENS + wl.KV_HEADROOM_ROWS
     regions = m.kv.KvRegions(g.n_layer, g.row_width, cap, device=dev)
@@ -498,6 +527,7 @@ def run_prefill(m, torch, wl, dev, steps):
         d["xn"] = torch.empty_like(d["h"])
         d["out"] = torch.empty(nt, g.out_width, device=dev)
         L.append(d)
+    orig = [{k: d[k].clone() for k in ("q", "k")} for d in L]
     pos = torch.arange(nt, dtype=torch.int32, device=dev)
     err = torch.zeros(1, dtype=torch.int32, device=dev)
     ws = m.kv.prefill_workspace(nt, g.n_head, g.n_kv_head, g.hd_kv, cap, device=dev)
@@ -510,8 +540,26 @@ def run_prefill(m, torch, wl, dev, steps):
                                            g.n_head, g.n_kv_head, g.hd, g.hd_kv, g.theta, 1.0, 0, d["out"], ws,
                                            err)
 
+    def reset():  # the inputs as drawn (q and k unrotated) before a checked replay
+        for d, o in zip(L, orig):
+            d["q"].copy_(o["q"])
+            d["k"].copy_(o["k"])
+
+    return {"g": g, "nt": nt, "cap": cap, "regions": regions, "layers": L, "pos": pos, "err": err, "ws": ws,
+            "step": step, "reset": reset}
+
+
+def prefill_flops_per_layer(g, nt):
+    """Useful work of one causal prefill layer from position 0: QK^T and PV over each token's
+    window, 2 flops a multiply-add each, 4 * n_head * hd * sum_t (t + 1)."""
+    return 4 * g.n_head * g.hd * (nt * (nt + 1) // 2)
+
+
+def run_prefill(m, torch, wl, dev, steps):
+    P = setup_prefill(m, torch, wl, dev)
+    g, nt = P["g"], P["nt"]
     stream = torch.cuda.Stream()
-    graph = capture(torch, stream, step)
+    graph = capture(torch, stream, P["step"])
     flush = torch.empty(2 * L2_BYTES // 4, device=dev)
     times = []
     for i in range(steps + 3):
@@ -525,12 +573,16 @@ def run_prefill(m, torch, wl, dev, steps):
         if i >= 3:
             times.append(a.elapsed_time(b))
     ms = statistics.median(times)
+    del graph, flush
+    P.clear()
+    torch.cuda.empty_cache()
     return round(nt / (ms * 1e-3), 1), round(ms * 1e3 / g.n_layer, 2)
 
 
-def run_decode_loop(m, torch, wl, dev):
-    """Decode loop, Qwen3-0.6B shape: 511-token prefill into 1023-row regions, then 64
-    decode steps (28 layers each) replayed from one graph with pos 511..574."""
+def setup_decode_loop(m, torch, wl, dev):
+    """Decode loop, Qwen3-0.6B shape: seeded inputs for all 511 + 64 tokens of every layer
+    (h, q, k, v; gains per layer), 1023-row regions, the prefill launches and the decode step
+    the bench captures.  Token t's inputs are the same whether it is prefilled or decoded."""
     g = wl.QWEN3_06B
     n0, cap, steps = wl.DECODE_LOOP_PROMPT, wl.DECODE_LOOP_PROMPT + wl.KV_HEADROOM_ROWS, wl.DECODE_LOOP_STEPS
     regions = m.kv.KvRegions(g.n_layer, g.row_width, cap, device=dev)
@@ -539,31 +591,54 @@ def run_decode_loop(m, torch, wl, dev):
     err = torch.zeros(1, dtype=torch.int32, device=dev)
     ws = m.kv.prefill_workspace(n0, g.n_head, g.n_kv_head, g.hd_kv, cap, device=dev)
     pos_p = torch.arange(n0, dtype=torch.int32, device=dev)
-    for layer in range(g.n_layer):
-        d = {k: v.to(dev) for k, v in wl.layer_inputs(g, "decode-loop", layer, n0 + steps).items()}
-        K, V = regions.view(layer)
-        xn = torch.empty(n0, g.n_embd, device=dev)
-        out = torch.empty(n0, g.out_width, device=dev)
-        m.binding.minf_layer_attn_step(xn, d["h"][:n0].contiguous(), d["gain"], g.eps, d["q"][:n0].contiguous(),
-                                       d["k"][:n0].contiguous(), d["v"][:n0].contiguous(), pos_p, K, V, g.n_head,
-                                       g.n_kv_head, g.hd, g.hd_kv, g.theta, 1.0, 0, out, ws, err)
+    inp = [{k: v.to(dev) for k, v in wl.layer_inputs(g, "decode-loop", layer, n0 + steps).items()}
+           for layer in range(g.n_layer)]
+    pre = [{"h": d["h"][:n0].contiguous(), "q": d["q"][:n0].contiguous(), "k": d["k"][:n0].contiguous(),
+            "v": d["v"][:n0].contiguous(), "xn": torch.empty(n0, g.n_embd, device=dev),
+            "out": torch.empty(n0, g.out_width, device=dev)} for d in inp]
     pos = torch.tensor([n0], dtype=torch.int32, device=dev)
     wsd = m.kv.decode_workspace(1, g.n_head, g.n_kv_head, g.hd_kv, cap, device=dev)
-    bufs = [{"h": torch.randn(1, g.n_embd, device=dev), "gain": torch.ones(g.n_embd, device=dev),
-             "q": torch.randn(1, g.q_width, device=dev), "k": torch.randn(1, g.row_width, device=dev),
-             "v": torch.randn(1, g.row_width, device=dev), "xn": torch.empty(1, g.n_embd, device=dev),
-             "out": torch.empty(1, g.out_width, device=dev)} for _ in range(g.n_layer)]
+    bufs = [{"h": torch.empty(1, g.n_embd, device=dev), "q": torch.empty(1, g.q_width, device=dev),
+             "k": torch.empty(1, g.row_width, device=dev), "v": torch.empty(1, g.row_width, device=dev),
+             "xn": torch.empty(1, g.n_embd, device=dev), "out": torch.empty(1, g.out_width, device=dev)}
+            for _ in range(g.n_layer)]
 
-    def step():
+    def prefill():
         for layer in range(g.n_layer):
-            b = bufs[layer]
+            d, b = inp[layer], pre[layer]
             K, V = regions.view(layer)
-            m.binding.minf_layer_attn_step(b["xn"], b["h"], b["gain"], g.eps, b["q"], b["k"], b["v"], pos, K, V,
-                                           g.n_head, g.n_kv_head, g.hd, g.hd_kv, g.theta, 1.0, 0, b["out"], wsd,
+            m.binding.minf_layer_attn_step(b["xn"], b["h"], d["gain"], g.eps, b["q"], b["k"], b["v"], pos_p, K, V,
+                                           g.n_head, g.n_kv_head, g.hd, g.hd_kv, g.theta, 1.0, 0, b["out"], ws,
                                            err)
 
+    def step():  # early start: each layer follows the previous layer's launch
+        for layer in range(g.n_layer):
+            d, b = inp[layer], bufs[layer]
+            K, V = regions.view(layer)
+            m.binding.minf_layer_attn_step_chained(b["xn"], b["h"], d["gain"], g.eps, b["q"], b["k"], b["v"], pos,
+                                                   K, V, g.n_head, g.n_kv_head, g.hd, g.hd_kv, g.theta, 1.0, 0,
+                                                   b["out"], wsd, err)
+
+    def load(t):  # token t's inputs into the step's buffers (device copies, before the replay)
+        for d, b in zip(inp, bufs):
+            for k in ("h", "q", "k", "v"):
+                b[k].copy_(d[k][t:t + 1])
+
+    return {"g": g, "n0": n0, "cap": cap, "steps": steps, "regions": regions, "inputs": inp, "prefill_bufs": pre,
+            "bufs": bufs, "pos": pos, "err": err, "prefill": prefill, "step": step, "load": load}
+
+
+def run_decode_loop(m, torch, wl, dev):
+    """Decode loop, Qwen3-0.6B shape: 511-token prefill into 1023-row regions, then 64
+    decode steps (28 layers each) replayed from one graph with pos 511..574."""
+    D = setup_decode_loop(m, torch, wl, dev)
+    g, n0, steps, pos = D["g"], D["n0"], D["steps"], D["pos"]
+    D["load"](n0)
+    torch.cuda.synchronize()
     stream = torch.cuda.Stream()
-    graph = capture(torch, stream, step)  # the capture's warm-up wrote row 511: rewritten below
+    graph = capture(torch, stream, D["step"])  # the capture's warm-up appended row 511 before the prefill
+    D["prefill"]()
+    torch.cuda.synchronize()
     pos_host = torch.empty(1, dtype=torch.int32).pin_memory()
     times, kv = [], 0
     for i in range(steps):
@@ -571,6 +646,7 @@ def run_decode_loop(m, torch, wl, dev):
         pos_host.fill_(p)
         a, b = Timer(torch, stream).pair()
         with torch.cuda.stream(stream):
+            D["load"](p)
             pos.copy_(pos_host, non_blocking=True)
             a.record(stream)
             graph.replay()
@@ -579,8 +655,12 @@ def run_decode_loop(m, torch, wl, dev):
         times.append(a.elapsed_time(b))
         kv += g.n_layer * 2 * (p + 1) * g.row_width * 4
     total_ms = sum(times)
+    err = int(D["err"].item())
+    del graph
+    D.clear()
+    torch.cuda.empty_cache()
     return {"step_us_median": round(statistics.median(times) * 1e3, 2),
-            "kv_read_gbs": round(kv / (total_ms * 1e-3) / 1e9, 1), "err": int(err.item())}
+            "kv_read_gbs": round(kv / (total_ms * 1e-3) / 1e9, 1), "err": err}
 
 
 def run_batched_paged(m, torch, wl, dev, steps, block_rows=64):
@@ -810,9 +890,14 @@ def run_elementwise(m, torch, dev, reps=20):
     ms_rms = timed(lambda: m.binding.minf_rms_norm(y, x, w, 1e-6))
     ms_rms_l = timed(lambda: m.binding.minf_rms_norm(yl, xl, w, 1e-6))
     ms_silu = timed(lambda: m.binding.minf_silu_mul(o, g, u))
-    res = {"rms_norm_4096x1024_gbs": round((2 * x.numel() + w.numel()) * 4 / (ms_rms * 1e-3) / 1e9, 1),
-           "rms_norm_32768x1024_gbs": round((2 * xl.numel() + w.numel()) * 4 / (ms_rms_l * 1e-3) / 1e9, 1),
-           "silu_mul_64Mi_gbs": round(3 * n * 4 / (ms_silu * 1e-3) / 1e9, 1)}
+    peak, _ = measured_peaks()
+    rms_l = (2 * xl.numel() + w.numel()) * 4 / (ms_rms_l * 1e-3) / 1e9
+    silu = 3 * n * 4 / (ms_silu * 1e-3) / 1e9
+    res = {"hbm": {"rms_norm_32768x1024_gbs": round(rms_l, 1), "rms_norm_32768x1024_frac": round(rms_l / peak, 4),
+                   "silu_mul_64Mi_gbs": round(silu, 1), "silu_mul_64Mi_frac": round(silu / peak, 4)},
+           # 16 MiB each way fits L2 (129 MB): a latency-bound case, not an HBM figure
+           "l2_resident": {"rms_norm_4096x1024_gbs": round((2 * x.numel() + w.numel()) * 4 / (ms_rms * 1e-3) / 1e9,
+                                                           1)}}
     del flush, x, y, xl, yl, g, u, o
     return res
 
@@ -954,6 +1039,21 @@ def main(argv=None):
         tok_s, layer_us = run_prefill(m, torch, wl, dev, max(5, args.steps // 2))
         secondary["prefill_tok_s"] = tok_s
         secondary["prefill_layer_us"] = layer_us
+        flops = prefill_flops_per_layer(wl.QWEN25_05B, wl.PREFILL_TOKENS)
+        bf16, bf16_kind = measured_bf16_peak()
+        useful = flops / (layer_us * 1e-6) / 1e12
+        prof = prefill_profile_record()
+        secondary["prefill"] = {
+            "tok_s": tok_s, "layer_us": layer_us, "flops_per_layer": flops,
+            "useful_tflops": round(useful, 2),
+            "executed_tflops": round(3 * useful, 2),
+            "peak_tflops": round(bf16 / 2, 1),
+            "peak_derivation": f"TF32 dense = {bf16_kind} bf16 burst ({bf16} TFLOP/s) x 1/2, the nominal "
+                               "TF32:bf16 ratio (1.1 : 2.25 PFLOP/s dense); only bf16 is measured",
+            "frac": round(useful / (bf16 / 2), 4),
+            "executed_note": "each product is three split-precision MMAs (hi*hi + hi*lo + lo*hi)",
+            "ncu_tensor_pipe_pct": prof.get("tensor_pipe_pct_of_active") if prof else None,
+            "ncu_record": prof.get("summary") if prof else None}
         secondary["decode_loop"] = run_decode_loop(m, torch, wl, dev)
         secondary["batched_decode"] = run_batched(m, torch, wl, dev, max(3, args.steps // 4))
         secondary["batched_decode_paged"] = run_batched_paged(m, torch, wl, dev, max(3, args.steps // 4))

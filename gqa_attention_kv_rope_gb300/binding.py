@@ -29,6 +29,8 @@ ERRBIT_STORE_POS = 0x1
 ERRBIT_ROPE_POS = 0x2
 ERRBIT_ATTN_POS = 0x4
 ERRBIT_TIMEOUT = 0x8
+ERRBIT_BLOCK = 0x10
+ERRBIT_WORKSPACE = 0x20
 
 _P = ctypes.c_void_p
 _I = ctypes.c_int
@@ -51,6 +53,13 @@ _SIGS = {
     "minf_gqa_attn_prefill": ([_P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _I, _F, _P, _SZ, _P, _P], _I),
     "minf_layer_attn_step": ([_P, _P, _P, _F, _I, _P, _P, _P, _P, _I, _P, _P, _I, _I, _I, _I, _I,
                               _F, _F, _I, _P, _P, _SZ, _P, _P], _I),
+    # the same step with early start (the launch before writes neither pos nor cached rows)
+    "minf_layer_attn_step_chained": ([_P, _P, _P, _F, _I, _P, _P, _P, _P, _I, _P, _P, _I, _I, _I, _I, _I,
+                                      _F, _F, _I, _P, _P, _SZ, _P, _P], _I),
+    "minf_layer_attn_step_chained_f16": ([_P, _P, _P, _F, _I, _P, _P, _P, _P, _I, _P, _P, _I, _I, _I, _I, _I,
+                                          _F, _F, _I, _P, _P, _SZ, _P, _P], _I),
+    "minf_layer_attn_step_chained_q8": ([_P, _P, _P, _F, _I, _P, _P, _P, _P, _I, _P, _P, _I, _I, _I, _I, _I,
+                                         _F, _F, _I, _P, _P, _SZ, _P, _P], _I),
     "minf_layer_attn_step_batched": ([_P, _P, _P, _F, _I, _P, _P, _P, _P, _I, _P, _P, _P, _P, _I, _I64,
                                       _I, _I, _I, _I, _F, _F, _I, _P, _P, _SZ, _P, _P], _I),
     "minf_silu_mul": ([_P, _P, _P, _I64, _P], _I),
@@ -239,16 +248,40 @@ def minf_gqa_attn_prefill(out, q, k_reg, v_reg, pos, n_head, n_kv_head, hd, hd_k
         "minf_gqa_attn_prefill")
 
 
-def minf_layer_attn_step(xn, h, gain, eps, q, k, v, pos, k_reg, v_reg, n_head, n_kv_head, hd, hd_kv,
-                         theta, freq_scale, style, out, ws, err, stream=None):
+def _layer_step(name, reg_dtype, xn, h, gain, eps, q, k, v, pos, k_reg, v_reg, n_head, n_kv_head, hd, hd_kv,
+                theta, freq_scale, style, out, ws, err, stream):
     nt, n_embd = h.shape
     cap = k_reg.shape[0]
-    _check(lib().minf_layer_attn_step(
+    _check(getattr(lib(), name)(
         _dev(xn, name="xn"), _dev(h, name="h"), _dev(gain, name="gain"), eps, n_embd,
         _dev(q, name="q"), _dev(k, name="k"), _dev(v, name="v"), _dev(pos, torch.int32, "pos"), nt,
-        _dev(k_reg, name="k_reg"), _dev(v_reg, name="v_reg"), cap, n_head, n_kv_head, hd, hd_kv,
+        _dev(k_reg, reg_dtype, "k_reg"), _dev(v_reg, reg_dtype, "v_reg"), cap, n_head, n_kv_head, hd, hd_kv,
         theta, freq_scale, style, _dev(out, name="out"), _dev(ws, torch.uint8, "ws"), _nbytes(ws),
-        _dev(err, torch.int32, "err"), _stream(stream)), "minf_layer_attn_step")
+        _dev(err, torch.int32, "err"), _stream(stream)), name)
+
+
+def minf_layer_attn_step(xn, h, gain, eps, q, k, v, pos, k_reg, v_reg, n_head, n_kv_head, hd, hd_kv,
+                         theta, freq_scale, style, out, ws, err, stream=None):
+    _layer_step("minf_layer_attn_step", torch.float32, xn, h, gain, eps, q, k, v, pos, k_reg, v_reg, n_head,
+                n_kv_head, hd, hd_kv, theta, freq_scale, style, out, ws, err, stream)
+
+
+def minf_layer_attn_step_chained(xn, h, gain, eps, q, k, v, pos, k_reg, v_reg, n_head, n_kv_head, hd, hd_kv,
+                                 theta, freq_scale, style, out, ws, err, stream=None):
+    _layer_step("minf_layer_attn_step_chained", torch.float32, xn, h, gain, eps, q, k, v, pos, k_reg, v_reg,
+                n_head, n_kv_head, hd, hd_kv, theta, freq_scale, style, out, ws, err, stream)
+
+
+def minf_layer_attn_step_chained_f16(xn, h, gain, eps, q, k, v, pos, k_reg, v_reg, n_head, n_kv_head, hd, hd_kv,
+                                     theta, freq_scale, style, out, ws, err, stream=None):
+    _layer_step("minf_layer_attn_step_chained_f16", torch.float16, xn, h, gain, eps, q, k, v, pos, k_reg, v_reg,
+                n_head, n_kv_head, hd, hd_kv, theta, freq_scale, style, out, ws, err, stream)
+
+
+def minf_layer_attn_step_chained_q8(xn, h, gain, eps, q, k, v, pos, k_reg, v_reg, n_head, n_kv_head, hd, hd_kv,
+                                    theta, freq_scale, style, out, ws, err, stream=None):
+    _layer_step("minf_layer_attn_step_chained_q8", torch.uint8, xn, h, gain, eps, q, k, v, pos, k_reg, v_reg,
+                n_head, n_kv_head, hd, hd_kv, theta, freq_scale, style, out, ws, err, stream)
 
 
 def minf_layer_attn_step_batched(xn, h, gain, eps, q, k, v, pos, k_arena, v_arena, seq_row_off, seq_cap,

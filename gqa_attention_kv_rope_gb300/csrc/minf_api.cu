@@ -369,7 +369,8 @@ static int layer_attn_step(float *xn, const float *h, const float *gain, float e
                            float *q, float *k, const float *v, const int32_t *pos, int nt,
                            void *k_reg, void *v_reg, int kv, int cap, int n_head, int n_kv_head, int hd,
                            int hd_kv, float theta, float freq_scale, int style, float *out,
-                           void *ws, size_t ws_bytes, int32_t *err, minf_stream_t stream) {
+                           void *ws, size_t ws_bytes, int32_t *err, minf_stream_t stream,
+                           bool chained = false) {
     int st = check_attn(n_head, n_kv_head, hd, hd_kv);
     if (st != MINF_OK) return st;
     if (!xn || !h || n_embd <= 0 || nt < 0 || cap <= 0 || (style != 0 && style != 1))
@@ -388,7 +389,9 @@ static int layer_attn_step(float *xn, const float *h, const float *gain, float e
         // one launch: RMSNorm, RoPE on q and k, the K/V append and split-KV attention
         DecodeArgs d = decode_args(out, q, k_reg, v_reg, kv, nullptr, nullptr, cap, pos, 1, n_head,
                                    n_kv_head, hd, hd_kv, scale, ws, ws_bytes, err);
-        DecodeStepExtra x = {k, v, xn, h, gain, eps, theta, freq_scale, n_embd, style, true};
+        // a programmatic dependent launch either way (its start overlaps the launch before it);
+        // chained: positions and cached rows read before the dependency wait
+        DecodeStepExtra x = {k, v, xn, h, gain, eps, theta, freq_scale, n_embd, style, true, chained};
         return launch_decode_step(d, x, s);
     }
     if (nt > 1 && kv != kKvQ8) {
@@ -437,6 +440,35 @@ int minf_layer_attn_step_f16(float *xn, const float *h, const float *gain, float
                            n_kv_head, hd, hd_kv, theta, freq_scale, style, out, ws, ws_bytes, err, stream);
 }
 
+// The same steps with early start (the launch before writes neither pos nor cached rows).
+int minf_layer_attn_step_chained(float *xn, const float *h, const float *gain, float eps, int n_embd, float *q,
+                                 float *k, const float *v, const int32_t *pos, int nt, float *k_reg, float *v_reg,
+                                 int cap, int n_head, int n_kv_head, int hd, int hd_kv, float theta,
+                                 float freq_scale, int style, float *out, void *ws, size_t ws_bytes, int32_t *err,
+                                 minf_stream_t stream) {
+    return layer_attn_step(xn, h, gain, eps, n_embd, q, k, v, pos, nt, k_reg, v_reg, kKvF32, cap, n_head,
+                           n_kv_head, hd, hd_kv, theta, freq_scale, style, out, ws, ws_bytes, err, stream, true);
+}
+
+int minf_layer_attn_step_chained_f16(float *xn, const float *h, const float *gain, float eps, int n_embd, float *q,
+                                     float *k, const float *v, const int32_t *pos, int nt, uint16_t *k_reg,
+                                     uint16_t *v_reg, int cap, int n_head, int n_kv_head, int hd, int hd_kv,
+                                     float theta, float freq_scale, int style, float *out, void *ws,
+                                     size_t ws_bytes, int32_t *err, minf_stream_t stream) {
+    return layer_attn_step(xn, h, gain, eps, n_embd, q, k, v, pos, nt, k_reg, v_reg, kKvF16, cap, n_head,
+                           n_kv_head, hd, hd_kv, theta, freq_scale, style, out, ws, ws_bytes, err, stream, true);
+}
+
+int minf_layer_attn_step_chained_q8(float *xn, const float *h, const float *gain, float eps, int n_embd, float *q,
+                                    float *k, const float *v, const int32_t *pos, int nt, uint8_t *k_reg,
+                                    uint8_t *v_reg, int cap, int n_head, int n_kv_head, int hd, int hd_kv,
+                                    float theta, float freq_scale, int style, float *out, void *ws,
+                                    size_t ws_bytes, int32_t *err, minf_stream_t stream) {
+    if ((n_kv_head * hd_kv) % 32) return MINF_ERR_ARG;
+    return layer_attn_step(xn, h, gain, eps, n_embd, q, k, v, pos, nt, k_reg, v_reg, kKvQ8, cap, n_head,
+                           n_kv_head, hd, hd_kv, theta, freq_scale, style, out, ws, ws_bytes, err, stream, true);
+}
+
 static int layer_attn_step_batched(float *xn, const float *h, const float *gain, float eps,
                                    int n_embd, float *q, float *k, const float *v,
                                    const int32_t *pos, int n_seq, void *k_arena, void *v_arena, int kv,
@@ -460,7 +492,7 @@ static int layer_attn_step_batched(float *xn, const float *h, const float *gain,
         DecodeArgs d = decode_args(out, q, k_arena, v_arena, kv, seq_row_off, seq_cap, max_cap, pos,
                                    n_seq, n_head, n_kv_head, hd, hd_kv, scale, ws, ws_bytes, err,
                                    arena_rows);
-        DecodeStepExtra x = {k, v, xn, h, gain, eps, theta, freq_scale, n_embd, style, false};
+        DecodeStepExtra x = {k, v, xn, h, gain, eps, theta, freq_scale, n_embd, style, false, false};
         return launch_decode_step(d, x, s);
     }
     st = layer_prologue(xn, h, gain, eps, n_embd, q, k, v, pos, n_seq, n_head, n_kv_head, hd, hd_kv, theta,
@@ -636,7 +668,7 @@ static int layer_attn_step_paged(float *xn, const float *h, const float *gain, f
     set_paged(d, pg, pool_rows);
     if (fused_step_supported(n_head, n_kv_head, hd, hd_kv, n_embd) && aligned16(h) && aligned16(xn) &&
         (!gain || aligned16(gain))) {
-        DecodeStepExtra x = {k, v, xn, h, gain, eps, theta, freq_scale, n_embd, style, false};
+        DecodeStepExtra x = {k, v, xn, h, gain, eps, theta, freq_scale, n_embd, style, false, false};
         return launch_decode_step(d, x, s);
     }
     st = layer_prologue(xn, h, gain, eps, n_embd, q, k, v, pos, n_seq, n_head, n_kv_head, hd, hd_kv, theta,

@@ -72,6 +72,40 @@ __device__ __forceinline__ void flag_error(int32_t *err, int bit) {
     if (err) atomicOr(err, bit);
 }
 
+// The first 256 bytes of every attention workspace are a control block shared by the decode
+// and prefill layouts: the prefill step's grid-barrier counts, the decode kernel's unit
+// counters, and a tag naming the layout of the last call that used the workspace.  Every call
+// that finishes leaves its counters at zero.  A call takes the workspace only when the tag is
+// zero (freshly zero-filled) or one its merge tickets can follow (see each kernel); otherwise
+// it sets MINF_ERRBIT_WORKSPACE and computes nothing that depends on the workspace.  A call
+// whose bounded wait expired leaves the tag at kWsPoison, so the next call refuses it too.
+constexpr size_t kWsCtlBytes = 256;
+constexpr int kWsBarArrive = 0, kWsBarDepart = 1, kWsUnitCtr = 2, kWsUnitDone = 3, kWsTag = 4;
+constexpr int kWsPoison = -1;
+constexpr int kWsKindDecode = 1, kWsKindPrefill = 2;
+
+// A layout tag: 'MI' in the high half, a hash of the layout's offsets, the kind in the low bits.
+inline int ws_key(int kind, unsigned long long a, unsigned long long b, unsigned long long c,
+                  unsigned long long d) {
+    unsigned long long h = 1469598103934665603ull;
+    for (unsigned long long x : {a, b, c, d}) {
+        h ^= x;
+        h *= 1099511628211ull;
+    }
+    const unsigned v = static_cast<unsigned>(h ^ (h >> 29) ^ (h >> 47));
+    return static_cast<int>(0x4D490000u | (v & 0xFFFCu) | static_cast<unsigned>(kind));
+}
+__host__ __device__ __forceinline__ bool ws_key_valid(int t) {
+    const unsigned u = static_cast<unsigned>(t);
+    return (u & 0xFFFF0000u) == 0x4D490000u && ((u & 3u) == 1u || (u & 3u) == 2u);
+}
+
+__device__ __forceinline__ int ld_relaxed(const int *p) {
+    int v;
+    asm volatile("ld.relaxed.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
 inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 int sm_count();

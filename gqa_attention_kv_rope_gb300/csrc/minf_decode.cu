@@ -16,19 +16,23 @@ inline int stage_rows(int hd_kv, int kind) {
 }
 
 struct WsLayout {
-    size_t ml_off, acc_off, ticket_off, ctr_off, total;
+    size_t ml_off, acc_off, ticket_off, total;
+    int key;  // the layout tag a call of this layout leaves in the control block
 };
 
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
+// The control block (counters and layout tag, shared with the prefill layout), the partial
+// (m, l) pairs and accumulators, then one merge ticket per (sequence, kv group).
 WsLayout ws_layout(int n_seq, int nh, int pairs_per_seq, int hd_kv, int splits) {
     WsLayout w;
     const size_t parts = static_cast<size_t>(n_seq) * nh * splits;
-    w.ml_off = 0;
-    w.acc_off = align256(parts * 2 * sizeof(float));
+    const size_t tickets = static_cast<size_t>(n_seq) * pairs_per_seq;
+    w.ml_off = kWsCtlBytes;
+    w.acc_off = w.ml_off + align256(parts * 2 * sizeof(float));
     w.ticket_off = w.acc_off + align256(parts * hd_kv * sizeof(float));
-    w.ctr_off = w.ticket_off + align256(static_cast<size_t>(n_seq) * pairs_per_seq * sizeof(int));
-    w.total = w.ctr_off + 256;
+    w.total = w.ticket_off + align256(tickets * sizeof(int));
+    w.key = ws_key(kWsKindDecode, w.acc_off, w.ticket_off, tickets, w.total);
     return w;
 }
 
@@ -137,8 +141,11 @@ int launch_impl(const DecodeArgs &d, const DecodeStepExtra *x, cudaStream_t s) {
     k.ws_ml = reinterpret_cast<float *>(ws + pl.w.ml_off);
     k.ws_acc = reinterpret_cast<float *>(ws + pl.w.acc_off);
     k.ws_ticket = reinterpret_cast<int *>(ws + pl.w.ticket_off);
-    k.ws_ctr = reinterpret_cast<int *>(ws + pl.w.ctr_off);
-    k.ws_done = k.ws_ctr + 1;
+    k.ws_ctr = reinterpret_cast<int *>(ws) + kWsUnitCtr;
+    k.ws_done = reinterpret_cast<int *>(ws) + kWsUnitDone;
+    k.ws_tag = reinterpret_cast<int *>(ws) + kWsTag;
+    k.ws_key = pl.w.key;
+    k.early = 1;  // without programmatic dependent launch the waits are no-ops
     k.min_rows = pl.min_rows;
     k.sorted = pl.sorted;
     k.table = d.table;
@@ -162,6 +169,7 @@ int launch_impl(const DecodeArgs &d, const DecodeStepExtra *x, cudaStream_t s) {
         k.style = x->style;
         rope_table(&k.tab, d.hd_kv, x->theta, x->freq_scale);
         pdl = x->pdl;
+        k.early = x->early;
     }
     const int sms = sm_count();
     const int grid = static_cast<int>(units < sms ? units : sms);

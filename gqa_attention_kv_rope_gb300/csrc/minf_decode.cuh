@@ -46,6 +46,7 @@
 #include <cuda_fp16.h>
 #include <cudaTypedefs.h>
 
+#include <atomic>
 #include <cmath>
 
 #include "minf_common.cuh"
@@ -187,6 +188,9 @@ struct KParams {
     float *ws_ml, *ws_acc;
     int *ws_ticket;
     int *ws_ctr, *ws_done;  // dynamic unit counter and the count of finished producers
+    int *ws_tag;           // the workspace's layout tag (its control block)
+    int ws_key;            // this call's layout: the tags it accepts are 0 and this one
+    int early;             // positions and cached rows are read before the dependency wait
     // fused layer step only
     float *q_io, *k_io;    // rotated in place (q_io == q)
     void *k_reg, *v_reg;   // the new row is written here (the region's storage type)
@@ -450,7 +454,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __shared__ float4 sm_red[kCons];
     __shared__ float sm_redM[kCons], sm_redL[kCons];
     __shared__ __align__(16) float sm_knew[HDKV], sm_vnew[HDKV];
-    __shared__ int sm_last, sm_abort;
+    __shared__ int sm_last, sm_abort, sm_wsbad;
     __shared__ float sm_tab[kFused ? HDKV / 2 : 1];  // angular speeds, read by lane-varying index
     __shared__ float sm_sn[kFused ? HDKV / 2 : 1], sm_cs[kFused ? HDKV / 2 : 1];  // first unit's sin, cos
 
@@ -473,8 +477,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         sm_abort = 0;
         mbar_init_fence();
     }
-    // A batch is visited longest sequence first (positions are not written by a preceding
-    // kernel, so this runs before the dependency wait): rank = number of longer windows.
+    // Without early start nothing is read before the launch ahead of this one has finished:
+    // the positions and the cached rows may be its outputs.
+    if (!a.early) gdc_wait();
+    // A batch is visited longest sequence first (with early start the positions are not written
+    // by a preceding kernel, so this runs before the dependency wait): rank = number of longer
+    // windows.
     const int *order = nullptr;
     if (a.sorted) {
         for (int s = tid; s < a.n_seq; s += blockDim.x) {
@@ -568,6 +576,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             uint32_t it = 0;
             bool waited = false;
+            int ptag = 0;  // the workspace's tag, read once the launch before this one has finished
+            auto wait_dep = [&]() {
+                gdc_wait();
+                waited = true;
+                ptag = ld_relaxed(a.ws_tag);
+            };
             int u = blockIdx.x;  // the first unit is this CTA's own; the rest come from a counter
             while (u < n_units && !*abort_flag) {
                 const Unit t = unit_of<R>(a, u, order);
@@ -579,10 +593,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         // Cached rows need no wait, but only kPreWait stages go out before it:
                         // a deeper burst, issued while the previous launch merges its splits and
                         // completes, slows that launch's round trips more than it saves here.
-                        if (!waited && it >= kPreWait) {
-                            gdc_wait();
-                            waited = true;
-                        }
+                        if (!waited && it >= kPreWait) wait_dep();
                         if (it >= kNST) {
                             if (!mbar_wait(&empty[slot], ((it / kNST) & 1) ^ 1, abort_flag, a.err)) break;
                         }
@@ -625,13 +636,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                     }
                 }
-                if (!waited) {  // the unit counter lives in the workspace a preceding launch may use
-                    gdc_wait();
-                    waited = true;
-                }
-                u = gridDim.x + atomicAdd(a.ws_ctr, 1);
+                if (!waited) wait_dep();  // the unit counter lives in the workspace a preceding launch may use
+                // a workspace of another layout: no further units (the consumers flag it)
+                u = (ptag == 0 || ptag == a.ws_key) ? static_cast<int>(gridDim.x) + atomicAdd(a.ws_ctr, 1) : n_units;
             }
-            if (!waited) gdc_wait();
+            if (!waited) wait_dep();
             // end of the stream for this CTA's consumers
             const int slot = it % kNST;
             if (it < kNST || mbar_wait(&empty[slot], ((it / kNST) & 1) ^ 1, abort_flag, a.err)) {
@@ -645,6 +654,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 __threadfence();
                 *a.ws_ctr = 0;
                 *a.ws_done = 0;
+                // a fresh workspace takes this call's layout (never over a poisoned tag)
+                if (ptag == 0) atomicCAS(a.ws_tag, 0, a.ws_key);
             }
             if (*abort_flag) {
                 // let copies already issued land before the CTA's shared memory goes away
@@ -654,6 +665,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         while (!mbar_try(&full[k % kNST], (k / kNST) & 1) && gtimer() - t0 < kWaitBudgetNs) {
                         }
                     }
+                *a.ws_tag = kWsPoison;  // its counters may be left non-zero: refused until zero-filled
             }
         }
         return;  // the producer never releases dependents: only consumers know the rows are written
@@ -696,6 +708,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!util_append) gdc_launch_dependents();  // this CTA appends no row
         released = true;
     }
+    // The workspace's tag, checked before the first partial is written (the load is in flight
+    // meanwhile): a workspace another layout left may hold non-zero tickets where this call's are.
+    const int ctag = tid == 0 ? ld_relaxed(a.ws_tag) : 0;
+    bool ws_checked = false;
     while (true) {
         if (!have) {
             // the producer publishes the unit it drew with the unit's first stage
@@ -936,7 +952,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 sm_l[warp][hh] = l[hh];
             }
         }
+        if (tid == 0 && !ws_checked) {
+            sm_wsbad = !(ctag == 0 || ctag == a.ws_key);
+            if (sm_wsbad) flag_error(a.err, MINF_ERRBIT_WORKSPACE);
+        }
+        ws_checked = true;
         cons_sync(&cons_bar, cphase, abort_flag, a.err);
+        if (sm_wsbad) continue;  // nothing that depends on the workspace: no partial, merge or output
         float *out_s = a.out + (static_cast<size_t>(t.s) * a.nh + h0) * HDKV;
         const size_t part0 = (static_cast<size_t>(t.s) * a.nh + h0) * a.n_split;  // head h0, split 0
         for (int i = tid; i < GH * VL; i += kCons) {
@@ -1040,6 +1062,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
     }
+    if (*abort_flag && tid == 0) *a.ws_tag = kWsPoison;  // a wait expired: refused until zero-filled
     if (!released) gdc_launch_dependents();
 }
 
@@ -1048,12 +1071,14 @@ cudaError_t launch_t(const CUtensorMap &tk, const CUtensorMap &tv, const CUtenso
                      const CUtensorMap &tvs, const KParams &k, int grid, cudaStream_t s,
                      bool pdl) {
     const size_t smem = static_cast<size_t>(kNST) * Cfg<HDKV, T>::kSlotBytes + 1024;
-    static bool attr_set = false;
-    if (!attr_set) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    static std::atomic<bool> attr_set[64];  // per device, shared by host threads
+    if (!attr_set[dev].load(std::memory_order_acquire)) {
         cudaError_t e = cudaFuncSetAttribute(decode_kernel<HDKV, GH, kFused, T>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
         if (e != cudaSuccess) return e;
-        attr_set = true;
+        attr_set[dev].store(true, std::memory_order_release);
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);

@@ -114,6 +114,8 @@ struct DecodeStepExtra {
     float eps, theta, freq_scale;
     int n_embd, style;
     bool pdl;             // launch with programmatic stream serialization
+    bool early;           // with pdl: read the positions and stream cached rows before the
+                          // dependency wait (the launch before writes neither)
 };
 
 struct PrefillArgs {

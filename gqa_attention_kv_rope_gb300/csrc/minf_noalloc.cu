@@ -10,9 +10,12 @@
 //
 // The array is a file-scope __device__ variable, so every GPU that loads the library holds it
 // until the process exits.  Host code cannot use the variable's name as a device address (on
-// the host it only names a stand-in); the address is looked up once per device with
-// cudaGetSymbolAddress, with that device current, and then passed to the kernel like any
-// caller-provided workspace.
+// the host it only names a stand-in); the address is looked up with cudaGetSymbolAddress, with
+// the device current, and then passed to the kernel like any caller-provided workspace.  The
+// address belongs to the CUDA context that was current when it was looked up, so it is kept
+// per context (a caller that switches contexts on one device gets each context's own copy).
+#include <cudaTypedefs.h>
+
 #include <mutex>
 
 #include "minf_common.cuh"
@@ -22,24 +25,54 @@ namespace minf {
 namespace {
 
 constexpr size_t kStaticScratchBytes = 8u << 20;  // 8 MiB per device
-constexpr int kMaxDevices = 64;
+constexpr int kMaxContexts = 64;
 
 static __device__ __align__(256) unsigned char g_decode_scratch[kStaticScratchBytes];
 
 std::mutex g_scratch_mu;
-void *g_scratch_ptr[kMaxDevices] = {};
+struct ScratchEntry {
+    CUcontext ctx;
+    void *ptr;
+};
+ScratchEntry g_scratch[kMaxContexts] = {};
+int g_n_scratch = 0;
 
-// The device address of this device's copy of the scratch array (looked up on first use).
-int scratch_for_current_device(void **out) {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MINF_ERR_CUDA;
-    std::lock_guard<std::mutex> lock(g_scratch_mu);
-    if (!g_scratch_ptr[dev]) {
+// The driver's cuCtxGetCurrent, through the runtime's entry-point query (no link to libcuda).
+PFN_cuCtxGetCurrent_v4000 ctx_get_current() {
+    static PFN_cuCtxGetCurrent_v4000 fn = nullptr;  // guarded by g_scratch_mu
+    if (!fn) {
         void *p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_decode_scratch) != cudaSuccess || !p) return MINF_ERR_CUDA;
-        g_scratch_ptr[dev] = p;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 4000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(p);
     }
-    *out = g_scratch_ptr[dev];
+    return fn;
+}
+
+// The device address of the scratch array in the current context (looked up on first use).
+int scratch_for_current_context(void **out) {
+    std::lock_guard<std::mutex> lock(g_scratch_mu);
+    auto get = ctx_get_current();
+    if (!get) return MINF_ERR_CUDA;
+    CUcontext ctx = nullptr;
+    if (get(&ctx) != CUDA_SUCCESS) return MINF_ERR_CUDA;
+    void *p = nullptr;
+    if (!ctx) {
+        // no context is current yet: the runtime call below makes the device's primary context
+        // current (as any runtime call does), and the address is that context's
+        if (cudaGetSymbolAddress(&p, g_decode_scratch) != cudaSuccess || !p) return MINF_ERR_CUDA;
+        if (get(&ctx) != CUDA_SUCCESS || !ctx) return MINF_ERR_CUDA;
+    }
+    for (int i = 0; i < g_n_scratch; ++i)
+        if (g_scratch[i].ctx == ctx) {
+            *out = g_scratch[i].ptr;
+            return MINF_OK;
+        }
+    if (g_n_scratch == kMaxContexts) return MINF_ERR_CUDA;
+    if (!p && (cudaGetSymbolAddress(&p, g_decode_scratch) != cudaSuccess || !p)) return MINF_ERR_CUDA;
+    g_scratch[g_n_scratch++] = {ctx, p};
+    *out = p;
     return MINF_OK;
 }
 
@@ -65,7 +98,7 @@ extern "C" int minf_gqa_attn_decode_static_ws(float *out, const float *q, const 
     const size_t need = decode_workspace_bytes(n_seq, n_head, n_kv_head, hd_kv, max_cap);
     if (need == 0 || need > kStaticScratchBytes) return MINF_ERR_WORKSPACE;  // beyond the fixed 8 MiB
     void *ws = nullptr;
-    const int st = scratch_for_current_device(&ws);
+    const int st = scratch_for_current_context(&ws);
     if (st != MINF_OK) return st;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     // The merge tickets must start at zero; a previous call (or one that stopped early) may

@@ -49,6 +49,7 @@
 #include <cuda.h>
 #include <cuda_fp16.h>
 
+#include <atomic>
 #include <cmath>
 #include <cstddef>
 #include <type_traits>
@@ -251,6 +252,8 @@ struct PParams {
     float scale_log2;
     float *ws_o, *ws_ml;       // chunk partials: o as [.., d/4][row] of float4, (m, l) as [.., 2][row]
     int *ws_ticket;            // one per (query tile, head)
+    int *ws_tag;               // the workspace's layout tag (its control block), null without one
+    int ws_key;                // this call's layout
 };
 
 // Round to the nearest TF32 value (10 explicit mantissa bits), ties away from zero: half a TF32
@@ -315,17 +318,21 @@ struct StepParams {
     const float *hx, *gain; // [nt, n_embd], [n_embd] (gain nullable)
     int n_embd, norm_vec;   // norm_vec: float4 rows (n_embd % 4 == 0, 16-byte aligned rows and gain)
     float eps;
-    int *bar;               // grid barrier: arrivals, departures (zero between launches)
+    int *bar;               // grid barrier: arrivals, departures (zero between launches), then
+                            // the workspace's control block (its layout tag at bar[kWsTag])
 };
 
 
 // A CTA of the fused step counts its departure from the grid barrier once it has left the
 // wait; the last to depart zeroes both counts for the next launch.
-__device__ __forceinline__ void step_depart(const StepParams &x) {
-    const int old = atomicAdd(x.bar + 1, 1);
+__device__ __forceinline__ void step_depart(const StepParams &x, int key) {
+    const int old = atomicAdd(x.bar + kWsBarDepart, 1);
     if (old == static_cast<int>(gridDim.x) - 1) {
-        x.bar[0] = 0;
-        x.bar[1] = 0;
+        x.bar[kWsBarArrive] = 0;
+        x.bar[kWsBarDepart] = 0;
+        // the workspace now holds this layout (a tag a timed-out item has poisoned stays so)
+        const int tag = ld_relaxed(x.bar + kWsTag);
+        if (tag != kWsPoison) atomicCAS(x.bar + kWsTag, tag, key);
     }
 }
 
@@ -337,6 +344,8 @@ struct Item {
     int h, hk, qt, kc, t0, L_t, lmax, n_act, tile0, n_tiles;
     uint32_t tmem;
     const StepParams *dep;  // fused step: this CTA departs the grid barrier during this item
+    int ws_tag;             // thread 0: the workspace's tag as the call found it (checked before
+                            // a ticket is taken; the fused step checked it before its barrier)
 };
 
 // fp32 regions: K tiles arrive by TMA into kh and the staging warps convert them into kl.
@@ -423,7 +432,7 @@ __device__ __forceinline__ void attend(Smem<HDKV> &sm, const CUtensorMap &tm_q, 
         // O_t(i) = P(i) V(i) into O buffer i % 2 once P(i) is published and V^T(i) staged, from
         // a second thread: one thread issues a tensor-core instruction only every ~35-50 ns, and
         // S(i+1) and O_t(i) need not wait behind each other's issue
-        if (lane == 0 && it.dep) step_depart(*it.dep);  // (P(0) is microseconds away)
+        if (lane == 0 && it.dep) step_depart(*it.dep, a.ws_key);  // (P(0) is microseconds away)
         if (lane == 0 && n_tiles > 0) {
             uint64_t dp[NP][2][BN / 32], dv[NB][2][BN / 32];
 #pragma unroll
@@ -722,12 +731,19 @@ __device__ __forceinline__ void attend(Smem<HDKV> &sm, const CUtensorMap &tm_q, 
             pml[BM + tid] = l;
             named_sync(1, kSoftThreads);
             if (tid == 0) {
-                int old;
-                asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], 1;"
-                             : "=r"(old)
-                             : "l"(a.ws_ticket + static_cast<size_t>(qt) * a.nh + h)
-                             : "memory");
-                sm.lmax = (old == n_act - 1) ? -1 : 0;  // reuse as the "last" flag
+                if (it.ws_tag == 0 || it.ws_tag == a.ws_key) {
+                    if (it.ws_tag == 0) atomicCAS(a.ws_tag, 0, a.ws_key);  // a fresh workspace takes this layout
+                    int old;
+                    asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], 1;"
+                                 : "=r"(old)
+                                 : "l"(a.ws_ticket + static_cast<size_t>(qt) * a.nh + h)
+                                 : "memory");
+                    sm.lmax = (old == n_act - 1) ? -1 : 0;  // reuse as the "last" flag
+                } else {
+                    // another layout's workspace: its tickets are not this call's to trust
+                    flag_error(a.err, MINF_ERRBIT_WORKSPACE);
+                    sm.lmax = 0;
+                }
             }
             named_sync(1, kSoftThreads);
             write_out = sm.lmax == -1;
@@ -876,6 +892,11 @@ __global__ void __launch_bounds__(kThreadsP, 1)
         sm.lmax = 0;
         mbar_init_fence();
     }
+    // Nothing is read before the launch ahead of this one has finished: pos, q, the regions, the
+    // workspace and the output may all be its outputs (a no-op without programmatic launch).
+    gdc_wait();
+    // The workspace's tag, checked before a ticket is taken (the load is in flight meanwhile).
+    const int ws_tag0 = (tid == 0 && a.ws_tag) ? ld_relaxed(a.ws_tag) : 0;
     // this row's window ("11 . Attention...", §3.2.4: vl = min(pos[t] + 1, nkv), nkv <= n_ctx)
     int L_t = 0;
     const int t = t0 + tid;
@@ -909,13 +930,10 @@ __global__ void __launch_bounds__(kThreadsP, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = sm.tmem_base;
-    // everything above reads only positions; q, the regions, the workspace and the output may
-    // still be written by the preceding launch (a no-op without programmatic dependent launch)
-    gdc_wait();
     // The launch that follows may start now: this kernel writes no K/V rows (a following decode
     // kernel streams cached rows before its own wait), and every launch before it has completed.
     gdc_launch_dependents();
-    const Item it = {h, hk, qt, kc, t0, L_t, lmax, n_act, tile0, n_tiles, tmem, nullptr};
+    const Item it = {h, hk, qt, kc, t0, L_t, lmax, n_act, tile0, n_tiles, tmem, nullptr, ws_tag0};
     attend<HDKV, T>(sm, tm_q, tm_k, a, it);
     tc_fence_before();
     __syncthreads();
@@ -926,6 +944,7 @@ __global__ void __launch_bounds__(kThreadsP, 1)
             const unsigned long long t0n = gtimer();
             while (gtimer() - t0n < kWaitBudgetNs / 4) {
             }
+            if (a.ws_tag) *a.ws_tag = kWsPoison;  // a wait expired: refused until zero-filled
         }
         __syncwarp();
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(tmem_cols<HDKV>())
@@ -1137,6 +1156,14 @@ __global__ void __launch_bounds__(kThreadsP, 1)
     tc_fence_after();
     const uint32_t tmem = sm.tmem_base;
     gdc_wait();  // every input (pos included) and the workspace, only after the launch before this one
+    // The workspace's control block as the call found it (checked before the grid barrier, the
+    // loads in flight meanwhile): the tag of any layout will do -- this step zeroes its own
+    // tickets -- but not a poisoned or garbage one, and no CTA can have departed yet.
+    int ctl_tag = 0, ctl_dep = 0;
+    if (tid == 0) {
+        ctl_tag = ld_relaxed(x.bar + kWsTag);
+        ctl_dep = ld_relaxed(x.bar + kWsBarDepart);
+    }
     // This call's merge tickets start at zero whatever an earlier call of another shape left in
     // their words (its partial outputs, say): no item takes a ticket before the grid barrier.
     if (a.ws_ticket)
@@ -1160,11 +1187,17 @@ __global__ void __launch_bounds__(kThreadsP, 1)
     // Grid barrier: every CTA's row work before any item reads it.  Arrivals are counted; a CTA
     // leaves once all have arrived and later counts its departure; the last to depart zeroes both
     // counts for the next launch (every CTA has left the wait by then).  The tiles' windows and
-    // the item enumeration are computed between the arrival and the wait.
+    // the item enumeration are computed between the arrival and the wait.  Every CTA reads the
+    // same control block before any arrival, so on a refused workspace none arrives or waits.
+    if (tid == 0) {
+        sm.lmax = (ctl_tag == 0 || ws_key_valid(ctl_tag)) && ctl_dep == 0 ? 0 : 1;  // 1: refused
+        if (sm.lmax && blockIdx.x == 0) flag_error(a.err, MINF_ERRBIT_WORKSPACE);
+    }
     __syncthreads();
+    const bool ws_refused = sm.lmax != 0;
     // release: the CTA's writes (ordered before by the barrier above) before the arrival; it
     // waits for those writes to complete, so a thread outside the window loop below makes it
-    if (tid == kProducerWarp * 32)
+    if (tid == kProducerWarp * 32 && !ws_refused)
         asm volatile("red.release.gpu.global.add.s32 [%0], 1;" ::"l"(x.bar) : "memory");
     if (tid < BM) {
         for (int qt = 0; qt < a.n_qt; ++qt) {
@@ -1197,13 +1230,14 @@ __global__ void __launch_bounds__(kThreadsP, 1)
         ss.pref[a.n_qt] = acc;
         // acquire: every other CTA's writes before this CTA's reads after the wait
         const unsigned long long t0n = gtimer();
-        while (true) {
+        while (!ws_refused) {
             int n;
             asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(n) : "l"(x.bar) : "memory");
             if (n >= static_cast<int>(gridDim.x)) break;
             if (gtimer() - t0n > kWaitBudgetNs) {
                 sm.abort_flag = 1;
                 flag_error(a.err, MINF_ERRBIT_TIMEOUT);
+                x.bar[kWsTag] = kWsPoison;  // its counts are left non-zero: refused until zero-filled
                 break;
             }
         }
@@ -1216,9 +1250,9 @@ __global__ void __launch_bounds__(kThreadsP, 1)
     gdc_launch_dependents();
 
     const int g = a.nh / a.nk;
-    const int n_items = *abort_flag ? 0 : ss.pref[a.n_qt] * a.nh;
+    const int n_items = (*abort_flag || ws_refused) ? 0 : ss.pref[a.n_qt] * a.nh;
     // the departure: by the first item's P*V thread while it waits for P(0), else here
-    if (static_cast<int>(blockIdx.x) >= n_items && tid == 0) step_depart(x);
+    if (static_cast<int>(blockIdx.x) >= n_items && tid == 0 && !ws_refused) step_depart(x, a.ws_key);
     for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
         const int h = item % a.nh, pr = item / a.nh;
         int qt = 0;
@@ -1238,7 +1272,7 @@ __global__ void __launch_bounds__(kThreadsP, 1)
         __syncthreads();
         tc_fence_after();
         const Item it = {h, h / g, qt, kc, t0, -1, lmax, n_act, tile0, n_tiles, tmem,
-                         item == static_cast<int>(blockIdx.x) ? &x : nullptr};
+                         item == static_cast<int>(blockIdx.x) ? &x : nullptr, a.ws_key};
         attend<HDKV, T>(sm, tm_q, tm_k, a, it);
         tc_fence_before();
         __syncthreads();
@@ -1252,6 +1286,7 @@ __global__ void __launch_bounds__(kThreadsP, 1)
             const unsigned long long t0n = gtimer();
             while (gtimer() - t0n < kWaitBudgetNs / 4) {
             }
+            x.bar[kWsTag] = kWsPoison;  // a wait expired: refused until zero-filled
         }
         __syncwarp();
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(tmem_cols<HDKV>())
@@ -1279,8 +1314,8 @@ PrefillPlan prefill_plan(int nt, int nh, int hd_kv, int cap) {
     p.kc_tiles = static_cast<int>(kc_keys / BN);
     p.n_kc = static_cast<int>((cap + kc_keys - 1) / kc_keys);
     const size_t parts = static_cast<size_t>(p.n_qt) * nh * p.n_kc;
-    p.step_off = 0;
-    p.o_off = align256p(2 * sizeof(int));
+    p.step_off = 0;          // the control block: the step's barrier counts and the layout tag
+    p.o_off = kWsCtlBytes;
     p.ml_off = p.o_off + (p.n_kc > 1 ? align256p(parts * hd_kv * BM * sizeof(float)) : 0);
     p.ticket_off = p.ml_off + (p.n_kc > 1 ? align256p(parts * 2 * BM * sizeof(float)) : 0);
     p.total = p.ticket_off + (p.n_kc > 1 ? align256p(static_cast<size_t>(p.n_qt) * nh * sizeof(int)) : 0);
@@ -1321,6 +1356,8 @@ int prefill_setup(const PrefillArgs &pa, CUtensorMap *tq, CUtensorMap *tk, PPara
     a.ws_o = pl.n_kc > 1 ? reinterpret_cast<float *>(ws + pl.o_off) : nullptr;
     a.ws_ml = pl.n_kc > 1 ? reinterpret_cast<float *>(ws + pl.ml_off) : nullptr;
     a.ws_ticket = pl.n_kc > 1 ? reinterpret_cast<int *>(ws + pl.ticket_off) : nullptr;
+    a.ws_tag = pl.n_kc > 1 ? reinterpret_cast<int *>(ws) + kWsTag : nullptr;
+    a.ws_key = ws_key(kWsKindPrefill, pl.o_off, pl.ml_off, pl.ticket_off, pl.total);
     *out = a;
     *plan = pl;
     return MINF_OK;
@@ -1336,12 +1373,12 @@ int launch_t(const PrefillArgs &pa, cudaStream_t s) {
     const size_t smem = sizeof(Smem<HDKV>) + 1024;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return MINF_ERR_CUDA;
-    static bool attr_set[64] = {};
-    if (!attr_set[dev]) {
+    static std::atomic<bool> attr_set[64];
+    if (!attr_set[dev].load(std::memory_order_acquire)) {
         if (cudaFuncSetAttribute(prefill_kernel<HDKV, T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  static_cast<int>(smem)) != cudaSuccess)
             return MINF_ERR_CUDA;
-        attr_set[dev] = true;
+        attr_set[dev].store(true, std::memory_order_release);
     }
     const long long ctas = static_cast<long long>(pl.n_qt) * pa.nh * pl.n_kc;
     if (ctas > 0x7fffffffLL) return MINF_ERR_UNSUPPORTED;
@@ -1396,9 +1433,12 @@ int launch_step_t(const PrefillArgs &pa, const PrefillStepExtra &xs, cudaStream_
     const size_t smem = sizeof(Smem<HDKV>) + sizeof(StepSmem) + 1024;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return MINF_ERR_CUDA;
-    static int resident[64] = {};  // CTAs that can be resident at once (0: not yet known)
-    static bool no_pdl[64] = {};   // the runtime refused the cooperative launch with early start
-    if (!resident[dev]) {
+    // per device, shared by host threads: CTAs that can be resident at once (0: not yet known),
+    // and whether the runtime refused the cooperative launch with early start
+    static std::atomic<int> resident[64];
+    static std::atomic<bool> no_pdl[64];
+    int res = resident[dev].load(std::memory_order_acquire);
+    if (!res) {
         if (cudaFuncSetAttribute(prefill_step_kernel<HDKV, T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  static_cast<int>(smem)) != cudaSuccess)
             return MINF_ERR_CUDA;
@@ -1407,10 +1447,11 @@ int launch_step_t(const PrefillArgs &pa, const PrefillStepExtra &xs, cudaStream_
                 cudaSuccess ||
             per_sm < 1)
             return MINF_ERR_UNSUPPORTED;
-        resident[dev] = per_sm * sm_count();
+        res = per_sm * sm_count();
+        resident[dev].store(res, std::memory_order_release);
     }
     const long long items = static_cast<long long>(pl.n_qt) * pa.nh * pl.n_kc;
-    const int grid = static_cast<int>(items < resident[dev] ? items : resident[dev]);
+    const int grid = static_cast<int>(items < res ? items : res);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(grid));
     cfg.blockDim = dim3(kThreadsP);
@@ -1422,13 +1463,16 @@ int launch_step_t(const PrefillArgs &pa, const PrefillStepExtra &xs, cudaStream_
     attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = no_pdl[dev] ? 1 : 2;
+    const bool pdl = !no_pdl[dev].load(std::memory_order_relaxed);
+    cfg.numAttrs = pdl ? 2 : 1;
     cudaError_t e = cudaLaunchKernelEx(&cfg, prefill_step_kernel<HDKV, T>, tq, tk, a, x, rq, rk);
-    if (e != cudaSuccess && !no_pdl[dev]) {
+    if (e != cudaSuccess && pdl) {
+        // Retried without early start; only when that launch succeeds was the refusal the
+        // attribute's, and later calls on this device skip it.  Any other failure is returned.
         (void)cudaGetLastError();
-        no_pdl[dev] = true;
         cfg.numAttrs = 1;
         e = cudaLaunchKernelEx(&cfg, prefill_step_kernel<HDKV, T>, tq, tk, a, x, rq, rk);
+        if (e == cudaSuccess) no_pdl[dev].store(true, std::memory_order_relaxed);
     }
     return e == cudaSuccess ? MINF_OK : MINF_ERR_CUDA;
 }

@@ -16,6 +16,7 @@
 // weight and bias reads go out before griddepcontrol.wait, so they overlap the end of the
 // preceding kernel; everything else (h, gain, pos, all writes) comes after the wait.
 #include <cmath>
+#include <mutex>
 
 #include "minf_common.cuh"
 #include "minf_kernels.h"
@@ -262,13 +263,18 @@ int launch_fused_qkv(const QkvArgs &a, float theta, float freq_scale, cudaStream
         inst == 0 ? fused_qkv_kernel<1> : inst == 1 ? fused_qkv_kernel<4> : fused_qkv_kernel<kQkvMaxTok>;
     const size_t smem = static_cast<size_t>(a.nt) * a.n_embd * sizeof(float);
     if (smem > kQkvMaxSmem) return MINF_ERR_UNSUPPORTED;  // the tokens' rows must fit shared memory
+    // per device and instantiation, raised (never lowered) to the largest size a call has taken,
+    // under a lock so that host threads with different token counts cannot undo one another
+    static std::mutex attr_mu;
     static size_t attr_smem[64][3] = {};
-    size_t &have = attr_smem[dev][inst];
-    if (smem > 48 * 1024 && have < smem) {
-        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
-            cudaSuccess)
-            return MINF_ERR_UNSUPPORTED;
-        have = smem;
+    if (smem > 48 * 1024) {
+        std::lock_guard<std::mutex> lock(attr_mu);
+        if (attr_smem[dev][inst] < smem) {
+            if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
+                cudaSuccess)
+                return MINF_ERR_UNSUPPORTED;
+            attr_smem[dev][inst] = smem;
+        }
     }
     const int pairs = (a.nh * a.hd + 2 * a.nk * a.hd_kv) / 2;
     const int blocks = (pairs + kWarps - 1) / kWarps;

@@ -69,6 +69,16 @@ enum {
                                       missing from the table (id < 0 or past the pool); its rows
                                       read as zeros, the store is skipped, the outputs of that
                                       sequence are invalid */
+#define MINF_ERRBIT_WORKSPACE 0x20 /* the workspace was last used by a call of another layout
+                                      (a decode call of another shape, a prefill after a decode
+                                      or the reverse: its merge tickets may not be zero), was
+                                      never zero-filled, or held the workspace of a call whose
+                                      bounded wait expired.  Nothing that depends on the
+                                      workspace was computed (the attention output is not
+                                      written); zero-fill it and call again.  The test reads a
+                                      tag in the workspace's first 256 bytes (its control block:
+                                      the counters every call leaves at zero, and the layout of
+                                      the last call that used it). */
 
 /* Human-readable name of a status code (static storage). */
 MINF_API const char *minf_status_string(int status);
@@ -135,9 +145,14 @@ MINF_API int minf_rope_kv_append(float *q, float *k, const float *v, const int32
 /*
  * Bytes of device workspace minf_gqa_attn_decode needs for n_seq sequences
  * whose regions hold at most max_cap rows.  Returns 0 for invalid arguments.
- * The workspace must be zero-filled before its first use; every call leaves
- * it zero-filled again on return, so it can be reused (and captured in a CUDA
- * graph) without clearing.  Two calls that run concurrently must not share it.
+ * The workspace must be zero-filled before its first use.  Every call leaves its
+ * counters and merge tickets at zero, so calls of the same shape (n_seq, heads,
+ * hd_kv, max_cap) can reuse it, and be captured in a CUDA graph, without clearing.
+ * Its first 256 bytes are a control block that also records the layout of the last
+ * call that used it: a call of another layout (another shape, or a prefill) leaves
+ * partials where this one's tickets are, so the call refuses such a workspace with
+ * MINF_ERRBIT_WORKSPACE until it is zero-filled again.  Two calls that run
+ * concurrently must not share it.
  */
 MINF_API size_t minf_attn_decode_workspace_bytes(int n_seq, int n_head, int n_kv_head, int hd_kv,
                                         int max_cap);
@@ -179,8 +194,9 @@ MINF_API int minf_gqa_attn_decode(float *out, const float *q, const float *k_reg
  * owns (every GPU that loads the library holds it until the process exits).
  *   - A call that would need more than 8 MiB of workspace (see
  *     minf_attn_decode_workspace_bytes) returns MINF_ERR_WORKSPACE and launches nothing.
- *   - The first call on a device looks up that device's copy of the array (with the device
- *     current); make that first call before any stream capture on the device.
+ *   - The first call in a CUDA context looks up that context's copy of the array (with the
+ *     context current; one entry per context, so a caller that switches contexts on a device
+ *     is served too); make that first call before any stream capture in the context.
  *   - Each call clears the part of the array it uses (an asynchronous memset on `stream`)
  *     before its kernel.
  *   - Every call shares the one array: calls whose work overlaps on the GPU (different
@@ -206,11 +222,13 @@ MINF_API int minf_gqa_attn_decode_static_ws(float *out, const float *q, const fl
  * an fp32 evaluation to a few 1e-6; max, exp and sums run in fp32.
  * The keys of a query tile are cut into chunks processed by separate CTAs whose
  * partials are folded at the end: ws must hold minf_attn_prefill_workspace_bytes
- * (zero-filled before its first use; every call leaves its counters at zero, the
- * partial outputs not, so a workspace used for another shape, or for decode, must
- * be zero-filled again first; concurrent calls must not share it); it may be NULL
- * when no query tile has more than one key chunk.
- * Device errors: MINF_ERRBIT_ATTN_POS, MINF_ERRBIT_TIMEOUT.
+ * (zero-filled before its first use; every call leaves its counters and tickets at
+ * zero, the partial outputs not, so a workspace last used by a call of another
+ * shape, or by decode, is refused with MINF_ERRBIT_WORKSPACE until it is zero-filled
+ * again; concurrent calls must not share it); it may be NULL when no query tile has
+ * more than one key chunk.  The call reads pos only after the launch before it on
+ * the stream has finished.
+ * Device errors: MINF_ERRBIT_ATTN_POS, MINF_ERRBIT_TIMEOUT, MINF_ERRBIT_WORKSPACE.
  * Errors: as minf_gqa_attn_decode.
  */
 MINF_API int minf_gqa_attn_prefill(float *out, const float *q, const float *k_reg, const float *v_reg,
@@ -236,19 +254,20 @@ MINF_API size_t minf_attn_prefill_workspace_bytes(int nt, int n_head, int n_kv_h
  * ws/ws_bytes: for nt == 1 at least
  * minf_attn_decode_workspace_bytes(1, n_head, n_kv_head, hd_kv, cap), for nt > 1
  * at least minf_attn_prefill_workspace_bytes(nt, n_head, n_kv_head, hd_kv, cap);
- * zero-filled before its first use.  The single-launch prefill keeps its first
- * 256 bytes (the grid barrier's counts) at zero between calls and resets its own
- * merge counters, so consecutive nt > 1 steps of any shape may share one
- * workspace; a workspace that decode has used must be zero-filled again first.
- * Early start: the nt == 1 path is a programmatic dependent launch that reads pos and
- * begins streaming the cached rows [0, pos) of the regions before the launch just before
- * it on the stream has finished (h, gain, q, k, v, ws and every output only after): pos
- * and those rows must not be written by that launch (a host-to-device copy is not a
- * launch).  For nt > 1 the first launch is a programmatic dependent launch too; it touches
- * memory only once the launch before it has finished (on the two-launch path the attention
- * launch after it reads pos as soon as every block of the first has started): pos must not be
- * written by the launch just before the step on either path.  A launch after an nt > 1 step
- * may start early once the step's rows are stored (its grid barrier).
+ * zero-filled before its first use.  Every call leaves the workspace's first
+ * 256 bytes (its control block: counters and the tag of the last layout that used
+ * it) ready for the next: consecutive nt > 1 steps of any shape may share one
+ * workspace, a single-launch prefill step may follow a decode step on it, and a
+ * decode step may follow decode steps of the same shape.  Any other reuse (a decode
+ * step after a prefill, or after a decode of another shape) is refused on the
+ * device with MINF_ERRBIT_WORKSPACE until the workspace is zero-filled again.
+ * Ordering: safe after any launch.  Every launch of the step is a programmatic
+ * dependent launch -- its blocks may be scheduled while the launch just before it on the
+ * stream finishes -- but it reads nothing (pos included) before that launch has
+ * finished, so a kernel that writes pos or the cached rows right before the call (an
+ * eager pos.fill_, a copy kernel) is safe.  For early start use the _chained form below.
+ * A launch after an nt > 1 step may start early once the step's rows are stored (its
+ * grid barrier).
  * Device errors: any of the bits above.
  */
 MINF_API int minf_layer_attn_step(float *xn, const float *h, const float *gain, float eps, int n_embd,
@@ -256,6 +275,35 @@ MINF_API int minf_layer_attn_step(float *xn, const float *h, const float *gain, 
                          float *k_reg, float *v_reg, int cap, int n_head, int n_kv_head, int hd,
                          int hd_kv, float theta, float freq_scale, int style, float *out,
                          void *ws, size_t ws_bytes, int32_t *err, minf_stream_t stream);
+
+/*
+ * minf_layer_attn_step with early start: the same arguments, results and errors, but the
+ * nt == 1 (decode) launch reads pos and begins streaming the cached rows [0, pos) of the
+ * regions before the launch just before it on the stream has finished (h, gain, q, k, v,
+ * ws and every output only after it).  Use it when that launch writes neither pos nor
+ * those rows -- the previous layer's step, a projection kernel -- so the row stream
+ * overlaps its end; a host-to-device copy of pos is not a launch and is always safe.  If a
+ * kernel writes pos or the rows just before, the call may read the old values: use
+ * minf_layer_attn_step.  nt > 1 runs exactly as minf_layer_attn_step.  The _f16 and _q8
+ * forms take the regions of minf_layer_attn_step_f16 and minf_layer_attn_step_q8.
+ */
+MINF_API int minf_layer_attn_step_chained(float *xn, const float *h, const float *gain, float eps, int n_embd,
+                                          float *q, float *k, const float *v, const int32_t *pos, int nt,
+                                          float *k_reg, float *v_reg, int cap, int n_head, int n_kv_head, int hd,
+                                          int hd_kv, float theta, float freq_scale, int style, float *out,
+                                          void *ws, size_t ws_bytes, int32_t *err, minf_stream_t stream);
+MINF_API int minf_layer_attn_step_chained_f16(float *xn, const float *h, const float *gain, float eps, int n_embd,
+                                              float *q, float *k, const float *v, const int32_t *pos, int nt,
+                                              uint16_t *k_reg, uint16_t *v_reg, int cap, int n_head, int n_kv_head,
+                                              int hd, int hd_kv, float theta, float freq_scale, int style,
+                                              float *out, void *ws, size_t ws_bytes, int32_t *err,
+                                              minf_stream_t stream);
+MINF_API int minf_layer_attn_step_chained_q8(float *xn, const float *h, const float *gain, float eps, int n_embd,
+                                             float *q, float *k, const float *v, const int32_t *pos, int nt,
+                                             uint8_t *k_reg, uint8_t *v_reg, int cap, int n_head, int n_kv_head,
+                                             int hd, int hd_kv, float theta, float freq_scale, int style,
+                                             float *out, void *ws, size_t ws_bytes, int32_t *err,
+                                             minf_stream_t stream);
 
 /*
  * One layer's attention stage for a batch of n_seq independent sequences, one

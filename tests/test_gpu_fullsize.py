@@ -10,8 +10,15 @@ Batched decode (64 sequences, lengths U{1..8192} from seed 0, 28 layers, one are
 layer, ~60 GB): the bench's 28 batched layer steps run once; layers 0 and 27 are checked for
 all 64 sequences, one sequence at a time on the host.
 
+Decode loop (Qwen3-0.6B shape, 28 layers): the bench's 511-token prefill into 1023-row regions,
+then its captured decode step replayed at pos 511..574; layers 0 and 27 checked at the prefill
+and at every step.
+
+Causal prefill (Qwen2.5-0.5B shape, 24 layers, 512 tokens): the bench's captured graph replayed
+once; layers 0 and 23 checked whole.
+
 Tolerance: |d| <= 1e-5 + 1e-4 |ref| per element (fp32 arithmetic against the oracle's
-double-accumulated reference)."""
+double-accumulated reference); tensor-core prefill outputs also within max-abs 2e-3."""
 import numpy as np
 import pytest
 import torch
@@ -152,4 +159,120 @@ def test_batched_full_size(m, orc):
                 close(out[s:s + 1], ref, what=f"out layer={layer} seq={s} len={ln}")
     finally:
         del arena, L
+        torch.cuda.empty_cache()
+
+
+def test_decode_loop_full_size(m, orc):
+    """Decode loop (Qwen3-0.6B shape, 28 layers): the bench's 511-token prefill into 1023-row
+    regions, then its captured decode step replayed at pos 511..574 with the step's seeded
+    inputs.  Layers 0 and 27 are checked at the prefill and at every step of the loop."""
+    import bench
+    from gqa_attention_kv_rope_gb300 import workloads as wl
+
+    dev = torch.device("cuda")
+    D = bench.setup_decode_loop(m, torch, wl, dev)
+    g, n0, steps = D["g"], D["n0"], D["steps"]
+    scale = float(np.float32(1.0) / np.sqrt(np.float32(g.hd)))
+    inp = {layer: {k: v.cpu().numpy() for k, v in D["inputs"][layer].items()} for layer in CHECK_LAYERS}
+    stream = torch.cuda.Stream()
+    try:
+        with torch.cuda.stream(stream):
+            D["prefill"]()
+        torch.cuda.synchronize()
+        assert int(D["err"].item()) == 0
+        pos_p = np.arange(n0, dtype=np.int32)
+        for layer in CHECK_LAYERS:
+            x, b = inp[layer], D["prefill_bufs"][layer]
+            K, V = (t[:n0].cpu().numpy() for t in D["regions"].view(layer))
+            q = b["q"].cpu().numpy()
+            k = b["k"].cpu().numpy()
+            close(b["xn"].cpu().numpy(), orc.rms_norm(x["h"][:n0], x["gain"], g.eps), what=f"prefill xn {layer}")
+            close(q, orc.rope(x["q"][:n0].copy().reshape(n0, g.n_head, g.hd), pos_p, g.n_head, g.hd,
+                              g.theta).reshape(n0, -1), what=f"prefill q {layer}")
+            close(k, orc.rope(x["k"][:n0].copy().reshape(n0, g.n_kv_head, g.hd_kv), pos_p, g.n_kv_head, g.hd_kv,
+                              g.theta).reshape(n0, -1), what=f"prefill k {layer}")
+            assert np.array_equal(K, k) and np.array_equal(V, x["v"][:n0]), layer
+            ref = orc.gqa_attn(q.reshape(n0, g.n_head, g.hd), K, V, pos_p, g.n_head, g.n_kv_head, g.hd, g.hd_kv,
+                               scale=scale, n_threads=8)
+            got = b["out"].cpu().numpy()
+            assert np.abs(got - ref).max() <= 2e-3, f"prefill out {layer}: tensor-core bound"
+            close(got, ref, what=f"prefill out {layer}")
+        D["load"](n0)
+        torch.cuda.synchronize()
+        graph = bench.capture(torch, stream, D["step"])  # its warm-up ran the step at pos 511 once
+        pos_host = torch.empty(1, dtype=torch.int32).pin_memory()
+        for i in range(steps):
+            t = n0 + i
+            pos_host.fill_(t)
+            with torch.cuda.stream(stream):
+                D["load"](t)
+                D["pos"].copy_(pos_host, non_blocking=True)
+                graph.replay()
+            torch.cuda.synchronize()
+            assert int(D["err"].item()) == 0, t
+            for layer in CHECK_LAYERS:
+                x, b = inp[layer], D["bufs"][layer]
+                K, V = (r[: t + 1].cpu().numpy() for r in D["regions"].view(layer))
+                q, k = b["q"].cpu().numpy(), b["k"].cpu().numpy()
+                close(b["xn"].cpu().numpy(), orc.rms_norm(x["h"][t:t + 1], x["gain"], g.eps), what=f"xn {t} {layer}")
+                close(q, orc.rope(x["q"][t:t + 1].copy().reshape(1, g.n_head, g.hd), [t], g.n_head, g.hd,
+                                  g.theta).reshape(1, -1), what=f"q {t} {layer}")
+                close(k, orc.rope(x["k"][t:t + 1].copy().reshape(1, g.n_kv_head, g.hd_kv), [t], g.n_kv_head,
+                                  g.hd_kv, g.theta).reshape(1, -1), what=f"k {t} {layer}")
+                assert np.array_equal(K[t], k[0]) and np.array_equal(V[t], x["v"][t]), (t, layer)
+                ref = orc.gqa_attn(q.reshape(1, g.n_head, g.hd), K, V, [t], g.n_head, g.n_kv_head, g.hd, g.hd_kv,
+                                   scale=scale, n_threads=8)
+                close(b["out"].cpu().numpy(), ref, what=f"out {t} {layer}")
+        del graph
+    finally:
+        D.clear()
+        torch.cuda.empty_cache()
+
+
+def test_prefill_full_size(m, orc):
+    """Causal prefill (Qwen2.5-0.5B shape, 24 layers, 512 tokens at 0..511): the bench's
+    captured graph replayed once on its seeded inputs; layers 0 and 23 checked whole -- xn, q
+    and k rotated, the stored K/V rows, and the tensor-core attention output (max-abs 2e-3 and
+    the fp32 bound element by element)."""
+    import bench
+    from gqa_attention_kv_rope_gb300 import workloads as wl
+
+    dev = torch.device("cuda")
+    P = bench.setup_prefill(m, torch, wl, dev)
+    g, nt = P["g"], P["nt"]
+    layers = (0, g.n_layer - 1)
+    scale = float(np.float32(1.0) / np.sqrt(np.float32(g.hd)))
+    stream = torch.cuda.Stream()
+    try:
+        graph = bench.capture(torch, stream, P["step"])  # the warm-up rotated q and k in place
+        P["reset"]()
+        P["regions"].k.zero_()
+        P["regions"].v.zero_()
+        torch.cuda.synchronize()
+        with torch.cuda.stream(stream):
+            graph.replay()
+        torch.cuda.synchronize()
+        assert int(P["err"].item()) == 0
+        pos = np.arange(nt, dtype=np.int32)
+        for layer in layers:
+            x = wl.layer_inputs(g, "prefill", layer, nt)
+            d = P["layers"][layer]
+            K, V = (t[:nt].cpu().numpy() for t in P["regions"].view(layer))
+            q, k = d["q"].cpu().numpy(), d["k"].cpu().numpy()
+            close(d["xn"].cpu().numpy(), orc.rms_norm(x["h"].numpy(), x["gain"].numpy(), g.eps), what=f"xn {layer}")
+            close(q, orc.rope(x["q"].numpy().copy().reshape(nt, g.n_head, g.hd), pos, g.n_head, g.hd,
+                              g.theta).reshape(nt, -1), what=f"q {layer}")
+            close(k, orc.rope(x["k"].numpy().copy().reshape(nt, g.n_kv_head, g.hd_kv), pos, g.n_kv_head, g.hd_kv,
+                              g.theta).reshape(nt, -1), what=f"k {layer}")
+            assert np.array_equal(K, k) and np.array_equal(V, x["v"].numpy()), layer
+            rest = P["regions"].k[layer][nt:]
+            assert not rest.any().item(), "rows past the prompt untouched"
+            ref = orc.gqa_attn(q.reshape(nt, g.n_head, g.hd), K, V, pos, g.n_head, g.n_kv_head, g.hd, g.hd_kv,
+                               scale=scale, n_threads=8)
+            got = d["out"].cpu().numpy()
+            assert np.abs(got - ref).max() <= 2e-3, f"out {layer}: tensor-core bound"
+            close(got, ref, what=f"out {layer}")
+        del graph
+    finally:
+        P.clear()
         torch.cuda.empty_cache()

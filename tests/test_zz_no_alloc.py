@@ -1,7 +1,9 @@
 """The allocation-free decode entry point (for callers that cannot allocate device memory):
 called through the C ABI, its output must match minf_gqa_attn_decode's, which uses a
-caller-allocated workspace, on two calls in a row that share the library's fixed scratch.
-This file is collected last so that a failure here does not hide the other GPU tests."""
+caller-allocated workspace, on two calls in a row that share the library's fixed scratch, and
+both must match the CPU oracle (|d| <= 1e-5 + 1e-4 |ref| element by element), so that a
+mistake the two entry points share cannot pass.  This file is collected last so that a failure
+here does not hide the other GPU tests."""
 import ctypes
 
 import numpy as np
@@ -31,7 +33,7 @@ def _ptr(t):
     return ctypes.c_void_p(t.data_ptr() if t is not None else 0)
 
 
-def test_static_workspace_matches_the_allocating_entry_point(lib):
+def test_static_workspace_matches_the_allocating_entry_point(lib, orc):
     from gqa_attention_kv_rope_gb300 import binding, kv
 
     nh, nk, hd = 16, 8, 128
@@ -65,6 +67,14 @@ def test_static_workspace_matches_the_allocating_entry_point(lib):
         assert err_got.item() == 0 and err_ref.item() == 0
         r, g = ref.cpu().numpy(), got.cpu().numpy()
         assert np.all(np.abs(g - r) <= ATOL + RTOL * np.abs(r)), f"call {call}: max abs {np.abs(g - r).max()}"
+        # and the oracle, one sequence at a time over its own rows of the arena
+        Kh, Vh, qh = K.cpu().numpy(), V.cpu().numpy(), q.cpu().numpy()
+        o = offs.cpu().numpy()
+        for s_, (c, ln) in enumerate(zip(caps, lengths)):
+            Ks, Vs = Kh[o[s_]:o[s_] + c], Vh[o[s_]:o[s_] + c]
+            want = orc.gqa_attn(qh[s_:s_ + 1], Ks, Vs, [ln], nh, nk, hd, hd, scale=scale, n_threads=8)
+            d = np.abs(g[s_:s_ + 1].astype(np.float64) - want)
+            assert np.all(d <= ATOL + RTOL * np.abs(want)), f"call {call}, sequence {s_}: max abs {d.max()}"
 
 
 def test_static_workspace_rejects_oversized_calls(lib):
