@@ -16,23 +16,21 @@ inline int stage_rows(int hd_kv, int kind) {
 }
 
 struct WsLayout {
-    size_t ml_off, acc_off, ticket_off, total;
+    size_t ml_off, acc_off, total;
     int key;  // the layout tag a call of this layout leaves in the control block
 };
 
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
-// The control block (counters and layout tag, shared with the prefill layout), the partial
-// (m, l) pairs and accumulators, then one merge ticket per (sequence, kv group).
-WsLayout ws_layout(int n_seq, int nh, int pairs_per_seq, int hd_kv, int splits) {
+// The control block (counters and layout tag, shared with the prefill layout), then the split
+// partials: (m, l) pairs and accumulators, zero (not yet written) between calls.
+WsLayout ws_layout(int n_seq, int nh, int hd_kv, int splits) {
     WsLayout w;
     const size_t parts = static_cast<size_t>(n_seq) * nh * splits;
-    const size_t tickets = static_cast<size_t>(n_seq) * pairs_per_seq;
     w.ml_off = kWsCtlBytes;
     w.acc_off = w.ml_off + align256(parts * 2 * sizeof(float));
-    w.ticket_off = w.acc_off + align256(parts * hd_kv * sizeof(float));
-    w.total = w.ticket_off + align256(tickets * sizeof(int));
-    w.key = ws_key(kWsKindDecode, w.acc_off, w.ticket_off, tickets, w.total);
+    w.total = w.acc_off + align256(parts * hd_kv * sizeof(float));
+    w.key = ws_key(kWsKindDecode, w.acc_off, w.total, parts, static_cast<unsigned long long>(splits));
     return w;
 }
 
@@ -77,7 +75,7 @@ Plan plan_for(int n_seq, int nh, int nk, int hd_kv, int max_cap, int kind) {
     const bool batch = pairs >= kGridTarget;
     p.min_rows = batch ? kBatchMinRows : stage_rows(hd_kv, kind);
     p.sorted = batch && n_seq > 1 && n_seq <= kMaxSort;
-    p.w = ws_layout(n_seq, nh, nk * p.groups, hd_kv, choose_splits(pairs, hd_kv, max_cap, kKvF32));
+    p.w = ws_layout(n_seq, nh, hd_kv, choose_splits(pairs, hd_kv, max_cap, kKvF32));
     return p;
 }
 
@@ -140,7 +138,6 @@ int launch_impl(const DecodeArgs &d, const DecodeStepExtra *x, cudaStream_t s) {
     k.err = d.err;
     k.ws_ml = reinterpret_cast<float *>(ws + pl.w.ml_off);
     k.ws_acc = reinterpret_cast<float *>(ws + pl.w.acc_off);
-    k.ws_ticket = reinterpret_cast<int *>(ws + pl.w.ticket_off);
     k.ws_ctr = reinterpret_cast<int *>(ws) + kWsUnitCtr;
     k.ws_done = reinterpret_cast<int *>(ws) + kWsUnitDone;
     k.ws_tag = reinterpret_cast<int *>(ws) + kWsTag;

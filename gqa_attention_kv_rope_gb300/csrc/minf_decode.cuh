@@ -26,10 +26,12 @@
 // that, like every other wait here, the wait is bounded.  Warp 9 (the utility warp) zeroes
 // the outputs of empty windows and flags out-of-range positions.
 //
-// Merge.  A unit writes its partial (m, l, acc) to the workspace; the last unit of a
-// (sequence, kv group) to arrive -- an atomic ticket, no spinning -- folds all partials in
-// one round trip: every consumer thread loads its share of the (m, l, acc) triples at once
-// and folds them online, then the shares are folded in shared memory; it resets the ticket.
+// Merge.  The run that ends the window (a group's last split, the shortest) is the merger.
+// Every other unit stores its partial (m, l, acc) in the workspace, each word encoded so that
+// zero means "not yet written", and is done -- no atomic, no wait.  The merger polls those words
+// (every consumer thread its share of the splits, all of a chunk's loads in flight together)
+// until each is written, folds them in split order, adds its own partial, writes the output and
+// zeroes the words it read for the next call.
 //
 // Fused layer step (kFused).  For one query token per sequence the same launch also does
 // the rest of the layer's attention stage: each unit rotates its q heads in registers
@@ -57,12 +59,20 @@
 namespace minf {
 namespace dec {
 
-constexpr int kNW = 8;                  // consumer warps
-constexpr int kCons = kNW * 32;         // consumer threads
-constexpr int kProducer = kNW;          // warp 8: TMA producer
-constexpr int kUtility = kNW + 1;       // warp 9: RMSNorm rows, empty windows, position flags
-constexpr int kThreads = kCons + 64;    // + producer + utility (same register budget as 9 warps)
-constexpr int kSub = 8;                 // rows per warp sub-tile
+// Consumer warps: 16 (4-row sub-tiles) when a unit's q heads are few enough for their registers,
+// else 8 (8-row sub-tiles); either way a 64-row slice of a stage is one sub-tile per warp.  Then
+// a producer warp and a utility warp.
+template <int NW>
+struct Warps {
+    static constexpr int kNW = NW;               // consumer warps
+    static constexpr int kCons = NW * 32;        // consumer threads
+    static constexpr int kProducer = NW;         // TMA producer warp
+    static constexpr int kUtility = NW + 1;      // RMSNorm rows, the appended row, empty windows, flags
+    static constexpr int kThreads = kCons + 64;  // + producer + utility
+    static constexpr int kSub = 64 / NW;         // rows per warp sub-tile
+};
+// The consumer warp count for a unit of GH q heads of width HDKV.
+constexpr int consumer_warps(int gh, int hd_kv) { return (void)gh, (void)hd_kv, 8; }
 constexpr int kNST = 3;                 // pipeline stages
 constexpr int kPreWait = 2;             // stages a producer issues before the dependency wait
 constexpr int kStageBytes = 64 * 1024;  // K + V tile of one stage
@@ -111,7 +121,7 @@ template <int HDKV, typename T>
 struct Cfg {
     static constexpr bool Q = Elem<T>::q8;
     static constexpr int R = Q ? (HDKV == 64 ? 256 : 128) : kStageBytes / (2 * HDKV * Elem<T>::bytes);
-    static constexpr int SPW = R / (kSub * kNW);                  // sub-tiles per warp per stage
+    static constexpr int SPW = R / 64;                            // sub-tiles per warp per stage
     static constexpr int kQBytes = R * HDKV * Elem<T>::bytes;     // values (or quants) of one tensor
     static constexpr int kSBytes = Q ? R * 16 : 0;                // scale slices of one tensor
     static constexpr int kTensorBytes = kQBytes + kSBytes;
@@ -186,7 +196,6 @@ struct KParams {
     float scale_log2;
     int32_t *err;
     float *ws_ml, *ws_acc;
-    int *ws_ticket;
     int *ws_ctr, *ws_done;  // dynamic unit counter and the count of finished producers
     int *ws_tag;           // the workspace's layout tag (its control block)
     int ws_key;            // this call's layout: the tags it accepts are 0 and this one
@@ -207,6 +216,29 @@ struct KParams {
 __device__ __forceinline__ void prefetch_l2(const void *p, int bytes, int lane) {
     for (int off = lane * 128; off < bytes; off += 32 * 128)
         asm volatile("prefetch.global.L2 [%0];" ::"l"(static_cast<const char *>(p) + off));
+}
+
+// Split partials in the workspace are stored encoded so that an all-zero word means "not yet
+// written": the bits of the value, complemented (the one pattern that would encode to zero, a
+// NaN with every bit set, is stored as the canonical NaN instead).
+__device__ __forceinline__ uint32_t part_enc(float x) {
+    const uint32_t b = __float_as_uint(x);
+    return (b == 0xFFFFFFFFu ? 0x7FFFFFFFu : b) ^ 0xFFFFFFFFu;
+}
+__device__ __forceinline__ float part_dec(uint32_t e) { return __uint_as_float(e ^ 0xFFFFFFFFu); }
+// Loads that see other CTAs' stores each time they run (no L1, never merged across a poll loop).
+__device__ __forceinline__ uint2 ld_relaxed_v2(const uint2 *p) {
+    uint2 v;
+    asm volatile("ld.relaxed.gpu.global.v2.b32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ uint4 ld_relaxed_v4(const uint4 *p) {
+    uint4 v;
+    asm volatile("ld.relaxed.gpu.global.v4.b32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p)
+                 : "memory");
+    return v;
 }
 
 __device__ __forceinline__ float4 f4scale(float4 v, float s) {
@@ -424,12 +456,15 @@ __device__ __forceinline__ void append_new_row(const KParams &a, const Unit &t, 
     }
 }
 
-template <int HDKV, int GH, bool kFused, typename T>
-__global__ void __launch_bounds__(kThreads, 1)
+template <int HDKV, int GH, bool kFused, typename T, int NW = consumer_warps(GH, HDKV)>
+__global__ void __launch_bounds__(Warps<NW>::kThreads, 1)
     decode_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                   const __grid_constant__ CUtensorMap tmKs, const __grid_constant__ CUtensorMap tmVs,
                   const KParams a) {
     using C = Cfg<HDKV, T>;
+    constexpr int kNW = Warps<NW>::kNW, kCons = Warps<NW>::kCons, kSub = Warps<NW>::kSub;
+    constexpr int kProducer = Warps<NW>::kProducer, kUtility = Warps<NW>::kUtility;
+    constexpr int KP = kSub / 4;  // K passes of four rows per sub-tile
     constexpr bool Q = C::Q;
     constexpr int R = C::R, SPW = C::SPW;
     constexpr int EB = Elem<T>::bytes;
@@ -454,7 +489,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __shared__ float4 sm_red[kCons];
     __shared__ float sm_redM[kCons], sm_redL[kCons];
     __shared__ __align__(16) float sm_knew[HDKV], sm_vnew[HDKV];
-    __shared__ int sm_last, sm_abort, sm_wsbad;
+    __shared__ int sm_abort, sm_wsbad;
     __shared__ float sm_tab[kFused ? HDKV / 2 : 1];  // angular speeds, read by lane-varying index
     __shared__ float sm_sn[kFused ? HDKV / 2 : 1], sm_cs[kFused ? HDKV / 2 : 1];  // first unit's sin, cos
 
@@ -464,9 +499,59 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int n_units = a.n_seq * P * a.n_split;
     volatile int *abort_flag = &sm_abort;
 
-    if (kFused)
-        for (int i = tid; i < HDKV / 2; i += blockDim.x) sm_tab[i] = a.tab.f[i];
-    if (tid == 0) {
+    // The producer lane issues ring stage p_it next; the first p_st0 stages of its first unit go
+    // out before the CTA's first barrier (the stage copies need nothing the other threads set up).
+    uint32_t p_it = 0;
+    int p_st0 = 0;
+    // Copies one stage (st) of unit t (number u) into the next ring slot.
+    auto issue_stage = [&](const Unit &t, int u, int st, uint32_t it_) {
+        const int slot = it_ % kNST;
+        const int hk = t.y / a.groups;
+        sm_meta[slot] = make_int2(u, st);
+        mbar_arrive(&meta_full[slot]);  // publishes the slot's unit to the consumers
+        unsigned char *sb = ring + static_cast<size_t>(slot) * C::kSlotBytes;
+        mbar_expect_tx(&full[slot], C::kSlotBytes);
+        // x of the tile copies: in elements of the map (bytes for Q8_0, whose scale slice of this
+        // kv head starts xs bytes into the row)
+        const int xs = a.row_bytes ? static_cast<int>(W + (hk / kScaleHeads) * 16) : 0;
+        if (!a.table) {
+            const int row = static_cast<int>(t.base) + t.r_begin + st * R;
+            tma_load_2d_stream(sb, &tmK, hk * HDKV, row, &full[slot]);
+            tma_load_2d_stream(sb + C::kTensorBytes, &tmV, hk * HDKV, row, &full[slot]);
+            if (Q) {
+                tma_load_2d(sb + C::kQBytes, &tmKs, xs, row, &full[slot]);
+                tma_load_2d(sb + C::kTensorBytes + C::kQBytes, &tmVs, xs, row, &full[slot]);
+            }
+        } else {
+            // one copy per block piece; a block the table does not hold reads as zeros (its rows
+            // start past the pool) and is reported
+            for (int c = 0; c < R / a.box_rows; ++c) {
+                const int lrow = t.r_begin + st * R + c * a.box_rows;
+                const int blk = lrow / a.block_rows;
+                const int b = blk < a.max_blocks ? __ldg(a.table + static_cast<size_t>(t.s) * a.max_blocks + blk) : -1;
+                const long long prow = static_cast<long long>(b) * a.block_rows + lrow % a.block_rows;
+                const bool ok = b >= 0 && prow < a.pool_rows;
+                if (!ok && lrow < t.L) flag_error(a.err, MINF_ERRBIT_BLOCK);
+                const int row = ok ? static_cast<int>(prow) : static_cast<int>(a.pool_rows);
+                const int qo = c * a.box_rows * HDKV * EB;
+                tma_load_2d(sb + qo, &tmK, hk * HDKV, row, &full[slot]);
+                tma_load_2d(sb + C::kTensorBytes + qo, &tmV, hk * HDKV, row, &full[slot]);
+                if (Q) {
+                    const int so = C::kQBytes + c * a.box_rows * 16;
+                    tma_load_2d(sb + so, &tmKs, xs, row, &full[slot]);
+                    tma_load_2d(sb + C::kTensorBytes + so, &tmVs, xs, row, &full[slot]);
+                }
+            }
+        }
+    };
+    if (tid == kProducer * 32) {
+        // the tensor maps and every barrier of the CTA, by the lane that issues the copies
+        prefetch_tensormap(&tmK);
+        prefetch_tensormap(&tmV);
+        if (Q) {
+            prefetch_tensormap(&tmKs);
+            prefetch_tensormap(&tmVs);
+        }
         for (int i = 0; i < kNST; ++i) {
             mbar_init(&full[i], 1);
             mbar_init(&empty[i], kNW);
@@ -476,7 +561,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(&knew_bar, 1);
         sm_abort = 0;
         mbar_init_fence();
+        // With early start and no ordering of a batch to wait for, the first unit's first stages
+        // go out now: before the angular speeds are staged and the CTA's barrier, a few
+        // microseconds earlier than the rest of the CTA gets going.
+        if (a.early && !a.sorted) {
+            const Unit t = unit_of<R>(a, blockIdx.x, nullptr);
+            if (unit_active(t)) {
+                const int n_st = (t.r_end - t.r_begin + R - 1) / R;
+                for (; p_st0 < n_st && p_st0 < kPreWait; ++p_st0, ++p_it)
+                    issue_stage(t, static_cast<int>(blockIdx.x), p_st0, p_it);
+            }
+        }
     }
+    if (kFused)
+        for (int i = tid; i < HDKV / 2; i += blockDim.x) sm_tab[i] = a.tab.f[i];
     // Without early start nothing is read before the launch ahead of this one has finished:
     // the positions and the cached rows may be its outputs.
     if (!a.early) gdc_wait();
@@ -574,7 +672,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == kProducer) {
         // ---------------------------------------------------------------- producer
         if (lane == 0) {
-            uint32_t it = 0;
+            uint32_t it = p_it;
             bool waited = false;
             int ptag = 0;  // the workspace's tag, read once the launch before this one has finished
             auto wait_dep = [&]() {
@@ -586,9 +684,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             while (u < n_units && !*abort_flag) {
                 const Unit t = unit_of<R>(a, u, order);
                 if (unit_active(t)) {
-                    const int hk = t.y / a.groups;
                     const int n_st = (t.r_end - t.r_begin + R - 1) / R;
-                    for (int st = 0; st < n_st && !*abort_flag; ++st, ++it) {
+                    // the first unit's first p_st0 stages went out before the CTA's barrier
+                    for (int st = u == static_cast<int>(blockIdx.x) ? p_st0 : 0; st < n_st && !*abort_flag;
+                         ++st, ++it) {
                         const int slot = it % kNST;
                         // Cached rows need no wait, but only kPreWait stages go out before it:
                         // a deeper burst, issued while the previous launch merges its splits and
@@ -597,43 +696,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         if (it >= kNST) {
                             if (!mbar_wait(&empty[slot], ((it / kNST) & 1) ^ 1, abort_flag, a.err)) break;
                         }
-                        sm_meta[slot] = make_int2(u, st);
-                        mbar_arrive(&meta_full[slot]);  // publishes the slot's unit to the consumers
-                        unsigned char *sb = ring + static_cast<size_t>(slot) * C::kSlotBytes;
-                        mbar_expect_tx(&full[slot], C::kSlotBytes);
-                        // x of the tile copies: in elements of the map (bytes for Q8_0, whose
-                        // scale slice of this kv head starts xs bytes into the row)
-                        const int xs = a.row_bytes ? static_cast<int>(W + (hk / kScaleHeads) * 16) : 0;
-                        if (!a.table) {
-                            const int row = static_cast<int>(t.base) + t.r_begin + st * R;
-                            tma_load_2d(sb, &tmK, hk * HDKV, row, &full[slot]);
-                            tma_load_2d(sb + C::kTensorBytes, &tmV, hk * HDKV, row, &full[slot]);
-                            if (Q) {
-                                tma_load_2d(sb + C::kQBytes, &tmKs, xs, row, &full[slot]);
-                                tma_load_2d(sb + C::kTensorBytes + C::kQBytes, &tmVs, xs, row, &full[slot]);
-                            }
-                        } else {
-                            // one copy per block piece; a block the table does not hold reads
-                            // as zeros (its rows start past the pool) and is reported
-                            for (int c = 0; c < R / a.box_rows; ++c) {
-                                const int lrow = t.r_begin + st * R + c * a.box_rows;
-                                const int blk = lrow / a.block_rows;
-                                const int b = blk < a.max_blocks ? __ldg(a.table + static_cast<size_t>(t.s) * a.max_blocks + blk)
-                                                                  : -1;
-                                const long long prow = static_cast<long long>(b) * a.block_rows + lrow % a.block_rows;
-                                const bool ok = b >= 0 && prow < a.pool_rows;
-                                if (!ok && lrow < t.L) flag_error(a.err, MINF_ERRBIT_BLOCK);
-                                const int row = ok ? static_cast<int>(prow) : static_cast<int>(a.pool_rows);
-                                const int qo = c * a.box_rows * HDKV * EB;
-                                tma_load_2d(sb + qo, &tmK, hk * HDKV, row, &full[slot]);
-                                tma_load_2d(sb + C::kTensorBytes + qo, &tmV, hk * HDKV, row, &full[slot]);
-                                if (Q) {
-                                    const int so = C::kQBytes + c * a.box_rows * 16;
-                                    tma_load_2d(sb + so, &tmKs, xs, row, &full[slot]);
-                                    tma_load_2d(sb + C::kTensorBytes + so, &tmVs, xs, row, &full[slot]);
-                                }
-                            }
-                        }
+                        issue_stage(t, u, st, it);
                     }
                 }
                 if (!waited) wait_dep();  // the unit counter lives in the workspace a preceding launch may use
@@ -709,7 +772,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         released = true;
     }
     // The workspace's tag, checked before the first partial is written (the load is in flight
-    // meanwhile): a workspace another layout left may hold non-zero tickets where this call's are.
+    // meanwhile): a workspace another layout left may hold non-zero words where this call's
+    // partials are, which would read as written.
     const int ctag = tid == 0 ? ld_relaxed(a.ws_tag) : 0;
     bool ws_checked = false;
     while (true) {
@@ -822,18 +886,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 cons_sync(&cons_bar, cphase, abort_flag, a.err);
             }
-            // The warp's SPW sub-tiles of 8 rows, GRP at a time: the scores of all their rows
+            // The warp's SPW sub-tiles of kSub rows, GRP at a time: the scores of all their rows
             // first (a K row is spread over 8 lanes, four rows per pass), then one online-softmax
             // update for them, then their V rows (one per pass of VL lanes).  Q8_0 blocks apply
             // their scale once: to a block's partial dot product (K), and to the weight (V).
 #pragma unroll 1
             for (int g0 = 0; g0 < SPW; g0 += GRP) {  // one pass when the heads are few
-            float sc[GRP][2][GH];
+            float sc[GRP][KP][GH];
 #pragma unroll
             for (int sp = 0; sp < GRP; ++sp) {
                 const int rr0 = (warp * SPW + g0 + sp) * kSub;  // sub-tile's first row within the stage
 #pragma unroll
-                for (int it2 = 0; it2 < 2; ++it2) {
+                for (int it2 = 0; it2 < KP; ++it2) {
                     const int rr = rr0 + 4 * it2 + r4;
                     float4 kv[KF4];
 #pragma unroll
@@ -870,7 +934,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int sp = 0; sp < GRP; ++sp)
 #pragma unroll
-                    for (int it2 = 0; it2 < 2; ++it2) mx = fmaxf(mx, sc[sp][it2][hh]);
+                    for (int it2 = 0; it2 < KP; ++it2) mx = fmaxf(mx, sc[sp][it2][hh]);
                 mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
                 mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
                 const float m_new = fmaxf(m[hh], mx);
@@ -881,7 +945,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int sp = 0; sp < GRP; ++sp)
 #pragma unroll
-                    for (int it2 = 0; it2 < 2; ++it2) {
+                    for (int it2 = 0; it2 < KP; ++it2) {
                         const float pv = none ? 0.0f : ex2_approx(sc[sp][it2][hh] - m_new);
                         sc[sp][it2][hh] = pv;  // from here on: the row's weight
                         ps += pv;
@@ -898,7 +962,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int rr0 = (warp * SPW + g0 + sp) * kSub;
 #pragma unroll
                 for (int jv = 0; jv < VJ; ++jv) {
-                    const int rl = vrow + VRP * jv;  // row within the sub-tile, 0..7
+                    const int rl = vrow + VRP * jv;  // row within the sub-tile, 0..kSub-1
                     const int rr = rr0 + rl;
                     const bool in_run = row0 + rr < t.r_end;
                     // past the run: anything finite (its weight is 0)
@@ -959,10 +1023,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         ws_checked = true;
         cons_sync(&cons_bar, cphase, abort_flag, a.err);
         if (sm_wsbad) continue;  // nothing that depends on the workspace: no partial, merge or output
+        // The run that ends the window (the group's last split, the shortest) merges: every other
+        // split stores its partial (m, l, acc) encoded so that zero reads as "not yet written" and
+        // leaves at once -- no atomic, no wait -- and the merger polls the partial words themselves
+        // until all are written, folds them in a fixed order and zeroes them for the next call.
         float *out_s = a.out + (static_cast<size_t>(t.s) * a.nh + h0) * HDKV;
         const size_t part0 = (static_cast<size_t>(t.s) * a.nh + h0) * a.n_split;  // head h0, split 0
-        for (int i = tid; i < GH * VL; i += kCons) {
-            const int hh = i / VL, c = i % VL;
+        constexpr int kPairs = GH * VL;  // (head, float4 column) pairs of the unit's output
+        static_assert(kPairs <= kCons, "one pair per consumer thread");
+        const bool multi = t.n_act > 1;
+        const bool merger = t.j == t.n_act - 1;
+        float own_M = -INFINITY, own_L = 0.0f;  // this unit's partial, for thread tid's pair
+        float4 own_A = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (tid < kPairs) {
+            const int hh = tid / VL, c = tid % VL;
             float M = sm_m[0][hh];
 #pragma unroll
             for (int w = 1; w < kNW; ++w) M = fmaxf(M, sm_m[w][hh]);
@@ -978,78 +1052,109 @@ __global__ void __launch_bounds__(kThreads, 1)
                 A.z = fmaf(x.z, f, A.z);
                 A.w = fmaf(x.w, f, A.w);
             }
-            if (t.n_act == 1) {
+            if (!multi) {
                 reinterpret_cast<float4 *>(out_s + hh * HDKV)[c] = f4scale(A, 1.0f / Ls);
-            } else {
+            } else if (!merger) {
                 const size_t part = part0 + static_cast<size_t>(hh) * a.n_split + t.j;
-                if (c == 0) {
-                    a.ws_ml[2 * part] = M;
-                    a.ws_ml[2 * part + 1] = Ls;
-                }
-                reinterpret_cast<float4 *>(a.ws_acc + part * HDKV)[c] = A;
+                if (c == 0)
+                    reinterpret_cast<uint2 *>(a.ws_ml)[part] = make_uint2(part_enc(M), part_enc(Ls));
+                reinterpret_cast<uint4 *>(a.ws_acc + part * HDKV)[c] =
+                    make_uint4(part_enc(A.x), part_enc(A.y), part_enc(A.z), part_enc(A.w));
+            } else {
+                own_M = M;
+                own_L = Ls;
+                own_A = A;
             }
         }
+        if (multi && !merger) continue;  // the partial is stored: this unit is done
 
-        bool last = true;
-        int *ticket = a.ws_ticket + static_cast<size_t>(t.s) * P + t.y;
-        if (t.n_act > 1) {
-            cons_sync(&cons_bar, cphase, abort_flag, a.err);
-            if (tid == 0) {
-                // acq_rel: publishes this CTA's partials (ordered before it by the barrier) and,
-                // for the last arrival, makes every other unit's partials visible to its loads
-                int old;
-                asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], 1;" : "=r"(old) : "l"(ticket) : "memory");
-                sm_last = old == t.n_act - 1;
-            }
-            cons_sync(&cons_bar, cphase, abort_flag, a.err);
-            last = sm_last;
-        }
-        if (!last) continue;
-
-        if (t.n_act > 1) {
-            // One round trip for the merge: each thread folds its share of the splits online
-            // (running max and rescaled sums), then the shares are folded in shared memory.
-            constexpr int kPairs = GH * VL;
-            constexpr int kWays = kCons / kPairs > 0 ? kCons / kPairs : 1;
+        if (multi) {
+            // Each thread polls and folds its share of the other splits (those of index
+            // way mod kWays, kChunk of them with their loads in flight together), in split order;
+            // then the shares are folded in shared memory, and this unit's own partial last.
+            constexpr int kWays = kCons / kPairs;
+            constexpr int kChunk = GH <= 2 ? 8 : (GH <= 4 ? 4 : 2);
+            const int n_oth = t.n_act - 1;  // the other splits: 0 .. n_act - 2
             for (int i = tid; i < kPairs * kWays; i += kCons) {
                 const int pair = i % kPairs, way = i / kPairs;
                 const int hh = pair / VL, c = pair % VL;
                 const size_t ph2 = part0 + static_cast<size_t>(hh) * a.n_split;
                 float M = -INFINITY, Ls = 0.0f;
                 float4 A = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 8
-                for (int j = way; j < t.n_act; j += kWays) {
-                    const float2 ml = __ldcg(reinterpret_cast<const float2 *>(a.ws_ml) + (ph2 + j));
-                    const float4 x = __ldcg(reinterpret_cast<const float4 *>(a.ws_acc + (ph2 + j) * HDKV) + c);
-                    const float Mn = fmaxf(M, ml.x);
-                    const float fo = M == -INFINITY ? 0.0f : ex2_approx(M - Mn);
-                    const float fn = ex2_approx(ml.x - Mn);
-                    A = make_float4(fmaf(x.x, fn, A.x * fo), fmaf(x.y, fn, A.y * fo), fmaf(x.z, fn, A.z * fo),
-                                    fmaf(x.w, fn, A.w * fo));
-                    Ls = fmaf(ml.y, fn, Ls * fo);
-                    M = Mn;
+                for (int j0 = way; j0 < n_oth; j0 += kWays * kChunk) {
+                    uint2 mlv[kChunk];
+                    uint4 xv[kChunk];
+                    uint32_t pend = 0;
+#pragma unroll
+                    for (int k = 0; k < kChunk; ++k)
+                        if (j0 + k * kWays < n_oth) pend |= 1u << k;
+                    const unsigned long long tb = gtimer();
+                    while (pend && !*abort_flag) {
+#pragma unroll
+                        for (int k = 0; k < kChunk; ++k)
+                            if (pend >> k & 1u) {
+                                const size_t part = ph2 + j0 + k * kWays;
+                                mlv[k] = ld_relaxed_v2(reinterpret_cast<const uint2 *>(a.ws_ml) + part);
+                                xv[k] = ld_relaxed_v4(reinterpret_cast<const uint4 *>(a.ws_acc + part * HDKV) + c);
+                            }
+#pragma unroll
+                        for (int k = 0; k < kChunk; ++k)
+                            if ((pend >> k & 1u) && mlv[k].x && mlv[k].y && xv[k].x && xv[k].y && xv[k].z && xv[k].w)
+                                pend &= ~(1u << k);
+                        if (pend && gtimer() - tb > kWaitBudgetNs) {
+                            *abort_flag = 1;
+                            flag_error(a.err, MINF_ERRBIT_TIMEOUT);
+                        }
+                    }
+#pragma unroll
+                    for (int k = 0; k < kChunk; ++k) {
+                        if (j0 + k * kWays >= n_oth) break;
+                        const float mj = part_dec(mlv[k].x), lj = part_dec(mlv[k].y);
+                        const float4 x = make_float4(part_dec(xv[k].x), part_dec(xv[k].y), part_dec(xv[k].z),
+                                                     part_dec(xv[k].w));
+                        const float Mn = fmaxf(M, mj);
+                        const float fo = M == -INFINITY ? 0.0f : ex2_approx(M - Mn);
+                        const float fn = mj == -INFINITY ? 0.0f : ex2_approx(mj - Mn);
+                        A = make_float4(fmaf(x.x, fn, A.x * fo), fmaf(x.y, fn, A.y * fo), fmaf(x.z, fn, A.z * fo),
+                                        fmaf(x.w, fn, A.w * fo));
+                        Ls = fmaf(lj, fn, Ls * fo);
+                        M = Mn;
+                    }
                 }
                 sm_red[way * kPairs + pair] = A;
                 sm_redM[way * kPairs + pair] = M;
                 sm_redL[way * kPairs + pair] = Ls;
             }
             cons_sync(&cons_bar, cphase, abort_flag, a.err);
-            for (int i = tid; i < kPairs; i += kCons) {
-                const int hh = i / VL, c = i % VL;
-                float M = sm_redM[i];
-                for (int w = 1; w < kWays; ++w) M = fmaxf(M, sm_redM[w * kPairs + i]);
+            // every poll is done: the partials read go back to zero for the next call
+            for (int i = tid; i < kPairs * kWays; i += kCons) {
+                const int pair = i % kPairs, way = i / kPairs;
+                const int hh = pair / VL, c = pair % VL;
+                const size_t ph2 = part0 + static_cast<size_t>(hh) * a.n_split;
+                for (int j = way; j < n_oth; j += kWays) {
+                    reinterpret_cast<uint4 *>(a.ws_acc + (ph2 + j) * HDKV)[c] = make_uint4(0u, 0u, 0u, 0u);
+                    if (c == 0) reinterpret_cast<uint2 *>(a.ws_ml)[ph2 + j] = make_uint2(0u, 0u);
+                }
+            }
+            if (tid < kPairs) {
+                const int hh = tid / VL, c = tid % VL;
+                float M = own_M;
+                for (int w = 0; w < kWays; ++w) M = fmaxf(M, sm_redM[w * kPairs + tid]);
+                const float fo = own_M == -INFINITY ? 0.0f : ex2_approx(own_M - M);
                 float Ls = 0.0f;
                 float4 A = make_float4(0.f, 0.f, 0.f, 0.f);
                 for (int w = 0; w < kWays; ++w) {
-                    const float mw = sm_redM[w * kPairs + i];
+                    const float mw = sm_redM[w * kPairs + tid];
                     const float f = mw == -INFINITY ? 0.0f : ex2_approx(mw - M);
-                    const float4 x = sm_red[w * kPairs + i];
+                    const float4 x = sm_red[w * kPairs + tid];
                     A = make_float4(fmaf(x.x, f, A.x), fmaf(x.y, f, A.y), fmaf(x.z, f, A.z), fmaf(x.w, f, A.w));
-                    Ls = fmaf(sm_redL[w * kPairs + i], f, Ls);
+                    Ls = fmaf(sm_redL[w * kPairs + tid], f, Ls);
                 }
+                A = make_float4(fmaf(own_A.x, fo, A.x), fmaf(own_A.y, fo, A.y), fmaf(own_A.z, fo, A.z),
+                                fmaf(own_A.w, fo, A.w));
+                Ls = fmaf(own_L, fo, Ls);
                 reinterpret_cast<float4 *>(out_s + hh * HDKV)[c] = f4scale(A, 1.0f / Ls);
             }
-            if (tid == 0) *ticket = 0;  // ready for the next call or graph replay
         }
         if (kFused && lane < 8) {
             // every other unit of this group has finished reading q: write it back rotated
@@ -1071,6 +1176,7 @@ cudaError_t launch_t(const CUtensorMap &tk, const CUtensorMap &tv, const CUtenso
                      const CUtensorMap &tvs, const KParams &k, int grid, cudaStream_t s,
                      bool pdl) {
     const size_t smem = static_cast<size_t>(kNST) * Cfg<HDKV, T>::kSlotBytes + 1024;
+    constexpr int kThreads = Warps<consumer_warps(GH, HDKV)>::kThreads;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     static std::atomic<bool> attr_set[64];  // per device, shared by host threads

@@ -78,6 +78,25 @@ __device__ __forceinline__ bool mbar_wait(unsigned long long *b, uint32_t parity
     }
 }
 
+// Brings a tensor map (a __grid_constant__ kernel parameter) into the TMA unit's descriptor
+// cache ahead of its first copy.
+__device__ __forceinline__ void prefetch_tensormap(const CUtensorMap *m) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(m) : "memory");
+}
+
+// The same copy with an evict-first L2 policy: for rows streamed once per step, so that they
+// leave L2 before the small operands (q, positions, partials) that other requests wait on.
+__device__ __forceinline__ void tma_load_2d_stream(void *dst, const CUtensorMap *map, int x, int y,
+                                                   unsigned long long *bar) {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1, {%2, "
+        "%3}], [%4], %5;" ::"r"(su32(dst)),
+        "l"(map), "r"(x), "r"(y), "r"(su32(bar)), "l"(pol)
+        : "memory");
+}
+
 // 2-D tensor copy global -> shared, completion counted in bytes on the mbarrier.
 __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, int x, int y,
                                             unsigned long long *bar) {
