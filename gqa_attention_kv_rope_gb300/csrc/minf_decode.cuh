@@ -75,6 +75,7 @@ struct Warps {
 constexpr int consumer_warps(int gh, int hd_kv) { return (void)gh, (void)hd_kv, 8; }
 constexpr int kNST = 3;                 // pipeline stages
 constexpr int kPreWait = 2;             // stages a producer issues before the dependency wait
+constexpr unsigned kPreWaitGapNs = 500; // between two of them: the previous launch merges meanwhile
 constexpr int kStageBytes = 64 * 1024;  // K + V tile of one stage
 constexpr int kGridTarget = 152;        // GB300: one persistent CTA per SM
 constexpr int kMaxSplit = 64;           // partials per (sequence, kv group)
@@ -503,6 +504,7 @@ __global__ void __launch_bounds__(Warps<NW>::kThreads, 1)
     // out before the CTA's first barrier (the stage copies need nothing the other threads set up).
     uint32_t p_it = 0;
     int p_st0 = 0;
+    unsigned long long t_first = 0;  // when the producer issued its first stage before the barrier
     // Copies one stage (st) of unit t (number u) into the next ring slot.
     auto issue_stage = [&](const Unit &t, int u, int st, uint32_t it_) {
         const int slot = it_ % kNST;
@@ -561,15 +563,16 @@ __global__ void __launch_bounds__(Warps<NW>::kThreads, 1)
         mbar_init(&knew_bar, 1);
         sm_abort = 0;
         mbar_init_fence();
-        // With early start and no ordering of a batch to wait for, the first unit's first stages
-        // go out now: before the angular speeds are staged and the CTA's barrier, a few
+        // With early start and no ordering of a batch to wait for, the first unit's first stage
+        // goes out now: before the angular speeds are staged and the CTA's barrier, a few
         // microseconds earlier than the rest of the CTA gets going.
         if (a.early && !a.sorted) {
             const Unit t = unit_of<R>(a, blockIdx.x, nullptr);
             if (unit_active(t)) {
-                const int n_st = (t.r_end - t.r_begin + R - 1) / R;
-                for (; p_st0 < n_st && p_st0 < kPreWait; ++p_st0, ++p_it)
-                    issue_stage(t, static_cast<int>(blockIdx.x), p_st0, p_it);
+                issue_stage(t, static_cast<int>(blockIdx.x), 0, 0);
+                p_st0 = 1;
+                p_it = 1;
+                t_first = gtimer();
             }
         }
     }
@@ -689,9 +692,13 @@ __global__ void __launch_bounds__(Warps<NW>::kThreads, 1)
                     for (int st = u == static_cast<int>(blockIdx.x) ? p_st0 : 0; st < n_st && !*abort_flag;
                          ++st, ++it) {
                         const int slot = it % kNST;
-                        // Cached rows need no wait, but only kPreWait stages go out before it:
-                        // a deeper burst, issued while the previous launch merges its splits and
-                        // completes, slows that launch's round trips more than it saves here.
+                        // Cached rows need no wait, but only kPreWait stages go out before it, and
+                        // kPreWaitGapNs apart: this launch's CTAs start as the previous launch's
+                        // leave, while its merging splits poll their partials in L2, and a deeper
+                        // or denser burst slows those round trips more than it saves here.
+                        if (!waited && it > 0 && it < kPreWait && t_first)
+                            while (gtimer() - t_first < kPreWaitGapNs) {
+                            }
                         if (!waited && it >= kPreWait) wait_dep();
                         if (it >= kNST) {
                             if (!mbar_wait(&empty[slot], ((it / kNST) & 1) ^ 1, abort_flag, a.err)) break;
