@@ -706,11 +706,14 @@ __global__ void __launch_bounds__(Warps<NW>::kThreads, 1)
                         issue_stage(t, u, st, it);
                     }
                 }
+                if (early) break;  // every unit is a first unit: nothing to draw
                 if (!waited) wait_dep();  // the unit counter lives in the workspace a preceding launch may use
                 // a workspace of another layout: no further units (the consumers flag it)
                 u = (ptag == 0 || ptag == a.ws_key) ? static_cast<int>(gridDim.x) + atomicAdd(a.ws_ctr, 1) : n_units;
             }
-            if (!waited) wait_dep();
+            // With one unit a CTA the producer touches nothing a preceding launch may write: the end
+            // of the stream goes out without waiting, and the counters stay unused.
+            if (!waited && !early) wait_dep();
             // end of the stream for this CTA's consumers
             const int slot = it % kNST;
             if (it < kNST || mbar_wait(&empty[slot], ((it / kNST) & 1) ^ 1, abort_flag, a.err)) {
@@ -719,8 +722,8 @@ __global__ void __launch_bounds__(Warps<NW>::kThreads, 1)
             }
             // the last producer to finish resets the counters for the next call or graph replay
             // (the fences order every producer's draws before its count, and the reset after)
-            __threadfence();
-            if (atomicAdd(a.ws_done, 1) == static_cast<int>(gridDim.x) - 1) {
+            if (!early) __threadfence();
+            if (!early && atomicAdd(a.ws_done, 1) == static_cast<int>(gridDim.x) - 1) {
                 __threadfence();
                 *a.ws_ctr = 0;
                 *a.ws_done = 0;
@@ -735,6 +738,7 @@ __global__ void __launch_bounds__(Warps<NW>::kThreads, 1)
                         while (!mbar_try(&full[k % kNST], (k / kNST) & 1) && gtimer() - t0 < kWaitBudgetNs) {
                         }
                     }
+                if (!waited) gdc_wait();  // (the workspace may still be the preceding launch's)
                 *a.ws_tag = kWsPoison;  // its counters may be left non-zero: refused until zero-filled
             }
         }
@@ -1026,6 +1030,9 @@ __global__ void __launch_bounds__(Warps<NW>::kThreads, 1)
         if (tid == 0 && !ws_checked) {
             sm_wsbad = !(ctag == 0 || ctag == a.ws_key);
             if (sm_wsbad) flag_error(a.err, MINF_ERRBIT_WORKSPACE);
+            // a fresh workspace takes this call's layout (when units are drawn, the last producer
+            // does it; here no producer counts its finish)
+            if (early && ctag == 0) atomicCAS(a.ws_tag, 0, a.ws_key);
         }
         ws_checked = true;
         cons_sync(&cons_bar, cphase, abort_flag, a.err);
