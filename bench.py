@@ -295,7 +295,15 @@ class Timer:
 
 
 def flush_l2(buf):
-    buf.zero_()
+    """Evicts L2 by reading a buffer twice its size.  A read, not a write: a written buffer would
+    leave its dirty lines in L2 for the timed work to write back."""
+    buf.sum()
+
+
+def l2_flush_buffer(torch, dev):
+    buf = torch.ones(2 * L2_BYTES // 4, device=dev)  # written once, here; the flushes only read it
+    torch.cuda.synchronize()
+    return buf
 
 
 # ----------------------------------------------------------------------------- workloads
@@ -450,7 +458,7 @@ def run_headline(m, torch, wl, args, world, dev):
 def run_sweep(m, torch, wl, H, args):
     S, graph, stream = H["S"], H["graph"], H["stream"]
     g = S["g"]
-    flush = torch.empty(2 * L2_BYTES // 4, device=S["inputs"].device)
+    flush = l2_flush_buffer(torch, S["inputs"].device)
     out = {}
     for n in wl.LONG_CONTEXT_SWEEP:
         S["pos"].fill_(n)
@@ -459,9 +467,9 @@ def run_sweep(m, torch, wl, H, args):
             graph.replay()
         times = []
         for _ in range(max(3, args.steps // 2)):
-            flush_l2(flush)
             a, b = Timer(torch, stream).pair()
             with torch.cuda.stream(stream):
+                flush_l2(flush)  # on the stream the replay runs on, before its start event
                 a.record(stream)
                 graph.replay()
                 b.record(stream)
@@ -560,12 +568,12 @@ def run_prefill(m, torch, wl, dev, steps):
     g, nt = P["g"], P["nt"]
     stream = torch.cuda.Stream()
     graph = capture(torch, stream, P["step"])
-    flush = torch.empty(2 * L2_BYTES // 4, device=dev)
+    flush = l2_flush_buffer(torch, dev)
     times = []
     for i in range(steps + 3):
-        flush_l2(flush)
         a, b = Timer(torch, stream).pair()
         with torch.cuda.stream(stream):
+            flush_l2(flush)  # on the stream the replay runs on, before its start event
             a.record(stream)
             graph.replay()
             b.record(stream)
@@ -862,7 +870,7 @@ def run_elementwise(m, torch, dev, reps=20):
     """HBM throughput of the stand-alone RMSNorm (4096 and 32768 rows of 1024, gains) and
     SiLU*mul (64 Mi elements) kernels, L2 flushed before every timed launch.  The 32768-row
     case moves 128 MiB each way (more than L2); the 4096-row case is latency-bound."""
-    flush = torch.empty(2 * L2_BYTES // 4, device=dev)
+    flush = l2_flush_buffer(torch, dev)
     stream = torch.cuda.current_stream()
     x = torch.randn(4096, 1024, device=dev)
     w = torch.rand(1024, device=dev) + 0.5
