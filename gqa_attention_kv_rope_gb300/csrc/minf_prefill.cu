@@ -971,12 +971,15 @@ struct StepSmem {
 // The row work of the step, spread over every thread of the grid.  The first warps take the
 // RMSNorm rows (a warp a row); every other thread takes one unit at a time: a RoPE unit -- pair
 // group j (pairs 4j .. 4j+3) of token t in up to kRopeHeads q heads or k heads, rotated in place,
-// the k rows also stored at pos -- or a float4 of v, stored at pos.  A RoPE unit computes its
+// the k rows also stored at pos -- or kVPerUnit float4 of v, stored at pos.  A RoPE unit computes its
 // four angles' sines and cosines once for its heads and loads all of its heads before it stores
 // any, so that those loads are in flight together.  A pair group is two float4: elements
 // i..i+3 and i+hd/2.. (style 0) or 8j..8j+7 (style 1).  The error bits are those of the
 // separate RoPE + store launch.
 constexpr int kRopeHeads = 8;
+// float4 of v a unit copies: few enough units that a grid of one CTA an SM takes every RoPE and
+// v unit of a 512-token step in one pass (a second unit a thread was the slowest CTAs' tail)
+constexpr int kVPerUnit = 4;
 
 struct RopeGroup {
     float4 u0[kRopeHeads], u1[kRopeHeads];
@@ -1046,20 +1049,27 @@ __device__ __forceinline__ void step_rows(const PParams &a, const StepParams &x,
     const int gq = a.hd >> 3, gk = hd_kv >> 3;  // pair groups of a head
     const int bq = (a.nh + kRopeHeads - 1) / kRopeHeads, bk = (a.nk + kRopeHeads - 1) / kRopeHeads;
     const int per_tok = gq * bq + gk * bk;  // RoPE units of a token
-    const int nvu = a.W >> 2;
+    const int nvu = a.W >> 2;                          // float4 of a v row
+    const int nvg = (nvu + kVPerUnit - 1) / kVPerUnit;  // v units of a token
     const int n_rope = a.nt * per_tok;  // the host keeps nt * (per_tok + nvu) below 2^30
-    const int total = n_rope + a.nt * nvu;
+    const int total = n_rope + a.nt * nvg;
     for (int u = gt; u < total; u += G) {
-        if (u >= n_rope) {  // a float4 of v (loaded together with its position)
+        if (u >= n_rope) {  // kVPerUnit float4 of v (loaded together with their position)
             const int w = u - n_rope;
-            const int t = w / nvu, c = w - t * nvu;
+            const int t = w / nvg, c0 = (w - t * nvg) * kVPerUnit;
             const int p = __ldg(a.pos + t);
-            const float4 vv = reinterpret_cast<const float4 *>(x.v)[static_cast<size_t>(t) * nvu + c];
+            const float4 *vr = reinterpret_cast<const float4 *>(x.v) + static_cast<size_t>(t) * nvu;
+            float4 vv[kVPerUnit];
+#pragma unroll
+            for (int e = 0; e < kVPerUnit; ++e)
+                if (c0 + e < nvu) vv[e] = vr[c0 + e];
             if (p < 0 || p >= a.cap) {
-                if (c == 0) flag_error(a.err, MINF_ERRBIT_STORE_POS);
+                if (c0 == 0) flag_error(a.err, MINF_ERRBIT_STORE_POS);
                 continue;
             }
-            put4(static_cast<T *>(x.v_st), static_cast<size_t>(p) * nvu + c, vv);
+#pragma unroll
+            for (int e = 0; e < kVPerUnit; ++e)
+                if (c0 + e < nvu) put4(static_cast<T *>(x.v_st), static_cast<size_t>(p) * nvu + c0 + e, vv[e]);
             continue;
         }
         const int t = u / per_tok;

@@ -136,6 +136,43 @@ def test_fused_qkv_position_errors(m):
     assert np.array_equal(Kd.cpu().numpy(), K0) and np.array_equal(Vd.cpu().numpy(), K0)
 
 
+def test_fused_qkv_one_token_edges(m, orc):
+    """One token (the one-token instantiation): without a gain (a gain of ones in the oracle),
+    and at a position past the region (rotated, written, not stored) and before it (not
+    rotated, not stored)."""
+    from gqa_attention_kv_rope_gb300 import workloads as wl
+
+    g, cap = wl.QWEN25_05B, 64
+    h, gain, w, b = _case(g, 1, 60)
+    K0 = rnd((cap, g.row_width), 61)
+    for p, want in ((5, 0), (cap, m.ERRBIT_STORE_POS), (-1, m.ERRBIT_STORE_POS | m.ERRBIT_ROPE_POS)):
+        Kd, Vd = dev(K0), dev(K0)
+        xn = torch.empty(1, g.n_embd, device="cuda")
+        q = torch.empty(1, g.q_width, device="cuda")
+        k = torch.empty(1, g.row_width, device="cuda")
+        v = torch.empty(1, g.row_width, device="cuda")
+        err = err_word()
+        m.minf_fused_qkv(xn, dev(h), None, g.eps, dev(w), dev(b), dev(np.array([p], np.int32)), q, k, v, Kd, Vd,
+                         g.n_head, g.n_kv_head, g.hd, g.hd_kv, g.theta, 1.0, 0, err)
+        torch.cuda.synchronize()
+        assert err.item() == want, (p, err.item())
+        # the oracle stores every token, so it gets a region that holds row p (and row 0 for p < 0)
+        Ko = np.zeros((max(p, 0) + 1, g.row_width), np.float32)
+        Vo = Ko.copy()
+        xn_r, q_r, k_r, v_r = orc.fused_qkv(h, np.ones(g.n_embd, np.float32), w, b, np.array([max(p, 0)], np.int32),
+                                            Ko, Vo, n_head=g.n_head, n_kv_head=g.n_kv_head, hd=g.hd, hd_kv=g.hd_kv,
+                                            eps=g.eps, theta=g.theta, style=0)
+        close(xn.cpu().numpy(), xn_r, what="xn")
+        close(v.cpu().numpy(), v_r, what="v")
+        if p >= 0:  # rotated at p
+            close(q.cpu().numpy(), q_r, what="q")
+            close(k.cpu().numpy(), k_r, what="k")
+        if 0 <= p < cap:
+            assert np.array_equal(Kd.cpu().numpy()[p], k.cpu().numpy()[0])
+        else:
+            assert np.array_equal(Kd.cpu().numpy(), K0) and np.array_equal(Vd.cpu().numpy(), K0)
+
+
 @pytest.mark.parametrize("which", ["qwen25", "qwen3"])
 def test_layer_step_qkv_decode(m, orc, which):
     from gqa_attention_kv_rope_gb300 import workloads as wl
