@@ -416,10 +416,13 @@ def run_headline(m, torch, wl, args, world, dev):
     err = int(S["err"].item())
 
     # the dominant kernel -- each layer step is one fused launch -- timed per launch with
-    # events on the stream it runs on
+    # events on the stream it runs on, alone (an event between launches, so none overlaps
+    # another).  A device-side sleep first holds the stream while the host enqueues a pass of
+    # launches, so that the events time the device, not the host's submission.
     kern_ms = []
     with torch.cuda.stream(stream):
         for it in range(max(2, args.steps // 4)):
+            torch.cuda._sleep(20_000_000)  # ~10 ms at 2 GHz: longer than enqueueing 28 launches
             for layer in range(g.n_layer):
                 a, b = Timer(torch, stream).pair()
                 a.record(stream)

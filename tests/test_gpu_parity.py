@@ -52,7 +52,9 @@ def err_word():
 # rows of 128..2048 values in whole 128-value chunks take the register-resident kernel (one
 # read of x); the others (2176, 1001, 4) the two-pass one
 @pytest.mark.parametrize("rows,n", [(1, 896), (512, 896), (1, 1024), (4096, 1024), (5, 128), (9, 2048),
-                                    (3, 640), (2, 2176), (3, 1001), (7, 4)])
+                                    (3, 640), (2, 2176), (3, 1001), (7, 4),
+                                    # many rows: more blocks than one wave of the GPU
+                                    (9001, 1024), (3001, 2048)])
 def test_rms_norm(m, orc, rows, n):
     x = rnd((rows, n), 1 + n)
     w = torch.rand(n, generator=torch.Generator().manual_seed(2)) + 0.5
@@ -405,7 +407,7 @@ def test_layer_step_batched(m, orc, n_seq, hi):
 
 
 # --------------------------------------------------------------------------- SiLU * up
-@pytest.mark.parametrize("n", [4, 1000, 1 << 20, 1023])
+@pytest.mark.parametrize("n", [4, 1000, 1 << 20, 1023, (1 << 23) + 40])  # the last: several grid strides
 def test_silu_mul(m, orc, n):
     gate = rnd((n,), n, 4.0)
     up = rnd((n,), n + 1)
