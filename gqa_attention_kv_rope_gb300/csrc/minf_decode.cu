@@ -16,20 +16,22 @@ inline int stage_rows(int hd_kv, int kind) {
 }
 
 struct WsLayout {
-    size_t ml_off, acc_off, total;
+    size_t ml_off, acc_off, tk_off, total;
     int key;  // the layout tag a call of this layout leaves in the control block
 };
 
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
 // The control block (counters and layout tag, shared with the prefill layout), then the split
-// partials: (m, l) pairs and accumulators, zero (not yet written) between calls.
+// partials: (m, l) pairs and accumulators, zero (not yet written) between calls, then one merge
+// ticket per (sequence, q head) for the units of many heads, which merge by ticket.
 WsLayout ws_layout(int n_seq, int nh, int hd_kv, int splits) {
     WsLayout w;
     const size_t parts = static_cast<size_t>(n_seq) * nh * splits;
     w.ml_off = kWsCtlBytes;
     w.acc_off = w.ml_off + align256(parts * 2 * sizeof(float));
-    w.total = w.acc_off + align256(parts * hd_kv * sizeof(float));
+    w.tk_off = w.acc_off + align256(parts * hd_kv * sizeof(float));
+    w.total = w.tk_off + align256(static_cast<size_t>(n_seq) * nh * sizeof(int));
     w.key = ws_key(kWsKindDecode, w.acc_off, w.total, parts, static_cast<unsigned long long>(splits));
     return w;
 }
@@ -138,6 +140,7 @@ int launch_impl(const DecodeArgs &d, const DecodeStepExtra *x, cudaStream_t s) {
     k.err = d.err;
     k.ws_ml = reinterpret_cast<float *>(ws + pl.w.ml_off);
     k.ws_acc = reinterpret_cast<float *>(ws + pl.w.acc_off);
+    k.ws_ticket = reinterpret_cast<int *>(ws + pl.w.tk_off);
     k.ws_ctr = reinterpret_cast<int *>(ws) + kWsUnitCtr;
     k.ws_done = reinterpret_cast<int *>(ws) + kWsUnitDone;
     k.ws_tag = reinterpret_cast<int *>(ws) + kWsTag;

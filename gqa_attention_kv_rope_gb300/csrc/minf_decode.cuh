@@ -197,6 +197,7 @@ struct KParams {
     float scale_log2;
     int32_t *err;
     float *ws_ml, *ws_acc;
+    int *ws_ticket;        // units of many heads: one merge ticket per (sequence, first q head)
     int *ws_ctr, *ws_done;  // dynamic unit counter and the count of finished producers
     int *ws_tag;           // the workspace's layout tag (its control block)
     int ws_key;            // this call's layout: the tags it accepts are 0 and this one
@@ -490,7 +491,7 @@ __global__ void __launch_bounds__(Warps<NW>::kThreads, 1)
     __shared__ float4 sm_red[kCons];
     __shared__ float sm_redM[kCons], sm_redL[kCons];
     __shared__ __align__(16) float sm_knew[HDKV], sm_vnew[HDKV];
-    __shared__ int sm_abort, sm_wsbad;
+    __shared__ int sm_abort, sm_wsbad, sm_last;
     __shared__ float sm_tab[kFused ? HDKV / 2 : 1];  // angular speeds, read by lane-varying index
     __shared__ float sm_sn[kFused ? HDKV / 2 : 1], sm_cs[kFused ? HDKV / 2 : 1];  // first unit's sin, cos
 
@@ -1046,7 +1047,11 @@ __global__ void __launch_bounds__(Warps<NW>::kThreads, 1)
         constexpr int kPairs = GH * VL;  // (head, float4 column) pairs of the unit's output
         static_assert(kPairs <= kCons, "one pair per consumer thread");
         const bool multi = t.n_act > 1;
-        const bool merger = t.j == t.n_act - 1;
+        // Units of many heads (GH >= 5) merge by ticket instead: every split stores its partial
+        // and the last to arrive folds them all.  The polling merge's registers weighed on their
+        // stage loop (the 7-head decode step: 12.8 against 10.8 us without it).
+        constexpr bool kTicket = GH >= 5;
+        const bool merger = !kTicket && t.j == t.n_act - 1;
         float own_M = -INFINITY, own_L = 0.0f;  // this unit's partial, for thread tid's pair
         float4 own_A = make_float4(0.f, 0.f, 0.f, 0.f);
         if (tid < kPairs) {
@@ -1080,9 +1085,76 @@ __global__ void __launch_bounds__(Warps<NW>::kThreads, 1)
                 own_A = A;
             }
         }
+        if constexpr (kTicket) {
+            if (multi) {
+                int *ticket = a.ws_ticket + static_cast<size_t>(t.s) * a.nh + h0;
+                cons_sync(&cons_bar, cphase, abort_flag, a.err);  // every partial store of the CTA first
+                if (tid == 0) {
+                    // acq_rel: publishes this CTA's partials and, for the last arrival, makes every
+                    // other split's visible to the loads below
+                    int old;
+                    asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], 1;" : "=r"(old) : "l"(ticket) : "memory");
+                    sm_last = old == t.n_act - 1;
+                }
+                cons_sync(&cons_bar, cphase, abort_flag, a.err);
+                if (!sm_last) continue;
+                // one round trip: each thread folds its share of the splits, then the shares
+                constexpr int kWays = kCons / kPairs;
+                for (int i = tid; i < kPairs * kWays; i += kCons) {
+                    const int pair = i % kPairs, way = i / kPairs;
+                    const int hh = pair / VL, c = pair % VL;
+                    const size_t ph2 = part0 + static_cast<size_t>(hh) * a.n_split;
+                    float M = -INFINITY, Ls = 0.0f;
+                    float4 A = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
+                    for (int j = way; j < t.n_act; j += kWays) {
+                        const uint2 mlv = __ldcg(reinterpret_cast<const uint2 *>(a.ws_ml) + (ph2 + j));
+                        const uint4 xv = __ldcg(reinterpret_cast<const uint4 *>(a.ws_acc + (ph2 + j) * HDKV) + c);
+                        const float mj = part_dec(mlv.x), lj = part_dec(mlv.y);
+                        const float Mn = fmaxf(M, mj);
+                        const float fo = M == -INFINITY ? 0.0f : ex2_approx(M - Mn);
+                        const float fn = mj == -INFINITY ? 0.0f : ex2_approx(mj - Mn);
+                        A = make_float4(fmaf(part_dec(xv.x), fn, A.x * fo), fmaf(part_dec(xv.y), fn, A.y * fo),
+                                        fmaf(part_dec(xv.z), fn, A.z * fo), fmaf(part_dec(xv.w), fn, A.w * fo));
+                        Ls = fmaf(lj, fn, Ls * fo);
+                        M = Mn;
+                    }
+                    sm_red[way * kPairs + pair] = A;
+                    sm_redM[way * kPairs + pair] = M;
+                    sm_redL[way * kPairs + pair] = Ls;
+                }
+                cons_sync(&cons_bar, cphase, abort_flag, a.err);
+                // the partials read go back to zero for the next call, and the ticket
+                for (int i = tid; i < kPairs * kWays; i += kCons) {
+                    const int pair = i % kPairs, way = i / kPairs;
+                    const int hh = pair / VL, c = pair % VL;
+                    const size_t ph2 = part0 + static_cast<size_t>(hh) * a.n_split;
+                    for (int j = way; j < t.n_act; j += kWays) {
+                        reinterpret_cast<uint4 *>(a.ws_acc + (ph2 + j) * HDKV)[c] = make_uint4(0u, 0u, 0u, 0u);
+                        if (c == 0) reinterpret_cast<uint2 *>(a.ws_ml)[ph2 + j] = make_uint2(0u, 0u);
+                    }
+                }
+                if (tid == 0) *ticket = 0;
+                if (tid < kPairs) {
+                    const int hh = tid / VL, c = tid % VL;
+                    float M = sm_redM[tid];
+                    for (int w = 1; w < kWays; ++w) M = fmaxf(M, sm_redM[w * kPairs + tid]);
+                    float Ls = 0.0f;
+                    float4 A = make_float4(0.f, 0.f, 0.f, 0.f);
+                    for (int w = 0; w < kWays; ++w) {
+                        const float mw = sm_redM[w * kPairs + tid];
+                        const float f = mw == -INFINITY ? 0.0f : ex2_approx(mw - M);
+                        const float4 x = sm_red[w * kPairs + tid];
+                        A = make_float4(fmaf(x.x, f, A.x), fmaf(x.y, f, A.y), fmaf(x.z, f, A.z), fmaf(x.w, f, A.w));
+                        Ls = fmaf(sm_redL[w * kPairs + tid], f, Ls);
+                    }
+                    reinterpret_cast<float4 *>(out_s + hh * HDKV)[c] = f4scale(A, 1.0f / Ls);
+                }
+            }
+        } else {
         if (multi && !merger) continue;  // the partial is stored: this unit is done
 
-        if (multi) {
+        if (multi) {  // (polling merge)
             // Each thread polls and folds its share of the other splits (those of index
             // way mod kWays, kChunk of them with their loads in flight together), in split order;
             // then the shares are folded in shared memory, and this unit's own partial last.
@@ -1170,6 +1242,7 @@ __global__ void __launch_bounds__(Warps<NW>::kThreads, 1)
                 reinterpret_cast<float4 *>(out_s + hh * HDKV)[c] = f4scale(A, 1.0f / Ls);
             }
         }
+        }  // (polling merge)
         if (kFused && lane < 8) {
             // every other unit of this group has finished reading q: write it back rotated
 #pragma unroll
