@@ -197,6 +197,41 @@ def test_decode_qwen3_geometry(m, orc, L):
     assert err.item() == 0
 
 
+@pytest.mark.parametrize("geom,caps,seed", [((14, 2, 64, 64), [639], 300),            # 7 heads a unit: ticket merge
+                                             ((16, 8, 128, 128), [1023, 700], 310),    # 2 heads a unit: polling merge
+                                             ((16, 2, 64, 64), [900, 300, 640], 320)])  # 8 heads a unit
+def test_decode_workspace_left_clean(m, orc, geom, caps, seed):
+    """Three calls with multi-split windows on one workspace, each against the oracle: after
+    every call the workspace is zero except the layout tag (partials consumed, counters and
+    merge tickets back at zero), so graph replays need no clearing."""
+    nh, nk, hd, hdkv = geom
+    W = nk * hdkv
+    offs = np.concatenate([[0], np.cumsum(caps)[:-1]]).astype(np.int64)
+    rows = int(np.sum(caps))
+    ws = m.kv.decode_workspace(len(caps), nh, nk, hdkv, max(caps))
+    scale = float(np.float32(1.0) / np.sqrt(np.float32(hd)))
+    for call in range(3):
+        K = rnd((rows, W), seed + 10 * call)
+        V = rnd((rows, W), seed + 10 * call + 1)
+        q = rnd((len(caps), nh, hd), seed + 10 * call + 2)
+        pos = np.array([c - 1 - 37 * call for c in caps], np.int32)  # long windows: several splits
+        out = torch.empty(len(caps), nh * hdkv, device="cuda")
+        err = err_word()
+        m.minf_gqa_attn_decode(out, dev(q), dev(K), dev(V), dev(offs), dev(np.array(caps, np.int32)), max(caps),
+                               dev(pos), nh, nk, hd, hdkv, scale, ws, err)
+        torch.cuda.synchronize()
+        assert err.item() == 0
+        got = out.cpu().numpy()
+        for s_, (o, c) in enumerate(zip(offs, caps)):
+            ref = orc.gqa_attn(q[s_:s_ + 1].numpy(), K[o:o + c].numpy(), V[o:o + c].numpy(), [pos[s_]], nh, nk, hd,
+                               hdkv, scale=scale)
+            close(got[s_:s_ + 1], ref, what=f"call {call} seq {s_}")
+        words = ws.cpu().numpy().view(np.int32).copy()
+        assert (words[4] >> 16) & 0xFFFF == 0x4D49  # the decode layout's tag
+        words[4] = 0
+        assert not words.any(), f"call {call}: {int(np.count_nonzero(words))} workspace words left non-zero"
+
+
 @pytest.mark.parametrize("L", [1, 9, 128, 639])
 def test_decode_qwen25_geometry(m, orc, L):
     err, _ = _decode_case(m, orc, 14, 2, 64, 64, [639], [L - 1], seed=100 + L)
