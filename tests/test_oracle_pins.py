@@ -370,6 +370,28 @@ def test_silu_mul(orc):
     assert y[0] == 0.0
 
 
+def test_silu_mul_closed_forms(orc):
+    """Pins that do not restate the formula: sigma(ln 3) = 3/4 exactly, the reflection
+    silu(-x) = silu(x) - x, the gate's minimum at x* = -1 - W(1/e) where silu(x*) = x* + 1
+    (sigma(x*) = 1 + 1/x*), and up scaling the product linearly."""
+    ln3 = math.log(3.0)
+    x = np.array([ln3, -ln3], np.float32)
+    y = orc.silu_mul(x, np.ones(2, np.float32))
+    np.testing.assert_allclose(y, [float(x[0]) * 0.75, float(x[1]) * 0.25], rtol=2e-7)
+    xs = np.linspace(-12.0, 12.0, 97).astype(np.float32)
+    ones = np.ones_like(xs)
+    yp, ym = orc.silu_mul(xs, ones), orc.silu_mul(-xs, ones)
+    np.testing.assert_allclose(ym, yp - xs, atol=3e-6)
+    # x* solves 1 + x(1 - sigma(x)) = 0, i.e. x* = -1 - W(1/e) with W(1/e) = 0.2784645427610738
+    x_star = -1.2784645427610738
+    y_star = orc.silu_mul(np.array([x_star, x_star - 0.01, x_star + 0.01], np.float32), np.ones(3, np.float32))
+    assert abs(float(y_star[0]) - (x_star + 1.0)) < 1e-6
+    assert y_star[1] > y_star[0] and y_star[2] > y_star[0]
+    up = np.array([2.0, -3.0, 0.5], np.float32)
+    g = np.array([0.7, -0.3, 5.0], np.float32)
+    np.testing.assert_allclose(orc.silu_mul(g, up), orc.silu_mul(g, np.ones(3, np.float32)) * up, rtol=2e-7)
+
+
 def test_layer_step_is_the_composition(orc):
     r = _rng(14)
     nh, nk, hd, hdkv, n_embd, cap = 4, 2, 16, 16, 24, 12
